@@ -1,0 +1,119 @@
+"""CPU oracle for the q6_K x int8 GEMM -- TEST INFRASTRUCTURE ONLY.
+
+Loads ``q6k_oracle.c`` (plain single-threaded C, built with gcc) through
+ctypes. Only the test-suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline leg may import this package; the CUDA library never does.
+The C source cites the passages of the pages each function follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q6k_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fexcess-precision=standard",
+          "-fPIC", "-shared", "-Wall"]
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the oracle (or a planted-mistake variant) and return the .so path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    name = "liborc.so" if mutant == 0 else f"liborc_m{mutant}.so"
+    out = os.path.join(_BUILD, name)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", *CFLAGS, f"-DORC_MUTANT={mutant}", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+class Oracle:
+    """ctypes front of one build of the oracle."""
+
+    def __init__(self, mutant: int = 0):
+        self.path = build(mutant)
+        lib = ctypes.CDLL(self.path)
+        lib.orc_f16_to_f64.restype = ctypes.c_double
+        lib.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.orc_q6k_decode_block.argtypes = [_P, _P]
+        lib.orc_q6k_wexp.argtypes = [_P, _I, _I, _P]
+        lib.orc_q6k_dsc.argtypes = [_P, _I, _I, _P]
+        lib.orc_q8_quantize.argtypes = [_P, _I, _I, _I, _P, _P]
+        lib.orc_mmq.argtypes = [_P, _I, _I, _P, _P, _I, _P, _P]
+        lib.orc_mutant.restype = _I
+        self.lib = lib
+        self.mutant = lib.orc_mutant()
+
+    @staticmethod
+    def _ptr(a: np.ndarray):
+        assert a.flags["C_CONTIGUOUS"]
+        return a.ctypes.data_as(ctypes.c_void_p)
+
+    def f16_to_f64(self, h: int) -> float:
+        return self.lib.orc_f16_to_f64(int(h) & 0xFFFF)
+
+    def decode_block(self, blk: np.ndarray) -> np.ndarray:
+        blk = np.ascontiguousarray(blk, dtype=np.uint8)
+        assert blk.size == 210
+        out = np.empty(256, dtype=np.int8)
+        self.lib.orc_q6k_decode_block(self._ptr(blk), self._ptr(out))
+        return out
+
+    def wexp(self, raw: np.ndarray, M: int, K: int) -> np.ndarray:
+        raw = np.ascontiguousarray(raw, dtype=np.uint8)
+        assert raw.size == M * (K // 256) * 210
+        out = np.empty((M, K), dtype=np.int8)
+        self.lib.orc_q6k_wexp(self._ptr(raw), M, K, self._ptr(out))
+        return out
+
+    def dsc(self, raw: np.ndarray, M: int, K: int) -> np.ndarray:
+        raw = np.ascontiguousarray(raw, dtype=np.uint8)
+        assert raw.size == M * (K // 256) * 210
+        out = np.empty((M, K // 16), dtype=np.float32)
+        self.lib.orc_q6k_dsc(self._ptr(raw), M, K, self._ptr(out))
+        return out
+
+    def quantize(self, X: np.ndarray):
+        """(xq int8 [N,K], da f32 [N,K/32])."""
+        X = np.ascontiguousarray(X, dtype=np.float32)
+        N, K = X.shape
+        assert K % 32 == 0
+        xq = np.empty((N, K), dtype=np.int8)
+        da = np.empty((N, K // 32), dtype=np.float32)
+        self.lib.orc_q8_quantize(self._ptr(X), N, K, K, self._ptr(xq), self._ptr(da))
+        return xq, da
+
+    def mmq(self, raw: np.ndarray, M: int, K: int, xq: np.ndarray, da: np.ndarray,
+            partials: bool = False):
+        """Y f64 [N,M] (and int32 partials [N,M,K/16] when asked)."""
+        raw = np.ascontiguousarray(raw, dtype=np.uint8)
+        xq = np.ascontiguousarray(xq, dtype=np.int8)
+        da = np.ascontiguousarray(da, dtype=np.float32)
+        N = xq.shape[0]
+        assert raw.size == M * (K // 256) * 210 and xq.shape == (N, K)
+        assert da.shape == (N, K // 32)
+        Y = np.empty((N, M), dtype=np.float64)
+        P = np.empty((N, M, K // 16), dtype=np.int32) if partials else None
+        self.lib.orc_mmq(self._ptr(raw), M, K, self._ptr(xq), self._ptr(da), N,
+                         self._ptr(Y), self._ptr(P) if partials else None)
+        return (Y, P) if partials else Y
+
+
+_default = None
+
+
+def get() -> Oracle:
+    """The (lazily built) default oracle."""
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

@@ -1,0 +1,36 @@
+"""The oracle checked against what the pages and mathematics fix (CPU only)."""
+import pytest
+
+import oracle
+import oracle_pins
+
+
+@pytest.mark.parametrize("pin", oracle_pins.PINS, ids=lambda p: p.__name__)
+def test_pin(orc, pin):
+    pin(orc)
+
+
+# Each planted mistake (see the ORC_MUTANT branches of the oracle source) must
+# fail at least one pin; otherwise the pins would not guard that part.
+MUTANTS = {
+    1: "ql byte index masked to 5 bits",
+    2: "qh byte index taken as r/4",
+    3: "low and high ql nibbles swapped",
+    4: "-32 centering dropped",
+    5: "neighbouring sub-block's scale",
+    6: "sub-block number used as the activation block",
+    7: "super-block scale d dropped",
+    8: "sign flip on odd sub-blocks",
+    9: "da read with the [K/32][N] layout",
+    10: "quantiser divides amax by 128",
+    11: "quantiser truncates",
+    12: "f16 subnormals flushed",
+    13: "f16 exponent bias off by one",
+    14: "sequential byte map (ql[e/2], qh[e/4])",
+}
+
+
+@pytest.mark.parametrize("k", sorted(MUTANTS), ids=lambda k: f"m{k}")
+def test_planted_mistake_is_caught(k):
+    bad = oracle_pins.failing_pins(oracle.Oracle(mutant=k))
+    assert bad, f"no pin catches planted mistake {k}: {MUTANTS[k]}"
