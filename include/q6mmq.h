@@ -1,0 +1,155 @@
+/*
+ * q6mmq -- q6_K x int8 ("MMQ") prefill GEMM for GB300 (sm_103a), C ABI.
+ *
+ * The operation (pages of the minfer CUDA optimisation log on the q6_K GEMM):
+ *   "r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.1 and 2.2: weights are
+ *   q6_K super-blocks of 256 elements (ql[128] low nibbles, qh[64] high 2-bit
+ *   fields, 16 int8 sub-block scales sc, one f16 scale d); the dequantised
+ *   weight is d * sc[sub] * (q - 32); activations are int8 with one f32 scale
+ *   da per 32 elements; the product is rescaled per 16-element sub-block with
+ *   sum += da * (d * sc), and there is no dmin term.
+ *
+ *   Y[n][m] = sum_k (d*sc*(q-32))[m][k] * (da*xq)[n][k], formed as one exact
+ *   integer partial per (n, m, 16-element sub-block) and an f32 rescale.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are device memory owned by the caller; the
+ *     library never frees or keeps them. Calls allocate nothing, except that
+ *     the first call on a device allocates one 256-byte status block there,
+ *     kept until process exit.
+ *   - Every call is asynchronous on stream `s` (NULL = legacy default stream)
+ *     and returns once the work is enqueued. Argument errors are detected on
+ *     the host before anything is enqueued.
+ *   - A device-side wait that exceeds its time limit (about one second) makes
+ *     the kernel record a code and return early; q6_sync_status() reports it.
+ *   - The current CUDA device must be compute capability 10.3 (GB300).
+ *   - Return value: one of the Q6_* codes below; q6_last_error() gives a
+ *     one-line text for the calling thread's last non-zero return.
+ */
+#ifndef Q6MMQ_H
+#define Q6MMQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
+
+#define Q6_OK 0
+#define Q6_EINVAL 1   /* null pointer, bad size, K % 256 != 0, leading dimension too small */
+#define Q6_EALIGN 2   /* a pointer or leading dimension breaks its stated alignment */
+#define Q6_ESIZE 3    /* a size outside the supported range */
+#define Q6_EARCH 4    /* the current device is not compute capability 10.3 */
+#define Q6_ECUDA 5    /* a CUDA call failed */
+#define Q6_ETIMEOUT 6 /* a bounded device-side wait expired (from q6_sync_status) */
+
+/* Which kernel a q6k_mmq call ran (written to *path_out). */
+#define Q6_PATH_NONE 0    /* nothing to do (N == 0) */
+#define Q6_PATH_TC_RAW 1  /* tensor-core kernel, weights unpacked from the packed q6_K plane */
+#define Q6_PATH_TC_WEXP 2 /* tensor-core kernel, weights taken from the W_exp plane */
+#define Q6_PATH_SKINNY 3  /* CUDA-core kernel for N <= Q6_SKINNY_MAX_N, packed q6_K plane */
+
+#define Q6_SKINNY_MAX_N 16
+
+/* Text of the calling thread's last error ("" if none). Owned by the library. */
+const char *q6_last_error(void);
+
+/* Q6_OK if the current device is compute capability 10.3, else Q6_EARCH. */
+int q6_device_check(void);
+
+/* Waits for stream `s`, then reads and clears this device's status word.
+ * Returns Q6_OK, Q6_ETIMEOUT (a kernel gave up a bounded wait; the text names
+ * the wait) or Q6_ECUDA (the stream itself reported an error). */
+int q6_sync_status(q6_stream_t s);
+
+/* Diagnostic: launches one single-warp kernel whose only work is a bounded
+ * wait on a barrier that nothing completes, with a limit of `limit_ms`
+ * milliseconds (1..2000). The kernel records the time-out in the status word
+ * and returns, so a following q6_sync_status() reports Q6_ETIMEOUT and the
+ * context stays usable. Used to test the time-out path without a fault. */
+int q6_selftest_wait_timeout(int limit_ms, q6_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Activation quantisation (the activation prepass; "r38 -- q6_K BT-style
+ * raw-byte mma kernel", Sec. 2.2 names its per-32 scale da).
+ *
+ * For token n and 32-element block c: amax = max|x|, da = amax/127 (f32),
+ * xq = clamp(round_half_away(x / da), -127, 127) with an IEEE f32 division;
+ * amax == 0 gives da = 0 and xq = 0. Inputs must be finite.
+ *
+ * Output layouts (all device, caller-allocated):
+ *   Xq : int8 [N][K], row stride K.
+ *   da : f32 [K/32][ldda], ldda = N rounded up to a multiple of 4;
+ *        da[c * ldda + n]. Entries n >= N are left untouched.
+ *   Xh : binary16 [N][K], row stride K; Xh[n][k] = (half)Xq[n][k] (exact).
+ *        This is the operand plane the tensor-core GEMM reads. Optional.
+ * -------------------------------------------------------------------- */
+
+/* Sizes in bytes of the three outputs for an N x K activation, and ldda.
+ * Any output pointer may be NULL. Q6_EINVAL if N < 0, K <= 0 or K % 256. */
+int q8_act_plane_bytes(int N, int K, size_t *xq_bytes, size_t *da_bytes,
+                       size_t *xh_bytes, int *ldda);
+
+/* X: device f32 [N][ldx], ldx >= K, X and ldx*4 16-byte aligned.
+ * Xq, da required; Xh may be NULL. Xq, Xh, da 16-byte aligned.
+ * K % 256 == 0. N == 0 is a no-op. */
+int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da,
+                    uint16_t *Xh, q6_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * Weight packing (load time; "r53 -- q6_K bundle: W_exp pre-expansion
+ * plane", Sec. 2.3 and 3.2, and "r42 -- q6_K stage-wide dsc scale reads",
+ * Sec. 3.2 for the precomputed d*sc plane).
+ *
+ * raw: device bytes of an M x K q6_K weight in the GGUF layout: M rows, each
+ *      K/256 consecutive 210-byte super-blocks (ql[128] @0, qh[64] @128,
+ *      sc[16] int8 @192, d f16 little endian @208). No alignment needed.
+ *
+ * plane (device, 256-byte aligned, q6k_plane_bytes() bytes), four sub-planes
+ * at 256-byte aligned offsets, in this order:
+ *   qlh : uint8 [M][K/128][96]. For each 128-element half h of a row
+ *         (super-block h/2, half h%2): bytes 0..63 = ql[64*(h%2) .. +63],
+ *         bytes 64..95 = qh[32*(h%2) .. +31] of that super-block.
+ *         Row stride 3*K/4 bytes.
+ *   dsc : f32 [M][K/16] = f32(d) * sc for every 16-element sub-block (exact).
+ *   sc  : int8 [M][K/16], the raw sub-block scales.
+ *   d   : binary16 bits [M][K/256], the raw super-block scales.
+ * wexp (device, optional, 16-byte aligned): int8 [M][K], row stride K, the
+ *      centered values q - 32 in [-32, 31] (the W_exp plane).
+ * -------------------------------------------------------------------- */
+
+/* Byte sizes of the packed plane and of the W_exp plane. Either may be NULL. */
+int q6k_plane_bytes(int M, int K, size_t *plane_bytes, size_t *wexp_bytes);
+
+/* Fills `plane` (and `wexp` when not NULL) from `raw`. M > 0, K % 256 == 0. */
+int q6k_pack_weights(const uint8_t *raw, int M, int K, void *plane, int8_t *wexp,
+                     q6_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * The GEMM.  Y[n][m] for n < N, m < M (f32, row stride ldy >= M, device).
+ *
+ *   plane : packed weights from q6k_pack_weights (required).
+ *   wexp  : W_exp plane or NULL. When given and N > Q6_SKINNY_MAX_N, the
+ *           tensor-core kernel stages weights from it (Q6_PATH_TC_WEXP);
+ *           otherwise it unpacks the packed plane (Q6_PATH_TC_RAW).
+ *   Xq, da: quantised activations (layouts above). Xq is read by the skinny
+ *           kernel (N <= Q6_SKINNY_MAX_N).
+ *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
+ *   partials : NULL, or device int32 [N][M][K/16] that receives every exact
+ *           sub-block partial P[n][m][s] = sum over the 16 elements of
+ *           (q - 32) * xq (a debug mode; slower).
+ *   path_out : NULL or receives a Q6_PATH_* code.
+ * Alignment: plane 256 B; Xh, da, wexp, Xq 16 B; Y 4 B.
+ * -------------------------------------------------------------------- */
+int q6k_mmq(const void *plane, const int8_t *wexp, int M, int K, const int8_t *Xq,
+            const float *da, const uint16_t *Xh, int N, float *Y, int ldy,
+            int32_t *partials, int *path_out, q6_stream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q6MMQ_H */

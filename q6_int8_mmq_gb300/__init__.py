@@ -1,0 +1,165 @@
+"""q6_K x int8 MMQ prefill GEMM for GB300 (sm_103a): thin Python binding.
+
+Argument marshalling over the C ABI of ``libq6mmq.so`` (declared in
+``include/q6mmq.h``): every step of the computation runs in the library's
+CUDA kernels. PyTorch supplies device memory and the current stream. There
+is no CPU path: calls raise ``Q6Error`` when the library is missing, the
+device is not sm_103, or an argument is rejected.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
+
+Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
+PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY = range(4)
+PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
+              PATH_SKINNY: "skinny"}
+SKINNY_MAX_N = 16
+
+# Every function include/q6mmq.h declares: (name, restype, argtypes).
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)
+_IP = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = [
+    ("q6_last_error", ctypes.c_char_p, []),
+    ("q6_device_check", _I, []),
+    ("q6_sync_status", _I, [_P]),
+    ("q6_selftest_wait_timeout", _I, [_I, _P]),
+    ("q8_act_plane_bytes", _I, [_I, _I, _SZ, _SZ, _SZ, _IP]),
+    ("q8_quantize_act", _I, [_P, _I, _I, _I, _P, _P, _P, _P]),
+    ("q6k_plane_bytes", _I, [_I, _I, _SZ, _SZ]),
+    ("q6k_pack_weights", _I, [_P, _I, _I, _P, _P, _P]),
+    ("q6k_mmq", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _IP, _P]),
+]
+
+
+class Q6Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"q6mmq error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Loads the library (once) and declares every exported signature."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise Q6Error(-1, f"CUDA library not built ({p}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != Q6_OK:
+        raise Q6Error(rc, load().q6_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ---------------------------------------------------------------- sizes ---
+
+def act_plane_bytes(N: int, K: int):
+    """(xq_bytes, da_bytes, xh_bytes, ldda) of an N x K activation."""
+    a, b, c, ld = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int()
+    _check(load().q8_act_plane_bytes(N, K, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
+                                     ctypes.byref(ld)))
+    return a.value, b.value, c.value, ld.value
+
+
+def plane_bytes(M: int, K: int):
+    """(packed plane bytes, W_exp bytes) of an M x K q6_K weight."""
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().q6k_plane_bytes(M, K, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+# ------------------------------------------------------------ operations ---
+
+class Activations:
+    """Quantised activations on the device: xq [N,K] int8, da [K/32, ldda] f32,
+    xh [N,K] f16 (or None)."""
+
+    def __init__(self, N, K, xq, da, xh, ldda):
+        self.N, self.K, self.xq, self.da, self.xh, self.ldda = N, K, xq, da, xh, ldda
+
+
+def alloc_activations(N: int, K: int, device=None, want_xh: bool = True) -> Activations:
+    import torch
+    dev = device or torch.device("cuda")
+    _, dab, _, ldda = act_plane_bytes(N, K)
+    xq = torch.empty((N, K), dtype=torch.int8, device=dev)
+    da = torch.empty((K // 32, ldda), dtype=torch.float32, device=dev)
+    xh = torch.empty((N, K), dtype=torch.float16, device=dev) if want_xh else None
+    return Activations(N, K, xq, da, xh, ldda)
+
+
+def quantize_act(X, out: Activations | None = None, want_xh: bool = True, stream=None) -> Activations:
+    """Quantises f32 activations X [N, K] (CUDA tensor, last dim contiguous)."""
+    N, K = X.shape
+    if out is None:
+        out = alloc_activations(N, K, X.device, want_xh)
+    _check(load().q8_quantize_act(_ptr(X), N, K, X.stride(0), _ptr(out.xq), _ptr(out.da),
+                                  _ptr(out.xh), _stream(stream)))
+    return out
+
+
+class Weights:
+    """A packed q6_K weight on the device (plane, optional W_exp)."""
+
+    def __init__(self, M, K, plane, wexp):
+        self.M, self.K, self.plane, self.wexp = M, K, plane, wexp
+
+
+def pack_weights(raw, M: int, K: int, wexp: bool = False, stream=None) -> Weights:
+    """Packs raw GGUF q6_K bytes (a uint8 CUDA tensor of M*K/256*210 bytes)."""
+    import torch
+    pb, wb = plane_bytes(M, K)
+    if raw.numel() != M * (K // 256) * 210 or raw.dtype != torch.uint8 or not raw.is_cuda:
+        raise Q6Error(Q6_EINVAL, "raw must be a CUDA uint8 tensor of M*K/256*210 bytes")
+    plane = torch.empty(pb, dtype=torch.uint8, device=raw.device)
+    w = torch.empty((M, K), dtype=torch.int8, device=raw.device) if wexp else None
+    _check(load().q6k_pack_weights(_ptr(raw), M, K, _ptr(plane), _ptr(w), _stream(stream)))
+    return Weights(M, K, plane, w)
+
+
+def mmq(w: Weights, act: Activations, Y=None, use_wexp: bool = True, partials: bool = False,
+        stream=None):
+    """Y [N, M] f32 = the q6_K x int8 GEMM. Returns (Y, path name, partials or None)."""
+    import torch
+    N, M, K = act.N, w.M, w.K
+    if act.K != K:
+        raise Q6Error(Q6_EINVAL, "activation K does not match the weight")
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=w.plane.device)
+    P = torch.empty((N, M, K // 16), dtype=torch.int32, device=w.plane.device) if partials else None
+    path = ctypes.c_int(-1)
+    wx = w.wexp if use_wexp else None
+    _check(load().q6k_mmq(_ptr(w.plane), _ptr(wx), M, K, _ptr(act.xq), _ptr(act.da), _ptr(act.xh),
+                          N, _ptr(Y), Y.stride(0), _ptr(P), ctypes.byref(path), _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value)), P
+
+
+def sync_status(stream=None):
+    """Waits for the stream and raises if a kernel gave up a bounded wait."""
+    _check(load().q6_sync_status(_stream(stream)))

@@ -1,0 +1,237 @@
+// C-ABI entry points of the q6mmq library: argument checks, per-device
+// state, TMA descriptor encoding and kernel dispatch by shape.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "q6_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(Q6_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+  bool init = false;
+  int arch_ok = 0;
+  unsigned int* status = nullptr;  // 256-byte block; word 0 is the status word
+};
+
+std::mutex g_mu;
+DevState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// The calling thread's current device, checked to be sm_103 and prepared
+// (status block allocated, kernel attributes raised) on first use.
+int device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(Q6_ECUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& st = g_dev[dev];
+  if (!st.init) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)))
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3) {
+      return fail(Q6_EARCH, "device %d is compute capability %d.%d; this library is built for 10.3",
+                  dev, major, minor);
+    }
+    if ((e = cudaMalloc(&st.status, 256))) return cuda_fail(e, "cudaMalloc(status)");
+    if ((e = cudaMemset(st.status, 0, 256))) return cuda_fail(e, "cudaMemset(status)");
+    if ((e = q6::mmq_tc_prepare())) return cuda_fail(e, "cudaFuncSetAttribute");
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.arch_ok = 1;
+    st.init = true;
+  }
+  *out = &st;
+  return Q6_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swz, const char* what) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(Q6_ECUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return Q6_OK;
+}
+
+int ldda_of(int N) { return (N + 3) / 4 * 4; }
+
+}  // namespace
+
+extern "C" {
+
+const char* q6_last_error(void) { return g_err; }
+
+int q6_device_check(void) {
+  DevState* st;
+  return device_state(&st);
+}
+
+int q6_sync_status(q6_stream_t s) {
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  if ((e = cudaMemcpy(&word, st->status, sizeof(word), cudaMemcpyDeviceToHost)))
+    return cuda_fail(e, "cudaMemcpy(status)");
+  if (word == 0) return Q6_OK;
+  if ((e = cudaMemset(st->status, 0, sizeof(word)))) return cuda_fail(e, "cudaMemset(status)");
+  return fail(Q6_ETIMEOUT, "a kernel gave up a bounded wait (status 0x%x, wait site %u)", word,
+              (word >> 8) & 0xFFu);
+}
+
+int q6_selftest_wait_timeout(int limit_ms, q6_stream_t s) {
+  if (limit_ms < 1 || limit_ms > 2000) return fail(Q6_EINVAL, "limit_ms must be in 1..2000");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = q6::launch_wait_selftest((unsigned long long)limit_ms * 1000000ull, st->status,
+                                           (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return Q6_OK;
+}
+
+int q8_act_plane_bytes(int N, int K, size_t* xq_bytes, size_t* da_bytes, size_t* xh_bytes,
+                       int* ldda) {
+  if (N < 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need N >= 0, K > 0, K %% 256 == 0");
+  const size_t n = (size_t)N, k = (size_t)K;
+  if (xq_bytes) *xq_bytes = n * k;
+  if (da_bytes) *da_bytes = (k / 32) * (size_t)ldda_of(N) * 4;
+  if (xh_bytes) *xh_bytes = n * k * 2;
+  if (ldda) *ldda = ldda_of(N);
+  return Q6_OK;
+}
+
+int q8_quantize_act(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, uint16_t* Xh,
+                    q6_stream_t s) {
+  if (N < 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need N >= 0, K > 0, K %% 256 == 0");
+  if (ldx < K) return fail(Q6_EINVAL, "ldx (%d) < K (%d)", ldx, K);
+  if (N == 0) return Q6_OK;
+  if (!X || !Xq || !da) return fail(Q6_EINVAL, "X, Xq and da are required");
+  if (!aligned(X, 16) || ldx % 4 || !aligned(Xq, 16) || !aligned(da, 16) || (Xh && !aligned(Xh, 16)))
+    return fail(Q6_EALIGN, "X, Xq, da, Xh must be 16-byte aligned and ldx a multiple of 4");
+  if ((long long)N * K > (1LL << 40)) return fail(Q6_ESIZE, "N*K too large");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = q6::launch_quantize(X, N, K, ldx, Xq, da, ldda_of(N),
+                                      reinterpret_cast<__half*>(Xh), (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "q8_quantize_act launch");
+  return Q6_OK;
+}
+
+int q6k_plane_bytes(int M, int K, size_t* plane_bytes, size_t* wexp_bytes) {
+  if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
+  const q6::PlaneGeom g = q6::plane_geom(M, K);
+  if (plane_bytes) *plane_bytes = g.total;
+  if (wexp_bytes) *wexp_bytes = (size_t)M * (size_t)K;
+  return Q6_OK;
+}
+
+int q6k_pack_weights(const uint8_t* raw, int M, int K, void* plane, int8_t* wexp, q6_stream_t s) {
+  if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
+  if (!raw || !plane) return fail(Q6_EINVAL, "raw and plane are required");
+  if (!aligned(plane, 256) || (wexp && !aligned(wexp, 16)))
+    return fail(Q6_EALIGN, "plane must be 256-byte aligned, wexp 16-byte aligned");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = q6::launch_pack(raw, M, K, static_cast<uint8_t*>(plane), wexp, (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "q6k_pack_weights launch");
+  return Q6_OK;
+}
+
+int q6k_mmq(const void* plane, const int8_t* wexp, int M, int K, const int8_t* Xq, const float* da,
+            const uint16_t* Xh, int N, float* Y, int ldy, int32_t* partials, int* path_out,
+            q6_stream_t s) {
+  if (path_out) *path_out = Q6_PATH_NONE;
+  if (M <= 0 || K <= 0 || K % 256 || N < 0)
+    return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
+  if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
+  if (N == 0) return Q6_OK;
+  if (!plane || !da || !Y) return fail(Q6_EINVAL, "plane, da and Y are required");
+  const bool skinny = N <= Q6_SKINNY_MAX_N;
+  if (skinny && !Xq) return fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_SKINNY_MAX_N);
+  if (!skinny && !Xh) return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
+  if (!aligned(plane, 256) || !aligned(da, 16) || !aligned(Y, 4) ||
+      (wexp && !aligned(wexp, 16)) || (Xq && !aligned(Xq, 16)) || (Xh && !aligned(Xh, 16)) ||
+      (partials && !aligned(partials, 4)))
+    return fail(Q6_EALIGN, "plane 256 B; Xq, Xh, da, wexp 16 B; Y, partials 4 B");
+  if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
+    return fail(Q6_ESIZE, "problem too large");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e;
+  if (skinny) {
+    e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda_of(N), N, Y,
+                              ldy, partials, (cudaStream_t)s);
+    if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
+    if (path_out) *path_out = Q6_PATH_SKINNY;
+    return Q6_OK;
+  }
+  const q6::PlaneGeom g = q6::plane_geom(M, K);
+  const uint8_t* pb = static_cast<const uint8_t*>(plane);
+  q6::TcMaps maps;
+  if ((rc = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Xh")))
+    return rc;
+  if (wexp)
+    rc = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wexp, (uint64_t)K, (uint64_t)M,
+                   (uint64_t)K, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE, "wexp");
+  else
+    rc = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, pb + g.qlh_off, (uint64_t)g.qlh_row,
+                   (uint64_t)M, (uint64_t)g.qlh_row, 96, 128, CU_TENSOR_MAP_SWIZZLE_NONE, "qlh");
+  if (rc) return rc;
+  if ((rc = encode_2d(&maps.da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
+                      (uint64_t)ldda_of(N) * 4, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE, "da")))
+    return rc;
+  if ((rc = encode_2d(&maps.dsc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb + g.dsc_off, (uint64_t)K / 16,
+                      (uint64_t)M, (uint64_t)K / 16 * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE, "dsc")))
+    return rc;
+  e = q6::launch_mmq_tc(maps, wexp != nullptr, M, K, N, Y, ldy, partials, st->status,
+                        (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+  if (path_out) *path_out = wexp ? Q6_PATH_TC_WEXP : Q6_PATH_TC_RAW;
+  return Q6_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports what include/q6mmq.h declares (CPU only).
+
+Only host-side argument checks are called here: every such call returns before
+touching a device, so no GPU is needed.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import q6_int8_mmq_gb300 as q6
+from q6_int8_mmq_gb300 import build as q6build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "q6mmq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    q6build.build()
+    return q6.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(q[68]\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("q8_quantize_act", "q6k_pack_weights", "q6k_mmq", "q8_act_plane_bytes",
+                     "q6k_plane_bytes", "q6_last_error", "q6_sync_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    bound = {name for name, _, _ in q6.SIGNATURES}
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+        assert name in bound, f"{name} has no binding"
+
+
+def test_plane_sizes(lib):
+    pb, wb = q6.plane_bytes(4096, 11008)
+    M, K = 4096, 11008
+    r = lambda x: (x + 255) // 256 * 256
+    assert pb == r(M * K * 3 // 4) + r(M * K // 16 * 4) + r(M * K // 16) + r(M * K // 256 * 2)
+    assert wb == M * K
+    xq, dab, xh, ldda = q6.act_plane_bytes(3314, 11008)
+    assert (xq, xh, ldda) == (3314 * 11008, 3314 * 11008 * 2, 3316)
+    assert dab == 11008 // 32 * 3316 * 4
+
+
+@pytest.mark.parametrize("M,K", [(0, 256), (4, 0), (4, 100), (4, 255), (-1, 256)])
+def test_plane_bytes_rejects(lib, M, K):
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.q6k_plane_bytes(M, K, ctypes.byref(a), ctypes.byref(b)) == q6.Q6_EINVAL
+    assert lib.q6_last_error()
+
+
+def test_host_side_rejections(lib):
+    fake = ctypes.c_void_p(0x10000)          # never dereferenced: rejected before any use
+    odd = ctypes.c_void_p(0x10004)
+    path = ctypes.c_int(-1)
+    # K not a multiple of 256
+    assert lib.q6k_mmq(fake, None, 64, 300, fake, fake, fake, 64, fake, 64, None,
+                       ctypes.byref(path), None) == q6.Q6_EINVAL
+    assert path.value == q6.PATH_NONE
+    # ldy < M
+    assert lib.q6k_mmq(fake, None, 64, 256, fake, fake, fake, 64, fake, 32, None, None,
+                       None) == q6.Q6_EINVAL
+    # N == 0 is a no-op
+    assert lib.q6k_mmq(fake, None, 64, 256, None, None, None, 0, fake, 64, None,
+                       ctypes.byref(path), None) == q6.Q6_OK
+    assert path.value == q6.PATH_NONE
+    # missing operand plane for a prefill-sized N
+    assert lib.q6k_mmq(fake, None, 64, 256, fake, fake, None, 64, fake, 64, None, None,
+                       None) == q6.Q6_EINVAL
+    # misaligned da
+    assert lib.q6k_mmq(fake, None, 64, 256, fake, odd, fake, 64, fake, 64, None, None,
+                       None) == q6.Q6_EALIGN
+    # quantiser: ldx < K, misaligned X, N == 0
+    assert lib.q8_quantize_act(fake, 4, 256, 128, fake, fake, None, None) == q6.Q6_EINVAL
+    assert lib.q8_quantize_act(odd, 4, 256, 256, fake, fake, None, None) == q6.Q6_EALIGN
+    assert lib.q8_quantize_act(None, 0, 256, 256, None, None, None, None) == q6.Q6_OK
+    # pack: misaligned plane, missing raw
+    assert lib.q6k_pack_weights(fake, 4, 256, odd, None, None) == q6.Q6_EALIGN
+    assert lib.q6k_pack_weights(None, 4, 256, fake, None, None) == q6.Q6_EINVAL
+    assert lib.q6_selftest_wait_timeout(0, None) == q6.Q6_EINVAL
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(q6.Q6Error):
+        q6.load(str(tmp_path / "nope.so"))

@@ -1,0 +1,264 @@
+"""Parity of the CUDA library with the CPU oracle (needs a GB300).
+
+Integer results (quantised activations, packed planes, sub-block partials) must
+be bit-exact. Y must satisfy the floating-point tolerance of the method:
+max|Y - Yo| <= 1e-3 * max|Yo| and sum|Y - Yo| / sum|Yo| <= 1e-5 (the normwise
+reading of "mean relative error"). Full-size workloads are checked on sampled
+tokens against all weight rows, in the launch configuration the benchmark uses.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import restate
+from q6_int8_mmq_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+MAX_REL = 1e-3
+NORMWISE = 1e-5
+
+
+@pytest.fixture(scope="module")
+def q6():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import q6_int8_mmq_gb300 as q6mod
+    from q6_int8_mmq_gb300 import build as q6build
+    q6build.build()
+    q6mod.load()
+    return q6mod
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def check_y(Y, Yo, label=""):
+    Y = np.asarray(Y, dtype=np.float64)
+    err = np.abs(Y - Yo)
+    scale = np.abs(Yo).max()
+    assert np.all(np.isfinite(Y)), label
+    if scale == 0:
+        assert err.max() == 0, label
+        return
+    maxrel = err.max() / scale
+    normwise = err.sum() / np.abs(Yo).sum()
+    assert maxrel <= MAX_REL, f"{label}: max error {maxrel:.3e} of max|Y|"
+    assert normwise <= NORMWISE, f"{label}: normwise error {normwise:.3e}"
+
+
+def quant_check(act, X, orc):
+    xq_o, da_o = orc.quantize(X)
+    N = X.shape[0]
+    assert np.array_equal(host(act.xq), xq_o)
+    assert np.array_equal(host(act.da)[:, :N].T, da_o)
+    if act.xh is not None:
+        assert np.array_equal(host(act.xh).astype(np.float32), xq_o.astype(np.float32))
+    return xq_o, da_o
+
+
+def run_gemm(q6, raw, X, M, K, use_wexp, partials=False):
+    w = q6.pack_weights(dev(raw), M, K, wexp=use_wexp)
+    act = q6.quantize_act(dev(X))
+    Y, path, P = q6.mmq(w, act, use_wexp=use_wexp, partials=partials)
+    q6.sync_status()
+    return w, act, Y, path, P
+
+
+# --------------------------------------------------------------- failures ---
+
+def test_bounded_wait_times_out_and_context_survives(q6):
+    lib = q6.load()
+    assert lib.q6_selftest_wait_timeout(50, None) == q6.Q6_OK
+    with pytest.raises(q6.Q6Error) as ei:
+        q6.sync_status()
+    assert ei.value.code == q6.Q6_ETIMEOUT
+    q6.sync_status()                    # the status word was cleared
+    X = synth.activations(1, 4, 256)
+    act = q6.quantize_act(dev(X))       # the context still works
+    q6.sync_status()
+    quant_check(act, X, oracle.get())
+
+
+# -------------------------------------------------------------- quantiser ---
+
+@pytest.mark.parametrize("N,K,frac", [(1, 256, 0.0), (8, 512, 0.0), (513, 4096, 0.0),
+                                      (77, 11008, 0.01)])
+def test_quantize_bitexact(q6, orc, N, K, frac):
+    X = synth.activations(100 + N, N, K, outlier_frac=frac)
+    X[0, 32:64] = 0.0                                   # all-zero block
+    if N > 2:
+        X[2, :32] = np.float32(1e-30)                   # tiny block
+        X[1, :32] = 0.0
+        X[1, 0] = 127.0
+        X[1, 1:7] = [2.5, -2.5, 0.5, -0.5, 126.5, -126.5]   # exact halfway quotients
+    act = q6.quantize_act(dev(X))
+    q6.sync_status()
+    quant_check(act, X, orc)
+
+
+def test_quantize_strided_input(q6, orc):
+    import torch
+    X = synth.activations(7, 33, 512)
+    big = torch.zeros((33, 640), dtype=torch.float32, device="cuda")
+    big[:, :512] = dev(X)
+    act = q6.quantize_act(big[:, :512])
+    q6.sync_status()
+    quant_check(act, X, orc)
+
+
+# ------------------------------------------------------------------- pack ---
+
+@pytest.mark.parametrize("M,K", [(64, 256), (40, 512), (24, 768), (131, 1024)])
+def test_pack_bitexact(q6, orc, M, K):
+    raw = synth.q6k_raw_weights(200 + M, M, K)
+    w = q6.pack_weights(dev(raw), M, K, wexp=True)
+    q6.sync_status()
+    plane = host(w.plane)
+    blocks = raw.reshape(M, K // 256, 210)
+    r = lambda x: (x + 255) // 256 * 256
+    qlh_sz, dsc_sz, sc_sz = M * K * 3 // 4, M * K // 16 * 4, M * K // 16
+    o_dsc = r(qlh_sz)
+    o_sc = o_dsc + r(dsc_sz)
+    o_d = o_sc + r(sc_sz)
+    # qlh: per half h of super-block b: ql[64h:64h+64] then qh[32h:32h+32]
+    qlh = plane[:qlh_sz].reshape(M, K // 256, 2, 96)
+    for h in range(2):
+        assert np.array_equal(qlh[:, :, h, :64], blocks[:, :, 64 * h: 64 * h + 64])
+        assert np.array_equal(qlh[:, :, h, 64:], blocks[:, :, 128 + 32 * h: 160 + 32 * h])
+    dsc = plane[o_dsc:o_dsc + dsc_sz].view(np.float32).reshape(M, K // 16)
+    assert np.array_equal(dsc, orc.dsc(raw, M, K))
+    sc = plane[o_sc:o_sc + sc_sz].view(np.int8).reshape(M, K // 256, 16)
+    assert np.array_equal(sc, blocks[:, :, 192:208].view(np.int8))
+    d = plane[o_d:o_d + M * K // 256 * 2].reshape(M, K // 256, 2)
+    assert np.array_equal(d, blocks[:, :, 208:210])
+    assert np.array_equal(host(w.wexp), orc.wexp(raw, M, K))
+    assert np.array_equal(host(w.wexp).astype(np.int64), restate.int_values(raw, M, K))
+
+
+# --------------------------------------------------------- GEMM, small ------
+
+SMALL = [
+    # (M, K, N) spanning tiles and ragged tails of both kernels
+    (256, 512, 1), (256, 512, 4), (256, 512, 8), (200, 768, 16),      # skinny kernel
+    (128, 256, 17), (256, 512, 128), (200, 512, 129), (384, 768, 300),  # tensor-core kernel
+    (130, 1024, 255), (64, 256, 40),
+]
+
+
+@pytest.mark.parametrize("use_wexp", [False, True], ids=["raw", "wexp"])
+@pytest.mark.parametrize("M,K,N", SMALL, ids=lambda v: str(v))
+def test_mmq_small_bitexact_partials(q6, orc, M, K, N, use_wexp):
+    raw = synth.q6k_raw_weights(300 + M + N, M, K)
+    X = synth.activations(400 + M + N, N, K, outlier_frac=0.02)
+    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, use_wexp, partials=True)
+    xq_o, da_o = quant_check(act, X, orc)
+    Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+    if N <= q6.SKINNY_MAX_N:
+        assert path == "skinny"
+    else:
+        assert path == ("tc_wexp" if use_wexp else "tc_raw")
+    assert np.array_equal(host(P), Po), "sub-block partials differ"
+    check_y(host(Y), Yo, f"{M}x{K}x{N}")
+    # the fast (non-debug) variant gives the same Y
+    Y2, _, _ = q6.mmq(w, act, use_wexp=use_wexp)
+    q6.sync_status()
+    check_y(host(Y2), Yo, "fast variant")
+
+
+def test_mmq_degenerate_inputs(q6, orc):
+    M, K, N = 128, 512, 130
+    blk = np.zeros(210, np.uint8)
+    blk[128:192] = 0xAA                     # every code 32: all values zero
+    blk[192:208] = 7
+    blk[208:210] = [0x00, 0x3C]
+    raw = np.tile(blk, (M, K // 256))
+    X = synth.activations(5, N, K)
+    for n in (N, 3):                         # tensor-core and skinny kernels
+        _, _, Y, _, _ = run_gemm(q6, raw, X[:n], M, K, False)
+        assert np.all(host(Y) == 0.0)
+    raw = synth.q6k_raw_weights(6, M, K).reshape(-1, 210).copy()
+    raw[:, 208:210] = 0                      # d = 0 everywhere
+    _, _, Y, _, _ = run_gemm(q6, raw.reshape(M, -1), X, M, K, True)
+    assert np.all(host(Y) == 0.0)
+    X0 = X.copy()
+    X0[5] = 0.0                              # a zero token
+    raw = synth.q6k_raw_weights(7, M, K)
+    _, _, Y, _, _ = run_gemm(q6, raw, X0, M, K, False)
+    assert np.all(host(Y)[5] == 0.0)
+
+
+def test_mmq_empty(q6):
+    import torch
+    M, K = 128, 256
+    raw = synth.q6k_raw_weights(8, M, K)
+    w = q6.pack_weights(dev(raw), M, K)
+    act = q6.alloc_activations(0, K)
+    Y, path, _ = q6.mmq(w, act, Y=torch.empty((0, M), device="cuda"))
+    q6.sync_status()
+    assert path == "none"
+
+
+# ------------------------------------------------------ full-size workloads --
+
+def sampled_tokens(N, extra=()):
+    idx = {0, 1, N - 1, N // 2, (N // 128) * 128, max(0, (N // 128) * 128 - 1), *extra}
+    return np.array(sorted(i for i in idx if 0 <= i < N))
+
+
+def check_full(q6, orc, raw, X, M, K, use_wexp, label, partial_tokens=0):
+    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, use_wexp)
+    xq_o, da_o = quant_check(act, X, orc)
+    tok = sampled_tokens(X.shape[0])
+    Yo = orc.mmq(raw, M, K, xq_o[tok], da_o[tok])
+    check_y(host(Y)[tok], Yo, label)
+    return w, act, path
+
+
+@pytest.mark.parametrize("use_wexp", [False, True], ids=["raw", "wexp"])
+def test_attn_v_full(q6, orc, use_wexp):
+    raw, X, cfg = synth.workload("attn_v")
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    w, act, path = check_full(q6, orc, raw, X, M, K, use_wexp, "attn_v")
+    assert path == ("tc_wexp" if use_wexp else "tc_raw")
+    # sub-block partials of four tokens, bit-exact
+    Y, _, P = q6.mmq(w, act, use_wexp=use_wexp, partials=True)
+    q6.sync_status()
+    tok = np.array([0, 129, 300, N - 1])
+    xq_o, da_o = orc.quantize(X[tok])
+    _, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+    assert np.array_equal(host(P[tok]), Po)
+
+
+@pytest.mark.parametrize("use_wexp", [False, True], ids=["raw", "wexp"])
+def test_ffn_down_full(q6, orc, use_wexp):
+    raw, X, cfg = synth.workload("ffn_down")
+    check_full(q6, orc, raw, X, cfg["M"], cfg["K"], use_wexp, "ffn_down")
+
+
+@pytest.mark.parametrize("weight", ["ffn_down", "attn_v"])
+@pytest.mark.parametrize("N", synth.SKINNY_N)
+def test_skinny_full(q6, orc, weight, N):
+    raw, X, cfg = synth.skinny_workload(weight, N)
+    M, K = cfg["M"], cfg["K"]
+    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, False, partials=True)
+    assert path == "skinny"
+    xq_o, da_o = quant_check(act, X, orc)
+    Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+    assert np.array_equal(host(P), Po)
+    check_y(host(Y), Yo, f"skinny {weight} N={N}")
+
+
+@pytest.mark.parametrize("layer", [0, 31])
+def test_sweep_layers(q6, orc, layer):
+    raw_v, raw_d = synth.sweep_layer(layer)
+    X_v, X_d = synth.sweep_activations()
+    check_full(q6, orc, raw_v, X_v, 4096, 4096, False, f"sweep layer {layer} attn_v")
+    check_full(q6, orc, raw_d, X_d, 4096, 11008, False, f"sweep layer {layer} ffn_down")
