@@ -46,11 +46,12 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_ECUDA 5    /* a CUDA call failed */
 #define Q6_ETIMEOUT 6 /* a bounded device-side wait expired (from q6_sync_status) */
 
-/* Which kernel a q6k_mmq call ran (written to *path_out). */
+/* Which kernels a q6k_mmq call ran (written to *path_out). */
 #define Q6_PATH_NONE 0    /* nothing to do (N == 0) */
-#define Q6_PATH_TC_RAW 1  /* tensor-core kernel, weights unpacked from the packed q6_K plane */
-#define Q6_PATH_TC_WEXP 2 /* tensor-core kernel, weights taken from the W_exp plane */
-#define Q6_PATH_SKINNY 3  /* CUDA-core kernel for N <= Q6_SKINNY_MAX_N, packed q6_K plane */
+#define Q6_PATH_TC_RAW 1  /* unpack of the packed q6_K plane into the workspace + tensor-core GEMM */
+#define Q6_PATH_TC_WEXP 2 /* conversion of the W_exp plane into the workspace + tensor-core GEMM */
+#define Q6_PATH_SKINNY 3  /* CUDA-core kernel for N <= Q6_SKINNY_MAX_N on the packed q6_K plane */
+#define Q6_PATH_TC_WH 4   /* tensor-core GEMM on a resident binary16 operand plane */
 
 #define Q6_SKINNY_MAX_N 16
 
@@ -119,34 +120,54 @@ int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da
  *   d   : binary16 bits [M][K/256], the raw super-block scales.
  * wexp (device, optional, 16-byte aligned): int8 [M][K], row stride K, the
  *      centered values q - 32 in [-32, 31] (the W_exp plane).
+ * wh   (device, optional, 16-byte aligned): binary16 [M][K], row stride K,
+ *      the same centered values as exact binary16: the operand-ready plane
+ *      the tensor-core GEMM reads (2 bytes per weight).
  * -------------------------------------------------------------------- */
 
-/* Byte sizes of the packed plane and of the W_exp plane. Either may be NULL. */
+/* Byte sizes of the packed plane and of the W_exp plane (the wh plane is
+ * twice the W_exp size). Either pointer may be NULL. */
 int q6k_plane_bytes(int M, int K, size_t *plane_bytes, size_t *wexp_bytes);
 
-/* Fills `plane` (and `wexp` when not NULL) from `raw`. M > 0, K % 256 == 0. */
+/* Fills `plane` (and `wexp`, `wh` when not NULL) from `raw`. M > 0,
+ * K % 256 == 0. */
 int q6k_pack_weights(const uint8_t *raw, int M, int K, void *plane, int8_t *wexp,
-                     q6_stream_t s);
+                     uint16_t *wh, q6_stream_t s);
+
+/* The weight unpack pass alone: writes the binary16 operand plane wh [M][K]
+ * (the layout described above) from wexp when it is not NULL, else from the
+ * packed plane's qlh sub-plane ("r41 -- q6_K B-expand widened to uint4 group
+ * loads", Sec. 3.2: 16-element groups from one 16-byte ql run and one 16-byte
+ * qh run). q6k_mmq runs this into its workspace when it gets no wh plane. */
+int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint16_t *wh,
+                       q6_stream_t s);
 
 /* ------------------------------------------------------------------------
  * The GEMM.  Y[n][m] for n < N, m < M (f32, row stride ldy >= M, device).
  *
  *   plane : packed weights from q6k_pack_weights (required).
- *   wexp  : W_exp plane or NULL. When given and N > Q6_SKINNY_MAX_N, the
- *           tensor-core kernel stages weights from it (Q6_PATH_TC_WEXP);
- *           otherwise it unpacks the packed plane (Q6_PATH_TC_RAW).
+ *   wexp, wh : the optional planes from q6k_pack_weights, or NULL.
  *   Xq, da: quantised activations (layouts above). Xq is read by the skinny
  *           kernel (N <= Q6_SKINNY_MAX_N).
  *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
+ *   workspace : device scratch of at least q6k_mmq_workspace_bytes() bytes
+ *           (256-byte aligned) when N > Q6_SKINNY_MAX_N and wh is NULL: the
+ *           weights are first unpacked there (from wexp when given, else from
+ *           the packed plane) into the binary16 operand layout. Unused
+ *           otherwise. Its contents after the call are unspecified.
  *   partials : NULL, or device int32 [N][M][K/16] that receives every exact
  *           sub-block partial P[n][m][s] = sum over the 16 elements of
  *           (q - 32) * xq (a debug mode; slower).
  *   path_out : NULL or receives a Q6_PATH_* code.
- * Alignment: plane 256 B; Xh, da, wexp, Xq 16 B; Y 4 B.
+ * Alignment: plane, workspace 256 B; Xh, da, wexp, wh, Xq 16 B; Y 4 B.
+ * Q6_ESIZE when the workspace is missing or too small.
  * -------------------------------------------------------------------- */
-int q6k_mmq(const void *plane, const int8_t *wexp, int M, int K, const int8_t *Xq,
-            const float *da, const uint16_t *Xh, int N, float *Y, int ldy,
-            int32_t *partials, int *path_out, q6_stream_t s);
+int q6k_mmq_workspace_bytes(int M, int K, int N, size_t *bytes);
+
+int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, int K,
+            const int8_t *Xq, const float *da, const uint16_t *Xh, int N, float *Y, int ldy,
+            void *workspace, size_t workspace_bytes, int32_t *partials, int *path_out,
+            q6_stream_t s);
 
 #ifdef __cplusplus
 }

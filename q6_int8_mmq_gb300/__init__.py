@@ -15,9 +15,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
 
 Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
-PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY = range(4)
+PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH = range(5)
 PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
-              PATH_SKINNY: "skinny"}
+              PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh"}
 SKINNY_MAX_N = 16
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).
@@ -31,8 +31,11 @@ SIGNATURES = [
     ("q8_act_plane_bytes", _I, [_I, _I, _SZ, _SZ, _SZ, _IP]),
     ("q8_quantize_act", _I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     ("q6k_plane_bytes", _I, [_I, _I, _SZ, _SZ]),
-    ("q6k_pack_weights", _I, [_P, _I, _I, _P, _P, _P]),
-    ("q6k_mmq", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, _IP, _P]),
+    ("q6k_pack_weights", _I, [_P, _I, _I, _P, _P, _P, _P]),
+    ("q6k_unpack_weights", _I, [_P, _P, _I, _I, _P, _P]),
+    ("q6k_mmq_workspace_bytes", _I, [_I, _I, _I, _SZ]),
+    ("q6k_mmq", _I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP,
+                     _P]),
 ]
 
 
@@ -125,38 +128,88 @@ def quantize_act(X, out: Activations | None = None, want_xh: bool = True, stream
 
 
 class Weights:
-    """A packed q6_K weight on the device (plane, optional W_exp)."""
+    """A packed q6_K weight on the device: the packed plane, and optionally the
+    W_exp (int8) and operand-ready binary16 planes."""
 
-    def __init__(self, M, K, plane, wexp):
-        self.M, self.K, self.plane, self.wexp = M, K, plane, wexp
+    def __init__(self, M, K, plane, wexp, wh):
+        self.M, self.K, self.plane, self.wexp, self.wh = M, K, plane, wexp, wh
 
 
-def pack_weights(raw, M: int, K: int, wexp: bool = False, stream=None) -> Weights:
+def pack_weights(raw, M: int, K: int, wexp: bool = False, wh: bool = False, stream=None) -> Weights:
     """Packs raw GGUF q6_K bytes (a uint8 CUDA tensor of M*K/256*210 bytes)."""
     import torch
     pb, wb = plane_bytes(M, K)
     if raw.numel() != M * (K // 256) * 210 or raw.dtype != torch.uint8 or not raw.is_cuda:
         raise Q6Error(Q6_EINVAL, "raw must be a CUDA uint8 tensor of M*K/256*210 bytes")
     plane = torch.empty(pb, dtype=torch.uint8, device=raw.device)
-    w = torch.empty((M, K), dtype=torch.int8, device=raw.device) if wexp else None
-    _check(load().q6k_pack_weights(_ptr(raw), M, K, _ptr(plane), _ptr(w), _stream(stream)))
-    return Weights(M, K, plane, w)
+    w8 = torch.empty((M, K), dtype=torch.int8, device=raw.device) if wexp else None
+    w16 = torch.empty((M, K), dtype=torch.float16, device=raw.device) if wh else None
+    _check(load().q6k_pack_weights(_ptr(raw), M, K, _ptr(plane), _ptr(w8), _ptr(w16),
+                                   _stream(stream)))
+    return Weights(M, K, plane, w8, w16)
 
 
-def mmq(w: Weights, act: Activations, Y=None, use_wexp: bool = True, partials: bool = False,
-        stream=None):
-    """Y [N, M] f32 = the q6_K x int8 GEMM. Returns (Y, path name, partials or None)."""
+def unpack_weights(w: Weights, out=None, from_wexp: bool = False, stream=None):
+    """The weight unpack pass: binary16 operand plane [M, K] from the packed
+    plane (or from the W_exp plane)."""
+    import torch
+    if out is None:
+        out = torch.empty((w.M, w.K), dtype=torch.float16, device=w.plane.device)
+    src8 = w.wexp if from_wexp else None
+    if from_wexp and src8 is None:
+        raise Q6Error(Q6_EINVAL, "weights were packed without the W_exp plane")
+    _check(load().q6k_unpack_weights(_ptr(w.plane), _ptr(src8), w.M, w.K, _ptr(out),
+                                     _stream(stream)))
+    return out
+
+
+def workspace_bytes(M: int, K: int, N: int) -> int:
+    b = ctypes.c_size_t()
+    _check(load().q6k_mmq_workspace_bytes(M, K, N, ctypes.byref(b)))
+    return b.value
+
+
+_workspaces = {}
+
+
+def _workspace(nbytes: int, device):
+    """A cached device scratch buffer of at least nbytes (one per device)."""
+    import torch
+    key = str(device)
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _workspaces[key] = buf
+    return buf
+
+
+def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bool = False,
+        workspace=None, wh=None, stream=None):
+    """Y [N, M] f32 = the q6_K x int8 GEMM. Returns (Y, path name, partials or None).
+
+    source: "raw" (unpack the packed plane), "wexp" (convert the W_exp plane),
+    "wh" (resident binary16 plane) or "auto" (wh, else wexp, else raw)."""
     import torch
     N, M, K = act.N, w.M, w.K
     if act.K != K:
         raise Q6Error(Q6_EINVAL, "activation K does not match the weight")
+    if source == "auto":
+        source = "wh" if w.wh is not None else ("wexp" if w.wexp is not None else "raw")
+    wx = w.wexp if source == "wexp" else None
+    w16 = (wh if wh is not None else w.wh) if source == "wh" else None
+    if source in ("wexp", "wh") and (wx if source == "wexp" else w16) is None:
+        raise Q6Error(Q6_EINVAL, f"weights were packed without the {source} plane")
+    dev = w.plane.device
     if Y is None:
-        Y = torch.empty((N, M), dtype=torch.float32, device=w.plane.device)
-    P = torch.empty((N, M, K // 16), dtype=torch.int32, device=w.plane.device) if partials else None
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    P = torch.empty((N, M, K // 16), dtype=torch.int32, device=dev) if partials else None
+    ws_need = workspace_bytes(M, K, N) if w16 is None else 0
+    ws = workspace if workspace is not None else (_workspace(ws_need, dev) if ws_need else None)
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     path = ctypes.c_int(-1)
-    wx = w.wexp if use_wexp else None
-    _check(load().q6k_mmq(_ptr(w.plane), _ptr(wx), M, K, _ptr(act.xq), _ptr(act.da), _ptr(act.xh),
-                          N, _ptr(Y), Y.stride(0), _ptr(P), ctypes.byref(path), _stream(stream)))
+    _check(load().q6k_mmq(_ptr(w.plane), _ptr(wx), _ptr(w16), M, K, _ptr(act.xq), _ptr(act.da),
+                          _ptr(act.xh), N, _ptr(Y), Y.stride(0), _ptr(ws), ws_bytes, _ptr(P),
+                          ctypes.byref(path), _stream(stream)))
     return Y, PATH_NAMES.get(path.value, str(path.value)), P
 
 

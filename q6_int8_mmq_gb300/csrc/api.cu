@@ -166,21 +166,52 @@ int q6k_plane_bytes(int M, int K, size_t* plane_bytes, size_t* wexp_bytes) {
   return Q6_OK;
 }
 
-int q6k_pack_weights(const uint8_t* raw, int M, int K, void* plane, int8_t* wexp, q6_stream_t s) {
+int q6k_pack_weights(const uint8_t* raw, int M, int K, void* plane, int8_t* wexp, uint16_t* wh,
+                     q6_stream_t s) {
   if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
   if (!raw || !plane) return fail(Q6_EINVAL, "raw and plane are required");
-  if (!aligned(plane, 256) || (wexp && !aligned(wexp, 16)))
-    return fail(Q6_EALIGN, "plane must be 256-byte aligned, wexp 16-byte aligned");
+  if (!aligned(plane, 256) || (wexp && !aligned(wexp, 16)) || (wh && !aligned(wh, 16)))
+    return fail(Q6_EALIGN, "plane must be 256-byte aligned, wexp and wh 16-byte aligned");
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
   cudaError_t e = q6::launch_pack(raw, M, K, static_cast<uint8_t*>(plane), wexp, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "q6k_pack_weights launch");
+  if (wh) {
+    e = q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K,
+                              reinterpret_cast<__half*>(wh), (cudaStream_t)s);
+    if (e != cudaSuccess) return cuda_fail(e, "q6k_pack_weights expand launch");
+  }
   return Q6_OK;
 }
 
-int q6k_mmq(const void* plane, const int8_t* wexp, int M, int K, const int8_t* Xq, const float* da,
-            const uint16_t* Xh, int N, float* Y, int ldy, int32_t* partials, int* path_out,
+int q6k_unpack_weights(const void* plane, const int8_t* wexp, int M, int K, uint16_t* wh,
+                       q6_stream_t s) {
+  if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
+  if (!wh || (!plane && !wexp)) return fail(Q6_EINVAL, "wh and one of plane, wexp are required");
+  if ((plane && !aligned(plane, 256)) || (wexp && !aligned(wexp, 16)) || !aligned(wh, 16))
+    return fail(Q6_EALIGN, "plane 256 B; wexp, wh 16 B");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = wexp ? q6::launch_expand_wexp(wexp, M, K, reinterpret_cast<__half*>(wh),
+                                                (cudaStream_t)s)
+                       : q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K,
+                                               reinterpret_cast<__half*>(wh), (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "q6k_unpack_weights launch");
+  return Q6_OK;
+}
+
+int q6k_mmq_workspace_bytes(int M, int K, int N, size_t* bytes) {
+  if (M <= 0 || K <= 0 || K % 256 || N < 0 || !bytes)
+    return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0, bytes != NULL");
+  *bytes = N > Q6_SKINNY_MAX_N ? (size_t)M * (size_t)K * 2 : 0;
+  return Q6_OK;
+}
+
+int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, int K,
+            const int8_t* Xq, const float* da, const uint16_t* Xh, int N, float* Y, int ldy,
+            void* workspace, size_t workspace_bytes, int32_t* partials, int* path_out,
             q6_stream_t s) {
   if (path_out) *path_out = Q6_PATH_NONE;
   if (M <= 0 || K <= 0 || K % 256 || N < 0)
@@ -192,11 +223,18 @@ int q6k_mmq(const void* plane, const int8_t* wexp, int M, int K, const int8_t* X
   if (skinny && !Xq) return fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_SKINNY_MAX_N);
   if (!skinny && !Xh) return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
   if (!aligned(plane, 256) || !aligned(da, 16) || !aligned(Y, 4) ||
-      (wexp && !aligned(wexp, 16)) || (Xq && !aligned(Xq, 16)) || (Xh && !aligned(Xh, 16)) ||
-      (partials && !aligned(partials, 4)))
-    return fail(Q6_EALIGN, "plane 256 B; Xq, Xh, da, wexp 16 B; Y, partials 4 B");
+      (wexp && !aligned(wexp, 16)) || (wh && !aligned(wh, 16)) || (Xq && !aligned(Xq, 16)) ||
+      (Xh && !aligned(Xh, 16)) || (partials && !aligned(partials, 4)) ||
+      (workspace && !aligned(workspace, 256)))
+    return fail(Q6_EALIGN, "plane, workspace 256 B; Xq, Xh, da, wexp, wh 16 B; Y, partials 4 B");
   if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
     return fail(Q6_ESIZE, "problem too large");
+  if (!skinny && !wh) {
+    const size_t need = (size_t)M * (size_t)K * 2;
+    if (!workspace || workspace_bytes < need)
+      return fail(Q6_ESIZE, "workspace of %zu bytes needed to unpack the weights (got %zu)", need,
+                  workspace ? workspace_bytes : (size_t)0);
+  }
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
@@ -208,29 +246,38 @@ int q6k_mmq(const void* plane, const int8_t* wexp, int M, int K, const int8_t* X
     if (path_out) *path_out = Q6_PATH_SKINNY;
     return Q6_OK;
   }
+  int path = Q6_PATH_TC_WH;
+  const void* wop = wh;
+  if (!wh) {
+    __half* ws = static_cast<__half*>(workspace);
+    if (wexp) {
+      e = q6::launch_expand_wexp(wexp, M, K, ws, (cudaStream_t)s);
+      path = Q6_PATH_TC_WEXP;
+    } else {
+      e = q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K, ws, (cudaStream_t)s);
+      path = Q6_PATH_TC_RAW;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "weight unpack launch");
+    wop = ws;
+  }
   const q6::PlaneGeom g = q6::plane_geom(M, K);
   const uint8_t* pb = static_cast<const uint8_t*>(plane);
   q6::TcMaps maps;
   if ((rc = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
                       (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Xh")))
     return rc;
-  if (wexp)
-    rc = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wexp, (uint64_t)K, (uint64_t)M,
-                   (uint64_t)K, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE, "wexp");
-  else
-    rc = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, pb + g.qlh_off, (uint64_t)g.qlh_row,
-                   (uint64_t)M, (uint64_t)g.qlh_row, 96, 128, CU_TENSOR_MAP_SWIZZLE_NONE, "qlh");
-  if (rc) return rc;
+  if ((rc = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wop, (uint64_t)K, (uint64_t)M,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Wh")))
+    return rc;
   if ((rc = encode_2d(&maps.da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
                       (uint64_t)ldda_of(N) * 4, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE, "da")))
     return rc;
   if ((rc = encode_2d(&maps.dsc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb + g.dsc_off, (uint64_t)K / 16,
                       (uint64_t)M, (uint64_t)K / 16 * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE, "dsc")))
     return rc;
-  e = q6::launch_mmq_tc(maps, wexp != nullptr, M, K, N, Y, ldy, partials, st->status,
-                        (cudaStream_t)s);
+  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, partials, st->status, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
-  if (path_out) *path_out = wexp ? Q6_PATH_TC_WEXP : Q6_PATH_TC_RAW;
+  if (path_out) *path_out = path;
   return Q6_OK;
 }
 

@@ -1,0 +1,107 @@
+// Weight unpack pass: q6_K codes -> the binary16 operand plane Wh [M][K]
+// that the tensor-core GEMM stages with TMA.
+//
+// Element map ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 3.2; the
+// 16-element group form of "r41 -- q6_K B-expand widened to uint4 group
+// loads", Sec. 3.2): within a 128-element half block, 16-element group g
+// takes its low 4 bits from the 16 ql bytes at 16*(g mod 4) (low nibble for
+// g < 4, high nibble otherwise) and its high 2 bits from field (g/2) mod 4 of
+// the 16 qh bytes at 16*(g mod 2); the value is code - 32, in [-32, 31]. The
+// W_exp source ("r53 -- q6_K bundle: W_exp pre-expansion plane", Sec. 2.3)
+// already holds the centered values as int8.
+//
+// Both kernels are bandwidth-bound: one thread per 16 elements, two 16-byte
+// loads (raw) or one (W_exp), two 16-byte stores.
+#include "q6_internal.cuh"
+
+namespace q6 {
+namespace {
+
+// Four 6-bit codes -> two binary16 pairs holding code - 32 exactly: bytes
+// 0x64cc are the f16 value 1024 + cc, and subtracting 1056 leaves cc - 32.
+__device__ __forceinline__ void codes_to_f16(uint32_t code, uint32_t& lo, uint32_t& hi) {
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6420));  // 1056
+  uint32_t a = __byte_perm(code, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(code, 0x64646464u, 0x4342);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// Four int8 values -> two binary16 pairs: flipping bit 7 gives v + 128 as an
+// unsigned byte, 0x64xx is 1024 + that, and subtracting 1152 leaves v.
+__device__ __forceinline__ void i8_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+  lo = *reinterpret_cast<uint32_t*>(&ha);
+  hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+__global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restrict__ qlh, int M, int K,
+                                                         size_t qlh_row, __half* __restrict__ wh) {
+  const int groups = K / 16;
+  const long long items = (long long)M * groups;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
+    const int m = (int)(i / groups), r = (int)(i - (long long)m * groups);
+    const int hb = r >> 3, g = r & 7;  // half block, group within it
+    const uint8_t* src = qlh + (size_t)m * qlh_row + (size_t)hb * 96;
+    const uint4 L = __ldg(reinterpret_cast<const uint4*>(src + 16 * (g & 3)));
+    const uint4 H = __ldg(reinterpret_cast<const uint4*>(src + 64 + 16 * (g & 1)));
+    const int nsh = 4 * (g >> 2), fsh = 2 * ((g >> 1) & 3);
+    const uint32_t Lw[4] = {L.x, L.y, L.z, L.w}, Hw[4] = {H.x, H.y, H.z, H.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t code = ((Lw[w] >> nsh) & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
+      codes_to_f16(code, o[2 * w], o[2 * w + 1]);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(wh + (size_t)m * K + (size_t)r * 16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+__global__ void __launch_bounds__(256) expand_wexp_kernel(const int8_t* __restrict__ wexp, long long n16,
+                                                          __half* __restrict__ wh) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(wexp) + i);
+    uint32_t o[8];
+    i8_to_f16(v.x, o[0], o[1]);
+    i8_to_f16(v.y, o[2], o[3]);
+    i8_to_f16(v.z, o[4], o[5]);
+    i8_to_f16(v.w, o[6], o[7]);
+    uint4* dst = reinterpret_cast<uint4*>(wh) + 2 * i;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+unsigned grid_for(long long items) {
+  long long blocks = (items + 255) / 256;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  return (unsigned)(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s) {
+  const PlaneGeom g = plane_geom(M, K);
+  expand_raw_kernel<<<grid_for((long long)M * (K / 16)), 256, 0, s>>>(plane + g.qlh_off, M, K,
+                                                                      g.qlh_row, wh);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand_wexp(const int8_t* wexp, int M, int K, __half* wh, cudaStream_t s) {
+  const long long n16 = (long long)M * K / 16;
+  expand_wexp_kernel<<<grid_for(n16), 256, 0, s>>>(wexp, n16, wh);
+  return cudaGetLastError();
+}
+
+}  // namespace q6

@@ -7,84 +7,107 @@
 // per 32-element chunk c, with dsc = f32(d) * sc (no dmin term). The pages run
 // this as KSPLIT=2 pairs of int8 mma.sync m16n8k16 per chunk.
 //
-// Here, sm_103a offers no tcgen05 int8 MMA, so both operands are staged as
-// binary16 holding the small integers exactly (weights -32..31, activations
-// -127..127) and multiplied by tcgen05.mma kind::f16 with f32 accumulation in
-// TMEM: every sub-block sum is at most 16 * 32 * 127 = 65024 < 2^24, so the
-// f32 partial equals the integer partial exactly. One K=16 MMA per sub-block
-// writes a fresh accumulator, so each sub-block keeps its own scale.
+// sm_103a has no tcgen05 int8 MMA, so both operands are binary16 planes
+// holding the small integers exactly (weights -32..31 from the unpack pass,
+// activations -127..127 from the quantiser) and are multiplied by tcgen05.mma
+// kind::f16 with f32 accumulation in TMEM: every sub-block sum is at most
+// 16 * 32 * 127 = 65024 < 2^24, so the f32 partial is the integer partial
+// exactly. One K=16 MMA per sub-block writes a fresh accumulator, so each
+// sub-block keeps its own scale.
 //
-// CTA tile: 128 weight rows (MMA M, TMEM lanes) x 128 tokens (MMA N), K staged
-// 128 at a time (one half super-block) in a 2-stage mbarrier ring.
-//   warp 0      TMA producer: Xh tile (two 64-wide 128B-swizzled boxes), the
-//               weight source (96-byte qlh rows, or 128-byte W_exp rows), the
-//               da slice [4 chunks][128 tokens], the dsc slice [128 rows][8].
-//   warp 1      allocates 512 TMEM columns; lane 0 issues the MMAs: per chunk
-//               two MMAs (sub-blocks 2c, 2c+1) into one of two TMEM buffers of
-//               2 x 128 columns, then tcgen05.commit to the buffer's barrier.
-//   warps 2-5   unpack the weight source into the binary16 operand tile in the
-//               128B-swizzled K-major layout (raw: ql nibble | qh field << 4,
-//               minus 32; W_exp: int8 -> f16), fence to the async proxy.
-//   warps 6-13  epilogue: tcgen05.ld both sub-block partials of a chunk, scale
-//               with dsc (per row, this thread's lane) and da (per column),
-//               accumulate Y in registers, release the TMEM buffer.
+// CTA tile: 128 weight rows (MMA M, TMEM lanes) x 128 tokens (MMA N). Two
+// shared-memory rings filled by TMA:
+//   operand ring (5 stages x 64 of K): Xh and Wh tiles, 128 rows x 128 bytes
+//          each, 128-byte swizzled; freed by the MMA (tcgen05.commit).
+//   scale ring (6 stages x 128 of K): dsc [128 rows][8] and da [4][128];
+//          freed by the epilogue.
+// Warp roles (12 warps; warpgroup 0 gives registers to warpgroups 1-2):
+//   0      TMA producer for both rings.
+//   1      TMEM allocation (512 columns); lane 0 issues the MMAs: per chunk two
+//          K=16 MMAs (sub-blocks 2c, 2c+1) into one of two TMEM buffers of
+//          2 x 128 columns, then tcgen05.commit to that buffer's barrier.
+//   2-3    idle (their registers go to the epilogue).
+//   4-11   epilogue: warp w owns TMEM lanes 32(w%4).. and 64 token columns.
+//          Per chunk it loads the two sub-block partials of its columns in
+//          two halves of 32 columns, software-pipelined across chunks (the
+//          load of one half overlaps the math of the other), releases the
+//          TMEM buffer as soon as both halves are in registers, and
+//          accumulates Y in registers: acc += da * (dsc0 * P0 + dsc1 * P1).
 // Every mbarrier wait is bounded (see q6_internal.cuh).
 #include "q6_internal.cuh"
 
 namespace q6 {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 128, STAGES = 2;
-constexpr int kThreads = 448;
-constexpr int kConvWarp0 = 2, kNumConvWarps = 4;
-constexpr int kEpiWarp0 = 6, kNumEpiWarps = 8;
-constexpr int kConvThreads = kNumConvWarps * 32;
+constexpr int BM = 128, BN = 128;
+constexpr int KB = 64, SB = 5;   // operand ring: K per stage, stages
+constexpr int KS = 128, SS = 6;  // scale ring
+constexpr int kThreads = 384;                 // launched with 168 registers per thread
+constexpr int kCtlRegs = 56, kEpiRegs = 224;  // 128 * 56 + 256 * 224 == 384 * 168
+static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * 168, "register split");
+constexpr int kEpiWarp0 = 4, kNumEpiWarps = 8;
 
-constexpr int kXOff = 0;                      // Xh tile: 2 x [128 rows][128 B], swizzled
-constexpr int kAOff = kXOff + BN * BK * 2;    // weight operand: same layout
-constexpr int kWOff = kAOff + BM * BK * 2;    // weight source (qlh 96 B or W_exp 128 B per row)
-constexpr int kDaOff = kWOff + BM * BK;       // da [4][128] f32
-constexpr int kDscOff = kDaOff + 4 * BN * 4;  // dsc [128][8] f32
-constexpr int kStageBytes = kDscOff + BM * 8 * 4;
-static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+constexpr int kOpX = 0, kOpW = BN * 128, kOpStage = kOpW + BM * 128;
+constexpr int kScDsc = 0, kScDa = BM * 8 * 4, kScStage = kScDa + 4 * BN * 4;
+constexpr int kRingS = SB * kOpStage;  // the scale ring follows the operand ring
+constexpr int kRingsBytes = kRingS + SS * kScStage;
+static_assert(kOpStage % 1024 == 0, "operand stages must keep 1024-byte alignment");
+static_assert(kScStage % 128 == 0, "scale stages must keep 128-byte alignment");
 constexpr int kTmemCols = 512;
 
-enum : uint32_t { kSiteEmpty = 1, kSiteFull = 2, kSiteConv = 3, kSiteTFull = 4, kSiteTEmpty = 5,
-                  kSiteDrain = 6 };
+enum : uint32_t { kSiteSEmpty = 1, kSiteSFull = 2, kSiteBEmpty = 3, kSiteBFull = 4,
+                  kSiteTFull = 6, kSiteTEmpty = 7, kSiteDrain = 8 };
 
 struct Bars {
-  uint64_t full[STAGES], conv[STAGES], empty[STAGES], tfull[2], tempty[2], drain;
+  uint64_t s_full[SS], s_empty[SS];
+  uint64_t b_full[SB], b_empty[SB];
+  uint64_t tfull[2], tempty[2], drain;
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * kStageBytes + sizeof(Bars);
+constexpr size_t kSmemBytes = 1024 + (size_t)kRingsBytes + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// Four 6-bit codes -> two binary16 pairs holding code - 32 exactly:
-// bytes 0x64cc are the f16 value 1024 + cc; subtracting 1056 leaves cc - 32.
-__device__ __forceinline__ void codes_to_f16(uint32_t code, uint32_t& lo, uint32_t& hi) {
-  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6420));  // 1056
-  uint32_t a = __byte_perm(code, 0x64646464u, 0x4140);
-  uint32_t b = __byte_perm(code, 0x64646464u, 0x4342);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-  lo = *reinterpret_cast<uint32_t*>(&ha);
-  hi = *reinterpret_cast<uint32_t*>(&hb);
-}
-// Four int8 values -> two binary16 pairs: flipping bit 7 gives v + 128 as an
-// unsigned byte, 0x64xx is 1024 + that, and subtracting 1152 leaves v.
-__device__ __forceinline__ void i8_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-  const uint32_t u = w ^ 0x80808080u;
-  uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-  uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-  __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-  __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
-  lo = *reinterpret_cast<uint32_t*>(&ha);
-  hi = *reinterpret_cast<uint32_t*>(&hb);
+// acc[j] += da[j] * (s0 * P0[j] + s1 * P1[j]) for 32 columns (16 pairs).
+__device__ __forceinline__ void rescale32(float2 (&acc)[16], const uint32_t (&p0)[32],
+                                          const uint32_t (&p1)[32], float2 s0v, float2 s1v,
+                                          const float* __restrict__ dq) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const float4 a4 = reinterpret_cast<const float4*>(dq)[v];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = 4 * v + 2 * e;
+      float2 t = __fmul2_rn(s0v, make_float2(__uint_as_float(p0[j]), __uint_as_float(p0[j + 1])));
+      t = __ffma2_rn(s1v, make_float2(__uint_as_float(p1[j]), __uint_as_float(p1[j + 1])), t);
+      const float2 dav = e ? make_float2(a4.z, a4.w) : make_float2(a4.x, a4.y);
+      acc[2 * v + e] = __ffma2_rn(dav, t, acc[2 * v + e]);
+    }
+  }
 }
 
-template <bool kWexp, bool kPartials>
+template <bool kPartials>
+__device__ __forceinline__ void dump_partials(int32_t* __restrict__ partials, int M, int K, int N,
+                                              int m, int n_first, size_t sub,
+                                              const uint32_t (&p0)[32], const uint32_t (&p1)[32]) {
+  if (kPartials) {
+    if (m < M) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int n = n_first + j;
+        if (n < N) {
+          int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 16) + sub;
+          pr[0] = (int32_t)__uint_as_float(p0[j]);
+          pr[1] = (int32_t)__uint_as_float(p1[j]);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+template <bool kPartials>
 __global__ void __launch_bounds__(kThreads, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                   const __grid_constant__ CUtensorMap tmDa, const __grid_constant__ CUtensorMap tmDsc,
@@ -93,17 +116,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + STAGES * kStageBytes);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kRingsBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
-  const int nk = K / BK;
+  const int ns = K / KS;   // scale-ring steps (half super-blocks)
+  const int nb = K / KB;   // operand-ring steps
+  const int nc = K / 32;   // chunks
   volatile int* abort_flag = &bars->abort;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->conv[s], kConvThreads);
-      mbar_init(&bars->empty[s], 1 + kNumEpiWarps);
+    for (int s = 0; s < SS; ++s) {
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_empty[s], kNumEpiWarps);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(&bars->b_full[s], 1);
+      mbar_init(&bars->b_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->tfull[b], 1);
@@ -128,206 +156,164 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      constexpr uint32_t kTx = BN * BK * 2 + (kWexp ? BM * BK : BM * 96) + 4 * BN * 4 + BM * 8 * 4;
-      int issued = 0;
-      for (int kt = 0; kt < nk; ++kt) {
-        const int s = kt % STAGES;
-        const uint32_t ph = (kt / STAGES) & 1;
-        if (!mbar_wait_bounded(&bars->empty[s], ph ^ 1, abort_flag, status, kSiteEmpty)) break;
-        uint8_t* st = smem + s * kStageBytes;
-        mbar_arrive_expect_tx(&bars->full[s], kTx);
-        tma_load_2d(st + kXOff, &tmX, &bars->full[s], kt * BK, n0);
-        tma_load_2d(st + kXOff + BN * 128, &tmX, &bars->full[s], kt * BK + 64, n0);
-        if (kWexp)
-          tma_load_2d(st + kWOff, &tmW, &bars->full[s], kt * BK, m0);
-        else
-          tma_load_2d(st + kWOff, &tmW, &bars->full[s], kt * 96, m0);
-        tma_load_2d(st + kDaOff, &tmDa, &bars->full[s], n0, kt * 4);
-        tma_load_2d(st + kDscOff, &tmDsc, &bars->full[s], kt * 8, m0);
-        issued = kt + 1;
-      }
-      if (*abort_flag) {
-        // Let the copies already issued land before the CTA exits.
-        for (int kt = (issued > STAGES ? issued - STAGES : 0); kt < issued; ++kt) {
-          volatile int no_abort = 0;
-          mbar_wait_bounded(&bars->full[kt % STAGES], (kt / STAGES) & 1, &no_abort, status,
-                            kSiteFull);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ----------------------------------------------------------------- MMA --
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
-      int cc = 0;
-      bool ok = true;
-      for (int kt = 0; kt < nk && ok; ++kt) {
-        const int s = kt % STAGES;
-        const uint32_t ph = (kt / STAGES) & 1;
-        ok = mbar_wait_bounded(&bars->full[s], ph, abort_flag, status, kSiteFull) &&
-             mbar_wait_bounded(&bars->conv[s], ph, abort_flag, status, kSiteConv);
-        if (!ok) break;
-        tc_fence_after();
-        const uint8_t* st = smem + s * kStageBytes;
-        const uint32_t a_base = smem_u32(st + kAOff), b_base = smem_u32(st + kXOff);
-        for (int q = 0; q < 4; ++q, ++cc) {
-          const int b = cc & 1;
-          const uint32_t use = (uint32_t)(cc >> 1);
-          if (!mbar_wait_bounded(&bars->tempty[b], (use & 1) ^ 1, abort_flag, status,
-                                 kSiteTEmpty)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
+  if (warp < kEpiWarp0) {
+    // --------------------------------------------------- warpgroup 0: control --
+    regs_dealloc<kCtlRegs>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer --
+      if (lane == 0) {
+        constexpr uint32_t kTxS = BM * 8 * 4 + 4 * BN * 4;
+        constexpr uint32_t kTxB = (BN + BM) * 128;
+        int s_issued = 0, b_issued = 0;
+        bool ok = true;
+        for (int ks = 0; ks < ns && ok; ++ks) {
+          const int ss = ks % SS;
+          ok = mbar_wait_bounded(&bars->s_empty[ss], ((ks / SS) & 1) ^ 1, abort_flag, status,
+                                 kSiteSEmpty);
+          if (!ok) break;
+          uint8_t* st = smem + kRingS + ss * kScStage;
+          mbar_arrive_expect_tx(&bars->s_full[ss], kTxS);
+          tma_load_2d(st + kScDsc, &tmDsc, &bars->s_full[ss], ks * 8, m0);
+          tma_load_2d(st + kScDa, &tmDa, &bars->s_full[ss], n0, ks * 4);
+          s_issued = ks + 1;
           for (int h = 0; h < 2; ++h) {
-            const int j = 2 * q + h;  // sub-block within the stage
-            const uint32_t koff = (uint32_t)((j >> 2) * (BN * 128) + (j & 3) * 32);
-            umma_f16(tmem + (uint32_t)(b * 256 + h * 128), sw128_kmajor_desc(a_base + koff),
-                     sw128_kmajor_desc(b_base + koff), idesc, 0u);
+            const int kb = 2 * ks + h, sb = kb % SB;
+            ok = mbar_wait_bounded(&bars->b_empty[sb], ((kb / SB) & 1) ^ 1, abort_flag, status,
+                                   kSiteBEmpty);
+            if (!ok) break;
+            uint8_t* bt = smem + sb * kOpStage;
+            mbar_arrive_expect_tx(&bars->b_full[sb], kTxB);
+            tma_load_2d(bt + kOpX, &tmX, &bars->b_full[sb], kb * KB, n0);
+            tma_load_2d(bt + kOpW, &tmW, &bars->b_full[sb], kb * KB, m0);
+            b_issued = kb + 1;
           }
-          umma_commit(&bars->tfull[b]);
         }
-        if (ok) umma_commit(&bars->empty[s]);
+        if (!ok) {
+          // Let copies already issued land before the CTA exits.
+          volatile int no_abort = 0;
+          for (int k = (s_issued > SS ? s_issued - SS : 0); k < s_issued; ++k)
+            mbar_wait_bounded(&bars->s_full[k % SS], (k / SS) & 1, &no_abort, status, kSiteSFull);
+          for (int k = (b_issued > SB ? b_issued - SB : 0); k < b_issued; ++k)
+            mbar_wait_bounded(&bars->b_full[k % SB], (k / SB) & 1, &no_abort, status, kSiteBFull);
+        }
       }
-      // Every MMA must be finished before TMEM is released.
-      umma_commit(&bars->drain);
-      volatile int no_abort = 0;
-      mbar_wait_bounded(&bars->drain, 0, &no_abort, status, kSiteDrain);
+    } else if (warp == 1) {
+      // --------------------------------------------------------------- MMA --
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+        int cc = 0;
+        bool ok = true;
+        for (int kb = 0; kb < nb && ok; ++kb) {
+          const int sb = kb % SB;
+          if (!mbar_wait_bounded(&bars->b_full[sb], (kb / SB) & 1, abort_flag, status, kSiteBFull))
+            break;
+          tc_fence_after();
+          const uint8_t* bt = smem + sb * kOpStage;
+          const uint32_t w_base = smem_u32(bt + kOpW), x_base = smem_u32(bt + kOpX);
+          for (int q = 0; q < 2; ++q, ++cc) {
+            const int b = cc & 1;
+            const uint32_t use = (uint32_t)(cc >> 1);
+            if (!mbar_wait_bounded(&bars->tempty[b], (use & 1) ^ 1, abort_flag, status,
+                                   kSiteTEmpty)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t koff = (uint32_t)((2 * q + h) * 32);  // sub-block within the stage
+              umma_f16(tmem + (uint32_t)(b * 256 + h * 128), sw128_kmajor_desc(w_base + koff),
+                       sw128_kmajor_desc(x_base + koff), idesc, 0u);
+            }
+            umma_commit(&bars->tfull[b]);
+          }
+          if (ok) umma_commit(&bars->b_empty[sb]);
+        }
+        // Every MMA must be finished before TMEM is released.
+        umma_commit(&bars->drain);
+        volatile int no_abort = 0;
+        mbar_wait_bounded(&bars->drain, 0, &no_abort, status, kSiteDrain);
+      }
     }
     __syncwarp();
-  } else if (warp < kEpiWarp0) {
-    // -------------------------------------------------------------- unpack --
-    const int ct = threadIdx.x - kConvWarp0 * 32;  // 0..127
-    for (int kt = 0; kt < nk; ++kt) {
-      const int s = kt % STAGES;
-      const uint32_t ph = (kt / STAGES) & 1;
-      if (!mbar_wait_bounded(&bars->full[s], ph, abort_flag, status, kSiteFull)) break;
-      uint8_t* st = smem + s * kStageBytes;
-      const uint8_t* wsrc = st + kWOff;
-      uint8_t* aop = st + kAOff;
-#pragma unroll 2
-      for (int it = 0; it < (BM * 8) / kConvThreads; ++it) {
-        const int item = it * kConvThreads + ct;
-        const int r = item >> 3, g = item & 7;  // row, 16-element group of the half block
-        uint32_t o[8];
-        if (kWexp) {
-          const uint4 v = *reinterpret_cast<const uint4*>(wsrc + r * 128 + g * 16);
-          i8_to_f16(v.x, o[0], o[1]);
-          i8_to_f16(v.y, o[2], o[3]);
-          i8_to_f16(v.z, o[4], o[5]);
-          i8_to_f16(v.w, o[6], o[7]);
-        } else {
-          // elements 16g .. 16g+15 of the half: ql bytes 16(g&3).., nibble g>>2;
-          // qh bytes 16(g&1).., 2-bit field (g>>1)&3.
-          const uint4 L = *reinterpret_cast<const uint4*>(wsrc + r * 96 + 16 * (g & 3));
-          const uint4 H = *reinterpret_cast<const uint4*>(wsrc + r * 96 + 64 + 16 * (g & 1));
-          const int nsh = 4 * (g >> 2), fsh = 2 * ((g >> 1) & 3);
-          const uint32_t Lw[4] = {L.x, L.y, L.z, L.w}, Hw[4] = {H.x, H.y, H.z, H.w};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint32_t code =
-                ((Lw[w] >> nsh) & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
-            codes_to_f16(code, o[2 * w], o[2 * w + 1]);
-          }
-        }
-        // 16 elements = 16B chunks 2(g&3), 2(g&3)+1 of 64-wide k-block g>>2, swizzled.
-        uint8_t* row = aop + (g >> 2) * (BM * 128) + r * 128;
-        const int c0 = 2 * (g & 3);
-        *reinterpret_cast<uint4*>(row + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (r & 7)) << 4)) =
-            make_uint4(o[4], o[5], o[6], o[7]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->conv[s]);
-    }
   } else {
-    // ------------------------------------------------------------ epilogue --
-    const int ew = warp - kEpiWarp0;   // 0..7
-    const int quarter = warp & 3;      // TMEM lanes 32*quarter .. +31
-    const int colh = ew >> 2;          // token columns 64*colh .. +63
+    // ------------------------------------------------ warpgroups 1-2: epilogue --
+    regs_alloc<kEpiRegs>();
+    const int ew = warp - kEpiWarp0;  // 0..7
+    const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
+    const int colh = ew >> 2;         // token columns 64*colh .. +63
     const int row = 32 * quarter + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16);
-    float2 acc[32];
+    const int m = m0 + row;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(64 * colh);
+    float2 accA[16], accB[16];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.0f, 0.0f);
-    int cc = 0;
-    bool ok = true;
-    for (int kt = 0; kt < nk && ok; ++kt) {
-      const int s = kt % STAGES;
-      const uint32_t ph = (kt / STAGES) & 1;
-      if (!mbar_wait_warp(&bars->full[s], ph, abort_flag, status, kSiteFull)) break;
-      const uint8_t* st = smem + s * kStageBytes;
-      const float* sda = reinterpret_cast<const float*>(st + kDaOff);
-      const float4 d0 = reinterpret_cast<const float4*>(st + kDscOff + row * 32)[0];
-      const float4 d1 = reinterpret_cast<const float4*>(st + kDscOff + row * 32)[1];
-      const float dscv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-      for (int q = 0; q < 4; ++q, ++cc) {
-        const int b = cc & 1;
-        const uint32_t use = (uint32_t)(cc >> 1);
-        if (!mbar_wait_warp(&bars->tfull[b], use & 1, abort_flag, status, kSiteTFull)) {
+    for (int j = 0; j < 16; ++j) accA[j] = accB[j] = make_float2(0.0f, 0.0f);
+    uint32_t pA0[32], pA1[32], pB0[32], pB1[32];
+    float4 d0 = make_float4(0.f, 0.f, 0.f, 0.f), d1 = d0;  // dsc of the current scale stage
+    const float* sda = nullptr;
+    bool ok = mbar_wait_warp(&bars->tfull[0], 0, abort_flag, status, kSiteTFull);
+    if (ok) {
+      tc_fence_after();
+      tmem_ld32(lane_addr, pA0);
+      tmem_ld32(lane_addr + 128u, pA1);
+      tmem_wait_ld2(pA0, pA1);
+    }
+    for (int c = 0; c < nc && ok; ++c) {
+      const int b = c & 1, q = c & 3, ks = c >> 2;
+      if (q == 0) {  // a new scale stage
+        const int ss = ks % SS;
+        if (!mbar_wait_warp(&bars->s_full[ss], (ks / SS) & 1, abort_flag, status, kSiteSFull)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const float s0 = (q == 0) ? dscv[0] : (q == 1) ? dscv[2] : (q == 2) ? dscv[4] : dscv[6];
-        const float s1 = (q == 0) ? dscv[1] : (q == 1) ? dscv[3] : (q == 2) ? dscv[5] : dscv[7];
-        const float2 s0v = make_float2(s0, s0), s1v = make_float2(s1, s1);
-#pragma unroll
-        for (int sl = 0; sl < 4; ++sl) {
-          const int col = 64 * colh + 16 * sl;
-          uint32_t p0[16], p1[16];
-          tmem_ld2x16(lane_addr + (uint32_t)(b * 256 + col), lane_addr + (uint32_t)(b * 256 + 128 + col),
-                      p0, p1);
-          const float4* dap = reinterpret_cast<const float4*>(sda + q * 128 + col);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float4 a4 = dap[v];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int j = 4 * v + 2 * e;
-              const float2 pa = make_float2(__uint_as_float(p0[j]), __uint_as_float(p0[j + 1]));
-              const float2 pb = make_float2(__uint_as_float(p1[j]), __uint_as_float(p1[j + 1]));
-              float2 t = __fmul2_rn(s0v, pa);
-              t = __ffma2_rn(s1v, pb, t);
-              const float2 dav = e ? make_float2(a4.z, a4.w) : make_float2(a4.x, a4.y);
-              acc[8 * sl + 2 * v + e] = __ffma2_rn(dav, t, acc[8 * sl + 2 * v + e]);
-            }
-          }
-          if (kPartials) {
-            const int m = m0 + row;
-            if (m < M) {
-              const size_t sub = (size_t)kt * 8 + 2 * q;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int n = n0 + col + j;
-                if (n < N) {
-                  int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 16) + sub;
-                  pr[0] = (int32_t)__uint_as_float(p0[j]);
-                  pr[1] = (int32_t)__uint_as_float(p1[j]);
-                }
-              }
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tempty[b]);
+        const uint8_t* st = smem + kRingS + ss * kScStage;
+        sda = reinterpret_cast<const float*>(st + kScDa) + 64 * colh;
+        d0 = reinterpret_cast<const float4*>(st + kScDsc + row * 32)[0];
+        d1 = reinterpret_cast<const float4*>(st + kScDsc + row * 32)[1];
       }
+      const float s0 = (q == 0) ? d0.x : (q == 1) ? d0.z : (q == 2) ? d1.x : d1.z;
+      const float s1 = (q == 0) ? d0.y : (q == 1) ? d0.w : (q == 2) ? d1.y : d1.w;
+      const float2 s0v = make_float2(s0, s0), s1v = make_float2(s1, s1);
+      const float* dq = sda + q * 128;
+      // second half of this chunk in flight while the first half is scaled
+      tmem_ld32(lane_addr + (uint32_t)(b * 256 + 32), pB0);
+      tmem_ld32(lane_addr + (uint32_t)(b * 256 + 160), pB1);
+      rescale32(accA, pA0, pA1, s0v, s1v, dq);
+      dump_partials<kPartials>(partials, M, K, N, m, n0 + 64 * colh, (size_t)c * 2, pA0, pA1);
+      tmem_wait_ld2(pB0, pB1);
+      // both halves are in registers: the TMEM buffer can take chunk c + 2
+      tc_fence_before();
       __syncwarp();
-      if (ok && lane == 0) mbar_arrive(&bars->empty[s]);
+      if (lane == 0) mbar_arrive(&bars->tempty[b]);
+      // first half of the next chunk in flight while the second half is scaled
+      bool next = c + 1 < nc;
+      if (next) {
+        next = mbar_wait_warp(&bars->tfull[b ^ 1], ((c + 1) >> 1) & 1, abort_flag, status,
+                              kSiteTFull);
+        if (next) {
+          tc_fence_after();
+          tmem_ld32(lane_addr + (uint32_t)((b ^ 1) * 256), pA0);
+          tmem_ld32(lane_addr + (uint32_t)((b ^ 1) * 256 + 128), pA1);
+        } else {
+          ok = false;
+        }
+      }
+      rescale32(accB, pB0, pB1, s0v, s1v, dq + 32);
+      dump_partials<kPartials>(partials, M, K, N, m, n0 + 64 * colh + 32, (size_t)c * 2, pB0, pB1);
+      if (next) tmem_wait_ld2(pA0, pA1);
+      if (q == 3) {  // done with this scale stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_empty[ks % SS]);
+      }
     }
-    const int m = m0 + row;
     if (m < M) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < 16; ++j) {
         const int n = n0 + 64 * colh + 2 * j;
-        if (n < N) Y[(size_t)n * ldy + m] = acc[j].x;
-        if (n + 1 < N) Y[(size_t)(n + 1) * ldy + m] = acc[j].y;
+        if (n < N) Y[(size_t)n * ldy + m] = accA[j].x;
+        if (n + 1 < N) Y[(size_t)(n + 1) * ldy + m] = accA[j].y;
+        if (n + 32 < N) Y[(size_t)(n + 32) * ldy + m] = accB[j].x;
+        if (n + 33 < N) Y[(size_t)(n + 33) * ldy + m] = accB[j].y;
       }
     }
   }
@@ -340,12 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool W, bool P>
+template <bool P>
 cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ldy, int32_t* partials,
                        unsigned int* status, cudaStream_t s) {
   dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM));
-  mmq_tc_kernel<W, P><<<grid, kThreads, kSmemBytes, s>>>(maps.x, maps.w, maps.da, maps.dsc, M, K, N,
-                                                        Y, ldy, partials, status);
+  mmq_tc_kernel<P><<<grid, kThreads, kSmemBytes, s>>>(maps.x, maps.w, maps.da, maps.dsc, M, K, N, Y,
+                                                     ldy, partials, status);
   return cudaGetLastError();
 }
 
@@ -353,29 +339,19 @@ cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ld
 
 size_t mmq_tc_smem_bytes() { return kSmemBytes; }
 
-// Raises the dynamic shared-memory limit of every instantiation; once per device.
+// Raises the dynamic shared-memory limit of both instantiations; once per device.
 cudaError_t mmq_tc_prepare() {
-  cudaError_t e;
-  if ((e = cudaFuncSetAttribute(mmq_tc_kernel<false, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)))
-    return e;
-  if ((e = cudaFuncSetAttribute(mmq_tc_kernel<false, true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)))
-    return e;
-  if ((e = cudaFuncSetAttribute(mmq_tc_kernel<true, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes)))
-    return e;
-  return cudaFuncSetAttribute(mmq_tc_kernel<true, true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(mmq_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSmemBytes);
 }
 
-cudaError_t launch_mmq_tc(const TcMaps& maps, bool wexp, int M, int K, int N, float* Y, int ldy,
+cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                           int32_t* partials, unsigned int* status, cudaStream_t s) {
-  if (wexp)
-    return partials ? launch_one<true, true>(maps, M, K, N, Y, ldy, partials, status, s)
-                    : launch_one<true, false>(maps, M, K, N, Y, ldy, nullptr, status, s);
-  return partials ? launch_one<false, true>(maps, M, K, N, Y, ldy, partials, status, s)
-                  : launch_one<false, false>(maps, M, K, N, Y, ldy, nullptr, status, s);
+  return partials ? launch_one<true>(maps, M, K, N, Y, ldy, partials, status, s)
+                  : launch_one<false>(maps, M, K, N, Y, ldy, nullptr, status, s);
 }
 
 }  // namespace q6

@@ -47,19 +47,26 @@ cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* 
                               cudaStream_t s);
 
 struct TcMaps {
-  CUtensorMap x;    // Xh   [N][K] f16, box {64, 128}, 128B swizzle
-  CUtensorMap w;    // qlh  [M][3K/4] u8, box {96, 128}  or  wexp [M][K] u8, box {128, 128}
-  CUtensorMap da;   // da   [K/32][ldda] f32, box {128, 4}
-  CUtensorMap dsc;  // dsc  [M][K/16] f32, box {8, 128}
+  CUtensorMap x;    // Xh  [N][K] f16, box {64, 128}, 128B swizzle
+  CUtensorMap w;    // Wh  [M][K] f16, box {64, 128}, 128B swizzle
+  CUtensorMap da;   // da  [K/32][ldda] f32, box {128, 4}
+  CUtensorMap dsc;  // dsc [M][K/16] f32, box {8, 128}
 };
-cudaError_t launch_mmq_tc(const TcMaps& maps, bool wexp, int M, int K, int N, float* Y, int ldy,
+cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                           int32_t* partials, unsigned int* status, cudaStream_t s);
+// Binary16 operand plane Wh [M][K] from the packed plane's qlh sub-plane, or
+// from the W_exp plane.
+cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s);
+cudaError_t launch_expand_wexp(const int8_t* wexp, int M, int K, __half* wh, cudaStream_t s);
 size_t mmq_tc_smem_bytes();
 cudaError_t mmq_tc_prepare();
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t s);
 
 // ---------------------------------------------------------- device helpers ---
 #if defined(__CUDACC__)
+#ifndef MBAR_POLL
+#define MBAR_POLL mbar_try_wait
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -98,21 +105,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete, giving up after `limit_ns`
-// or as soon as another thread of the CTA has given up (*abort != 0). On
-// expiry it records (site, timeout) in *status and sets *abort. Returns false
-// when it gave up.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete, giving up after about
+// `limit_ns` (measured with the SM cycle counter at up to 2.1 GHz, so the real
+// limit is at least that long) or as soon as another thread of the CTA has
+// given up (*abort != 0). On expiry it records (site, timeout) in *status and
+// sets *abort. Returns false when it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort, unsigned int* status,
                                                   uint32_t site,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  if (MBAR_POLL(bar, parity)) return true;
+  const long long limit_cycles = (long long)(limit_ns * 21ull / 10ull);
+  const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0u) {
+    if (MBAR_POLL(bar, parity)) return true;
+    if ((i & 63u) == 0u) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
+      if (clock64() - t0 > limit_cycles) {
         atomicOr(status, kStatusTimeout | (site << 8));
         *abort = 1;
         return false;
@@ -207,24 +228,33 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | ((uint32_t)(M >> 4) << 24);  // M >> 4
 }
 
-// Loads 2 x 16 consecutive 32-bit TMEM columns of this thread's lane (one
-// 32x32b.x16 load from each address) and waits for both.
-__device__ __forceinline__ void tmem_ld2x16(uint32_t a0, uint32_t a1, uint32_t (&r0)[16],
-                                            uint32_t (&r1)[16]) {
+// Issues one 32x32b.x32 TMEM load: 32 consecutive 32-bit columns of this
+// thread's lane. The registers are valid only after tmem_wait_ld4().
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]),
-        "=r"(r0[6]), "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]),
-        "=r"(r0[12]), "=r"(r0[13]), "=r"(r0[14]), "=r"(r0[15]), "=r"(r1[0]), "=r"(r1[1]),
-        "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]), "=r"(r1[7]),
-        "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]),
-        "=r"(r1[14]), "=r"(r1[15])
-      : "r"(a0), "r"(a1)
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(addr)
       : "memory");
+}
+// Waits for this thread's outstanding TMEM loads. The two arrays are in-out
+// operands so no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]), "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+               :
+               : "memory");
+}
+
+// Moves this warpgroup's per-thread register budget (all four warps of the
+// warpgroup must execute the same call).
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegs));
 }
 
 #endif  // __CUDACC__

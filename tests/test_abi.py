@@ -64,30 +64,36 @@ def test_host_side_rejections(lib):
     fake = ctypes.c_void_p(0x10000)          # never dereferenced: rejected before any use
     odd = ctypes.c_void_p(0x10004)
     path = ctypes.c_int(-1)
-    # K not a multiple of 256
-    assert lib.q6k_mmq(fake, None, 64, 300, fake, fake, fake, 64, fake, 64, None,
-                       ctypes.byref(path), None) == q6.Q6_EINVAL
+
+    def mmq(plane=fake, wexp=None, wh=None, M=64, K=256, xq=fake, da=fake, xh=fake, N=64,
+            Y=fake, ldy=64, ws=fake, ws_bytes=1 << 30, partials=None):
+        return lib.q6k_mmq(plane, wexp, wh, M, K, xq, da, xh, N, Y, ldy, ws, ws_bytes, partials,
+                           ctypes.byref(path), None)
+
+    assert mmq(K=300) == q6.Q6_EINVAL                       # K not a multiple of 256
     assert path.value == q6.PATH_NONE
-    # ldy < M
-    assert lib.q6k_mmq(fake, None, 64, 256, fake, fake, fake, 64, fake, 32, None, None,
-                       None) == q6.Q6_EINVAL
-    # N == 0 is a no-op
-    assert lib.q6k_mmq(fake, None, 64, 256, None, None, None, 0, fake, 64, None,
-                       ctypes.byref(path), None) == q6.Q6_OK
+    assert mmq(ldy=32) == q6.Q6_EINVAL                      # ldy < M
+    assert mmq(N=0, xq=None, da=None, xh=None) == q6.Q6_OK  # empty: a no-op
     assert path.value == q6.PATH_NONE
-    # missing operand plane for a prefill-sized N
-    assert lib.q6k_mmq(fake, None, 64, 256, fake, fake, None, 64, fake, 64, None, None,
-                       None) == q6.Q6_EINVAL
-    # misaligned da
-    assert lib.q6k_mmq(fake, None, 64, 256, fake, odd, fake, 64, fake, 64, None, None,
-                       None) == q6.Q6_EALIGN
+    assert mmq(xh=None) == q6.Q6_EINVAL                     # operand plane needed for N > 16
+    assert mmq(N=8, xq=None) == q6.Q6_EINVAL                # int8 activations needed for N <= 16
+    assert mmq(da=odd) == q6.Q6_EALIGN                      # misaligned da
+    assert mmq(ws=odd) == q6.Q6_EALIGN                      # misaligned workspace
+    assert mmq(ws=None) == q6.Q6_ESIZE                      # unpack needs a workspace
+    assert mmq(ws_bytes=64 * 256 * 2 - 1) == q6.Q6_ESIZE    # ... of M*K*2 bytes
+    size = ctypes.c_size_t()
+    assert lib.q6k_mmq_workspace_bytes(64, 256, 64, ctypes.byref(size)) == q6.Q6_OK
+    assert size.value == 64 * 256 * 2
+    assert lib.q6k_mmq_workspace_bytes(64, 256, 16, ctypes.byref(size)) == q6.Q6_OK
+    assert size.value == 0
     # quantiser: ldx < K, misaligned X, N == 0
     assert lib.q8_quantize_act(fake, 4, 256, 128, fake, fake, None, None) == q6.Q6_EINVAL
     assert lib.q8_quantize_act(odd, 4, 256, 256, fake, fake, None, None) == q6.Q6_EALIGN
     assert lib.q8_quantize_act(None, 0, 256, 256, None, None, None, None) == q6.Q6_OK
-    # pack: misaligned plane, missing raw
-    assert lib.q6k_pack_weights(fake, 4, 256, odd, None, None) == q6.Q6_EALIGN
-    assert lib.q6k_pack_weights(None, 4, 256, fake, None, None) == q6.Q6_EINVAL
+    # pack: misaligned plane or wh, missing raw
+    assert lib.q6k_pack_weights(fake, 4, 256, odd, None, None, None) == q6.Q6_EALIGN
+    assert lib.q6k_pack_weights(fake, 4, 256, fake, None, odd, None) == q6.Q6_EALIGN
+    assert lib.q6k_pack_weights(None, 4, 256, fake, None, None, None) == q6.Q6_EINVAL
     assert lib.q6_selftest_wait_timeout(0, None) == q6.Q6_EINVAL
 
 

@@ -64,10 +64,14 @@ def quant_check(act, X, orc):
     return xq_o, da_o
 
 
-def run_gemm(q6, raw, X, M, K, use_wexp, partials=False):
-    w = q6.pack_weights(dev(raw), M, K, wexp=use_wexp)
+SOURCES = ["raw", "wexp", "wh"]
+TC_PATH = {"raw": "tc_raw", "wexp": "tc_wexp", "wh": "tc_wh"}
+
+
+def run_gemm(q6, raw, X, M, K, source, partials=False):
+    w = q6.pack_weights(dev(raw), M, K, wexp=source == "wexp", wh=source == "wh")
     act = q6.quantize_act(dev(X))
-    Y, path, P = q6.mmq(w, act, use_wexp=use_wexp, partials=partials)
+    Y, path, P = q6.mmq(w, act, source=source, partials=partials)
     q6.sync_status()
     return w, act, Y, path, P
 
@@ -119,7 +123,7 @@ def test_quantize_strided_input(q6, orc):
 @pytest.mark.parametrize("M,K", [(64, 256), (40, 512), (24, 768), (131, 1024)])
 def test_pack_bitexact(q6, orc, M, K):
     raw = synth.q6k_raw_weights(200 + M, M, K)
-    w = q6.pack_weights(dev(raw), M, K, wexp=True)
+    w = q6.pack_weights(dev(raw), M, K, wexp=True, wh=True)
     q6.sync_status()
     plane = host(w.plane)
     blocks = raw.reshape(M, K // 256, 210)
@@ -141,6 +145,7 @@ def test_pack_bitexact(q6, orc, M, K):
     assert np.array_equal(d, blocks[:, :, 208:210])
     assert np.array_equal(host(w.wexp), orc.wexp(raw, M, K))
     assert np.array_equal(host(w.wexp).astype(np.int64), restate.int_values(raw, M, K))
+    assert np.array_equal(host(w.wh), orc.wexp(raw, M, K).astype(np.float16))
 
 
 # --------------------------------------------------------- GEMM, small ------
@@ -153,22 +158,19 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("use_wexp", [False, True], ids=["raw", "wexp"])
+@pytest.mark.parametrize("source", SOURCES)
 @pytest.mark.parametrize("M,K,N", SMALL, ids=lambda v: str(v))
-def test_mmq_small_bitexact_partials(q6, orc, M, K, N, use_wexp):
+def test_mmq_small_bitexact_partials(q6, orc, M, K, N, source):
     raw = synth.q6k_raw_weights(300 + M + N, M, K)
     X = synth.activations(400 + M + N, N, K, outlier_frac=0.02)
-    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, use_wexp, partials=True)
+    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, source, partials=True)
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-    if N <= q6.SKINNY_MAX_N:
-        assert path == "skinny"
-    else:
-        assert path == ("tc_wexp" if use_wexp else "tc_raw")
+    assert path == ("skinny" if N <= q6.SKINNY_MAX_N else TC_PATH[source])
     assert np.array_equal(host(P), Po), "sub-block partials differ"
     check_y(host(Y), Yo, f"{M}x{K}x{N}")
     # the fast (non-debug) variant gives the same Y
-    Y2, _, _ = q6.mmq(w, act, use_wexp=use_wexp)
+    Y2, _, _ = q6.mmq(w, act, source=source)
     q6.sync_status()
     check_y(host(Y2), Yo, "fast variant")
 
@@ -182,16 +184,16 @@ def test_mmq_degenerate_inputs(q6, orc):
     raw = np.tile(blk, (M, K // 256))
     X = synth.activations(5, N, K)
     for n in (N, 3):                         # tensor-core and skinny kernels
-        _, _, Y, _, _ = run_gemm(q6, raw, X[:n], M, K, False)
+        _, _, Y, _, _ = run_gemm(q6, raw, X[:n], M, K, "raw")
         assert np.all(host(Y) == 0.0)
     raw = synth.q6k_raw_weights(6, M, K).reshape(-1, 210).copy()
     raw[:, 208:210] = 0                      # d = 0 everywhere
-    _, _, Y, _, _ = run_gemm(q6, raw.reshape(M, -1), X, M, K, True)
+    _, _, Y, _, _ = run_gemm(q6, raw.reshape(M, -1), X, M, K, "wexp")
     assert np.all(host(Y) == 0.0)
     X0 = X.copy()
     X0[5] = 0.0                              # a zero token
     raw = synth.q6k_raw_weights(7, M, K)
-    _, _, Y, _, _ = run_gemm(q6, raw, X0, M, K, False)
+    _, _, Y, _, _ = run_gemm(q6, raw, X0, M, K, "wh")
     assert np.all(host(Y)[5] == 0.0)
 
 
@@ -213,8 +215,8 @@ def sampled_tokens(N, extra=()):
     return np.array(sorted(i for i in idx if 0 <= i < N))
 
 
-def check_full(q6, orc, raw, X, M, K, use_wexp, label, partial_tokens=0):
-    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, use_wexp)
+def check_full(q6, orc, raw, X, M, K, source, label):
+    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, source)
     xq_o, da_o = quant_check(act, X, orc)
     tok = sampled_tokens(X.shape[0])
     Yo = orc.mmq(raw, M, K, xq_o[tok], da_o[tok])
@@ -222,14 +224,14 @@ def check_full(q6, orc, raw, X, M, K, use_wexp, label, partial_tokens=0):
     return w, act, path
 
 
-@pytest.mark.parametrize("use_wexp", [False, True], ids=["raw", "wexp"])
-def test_attn_v_full(q6, orc, use_wexp):
+@pytest.mark.parametrize("source", SOURCES)
+def test_attn_v_full(q6, orc, source):
     raw, X, cfg = synth.workload("attn_v")
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
-    w, act, path = check_full(q6, orc, raw, X, M, K, use_wexp, "attn_v")
-    assert path == ("tc_wexp" if use_wexp else "tc_raw")
+    w, act, path = check_full(q6, orc, raw, X, M, K, source, "attn_v")
+    assert path == TC_PATH[source]
     # sub-block partials of four tokens, bit-exact
-    Y, _, P = q6.mmq(w, act, use_wexp=use_wexp, partials=True)
+    Y, _, P = q6.mmq(w, act, source=source, partials=True)
     q6.sync_status()
     tok = np.array([0, 129, 300, N - 1])
     xq_o, da_o = orc.quantize(X[tok])
@@ -237,10 +239,10 @@ def test_attn_v_full(q6, orc, use_wexp):
     assert np.array_equal(host(P[tok]), Po)
 
 
-@pytest.mark.parametrize("use_wexp", [False, True], ids=["raw", "wexp"])
-def test_ffn_down_full(q6, orc, use_wexp):
+@pytest.mark.parametrize("source", SOURCES)
+def test_ffn_down_full(q6, orc, source):
     raw, X, cfg = synth.workload("ffn_down")
-    check_full(q6, orc, raw, X, cfg["M"], cfg["K"], use_wexp, "ffn_down")
+    check_full(q6, orc, raw, X, cfg["M"], cfg["K"], source, "ffn_down")
 
 
 @pytest.mark.parametrize("weight", ["ffn_down", "attn_v"])
@@ -248,7 +250,7 @@ def test_ffn_down_full(q6, orc, use_wexp):
 def test_skinny_full(q6, orc, weight, N):
     raw, X, cfg = synth.skinny_workload(weight, N)
     M, K = cfg["M"], cfg["K"]
-    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, False, partials=True)
+    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, "raw", partials=True)
     assert path == "skinny"
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
@@ -260,5 +262,5 @@ def test_skinny_full(q6, orc, weight, N):
 def test_sweep_layers(q6, orc, layer):
     raw_v, raw_d = synth.sweep_layer(layer)
     X_v, X_d = synth.sweep_activations()
-    check_full(q6, orc, raw_v, X_v, 4096, 4096, False, f"sweep layer {layer} attn_v")
-    check_full(q6, orc, raw_d, X_d, 4096, 11008, False, f"sweep layer {layer} ffn_down")
+    check_full(q6, orc, raw_v, X_v, 4096, 4096, "raw", f"sweep layer {layer} attn_v")
+    check_full(q6, orc, raw_d, X_d, 4096, 11008, "raw", f"sweep layer {layer} ffn_down")
