@@ -169,6 +169,31 @@ int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, in
             void *workspace, size_t workspace_bytes, int32_t *partials, int *path_out,
             q6_stream_t s);
 
+/* ------------------------------------------------------------------------
+ * For callers that cannot allocate device memory when they make this call
+ * (code under a fixed budget or pool that forbids new allocations, or a
+ * latency-critical path that must never enter the allocator). The pages have
+ * no counterpart: this is an alternative way to run q6k_mmq.
+ *
+ * Computes what q6k_mmq computes with the weights unpacked per call (from
+ * wexp when not NULL, else from the packed plane; no resident wh plane and no
+ * workspace argument), but its scratch is one static device array of the
+ * library: 256 bytes for the kernel's status word plus 32 MiB for the
+ * unpacked binary16 weights, so for N > Q6_SKINNY_MAX_N it needs
+ * M * K <= 16,777,216 (a 4096 x 4096 layer) and returns Q6_ESIZE otherwise.
+ * Nothing on this path allocates; no partials (debug) output.
+ *
+ * The array is held by every GPU that loads this part of the library until
+ * the process exits. All calls share it and it keeps the last call's
+ * contents: calls that overlap on the GPU race on it. The status word is
+ * cleared on the call's stream at the start of every call; a bounded-wait
+ * time-out is recorded there and is not reported back. The first call on a
+ * device does the set-up (architecture check, kernel attributes, the array's
+ * device address) and should come before any stream capture. */
+int q6k_mmq_noalloc(const void *plane, const int8_t *wexp, int M, int K, const int8_t *Xq,
+                    const float *da, const uint16_t *Xh, int N, float *Y, int ldy, int *path_out,
+                    q6_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,6 +36,7 @@ SIGNATURES = [
     ("q6k_mmq_workspace_bytes", _I, [_I, _I, _I, _SZ]),
     ("q6k_mmq", _I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP,
                      _P]),
+    ("q6k_mmq_noalloc", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _IP, _P]),
 ]
 
 

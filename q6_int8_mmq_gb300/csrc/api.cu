@@ -94,6 +94,15 @@ int ldda_of(int N) { return (N + 3) / 4 * 4; }
 
 }  // namespace
 
+namespace q6 {
+// Records `code` and its text as the calling thread's last error (for the
+// entry points defined in other translation units).
+int record_error(int code, const char* fmt, va_list ap) {
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  return code;
+}
+}  // namespace q6
+
 extern "C" {
 
 const char* q6_last_error(void) { return g_err; }

@@ -1,0 +1,167 @@
+// q6k_mmq_noalloc: the q6_K x int8 GEMM for callers that cannot allocate
+// device memory when they call it -- for example code that runs under a
+// fixed memory budget or pool that forbids new allocations, or a latency-
+// critical path that must never enter the allocator.
+//
+// It computes what q6k_mmq computes with the weights unpacked per call, but
+// its scratch memory lives in one file-scope static device array instead of a
+// caller workspace or a library allocation: the first 256 bytes hold the
+// status word the tensor-core kernel records a bounded-wait time-out in, the
+// rest holds the binary16 weight plane the unpack pass writes (so M * K * 2
+// must fit in kScratchWeightBytes). Nothing on this path calls cudaMalloc,
+// cudaFree or any allocating routine.
+//
+// The array belongs to the module: every GPU that loads this part of the
+// library holds it until the process exits. All calls share it and it keeps
+// the last call's contents, so calls that overlap on the GPU (different
+// streams, or other devices' threads racing on the same device) race on it.
+// The status word is cleared on the call's stream at the start of each call.
+//
+// Set-up happens in the first call on each device (with that device
+// current): the architecture check, the kernels' shared-memory limits, the
+// tensor-map encoder and the array's device address (cudaGetSymbolAddress).
+// That first call should come before any stream capture.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "q6_internal.cuh"
+
+namespace q6 {
+int record_error(int code, const char* fmt, va_list ap);  // defined with q6_last_error()
+}
+
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kScratchWeightBytes = 32u << 20;  // a 4096 x 4096 layer in binary16
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kStatusBytes + kScratchWeightBytes];
+
+int na_fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  const int rc = q6::record_error(code, fmt, ap);
+  va_end(ap);
+  return rc;
+}
+
+struct NaDev {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
+};
+std::mutex g_na_mu;
+NaDev g_na_dev[64];
+PFN_cuTensorMapEncodeTiled_v12000 g_na_encode = nullptr;
+
+int na_setup(NaDev** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return na_fail(Q6_ECUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return na_fail(Q6_ECUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_na_mu);
+  NaDev& st = g_na_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)))
+      return na_fail(Q6_ECUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    if (major != 10 || minor != 3)
+      return na_fail(Q6_EARCH, "device %d is compute capability %d.%d; needs 10.3", dev, major,
+                     minor);
+    if ((e = q6::mmq_tc_prepare()))
+      return na_fail(Q6_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    void* addr = nullptr;
+    if ((e = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) || !addr)
+      return na_fail(Q6_ECUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    if (!g_na_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return na_fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
+      g_na_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.scratch = static_cast<unsigned char*>(addr);
+    st.ready = true;
+  }
+  *out = &st;
+  return Q6_OK;
+}
+
+bool na_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int na_encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swz) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_na_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? Q6_OK : na_fail(Q6_ECUDA, "cuTensorMapEncodeTiled failed: %d", (int)r);
+}
+
+}  // namespace
+
+extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int K,
+                               const int8_t* Xq, const float* da, const uint16_t* Xh, int N,
+                               float* Y, int ldy, int* path_out, q6_stream_t s) {
+  if (path_out) *path_out = Q6_PATH_NONE;
+  if (M <= 0 || K <= 0 || K % 256 || N < 0)
+    return na_fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
+  if (ldy < M) return na_fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
+  if (N == 0) return Q6_OK;
+  if (!plane || !da || !Y) return na_fail(Q6_EINVAL, "plane, da and Y are required");
+  const bool skinny = N <= Q6_SKINNY_MAX_N;
+  if (skinny && !Xq) return na_fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_SKINNY_MAX_N);
+  if (!skinny && !Xh) return na_fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
+  if (!na_aligned(plane, 256) || !na_aligned(da, 16) || !na_aligned(Y, 4) ||
+      (wexp && !na_aligned(wexp, 16)) || (Xq && !na_aligned(Xq, 16)) || (Xh && !na_aligned(Xh, 16)))
+    return na_fail(Q6_EALIGN, "plane 256 B; Xq, Xh, da, wexp 16 B; Y 4 B");
+  if (!skinny && (size_t)M * (size_t)K * 2 > kScratchWeightBytes)
+    return na_fail(Q6_ESIZE,
+                   "M*K*2 = %zu bytes exceeds this entry point's static scratch of %zu bytes "
+                   "(M*K <= %zu weights)",
+                   (size_t)M * (size_t)K * 2, kScratchWeightBytes, kScratchWeightBytes / 2);
+  if ((long long)N * ldy > (1LL << 40)) return na_fail(Q6_ESIZE, "problem too large");
+  NaDev* st;
+  int rc = na_setup(&st);
+  if (rc) return rc;
+  const int ldda = (N + 3) / 4 * 4;
+  cudaError_t e;
+  if (skinny) {
+    e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda, N, Y, ldy,
+                              nullptr, (cudaStream_t)s);
+    if (e != cudaSuccess) return na_fail(Q6_ECUDA, "skinny kernel launch: %s", cudaGetErrorString(e));
+    if (path_out) *path_out = Q6_PATH_SKINNY;
+    return Q6_OK;
+  }
+  unsigned int* status = reinterpret_cast<unsigned int*>(st->scratch);
+  __half* wh = reinterpret_cast<__half*>(st->scratch + kStatusBytes);
+  if ((e = cudaMemsetAsync(status, 0, sizeof(unsigned int), (cudaStream_t)s)))
+    return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
+  e = wexp ? q6::launch_expand_wexp(wexp, M, K, wh, (cudaStream_t)s)
+           : q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K, wh, (cudaStream_t)s);
+  if (e != cudaSuccess) return na_fail(Q6_ECUDA, "weight unpack launch: %s", cudaGetErrorString(e));
+  const q6::PlaneGeom g = q6::plane_geom(M, K);
+  const uint8_t* pb = static_cast<const uint8_t*>(plane);
+  q6::TcMaps maps;
+  if ((rc = na_encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
+      (rc = na_encode(&maps.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wh, (uint64_t)K, (uint64_t)M,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
+      (rc = na_encode(&maps.da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
+                      (uint64_t)ldda * 4, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+      (rc = na_encode(&maps.dsc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb + g.dsc_off, (uint64_t)K / 16,
+                      (uint64_t)M, (uint64_t)K / 16 * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
+    return rc;
+  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, nullptr, status, (cudaStream_t)s);
+  if (e != cudaSuccess) return na_fail(Q6_ECUDA, "tensor-core kernel launch: %s", cudaGetErrorString(e));
+  if (path_out) *path_out = wexp ? Q6_PATH_TC_WEXP : Q6_PATH_TC_RAW;
+  return Q6_OK;
+}
