@@ -43,7 +43,7 @@ constexpr int BM = 128, BN = 128;
 constexpr int KB = 64, SB = 5;   // operand ring: K per stage, stages
 constexpr int KS = 128, SS = 6;  // scale ring
 constexpr int kThreads = 384;                 // launched with 168 registers per thread
-constexpr int kCtlRegs = 56, kEpiRegs = 224;  // 128 * 56 + 256 * 224 == 384 * 168
+constexpr int kCtlRegs = 40, kEpiRegs = 232;  // 128 * 40 + 256 * 232 == 384 * 168
 static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * 168, "register split");
 constexpr int kEpiWarp0 = 4, kNumEpiWarps = 8;
 
@@ -249,8 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int j = 0; j < 16; ++j) accA[j] = accB[j] = make_float2(0.0f, 0.0f);
     uint32_t pA0[32], pA1[32], pB0[32], pB1[32];
-    float4 d0 = make_float4(0.f, 0.f, 0.f, 0.f), d1 = d0;  // dsc of the current scale stage
-    const float* sda = nullptr;
     bool ok = mbar_wait_warp(&bars->tfull[0], 0, abort_flag, status, kSiteTFull);
     if (ok) {
       tc_fence_after();
@@ -258,53 +256,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(lane_addr + 128u, pA1);
       tmem_wait_ld2(pA0, pA1);
     }
-    for (int c = 0; c < nc && ok; ++c) {
-      const int b = c & 1, q = c & 3, ks = c >> 2;
-      if (q == 0) {  // a new scale stage
-        const int ss = ks % SS;
-        if (!mbar_wait_warp(&bars->s_full[ss], (ks / SS) & 1, abort_flag, status, kSiteSFull)) {
-          ok = false;
-          break;
-        }
-        const uint8_t* st = smem + kRingS + ss * kScStage;
-        sda = reinterpret_cast<const float*>(st + kScDa) + 64 * colh;
-        d0 = reinterpret_cast<const float4*>(st + kScDsc + row * 32)[0];
-        d1 = reinterpret_cast<const float4*>(st + kScDsc + row * 32)[1];
-      }
-      const float s0 = (q == 0) ? d0.x : (q == 1) ? d0.z : (q == 2) ? d1.x : d1.z;
-      const float s1 = (q == 0) ? d0.y : (q == 1) ? d0.w : (q == 2) ? d1.y : d1.w;
-      const float2 s0v = make_float2(s0, s0), s1v = make_float2(s1, s1);
-      const float* dq = sda + q * 128;
-      // second half of this chunk in flight while the first half is scaled
-      tmem_ld32(lane_addr + (uint32_t)(b * 256 + 32), pB0);
-      tmem_ld32(lane_addr + (uint32_t)(b * 256 + 160), pB1);
-      rescale32(accA, pA0, pA1, s0v, s1v, dq);
-      dump_partials<kPartials>(partials, M, K, N, m, n0 + 64 * colh, (size_t)c * 2, pA0, pA1);
-      tmem_wait_ld2(pB0, pB1);
-      // both halves are in registers: the TMEM buffer can take chunk c + 2
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tempty[b]);
-      // first half of the next chunk in flight while the second half is scaled
-      bool next = c + 1 < nc;
-      if (next) {
-        next = mbar_wait_warp(&bars->tfull[b ^ 1], ((c + 1) >> 1) & 1, abort_flag, status,
-                              kSiteTFull);
-        if (next) {
-          tc_fence_after();
-          tmem_ld32(lane_addr + (uint32_t)((b ^ 1) * 256), pA0);
-          tmem_ld32(lane_addr + (uint32_t)((b ^ 1) * 256 + 128), pA1);
-        } else {
-          ok = false;
-        }
-      }
-      rescale32(accB, pB0, pB1, s0v, s1v, dq + 32);
-      dump_partials<kPartials>(partials, M, K, N, m, n0 + 64 * colh + 32, (size_t)c * 2, pB0, pB1);
-      if (next) tmem_wait_ld2(pA0, pA1);
-      if (q == 3) {  // done with this scale stage
+    // Outer loop: one scale stage (four 32-element chunks); inner loop unrolled,
+    // so the TMEM buffer (chunk & 1), the barrier parities and the scale
+    // selection are compile-time constants.
+    for (int ks = 0; ks < ns && ok; ++ks) {
+      const int ss = ks % SS;
+      if (!mbar_wait_warp(&bars->s_full[ss], (ks / SS) & 1, abort_flag, status, kSiteSFull)) break;
+      const uint8_t* st = smem + kRingS + ss * kScStage;
+      const float* sda = reinterpret_cast<const float*>(st + kScDa) + 64 * colh;
+      const float4 d0 = reinterpret_cast<const float4*>(st + kScDsc + row * 32)[0];
+      const float4 d1 = reinterpret_cast<const float4*>(st + kScDsc + row * 32)[1];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = 4 * ks + q;
+        const uint32_t b = (uint32_t)(q & 1);
+        const float s0 = q == 0 ? d0.x : q == 1 ? d0.z : q == 2 ? d1.x : d1.z;
+        const float s1 = q == 0 ? d0.y : q == 1 ? d0.w : q == 2 ? d1.y : d1.w;
+        const float2 s0v = make_float2(s0, s0), s1v = make_float2(s1, s1);
+        const float* dq = sda + q * 128;
+        // second half of this chunk in flight while the first half is scaled
+        tmem_ld32(lane_addr + b * 256u + 32u, pB0);
+        tmem_ld32(lane_addr + b * 256u + 160u, pB1);
+        rescale32(accA, pA0, pA1, s0v, s1v, dq);
+        dump_partials<kPartials>(partials, M, K, N, m, n0 + 64 * colh, (size_t)c * 2, pA0, pA1);
+        tmem_wait_ld2(pB0, pB1);
+        // both halves are in registers: the TMEM buffer can take chunk c + 2
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_empty[ks % SS]);
+        if (lane == 0) mbar_arrive(&bars->tempty[b]);
+        // First half of the next chunk in flight while the second half is
+        // scaled. The loads are unconditional (after the last chunk they
+        // re-read the other buffer, which no MMA writes any more): keeping the
+        // async loads and their wait out of branches lets them overlap the math.
+        if ((q < 3 || c + 1 < nc) &&
+            !mbar_wait_warp(&bars->tfull[b ^ 1u], (uint32_t)(((q + 1) >> 1) & 1), abort_flag, status,
+                            kSiteTFull))
+          ok = false;
+        tc_fence_after();
+        tmem_ld32(lane_addr + (b ^ 1u) * 256u, pA0);
+        tmem_ld32(lane_addr + (b ^ 1u) * 256u + 128u, pA1);
+        rescale32(accB, pB0, pB1, s0v, s1v, dq + 32);
+        dump_partials<kPartials>(partials, M, K, N, m, n0 + 64 * colh + 32, (size_t)c * 2, pB0, pB1);
+        tmem_wait_ld2(pA0, pA1);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_empty[ss]);
     }
     if (m < M) {
 #pragma unroll
