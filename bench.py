@@ -165,7 +165,7 @@ def run_reference(args):
     import numpy as np
     import oracle
     from q6_int8_mmq_gb300 import synth
-    raw, X, cfg = synth.workload(args.workload)
+    raw, X, cfg, config = workload_inputs(args, synth)
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     orc = oracle.get()
     # size one step (one token against `rows` weight rows) so the run takes ~1-2 min
@@ -192,7 +192,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(len(times), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(args, cfg),
+        "data": "synthetic", "config": config,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -203,19 +203,149 @@ def run_reference(args):
 def workload_config(args, cfg):
     return {"workload": f"{args.workload} q6_K GEMM M={cfg['M']} K={cfg['K']} N={cfg['N']}",
             "M": cfg["M"], "K": cfg["K"], "N": cfg["N"],
-            "weights": {"raw": "packed q6_K plane, unpacked to binary16 in a workspace per call",
+            "weights": {"raw": "packed q6_K plane, unpacked to the two binary16 operand "
+                               "planes in a workspace per call",
                         "wexp": "W_exp centered-int8 plane, converted per call",
-                        "wh": "resident binary16 operand plane"}[args.weights],
+                        "wh": "resident binary16 operand planes"}[args.weights],
             "step": "q8_quantize_act + q6k_mmq (weights packed once, off the step)",
             "l2": "inputs larger than L2 (146 MB f32 activation per step); 2 copies of every "
-                  "input used in turn",
+                  "input used in turn" if args.workload == "ffn_down" else
+                  "2 copies of every input used in turn (attn_v inputs fit in L2)",
             "parallelism": "replicas"}
+
+
+def skinny_config(args, M, K):
+    return {"workload": f"skinny q6_K GEMM ({args.skinny_weight} weights) M={M} K={K} "
+                        f"N={args.tokens}",
+            "M": M, "K": K, "N": args.tokens,
+            "step": "q8_quantize_act + q6k_mmq (skinny path)",
+            "l2": "weights rotated over packed copies totalling more than 4x L2",
+            "parallelism": "replicas"}
+
+
+def sweep_config(synth):
+    L, N = synth.SWEEP_LAYERS, synth.SWEEP_N
+    return {"workload": f"sweep: {L} layers x (attn_v 4096x4096 + ffn_down 4096x11008), N={N}",
+            "layers": L, "N": N,
+            "step": "per layer: q8_quantize_act + q6k_mmq (raw plane) for each weight",
+            "l2": "inputs larger than L2", "parallelism": "replicas"}
+
+
+def workload_inputs(args, synth):
+    """(raw weights, f32 activations, shape, config) of the reference arm's
+    workload; for the sweep, its layer-0 ffn_down GEMM."""
+    if args.workload == "skinny":
+        raw, X, cfg = synth.skinny_workload(args.skinny_weight, args.tokens)
+        return raw, X, cfg, skinny_config(args, cfg["M"], cfg["K"])
+    if args.workload == "sweep":
+        _, raw = synth.sweep_layer(0)
+        _, X = synth.sweep_activations()
+        return raw, X, dict(M=4096, K=11008, N=synth.SWEEP_N), sweep_config(synth)
+    raw, X, cfg = synth.workload(args.workload)
+    return raw, X, cfg, workload_config(args, cfg)
 
 
 # ------------------------------------------------------------ GPU arm ---
 
+def ev_pair():
+    import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def timed_region(step, steps: int, device, sampler_on: bool):
+    """Runs `steps` steps between a barrier + device synchronise on both sides,
+    with clocks sampled meanwhile. Returns (max-over-ranks ms, clock summary)."""
+    import torch
+    start, end = ev_pair()
+    sampler = ClockSampler(device.index) if sampler_on else None
+    if sampler:
+        sampler.__enter__()
+    barrier(device)
+    start.record()
+    for i in range(steps):
+        step(i)
+    end.record()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    if sampler:
+        sampler.__exit__(None, None, None)
+    return reduce_max(start.elapsed_time(end), device), (sampler.summary() if sampler else None)
+
+
+def kernel_ms(step, steps: int, marks: int):
+    """Per-kernel device times: runs `steps` steps, each recording `marks`
+    events on the launching stream between its kernels; returns the mean
+    duration between consecutive marks."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(steps)]
+    for i in range(steps):
+        step(i, evs[i])
+    torch.cuda.synchronize()
+    return [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs) for k in range(marks - 1)]
+
+
+def e2e_run(step_host, steps: int, device):
+    """End to end: each step copies its input from pinned host memory, runs the
+    path through the public API and copies the result back."""
+    import torch
+    for i in range(2):
+        step_host(i)
+    a, b = ev_pair()
+    barrier(device)
+    a.record()
+    for i in range(steps):
+        step_host(i)
+    b.record()
+    torch.cuda.synchronize(device)
+    return reduce_max(a.elapsed_time(b), device)
+
+
+def clocks_ok(clk) -> bool:
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    return clk is None or not (bad & set(clk.get("reasons", [])))
+
+
+def skinny_bytes(M, K, N):
+    """Algorithmic HBM bytes of one skinny GEMM: q6_K weights at 210 B per 256,
+    int8 activations + their per-32 scales, f32 output."""
+    return M * K * 210 / 256 + N * K + N * (K // 32) * 4 + 4 * N * M
+
+
+def skinny_kernel_times(q6, synth, device, iters: int = 20):
+    """Skinny (memory-bound) GEMM on the ffn_down and attn_v weights for
+    N = 1, 4, 16, weights rotated over copies totalling more than 4x L2.
+    Returns {name: {us, gbs, frac_hbm}} without the fraction."""
+    import torch
+    out = {}
+    for wname in ("ffn_down", "attn_v"):
+        M, K = synth.SKINNY_SHAPES[wname]
+        raw, _, _ = synth.skinny_workload(wname, 1)
+        raw_d = torch.from_numpy(raw).to(device)
+        R = max(4, (4 * 129 * 2 ** 20) // q6.plane_bytes(M, K)[0] + 1)
+        Ws = [q6.pack_weights(raw_d, M, K) for _ in range(R)]
+        del raw_d
+        for n in synth.SKINNY_N:
+            _, X, _ = synth.skinny_workload(wname, n)
+            act = q6.quantize_act(torch.from_numpy(X).to(device), want_xh=False)
+            Y = torch.empty((n, M), dtype=torch.float32, device=device)
+            for i in range(2 * R):
+                q6.mmq(Ws[i % R], act, Y=Y)
+            a, b = ev_pair()
+            a.record()
+            for i in range(iters * R):
+                q6.mmq(Ws[i % R], act, Y=Y)
+            b.record()
+            torch.cuda.synchronize()
+            q6.sync_status()
+            us = a.elapsed_time(b) / (iters * R) * 1e3
+            gbs = skinny_bytes(M, K, n) / us / 1e3
+            out[f"{wname}_N{n}"] = {"us": us, "gbs": gbs, "weight_copies": R,
+                                    "path": q6.mmq(Ws[0], act, Y=Y)[1]}
+        del Ws
+    return out
+
+
 def run_ours(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -232,30 +362,52 @@ def run_ours(args):
         q6build.build()
     barrier(device)
     q6.load()
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    {"ffn_down": run_gemm, "attn_v": run_gemm, "skinny": run_skinny,
+     "sweep": run_sweep}[args.workload](args, q6, synth, device, rank, world, peaks, hbm, hbm_src)
 
+
+def tensor_peak(peaks):
+    p = peaks.get("bf16_tflops_sustained")
+    if p is None:
+        return 1700.0, "fallback sustained bf16 (f16 has the same nominal dense rate)"
+    return p, "measured bf16 sustained (f16 has the same nominal dense rate)"
+
+
+def oracle_baseline(raw, X, M, K, budget, N):
+    ops, secs, ntok = time_oracle(raw, X, M, K, budget, N)
+    return {"value": ops / secs / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{ntok} of {N} tokens x all {M} weight rows (quantise + GEMM), "
+                      f"{secs:.1f} s single-threaded"}
+
+
+def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
+    """The prefill GEMM workloads (ffn_down, attn_v): one step = quantise the
+    step's f32 activation + q6k_mmq against weights packed at load time."""
+    import torch
     raw, X, cfg = synth.workload(args.workload)
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     src = args.weights
     R = 2
     raw_d = torch.from_numpy(raw).to(device)
-    # weights: R packed copies; pack timed with events
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
+    e0, e1 = ev_pair()
+    e0.record()
     Ws = [q6.pack_weights(raw_d, M, K, wexp=src == "wexp", wh=src == "wh") for _ in range(R)]
-    ev1.record()
+    e1.record()
     torch.cuda.synchronize()
-    pack_ms = ev0.elapsed_time(ev1) / R
+    pack_ms = e0.elapsed_time(e1) / R
     del raw_d
     Xs = [torch.from_numpy(X).to(device) for _ in range(R)]
     acts = [q6.alloc_activations(N, K, device) for _ in range(R)]
     Ys = [torch.empty((N, M), dtype=torch.float32, device=device) for _ in range(R)]
-    # operand plane the GEMM reads: resident (wh) or unpacked per step into a workspace
-    whs = [W.wh if src == "wh" else torch.empty((M, K), dtype=torch.float16, device=device)
+    # the operand plane the GEMM reads: resident (wh) or unpacked per step
+    whs = [W.wh if src == "wh" else torch.empty((2, M, K), dtype=torch.float16, device=device)
            for W in Ws]
-    path = None
+    path = [None]
 
     def step(i, ev=None):
-        nonlocal path
         j = i % R
         if ev is not None:
             ev[0].record()
@@ -266,51 +418,30 @@ def run_ours(args):
             q6.unpack_weights(Ws[j], out=whs[j], from_wexp=src == "wexp")
         if ev is not None:
             ev[2].record()
-        _, path, _ = q6.mmq(Ws[j], acts[j], Y=Ys[j], source="wh", wh=whs[j])
+        _, path[0], _ = q6.mmq(Ws[j], acts[j], Y=Ys[j], source="wh", wh=whs[j])
         if ev is not None:
             ev[3].record()
 
     for i in range(args.warmup):
         step(i)
     q6.sync_status()
-
-    mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4))
-           for _ in range(args.steps)]
-    start, end = mk()
-    sampler = ClockSampler(local_rank) if rank == 0 else None
-    if sampler:
-        sampler.__enter__()
-    barrier(device)
-    start.record()
-    for i in range(args.steps):
-        step(i, evs[i])
-    end.record()
-    torch.cuda.synchronize(device)
-    barrier(device)
-    if sampler:
-        sampler.__exit__(None, None, None)
+    max_ms, clk = timed_region(step, args.steps, device, rank == 0)
     q6.sync_status()
-    elapsed_ms = start.elapsed_time(end)
-    max_ms = reduce_max(elapsed_ms, device)
-    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    u_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    m_ms = [e[2].elapsed_time(e[3]) for e in evs]
-
+    q_ms, u_ms, m_ms = kernel_ms(step, max(20, min(args.steps, 200)), 4)
+    q6.sync_status()
     ops_per_step = 2.0 * M * N * K
     value = job_throughput(ops_per_step * args.steps, world, max_ms / 1e3) / 1e12
 
-    # q6k_mmq called with each weight source (unpack into its workspace + GEMM,
-    # or GEMM alone on the resident operand plane), shorter runs
     alt = {}
     if rank == 0 and args.alt_steps > 0:
+        # q6k_mmq with each weight source (unpack + GEMM, or the GEMM alone)
         raw_d = torch.from_numpy(raw).to(device)
         Wa = q6.pack_weights(raw_d, M, K, wexp=True, wh=True)
         del raw_d
         for other in ("raw", "wexp", "wh"):
             for i in range(3):
                 q6.mmq(Wa, acts[0], Y=Ys[0], source=other)
-            a, b = mk()
+            a, b = ev_pair()
             a.record()
             for i in range(args.alt_steps):
                 q6.mmq(Wa, acts[i % R], Y=Ys[i % R], source=other)
@@ -321,52 +452,38 @@ def run_ours(args):
             alt[other] = {"q6k_mmq_ms": ams, "q6k_mmq_tops": ops_per_step / ams / 1e9}
         del Wa
 
-    # end to end through the public API with host buffers
     e2e = None
     if args.e2e_steps > 0:
         Xh = torch.from_numpy(X).pin_memory()
         Yh = torch.empty((N, M), dtype=torch.float32).pin_memory()
-        for i in range(2):
-            Xs[0].copy_(Xh, non_blocking=True)
-            step(0)
-            Yh.copy_(Ys[0], non_blocking=True)
-        a, b = mk()
-        barrier(device)
-        a.record()
-        for i in range(args.e2e_steps):
+
+        def step_host(i):
             j = i % R
             Xs[j].copy_(Xh, non_blocking=True)
             step(i)
             Yh.copy_(Ys[j], non_blocking=True)
-        b.record()
-        torch.cuda.synchronize(device)
-        e_ms = reduce_max(a.elapsed_time(b), device)
+        e_ms = e2e_run(step_host, args.e2e_steps, device)
         q6.sync_status()
         e2e = {"value": job_throughput(ops_per_step * args.e2e_steps, world, e_ms / 1e3) / 1e12,
                "unit": UNIT, "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": N * M * 4,
                "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps}
 
+    others = {}
+    if rank == 0 and world == 1 and args.workload == "ffn_down" and args.other_configs:
+        others = other_configs(args, q6, synth, device, hbm)
+
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
-        ops, secs, ntok = time_oracle(raw, X, M, K, args.cpu_budget, N)
-        cpu = {"value": ops / secs / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{ntok} of {N} tokens x all {M} weight rows (quantise + GEMM), "
-                         f"{secs:.1f} s single-threaded"}
-
+        cpu = oracle_baseline(raw, X, M, K, args.cpu_budget, N)
     if rank != 0:
         return
-    peaks = measured_peaks()
-    mm = statistics.mean(m_ms)
-    qm = statistics.mean(q_ms)
-    um = statistics.mean(u_ms) if src != "wh" else 0.0
-    tflops = ops_per_step / mm / 1e9
-    peak_t = peaks.get("bf16_tflops_sustained")
-    peak_src = "measured bf16 sustained (f16 has the same nominal dense rate)"
-    if peak_t is None:
-        peak_t, peak_src = 1700.0, "fallback sustained"
-    hbm = peaks.get("hbm_gbs", 6800.0)
+    peak_t, peak_src = tensor_peak(peaks)
+    tflops = ops_per_step / m_ms / 1e9
     q_bytes = N * K * (4 + 1 + 2) + (K // 32) * N * 4
-    u_bytes = M * K * (1 if src == "wexp" else 0.75) + M * K * 2
+    # unpack: reads the codes (qlh 0.75 B or W_exp 1 B per weight) and sc
+    # (1/16 B), writes the two binary16 operand planes (4 B per weight)
+    u_bytes = M * K * ((1 if src == "wexp" else 0.75) + 1 / 16 + 4)
+    traffic = args.traffic if args.traffic is not None else TRAFFIC.get((args.workload, "mmq_tc"))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
@@ -374,23 +491,234 @@ def run_ours(args):
         "data": "synthetic", "config": workload_config(args, cfg),
         "roofline": {"bound": "tensor", "kernel": "mmq_tc_kernel (q6k_mmq on the operand plane)",
                      "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": tflops / peak_t, "peak_source": peak_src,
-                     "traffic": args.traffic,
+                     "frac": tflops / peak_t, "peak_source": peak_src, "traffic": traffic,
                      "algorithmic": f"2*M*N*K = {ops_per_step:.4g} flop per launch"},
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (2 if src == "wh" else 3) * args.steps,
-        "clocks": sampler.summary() if sampler else None,
+        "clocks": clk, "clocks_ok": clocks_ok(clk),
         "kernels": {
-            "q6k_mmq": {"ms": mm, "tflops": tflops, "path": path,
-                        "int8_tops_frac_of_4.5P": tflops / 4500.0},
-            "q8_quantize_act": {"ms": qm, "gbs": q_bytes / qm / 1e6,
-                                "frac_hbm": q_bytes / qm / 1e6 / hbm},
-            "q6k_unpack_weights": ({"ms": um, "gbs": u_bytes / um / 1e6,
-                                    "frac_hbm": u_bytes / um / 1e6 / hbm} if um else None),
+            "q6k_mmq": {"ms": m_ms, "tflops": tflops, "path": path[0],
+                        "frac_of_int8_4.5P": tflops / 4500.0},
+            "q8_quantize_act": {"ms": q_ms, "gbs": q_bytes / q_ms / 1e6,
+                                "frac_hbm": q_bytes / q_ms / 1e6 / hbm},
+            "q6k_unpack_weights": ({"ms": u_ms, "gbs": u_bytes / u_ms / 1e6,
+                                    "frac_hbm": u_bytes / u_ms / 1e6 / hbm}
+                                   if src != "wh" else None),
         },
-        "pack_ms": pack_ms, "other_weight_sources": alt,
+        "hbm_peak": {"gbs": hbm, "source": hbm_src},
+        "pack_ms": pack_ms, "other_weight_sources": alt, "other_configs": others,
     }
     print(json.dumps(line), flush=True)
+
+
+def other_configs(args, q6, synth, device, hbm):
+    """Short measurements of the other workloads beside the headline one: the
+    attn_v GEMM (q6k_mmq, raw plane and resident operand plane) and the skinny
+    memory-bound GEMM for N = 1, 4, 16."""
+    import torch
+    raw, X, cfg = synth.workload("attn_v")
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    raw_d = torch.from_numpy(raw).to(device)
+    W = q6.pack_weights(raw_d, M, K, wh=True)
+    act = q6.quantize_act(torch.from_numpy(X).to(device))
+    Y = torch.empty((N, M), dtype=torch.float32, device=device)
+    res = {}
+    for src in ("raw", "wh"):
+        for i in range(3):
+            q6.mmq(W, act, Y=Y, source=src)
+        a, b = ev_pair()
+        a.record()
+        for i in range(100):
+            q6.mmq(W, act, Y=Y, source=src)
+        b.record()
+        torch.cuda.synchronize()
+        q6.sync_status()
+        ms = a.elapsed_time(b) / 100
+        res[f"attn_v_{src}"] = {"ms": ms, "tops": 2.0 * M * N * K / ms / 1e9,
+                                "note": "inputs fit in L2 (back-to-back calls)"}
+    del W, raw_d
+    for k, v in skinny_kernel_times(q6, synth, device).items():
+        v["frac_hbm"] = v["gbs"] / hbm
+        res[f"skinny_{k}"] = v
+    return res
+
+
+def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
+    """The memory-bound case: N = --tokens (1, 4 or 16) tokens against the
+    ffn_down or attn_v weights. One step = quantise + q6k_mmq (skinny path),
+    weights rotated over copies totalling more than 4x L2."""
+    import torch
+    wname, n = args.skinny_weight, args.tokens
+    M, K = synth.SKINNY_SHAPES[wname]
+    raw, X, _ = synth.skinny_workload(wname, n)
+    raw_d = torch.from_numpy(raw).to(device)
+    R = max(4, (4 * 129 * 2 ** 20) // q6.plane_bytes(M, K)[0] + 1)
+    Ws = [q6.pack_weights(raw_d, M, K) for _ in range(R)]
+    del raw_d
+    Xd = torch.from_numpy(X).to(device)
+    act = q6.alloc_activations(n, K, device, want_xh=False)
+    Y = torch.empty((n, M), dtype=torch.float32, device=device)
+    path = [None]
+
+    def step(i, ev=None):
+        if ev is not None:
+            ev[0].record()
+        q6.quantize_act(Xd, out=act)
+        if ev is not None:
+            ev[1].record()
+        _, path[0], _ = q6.mmq(Ws[i % R], act, Y=Y)
+        if ev is not None:
+            ev[2].record()
+
+    for i in range(max(args.warmup, 2 * R)):
+        step(i)
+    q6.sync_status()
+    max_ms, clk = timed_region(step, args.steps, device, rank == 0)
+    q6.sync_status()
+    q_ms, m_ms = kernel_ms(step, max(20 * R, min(args.steps, 2000)), 3)
+    ops_per_step = 2.0 * M * n * K
+    value = job_throughput(ops_per_step * args.steps, world, max_ms / 1e3) / 1e12
+    e2e = None
+    if args.e2e_steps > 0:
+        Xh = torch.from_numpy(X).pin_memory()
+        Yh = torch.empty((n, M), dtype=torch.float32).pin_memory()
+
+        def step_host(i):
+            Xd.copy_(Xh, non_blocking=True)
+            step(i)
+            Yh.copy_(Y, non_blocking=True)
+        e_ms = e2e_run(step_host, args.e2e_steps, device)
+        e2e = {"value": job_throughput(ops_per_step * args.e2e_steps, world, e_ms / 1e3) / 1e12,
+               "unit": UNIT, "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": n * M * 4,
+               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps}
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        cpu = oracle_baseline(raw, X, M, K, args.cpu_budget, n)
+    if rank != 0:
+        return
+    alg = skinny_bytes(M, K, n)
+    gbs = alg / m_ms / 1e6
+    traffic = args.traffic if args.traffic is not None else TRAFFIC.get(
+        (f"skinny_{wname}_N{n}", "mmq_skinny"))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a -> f32",
+        "data": "synthetic",
+        "config": dict(skinny_config(args, M, K), weight_copies=R),
+        "roofline": {"bound": "hbm", "kernel": "mmq_skinny_kernel", "achieved": gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": gbs / hbm, "peak_source": hbm_src,
+                     "traffic": traffic,
+                     "algorithmic": f"M*K*210/256 + N*K + N*K/8 + 4*N*M = {alg:.4g} B per launch"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps,
+        "clocks": clk, "clocks_ok": clocks_ok(clk),
+        "kernels": {"q6k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
+                    "q8_quantize_act": {"us": q_ms * 1e3}},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
+    """The 32-layer 7B-shape prefill sweep: per layer, requantise the attn_v
+    stream X_v [3314,4096] and run the attn_v GEMM, then requantise X_d
+    [3314,11008] and run the ffn_down GEMM (both from the packed raw plane,
+    unpacked per call). One step = the whole sweep."""
+    import torch
+    L = synth.SWEEP_LAYERS
+    N = synth.SWEEP_N
+    layers = []
+    for l in range(L):
+        rv, rd = synth.sweep_layer(l)
+        wv = q6.pack_weights(torch.from_numpy(rv).to(device), 4096, 4096)
+        wd = q6.pack_weights(torch.from_numpy(rd).to(device), 4096, 11008)
+        layers.append((wv, wd))
+    resident = sum(w.plane.numel() for pair in layers for w in pair)
+    Xv, Xd = synth.sweep_activations()
+    Xvd, Xdd = torch.from_numpy(Xv).to(device), torch.from_numpy(Xd).to(device)
+    av, ad = q6.alloc_activations(N, 4096, device), q6.alloc_activations(N, 11008, device)
+    Yv = torch.empty((N, 4096), dtype=torch.float32, device=device)
+    Yd = torch.empty((N, 4096), dtype=torch.float32, device=device)
+    ws = torch.empty(q6.workspace_bytes(4096, 11008, N), dtype=torch.uint8, device=device)
+    marks = 1 + 4 * L
+
+    def step(i, ev=None):
+        k = 0
+        if ev is not None:
+            ev[0].record()
+        for wv, wd in layers:
+            q6.quantize_act(Xvd, out=av)
+            if ev is not None:
+                ev[k + 1].record()
+            q6.mmq(wv, av, Y=Yv, source="raw", workspace=ws)
+            if ev is not None:
+                ev[k + 2].record()
+            q6.quantize_act(Xdd, out=ad)
+            if ev is not None:
+                ev[k + 3].record()
+            q6.mmq(wd, ad, Y=Yd, source="raw", workspace=ws)
+            if ev is not None:
+                ev[k + 4].record()
+            k += 4
+
+    for i in range(args.warmup):
+        step(i)
+    q6.sync_status()
+    steps = args.steps
+    max_ms, clk = timed_region(step, steps, device, rank == 0)
+    q6.sync_status()
+    per = kernel_ms(step, 3, marks)
+    quant_ms = sum(per[k] for k in range(0, 4 * L, 2))
+    gemm_ms = sum(per[k] for k in range(1, 4 * L, 2))
+    ops_per_step = L * 2.0 * N * (4096 * 4096 + 4096 * 11008)
+    value = job_throughput(ops_per_step * steps, world, max_ms / 1e3) / 1e12
+    e2e = None
+    if args.e2e_steps > 0:
+        Xvh, Xdh = torch.from_numpy(Xv).pin_memory(), torch.from_numpy(Xd).pin_memory()
+        Yh = torch.empty((N, 4096), dtype=torch.float32).pin_memory()
+
+        def step_host(i):
+            Xvd.copy_(Xvh, non_blocking=True)
+            Xdd.copy_(Xdh, non_blocking=True)
+            step(i)
+            Yh.copy_(Yd, non_blocking=True)
+        e_steps = max(1, min(args.e2e_steps, 5))
+        e_ms = e2e_run(step_host, e_steps, device)
+        e2e = {"value": job_throughput(ops_per_step * e_steps, world, e_ms / 1e3) / 1e12,
+               "unit": UNIT, "h2d_bytes_per_step": Xv.nbytes + Xd.nbytes,
+               "d2h_bytes_per_step": N * 4096 * 4, "steps": e_steps,
+               "ms_per_step": e_ms / e_steps}
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        rv, rd = synth.sweep_layer(0)
+        c = oracle_baseline(rd, Xd, 4096, 11008, args.cpu_budget, N)
+        c["sample"] = "layer 0 ffn_down: " + c["sample"]
+        cpu = c
+    if rank != 0:
+        return
+    peak_t, peak_src = tensor_peak(peaks)
+    tflops = ops_per_step / gemm_ms / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": max_ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32 (exact int6 x int8)",
+        "data": "synthetic",
+        "config": dict(sweep_config(synth), resident_plane_bytes=resident),
+        "roofline": {"bound": "tensor", "kernel": "q6k_mmq (unpack + mmq_tc_kernel), all layers",
+                     "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": tflops / peak_t, "peak_source": peak_src, "traffic": None,
+                     "algorithmic": f"sum of 2*M*N*K = {ops_per_step:.4g} flop per sweep"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": L * 6 * steps,
+        "clocks": clk, "clocks_ok": clocks_ok(clk),
+        "kernels": {"gemm_total_ms": gemm_ms, "quantize_total_ms": quant_ms,
+                    "gemm_tops": tflops},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# DRAM bytes (read + write) per launch from ncu captures of the current
+# kernels, keyed by (workload, kernel); the capture each figure comes from is
+# summarised under profiles/.
+TRAFFIC = {}
 
 
 def main():
@@ -399,7 +727,13 @@ def main():
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="ffn_down", choices=["ffn_down", "attn_v"])
+    ap.add_argument("--workload", default="ffn_down",
+                    choices=["ffn_down", "attn_v", "skinny", "sweep"])
+    ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
+    ap.add_argument("--tokens", type=int, default=1, choices=[1, 4, 16],
+                    help="tokens of the skinny workload")
+    ap.add_argument("--no-other-configs", dest="other_configs", action="store_false",
+                    help="skip the attn_v and skinny measurements beside ffn_down")
     ap.add_argument("--weights", choices=["raw", "wexp", "wh"], default="raw")
     ap.add_argument("--alt-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=100)

@@ -9,8 +9,12 @@
  *   da per 32 elements; the product is rescaled per 16-element sub-block with
  *   sum += da * (d * sc), and there is no dmin term.
  *
- *   Y[n][m] = sum_k (d*sc*(q-32))[m][k] * (da*xq)[n][k], formed as one exact
- *   integer partial per (n, m, 16-element sub-block) and an f32 rescale.
+ *   Y[n][m] = sum_k (d*sc*(q-32))[m][k] * (da*xq)[n][k].
+ *
+ *   This library forms, per (n, m, 32-element chunk c), the exact integer
+ *   S = sum over the chunk's two sub-blocks s of sc[s] * P[s], where
+ *   P[s] = sum over the 16 elements of (q - 32) * xq, and then
+ *   Y = sum over super-blocks of d * (sum over their chunks of da * S) in f32.
  *
  * Conventions for every call:
  *   - Pointers marked "device" are device memory owned by the caller; the
@@ -51,7 +55,7 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_TC_RAW 1  /* unpack of the packed q6_K plane into the workspace + tensor-core GEMM */
 #define Q6_PATH_TC_WEXP 2 /* conversion of the W_exp plane into the workspace + tensor-core GEMM */
 #define Q6_PATH_SKINNY 3  /* CUDA-core kernel for N <= Q6_SKINNY_MAX_N on the packed q6_K plane */
-#define Q6_PATH_TC_WH 4   /* tensor-core GEMM on a resident binary16 operand plane */
+#define Q6_PATH_TC_WH 4   /* tensor-core GEMM on resident binary16 operand planes */
 
 #define Q6_SKINNY_MAX_N 16
 
@@ -102,8 +106,7 @@ int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da
 
 /* ------------------------------------------------------------------------
  * Weight packing (load time; "r53 -- q6_K bundle: W_exp pre-expansion
- * plane", Sec. 2.3 and 3.2, and "r42 -- q6_K stage-wide dsc scale reads",
- * Sec. 3.2 for the precomputed d*sc plane).
+ * plane", Sec. 2.3 and 3.2).
  *
  * raw: device bytes of an M x K q6_K weight in the GGUF layout: M rows, each
  *      K/256 consecutive 210-byte super-blocks (ql[128] @0, qh[64] @128,
@@ -115,18 +118,22 @@ int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da
  *         (super-block h/2, half h%2): bytes 0..63 = ql[64*(h%2) .. +63],
  *         bytes 64..95 = qh[32*(h%2) .. +31] of that super-block.
  *         Row stride 3*K/4 bytes.
- *   dsc : f32 [M][K/16] = f32(d) * sc for every 16-element sub-block (exact).
  *   sc  : int8 [M][K/16], the raw sub-block scales.
  *   d   : binary16 bits [M][K/256], the raw super-block scales.
+ *   dT  : f32 [K/256][ldm], ldm = M rounded up to a multiple of 4: the
+ *         super-block scales as f32 (exact), transposed; rows M..ldm-1 zero.
  * wexp (device, optional, 16-byte aligned): int8 [M][K], row stride K, the
- *      centered values q - 32 in [-32, 31] (the W_exp plane).
- * wh   (device, optional, 16-byte aligned): binary16 [M][K], row stride K,
- *      the same centered values as exact binary16: the operand-ready plane
- *      the tensor-core GEMM reads (2 bytes per weight).
+ *      centered values v = q - 32 in [-32, 31] (the W_exp plane).
+ * wh   (device, optional, 16-byte aligned): binary16 [2][M][K], the two
+ *      operand planes the tensor-core GEMM reads (4 bytes per weight), with
+ *      the sub-block scale folded in and split so both stay exact:
+ *      wh[0][m][k] = 16 * floor(sc/16) * v and wh[1][m][k] = (sc mod 16) * v,
+ *      sc the scale of k's sub-block; wh[0] + wh[1] = sc * v. (Zero may be
+ *      stored as -0.)
  * -------------------------------------------------------------------- */
 
-/* Byte sizes of the packed plane and of the W_exp plane (the wh plane is
- * twice the W_exp size). Either pointer may be NULL. */
+/* Byte sizes of the packed plane and of the W_exp plane (the wh planes are
+ * four times the W_exp size). Either pointer may be NULL. */
 int q6k_plane_bytes(int M, int K, size_t *plane_bytes, size_t *wexp_bytes);
 
 /* Fills `plane` (and `wexp`, `wh` when not NULL) from `raw`. M > 0,
@@ -134,11 +141,13 @@ int q6k_plane_bytes(int M, int K, size_t *plane_bytes, size_t *wexp_bytes);
 int q6k_pack_weights(const uint8_t *raw, int M, int K, void *plane, int8_t *wexp,
                      uint16_t *wh, q6_stream_t s);
 
-/* The weight unpack pass alone: writes the binary16 operand plane wh [M][K]
- * (the layout described above) from wexp when it is not NULL, else from the
- * packed plane's qlh sub-plane ("r41 -- q6_K B-expand widened to uint4 group
- * loads", Sec. 3.2: 16-element groups from one 16-byte ql run and one 16-byte
- * qh run). q6k_mmq runs this into its workspace when it gets no wh plane. */
+/* The weight unpack pass alone: writes the binary16 operand planes wh
+ * [2][M][K] (the layout described above) from wexp and the plane's sc
+ * sub-plane when wexp is not NULL, else from the packed plane's qlh and sc
+ * sub-planes ("r41 -- q6_K B-expand widened to uint4 group loads", Sec. 3.2:
+ * 16-element groups from one 16-byte ql run and one 16-byte qh run). plane is
+ * required in both cases. q6k_mmq runs this into its workspace when it gets
+ * no wh planes. */
 int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint16_t *wh,
                        q6_stream_t s);
 
@@ -151,13 +160,14 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *           kernel (N <= Q6_SKINNY_MAX_N).
  *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
  *   workspace : device scratch of at least q6k_mmq_workspace_bytes() bytes
- *           (256-byte aligned) when N > Q6_SKINNY_MAX_N and wh is NULL: the
- *           weights are first unpacked there (from wexp when given, else from
- *           the packed plane) into the binary16 operand layout. Unused
- *           otherwise. Its contents after the call are unspecified.
- *   partials : NULL, or device int32 [N][M][K/16] that receives every exact
- *           sub-block partial P[n][m][s] = sum over the 16 elements of
- *           (q - 32) * xq (a debug mode; slower).
+ *           (4 * M * K, 256-byte aligned) when N > Q6_SKINNY_MAX_N and wh is
+ *           NULL: the weights are first unpacked there (from wexp when given,
+ *           else from the packed plane) into the two binary16 operand planes.
+ *           Unused otherwise. Its contents after the call are unspecified.
+ *   partials : NULL, or device int32 [N][M][K/32] that receives every exact
+ *           chunk sum S[n][m][c] = sc[2c] * P[2c] + sc[2c+1] * P[2c+1], with
+ *           P[s] = sum over the 16 elements of sub-block s of (q - 32) * xq
+ *           (a debug mode; slower).
  *   path_out : NULL or receives a Q6_PATH_* code.
  * Alignment: plane, workspace 256 B; Xh, da, wexp, wh, Xq 16 B; Y 4 B.
  * Q6_ESIZE when the workspace is missing or too small.
@@ -178,8 +188,8 @@ int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, in
  * Computes what q6k_mmq computes with the weights unpacked per call (from
  * wexp when not NULL, else from the packed plane; no resident wh plane and no
  * workspace argument), but its scratch is one static device array of the
- * library: 256 bytes for the kernel's status word plus 32 MiB for the
- * unpacked binary16 weights, so for N > Q6_SKINNY_MAX_N it needs
+ * library: 256 bytes for the kernel's status word plus 64 MiB for the
+ * two unpacked binary16 operand planes, so for N > Q6_SKINNY_MAX_N it needs
  * M * K <= 16,777,216 (a 4096 x 4096 layer) and returns Q6_ESIZE otherwise.
  * Nothing on this path allocates; no partials (debug) output.
  *

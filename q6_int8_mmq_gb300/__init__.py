@@ -130,7 +130,8 @@ def quantize_act(X, out: Activations | None = None, want_xh: bool = True, stream
 
 class Weights:
     """A packed q6_K weight on the device: the packed plane, and optionally the
-    W_exp (int8) and operand-ready binary16 planes."""
+    W_exp (int8) plane and the resident operand planes wh [2, M, K] binary16
+    (W_hi, W_lo: the sub-block scale folded into the centered codes)."""
 
     def __init__(self, M, K, plane, wexp, wh):
         self.M, self.K, self.plane, self.wexp, self.wh = M, K, plane, wexp, wh
@@ -144,18 +145,19 @@ def pack_weights(raw, M: int, K: int, wexp: bool = False, wh: bool = False, stre
         raise Q6Error(Q6_EINVAL, "raw must be a CUDA uint8 tensor of M*K/256*210 bytes")
     plane = torch.empty(pb, dtype=torch.uint8, device=raw.device)
     w8 = torch.empty((M, K), dtype=torch.int8, device=raw.device) if wexp else None
-    w16 = torch.empty((M, K), dtype=torch.float16, device=raw.device) if wh else None
+    w16 = torch.empty((2, M, K), dtype=torch.float16, device=raw.device) if wh else None
     _check(load().q6k_pack_weights(_ptr(raw), M, K, _ptr(plane), _ptr(w8), _ptr(w16),
                                    _stream(stream)))
     return Weights(M, K, plane, w8, w16)
 
 
 def unpack_weights(w: Weights, out=None, from_wexp: bool = False, stream=None):
-    """The weight unpack pass: binary16 operand plane [M, K] from the packed
-    plane (or from the W_exp plane)."""
+    """The weight unpack pass: the binary16 operand planes [2, M, K] (W_hi,
+    W_lo) from the packed plane (or from the W_exp plane and the packed
+    plane's sub-block scales)."""
     import torch
     if out is None:
-        out = torch.empty((w.M, w.K), dtype=torch.float16, device=w.plane.device)
+        out = torch.empty((2, w.M, w.K), dtype=torch.float16, device=w.plane.device)
     src8 = w.wexp if from_wexp else None
     if from_wexp and src8 is None:
         raise Q6Error(Q6_EINVAL, "weights were packed without the W_exp plane")
@@ -186,7 +188,9 @@ def _workspace(nbytes: int, device):
 
 def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bool = False,
         workspace=None, wh=None, stream=None):
-    """Y [N, M] f32 = the q6_K x int8 GEMM. Returns (Y, path name, partials or None).
+    """Y [N, M] f32 = the q6_K x int8 GEMM. Returns (Y, path name, partials or None);
+    partials (debug) are the exact chunk sums S [N, M, K/32] int32 of
+    sc * (q - 32) * xq over each 32-element chunk.
 
     source: "raw" (unpack the packed plane), "wexp" (convert the W_exp plane),
     "wh" (resident binary16 plane) or "auto" (wh, else wexp, else raw)."""
@@ -203,7 +207,7 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
     dev = w.plane.device
     if Y is None:
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
-    P = torch.empty((N, M, K // 16), dtype=torch.int32, device=dev) if partials else None
+    P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
     ws_need = workspace_bytes(M, K, N) if w16 is None else 0
     ws = workspace if workspace is not None else (_workspace(ws_need, dev) if ws_need else None)
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0

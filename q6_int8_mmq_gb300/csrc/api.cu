@@ -95,6 +95,33 @@ int ldda_of(int N) { return (N + 3) / 4 * 4; }
 }  // namespace
 
 namespace q6 {
+// Tensor maps of one GEMM call: Xh [N][K] and the two weight operand planes
+// (W_hi at wop, W_lo at wop + M*K) as 64 x 128 boxes with the 128-byte
+// swizzle, da [K/32][ldda] as 128 tokens x 8 chunks, and the transposed d
+// sub-plane [K/256][ldm] as 128 rows x 1 super-block.
+int encode_tc_maps(TcMaps* maps, const uint8_t* plane, const void* wop, const void* Xh,
+                   const float* da, int M, int K, int N) {
+  const PlaneGeom g = plane_geom(M, K);
+  const uint16_t* whi = static_cast<const uint16_t*>(wop);
+  const uint16_t* wlo = whi + (size_t)M * (size_t)K;
+  int rc;
+  if ((rc = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Xh")) ||
+      (rc = encode_2d(&maps->whi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, whi, (uint64_t)K, (uint64_t)M,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "W_hi")) ||
+      (rc = encode_2d(&maps->wlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wlo, (uint64_t)K, (uint64_t)M,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "W_lo")) ||
+      (rc = encode_2d(&maps->da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
+                      (uint64_t)ldda_of(N) * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE, "da")) ||
+      (rc = encode_2d(&maps->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, plane + g.dt_off, (uint64_t)M,
+                      (uint64_t)K / 256, (uint64_t)g.ldm * 4, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      "d")))
+    return rc;
+  return Q6_OK;
+}
+}  // namespace q6
+
+namespace q6 {
 // Records `code` and its text as the calling thread's last error (for the
 // entry points defined in other translation units).
 int record_error(int code, const char* fmt, va_list ap) {
@@ -197,16 +224,17 @@ int q6k_pack_weights(const uint8_t* raw, int M, int K, void* plane, int8_t* wexp
 int q6k_unpack_weights(const void* plane, const int8_t* wexp, int M, int K, uint16_t* wh,
                        q6_stream_t s) {
   if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
-  if (!wh || (!plane && !wexp)) return fail(Q6_EINVAL, "wh and one of plane, wexp are required");
-  if ((plane && !aligned(plane, 256)) || (wexp && !aligned(wexp, 16)) || !aligned(wh, 16))
+  if (!wh || !plane) return fail(Q6_EINVAL, "plane and wh are required");
+  if (!aligned(plane, 256) || (wexp && !aligned(wexp, 16)) || !aligned(wh, 16))
     return fail(Q6_EALIGN, "plane 256 B; wexp, wh 16 B");
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
-  cudaError_t e = wexp ? q6::launch_expand_wexp(wexp, M, K, reinterpret_cast<__half*>(wh),
+  const uint8_t* pb = static_cast<const uint8_t*>(plane);
+  cudaError_t e = wexp ? q6::launch_expand_wexp(wexp, pb, M, K, reinterpret_cast<__half*>(wh),
                                                 (cudaStream_t)s)
-                       : q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K,
-                                               reinterpret_cast<__half*>(wh), (cudaStream_t)s);
+                       : q6::launch_expand_raw(pb, M, K, reinterpret_cast<__half*>(wh),
+                                               (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "q6k_unpack_weights launch");
   return Q6_OK;
 }
@@ -214,7 +242,7 @@ int q6k_unpack_weights(const void* plane, const int8_t* wexp, int M, int K, uint
 int q6k_mmq_workspace_bytes(int M, int K, int N, size_t* bytes) {
   if (M <= 0 || K <= 0 || K % 256 || N < 0 || !bytes)
     return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0, bytes != NULL");
-  *bytes = N > Q6_SKINNY_MAX_N ? (size_t)M * (size_t)K * 2 : 0;
+  *bytes = N > Q6_SKINNY_MAX_N ? (size_t)M * (size_t)K * 4 : 0;
   return Q6_OK;
 }
 
@@ -239,7 +267,7 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
     return fail(Q6_ESIZE, "problem too large");
   if (!skinny && !wh) {
-    const size_t need = (size_t)M * (size_t)K * 2;
+    const size_t need = (size_t)M * (size_t)K * 4;
     if (!workspace || workspace_bytes < need)
       return fail(Q6_ESIZE, "workspace of %zu bytes needed to unpack the weights (got %zu)", need,
                   workspace ? workspace_bytes : (size_t)0);
@@ -256,34 +284,22 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
     return Q6_OK;
   }
   int path = Q6_PATH_TC_WH;
+  const uint8_t* pb = static_cast<const uint8_t*>(plane);
   const void* wop = wh;
   if (!wh) {
     __half* ws = static_cast<__half*>(workspace);
     if (wexp) {
-      e = q6::launch_expand_wexp(wexp, M, K, ws, (cudaStream_t)s);
+      e = q6::launch_expand_wexp(wexp, pb, M, K, ws, (cudaStream_t)s);
       path = Q6_PATH_TC_WEXP;
     } else {
-      e = q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K, ws, (cudaStream_t)s);
+      e = q6::launch_expand_raw(pb, M, K, ws, (cudaStream_t)s);
       path = Q6_PATH_TC_RAW;
     }
     if (e != cudaSuccess) return cuda_fail(e, "weight unpack launch");
     wop = ws;
   }
-  const q6::PlaneGeom g = q6::plane_geom(M, K);
-  const uint8_t* pb = static_cast<const uint8_t*>(plane);
   q6::TcMaps maps;
-  if ((rc = encode_2d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Xh")))
-    return rc;
-  if ((rc = encode_2d(&maps.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wop, (uint64_t)K, (uint64_t)M,
-                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Wh")))
-    return rc;
-  if ((rc = encode_2d(&maps.da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
-                      (uint64_t)ldda_of(N) * 4, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE, "da")))
-    return rc;
-  if ((rc = encode_2d(&maps.dsc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb + g.dsc_off, (uint64_t)K / 16,
-                      (uint64_t)M, (uint64_t)K / 16 * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE, "dsc")))
-    return rc;
+  if ((rc = encode_tc_maps(&maps, pb, wop, Xh, da, M, K, N))) return rc;
   e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, partials, st->status, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
   if (path_out) *path_out = path;

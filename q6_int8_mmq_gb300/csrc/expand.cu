@@ -1,17 +1,24 @@
-// Weight unpack pass: q6_K codes -> the binary16 operand plane Wh [M][K]
-// that the tensor-core GEMM stages with TMA.
+// Weight unpack pass: q6_K codes and sub-block scales -> the two binary16
+// operand planes W_hi, W_lo [M][K] that the tensor-core GEMM stages with TMA.
 //
 // Element map ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 3.2; the
 // 16-element group form of "r41 -- q6_K B-expand widened to uint4 group
 // loads", Sec. 3.2): within a 128-element half block, 16-element group g
 // takes its low 4 bits from the 16 ql bytes at 16*(g mod 4) (low nibble for
 // g < 4, high nibble otherwise) and its high 2 bits from field (g/2) mod 4 of
-// the 16 qh bytes at 16*(g mod 2); the value is code - 32, in [-32, 31]. The
-// W_exp source ("r53 -- q6_K bundle: W_exp pre-expansion plane", Sec. 2.3)
-// already holds the centered values as int8.
+// the 16 qh bytes at 16*(g mod 2); the value is v = code - 32, in [-32, 31].
+// The W_exp source ("r53 -- q6_K bundle: W_exp pre-expansion plane",
+// Sec. 2.3) already holds v as int8. Each 16-element group is one sub-block.
 //
-// Both kernels are bandwidth-bound: one thread per 16 elements, two 16-byte
-// loads (raw) or one (W_exp), two 16-byte stores.
+// The sub-block scale sc (int8) is folded into the operand, split so both
+// parts stay exact in binary16: sc = 16*sh + sl with sh = floor(sc/16) in
+// [-8, 7] and sl in [0, 15]; W_hi = 16*sh*v (|.| <= 4096, a multiple of 16
+// with at most 9 significant bits) and W_lo = sl*v (|.| <= 480). So
+// W_hi + W_lo = sc * v exactly, and two MMAs over the same activation
+// operand give the integer sum of sc * v * xq of a sub-block.
+//
+// Both kernels are bandwidth-bound: one thread per 16 elements, one or two
+// 16-byte loads and one sc byte, four 16-byte stores.
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -42,17 +49,41 @@ __device__ __forceinline__ void i8_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-__global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restrict__ qlh, int M, int K,
+// o[8] (sixteen binary16 v) -> W_hi and W_lo runs of one sub-block.
+__device__ __forceinline__ void store_folded(const uint32_t (&o)[8], int sc, __half* hi, __half* lo) {
+  const int sh = sc >> 4, sl = sc & 15;  // arithmetic shift: floor(sc / 16)
+  const __half2 fh = __half2half2(__int2half_rn(16 * sh));
+  const __half2 fl = __half2half2(__int2half_rn(sl));
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const __half2 v = *reinterpret_cast<const __half2*>(&o[w]);
+    const __half2 a = __hmul2(v, fh), b = __hmul2(v, fl);
+    h[w] = *reinterpret_cast<const uint32_t*>(&a);
+    l[w] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  uint4* dh = reinterpret_cast<uint4*>(hi);
+  uint4* dl = reinterpret_cast<uint4*>(lo);
+  dh[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  dh[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  dl[0] = make_uint4(l[0], l[1], l[2], l[3]);
+  dl[1] = make_uint4(l[4], l[5], l[6], l[7]);
+}
+
+__global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restrict__ qlh,
+                                                         const int8_t* __restrict__ sc, int M, int K,
                                                          size_t qlh_row, __half* __restrict__ wh) {
   const int groups = K / 16;
   const long long items = (long long)M * groups;
   const long long stride = (long long)gridDim.x * blockDim.x;
+  const size_t plane = (size_t)M * K;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
     const int m = (int)(i / groups), r = (int)(i - (long long)m * groups);
     const int hb = r >> 3, g = r & 7;  // half block, group within it
     const uint8_t* src = qlh + (size_t)m * qlh_row + (size_t)hb * 96;
     const uint4 L = __ldg(reinterpret_cast<const uint4*>(src + 16 * (g & 3)));
     const uint4 H = __ldg(reinterpret_cast<const uint4*>(src + 64 + 16 * (g & 1)));
+    const int s = __ldg(sc + i);
     const int nsh = 4 * (g >> 2), fsh = 2 * ((g >> 1) & 3);
     const uint32_t Lw[4] = {L.x, L.y, L.z, L.w}, Hw[4] = {H.x, H.y, H.z, H.w};
     uint32_t o[8];
@@ -61,25 +92,25 @@ __global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restri
       const uint32_t code = ((Lw[w] >> nsh) & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
       codes_to_f16(code, o[2 * w], o[2 * w + 1]);
     }
-    uint4* dst = reinterpret_cast<uint4*>(wh + (size_t)m * K + (size_t)r * 16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    const size_t off = (size_t)m * K + (size_t)r * 16;
+    store_folded(o, s, wh + off, wh + plane + off);
   }
 }
 
-__global__ void __launch_bounds__(256) expand_wexp_kernel(const int8_t* __restrict__ wexp, long long n16,
+__global__ void __launch_bounds__(256) expand_wexp_kernel(const int8_t* __restrict__ wexp,
+                                                          const int8_t* __restrict__ sc, long long n16,
                                                           __half* __restrict__ wh) {
   const long long stride = (long long)gridDim.x * blockDim.x;
+  const size_t plane = (size_t)n16 * 16;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(wexp) + i);
+    const int s = __ldg(sc + i);
     uint32_t o[8];
     i8_to_f16(v.x, o[0], o[1]);
     i8_to_f16(v.y, o[2], o[3]);
     i8_to_f16(v.z, o[4], o[5]);
     i8_to_f16(v.w, o[6], o[7]);
-    uint4* dst = reinterpret_cast<uint4*>(wh) + 2 * i;
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    store_folded(o, s, wh + 16 * (size_t)i, wh + plane + 16 * (size_t)i);
   }
 }
 
@@ -93,14 +124,17 @@ unsigned grid_for(long long items) {
 
 cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
-  expand_raw_kernel<<<grid_for((long long)M * (K / 16)), 256, 0, s>>>(plane + g.qlh_off, M, K,
-                                                                      g.qlh_row, wh);
+  expand_raw_kernel<<<grid_for((long long)M * (K / 16)), 256, 0, s>>>(
+      plane + g.qlh_off, reinterpret_cast<const int8_t*>(plane + g.sc_off), M, K, g.qlh_row, wh);
   return cudaGetLastError();
 }
 
-cudaError_t launch_expand_wexp(const int8_t* wexp, int M, int K, __half* wh, cudaStream_t s) {
+cudaError_t launch_expand_wexp(const int8_t* wexp, const uint8_t* plane, int M, int K, __half* wh,
+                               cudaStream_t s) {
+  const PlaneGeom g = plane_geom(M, K);
   const long long n16 = (long long)M * K / 16;
-  expand_wexp_kernel<<<grid_for(n16), 256, 0, s>>>(wexp, n16, wh);
+  expand_wexp_kernel<<<grid_for(n16), 256, 0, s>>>(
+      wexp, reinterpret_cast<const int8_t*>(plane + g.sc_off), n16, wh);
   return cudaGetLastError();
 }
 

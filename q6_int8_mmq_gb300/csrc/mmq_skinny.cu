@@ -65,8 +65,9 @@ __global__ void __launch_bounds__(kWarps * 32) mmq_skinny_kernel(
       }
       const int sa = 8 * half + s4;  // sub-block (0..15) of the low nibbles; sb_b = sa + 4
       const float d = __half2float(__ushort_as_half(d_row[sb]));
-      const float dsc_a = d * (float)sc_row[16 * sb + sa];
-      const float dsc_b = d * (float)sc_row[16 * sb + sa + 4];
+      const int sc_a = sc_row[16 * sb + sa], sc_b = sc_row[16 * sb + sa + 4];
+      const float dsc_a = d * (float)sc_a;
+      const float dsc_b = d * (float)sc_b;
       const int ka = 256 * sb + 16 * sa;  // first element of sub-block a
       const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
 #pragma unroll
@@ -88,9 +89,17 @@ __global__ void __launch_bounds__(kWarps * 32) mmq_skinny_kernel(
           acc[n] = fmaf(dsc_a * daa, (float)pa, acc[n]);
           acc[n] = fmaf(dsc_b * dab, (float)pb, acc[n]);
           if (kPartials) {
-            int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 16) + (size_t)sb * 16;
-            pr[sa] = pa;
-            pr[sa + 4] = pb;
+            // chunk partials sc*P summed over the chunk's two sub-blocks; the
+            // other sub-block of each chunk is in lane ^ 1 (active together)
+            const unsigned act = __activemask();
+            const int ta = sc_a * pa, tb = sc_b * pb;
+            const int sa2 = ta + __shfl_xor_sync(act, ta, 1);
+            const int sb2 = tb + __shfl_xor_sync(act, tb, 1);
+            if ((s4 & 1) == 0) {
+              int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 32) + (size_t)sb * 8;
+              pr[sa >> 1] = sa2;
+              pr[(sa + 4) >> 1] = sb2;
+            }
           }
         }
       }

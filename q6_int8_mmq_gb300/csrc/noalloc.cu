@@ -7,8 +7,8 @@
 // its scratch memory lives in one file-scope static device array instead of a
 // caller workspace or a library allocation: the first 256 bytes hold the
 // status word the tensor-core kernel records a bounded-wait time-out in, the
-// rest holds the binary16 weight plane the unpack pass writes (so M * K * 2
-// must fit in kScratchWeightBytes). Nothing on this path calls cudaMalloc,
+// rest holds the two binary16 weight operand planes the unpack pass writes
+// (so M * K * 4 must fit in kScratchWeightBytes). Nothing on this path calls cudaMalloc,
 // cudaFree or any allocating routine.
 //
 // The array belongs to the module: every GPU that loads this part of the
@@ -36,7 +36,7 @@ int record_error(int code, const char* fmt, va_list ap);  // defined with q6_las
 namespace {
 
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kScratchWeightBytes = 32u << 20;  // a 4096 x 4096 layer in binary16
+constexpr size_t kScratchWeightBytes = 64u << 20;  // a 4096 x 4096 layer: two binary16 planes
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kStatusBytes + kScratchWeightBytes];
 
 int na_fail(int code, const char* fmt, ...) {
@@ -123,11 +123,11 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
   if (!na_aligned(plane, 256) || !na_aligned(da, 16) || !na_aligned(Y, 4) ||
       (wexp && !na_aligned(wexp, 16)) || (Xq && !na_aligned(Xq, 16)) || (Xh && !na_aligned(Xh, 16)))
     return na_fail(Q6_EALIGN, "plane 256 B; Xq, Xh, da, wexp 16 B; Y 4 B");
-  if (!skinny && (size_t)M * (size_t)K * 2 > kScratchWeightBytes)
+  if (!skinny && (size_t)M * (size_t)K * 4 > kScratchWeightBytes)
     return na_fail(Q6_ESIZE,
-                   "M*K*2 = %zu bytes exceeds this entry point's static scratch of %zu bytes "
+                   "M*K*4 = %zu bytes exceeds this entry point's static scratch of %zu bytes "
                    "(M*K <= %zu weights)",
-                   (size_t)M * (size_t)K * 2, kScratchWeightBytes, kScratchWeightBytes / 2);
+                   (size_t)M * (size_t)K * 4, kScratchWeightBytes, kScratchWeightBytes / 4);
   if ((long long)N * ldy > (1LL << 40)) return na_fail(Q6_ESIZE, "problem too large");
   NaDev* st;
   int rc = na_setup(&st);
@@ -145,20 +145,23 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
   __half* wh = reinterpret_cast<__half*>(st->scratch + kStatusBytes);
   if ((e = cudaMemsetAsync(status, 0, sizeof(unsigned int), (cudaStream_t)s)))
     return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
-  e = wexp ? q6::launch_expand_wexp(wexp, M, K, wh, (cudaStream_t)s)
-           : q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K, wh, (cudaStream_t)s);
+  const uint8_t* pb = static_cast<const uint8_t*>(plane);
+  e = wexp ? q6::launch_expand_wexp(wexp, pb, M, K, wh, (cudaStream_t)s)
+           : q6::launch_expand_raw(pb, M, K, wh, (cudaStream_t)s);
   if (e != cudaSuccess) return na_fail(Q6_ECUDA, "weight unpack launch: %s", cudaGetErrorString(e));
   const q6::PlaneGeom g = q6::plane_geom(M, K);
-  const uint8_t* pb = static_cast<const uint8_t*>(plane);
+  const __half* wlo = wh + (size_t)M * (size_t)K;
   q6::TcMaps maps;
   if ((rc = na_encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
                       (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-      (rc = na_encode(&maps.w, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wh, (uint64_t)K, (uint64_t)M,
+      (rc = na_encode(&maps.whi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wh, (uint64_t)K, (uint64_t)M,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
+      (rc = na_encode(&maps.wlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wlo, (uint64_t)K, (uint64_t)M,
                       (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
       (rc = na_encode(&maps.da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
-                      (uint64_t)ldda * 4, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-      (rc = na_encode(&maps.dsc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb + g.dsc_off, (uint64_t)K / 16,
-                      (uint64_t)M, (uint64_t)K / 16 * 4, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
+                      (uint64_t)ldda * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+      (rc = na_encode(&maps.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb + g.dt_off, (uint64_t)M,
+                      (uint64_t)K / 256, (uint64_t)g.ldm * 4, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE)))
     return rc;
   e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, nullptr, status, (cudaStream_t)s);
   if (e != cudaSuccess) return na_fail(Q6_ECUDA, "tensor-core kernel launch: %s", cudaGetErrorString(e));

@@ -1,5 +1,5 @@
 // Load-time weight packing: raw GGUF q6_K super-blocks -> the packed plane
-// (qlh / dsc / sc / d sub-planes) and, optionally, the W_exp plane.
+// (qlh / sc / d / d^T sub-planes) and, optionally, the W_exp plane.
 //
 // Element map ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 3.2): a
 // super-block is two 128-element halves; inside half h, element r takes its
@@ -7,9 +7,11 @@
 // high 2 bits from field floor(r/32) of qh[32h + r%32]; the value is code - 32.
 // The qlh sub-plane keeps each half's 64 ql bytes and 32 qh bytes together so
 // one 96-byte TMA row carries everything the unpack of that half needs.
-// dsc = f32(d) * sc per sub-block ("r42 -- q6_K stage-wide dsc scale reads",
-// Sec. 3.2; exact in f32). W_exp = centered int8, row stride K ("r53 -- q6_K
-// bundle: W_exp pre-expansion plane", Sec. 2.3).
+// The super-block scale d is kept twice: as the raw binary16 bits [M][K/256]
+// and as f32 transposed to [K/256][ldm] (weight rows contiguous, rows M..ldm-1
+// zero) so the GEMM can stage the d of 128 rows with one TMA copy. W_exp =
+// centered int8, row stride K ("r53 -- q6_K bundle: W_exp pre-expansion
+// plane", Sec. 2.3).
 //
 // One warp per super-block: lanes copy the 192 ql/qh bytes, the scales and,
 // for W_exp, expand eight elements each.
@@ -37,13 +39,13 @@ __global__ void __launch_bounds__(256) q6k_pack_kernel(const uint8_t* __restrict
     }
     const uint16_t dbits = (uint16_t)(src[208] | (src[209] << 8));
     if (lane < 16) {
-      const float d = __half2float(__ushort_as_half(dbits));
-      const int8_t sc = (int8_t)src[192 + lane];
       const size_t si = (size_t)m * (K / 16) + (size_t)b * 16 + lane;
-      reinterpret_cast<float*>(plane + g.dsc_off)[si] = d * (float)sc;
-      reinterpret_cast<int8_t*>(plane + g.sc_off)[si] = sc;
+      reinterpret_cast<int8_t*>(plane + g.sc_off)[si] = (int8_t)src[192 + lane];
     } else if (lane == 16) {
       reinterpret_cast<uint16_t*>(plane + g.d_off)[(size_t)m * nsb + b] = dbits;
+    } else if (lane == 17) {
+      reinterpret_cast<float*>(plane + g.dt_off)[(size_t)b * g.ldm + m] =
+          __half2float(__ushort_as_half(dbits));
     }
     if (wexp != nullptr) {
       // lane -> ql byte pair group: half h = lane / 16, bytes j0 = 4*(lane % 16) .. +3,
@@ -65,6 +67,13 @@ __global__ void __launch_bounds__(256) q6k_pack_kernel(const uint8_t* __restrict
       reinterpret_cast<uint32_t*>(dst + 64 + j0)[0] = hi_word;
     }
   }
+  // rows M .. ldm-1 of the transposed d sub-plane
+  const int pad = g.ldm - M;
+  const long long npad = (long long)pad * nsb;
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  for (long long i = tid; i < npad; i += (long long)gridDim.x * blockDim.x)
+    reinterpret_cast<float*>(plane + g.dt_off)[(size_t)(i / pad) * g.ldm + M + (size_t)(i % pad)] =
+        0.0f;
 }
 
 }  // namespace

@@ -20,19 +20,21 @@ constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 // Packed-plane geometry (all offsets 256-byte aligned).
 struct PlaneGeom {
-  size_t qlh_off, dsc_off, sc_off, d_off, total;
+  size_t qlh_off, sc_off, d_off, dt_off, total;
   size_t qlh_row;  // 3K/4 bytes
+  int ldm;         // row stride (elements) of the transposed d sub-plane: M rounded up to 4
 };
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline PlaneGeom plane_geom(int M, int K) {
   PlaneGeom g;
   const size_t m = (size_t)M, k = (size_t)K;
+  g.ldm = (M + 3) / 4 * 4;
   g.qlh_row = k / 128 * 96;
   g.qlh_off = 0;
-  g.dsc_off = round_up(m * g.qlh_row, 256);
-  g.sc_off = g.dsc_off + round_up(m * (k / 16) * 4, 256);
+  g.sc_off = round_up(m * g.qlh_row, 256);
   g.d_off = g.sc_off + round_up(m * (k / 16), 256);
-  g.total = g.d_off + round_up(m * (k / 256) * 2, 256);
+  g.dt_off = g.d_off + round_up(m * (k / 256) * 2, 256);
+  g.total = g.dt_off + round_up((k / 256) * (size_t)g.ldm * 4, 256);
   return g;
 }
 
@@ -47,17 +49,20 @@ cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* 
                               cudaStream_t s);
 
 struct TcMaps {
-  CUtensorMap x;    // Xh  [N][K] f16, box {64, 128}, 128B swizzle
-  CUtensorMap w;    // Wh  [M][K] f16, box {64, 128}, 128B swizzle
-  CUtensorMap da;   // da  [K/32][ldda] f32, box {128, 4}
-  CUtensorMap dsc;  // dsc [M][K/16] f32, box {8, 128}
+  CUtensorMap x;    // Xh   [N][K] f16, box {64, 128}, 128B swizzle
+  CUtensorMap whi;  // W_hi [M][K] f16, box {64, 128}, 128B swizzle
+  CUtensorMap wlo;  // W_lo [M][K] f16, box {64, 128}, 128B swizzle
+  CUtensorMap da;   // da   [K/32][ldda] f32, box {128, 8}
+  CUtensorMap d;    // d^T  [K/256][ldm] f32, box {128, 1}
 };
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                           int32_t* partials, unsigned int* status, cudaStream_t s);
-// Binary16 operand plane Wh [M][K] from the packed plane's qlh sub-plane, or
-// from the W_exp plane.
+// The two binary16 operand planes W_hi, W_lo [M][K] (W_lo at wh + M*K) with
+// the sub-block scale folded in, from the packed plane's qlh and sc
+// sub-planes, or from the W_exp plane and the sc sub-plane.
 cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s);
-cudaError_t launch_expand_wexp(const int8_t* wexp, int M, int K, __half* wh, cudaStream_t s);
+cudaError_t launch_expand_wexp(const int8_t* wexp, const uint8_t* plane, int M, int K, __half* wh,
+                               cudaStream_t s);
 size_t mmq_tc_smem_bytes();
 cudaError_t mmq_tc_prepare();
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t s);

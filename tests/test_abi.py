@@ -46,7 +46,8 @@ def test_plane_sizes(lib):
     pb, wb = q6.plane_bytes(4096, 11008)
     M, K = 4096, 11008
     r = lambda x: (x + 255) // 256 * 256
-    assert pb == r(M * K * 3 // 4) + r(M * K // 16 * 4) + r(M * K // 16) + r(M * K // 256 * 2)
+    ldm = (M + 3) // 4 * 4
+    assert pb == r(M * K * 3 // 4) + r(M * K // 16) + r(M * K // 256 * 2) + r(K // 256 * ldm * 4)
     assert wb == M * K
     xq, dab, xh, ldda = q6.act_plane_bytes(3314, 11008)
     assert (xq, xh, ldda) == (3314 * 11008, 3314 * 11008 * 2, 3316)
@@ -80,10 +81,10 @@ def test_host_side_rejections(lib):
     assert mmq(da=odd) == q6.Q6_EALIGN                      # misaligned da
     assert mmq(ws=odd) == q6.Q6_EALIGN                      # misaligned workspace
     assert mmq(ws=None) == q6.Q6_ESIZE                      # unpack needs a workspace
-    assert mmq(ws_bytes=64 * 256 * 2 - 1) == q6.Q6_ESIZE    # ... of M*K*2 bytes
+    assert mmq(ws_bytes=64 * 256 * 4 - 1) == q6.Q6_ESIZE    # ... of M*K*4 bytes
     size = ctypes.c_size_t()
     assert lib.q6k_mmq_workspace_bytes(64, 256, 64, ctypes.byref(size)) == q6.Q6_OK
-    assert size.value == 64 * 256 * 2
+    assert size.value == 64 * 256 * 4
     assert lib.q6k_mmq_workspace_bytes(64, 256, 16, ctypes.byref(size)) == q6.Q6_OK
     assert size.value == 0
     # quantiser: ldx < K, misaligned X, N == 0

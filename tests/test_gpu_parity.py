@@ -1,7 +1,10 @@
 """Parity of the CUDA library with the CPU oracle (needs a GB300).
 
-Integer results (quantised activations, packed planes, sub-block partials) must
-be bit-exact. Y must satisfy the floating-point tolerance of the method:
+Integer results (quantised activations, packed planes, chunk partials) must
+be bit-exact. The kernels' debug output is the exact integer chunk sum
+S[n][m][c] = sum over the chunk's two sub-blocks s of sc[m][s] * P[n][m][s];
+the expected S is formed here from the oracle's sub-block partials P and the
+raw sub-block scales. Y must satisfy the floating-point tolerance of the method:
 max|Y - Yo| <= 1e-3 * max|Yo| and sum|Y - Yo| / sum|Yo| <= 1e-5 (the normwise
 reading of "mean relative error"). Full-size workloads are checked on sampled
 tokens against all weight rows, in the launch configuration the benchmark uses.
@@ -62,6 +65,16 @@ def quant_check(act, X, orc):
     if act.xh is not None:
         assert np.array_equal(host(act.xh).astype(np.float32), xq_o.astype(np.float32))
     return xq_o, da_o
+
+
+def chunk_sums(Po, raw, M, K):
+    """Exact chunk sums from the oracle's sub-block partials Po [N][M][K/16]
+    and the raw sub-block scales sc (int8 bytes 192..207 of each block)."""
+    sc = raw.reshape(M, K // 256, 210)[:, :, 192:208].view(np.int8).reshape(M, K // 16)
+    S = (Po.astype(np.int64) * sc.astype(np.int64)[None]).reshape(Po.shape[0], M, K // 32, 2)
+    S = S.sum(-1)
+    assert np.abs(S).max() < 2 ** 31
+    return S.astype(np.int32)
 
 
 SOURCES = ["raw", "wexp", "wh"]
@@ -128,24 +141,40 @@ def test_pack_bitexact(q6, orc, M, K):
     plane = host(w.plane)
     blocks = raw.reshape(M, K // 256, 210)
     r = lambda x: (x + 255) // 256 * 256
-    qlh_sz, dsc_sz, sc_sz = M * K * 3 // 4, M * K // 16 * 4, M * K // 16
-    o_dsc = r(qlh_sz)
-    o_sc = o_dsc + r(dsc_sz)
+    ldm = (M + 3) // 4 * 4
+    qlh_sz, sc_sz, d_sz = M * K * 3 // 4, M * K // 16, M * K // 256 * 2
+    o_sc = r(qlh_sz)
     o_d = o_sc + r(sc_sz)
+    o_dt = o_d + r(d_sz)
+    assert plane.size == o_dt + r(K // 256 * ldm * 4)
     # qlh: per half h of super-block b: ql[64h:64h+64] then qh[32h:32h+32]
     qlh = plane[:qlh_sz].reshape(M, K // 256, 2, 96)
     for h in range(2):
         assert np.array_equal(qlh[:, :, h, :64], blocks[:, :, 64 * h: 64 * h + 64])
         assert np.array_equal(qlh[:, :, h, 64:], blocks[:, :, 128 + 32 * h: 160 + 32 * h])
-    dsc = plane[o_dsc:o_dsc + dsc_sz].view(np.float32).reshape(M, K // 16)
-    assert np.array_equal(dsc, orc.dsc(raw, M, K))
     sc = plane[o_sc:o_sc + sc_sz].view(np.int8).reshape(M, K // 256, 16)
     assert np.array_equal(sc, blocks[:, :, 192:208].view(np.int8))
-    d = plane[o_d:o_d + M * K // 256 * 2].reshape(M, K // 256, 2)
+    d = plane[o_d:o_d + d_sz].reshape(M, K // 256, 2)
     assert np.array_equal(d, blocks[:, :, 208:210])
-    assert np.array_equal(host(w.wexp), orc.wexp(raw, M, K))
+    # d transposed to [K/256][ldm] as f32, rows M..ldm-1 zero
+    dt = plane[o_dt:o_dt + K // 256 * ldm * 4].view(np.float32).reshape(K // 256, ldm)
+    d_f64 = np.array([[orc.f16_to_f64(int(b[0]) | (int(b[1]) << 8)) for b in row] for row in d])
+    assert np.array_equal(dt[:, :M].astype(np.float64), d_f64.T)
+    assert np.all(dt[:, M:] == 0)
+    v = orc.wexp(raw, M, K)
+    assert np.array_equal(host(w.wexp), v)
     assert np.array_equal(host(w.wexp).astype(np.int64), restate.int_values(raw, M, K))
-    assert np.array_equal(host(w.wh), orc.wexp(raw, M, K).astype(np.float16))
+    # resident operand planes: W_hi = 16*floor(sc/16)*v, W_lo = (sc mod 16)*v
+    sc16 = np.repeat(sc.reshape(M, K // 16).astype(np.int64), 16, axis=1)
+    sh = np.floor_divide(sc16, 16)
+    wh = host(w.wh).astype(np.float64)
+    assert wh.shape == (2, M, K)
+    assert np.array_equal(wh[0], 16 * sh * v)
+    assert np.array_equal(wh[1], (sc16 - 16 * sh) * v)
+    assert np.array_equal(wh[0] + wh[1], sc16 * v)
+    # the unpack pass from the W_exp plane gives the same planes
+    assert np.array_equal(host(q6.unpack_weights(w, from_wexp=True)).astype(np.float64), wh)
+    assert np.array_equal(host(q6.unpack_weights(w)).astype(np.float64), wh)
 
 
 # --------------------------------------------------------- GEMM, small ------
@@ -167,7 +196,7 @@ def test_mmq_small_bitexact_partials(q6, orc, M, K, N, source):
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
     assert path == ("skinny" if N <= q6.SKINNY_MAX_N else TC_PATH[source])
-    assert np.array_equal(host(P), Po), "sub-block partials differ"
+    assert np.array_equal(host(P), chunk_sums(Po, raw, M, K)), "chunk partials differ"
     check_y(host(Y), Yo, f"{M}x{K}x{N}")
     # the fast (non-debug) variant gives the same Y
     Y2, _, _ = q6.mmq(w, act, source=source)
@@ -195,6 +224,38 @@ def test_mmq_degenerate_inputs(q6, orc):
     raw = synth.q6k_raw_weights(7, M, K)
     _, _, Y, _, _ = run_gemm(q6, raw, X0, M, K, "wh")
     assert np.all(host(Y)[5] == 0.0)
+
+
+@pytest.mark.parametrize("N", [128, 4])
+def test_mmq_extreme_chunk_sums_exact(q6, orc, N):
+    """Chunk sums at the edge of the exact range: |v| = 32, |xq| = 127 and the
+    sub-block scales whose W_hi part is largest (sc = -128, -113: 16*floor(sc/16)
+    = -128), alone and mixed with positive scales and signs, so the MMA
+    accumulator passes through partial sums close to 2^24."""
+    M, K = 128, 512
+    nblk = M * (K // 256)
+    blocks = np.zeros((nblk, 210), np.uint8)
+    rng = np.random.default_rng(11)
+    codes_max = rng.random(nblk) < 0.5
+    codes_max[0] = False                                            # block 0: every v = -32
+    blocks[:, 0:192] = np.where(codes_max[:, None], 0xFF, 0x00)   # every code 63 or 0
+    scs = np.array([-128, -113, 127, -1, -128, -128, 112, -113], np.int8)
+    for i in range(nblk):
+        blocks[i, 192:208] = scs[(i + np.arange(16)) % len(scs)].view(np.uint8)
+    blocks[:, 208:210] = [0x00, 0x3C]                               # d = 1.0
+    raw = blocks.reshape(M, -1)
+    X = np.ones((N, K), np.float32)
+    X[1::2] *= -1.0                                                 # +-1 rows: xq = +-127
+    X[0, 256:] = np.where(np.arange(256) % 3 == 0, -1.0, 1.0)
+    for source in ("raw", "wh"):
+        w, act, Y, path, P = run_gemm(q6, raw, X, M, K, source, partials=True)
+        xq_o, da_o = quant_check(act, X, orc)
+        assert np.abs(xq_o).min() == 127
+        Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+        S = chunk_sums(Po, raw, M, K)
+        assert np.abs(S).max() == 32 * 128 * 32 * 127                # the bound is reached
+        assert np.array_equal(host(P), S)
+        check_y(host(Y), Yo, f"extreme N={N}")
 
 
 def test_mmq_empty(q6):
@@ -230,13 +291,13 @@ def test_attn_v_full(q6, orc, source):
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     w, act, path = check_full(q6, orc, raw, X, M, K, source, "attn_v")
     assert path == TC_PATH[source]
-    # sub-block partials of four tokens, bit-exact
+    # chunk partials of four tokens, bit-exact
     Y, _, P = q6.mmq(w, act, source=source, partials=True)
     q6.sync_status()
     tok = np.array([0, 129, 300, N - 1])
     xq_o, da_o = orc.quantize(X[tok])
     _, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-    assert np.array_equal(host(P[tok]), Po)
+    assert np.array_equal(host(P[tok]), chunk_sums(Po, raw, M, K))
 
 
 @pytest.mark.parametrize("source", SOURCES)
@@ -254,7 +315,7 @@ def test_skinny_full(q6, orc, weight, N):
     assert path == "skinny"
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-    assert np.array_equal(host(P), Po)
+    assert np.array_equal(host(P), chunk_sums(Po, raw, M, K))
     check_y(host(Y), Yo, f"skinny {weight} N={N}")
 
 
