@@ -38,14 +38,15 @@
 // TMEM: four accumulator buffers of 128 columns (chunk c uses buffer c % 4).
 // Warp roles (12 warps; warpgroup 0 gives registers to warpgroups 1-2):
 //   0      TMA producer for both rings.
-//   1      TMEM allocation (512 columns); lane 0 issues the MMAs and commits
-//          each chunk's buffer to its "full" barrier.
-//   2-3    idle (their registers go to the epilogue).
+//   1      TMEM allocation (512 columns); lane 0 issues the MMAs of the first
+//          chunk of every operand stage and commits its buffer.
+//   2      lane 0 issues the MMAs of the second chunk of every stage.
+//   3      idle (its registers go to the epilogue).
 //   4-11   epilogue: warp w owns TMEM lanes 32(w%4).. (32 tokens) and 64
-//          weight-row columns. Per chunk it loads its 64 words in two halves
-//          of 32, software-pipelined across chunks (the load of one half
-//          overlaps the math of the other), and frees the buffer as soon as
-//          both halves are in registers.
+//          weight-row columns. Per chunk it loads its 64 words, frees the
+//          buffer as soon as they are in registers and then does the math, so
+//          a buffer is back with the MMA issuer about two barrier hops after
+//          its chunk completes (the buffers, not the math, pace the pipeline).
 // Every mbarrier wait is bounded (see q6_internal.cuh).
 #include "q6_internal.cuh"
 
@@ -135,13 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < SB; ++s) {
       mbar_init(&bars->b_full[s], 1);
-      mbar_init(&bars->b_empty[s], 1);
+      mbar_init(&bars->b_empty[s], 2);  // both MMA-issuing threads
     }
     for (int b = 0; b < kNumBufs; ++b) {
       mbar_init(&bars->tfull[b], 1);
       mbar_init(&bars->tempty[b], kNumEpiWarps);
     }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->drain, 2);
     bars->abort = 0;
     mbar_fence_init();
   }
@@ -208,43 +209,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(&bars->b_full[k % SB], (k / SB) & 1, &no_abort, status, kSiteBFull);
         }
       }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 2) {
       // --------------------------------------------------------------- MMA --
+      // Two issuing threads: warp 1 takes the first chunk of every operand
+      // stage, warp 2 the second. tcgen05.mma issue stalls until the tensor
+      // pipe has room, so while one thread waits on a barrier or commits, the
+      // other keeps the pipe fed. Each thread commits only its own MMAs.
       if (lane == 0) {
         constexpr uint32_t idesc = idesc_f16_f32(BT, BW);
-        int gk = 0, gc = 0;  // operand stages consumed, chunks issued
+        const int q = warp - 1;  // chunk of the stage: 0 or 1
+        int gk = 0;              // operand stages consumed
         bool ok = true;
         for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-          for (int kb = 0; kb < nb && ok; ++kb) {
+          for (int kb = 0; kb < nb && ok; ++kb, ++gk) {
             const int slot = gk % SB;
+            const int gc = 2 * gk + q;  // global chunk index
+            const int b = gc & 3;
             if (!(ok = mbar_wait_bounded(&bars->b_full[slot], (gk / SB) & 1, abort_flag, status,
                                          kSiteBFull)))
               break;
+            if (!(ok = mbar_wait_bounded(&bars->tempty[b], ((gc >> 2) & 1) ^ 1, abort_flag, status,
+                                         kSiteTEmpty)))
+              break;
             tc_fence_after();
+            // descriptors of the stage's three tiles; a K step of 16 elements
+            // (32 bytes) adds 2 to the start-address field
             const uint8_t* bt = smem + slot * kOpStage;
-            const uint32_t x_base = smem_u32(bt + kOpX);
-            const uint32_t hi_base = smem_u32(bt + kOpWhi), lo_base = smem_u32(bt + kOpWlo);
-            for (int q = 0; q < 2; ++q, ++gc) {
-              const int b = gc & 3;
-              if (!(ok = mbar_wait_bounded(&bars->tempty[b], ((gc >> 2) & 1) ^ 1, abort_flag,
-                                           status, kSiteTEmpty)))
-                break;
-              tc_fence_after();
-              const uint32_t d_tmem = tmem + (uint32_t)(b * kBufCols);
+            const uint64_t xdesc = sw128_kmajor_desc(smem_u32(bt + kOpX));
+            const uint64_t hdesc = sw128_kmajor_desc(smem_u32(bt + kOpWhi));
+            const uint64_t ldesc = sw128_kmajor_desc(smem_u32(bt + kOpWlo));
+            const uint32_t d_tmem = tmem + (uint32_t)(b * kBufCols);
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const uint32_t koff = (uint32_t)((2 * q + h) * 32);  // sub-block within the stage
-                const uint64_t xd = sw128_kmajor_desc(x_base + koff);
-                umma_f16(d_tmem, xd, sw128_kmajor_desc(hi_base + koff), idesc, (uint32_t)h);
-                umma_f16(d_tmem, xd, sw128_kmajor_desc(lo_base + koff), idesc, 1u);
-              }
-              umma_commit(&bars->tfull[b]);
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t koff = (uint64_t)((2 * q + h) * 2);  // sub-block within the stage
+              umma_f16(d_tmem, xdesc + koff, hdesc + koff, idesc, (uint32_t)h);
+              umma_f16(d_tmem, xdesc + koff, ldesc + koff, idesc, 1u);
             }
-            if (ok) umma_commit(&bars->b_empty[slot]);
-            ++gk;
+            umma_commit(&bars->tfull[b]);
+            umma_commit(&bars->b_empty[slot]);
           }
         }
-        // Every MMA must be finished before TMEM is released.
+        // Every MMA of both threads must be finished before TMEM is released.
         umma_commit(&bars->drain);
         volatile int no_abort = 0;
         mbar_wait_bounded(&bars->drain, 0, &no_abort, status, kSiteDrain);
@@ -263,16 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pA[32], pB[32];
     int gs = 0;
     bool ok = true;
-    const int t_first = blockIdx.x;
-    const int t_last = t_first + ((T - 1 - t_first) / (int)gridDim.x) * (int)gridDim.x;
-    if (t_first < T) {
-      ok = mbar_wait_warp(&bars->tfull[0], 0, abort_flag, status, kSiteTFull);
-      tc_fence_after();
-      tmem_ld32(lane_addr, pA);
-      tmem_ld32(lane_addr + 32u, pB);
-      tmem_wait_ld2(pA, pB);
-    }
-    for (int t = t_first; t < T && ok; t += gridDim.x) {
+    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
       const int m0 = (t / NT) * BW, n0 = (t % NT) * BT;
       const int n = n0 + tok;
       const int mcol = m0 + 64 * colh;
@@ -286,40 +282,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint8_t* st = smem + kRingS + slot * kScStage;
         const float* sda = reinterpret_cast<const float*>(st + kScDa) + tok;
-        const bool last_stage = (t == t_last) && (s == nsb - 1);
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          const uint32_t b = (uint32_t)(cc & 3), bn = (uint32_t)((cc + 1) & 3);
-          const float da = sda[cc * BT];
+          // Chunk 8s + cc sits in buffer cc % 4 (a tile has a multiple of 8
+          // chunks), in its use (cc / 4) % 2 of this super-block's pair.
+          const uint32_t b = (uint32_t)(cc & 3);
           const int c = 8 * s + cc;
-          // second half of this chunk in flight while the first half is scaled
+          if (!mbar_wait_warp(&bars->tfull[b], (uint32_t)((cc >> 2) & 1), abort_flag, status,
+                              kSiteTFull))
+            ok = false;
+          tc_fence_after();
+          tmem_ld32(lane_addr + b * kBufCols, pA);
           tmem_ld32(lane_addr + b * kBufCols + 32u, pB);
-          if (cc == 0)
-            chunk_fma<true>(sb, pA, da);
-          else
-            chunk_fma<false>(sb, pA, da);
-          dump_partials<kPartials>(partials, M, N, nc, n, mcol, c, pA);
+          const float da = sda[cc * BT];
           tmem_wait_ld2(pA, pB);
-          // both halves are in registers: the buffer can take chunk c + 4
+          // the chunk is in registers: free the buffer before the math
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->tempty[b]);
-          // First half of the next chunk in flight while the second half is
-          // scaled. The loads are unconditional (after the CTA's last chunk
-          // they re-read a buffer no MMA writes any more): keeping the async
-          // loads out of branches lets them overlap the math.
-          if ((cc < 7 || !last_stage) &&
-              !mbar_wait_warp(&bars->tfull[bn], (uint32_t)(((cc + 1) >> 2) & 1), abort_flag,
-                              status, kSiteTFull))
-            ok = false;
-          tc_fence_after();
-          tmem_ld32(lane_addr + bn * kBufCols, pA);
-          if (cc == 0)
+          if (cc == 0) {
+            chunk_fma<true>(sb, pA, da);
             chunk_fma<true>(sb + 16, pB, da);
-          else
+          } else {
+            chunk_fma<false>(sb, pA, da);
             chunk_fma<false>(sb + 16, pB, da);
+          }
+          dump_partials<kPartials>(partials, M, N, nc, n, mcol, c, pA);
           dump_partials<kPartials>(partials, M, N, nc, n, mcol + 32, c, pB);
-          tmem_wait_ld2(pA, pB);
         }
         // Y += d * Sb for this super-block
         const float4* dv = reinterpret_cast<const float4*>(st + kScD) + 16 * colh;
