@@ -38,10 +38,9 @@
 // TMEM: four accumulator buffers of 128 columns (chunk c uses buffer c % 4).
 // Warp roles (12 warps; warpgroup 0 gives registers to warpgroups 1-2):
 //   0      TMA producer for both rings.
-//   1      TMEM allocation (512 columns); lane 0 issues the MMAs of the first
-//          chunk of every operand stage and commits its buffer.
-//   2      lane 0 issues the MMAs of the second chunk of every stage.
-//   3      idle (its registers go to the epilogue).
+//   1      TMEM allocation (512 columns).
+//   1-3    lane 0 of each issues the MMAs of every third chunk and commits
+//          its buffer (and its half of the operand stage).
 //   4-11   epilogue: warp w owns TMEM lanes 32(w%4).. (32 tokens) and 64
 //          weight-row columns. Per chunk it loads its 64 words, frees the
 //          buffer as soon as they are in registers and then does the math, so
@@ -60,6 +59,7 @@ constexpr int kThreads = 384;      // launched with 168 registers per thread
 constexpr int kCtlRegs = 24, kEpiRegs = 240;  // 128 * 24 + 256 * 240 == 384 * 168
 static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * 168, "register split");
 constexpr int kEpiWarp0 = 4, kNumEpiWarps = 8;
+constexpr int kNumIssuers = 3;  // MMA-issuing threads: lane 0 of warps 1-3
 constexpr int kTmemCols = 512, kBufCols = 128, kNumBufs = 4;
 
 constexpr int kOpX = 0, kOpWhi = BT * 128, kOpWlo = kOpWhi + BW * 128;
@@ -136,13 +136,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < SB; ++s) {
       mbar_init(&bars->b_full[s], 1);
-      mbar_init(&bars->b_empty[s], 2);  // both MMA-issuing threads
+      mbar_init(&bars->b_empty[s], 2);  // the two chunks' issuers
     }
     for (int b = 0; b < kNumBufs; ++b) {
       mbar_init(&bars->tfull[b], 1);
       mbar_init(&bars->tempty[b], kNumEpiWarps);
     }
-    mbar_init(&bars->drain, 2);
+    mbar_init(&bars->drain, kNumIssuers);
     bars->abort = 0;
     mbar_fence_init();
   }
@@ -209,22 +209,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_bounded(&bars->b_full[k % SB], (k / SB) & 1, &no_abort, status, kSiteBFull);
         }
       }
-    } else if (warp == 1 || warp == 2) {
+    } else {
       // --------------------------------------------------------------- MMA --
-      // Two issuing threads: warp 1 takes the first chunk of every operand
-      // stage, warp 2 the second. tcgen05.mma issue stalls until the tensor
-      // pipe has room, so while one thread waits on a barrier or commits, the
-      // other keeps the pipe fed. Each thread commits only its own MMAs.
+      // Three issuing threads (lane 0 of warps 1-3) take the chunks in turn:
+      // chunk g goes to issuer g % 3. tcgen05.mma issue stalls until the
+      // tensor pipe has room, so while one thread waits on a barrier or
+      // commits, the others keep the pipe fed. Each thread commits only its
+      // own MMAs: the chunk's buffer, and the chunk's half of its stage.
       if (lane == 0) {
         constexpr uint32_t idesc = idesc_f16_f32(BT, BW);
-        const int q = warp - 1;  // chunk of the stage: 0 or 1
-        int gk = 0;              // operand stages consumed
+        const int me = warp - 1;  // 0..2
         bool ok = true;
-        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-          for (int kb = 0; kb < nb && ok; ++kb, ++gk) {
-            const int slot = gk % SB;
-            const int gc = 2 * gk + q;  // global chunk index
-            const int b = gc & 3;
+        int gbase = 0;            // global chunk index of the tile's first chunk
+        for (int t = blockIdx.x; t < T && ok; t += gridDim.x, gbase += nc) {
+          for (int c = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; c < nc && ok;
+               c += kNumIssuers) {
+            const int gc = gbase + c;   // global chunk index
+            const int gk = gc >> 1;     // its operand stage
+            const int q = gc & 1;       // its half of the stage
+            const int slot = gk % SB, b = gc & 3;
             if (!(ok = mbar_wait_bounded(&bars->b_full[slot], (gk / SB) & 1, abort_flag, status,
                                          kSiteBFull)))
               break;
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&bars->b_empty[slot]);
           }
         }
-        // Every MMA of both threads must be finished before TMEM is released.
+        // Every MMA of every issuer must be finished before TMEM is released.
         umma_commit(&bars->drain);
         volatile int no_abort = 0;
         mbar_wait_bounded(&bars->drain, 0, &no_abort, status, kSiteDrain);
