@@ -300,6 +300,29 @@ def e2e_run(step_host, steps: int, device):
     return reduce_max(a.elapsed_time(b), device)
 
 
+def graph_ms(fn, calls: int, reps: int = 2) -> float:
+    """Device time per call of fn(i), i < calls, captured into one CUDA graph
+    and replayed `reps` times (launch overhead of the host excluded)."""
+    import torch
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(calls):
+                fn(i)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = ev_pair()
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (reps * calls)
+
+
 def clocks_ok(clk) -> bool:
     bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
     return clk is None or not (bad & set(clk.get("reasons", [])))
@@ -311,10 +334,10 @@ def skinny_bytes(M, K, N):
     return M * K * 210 / 256 + N * K + N * (K // 32) * 4 + 4 * N * M
 
 
-def skinny_kernel_times(q6, synth, device, iters: int = 20):
+def skinny_kernel_times(q6, synth, device, iters: int = 10):
     """Skinny (memory-bound) GEMM on the ffn_down and attn_v weights for
-    N = 1, 4, 16, weights rotated over copies totalling more than 4x L2.
-    Returns {name: {us, gbs, frac_hbm}} without the fraction."""
+    N = 1, 4, 16, weights rotated over copies totalling more than 4x L2,
+    timed by CUDA-graph replay. Returns {name: {us, gbs, ...}}."""
     import torch
     out = {}
     for wname in ("ffn_down", "attn_v"):
@@ -330,14 +353,8 @@ def skinny_kernel_times(q6, synth, device, iters: int = 20):
             Y = torch.empty((n, M), dtype=torch.float32, device=device)
             for i in range(2 * R):
                 q6.mmq(Ws[i % R], act, Y=Y)
-            a, b = ev_pair()
-            a.record()
-            for i in range(iters * R):
-                q6.mmq(Ws[i % R], act, Y=Y)
-            b.record()
-            torch.cuda.synchronize()
+            us = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y), iters * R) * 1e3
             q6.sync_status()
-            us = a.elapsed_time(b) / (iters * R) * 1e3
             gbs = skinny_bytes(M, K, n) / us / 1e3
             out[f"{wname}_N{n}"] = {"us": us, "gbs": gbs, "weight_copies": R,
                                     "path": q6.mmq(Ws[0], act, Y=Y)[1]}
@@ -573,9 +590,22 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     for i in range(max(args.warmup, 2 * R)):
         step(i)
     q6.sync_status()
-    max_ms, clk = timed_region(step, args.steps, device, rank == 0)
+    # the K timed steps run as one captured CUDA graph (small kernels: the
+    # host's launch rate would otherwise be what is measured)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                step(i)
+    graph.replay()
+    max_ms, clk = timed_region(lambda i: graph.replay(), 1, device, rank == 0)
     q6.sync_status()
-    q_ms, m_ms = kernel_ms(step, max(20 * R, min(args.steps, 2000)), 3)
+    m_ms = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y), 20 * R)
+    q_ms = graph_ms(lambda i: q6.quantize_act(Xd, out=act), 200)
+    q6.sync_status()
     ops_per_step = 2.0 * M * n * K
     value = job_throughput(ops_per_step * args.steps, world, max_ms / 1e3) / 1e12
     e2e = None
@@ -612,6 +642,7 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
                      "algorithmic": f"M*K*210/256 + N*K + N*K/8 + 4*N*M = {alg:.4g} B per launch"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "clocks": clk, "clocks_ok": clocks_ok(clk),
+        "timing": "the K steps replayed as one CUDA graph; kernel times by graph replay",
         "kernels": {"q6k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
                     "q8_quantize_act": {"us": q_ms * 1e3}},
     }
@@ -717,8 +748,9 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 # DRAM bytes (read + write) per launch from ncu captures of the current
 # kernels, keyed by (workload, kernel); the capture each figure comes from is
-# summarised under profiles/.
-TRAFFIC = {}
+# summarised under profiles/ (mmq_tc_ffn_down.md). An entry is removed when
+# its kernel changes.
+TRAFFIC = {("ffn_down", "mmq_tc"): 670.25e6 + 52.34e6}
 
 
 def main():

@@ -119,7 +119,8 @@ int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da
  *         bytes 64..95 = qh[32*(h%2) .. +31] of that super-block.
  *         Row stride 3*K/4 bytes.
  *   sc  : int8 [M][K/16], the raw sub-block scales.
- *   d   : binary16 bits [M][K/256], the raw super-block scales.
+ *   d   : binary16 bits [M][ldd], the raw super-block scales; row stride
+ *         ldd = K/256 rounded up to a multiple of 8 (16 bytes), padding zero.
  *   dT  : f32 [K/256][ldm], ldm = M rounded up to a multiple of 4: the
  *         super-block scales as f32 (exact), transposed; rows M..ldm-1 zero.
  * wexp (device, optional, 16-byte aligned): int8 [M][K], row stride K, the

@@ -57,7 +57,8 @@ int device_state(DevState** out) {
     }
     if ((e = cudaMalloc(&st.status, 256))) return cuda_fail(e, "cudaMalloc(status)");
     if ((e = cudaMemset(st.status, 0, 256))) return cuda_fail(e, "cudaMemset(status)");
-    if ((e = q6::mmq_tc_prepare())) return cuda_fail(e, "cudaFuncSetAttribute");
+    if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()))
+      return cuda_fail(e, "cudaFuncSetAttribute");
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -278,7 +279,7 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   cudaError_t e;
   if (skinny) {
     e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda_of(N), N, Y,
-                              ldy, partials, (cudaStream_t)s);
+                              ldy, partials, st->status, (cudaStream_t)s);
     if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
     if (path_out) *path_out = Q6_PATH_SKINNY;
     return Q6_OK;

@@ -1,23 +1,32 @@
 // q6_K x int8 GEMM for few tokens (N <= 16): a weight-streaming kernel on the
-// CUDA cores, bound by HBM (0.82 byte per weight).
+// CUDA cores, bound by HBM (0.82 byte per weight: 210 bytes per 256 weights,
+// plus the 16-byte padding of each d row).
 //
 // Math ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.1-2.2): for each
 // 16-element sub-block s the exact integer P = sum (q - 32) * xq is formed
 // with dp4a, then Y += (f32(d) * sc[s]) * da[chunk] * P. The element map is
 // the one of Sec. 3.2 (see pack.cu).
 //
-// Work split: one warp per weight row; per iteration a warp covers four
+// Row dot product: one warp per weight row; per iteration a warp covers four
 // super-blocks, eight lanes per super-block. Lane (half, s4) of a super-block
 // reads the 16 ql bytes at 16*s4 of its half and the 16 qh bytes at
 // 16*(s4&1): the low nibbles give sub-block 8*half + s4, the high nibbles
 // (same bytes) sub-block 8*half + s4 + 4; their 2-bit fields sit at bits
 // 2*(s4>>1) and 2*(s4>>1) + 4 of the qh bytes.
+//
+// Streaming: warps stride over the rows, with the grid sized to one resident
+// wave (4 warps per CTA, 64 registers, 8 CTAs per SM) so every warp starts at
+// once and reads its row's qlh run in coalesced 768-byte steps. Measured on
+// GB300, neither loading several steps ahead (fewer resident warps) nor a
+// cp.async.bulk ring of whole rows in shared memory beat this form.
 #include "q6_internal.cuh"
 
 namespace q6 {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;      // warps per CTA
+constexpr int kMinBlocks = 8;  // resident CTAs per SM (64 registers per thread)
+constexpr int kGroupGlobal = 1;  // iterations loaded ahead of the math
 
 // Bytes (code - 32) mod 256 of four 6-bit codes: code + 96 never carries out
 // of its byte, and adding 128 more is a flip of bit 7.
@@ -25,80 +34,96 @@ __device__ __forceinline__ uint32_t center4(uint32_t code) {
   return (code + 0x60606060u) ^ 0x80808080u;
 }
 
-template <bool kPartials>
-__global__ void __launch_bounds__(kWarps * 32) mmq_skinny_kernel(
-    const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
-    const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
-    int32_t* __restrict__ partials) {
+// The dot products of one weight row with the N activation rows. qlh, sc and
+// dbits point at the row's sub-plane runs; the result is reduced across the
+// warp and written by lane 0. Loads run kGroup iterations (4 super-blocks,
+// 768 bytes of codes each) ahead of the math.
+template <bool kPartials, int kGroup>
+__device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
+                                        const int8_t* __restrict__ sc_row,
+                                        const uint16_t* __restrict__ d_row, int m, int M, int K,
+                                        const int8_t* __restrict__ Xq, const float* __restrict__ da,
+                                        int ldda, int N, float* __restrict__ Y, int ldy,
+                                        int32_t* __restrict__ partials) {
   const int lane = threadIdx.x & 31;
-  const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
-  if (m >= M) return;
   const int nsb = K / 256;
-  const int sbi = lane >> 3;        // super-block within the iteration
+  const int sbi = lane >> 3;  // super-block within the iteration
   const int half = (lane >> 2) & 1;
   const int s4 = lane & 3;
-  const int fsh = 2 * (s4 >> 1);    // field of the low-nibble sub-block
-
-  const uint8_t* qlh_row = plane + g.qlh_off + (size_t)m * g.qlh_row;
-  const int8_t* sc_row = reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)m * (K / 16);
-  const uint16_t* d_row = reinterpret_cast<const uint16_t*>(plane + g.d_off) + (size_t)m * nsb;
+  const int fsh = 2 * (s4 >> 1);  // field of the low-nibble sub-block
+  const int sa = 8 * half + s4;   // sub-block (0..15) of the low nibbles; sb_b = sa + 4
 
   float acc[Q6_SKINNY_MAX_N];
 #pragma unroll
   for (int n = 0; n < Q6_SKINNY_MAX_N; ++n) acc[n] = 0.0f;
 
-  for (int sb0 = 0; sb0 < nsb; sb0 += 4) {
-    const int sb = sb0 + sbi;
-    if (sb < nsb) {
-      const uint8_t* hb = qlh_row + (size_t)(2 * sb + half) * 96;
-      const uint4 L = *reinterpret_cast<const uint4*>(hb + 16 * s4);
-      const uint4 H = *reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1));
-      const uint32_t Lw[4] = {L.x, L.y, L.z, L.w};
-      const uint32_t Hw[4] = {H.x, H.y, H.z, H.w};
-      uint32_t va[4], vb[4];
+  for (int g0 = 0; g0 < nsb; g0 += 4 * kGroup) {
+    uint4 L[kGroup], H[kGroup];
+    int sca[kGroup], scb[kGroup];
+    uint16_t dbits[kGroup];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint32_t ca = (Lw[w] & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
-        const uint32_t cb = ((Lw[w] >> 4) & 0x0F0F0F0Fu) | (((Hw[w] >> (fsh + 4)) & 0x03030303u) << 4);
-        va[w] = center4(ca);
-        vb[w] = center4(cb);
+    for (int u = 0; u < kGroup; ++u) {
+      const int sb = g0 + 4 * u + sbi;
+      if (sb < nsb) {
+        const uint8_t* hb = qlh_row + (size_t)(2 * sb + half) * 96;
+        L[u] = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
+        H[u] = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
+        sca[u] = __ldg(sc_row + 16 * sb + sa);
+        scb[u] = __ldg(sc_row + 16 * sb + sa + 4);
+        dbits[u] = __ldg(d_row + sb);
       }
-      const int sa = 8 * half + s4;  // sub-block (0..15) of the low nibbles; sb_b = sa + 4
-      const float d = __half2float(__ushort_as_half(d_row[sb]));
-      const int sc_a = sc_row[16 * sb + sa], sc_b = sc_row[16 * sb + sa + 4];
-      const float dsc_a = d * (float)sc_a;
-      const float dsc_b = d * (float)sc_b;
-      const int ka = 256 * sb + 16 * sa;  // first element of sub-block a
-      const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
+    }
 #pragma unroll
-      for (int n = 0; n < Q6_SKINNY_MAX_N; ++n) {
-        if (n < N) {
-          const int8_t* xr = Xq + (size_t)n * K;
-          const uint4 xa = *reinterpret_cast<const uint4*>(xr + ka);
-          const uint4 xb = *reinterpret_cast<const uint4*>(xr + ka + 64);
-          int pa = __dp4a((int)va[0], (int)xa.x, 0);
-          pa = __dp4a((int)va[1], (int)xa.y, pa);
-          pa = __dp4a((int)va[2], (int)xa.z, pa);
-          pa = __dp4a((int)va[3], (int)xa.w, pa);
-          int pb = __dp4a((int)vb[0], (int)xb.x, 0);
-          pb = __dp4a((int)vb[1], (int)xb.y, pb);
-          pb = __dp4a((int)vb[2], (int)xb.z, pb);
-          pb = __dp4a((int)vb[3], (int)xb.w, pb);
-          const float daa = da[(size_t)ca_blk * ldda + n];
-          const float dab = da[(size_t)cb_blk * ldda + n];
-          acc[n] = fmaf(dsc_a * daa, (float)pa, acc[n]);
-          acc[n] = fmaf(dsc_b * dab, (float)pb, acc[n]);
-          if (kPartials) {
-            // chunk partials sc*P summed over the chunk's two sub-blocks; the
-            // other sub-block of each chunk is in lane ^ 1 (active together)
-            const unsigned act = __activemask();
-            const int ta = sc_a * pa, tb = sc_b * pb;
-            const int sa2 = ta + __shfl_xor_sync(act, ta, 1);
-            const int sb2 = tb + __shfl_xor_sync(act, tb, 1);
-            if ((s4 & 1) == 0) {
-              int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 32) + (size_t)sb * 8;
-              pr[sa >> 1] = sa2;
-              pr[(sa + 4) >> 1] = sb2;
+    for (int u = 0; u < kGroup; ++u) {
+      const int sb = g0 + 4 * u + sbi;
+      if (sb < nsb) {
+        const uint32_t Lw[4] = {L[u].x, L[u].y, L[u].z, L[u].w};
+        const uint32_t Hw[4] = {H[u].x, H[u].y, H[u].z, H[u].w};
+        uint32_t va[4], vb[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t ca = (Lw[w] & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
+          const uint32_t cb =
+              ((Lw[w] >> 4) & 0x0F0F0F0Fu) | (((Hw[w] >> (fsh + 4)) & 0x03030303u) << 4);
+          va[w] = center4(ca);
+          vb[w] = center4(cb);
+        }
+        const float d = __half2float(__ushort_as_half(dbits[u]));
+        const int sc_a = sca[u], sc_b = scb[u];
+        const float dsc_a = d * (float)sc_a;
+        const float dsc_b = d * (float)sc_b;
+        const int ka = 256 * sb + 16 * sa;  // first element of sub-block a
+        const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
+#pragma unroll
+        for (int n = 0; n < Q6_SKINNY_MAX_N; ++n) {
+          if (n < N) {
+            const int8_t* xr = Xq + (size_t)n * K;
+            const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
+            const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
+            int pa = __dp4a((int)va[0], (int)xa.x, 0);
+            pa = __dp4a((int)va[1], (int)xa.y, pa);
+            pa = __dp4a((int)va[2], (int)xa.z, pa);
+            pa = __dp4a((int)va[3], (int)xa.w, pa);
+            int pb = __dp4a((int)vb[0], (int)xb.x, 0);
+            pb = __dp4a((int)vb[1], (int)xb.y, pb);
+            pb = __dp4a((int)vb[2], (int)xb.z, pb);
+            pb = __dp4a((int)vb[3], (int)xb.w, pb);
+            const float daa = __ldg(da + (size_t)ca_blk * ldda + n);
+            const float dab = __ldg(da + (size_t)cb_blk * ldda + n);
+            acc[n] = fmaf(dsc_a * daa, (float)pa, acc[n]);
+            acc[n] = fmaf(dsc_b * dab, (float)pb, acc[n]);
+            if (kPartials) {
+              // chunk partials sc*P summed over the chunk's two sub-blocks; the
+              // other sub-block of each chunk is in lane ^ 1 (active together)
+              const unsigned act = __activemask();
+              const int ta = sc_a * pa, tb = sc_b * pb;
+              const int sa2 = ta + __shfl_xor_sync(act, ta, 1);
+              const int sb2 = tb + __shfl_xor_sync(act, tb, 1);
+              if ((s4 & 1) == 0) {
+                int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 32) + (size_t)sb * 8;
+                pr[sa >> 1] = sa2;
+                pr[(sa + 4) >> 1] = sb2;
+              }
             }
           }
         }
@@ -119,13 +144,43 @@ __global__ void __launch_bounds__(kWarps * 32) mmq_skinny_kernel(
   }
 }
 
+// One warp per row, straight from global memory.
+template <bool kPartials>
+__global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
+    const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
+    const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
+    int32_t* __restrict__ partials) {
+  const int warps = (int)gridDim.x * kWarps;
+  for (int m = blockIdx.x * kWarps + (threadIdx.x >> 5); m < M; m += warps)
+    row_dot<kPartials, kGroupGlobal>(
+        plane + g.qlh_off + (size_t)m * g.qlh_row,
+        reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)m * (K / 16),
+        reinterpret_cast<const uint16_t*>(plane + g.d_off + (size_t)m * g.d_row), m, M, K, Xq, da,
+        ldda, N, Y, ldy, partials);
+}
+
+
 }  // namespace
+
+cudaError_t mmq_skinny_prepare() { return cudaSuccess; }
 
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
-                              cudaStream_t s) {
+                              unsigned int* status, cudaStream_t s) {
+  (void)status;  // the skinny kernel has no waits to bound
   const PlaneGeom g = plane_geom(M, K);
-  const unsigned blocks = (unsigned)((M + kWarps - 1) / kWarps);
+  // one resident wave: as many blocks as fit, warps striding over the rows
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  if (partials)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mmq_skinny_kernel<true>, kWarps * 32, 0);
+  else
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mmq_skinny_kernel<false>, kWarps * 32, 0);
+  if (e != cudaSuccess) return e;
+  const long long need = (M + kWarps - 1) / kWarps, cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
+  const unsigned blocks = (unsigned)(need < cap ? need : cap);
   if (partials)
     mmq_skinny_kernel<true><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y, ldy,
                                                            partials);

@@ -70,7 +70,7 @@ int na_setup(NaDev** out) {
     if (major != 10 || minor != 3)
       return na_fail(Q6_EARCH, "device %d is compute capability %d.%d; needs 10.3", dev, major,
                      minor);
-    if ((e = q6::mmq_tc_prepare()))
+    if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()))
       return na_fail(Q6_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     void* addr = nullptr;
     if ((e = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) || !addr)
@@ -134,17 +134,17 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
   if (rc) return rc;
   const int ldda = (N + 3) / 4 * 4;
   cudaError_t e;
+  unsigned int* status = reinterpret_cast<unsigned int*>(st->scratch);
+  if ((e = cudaMemsetAsync(status, 0, sizeof(unsigned int), (cudaStream_t)s)))
+    return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
   if (skinny) {
     e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda, N, Y, ldy,
-                              nullptr, (cudaStream_t)s);
+                              nullptr, status, (cudaStream_t)s);
     if (e != cudaSuccess) return na_fail(Q6_ECUDA, "skinny kernel launch: %s", cudaGetErrorString(e));
     if (path_out) *path_out = Q6_PATH_SKINNY;
     return Q6_OK;
   }
-  unsigned int* status = reinterpret_cast<unsigned int*>(st->scratch);
   __half* wh = reinterpret_cast<__half*>(st->scratch + kStatusBytes);
-  if ((e = cudaMemsetAsync(status, 0, sizeof(unsigned int), (cudaStream_t)s)))
-    return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
   const uint8_t* pb = static_cast<const uint8_t*>(plane);
   e = wexp ? q6::launch_expand_wexp(wexp, pb, M, K, wh, (cudaStream_t)s)
            : q6::launch_expand_raw(pb, M, K, wh, (cudaStream_t)s);

@@ -8,7 +8,7 @@
 // The qlh sub-plane keeps each half's 64 ql bytes and 32 qh bytes together so
 // one 96-byte TMA row carries everything the unpack of that half needs.
 // The super-block scale d is kept twice: as the raw binary16 bits [M][K/256]
-// and as f32 transposed to [K/256][ldm] (weight rows contiguous, rows M..ldm-1
+// (rows padded to 16 bytes, padding zero) and as f32 transposed to [K/256][ldm] (weight rows contiguous, rows M..ldm-1
 // zero) so the GEMM can stage the d of 128 rows with one TMA copy. W_exp =
 // centered int8, row stride K ("r53 -- q6_K bundle: W_exp pre-expansion
 // plane", Sec. 2.3).
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(256) q6k_pack_kernel(const uint8_t* __restrict
       const size_t si = (size_t)m * (K / 16) + (size_t)b * 16 + lane;
       reinterpret_cast<int8_t*>(plane + g.sc_off)[si] = (int8_t)src[192 + lane];
     } else if (lane == 16) {
-      reinterpret_cast<uint16_t*>(plane + g.d_off)[(size_t)m * nsb + b] = dbits;
+      reinterpret_cast<uint16_t*>(plane + g.d_off + (size_t)m * g.d_row)[b] = dbits;
     } else if (lane == 17) {
       reinterpret_cast<float*>(plane + g.dt_off)[(size_t)b * g.ldm + m] =
           __half2float(__ushort_as_half(dbits));
@@ -67,6 +67,12 @@ __global__ void __launch_bounds__(256) q6k_pack_kernel(const uint8_t* __restrict
       reinterpret_cast<uint32_t*>(dst + 64 + j0)[0] = hi_word;
     }
   }
+  // padding of the binary16 d rows
+  const int dpad = (int)(g.d_row / 2) - nsb;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < (long long)M * dpad;
+       i += (long long)gridDim.x * blockDim.x)
+    reinterpret_cast<uint16_t*>(plane + g.d_off + (size_t)(i / dpad) * g.d_row)[nsb + (int)(i % dpad)] =
+        0;
   // rows M .. ldm-1 of the transposed d sub-plane
   const int pad = g.ldm - M;
   const long long npad = (long long)pad * nsb;

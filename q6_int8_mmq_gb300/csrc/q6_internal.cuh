@@ -22,6 +22,7 @@ constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 struct PlaneGeom {
   size_t qlh_off, sc_off, d_off, dt_off, total;
   size_t qlh_row;  // 3K/4 bytes
+  size_t d_row;    // bytes per row of the binary16 d sub-plane: K/128 rounded up to 16
   int ldm;         // row stride (elements) of the transposed d sub-plane: M rounded up to 4
 };
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -32,8 +33,9 @@ inline PlaneGeom plane_geom(int M, int K) {
   g.qlh_row = k / 128 * 96;
   g.qlh_off = 0;
   g.sc_off = round_up(m * g.qlh_row, 256);
+  g.d_row = round_up(k / 256 * 2, 16);
   g.d_off = g.sc_off + round_up(m * (k / 16), 256);
-  g.dt_off = g.d_off + round_up(m * (k / 256) * 2, 256);
+  g.dt_off = g.d_off + round_up(m * g.d_row, 256);
   g.total = g.dt_off + round_up((k / 256) * (size_t)g.ldm * 4, 256);
   return g;
 }
@@ -46,7 +48,8 @@ cudaError_t launch_pack(const uint8_t* raw, int M, int K, uint8_t* plane, int8_t
                         cudaStream_t s);
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
-                              cudaStream_t s);
+                              unsigned int* status, cudaStream_t s);
+cudaError_t mmq_skinny_prepare();
 
 struct TcMaps {
   CUtensorMap x;    // Xh   [N][K] f16, box {64, 128}, 128B swizzle

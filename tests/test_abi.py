@@ -47,7 +47,8 @@ def test_plane_sizes(lib):
     M, K = 4096, 11008
     r = lambda x: (x + 255) // 256 * 256
     ldm = (M + 3) // 4 * 4
-    assert pb == r(M * K * 3 // 4) + r(M * K // 16) + r(M * K // 256 * 2) + r(K // 256 * ldm * 4)
+    d_row = (K // 256 * 2 + 15) // 16 * 16
+    assert pb == r(M * K * 3 // 4) + r(M * K // 16) + r(M * d_row) + r(K // 256 * ldm * 4)
     assert wb == M * K
     xq, dab, xh, ldda = q6.act_plane_bytes(3314, 11008)
     assert (xq, xh, ldda) == (3314 * 11008, 3314 * 11008 * 2, 3316)

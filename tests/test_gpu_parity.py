@@ -142,7 +142,8 @@ def test_pack_bitexact(q6, orc, M, K):
     blocks = raw.reshape(M, K // 256, 210)
     r = lambda x: (x + 255) // 256 * 256
     ldm = (M + 3) // 4 * 4
-    qlh_sz, sc_sz, d_sz = M * K * 3 // 4, M * K // 16, M * K // 256 * 2
+    d_row = (K // 256 * 2 + 15) // 16 * 16
+    qlh_sz, sc_sz, d_sz = M * K * 3 // 4, M * K // 16, M * d_row
     o_sc = r(qlh_sz)
     o_d = o_sc + r(sc_sz)
     o_dt = o_d + r(d_sz)
@@ -154,8 +155,10 @@ def test_pack_bitexact(q6, orc, M, K):
         assert np.array_equal(qlh[:, :, h, 64:], blocks[:, :, 128 + 32 * h: 160 + 32 * h])
     sc = plane[o_sc:o_sc + sc_sz].view(np.int8).reshape(M, K // 256, 16)
     assert np.array_equal(sc, blocks[:, :, 192:208].view(np.int8))
-    d = plane[o_d:o_d + d_sz].reshape(M, K // 256, 2)
+    d_all = plane[o_d:o_d + d_sz].reshape(M, d_row)
+    d = d_all[:, :K // 256 * 2].reshape(M, K // 256, 2)
     assert np.array_equal(d, blocks[:, :, 208:210])
+    assert np.all(d_all[:, K // 256 * 2:] == 0)
     # d transposed to [K/256][ldm] as f32, rows M..ldm-1 zero
     dt = plane[o_dt:o_dt + K // 256 * ldm * 4].view(np.float32).reshape(K // 256, ldm)
     d_f64 = np.array([[orc.f16_to_f64(int(b[0]) | (int(b[1]) << 8)) for b in row] for row in d])
