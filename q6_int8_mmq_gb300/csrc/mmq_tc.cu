@@ -35,17 +35,19 @@
 //          each, 128-byte swizzled; freed by the MMA (tcgen05.commit).
 //   scale ring (3 stages x one super-block): da [8 chunks][128 tokens] and
 //          d [128 rows]; freed by the epilogue.
-// TMEM: four accumulator buffers of 128 columns (chunk c uses buffer c % 4).
+// TMEM: two slots of two 128-column accumulator buffers; operand stage g (two
+// chunks) uses slot g % 2, and MMA and epilogue hand a slot over with one
+// mbarrier phase per stage.
 // Warp roles (12 warps; warpgroup 0 gives registers to warpgroups 1-2):
 //   0      TMA producer for both rings.
 //   1      TMEM allocation (512 columns).
-//   1-3    lane 0 of each issues the MMAs of every third chunk and commits
-//          its buffer (and its half of the operand stage).
+//   1-2    lane 0 of each issues the MMAs of every other operand stage and
+//          commits its TMEM slot and its operand stage.
+//   3      idle (its registers go to the epilogue).
 //   4-11   epilogue: warp w owns TMEM lanes 32(w%4).. (32 tokens) and 64
-//          weight-row columns. Per chunk it loads its 64 words, frees the
-//          buffer as soon as they are in registers and then does the math, so
-//          a buffer is back with the MMA issuer about two barrier hops after
-//          its chunk completes (the buffers, not the math, pace the pipeline).
+//          weight-row columns. Per chunk it loads its 64 words and does the
+//          math; the slot is freed as soon as the stage's second chunk is in
+//          registers.
 // Every mbarrier wait is bounded (see q6_internal.cuh).
 #include "q6_internal.cuh"
 
@@ -59,8 +61,9 @@ constexpr int kThreads = 384;      // launched with 168 registers per thread
 constexpr int kCtlRegs = 24, kEpiRegs = 240;  // 128 * 24 + 256 * 240 == 384 * 168
 static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * 168, "register split");
 constexpr int kEpiWarp0 = 4, kNumEpiWarps = 8;
-constexpr int kNumIssuers = 3;  // MMA-issuing threads: lane 0 of warps 1-3
-constexpr int kTmemCols = 512, kBufCols = 128, kNumBufs = 4;
+constexpr int kNumIssuers = 2;  // MMA-issuing threads: lane 0 of warps 1-2
+constexpr int kTmemCols = 512, kBufCols = 128;
+constexpr int kNumSlots = 2;  // TMEM slots of two chunk buffers (one operand stage) each
 
 constexpr int kOpX = 0, kOpWhi = BT * 128, kOpWlo = kOpWhi + BW * 128;
 constexpr int kOpStage = kOpWlo + BW * 128;                            // 48 KB
@@ -76,7 +79,7 @@ enum : uint32_t { kSiteSEmpty = 1, kSiteSFull = 2, kSiteBEmpty = 3, kSiteBFull =
 struct Bars {
   uint64_t s_full[SS], s_empty[SS];
   uint64_t b_full[SB], b_empty[SB];
-  uint64_t tfull[kNumBufs], tempty[kNumBufs], drain;
+  uint64_t tfull[kNumSlots], tempty[kNumSlots], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -136,13 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < SB; ++s) {
       mbar_init(&bars->b_full[s], 1);
-      mbar_init(&bars->b_empty[s], 2);  // the two chunks' issuers
+      mbar_init(&bars->b_empty[s], 1);
     }
-    for (int b = 0; b < kNumBufs; ++b) {
+    for (int b = 0; b < kNumSlots; ++b) {
       mbar_init(&bars->tfull[b], 1);
       mbar_init(&bars->tempty[b], kNumEpiWarps);
     }
-    mbar_init(&bars->drain, kNumIssuers);
+    mbar_init(&bars->drain, kNumIssuers);  // one commit per issuer
     bars->abort = 0;
     mbar_fence_init();
   }
@@ -211,28 +214,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // --------------------------------------------------------------- MMA --
-      // Three issuing threads (lane 0 of warps 1-3) take the chunks in turn:
-      // chunk g goes to issuer g % 3. tcgen05.mma issue stalls until the
-      // tensor pipe has room, so while one thread waits on a barrier or
-      // commits, the others keep the pipe fed. Each thread commits only its
-      // own MMAs: the chunk's buffer, and the chunk's half of its stage.
-      if (lane == 0) {
+      // Operand stage g (two chunks) goes to issuer g % kNumIssuers and into
+      // TMEM slot g % 2. tcgen05.mma issue stalls until the tensor pipe has
+      // room, so while one issuer waits on a barrier or commits, the other
+      // keeps the pipe fed. One commit per stage signals both its chunks:
+      // each mbarrier hand-off costs about 200 cycles, so hand-offs are per
+      // two chunks, not per chunk.
+      if (lane == 0 && warp <= kNumIssuers) {
         constexpr uint32_t idesc = idesc_f16_f32(BT, BW);
-        const int me = warp - 1;  // 0..2
+        const int me = warp - 1;
         bool ok = true;
-        int gbase = 0;            // global chunk index of the tile's first chunk
-        for (int t = blockIdx.x; t < T && ok; t += gridDim.x, gbase += nc) {
-          for (int c = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; c < nc && ok;
-               c += kNumIssuers) {
-            const int gc = gbase + c;   // global chunk index
-            const int gk = gc >> 1;     // its operand stage
-            const int q = gc & 1;       // its half of the stage
-            const int slot = gk % SB, b = gc & 3;
+        int gbase = 0;  // global index of the tile's first operand stage
+        for (int t = blockIdx.x; t < T && ok; t += gridDim.x, gbase += nb) {
+          for (int kb = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; kb < nb && ok;
+               kb += kNumIssuers) {
+            const int gk = gbase + kb;  // global operand stage
+            const int slot = gk % SB, ts = gk & 1;
             if (!(ok = mbar_wait_bounded(&bars->b_full[slot], (gk / SB) & 1, abort_flag, status,
                                          kSiteBFull)))
               break;
-            if (!(ok = mbar_wait_bounded(&bars->tempty[b], ((gc >> 2) & 1) ^ 1, abort_flag, status,
-                                         kSiteTEmpty)))
+            if (!(ok = mbar_wait_bounded(&bars->tempty[ts], ((gk >> 1) & 1) ^ 1, abort_flag,
+                                         status, kSiteTEmpty)))
               break;
             tc_fence_after();
             // descriptors of the stage's three tiles; a K step of 16 elements
@@ -241,14 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t xdesc = sw128_kmajor_desc(smem_u32(bt + kOpX));
             const uint64_t hdesc = sw128_kmajor_desc(smem_u32(bt + kOpWhi));
             const uint64_t ldesc = sw128_kmajor_desc(smem_u32(bt + kOpWlo));
-            const uint32_t d_tmem = tmem + (uint32_t)(b * kBufCols);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint64_t koff = (uint64_t)((2 * q + h) * 2);  // sub-block within the stage
-              umma_f16(d_tmem, xdesc + koff, hdesc + koff, idesc, (uint32_t)h);
-              umma_f16(d_tmem, xdesc + koff, ldesc + koff, idesc, 1u);
+            for (int q = 0; q < 2; ++q) {
+              const uint32_t d_tmem = tmem + (uint32_t)((2 * ts + q) * kBufCols);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint64_t koff = (uint64_t)((2 * q + h) * 2);  // sub-block within the stage
+                umma_f16(d_tmem, xdesc + koff, hdesc + koff, idesc, (uint32_t)h);
+                umma_f16(d_tmem, xdesc + koff, ldesc + koff, idesc, 1u);
+              }
             }
-            umma_commit(&bars->tfull[b]);
+            umma_commit(&bars->tfull[ts]);
             umma_commit(&bars->b_empty[slot]);
           }
         }
@@ -286,32 +291,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t* st = smem + kRingS + slot * kScStage;
         const float* sda = reinterpret_cast<const float*>(st + kScDa) + tok;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          // Chunk 8s + cc sits in buffer cc % 4 (a tile has a multiple of 8
-          // chunks), in its use (cc / 4) % 2 of this super-block's pair.
-          const uint32_t b = (uint32_t)(cc & 3);
-          const int c = 8 * s + cc;
-          if (!mbar_wait_warp(&bars->tfull[b], (uint32_t)((cc >> 2) & 1), abort_flag, status,
+        for (int pp = 0; pp < 4; ++pp) {
+          // Operand stage 4s + pp: its two chunks sit in TMEM slot pp % 2 (a
+          // tile has a multiple of four stages), in the slot's use (pp / 2) % 2.
+          const uint32_t ts = (uint32_t)(pp & 1);
+          if (!mbar_wait_warp(&bars->tfull[ts], (uint32_t)((pp >> 1) & 1), abort_flag, status,
                               kSiteTFull))
             ok = false;
           tc_fence_after();
-          tmem_ld32(lane_addr + b * kBufCols, pA);
-          tmem_ld32(lane_addr + b * kBufCols + 32u, pB);
-          const float da = sda[cc * BT];
-          tmem_wait_ld2(pA, pB);
-          // the chunk is in registers: free the buffer before the math
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tempty[b]);
-          if (cc == 0) {
-            chunk_fma<true>(sb, pA, da);
-            chunk_fma<true>(sb + 16, pB, da);
-          } else {
-            chunk_fma<false>(sb, pA, da);
-            chunk_fma<false>(sb + 16, pB, da);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int cc = 2 * pp + q, c = 8 * s + cc;
+            const uint32_t col = (2 * ts + (uint32_t)q) * kBufCols;
+            tmem_ld32(lane_addr + col, pA);
+            tmem_ld32(lane_addr + col + 32u, pB);
+            const float da = sda[cc * BT];
+            tmem_wait_ld2(pA, pB);
+            if (q == 1) {
+              // both chunks of the stage are in registers: free the slot
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->tempty[ts]);
+            }
+            if (cc == 0) {
+              chunk_fma<true>(sb, pA, da);
+              chunk_fma<true>(sb + 16, pB, da);
+            } else {
+              chunk_fma<false>(sb, pA, da);
+              chunk_fma<false>(sb + 16, pB, da);
+            }
+            dump_partials<kPartials>(partials, M, N, nc, n, mcol, c, pA);
+            dump_partials<kPartials>(partials, M, N, nc, n, mcol + 32, c, pB);
           }
-          dump_partials<kPartials>(partials, M, N, nc, n, mcol, c, pA);
-          dump_partials<kPartials>(partials, M, N, nc, n, mcol + 32, c, pB);
         }
         // Y += d * Sb for this super-block
         const float4* dv = reinterpret_cast<const float4*>(st + kScD) + 16 * colh;
