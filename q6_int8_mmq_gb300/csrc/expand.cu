@@ -17,8 +17,8 @@
 // W_hi + W_lo = sc * v exactly, and two MMAs over the same activation
 // operand give the integer sum of sc * v * xq of a sub-block.
 //
-// Both kernels are bandwidth-bound: one thread per 16 elements, one or two
-// 16-byte loads and one sc byte, four 16-byte stores.
+// Both kernels are bandwidth-bound (0.81 or 1.06 bytes read and 4 written per
+// weight).
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -70,30 +70,42 @@ __device__ __forceinline__ void store_folded(const uint32_t (&o)[8], int sc, __h
   dl[1] = make_uint4(l[4], l[5], l[6], l[7]);
 }
 
+// One thread per 32-element chunk (two sub-blocks of one half block): its
+// two 16-byte ql runs and the half block's 32 qh bytes are loaded together
+// before any conversion.
 __global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restrict__ qlh,
                                                          const int8_t* __restrict__ sc, int M, int K,
                                                          size_t qlh_row, __half* __restrict__ wh) {
-  const int groups = K / 16;
-  const long long items = (long long)M * groups;
+  const int chunks = K / 32;
+  const long long items = (long long)M * chunks;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const size_t plane = (size_t)M * K;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
-    const int m = (int)(i / groups), r = (int)(i - (long long)m * groups);
-    const int hb = r >> 3, g = r & 7;  // half block, group within it
+    const int m = (int)(i / chunks), c = (int)(i - (long long)m * chunks);
+    const int hb = c >> 2, g0 = 2 * (c & 3);  // half block, first group (even) within it
     const uint8_t* src = qlh + (size_t)m * qlh_row + (size_t)hb * 96;
-    const uint4 L = __ldg(reinterpret_cast<const uint4*>(src + 16 * (g & 3)));
-    const uint4 H = __ldg(reinterpret_cast<const uint4*>(src + 64 + 16 * (g & 1)));
-    const int s = __ldg(sc + i);
-    const int nsh = 4 * (g >> 2), fsh = 2 * ((g >> 1) & 3);
-    const uint32_t Lw[4] = {L.x, L.y, L.z, L.w}, Hw[4] = {H.x, H.y, H.z, H.w};
-    uint32_t o[8];
+    const uint4 La = __ldg(reinterpret_cast<const uint4*>(src + 16 * (g0 & 3)));
+    const uint4 Lb = __ldg(reinterpret_cast<const uint4*>(src + 16 * ((g0 + 1) & 3)));
+    const uint4 H0 = __ldg(reinterpret_cast<const uint4*>(src + 64));
+    const uint4 H1 = __ldg(reinterpret_cast<const uint4*>(src + 80));
+    const uint16_t s2 = __ldg(reinterpret_cast<const uint16_t*>(sc + 2 * i));
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const uint32_t code = ((Lw[w] >> nsh) & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
-      codes_to_f16(code, o[2 * w], o[2 * w + 1]);
+    for (int u = 0; u < 2; ++u) {
+      const int g = g0 + u;
+      const uint4 L = u ? Lb : La;
+      const uint4 H = (g & 1) ? H1 : H0;
+      const int nsh = 4 * (g >> 2), fsh = 2 * ((g >> 1) & 3);
+      const uint32_t Lw[4] = {L.x, L.y, L.z, L.w}, Hw[4] = {H.x, H.y, H.z, H.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t code = ((Lw[w] >> nsh) & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
+        codes_to_f16(code, o[2 * w], o[2 * w + 1]);
+      }
+      const int scv = (int)(int8_t)(u ? (s2 >> 8) : (s2 & 0xFF));
+      const size_t off = (size_t)m * K + (size_t)(2 * c + u) * 16;
+      store_folded(o, scv, wh + off, wh + plane + off);
     }
-    const size_t off = (size_t)m * K + (size_t)r * 16;
-    store_folded(o, s, wh + off, wh + plane + off);
   }
 }
 
@@ -124,7 +136,7 @@ unsigned grid_for(long long items) {
 
 cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
-  expand_raw_kernel<<<grid_for((long long)M * (K / 16)), 256, 0, s>>>(
+  expand_raw_kernel<<<grid_for((long long)M * (K / 32)), 256, 0, s>>>(
       plane + g.qlh_off, reinterpret_cast<const int8_t*>(plane + g.sc_off), M, K, g.qlh_row, wh);
   return cudaGetLastError();
 }

@@ -7,9 +7,7 @@
 // ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2); the pages print no
 // quantiser, so the division and the rounding are IEEE f32 and half-away.
 //
-// HBM-bound: 4 bytes read and 3 written per element. Each thread owns four
-// consecutive elements (one float4); eight threads of a warp form one block
-// and reduce amax with three xor-shuffles.
+// HBM-bound: 4 bytes read and 3 written per element (plus 4 per 32 for da).
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -21,35 +19,51 @@ __device__ __forceinline__ int quant1(float x, float d) {
   return (int)fminf(fmaxf(r, -127.0f), 127.0f);
 }
 
+// Eight elements of one row -> their int8 codes (as two words) and binary16 values.
+__device__ __forceinline__ void quant8(const float4 v0, const float4 v1, float d, uint2& q8,
+                                       uint4& h8) {
+  const int q0 = quant1(v0.x, d), q1 = quant1(v0.y, d), q2 = quant1(v0.z, d), q3 = quant1(v0.w, d);
+  const int q4 = quant1(v1.x, d), q5 = quant1(v1.y, d), q6 = quant1(v1.z, d), q7 = quant1(v1.w, d);
+  q8.x = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
+         ((uint32_t)(q3 & 0xFF) << 24);
+  q8.y = (uint32_t)(q4 & 0xFF) | ((uint32_t)(q5 & 0xFF) << 8) | ((uint32_t)(q6 & 0xFF) << 16) |
+         ((uint32_t)(q7 & 0xFF) << 24);
+  const __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
+  const __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
+  const __half2 h45 = __halves2half2(__int2half_rn(q4), __int2half_rn(q5));
+  const __half2 h67 = __halves2half2(__int2half_rn(q6), __int2half_rn(q7));
+  h8.x = *reinterpret_cast<const uint32_t*>(&h01);
+  h8.y = *reinterpret_cast<const uint32_t*>(&h23);
+  h8.z = *reinterpret_cast<const uint32_t*>(&h45);
+  h8.w = *reinterpret_cast<const uint32_t*>(&h67);
+}
+
+// Each thread owns eight consecutive elements (two float4 loads issued
+// together); four threads of a warp form one 32-element block and reduce amax
+// with two xor-shuffles.
 __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restrict__ X, int N, int K,
                                                           int ldx, int8_t* __restrict__ Xq,
                                                           float* __restrict__ da, int ldda,
                                                           __half* __restrict__ Xh) {
-  const long long per_row = K >> 2;
-  const long long total = (long long)N * per_row;  // a multiple of 64: whole warps stay active
+  const long long per_row = K >> 3;                // eight-element groups per row
+  const long long total = (long long)N * per_row;  // a multiple of 32: whole warps stay active
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += stride) {
     const int n = (int)(g / per_row);
-    const int j = (int)(g - (long long)n * per_row);  // float4 index in the row
-    const float4 v = __ldg(reinterpret_cast<const float4*>(X + (size_t)n * ldx) + j);
-    float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    const int j = (int)(g - (long long)n * per_row);  // eight-element group in the row
+    const float4* src = reinterpret_cast<const float4*>(X + (size_t)n * ldx) + 2 * j;
+    const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    float a = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                    fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
     const float d = __fdiv_rn(a, 127.0f);
-    const int q0 = quant1(v.x, d), q1 = quant1(v.y, d), q2 = quant1(v.z, d), q3 = quant1(v.w, d);
-    const uint32_t packed = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) |
-                            ((uint32_t)(q2 & 0xFF) << 16) | ((uint32_t)(q3 & 0xFF) << 24);
-    reinterpret_cast<uint32_t*>(Xq + (size_t)n * K)[j] = packed;
-    if (Xh != nullptr) {
-      const __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-      const __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-      uint2 w;
-      w.x = *reinterpret_cast<const uint32_t*>(&h01);
-      w.y = *reinterpret_cast<const uint32_t*>(&h23);
-      reinterpret_cast<uint2*>(Xh + (size_t)n * K)[j] = w;
-    }
-    if ((j & 7) == 0) da[(size_t)(j >> 3) * ldda + n] = d;
+    uint2 q8;
+    uint4 h8;
+    quant8(v0, v1, d, q8, h8);
+    reinterpret_cast<uint2*>(Xq + (size_t)n * K)[j] = q8;
+    if (Xh != nullptr) reinterpret_cast<uint4*>(Xh + (size_t)n * K)[j] = h8;
+    if ((j & 3) == 0) da[(size_t)(j >> 2) * ldda + n] = d;
   }
 }
 
@@ -57,7 +71,7 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
 
 cudaError_t launch_quantize(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, int ldda,
                             __half* Xh, cudaStream_t s) {
-  const long long total = (long long)N * (K / 4);
+  const long long total = (long long)N * (K / 8);
   long long blocks = (total + 255) / 256;
   const long long cap = 152LL * 16;
   if (blocks > cap) blocks = cap;
