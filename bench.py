@@ -208,9 +208,12 @@ def workload_config(args, cfg):
                         "wexp": "W_exp centered-int8 plane, converted per call",
                         "wh": "resident binary16 operand planes"}[args.weights],
             "step": "q8_quantize_act + q6k_mmq (weights packed once, off the step)",
-            "l2": "inputs larger than L2 (146 MB f32 activation per step); 2 copies of every "
-                  "input used in turn" if args.workload == "ffn_down" else
-                  "2 copies of every input used in turn (attn_v inputs fit in L2)",
+            "l2": {"ffn_down": "inputs larger than L2 (146 MB f32 activation per step); 2 copies "
+                               "of every input used in turn",
+                   "pages_ffn_down": "inputs larger than L2 (252 MB f32 activation per step); 2 "
+                                     "copies of every input used in turn",
+                   "pages_attn_v": "inputs larger than L2 (48 MB f32 activation, 2 copies)"}.get(
+                args.workload, "2 copies of every input used in turn (attn_v inputs fit in L2)"),
             "parallelism": "replicas"}
 
 
@@ -382,8 +385,8 @@ def run_ours(args):
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
     hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    {"ffn_down": run_gemm, "attn_v": run_gemm, "skinny": run_skinny,
-     "sweep": run_sweep}[args.workload](args, q6, synth, device, rank, world, peaks, hbm, hbm_src)
+    run = {"skinny": run_skinny, "sweep": run_sweep}.get(args.workload, run_gemm)
+    run(args, q6, synth, device, rank, world, peaks, hbm, hbm_src)
 
 
 def tensor_peak(peaks):
@@ -760,7 +763,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_down",
-                    choices=["ffn_down", "attn_v", "skinny", "sweep"])
+                    choices=["ffn_down", "attn_v", "pages_ffn_down", "pages_attn_v", "skinny",
+                             "sweep"])
     ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
     ap.add_argument("--tokens", type=int, default=1, choices=[1, 4, 16],
                     help="tokens of the skinny workload")

@@ -38,6 +38,8 @@ WORKLOAD_SEED = {
     "ffn_down": 0x51360002,
     "skinny": 0x51360003,
     "sweep": 0x51360004,
+    "pages_ffn_down": 0x51360005,
+    "pages_attn_v": 0x51360006,
 }
 SWEEP_SEED = 0x51364000
 
@@ -46,6 +48,10 @@ WORKLOADS = {
     "tiny": dict(M=256, K=512, N=8, outlier_frac=0.0),
     "attn_v": dict(M=4096, K=4096, N=512, outlier_frac=0.0),
     "ffn_down": dict(M=4096, K=11008, N=3314, outlier_frac=0.01),
+    # the shapes the pages measure (a Qwen2-class 7B: hidden 3584, FFN 18944,
+    # 512-wide grouped V projection) at their ~3325-token prefill
+    "pages_ffn_down": dict(M=3584, K=18944, N=3325, outlier_frac=0.01),
+    "pages_attn_v": dict(M=512, K=3584, N=3325, outlier_frac=0.0),
 }
 SKINNY_SHAPES = {"ffn_down": (4096, 11008), "attn_v": (4096, 4096)}
 SKINNY_N = (1, 4, 16)

@@ -309,6 +309,14 @@ def test_ffn_down_full(q6, orc, source):
     check_full(q6, orc, raw, X, cfg["M"], cfg["K"], source, "ffn_down")
 
 
+@pytest.mark.parametrize("name", ["pages_ffn_down", "pages_attn_v"])
+def test_pages_shapes_full(q6, orc, name):
+    """The shapes the pages measure (3584 x 18944 and 512 x 3584, N = 3325)."""
+    raw, X, cfg = synth.workload(name)
+    w, act, path = check_full(q6, orc, raw, X, cfg["M"], cfg["K"], "raw", name)
+    assert path == "tc_raw"
+
+
 @pytest.mark.parametrize("weight", ["ffn_down", "attn_v"])
 @pytest.mark.parametrize("N", synth.SKINNY_N)
 def test_skinny_full(q6, orc, weight, N):
