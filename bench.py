@@ -470,6 +470,19 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
             q6.sync_status()
             ams = a.elapsed_time(b) / args.alt_steps
             alt[other] = {"q6k_mmq_ms": ams, "q6k_mmq_tops": ops_per_step / ams / 1e9}
+        # the pages' route on the legacy mma.sync int8 path, as a comparison point
+        for i in range(3):
+            q6.mmq_mma_sync(Wa, acts[0], Y=Ys[0])
+        a, b = ev_pair()
+        a.record()
+        for i in range(args.alt_steps):
+            q6.mmq_mma_sync(Wa, acts[i % R], Y=Ys[i % R])
+        b.record()
+        torch.cuda.synchronize()
+        q6.sync_status()
+        ams = a.elapsed_time(b) / args.alt_steps
+        alt["mma_sync_wexp"] = {"q6k_mmq_mma_sync_ms": ams, "tops": ops_per_step / ams / 1e9,
+                                "note": "legacy mma.sync int8 comparison path"}
         del Wa
 
     e2e = None

@@ -56,6 +56,7 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_TC_WEXP 2 /* conversion of the W_exp plane into the workspace + tensor-core GEMM */
 #define Q6_PATH_SKINNY 3  /* CUDA-core kernel for N <= Q6_SKINNY_MAX_N on the packed q6_K plane */
 #define Q6_PATH_TC_WH 4   /* tensor-core GEMM on resident binary16 operand planes */
+#define Q6_PATH_SYNC_WEXP 5 /* legacy mma.sync int8 GEMM on the W_exp plane (q6k_mmq_mma_sync) */
 
 #define Q6_SKINNY_MAX_N 16
 
@@ -179,6 +180,25 @@ int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, in
             const int8_t *Xq, const float *da, const uint16_t *Xh, int N, float *Y, int ldy,
             void *workspace, size_t workspace_bytes, int32_t *partials, int *path_out,
             q6_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * The pages' own route on the legacy warp-level tensor path, kept as a
+ * measured comparison point for q6k_mmq ("r38 -- q6_K BT-style raw-byte mma
+ * kernel", Sec. 2.2-2.4; "r53 -- q6_K bundle: W_exp pre-expansion plane",
+ * Sec. 2.3): exact int32 sub-block partials from int8 mma.sync on the W_exp
+ * plane and Xq, sc folded per 32-element chunk in integers, f32 rescale.
+ * Same result contract as q6k_mmq (Y within the same tolerance; partials, when
+ * not NULL, are the same int32 [N][M][K/32] chunk sums).
+ *
+ *   plane : packed weights (its sc and dT sub-planes are read); required.
+ *   wexp  : the W_exp plane; required.
+ *   Xq, da: quantised activations (any N >= 0).
+ * Alignment: plane 256 B; wexp, Xq, da 16 B; Y, partials 4 B. Allocates
+ * nothing. path_out receives Q6_PATH_SYNC_WEXP (or Q6_PATH_NONE for N == 0).
+ * -------------------------------------------------------------------- */
+int q6k_mmq_mma_sync(const void *plane, const int8_t *wexp, int M, int K, const int8_t *Xq,
+                     const float *da, int N, float *Y, int ldy, int32_t *partials, int *path_out,
+                     q6_stream_t s);
 
 /* ------------------------------------------------------------------------
  * For callers that cannot allocate device memory when they make this call

@@ -15,9 +15,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
 
 Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
-PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH = range(5)
+PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH, PATH_SYNC_WEXP = range(6)
 PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
-              PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh"}
+              PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh", PATH_SYNC_WEXP: "sync_wexp"}
 SKINNY_MAX_N = 16
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).
@@ -37,6 +37,7 @@ SIGNATURES = [
     ("q6k_mmq", _I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP,
                      _P]),
     ("q6k_mmq_noalloc", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _IP, _P]),
+    ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _IP, _P]),
 ]
 
 
@@ -215,6 +216,26 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
     _check(load().q6k_mmq(_ptr(w.plane), _ptr(wx), _ptr(w16), M, K, _ptr(act.xq), _ptr(act.da),
                           _ptr(act.xh), N, _ptr(Y), Y.stride(0), _ptr(ws), ws_bytes, _ptr(P),
                           ctypes.byref(path), _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value)), P
+
+
+def mmq_mma_sync(w: Weights, act: Activations, Y=None, partials: bool = False, stream=None):
+    """The same GEMM on the legacy mma.sync int8 path (the pages' route), from
+    the W_exp plane: a comparison point for mmq(). Returns (Y, path, partials)."""
+    import torch
+    N, M, K = act.N, w.M, w.K
+    if act.K != K:
+        raise Q6Error(Q6_EINVAL, "activation K does not match the weight")
+    if w.wexp is None:
+        raise Q6Error(Q6_EINVAL, "weights were packed without the wexp plane")
+    dev = w.plane.device
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
+    path = ctypes.c_int(-1)
+    _check(load().q6k_mmq_mma_sync(_ptr(w.plane), _ptr(w.wexp), M, K, _ptr(act.xq), _ptr(act.da), N,
+                                   _ptr(Y), Y.stride(0), _ptr(P), ctypes.byref(path),
+                                   _stream(stream)))
     return Y, PATH_NAMES.get(path.value, str(path.value)), P
 
 

@@ -57,7 +57,8 @@ int device_state(DevState** out) {
     }
     if ((e = cudaMalloc(&st.status, 256))) return cuda_fail(e, "cudaMalloc(status)");
     if ((e = cudaMemset(st.status, 0, 256))) return cuda_fail(e, "cudaMemset(status)");
-    if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()))
+    if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()) ||
+        (e = q6::mmq_sync_prepare()))
       return cuda_fail(e, "cudaFuncSetAttribute");
     if (!g_encode) {
       void* fn = nullptr;
@@ -304,6 +305,31 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, partials, st->status, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
   if (path_out) *path_out = path;
+  return Q6_OK;
+}
+
+int q6k_mmq_mma_sync(const void* plane, const int8_t* wexp, int M, int K, const int8_t* Xq,
+                     const float* da, int N, float* Y, int ldy, int32_t* partials, int* path_out,
+                     q6_stream_t s) {
+  if (path_out) *path_out = Q6_PATH_NONE;
+  if (M <= 0 || K <= 0 || K % 256 || N < 0)
+    return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
+  if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
+  if (N == 0) return Q6_OK;
+  if (!plane || !wexp || !Xq || !da || !Y)
+    return fail(Q6_EINVAL, "plane, wexp, Xq, da and Y are required");
+  if (!aligned(plane, 256) || !aligned(wexp, 16) || !aligned(Xq, 16) || !aligned(da, 16) ||
+      !aligned(Y, 4) || (partials && !aligned(partials, 4)))
+    return fail(Q6_EALIGN, "plane 256 B; wexp, Xq, da 16 B; Y, partials 4 B");
+  if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
+    return fail(Q6_ESIZE, "problem too large");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = q6::launch_mmq_sync(static_cast<const uint8_t*>(plane), wexp, M, K, Xq, da,
+                                      ldda_of(N), N, Y, ldy, partials, (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "mma.sync kernel launch");
+  if (path_out) *path_out = Q6_PATH_SYNC_WEXP;
   return Q6_OK;
 }
 

@@ -70,7 +70,8 @@ int na_setup(NaDev** out) {
     if (major != 10 || minor != 3)
       return na_fail(Q6_EARCH, "device %d is compute capability %d.%d; needs 10.3", dev, major,
                      minor);
-    if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()))
+    if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()) ||
+        (e = q6::mmq_sync_prepare()))
       return na_fail(Q6_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     void* addr = nullptr;
     if ((e = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) || !addr)

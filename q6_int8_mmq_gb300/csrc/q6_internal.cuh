@@ -50,6 +50,10 @@ cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* 
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
                               unsigned int* status, cudaStream_t s);
 cudaError_t mmq_skinny_prepare();
+cudaError_t launch_mmq_sync(const uint8_t* plane, const int8_t* wexp, int M, int K,
+                            const int8_t* Xq, const float* da, int ldda, int N, float* Y, int ldy,
+                            int32_t* partials, cudaStream_t s);
+cudaError_t mmq_sync_prepare();
 
 struct TcMaps {
   CUtensorMap x;    // Xh   [N][K] f16, box {64, 128}, 128B swizzle

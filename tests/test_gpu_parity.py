@@ -309,6 +309,38 @@ def test_ffn_down_full(q6, orc, source):
     check_full(q6, orc, raw, X, cfg["M"], cfg["K"], source, "ffn_down")
 
 
+@pytest.mark.parametrize("M,K,N", [(256, 512, 8), (200, 768, 129), (384, 768, 300), (130, 1024, 1)],
+                         ids=lambda v: str(v))
+def test_mma_sync_comparison_path(q6, orc, M, K, N):
+    """The legacy mma.sync path: bit-exact chunk partials and Y within tolerance."""
+    raw = synth.q6k_raw_weights(500 + M + N, M, K)
+    X = synth.activations(600 + M + N, N, K, outlier_frac=0.02)
+    w = q6.pack_weights(dev(raw), M, K, wexp=True)
+    act = q6.quantize_act(dev(X))
+    Y, path, P = q6.mmq_mma_sync(w, act, partials=True)
+    q6.sync_status()
+    assert path == "sync_wexp"
+    xq_o, da_o = quant_check(act, X, orc)
+    Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+    assert np.array_equal(host(P), chunk_sums(Po, raw, M, K))
+    check_y(host(Y), Yo, f"mma.sync {M}x{K}x{N}")
+    Y2, _, _ = q6.mmq_mma_sync(w, act)
+    q6.sync_status()
+    check_y(host(Y2), Yo, "mma.sync fast variant")
+
+
+def test_mma_sync_ffn_down_full(q6, orc):
+    raw, X, cfg = synth.workload("ffn_down")
+    M, K = cfg["M"], cfg["K"]
+    w = q6.pack_weights(dev(raw), M, K, wexp=True)
+    act = q6.quantize_act(dev(X))
+    Y, path, _ = q6.mmq_mma_sync(w, act)
+    q6.sync_status()
+    xq_o, da_o = quant_check(act, X, orc)
+    tok = sampled_tokens(X.shape[0])
+    check_y(host(Y)[tok], orc.mmq(raw, M, K, xq_o[tok], da_o[tok]), "mma.sync ffn_down")
+
+
 @pytest.mark.parametrize("name", ["pages_ffn_down", "pages_attn_v"])
 def test_pages_shapes_full(q6, orc, name):
     """The shapes the pages measure (3584 x 18944 and 512 x 3584, N = 3325)."""
