@@ -1,0 +1,92 @@
+"""The C ABI on a caller's stream and inside a CUDA graph (needs a GB300).
+
+Every call is asynchronous on the stream it is given and allocates nothing on
+the hot path, so the whole per-batch path (quantise, unpack, GEMM) can run on
+a side stream and can be captured once into a CUDA graph and replayed with new
+inputs. Results are checked against the oracle with the GEMM tolerance.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from q6_int8_mmq_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+MAX_REL = 1e-3
+NORMWISE = 1e-5
+
+
+@pytest.fixture(scope="module")
+def q6():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import q6_int8_mmq_gb300 as q6mod
+    from q6_int8_mmq_gb300 import build as q6build
+    q6build.build()
+    q6mod.load()
+    return q6mod
+
+
+def close(Y, Yo):
+    Y = Y.detach().cpu().numpy().astype(np.float64)
+    err = np.abs(Y - Yo)
+    assert np.all(np.isfinite(Y))
+    assert err.max() <= MAX_REL * np.abs(Yo).max()
+    assert err.sum() <= NORMWISE * np.abs(Yo).sum()
+
+
+def expected(raw, M, K, X):
+    orc = oracle.get()
+    xq, da = orc.quantize(X)
+    return orc.mmq(raw, M, K, xq, da)
+
+
+@pytest.mark.parametrize("N", [200, 9])   # tensor-core and skinny kernels
+def test_path_on_a_side_stream(q6, N):
+    import torch
+    M, K = 256, 768
+    raw = synth.q6k_raw_weights(0x51360901, M, K)
+    X = synth.activations(0x51360902 + N, N, K)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        w = q6.pack_weights(torch.from_numpy(raw).cuda(), M, K, stream=side)
+        act = q6.quantize_act(torch.from_numpy(X).cuda(), stream=side)
+        Y, path, _ = q6.mmq(w, act, source="raw", stream=side)
+    q6.sync_status(side)
+    assert path == ("skinny" if N <= q6.SKINNY_MAX_N else "tc_raw")
+    close(Y, expected(raw, M, K, X))
+
+
+def test_whole_path_in_a_cuda_graph(q6):
+    """quantise + unpack + GEMM captured once, replayed for two inputs."""
+    import torch
+    M, K, N = 384, 1024, 300
+    raw = synth.q6k_raw_weights(0x51360903, M, K)
+    X1 = synth.activations(0x51360904, N, K)
+    X2 = synth.activations(0x51360905, N, K, outlier_frac=0.02)
+    w = q6.pack_weights(torch.from_numpy(raw).cuda(), M, K)
+    Xs = torch.from_numpy(X1).cuda()             # static input of the graph
+    act = q6.alloc_activations(N, K)
+    Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    ws = torch.empty(q6.workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
+
+    def step():
+        q6.quantize_act(Xs, out=act)
+        q6.mmq(w, act, Y=Y, source="raw", workspace=ws)
+
+    step()                                       # first use of the device: set-up runs here
+    q6.sync_status()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    for X in (X1, X2):
+        Xs.copy_(torch.from_numpy(X).cuda())
+        Y.fill_(float("nan"))
+        graph.replay()
+        q6.sync_status()
+        close(Y, expected(raw, M, K, X))
