@@ -16,9 +16,13 @@
 //
 // Streaming: warps stride over the rows, with the grid sized to one resident
 // wave (4 warps per CTA, 64 registers, 8 CTAs per SM) so every warp starts at
-// once and reads its row's qlh run in coalesced 768-byte steps. Measured on
-// GB300, neither loading several steps ahead (fewer resident warps) nor a
-// cp.async.bulk ring of whole rows in shared memory beat this form.
+// once and reads its row's qlh run in coalesced 768-byte steps; the loads of
+// the next step are in flight while the current step is computed. The kernel
+// is instantiated per token bucket (N = 1, <= 4, <= 16) so small N does not
+// pay registers for 16 accumulators. Measured on GB300 and not kept: loading
+// two to four steps ahead (more registers, fewer resident warps), a
+// cp.async.bulk ring of whole rows and a per-warp cp.async ring in shared
+// memory.
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -26,7 +30,6 @@ namespace {
 
 constexpr int kWarps = 4;      // warps per CTA
 constexpr int kMinBlocks = 8;  // resident CTAs per SM (64 registers per thread)
-constexpr int kGroupGlobal = 1;  // iterations loaded ahead of the math
 
 // Bytes (code - 32) mod 256 of four 6-bit codes: code + 96 never carries out
 // of its byte, and adding 128 more is a flip of bit 7.
@@ -34,113 +37,76 @@ __device__ __forceinline__ uint32_t center4(uint32_t code) {
   return (code + 0x60606060u) ^ 0x80808080u;
 }
 
-// The dot products of one weight row with the N activation rows. qlh, sc and
-// dbits point at the row's sub-plane runs; the result is reduced across the
-// warp and written by lane 0. Loads run kGroup iterations (4 super-blocks,
-// 768 bytes of codes each) ahead of the math.
-template <bool kPartials, int kGroup>
-__device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
-                                        const int8_t* __restrict__ sc_row,
-                                        const uint16_t* __restrict__ d_row, int m, int M, int K,
-                                        const int8_t* __restrict__ Xq, const float* __restrict__ da,
-                                        int ldda, int N, float* __restrict__ Y, int ldy,
-                                        int32_t* __restrict__ partials) {
+// One lane's share of one step: sub-blocks sa = 8*half + s4 and sa + 4 of
+// super-block sb, from its 16 ql bytes L and 16 qh bytes H, for every token.
+template <bool kPartials, int kMaxN>
+__device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a, int sc_b,
+                                         uint16_t dbits, int sb, int m, int M, int K,
+                                         const int8_t* __restrict__ Xq,
+                                         const float* __restrict__ da, int ldda, int N,
+                                         int32_t* __restrict__ partials, float (&acc)[kMaxN]) {
   const int lane = threadIdx.x & 31;
-  const int nsb = K / 256;
-  const int sbi = lane >> 3;  // super-block within the iteration
   const int half = (lane >> 2) & 1;
   const int s4 = lane & 3;
   const int fsh = 2 * (s4 >> 1);  // field of the low-nibble sub-block
   const int sa = 8 * half + s4;   // sub-block (0..15) of the low nibbles; sb_b = sa + 4
-
-  float acc[Q6_SKINNY_MAX_N];
+  const uint32_t Lw[4] = {L.x, L.y, L.z, L.w};
+  const uint32_t Hw[4] = {H.x, H.y, H.z, H.w};
+  uint32_t va[4], vb[4];
 #pragma unroll
-  for (int n = 0; n < Q6_SKINNY_MAX_N; ++n) acc[n] = 0.0f;
-
-  for (int g0 = 0; g0 < nsb; g0 += 4 * kGroup) {
-    // With several tokens the math per step is longer: an L2 prefetch of the
-    // next step's records keeps more bytes in flight without more registers
-    // (measured: N = 4 and 16 faster, N = 1 slower, so only for N > 1).
-    if (N > 1) {
-      const int pf = g0 + 4 * kGroup + sbi;
-      if (pf < nsb)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(qlh_row + (size_t)(2 * pf + half) * 96 +
-                                                      32 * (s4 & 1)));
-    }
-    uint4 L[kGroup], H[kGroup];
-    int sca[kGroup], scb[kGroup];
-    uint16_t dbits[kGroup];
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t ca = (Lw[w] & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
+    const uint32_t cb = ((Lw[w] >> 4) & 0x0F0F0F0Fu) | (((Hw[w] >> (fsh + 4)) & 0x03030303u) << 4);
+    va[w] = center4(ca);
+    vb[w] = center4(cb);
+  }
+  const float d = __half2float(__ushort_as_half(dbits));
+  const float dsc_a = d * (float)sc_a;
+  const float dsc_b = d * (float)sc_b;
+  const int ka = 256 * sb + 16 * sa;  // first element of sub-block a
+  const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
 #pragma unroll
-    for (int u = 0; u < kGroup; ++u) {
-      const int sb = g0 + 4 * u + sbi;
-      if (sb < nsb) {
-        const uint8_t* hb = qlh_row + (size_t)(2 * sb + half) * 96;
-        L[u] = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
-        H[u] = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
-        sca[u] = __ldg(sc_row + 16 * sb + sa);
-        scb[u] = __ldg(sc_row + 16 * sb + sa + 4);
-        dbits[u] = __ldg(d_row + sb);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kGroup; ++u) {
-      const int sb = g0 + 4 * u + sbi;
-      if (sb < nsb) {
-        const uint32_t Lw[4] = {L[u].x, L[u].y, L[u].z, L[u].w};
-        const uint32_t Hw[4] = {H[u].x, H[u].y, H[u].z, H[u].w};
-        uint32_t va[4], vb[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const uint32_t ca = (Lw[w] & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
-          const uint32_t cb =
-              ((Lw[w] >> 4) & 0x0F0F0F0Fu) | (((Hw[w] >> (fsh + 4)) & 0x03030303u) << 4);
-          va[w] = center4(ca);
-          vb[w] = center4(cb);
-        }
-        const float d = __half2float(__ushort_as_half(dbits[u]));
-        const int sc_a = sca[u], sc_b = scb[u];
-        const float dsc_a = d * (float)sc_a;
-        const float dsc_b = d * (float)sc_b;
-        const int ka = 256 * sb + 16 * sa;  // first element of sub-block a
-        const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
-#pragma unroll
-        for (int n = 0; n < Q6_SKINNY_MAX_N; ++n) {
-          if (n < N) {
-            const int8_t* xr = Xq + (size_t)n * K;
-            const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
-            const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
-            int pa = __dp4a((int)va[0], (int)xa.x, 0);
-            pa = __dp4a((int)va[1], (int)xa.y, pa);
-            pa = __dp4a((int)va[2], (int)xa.z, pa);
-            pa = __dp4a((int)va[3], (int)xa.w, pa);
-            int pb = __dp4a((int)vb[0], (int)xb.x, 0);
-            pb = __dp4a((int)vb[1], (int)xb.y, pb);
-            pb = __dp4a((int)vb[2], (int)xb.z, pb);
-            pb = __dp4a((int)vb[3], (int)xb.w, pb);
-            const float daa = __ldg(da + (size_t)ca_blk * ldda + n);
-            const float dab = __ldg(da + (size_t)cb_blk * ldda + n);
-            acc[n] = fmaf(dsc_a * daa, (float)pa, acc[n]);
-            acc[n] = fmaf(dsc_b * dab, (float)pb, acc[n]);
-            if (kPartials) {
-              // chunk partials sc*P summed over the chunk's two sub-blocks; the
-              // other sub-block of each chunk is in lane ^ 1 (active together)
-              const unsigned act = __activemask();
-              const int ta = sc_a * pa, tb = sc_b * pb;
-              const int sa2 = ta + __shfl_xor_sync(act, ta, 1);
-              const int sb2 = tb + __shfl_xor_sync(act, tb, 1);
-              if ((s4 & 1) == 0) {
-                int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 32) + (size_t)sb * 8;
-                pr[sa >> 1] = sa2;
-                pr[(sa + 4) >> 1] = sb2;
-              }
-            }
-          }
+  for (int n = 0; n < kMaxN; ++n) {
+    if (n < N) {
+      const int8_t* xr = Xq + (size_t)n * K;
+      const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
+      const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
+      int pa = __dp4a((int)va[0], (int)xa.x, 0);
+      pa = __dp4a((int)va[1], (int)xa.y, pa);
+      pa = __dp4a((int)va[2], (int)xa.z, pa);
+      pa = __dp4a((int)va[3], (int)xa.w, pa);
+      int pb = __dp4a((int)vb[0], (int)xb.x, 0);
+      pb = __dp4a((int)vb[1], (int)xb.y, pb);
+      pb = __dp4a((int)vb[2], (int)xb.z, pb);
+      pb = __dp4a((int)vb[3], (int)xb.w, pb);
+      const float daa = __ldg(da + (size_t)ca_blk * ldda + n);
+      const float dab = __ldg(da + (size_t)cb_blk * ldda + n);
+      acc[n] = fmaf(dsc_a * daa, (float)pa, acc[n]);
+      acc[n] = fmaf(dsc_b * dab, (float)pb, acc[n]);
+      if (kPartials) {
+        // chunk partials sc*P summed over the chunk's two sub-blocks; the
+        // other sub-block of each chunk is in lane ^ 1 (active together)
+        const unsigned act = __activemask();
+        const int ta = sc_a * pa, tb = sc_b * pb;
+        const int sa2 = ta + __shfl_xor_sync(act, ta, 1);
+        const int sb2 = tb + __shfl_xor_sync(act, tb, 1);
+        if ((s4 & 1) == 0) {
+          int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 32) + (size_t)sb * 8;
+          pr[sa >> 1] = sa2;
+          pr[(sa + 4) >> 1] = sb2;
         }
       }
     }
   }
+}
+
+// Reduces each token's sum across the warp; lane 0 writes Y[n][m].
+template <int kMaxN>
+__device__ __forceinline__ void row_store(float (&acc)[kMaxN], int m, int N, float* __restrict__ Y,
+                                          int ldy) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int n = 0; n < Q6_SKINNY_MAX_N; ++n) {
+  for (int n = 0; n < kMaxN; ++n) {
     if (n < N) {
       float v = acc[n];
       v += __shfl_xor_sync(0xffffffffu, v, 16);
@@ -153,50 +119,108 @@ __device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
   }
 }
 
+// The dot products of one weight row with the N <= kMaxN activation rows.
+// Each step covers 4 super-blocks (768 bytes of codes per warp); the loads of
+// step i + 1 are issued before the math of step i (a one-step software
+// pipeline held in registers). The result is reduced across the warp and
+// written by lane 0.
+template <bool kPartials, int kMaxN>
+__device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
+                                        const int8_t* __restrict__ sc_row,
+                                        const uint16_t* __restrict__ d_row, int m, int M, int K,
+                                        const int8_t* __restrict__ Xq, const float* __restrict__ da,
+                                        int ldda, int N, float* __restrict__ Y, int ldy,
+                                        int32_t* __restrict__ partials) {
+  const int lane = threadIdx.x & 31;
+  const int nsb = K / 256;
+  const int sbi = lane >> 3;  // super-block within the step
+  const int half = (lane >> 2) & 1;
+  const int s4 = lane & 3;
+  const int sa = 8 * half + s4;  // sub-block (0..15) of the low nibbles; sb_b = sa + 4
+
+  float acc[kMaxN];
+#pragma unroll
+  for (int n = 0; n < kMaxN; ++n) acc[n] = 0.0f;
+
+  uint4 L = make_uint4(0, 0, 0, 0), H = L;
+  int sca = 0, scb = 0;
+  uint16_t dbits = 0;
+  auto load = [&](int sb, uint4& l, uint4& h, int& a, int& b, uint16_t& dd) {
+    if (sb < nsb) {
+      const uint8_t* hb = qlh_row + (size_t)(2 * sb + half) * 96;
+      l = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
+      h = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
+      a = __ldg(sc_row + 16 * sb + sa);
+      b = __ldg(sc_row + 16 * sb + sa + 4);
+      dd = __ldg(d_row + sb);
+    }
+  };
+  load(sbi, L, H, sca, scb, dbits);
+  for (int g0 = 0; g0 < nsb; g0 += 4) {
+    uint4 L2 = make_uint4(0, 0, 0, 0), H2 = L2;
+    int sca2 = 0, scb2 = 0;
+    uint16_t dbits2 = 0;
+    load(g0 + 4 + sbi, L2, H2, sca2, scb2, dbits2);  // next step, in flight during this one
+    const int sb = g0 + sbi;
+    if (sb < nsb)
+      step_dot<kPartials, kMaxN>(L, H, sca, scb, dbits, sb, m, M, K, Xq, da, ldda, N, partials,
+                                 acc);
+    L = L2;
+    H = H2;
+    sca = sca2;
+    scb = scb2;
+    dbits = dbits2;
+  }
+  row_store<kMaxN>(acc, m, N, Y, ldy);
+}
+
 // One warp per row, straight from global memory.
-template <bool kPartials>
+template <bool kPartials, int kMaxN>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
     const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
     const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
     int32_t* __restrict__ partials) {
   const int warps = (int)gridDim.x * kWarps;
   for (int m = blockIdx.x * kWarps + (threadIdx.x >> 5); m < M; m += warps)
-    row_dot<kPartials, kGroupGlobal>(
+    row_dot<kPartials, kMaxN>(
         plane + g.qlh_off + (size_t)m * g.qlh_row,
         reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)m * (K / 16),
         reinterpret_cast<const uint16_t*>(plane + g.d_off + (size_t)m * g.d_row), m, M, K, Xq, da,
         ldda, N, Y, ldy, partials);
 }
 
-
 }  // namespace
 
 cudaError_t mmq_skinny_prepare() { return cudaSuccess; }
+
+template <bool P, int kMaxN>
+cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
+                          const float* da, int ldda, int N, float* Y, int ldy, int32_t* partials,
+                          cudaStream_t s) {
+  // one resident wave: as many blocks as fit, warps striding over the rows
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mmq_skinny_kernel<P, kMaxN>,
+                                                         kWarps * 32, 0)))
+    return e;
+  const long long need = (M + kWarps - 1) / kWarps, cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
+  const unsigned blocks = (unsigned)(need < cap ? need : cap);
+  mmq_skinny_kernel<P, kMaxN><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y,
+                                                             ldy, partials);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
                               unsigned int* status, cudaStream_t s) {
   (void)status;  // the skinny kernel has no waits to bound
   const PlaneGeom g = plane_geom(M, K);
-  // one resident wave: as many blocks as fit, warps striding over the rows
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
-  if (partials)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mmq_skinny_kernel<true>, kWarps * 32, 0);
-  else
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mmq_skinny_kernel<false>, kWarps * 32, 0);
-  if (e != cudaSuccess) return e;
-  const long long need = (M + kWarps - 1) / kWarps, cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
-  const unsigned blocks = (unsigned)(need < cap ? need : cap);
-  if (partials)
-    mmq_skinny_kernel<true><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y, ldy,
-                                                           partials);
-  else
-    mmq_skinny_kernel<false><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y,
-                                                            ldy, nullptr);
-  return cudaGetLastError();
+  if (partials) return launch_bucket<true, Q6_SKINNY_MAX_N>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s);
+  if (N == 1) return launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+  if (N <= 4) return launch_bucket<false, 4>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+  return launch_bucket<false, Q6_SKINNY_MAX_N>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
 }
 
 }  // namespace q6
