@@ -287,17 +287,87 @@ def kernel_ms(step, steps: int, marks: int):
     return [statistics.mean(e[k].elapsed_time(e[k + 1]) for e in evs) for k in range(marks - 1)]
 
 
-def e2e_run(step_host, steps: int, device):
-    """End to end: each step copies its input from pinned host memory, runs the
-    path through the public API and copies the result back."""
+OVERLAP = "H2D and D2H on their own streams, overlapped with the neighbouring steps' compute"
+GRAPHED = "each step's H2D, compute and D2H in order; the K steps replayed as one CUDA graph"
+
+
+def e2e_run_overlapped(step, ins, outs, steps: int, device):
+    """End to end as a serving loop runs it: step i copies its inputs in from
+    pinned host memory on an H2D stream while step i-1 computes, computes on
+    the current stream, and copies its result out on a D2H stream while step
+    i+1 computes. ins[j] / outs[j] are the (destination, source) copies of a
+    step that uses buffer slot j = i % len(ins); events keep a slot's inputs
+    until its step has read them and its result until it has been copied
+    out. Every step's copies lie inside the timed region, which ends when the
+    last result is on the host."""
+    import torch
+    cur = torch.cuda.current_stream(device)
+    h2d, d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    R = len(ins)
+    loaded = [torch.cuda.Event() for _ in range(R)]
+    computed = [torch.cuda.Event() for _ in range(R)]
+    drained = [torch.cuda.Event() for _ in range(R)]
+    used = [False] * R
+
+    def one(i):
+        j = i % R
+        with torch.cuda.stream(h2d):
+            if used[j]:
+                h2d.wait_event(computed[j])
+            for dst, src in ins[j]:
+                dst.copy_(src, non_blocking=True)
+            loaded[j].record(h2d)
+        cur.wait_event(loaded[j])
+        if used[j]:
+            cur.wait_event(drained[j])
+        step(i)
+        computed[j].record(cur)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(computed[j])
+            for dst, src in outs[j]:
+                dst.copy_(src, non_blocking=True)
+            drained[j].record(d2h)
+        used[j] = True
+
+    for i in range(2 * R):
+        one(i)
+    torch.cuda.synchronize(device)
+    a, b = ev_pair()
+    barrier(device)
+    a.record(cur)
+    h2d.wait_stream(cur)
+    d2h.wait_stream(cur)
+    for i in range(steps):
+        one(i)
+    cur.wait_stream(d2h)
+    b.record(cur)
+    torch.cuda.synchronize(device)
+    return reduce_max(a.elapsed_time(b), device)
+
+
+def e2e_graph(step_host, steps: int, device) -> float:
+    """End to end for the small-batch path, the way a decode loop runs it: the
+    K steps, each with its H2D copy from pinned host memory, its compute and
+    its D2H copy, captured once as a CUDA graph and replayed (the host's
+    launch rate would otherwise be what is measured). Returns the ms of one
+    replay of all K steps."""
     import torch
     for i in range(2):
         step_host(i)
+    torch.cuda.synchronize(device)
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(steps):
+                step_host(i)
+    g.replay()
+    torch.cuda.synchronize(device)
     a, b = ev_pair()
     barrier(device)
     a.record()
-    for i in range(steps):
-        step_host(i)
+    g.replay()
     b.record()
     torch.cuda.synchronize(device)
     return reduce_max(a.elapsed_time(b), device)
@@ -488,18 +558,14 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     e2e = None
     if args.e2e_steps > 0:
         Xh = torch.from_numpy(X).pin_memory()
-        Yh = torch.empty((N, M), dtype=torch.float32).pin_memory()
-
-        def step_host(i):
-            j = i % R
-            Xs[j].copy_(Xh, non_blocking=True)
-            step(i)
-            Yh.copy_(Ys[j], non_blocking=True)
-        e_ms = e2e_run(step_host, args.e2e_steps, device)
+        Yh = [torch.empty((N, M), dtype=torch.float32).pin_memory() for _ in range(R)]
+        e_ms = e2e_run_overlapped(step, [[(Xs[j], Xh)] for j in range(R)],
+                                  [[(Yh[j], Ys[j])] for j in range(R)], args.e2e_steps, device)
         q6.sync_status()
         e2e = {"value": job_throughput(ops_per_step * args.e2e_steps, world, e_ms / 1e3) / 1e12,
                "unit": UNIT, "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": N * M * 4,
-               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps}
+               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
+               "copies": OVERLAP}
 
     others = {}
     if rank == 0 and world == 1 and args.workload == "ffn_down" and args.other_configs:
@@ -527,7 +593,7 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
                      "frac": tflops / peak_t, "peak_source": peak_src, "traffic": traffic,
                      "algorithmic": f"2*M*N*K = {ops_per_step:.4g} flop per launch"},
         "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": (2 if src == "wh" else 3) * args.steps,
+        "gpu_launches": (1 + q6.mmq_launches(M, K, N, src == "wh")) * args.steps,
         "clocks": clk, "clocks_ok": clocks_ok(clk),
         "kernels": {
             "q6k_mmq": {"ms": m_ms, "tflops": tflops, "path": path[0],
@@ -588,18 +654,21 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     R = max(4, (4 * 129 * 2 ** 20) // q6.plane_bytes(M, K)[0] + 1)
     Ws = [q6.pack_weights(raw_d, M, K) for _ in range(R)]
     del raw_d
-    Xd = torch.from_numpy(X).to(device)
-    act = q6.alloc_activations(n, K, device, want_xh=False)
-    Y = torch.empty((n, M), dtype=torch.float32, device=device)
+    S = 2  # activation / result buffer slots (the end-to-end run overlaps two steps)
+    Xds = [torch.from_numpy(X).to(device) for _ in range(S)]
+    acts = [q6.alloc_activations(n, K, device, want_xh=False) for _ in range(S)]
+    Ys = [torch.empty((n, M), dtype=torch.float32, device=device) for _ in range(S)]
+    Xd, act, Y = Xds[0], acts[0], Ys[0]
     path = [None]
 
     def step(i, ev=None):
+        j = i % S
         if ev is not None:
             ev[0].record()
-        q6.quantize_act(Xd, out=act)
+        q6.quantize_act(Xds[j], out=acts[j])
         if ev is not None:
             ev[1].record()
-        _, path[0], _ = q6.mmq(Ws[i % R], act, Y=Y)
+        _, path[0], _ = q6.mmq(Ws[i % R], acts[j], Y=Ys[j])
         if ev is not None:
             ev[2].record()
 
@@ -627,16 +696,18 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     e2e = None
     if args.e2e_steps > 0:
         Xh = torch.from_numpy(X).pin_memory()
-        Yh = torch.empty((n, M), dtype=torch.float32).pin_memory()
+        Yh = [torch.empty((n, M), dtype=torch.float32).pin_memory() for _ in range(S)]
 
         def step_host(i):
-            Xd.copy_(Xh, non_blocking=True)
+            j = i % S
+            Xds[j].copy_(Xh, non_blocking=True)
             step(i)
-            Yh.copy_(Y, non_blocking=True)
-        e_ms = e2e_run(step_host, args.e2e_steps, device)
+            Yh[j].copy_(Ys[j], non_blocking=True)
+        e_ms = e2e_graph(step_host, args.e2e_steps, device)
         e2e = {"value": job_throughput(ops_per_step * args.e2e_steps, world, e_ms / 1e3) / 1e12,
                "unit": UNIT, "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": n * M * 4,
-               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps}
+               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
+               "copies": GRAPHED}
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         cpu = oracle_baseline(raw, X, M, K, args.cpu_budget, n)
@@ -688,8 +759,14 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     ws = torch.empty(q6.workspace_bytes(4096, 11008, N), dtype=torch.uint8, device=device)
     marks = 1 + 4 * L
 
+    # the streams the end-to-end run copies in and out alternate between two
+    # buffer slots; everything else is used by one step at a time
+    Xvds, Xdds = [Xvd, Xvd.clone()], [Xdd, Xdd.clone()]
+    Yds = [Yd, torch.empty_like(Yd)]
+
     def step(i, ev=None):
         k = 0
+        Xvd, Xdd, Yd = Xvds[i % 2], Xdds[i % 2], Yds[i % 2]
         if ev is not None:
             ev[0].record()
         for wv, wd in layers:
@@ -721,19 +798,14 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     e2e = None
     if args.e2e_steps > 0:
         Xvh, Xdh = torch.from_numpy(Xv).pin_memory(), torch.from_numpy(Xd).pin_memory()
-        Yh = torch.empty((N, 4096), dtype=torch.float32).pin_memory()
-
-        def step_host(i):
-            Xvd.copy_(Xvh, non_blocking=True)
-            Xdd.copy_(Xdh, non_blocking=True)
-            step(i)
-            Yh.copy_(Yd, non_blocking=True)
+        Yh = [torch.empty((N, 4096), dtype=torch.float32).pin_memory() for _ in range(2)]
         e_steps = max(1, min(args.e2e_steps, 5))
-        e_ms = e2e_run(step_host, e_steps, device)
+        e_ms = e2e_run_overlapped(step, [[(Xvds[j], Xvh), (Xdds[j], Xdh)] for j in range(2)],
+                                  [[(Yh[j], Yds[j])] for j in range(2)], e_steps, device)
         e2e = {"value": job_throughput(ops_per_step * e_steps, world, e_ms / 1e3) / 1e12,
                "unit": UNIT, "h2d_bytes_per_step": Xv.nbytes + Xd.nbytes,
                "d2h_bytes_per_step": N * 4096 * 4, "steps": e_steps,
-               "ms_per_step": e_ms / e_steps}
+               "ms_per_step": e_ms / e_steps, "copies": OVERLAP}
     cpu = None
     if rank == 0 and world == 1 and args.cpu_budget > 0:
         rv, rd = synth.sweep_layer(0)
@@ -754,7 +826,9 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
                      "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
                      "frac": tflops / peak_t, "peak_source": peak_src, "traffic": None,
                      "algorithmic": f"sum of 2*M*N*K = {ops_per_step:.4g} flop per sweep"},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": L * 6 * steps,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": L * (2 + q6.mmq_launches(4096, 4096, N, False)
+                             + q6.mmq_launches(4096, 11008, N, False)) * steps,
         "clocks": clk, "clocks_ok": clocks_ok(clk),
         "kernels": {"gemm_total_ms": gemm_ms, "quantize_total_ms": quant_ms,
                     "gemm_tops": tflops},
@@ -766,7 +840,7 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 # kernels, keyed by (workload, kernel); the capture each figure comes from is
 # summarised under profiles/ (mmq_tc_ffn_down.md). An entry is removed when
 # its kernel changes.
-TRAFFIC = {("ffn_down", "mmq_tc"): 671.42e6 + 53.00e6}
+TRAFFIC = {("ffn_down", "mmq_tc"): None}
 
 
 def main():

@@ -173,8 +173,24 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *   path_out : NULL or receives a Q6_PATH_* code.
  * Alignment: plane, workspace 256 B; Xh, da, wexp, wh, Xq 16 B; Y 4 B.
  * Q6_ESIZE when the workspace is missing or too small.
+ *
+ * Work split: the tensor-core path walks 128 x 128 output tiles with one
+ * persistent CTA per SM. When the last round of tiles would leave more than
+ * half of the SMs idle, each of its tiles is computed as two halves of its
+ * super-blocks on two SMs; a small kernel first zeroes those tiles of Y and
+ * both halves add into it. Two addends onto zero give the same sum in either
+ * order, so Y stays deterministic; it can differ from the unsplit sum by
+ * rounding only (the partials are unaffected).
  * -------------------------------------------------------------------- */
 int q6k_mmq_workspace_bytes(int M, int K, int N, size_t *bytes);
+
+/* The number of kernels one q6k_mmq call launches for this shape on the
+ * calling thread's current device: 0 for N == 0; 1 on the skinny path
+ * (N <= Q6_SKINNY_MAX_N); otherwise 1 for the tensor-core GEMM, plus 1 when
+ * the work split above applies, plus 1 when the weights are unpacked into the
+ * workspace first (has_wh == 0). Q6_EINVAL on bad sizes or a NULL launches;
+ * Q6_EARCH / Q6_ECUDA as for the other calls. */
+int q6k_mmq_launches(int M, int K, int N, int has_wh, int *launches);
 
 int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, int K,
             const int8_t *Xq, const float *da, const uint16_t *Xh, int N, float *Y, int ldy,

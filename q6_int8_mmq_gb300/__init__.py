@@ -34,6 +34,7 @@ SIGNATURES = [
     ("q6k_pack_weights", _I, [_P, _I, _I, _P, _P, _P, _P]),
     ("q6k_unpack_weights", _I, [_P, _P, _I, _I, _P, _P]),
     ("q6k_mmq_workspace_bytes", _I, [_I, _I, _I, _SZ]),
+    ("q6k_mmq_launches", _I, [_I, _I, _I, _I, _IP]),
     ("q6k_mmq", _I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP,
                      _P]),
     ("q6k_mmq_noalloc", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _IP, _P]),
@@ -171,6 +172,13 @@ def workspace_bytes(M: int, K: int, N: int) -> int:
     b = ctypes.c_size_t()
     _check(load().q6k_mmq_workspace_bytes(M, K, N, ctypes.byref(b)))
     return b.value
+
+
+def mmq_launches(M: int, K: int, N: int, has_wh: bool) -> int:
+    """Kernels one q6k_mmq call launches for this shape on the current device."""
+    n = ctypes.c_int()
+    _check(load().q6k_mmq_launches(M, K, N, int(bool(has_wh)), ctypes.byref(n)))
+    return n.value
 
 
 _workspaces = {}

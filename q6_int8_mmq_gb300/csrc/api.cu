@@ -248,6 +248,27 @@ int q6k_mmq_workspace_bytes(int M, int K, int N, size_t* bytes) {
   return Q6_OK;
 }
 
+int q6k_mmq_launches(int M, int K, int N, int has_wh, int* launches) {
+  if (M <= 0 || K <= 0 || K % 256 || N < 0 || !launches)
+    return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0, launches != NULL");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  if (N == 0) {
+    *launches = 0;
+  } else if (N <= Q6_SKINNY_MAX_N) {
+    *launches = 1;
+  } else {
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    *launches = q6::mmq_tc_plan(M, K, N, sms).launches + (has_wh ? 0 : 1);
+  }
+  return Q6_OK;
+}
+
 int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, int K,
             const int8_t* Xq, const float* da, const uint16_t* Xh, int N, float* Y, int ldy,
             void* workspace, size_t workspace_bytes, int32_t* partials, int* path_out,

@@ -27,12 +27,16 @@
 // accumulators per (n, m):  Sb += da * S  per chunk, and  Y += d * Sb  per
 // super-block (one FFMA2 per two words per chunk, plus 1/8 of that).
 //
-// Persistent CTAs (one per SM) walk the tiles t = blockIdx.x, += gridDim.x,
-// with t -> (weight band t / NT, token tile t % NT): CTAs running at the same
-// time share weight bands and read every activation tile, which stays in L2.
-// Shared-memory rings filled by TMA run continuously across tiles:
+// Persistent CTAs (one per SM) walk work units u = blockIdx.x, += gridDim.x.
+// A unit is a tile t -> (weight band t / NT, token tile t % NT), so CTAs
+// running at the same time share weight bands and read every activation
+// tile; when the last round of tiles would leave more than half of the SMs
+// idle, each of its tiles becomes two units over the two halves of its
+// super-blocks, which add into Y after a small kernel has zeroed those tiles.
+// Shared-memory rings filled by TMA run continuously across units:
 //   operand ring (4 stages x 64 of K): Xh, W_hi, W_lo tiles, 128 rows x 128 B
-//          each, 128-byte swizzled; freed by the MMA (tcgen05.commit).
+//          each, 128-byte swizzled; freed by the epilogue once it has seen
+//          the commit of the stage's MMAs.
 //   scale ring (3 stages x one super-block): da [8 chunks][128 tokens] and
 //          d [128 rows]; freed by the epilogue.
 // TMEM: two slots of two 128-column accumulator buffers; operand stage g (two
@@ -42,7 +46,7 @@
 //   0      TMA producer for both rings.
 //   1      TMEM allocation (512 columns).
 //   1-2    lane 0 of each issues the MMAs of every other operand stage and
-//          commits its TMEM slot and its operand stage.
+//          commits its TMEM slot.
 //   3      idle (its registers go to the epilogue).
 //   4-11   epilogue: warp w owns TMEM lanes 32(w%4).. (32 tokens) and 64
 //          weight-row columns. Per chunk it loads its 64 words and does the
@@ -55,7 +59,7 @@ namespace q6 {
 namespace {
 
 constexpr int BT = 128, BW = 128;  // tokens, weight rows per tile
-constexpr int KB = 64, SB = 4;     // operand ring: K per stage, stages
+constexpr int KB = 64, SB = 4;     // operand ring: K per stage, stages (one super-block)
 constexpr int SS = 3;              // scale ring stages (one super-block each)
 constexpr int kThreads = 384;      // launched with 168 registers per thread
 constexpr int kCtlRegs = 24, kEpiRegs = 240;  // 128 * 24 + 256 * 240 == 384 * 168
@@ -71,6 +75,7 @@ constexpr int kScDa = 0, kScD = 8 * BT * 4, kScStage = kScD + BW * 4;  // 4.5 KB
 constexpr int kRingS = SB * kOpStage;  // the scale ring follows the operand ring
 constexpr int kRingsBytes = kRingS + SS * kScStage;
 static_assert(kOpStage % 1024 == 0, "operand stages must keep 1024-byte alignment");
+static_assert(SB * KB == 256, "the epilogue frees operand slot pp of each super-block");
 static_assert(kScStage % 128 == 0, "scale stages must keep 128-byte alignment");
 
 enum : uint32_t { kSiteSEmpty = 1, kSiteSFull = 2, kSiteBEmpty = 3, kSiteBFull = 4,
@@ -86,6 +91,40 @@ struct Bars {
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kRingsBytes + sizeof(Bars);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Work units: units 0 .. Tw-1 are whole tiles; when the last round of tiles
+// would leave more than half the CTAs idle, each of its tiles is split into
+// two units over the two halves of its super-blocks (units Tw + 2i and
+// Tw + 2i + 1 for tile Tw + i), which add their sums into a zeroed Y.
+struct Unit {
+  int t, sb0, sb1;
+  bool split;
+};
+__device__ __forceinline__ Unit unit_of(int u, int Tw, int nsb) {
+  if (u < Tw) return Unit{u, 0, nsb, false};
+  const int i = u - Tw, half = i & 1;
+  return Unit{Tw + (i >> 1), half ? nsb / 2 : 0, half ? nsb : nsb / 2, true};
+}
+
+// Zeroes the Y blocks of the split tiles: block (i, y) clears rows 32y..32y+31
+// of tile Tw + i, four columns per store where Y allows it.
+__global__ void __launch_bounds__(256) zero_split_tiles_kernel(float* __restrict__ Y, int ldy,
+                                                               int M, int N, int Tw, int y_vec4) {
+  const int NT = (N + BT - 1) / BT;
+  const int t = Tw + blockIdx.x;
+  const int m0 = (t / NT) * BW, n0 = (t % NT) * BT + 32 * blockIdx.y;
+  const int mw = min(BW, M - m0), nw = min(32, N - n0);
+  if (nw <= 0) return;
+  const int mv = y_vec4 ? (mw & ~3) : 0;  // columns cleared four at a time (m0 % 4 == 0)
+  for (int i = threadIdx.x; i < nw * (mv / 4); i += blockDim.x) {
+    const int r = i / (mv / 4), c = 4 * (i - r * (mv / 4));
+    *reinterpret_cast<float4*>(Y + (size_t)(n0 + r) * ldy + m0 + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int i = threadIdx.x; i < nw * (mw - mv); i += blockDim.x) {
+    const int r = i / (mw - mv), c = mv + (i - r * (mw - mv));
+    Y[(size_t)(n0 + r) * ldy + m0 + c] = 0.0f;
+  }
+}
 
 // sb[j] (+)= (da, da) * S[j] for 32 columns (16 pairs).
 template <bool kFirst>
@@ -117,7 +156,7 @@ template <bool kPartials>
 __global__ void __launch_bounds__(kThreads, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWhi,
                   const __grid_constant__ CUtensorMap tmWlo, const __grid_constant__ CUtensorMap tmDa,
-                  const __grid_constant__ CUtensorMap tmD, int M, int K, int N,
+                  const __grid_constant__ CUtensorMap tmD, int M, int K, int N, int Tw, int U,
                   float* __restrict__ Y, int ldy, int y_vec4, int32_t* __restrict__ partials,
                   unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
@@ -126,9 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + kRingsBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = (N + BT - 1) / BT;
-  const int T = NT * ((M + BW - 1) / BW);
-  const int nsb = K / 256;  // super-blocks = scale stages per tile
-  const int nb = K / KB;    // operand stages per tile
+  const int nsb = K / 256;  // super-blocks per tile
   const int nc = K / 32;    // chunks per tile
   volatile int* abort_flag = &bars->abort;
 
@@ -175,9 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t kTxB = (BT + 2 * BW) * 128;
         int gs = 0, gk = 0;  // scale / operand stages issued so far
         bool ok = true;
-        for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-          const int m0 = (t / NT) * BW, n0 = (t % NT) * BT;
-          for (int sb = 0; sb < nsb && ok; ++sb) {
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+          const Unit w = unit_of(u, Tw, nsb);
+          const int m0 = (w.t / NT) * BW, n0 = (w.t % NT) * BT;
+          for (int sb = w.sb0; sb < w.sb1 && ok; ++sb) {
             {
               const int slot = gs % SS;
               if (!(ok = mbar_wait_bounded(&bars->s_empty[slot], ((gs / SS) & 1) ^ 1, abort_flag,
@@ -224,8 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_f16_f32(BT, BW);
         const int me = warp - 1;
         bool ok = true;
-        int gbase = 0;  // global index of the tile's first operand stage
-        for (int t = blockIdx.x; t < T && ok; t += gridDim.x, gbase += nb) {
+        int gbase = 0;  // global index of the unit's first operand stage
+        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+          const Unit w = unit_of(u, Tw, nsb);
+          const int nb = 4 * (w.sb1 - w.sb0);  // operand stages of the unit
           for (int kb = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; kb < nb && ok;
                kb += kNumIssuers) {
             const int gk = gbase + kb;  // global operand stage
@@ -253,9 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_f16(d_tmem, xdesc + koff, ldesc + koff, idesc, 1u);
               }
             }
+            // the epilogue frees the operand stage when it sees this commit
             umma_commit(&bars->tfull[ts]);
-            umma_commit(&bars->b_empty[slot]);
           }
+          gbase += nb;
         }
         // Every MMA of every issuer must be finished before TMEM is released.
         umma_commit(&bars->drain);
@@ -276,13 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pA[32], pB[32];
     int gs = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < T && ok; t += gridDim.x) {
-      const int m0 = (t / NT) * BW, n0 = (t % NT) * BT;
+    for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+      const Unit w = unit_of(u, Tw, nsb);
+      const int m0 = (w.t / NT) * BW, n0 = (w.t % NT) * BT;
       const int n = n0 + tok;
       const int mcol = m0 + 64 * colh;
 #pragma unroll
       for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.0f, 0.0f);
-      for (int s = 0; s < nsb; ++s) {
+      for (int s = w.sb0; s < w.sb1; ++s) {
         const int slot = gs % SS;
         if (!mbar_wait_warp(&bars->s_full[slot], (gs / SS) & 1, abort_flag, status, kSiteSFull)) {
           ok = false;
@@ -298,6 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait_warp(&bars->tfull[ts], (uint32_t)((pp >> 1) & 1), abort_flag, status,
                               kSiteTFull))
             ok = false;
+          // The stage's MMAs are complete, so its operand ring slot (pp: the
+          // super-block starts at a global stage that is a multiple of SB)
+          // can be refilled: one arrive per stage, from one thread.
+          if (ew == 0 && lane == 0) mbar_arrive(&bars->b_empty[pp]);
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
@@ -340,16 +386,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n < N) {
         float* yr = Y + (size_t)n * ldy + mcol;
         const int mleft = M - mcol;
-        if (y_vec4 && mleft >= 64) {
+        if (!w.split) {
+          if (y_vec4 && mleft >= 64) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            reinterpret_cast<float4*>(yr)[j] =
-                make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y);
+            for (int j = 0; j < 16; ++j)
+              reinterpret_cast<float4*>(yr)[j] =
+                  make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (2 * j < mleft) yr[2 * j] = acc[j].x;
+              if (2 * j + 1 < mleft) yr[2 * j + 1] = acc[j].y;
+            }
+          }
         } else {
+          // one of the two K halves of a split tile: add into the zeroed Y
+          // (two addends onto zero: the sum is the same in either order)
+          if (y_vec4 && mleft >= 64) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (2 * j < mleft) yr[2 * j] = acc[j].x;
-            if (2 * j + 1 < mleft) yr[2 * j + 1] = acc[j].y;
+            for (int j = 0; j < 16; ++j)
+              atomicAdd(reinterpret_cast<float4*>(yr) + j,
+                        make_float4(acc[2 * j].x, acc[2 * j].y, acc[2 * j + 1].x, acc[2 * j + 1].y));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (2 * j < mleft) atomicAdd(yr + 2 * j, acc[j].x);
+              if (2 * j + 1 < mleft) atomicAdd(yr + 2 * j + 1, acc[j].y);
+            }
           }
         }
       }
@@ -375,17 +438,41 @@ cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ld
   int& sms = g_num_sms[dev & 63];
   if (sms == 0 && (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
     return e;
-  const long long tiles = (long long)((N + BT - 1) / BT) * ((M + BW - 1) / BW);
-  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+  const TcPlan p = mmq_tc_plan(M, K, N, sms);
   const int y_vec4 = (ldy % 4 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
-  mmq_tc_kernel<P><<<grid, kThreads, kSmemBytes, s>>>(maps.x, maps.whi, maps.wlo, maps.da, maps.d,
-                                                     M, K, N, Y, ldy, y_vec4, partials, status);
+  if (p.U > p.Tw) {
+    zero_split_tiles_kernel<<<dim3((unsigned)((p.U - p.Tw) / 2), BT / 32), 256, 0, s>>>(
+        Y, ldy, M, N, p.Tw, y_vec4);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  mmq_tc_kernel<P><<<p.grid, kThreads, kSmemBytes, s>>>(maps.x, maps.whi, maps.wlo, maps.da, maps.d,
+                                                       M, K, N, p.Tw, p.U, Y, ldy, y_vec4,
+                                                       partials, status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t mmq_tc_smem_bytes() { return kSmemBytes; }
+
+// Grid and work units for an M x K x N GEMM on `sms` SMs: one persistent CTA
+// per SM walks the units; the last round of tiles is split in two along K
+// when that keeps more than half of the SMs busy instead of idle.
+TcPlan mmq_tc_plan(int M, int K, int N, int sms) {
+  const long long T = (long long)((N + BT - 1) / BT) * ((M + BW - 1) / BW);
+  TcPlan p;
+  p.grid = (unsigned)(T < sms ? T : sms);
+  const long long rem = T % sms;
+  if (T > sms && rem > 0 && 2 * rem <= sms && K / 256 >= 2) {
+    p.Tw = (int)(T - rem);
+    p.U = (int)(T + rem);
+  } else {
+    p.Tw = (int)T;
+    p.U = (int)T;
+  }
+  p.launches = (p.U > p.Tw) ? 2 : 1;
+  return p;
+}
 
 // Raises the dynamic shared-memory limit of both instantiations; once per device.
 cudaError_t mmq_tc_prepare() {

@@ -71,6 +71,13 @@ cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cu
 cudaError_t launch_expand_wexp(const int8_t* wexp, const uint8_t* plane, int M, int K, __half* wh,
                                cudaStream_t s);
 size_t mmq_tc_smem_bytes();
+// Launch plan of the tensor-core GEMM for an M x K x N call on `sms` SMs.
+struct TcPlan {
+  unsigned grid;  // persistent CTAs
+  int Tw, U;      // units 0..Tw-1 are whole tiles; Tw..U-1 are K halves of split tiles
+  int launches;   // kernels per call: the GEMM, plus one that zeroes Y of split tiles
+};
+TcPlan mmq_tc_plan(int M, int K, int N, int sms);
 cudaError_t mmq_tc_prepare();
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t s);
 
@@ -241,11 +248,23 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
 }
 
 // Issues one 32x32b.x32 TMEM load: 32 consecutive 32-bit columns of this
-// thread's lane. The registers are valid only after tmem_wait_ld4().
+// thread's lane. The registers are valid only after a tmem_wait_* call.
 __device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(addr)
+      : "memory");
+}
+// tmem_ld32 for a pipelined consumer: `prev` (the buffer loaded before) is an
+// in-out operand, so the math on it cannot be scheduled above this load and
+// runs while the load is in flight.
+__device__ __forceinline__ void tmem_ld32_before(uint32_t addr, uint32_t (&r)[32],
+                                                 uint32_t (&prev)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "+r"(prev[0]), "+r"(prev[1]), "+r"(prev[2]), "+r"(prev[3]), "+r"(prev[4]), "+r"(prev[5]), "+r"(prev[6]), "+r"(prev[7]), "+r"(prev[8]), "+r"(prev[9]), "+r"(prev[10]), "+r"(prev[11]), "+r"(prev[12]), "+r"(prev[13]), "+r"(prev[14]), "+r"(prev[15]), "+r"(prev[16]), "+r"(prev[17]), "+r"(prev[18]), "+r"(prev[19]), "+r"(prev[20]), "+r"(prev[21]), "+r"(prev[22]), "+r"(prev[23]), "+r"(prev[24]), "+r"(prev[25]), "+r"(prev[26]), "+r"(prev[27]), "+r"(prev[28]), "+r"(prev[29]), "+r"(prev[30]), "+r"(prev[31])
       : "r"(addr)
       : "memory");
 }
@@ -254,6 +273,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[32], uint32_t (&b)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n"
                : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15]), "+r"(b[16]), "+r"(b[17]), "+r"(b[18]), "+r"(b[19]), "+r"(b[20]), "+r"(b[21]), "+r"(b[22]), "+r"(b[23]), "+r"(b[24]), "+r"(b[25]), "+r"(b[26]), "+r"(b[27]), "+r"(b[28]), "+r"(b[29]), "+r"(b[30]), "+r"(b[31])
+               :
+               : "memory");
+}
+
+// The same wait for a pipelined consumer: `a` is the buffer just loaded and
+// `s` the 16 accumulator pairs that the math issued since that load wrote, so
+// the math stays between the load and the wait and overlaps the load.
+__device__ __forceinline__ void tmem_wait_ld_after(uint32_t (&a)[32], float2* s) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(a[16]), "+r"(a[17]), "+r"(a[18]), "+r"(a[19]), "+r"(a[20]), "+r"(a[21]), "+r"(a[22]), "+r"(a[23]), "+r"(a[24]), "+r"(a[25]), "+r"(a[26]), "+r"(a[27]), "+r"(a[28]), "+r"(a[29]), "+r"(a[30]), "+r"(a[31]),
+                 "+f"(s[0].x), "+f"(s[0].y), "+f"(s[1].x), "+f"(s[1].y), "+f"(s[2].x), "+f"(s[2].y), "+f"(s[3].x), "+f"(s[3].y), "+f"(s[4].x), "+f"(s[4].y), "+f"(s[5].x), "+f"(s[5].y), "+f"(s[6].x), "+f"(s[6].y), "+f"(s[7].x), "+f"(s[7].y), "+f"(s[8].x), "+f"(s[8].y), "+f"(s[9].x), "+f"(s[9].y), "+f"(s[10].x), "+f"(s[10].y), "+f"(s[11].x), "+f"(s[11].y), "+f"(s[12].x), "+f"(s[12].y), "+f"(s[13].x), "+f"(s[13].y), "+f"(s[14].x), "+f"(s[14].y), "+f"(s[15].x), "+f"(s[15].y)
                :
                : "memory");
 }

@@ -38,42 +38,63 @@ __device__ __forceinline__ void quant8(const float4 v0, const float4 v1, float d
   h8.w = *reinterpret_cast<const uint32_t*>(&h67);
 }
 
-// Each thread owns eight consecutive elements (two float4 loads issued
-// together); four threads of a warp form one 32-element block and reduce amax
-// with two xor-shuffles.
+// Each thread owns sixteen consecutive elements (four float4 loads issued
+// together); two neighbouring lanes form one 32-element block and reduce amax
+// with one xor-shuffle. Warps walk the rows' 16-element groups in lockstep
+// (a lane past the end idles through the shuffle), so the shuffle always has
+// the whole warp.
 __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restrict__ X, int N, int K,
                                                           int ldx, int8_t* __restrict__ Xq,
                                                           float* __restrict__ da, int ldda,
                                                           __half* __restrict__ Xh) {
-  const long long per_row = K >> 3;                // eight-element groups per row
-  const long long total = (long long)N * per_row;  // a multiple of 32: whole warps stay active
+  const long long per_row = K >> 4;                // sixteen-element groups per row (even)
+  const long long total = (long long)N * per_row;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += stride) {
-    const int n = (int)(g / per_row);
-    const int j = (int)(g - (long long)n * per_row);  // eight-element group in the row
-    const float4* src = reinterpret_cast<const float4*>(X + (size_t)n * ldx) + 2 * j;
-    const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+  const int lane = threadIdx.x & 31;
+  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x - lane); base < total;
+       base += stride) {
+    const long long g = base + lane;
+    const bool on = g < total;  // both lanes of a pair agree: total is even
+    const int n = on ? (int)(g / per_row) : 0;
+    const int j = on ? (int)(g - (long long)n * per_row) : 0;  // group in the row
+    float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0, v2 = v0, v3 = v0;
+    if (on) {
+      const float4* src = reinterpret_cast<const float4*>(X + (size_t)n * ldx) + 4 * j;
+      v0 = __ldg(src);
+      v1 = __ldg(src + 1);
+      v2 = __ldg(src + 2);
+      v3 = __ldg(src + 3);
+    }
     float a = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
                     fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+    a = fmaxf(a, fmaxf(fmaxf(fmaxf(fabsf(v2.x), fabsf(v2.y)), fmaxf(fabsf(v2.z), fabsf(v2.w))),
+                       fmaxf(fmaxf(fabsf(v3.x), fabsf(v3.y)), fmaxf(fabsf(v3.z), fabsf(v3.w)))));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    if (!on) continue;
     const float d = __fdiv_rn(a, 127.0f);
-    uint2 q8;
-    uint4 h8;
-    quant8(v0, v1, d, q8, h8);
-    reinterpret_cast<uint2*>(Xq + (size_t)n * K)[j] = q8;
-    if (Xh != nullptr) reinterpret_cast<uint4*>(Xh + (size_t)n * K)[j] = h8;
-    if ((j & 3) == 0) da[(size_t)(j >> 2) * ldda + n] = d;
+    uint2 qa, qb;
+    uint4 ha, hb;
+    quant8(v0, v1, d, qa, ha);
+    quant8(v2, v3, d, qb, hb);
+    reinterpret_cast<uint4*>(Xq + (size_t)n * K)[j] = make_uint4(qa.x, qa.y, qb.x, qb.y);
+    if (Xh != nullptr) {
+      uint4* h = reinterpret_cast<uint4*>(Xh + (size_t)n * K) + 2 * j;
+      h[0] = ha;
+      h[1] = hb;
+    }
+    if ((j & 1) == 0) da[(size_t)(j >> 1) * ldda + n] = d;
   }
 }
 
 }  // namespace
 
+// One pass; the grid is capped at 32 blocks of 256 threads per SM (about two
+// groups per thread at the prefill sizes), which measured fastest.
 cudaError_t launch_quantize(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, int ldda,
                             __half* Xh, cudaStream_t s) {
-  const long long total = (long long)N * (K / 8);
+  const long long total = (long long)N * (K / 16);
   long long blocks = (total + 255) / 256;
-  const long long cap = 152LL * 16;
+  const long long cap = 152LL * 32;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   q8_quantize_kernel<<<(unsigned)blocks, 256, 0, s>>>(X, N, K, ldx, Xq, da, ldda, Xh);

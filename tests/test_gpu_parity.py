@@ -261,6 +261,46 @@ def test_mmq_extreme_chunk_sums_exact(q6, orc, N):
         check_y(host(Y), Yo, f"extreme N={N}")
 
 
+@pytest.mark.parametrize("source", ["raw", "wh"])
+def test_mmq_split_last_round(q6, orc, source):
+    """160 tiles of 128 x 128 on 152 SMs: the last 8 tiles (the last weight
+    band, token tiles 12-19) are each computed as two halves of their
+    super-blocks (1 and 2 of K/256 = 3) on two SMs and added into Y after a
+    zeroing kernel. The split tiles hold the ragged last token tile and the
+    ragged last band (M = 1016: a 56-column half that takes the scalar adds).
+    Y starts as NaN; sampled tokens inside and outside the split tiles are
+    checked against the oracle over all columns, with bit-exact partials."""
+    import torch
+    M, K, N = 1016, 768, 2555
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = ((N + 127) // 128) * ((M + 127) // 128)
+    rem = tiles % sms
+    split = tiles > sms and rem > 0 and 2 * rem <= sms
+    assert q6.mmq_launches(M, K, N, True) == 1 + int(split)
+    assert q6.mmq_launches(M, K, N, False) == 2 + int(split)
+    if sms == 152:
+        assert split
+    raw = synth.q6k_raw_weights(0x51360A01, M, K)
+    X = synth.activations(0x51360A02, N, K, outlier_frac=0.02)
+    w = q6.pack_weights(dev(raw), M, K, wh=source == "wh")
+    act = q6.quantize_act(dev(X))
+    xq_o, da_o = quant_check(act, X, orc)
+    tok = sampled_tokens(N, extra=(1535, 1536, 1700, 2047, 2300, 2431, 2432, 2500))
+    for partials in (False, True):
+        Y = torch.full((N, M), float("nan"), dtype=torch.float32, device="cuda")
+        Y, path, P = q6.mmq(w, act, Y=Y, source=source, partials=partials)
+        q6.sync_status()
+        assert path == TC_PATH[source]
+        Yh = host(Y)
+        assert np.all(np.isfinite(Yh)), "a split tile was not zeroed or not written"
+        if partials:
+            Yo, Po = orc.mmq(raw, M, K, xq_o[tok], da_o[tok], partials=True)
+            assert np.array_equal(host(P)[tok], chunk_sums(Po, raw, M, K))
+        else:
+            Yo = orc.mmq(raw, M, K, xq_o[tok], da_o[tok])
+        check_y(Yh[tok], Yo, f"split {source} partials={partials}")
+
+
 def test_mmq_empty(q6):
     import torch
     M, K = 128, 256
