@@ -38,7 +38,37 @@ __device__ __forceinline__ void quant8(const float4 v0, const float4 v1, float d
   h8.w = *reinterpret_cast<const uint32_t*>(&h67);
 }
 
-// Each thread owns sixteen consecutive elements (four float4 loads issued
+// Small inputs (a few tokens): each thread owns eight consecutive elements
+// (two float4 loads issued together); four threads form one 32-element block
+// and reduce amax with two xor-shuffles. K % 256 == 0 makes the group count a
+// multiple of 32, so whole warps stay active.
+__global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restrict__ X, int N, int K,
+                                                           int ldx, int8_t* __restrict__ Xq,
+                                                           float* __restrict__ da, int ldda,
+                                                           __half* __restrict__ Xh) {
+  const long long per_row = K >> 3;  // eight-element groups per row
+  const long long total = (long long)N * per_row;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += stride) {
+    const int n = (int)(g / per_row);
+    const int j = (int)(g - (long long)n * per_row);  // eight-element group in the row
+    const float4* src = reinterpret_cast<const float4*>(X + (size_t)n * ldx) + 2 * j;
+    const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    float a = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                    fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    const float d = __fdiv_rn(a, 127.0f);
+    uint2 q8;
+    uint4 h8;
+    quant8(v0, v1, d, q8, h8);
+    reinterpret_cast<uint2*>(Xq + (size_t)n * K)[j] = q8;
+    if (Xh != nullptr) reinterpret_cast<uint4*>(Xh + (size_t)n * K)[j] = h8;
+    if ((j & 3) == 0) da[(size_t)(j >> 2) * ldda + n] = d;
+  }
+}
+
+// Large inputs: each thread owns sixteen consecutive elements (four float4 loads issued
 // together); two neighbouring lanes form one 32-element block and reduce amax
 // with one xor-shuffle. Warps walk the rows' 16-element groups in lockstep
 // (a lane past the end idles through the shuffle), so the shuffle always has
@@ -88,15 +118,22 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
 
 }  // namespace
 
-// One pass; the grid is capped at 32 blocks of 256 threads per SM (about two
-// groups per thread at the prefill sizes), which measured fastest.
+// One pass. Prefill-sized inputs take the sixteen-element form with the grid
+// capped at 32 blocks of 256 threads per SM (about two groups per thread),
+// which measured fastest; a few tokens take the eight-element form, whose
+// shorter per-thread chain and twice the threads finish sooner.
 cudaError_t launch_quantize(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, int ldda,
                             __half* Xh, cudaStream_t s) {
-  const long long total = (long long)N * (K / 16);
-  long long blocks = (total + 255) / 256;
+  const long long elems = (long long)N * K;
+  if (elems < (1LL << 20)) {
+    const long long blocks = (elems / 8 + 255) / 256;
+    q8_quantize8_kernel<<<(unsigned)(blocks < 1 ? 1 : blocks), 256, 0, s>>>(X, N, K, ldx, Xq, da,
+                                                                            ldda, Xh);
+    return cudaGetLastError();
+  }
+  long long blocks = (elems / 16 + 255) / 256;
   const long long cap = 152LL * 32;
   if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
   q8_quantize_kernel<<<(unsigned)blocks, 256, 0, s>>>(X, N, K, ldx, Xq, da, ldda, Xh);
   return cudaGetLastError();
 }

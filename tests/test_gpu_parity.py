@@ -107,7 +107,9 @@ def test_bounded_wait_times_out_and_context_survives(q6):
 # -------------------------------------------------------------- quantiser ---
 
 @pytest.mark.parametrize("N,K,frac", [(1, 256, 0.0), (8, 512, 0.0), (513, 4096, 0.0),
-                                      (77, 11008, 0.01)])
+                                      (77, 11008, 0.01),
+                                      # 16-element form with a partly idle last warp
+                                      (1001, 1280, 0.02)])
 def test_quantize_bitexact(q6, orc, N, K, frac):
     X = synth.activations(100 + N, N, K, outlier_frac=frac)
     X[0, 32:64] = 0.0                                   # all-zero block
