@@ -108,6 +108,33 @@ class Oracle:
         return (Y, P) if partials else Y
 
 
+    def mmq_all(self, raw: np.ndarray, M: int, K: int, xq: np.ndarray, da: np.ndarray,
+                threads: int | None = None) -> np.ndarray:
+        """Y f64 [N,M] for large shapes: the same orc_mmq run on disjoint ranges
+        of weight rows from several threads (ctypes releases the GIL), so every
+        output element comes from the unchanged single-threaded loop."""
+        import concurrent.futures as cf
+        raw = np.ascontiguousarray(raw, dtype=np.uint8).reshape(M, -1)
+        xq = np.ascontiguousarray(xq, dtype=np.int8)
+        da = np.ascontiguousarray(da, dtype=np.float32)
+        N = xq.shape[0]
+        T = max(1, min(threads or os.cpu_count() or 1, M))
+        bounds = [M * i // T for i in range(T + 1)]
+        parts = [None] * T
+
+        def run(i):
+            m0, m1 = bounds[i], bounds[i + 1]
+            sub = np.ascontiguousarray(raw[m0:m1])
+            y = np.empty((N, m1 - m0), dtype=np.float64)
+            self.lib.orc_mmq(self._ptr(sub), m1 - m0, K, self._ptr(xq), self._ptr(da), N,
+                             self._ptr(y), None)
+            parts[i] = y
+
+        with cf.ThreadPoolExecutor(max_workers=T) as ex:
+            list(ex.map(run, range(T)))
+        return np.concatenate(parts, axis=1)
+
+
 _default = None
 
 

@@ -1,4 +1,5 @@
 """The oracle checked against what the pages and mathematics fix (CPU only)."""
+import numpy as np
 import pytest
 
 import oracle
@@ -34,3 +35,15 @@ MUTANTS = {
 def test_planted_mistake_is_caught(k):
     bad = oracle_pins.failing_pins(oracle.Oracle(mutant=k))
     assert bad, f"no pin catches planted mistake {k}: {MUTANTS[k]}"
+
+
+def test_row_parallel_driver_matches(orc):
+    """mmq_all (the large-shape driver over disjoint row ranges) gives exactly
+    the single-threaded result, with ragged row splits."""
+    from q6_int8_mmq_gb300 import synth
+    M, K, N = 77, 768, 19
+    raw = synth.q6k_raw_weights(0x51360B01, M, K)
+    xq, da = orc.quantize(synth.activations(0x51360B02, N, K, outlier_frac=0.05))
+    Y = orc.mmq(raw, M, K, xq, da)
+    for t in (1, 3, 8, 77):
+        assert np.array_equal(orc.mmq_all(raw, M, K, xq, da, threads=t), Y)
