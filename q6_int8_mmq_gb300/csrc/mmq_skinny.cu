@@ -17,12 +17,13 @@
 // Streaming: warps stride over the rows, with the grid sized to one resident
 // wave (4 warps per CTA, 64 registers, 8 CTAs per SM) so every warp starts at
 // once and reads its row's qlh run in coalesced 768-byte steps; the loads of
-// the next step are in flight while the current step is computed. The kernel
-// is instantiated per token bucket (N = 1, <= 4, <= 16) so small N does not
-// pay registers for 16 accumulators. Measured on GB300 and not kept: loading
-// two to four steps ahead (more registers, fewer resident warps), a
-// cp.async.bulk ring of whole rows and a per-warp cp.async ring in shared
-// memory.
+// the next step are in flight while the current step is computed. One token
+// (and the debug partials) take one row per warp; N <= 4 and N <= 16 take two
+// rows per warp, so each activation load serves both rows. Measured on GB300
+// and not kept: loading two to four steps ahead (more registers, fewer
+// resident warps), a cp.async.bulk ring of whole rows, a per-warp cp.async
+// ring in shared memory, L2 prefetches (per step, or of whole rows with
+// cp.async.bulk.prefetch), and four rows per warp.
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -35,6 +36,22 @@ constexpr int kMinBlocks = 8;  // resident CTAs per SM (64 registers per thread)
 // of its byte, and adding 128 more is a flip of bit 7.
 __device__ __forceinline__ uint32_t center4(uint32_t code) {
   return (code + 0x60606060u) ^ 0x80808080u;
+}
+
+// Centered codes of a lane's two sub-blocks from its 16 ql bytes L and 16 qh
+// bytes H: va (low nibbles, qh field fsh) and vb (high nibbles, field fsh + 4),
+// four codes per word.
+__device__ __forceinline__ void unpack_pair(const uint4 L, const uint4 H, int fsh, uint32_t (&va)[4],
+                                            uint32_t (&vb)[4]) {
+  const uint32_t Lw[4] = {L.x, L.y, L.z, L.w};
+  const uint32_t Hw[4] = {H.x, H.y, H.z, H.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t ca = (Lw[w] & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
+    const uint32_t cb = ((Lw[w] >> 4) & 0x0F0F0F0Fu) | (((Hw[w] >> (fsh + 4)) & 0x03030303u) << 4);
+    va[w] = center4(ca);
+    vb[w] = center4(cb);
+  }
 }
 
 // One lane's share of one step: sub-blocks sa = 8*half + s4 and sa + 4 of
@@ -50,16 +67,8 @@ __device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a,
   const int s4 = lane & 3;
   const int fsh = 2 * (s4 >> 1);  // field of the low-nibble sub-block
   const int sa = 8 * half + s4;   // sub-block (0..15) of the low nibbles; sb_b = sa + 4
-  const uint32_t Lw[4] = {L.x, L.y, L.z, L.w};
-  const uint32_t Hw[4] = {H.x, H.y, H.z, H.w};
   uint32_t va[4], vb[4];
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t ca = (Lw[w] & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
-    const uint32_t cb = ((Lw[w] >> 4) & 0x0F0F0F0Fu) | (((Hw[w] >> (fsh + 4)) & 0x03030303u) << 4);
-    va[w] = center4(ca);
-    vb[w] = center4(cb);
-  }
+  unpack_pair(L, H, fsh, va, vb);
   const float d = __half2float(__ushort_as_half(dbits));
   const float dsc_a = d * (float)sc_a;
   const float dsc_b = d * (float)sc_b;
@@ -189,6 +198,138 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
         ldda, N, Y, ldy, partials);
 }
 
+
+// Several tokens: kRows weight rows per warp with the same lane mapping, so
+// each activation word and scale a lane loads serves kRows rows. With 16
+// tokens the activation loads through L1 bound the one-row form (ncu: L1 84%
+// busy); two rows per warp cut that traffic in half.
+template <int kMaxN, int kRows>
+__device__ __forceinline__ void step_rows(const uint4 (&L)[kRows], const uint4 (&H)[kRows],
+                                          const int (&sca)[kRows], const int (&scb)[kRows],
+                                          const uint16_t (&dbits)[kRows], int sb, int K,
+                                          const int8_t* __restrict__ Xq,
+                                          const float* __restrict__ da, int ldda, int N,
+                                          float (&acc)[kRows][kMaxN]) {
+  const int lane = threadIdx.x & 31;
+  const int half = (lane >> 2) & 1;
+  const int s4 = lane & 3;
+  const int sa = 8 * half + s4;
+  uint32_t va[kRows][4], vb[kRows][4];
+  float dsa[kRows], dsb[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    unpack_pair(L[r], H[r], 2 * (s4 >> 1), va[r], vb[r]);
+    const float d = __half2float(__ushort_as_half(dbits[r]));
+    dsa[r] = d * (float)sca[r];
+    dsb[r] = d * (float)scb[r];
+  }
+  const int ka = 256 * sb + 16 * sa;
+  const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
+#pragma unroll
+  for (int n = 0; n < kMaxN; ++n) {
+    if (n < N) {
+      const int8_t* xr = Xq + (size_t)n * K;
+      const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
+      const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
+      const float daa = __ldg(da + (size_t)ca_blk * ldda + n);
+      const float dab = __ldg(da + (size_t)cb_blk * ldda + n);
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) {
+        int pa = __dp4a((int)va[r][0], (int)xa.x, 0);
+        pa = __dp4a((int)va[r][1], (int)xa.y, pa);
+        pa = __dp4a((int)va[r][2], (int)xa.z, pa);
+        pa = __dp4a((int)va[r][3], (int)xa.w, pa);
+        int pb = __dp4a((int)vb[r][0], (int)xb.x, 0);
+        pb = __dp4a((int)vb[r][1], (int)xb.y, pb);
+        pb = __dp4a((int)vb[r][2], (int)xb.z, pb);
+        pb = __dp4a((int)vb[r][3], (int)xb.w, pb);
+        acc[r][n] = fmaf(dsa[r] * daa, (float)pa, acc[r][n]);
+        acc[r][n] = fmaf(dsb[r] * dab, (float)pb, acc[r][n]);
+      }
+    }
+  }
+}
+
+// Rows m0 .. m0 + kRows - 1 (those below M) against the N <= kMaxN
+// activation rows, with the same one-step software pipeline as row_dot.
+template <int kMaxN, int kRows>
+__device__ __forceinline__ void rows_dot(const uint8_t* __restrict__ plane, const PlaneGeom& g,
+                                         int m0, int M, int K, const int8_t* __restrict__ Xq,
+                                         const float* __restrict__ da, int ldda, int N,
+                                         float* __restrict__ Y, int ldy) {
+  const int lane = threadIdx.x & 31;
+  const int nsb = K / 256;
+  const int sbi = lane >> 3;
+  const int half = (lane >> 2) & 1;
+  const int s4 = lane & 3;
+  const int sa = 8 * half + s4;
+  const uint8_t* qrow[kRows];
+  const int8_t* srow[kRows];
+  const uint16_t* drow[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int m = min(m0 + r, M - 1);  // a row past the end re-reads row M-1 and is not stored
+    qrow[r] = plane + g.qlh_off + (size_t)m * g.qlh_row;
+    srow[r] = reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)m * (K / 16);
+    drow[r] = reinterpret_cast<const uint16_t*>(plane + g.d_off + (size_t)m * g.d_row);
+  }
+  float acc[kRows][kMaxN];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r)
+#pragma unroll
+    for (int n = 0; n < kMaxN; ++n) acc[r][n] = 0.0f;
+  uint4 L[kRows], H[kRows];
+  int sca[kRows], scb[kRows];
+  uint16_t db[kRows];
+  auto load = [&](int sb, uint4(&l)[kRows], uint4(&h)[kRows], int(&a)[kRows], int(&b)[kRows],
+                  uint16_t(&dd)[kRows]) {
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      l[r] = make_uint4(0, 0, 0, 0);
+      h[r] = l[r];
+      a[r] = b[r] = 0;
+      dd[r] = 0;
+      if (sb < nsb) {
+        const uint8_t* hb = qrow[r] + (size_t)(2 * sb + half) * 96;
+        l[r] = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
+        h[r] = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
+        a[r] = __ldg(srow[r] + 16 * sb + sa);
+        b[r] = __ldg(srow[r] + 16 * sb + sa + 4);
+        dd[r] = __ldg(drow[r] + sb);
+      }
+    }
+  };
+  load(sbi, L, H, sca, scb, db);
+  for (int g0 = 0; g0 < nsb; g0 += 4) {
+    uint4 L2[kRows], H2[kRows];
+    int sca2[kRows], scb2[kRows];
+    uint16_t db2[kRows];
+    load(g0 + 4 + sbi, L2, H2, sca2, scb2, db2);  // next step, in flight during this one
+    const int sb = g0 + sbi;
+    if (sb < nsb) step_rows<kMaxN, kRows>(L, H, sca, scb, db, sb, K, Xq, da, ldda, N, acc);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+      L[r] = L2[r];
+      H[r] = H2[r];
+      sca[r] = sca2[r];
+      scb[r] = scb2[r];
+      db[r] = db2[r];
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kRows; ++r)
+    if (m0 + r < M) row_store<kMaxN>(acc[r], m0 + r, N, Y, ldy);
+}
+
+// kRows rows per warp, warps striding over the row groups.
+template <int kMaxN, int kRows, int kMinB>
+__global__ void __launch_bounds__(kWarps * 32, kMinB) mmq_skinny_rows_kernel(
+    const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
+    const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy) {
+  const int warps = (int)gridDim.x * kWarps;
+  for (int m = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRows; m < M; m += warps * kRows)
+    rows_dot<kMaxN, kRows>(plane, g, m, M, K, Xq, da, ldda, N, Y, ldy);
+}
 }  // namespace
 
 cudaError_t mmq_skinny_prepare() { return cudaSuccess; }
@@ -212,6 +353,27 @@ cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K
   return cudaGetLastError();
 }
 
+// Two rows per warp for N <= 4 and N <= 16 (measured: 16 tokens 84 -> 58 us,
+// 4 tokens 20.8 -> 19.1 us on the ffn_down weights); the register budget per
+// thread sets the resident CTAs (5 and 3 per SM).
+template <int kMaxN, int kRows, int kMinB>
+cudaError_t launch_rows(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
+                        const float* da, int ldda, int N, float* Y, int ldy, cudaStream_t s) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+           &per_sm, mmq_skinny_rows_kernel<kMaxN, kRows, kMinB>, kWarps * 32, 0)))
+    return e;
+  const long long need = (M + kWarps * kRows - 1) / (kWarps * kRows);
+  const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
+  const unsigned blocks = (unsigned)(need < cap ? need : cap);
+  mmq_skinny_rows_kernel<kMaxN, kRows, kMinB>
+      <<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y, ldy);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
                               unsigned int* status, cudaStream_t s) {
@@ -219,8 +381,8 @@ cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* 
   const PlaneGeom g = plane_geom(M, K);
   if (partials) return launch_bucket<true, Q6_SKINNY_MAX_N>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s);
   if (N == 1) return launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
-  if (N <= 4) return launch_bucket<false, 4>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
-  return launch_bucket<false, Q6_SKINNY_MAX_N>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+  if (N <= 4) return launch_rows<4, 2, 5>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, s);
+  return launch_rows<Q6_SKINNY_MAX_N, 2, 3>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, s);
 }
 
 }  // namespace q6

@@ -189,6 +189,7 @@ def test_pack_bitexact(q6, orc, M, K):
 SMALL = [
     # (M, K, N) spanning tiles and ragged tails of both kernels
     (256, 512, 1), (256, 512, 4), (256, 512, 8), (200, 768, 16),      # skinny kernel
+    (257, 512, 3), (129, 768, 16),                                    # odd M: two-row warps
     (128, 256, 17), (256, 512, 128), (200, 512, 129), (384, 768, 300),  # tensor-core kernel
     (130, 1024, 255), (64, 256, 40),
 ]
@@ -403,6 +404,9 @@ def test_skinny_full(q6, orc, weight, N):
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
     assert np.array_equal(host(P), chunk_sums(Po, raw, M, K))
     check_y(host(Y), Yo, f"skinny {weight} N={N}")
+    Y2, _, _ = q6.mmq(w, act, source="raw")            # the fast kernel of this N
+    q6.sync_status()
+    check_y(host(Y2), Yo, f"skinny {weight} N={N} fast")
 
 
 @pytest.mark.parametrize("layer", [0, 31])
