@@ -18,8 +18,9 @@
 // wave (4 warps per CTA, 64 registers, 8 CTAs per SM) so every warp starts at
 // once and reads its row's qlh run in coalesced 768-byte steps; the loads of
 // the next step are in flight while the current step is computed. One token
-// (and the debug partials) take one row per warp; N <= 4 and N <= 16 take two
-// rows per warp, so each activation load serves both rows. Measured on GB300
+// (and the debug partials) take one row per warp; N <= 4 takes two rows per
+// warp, so each activation load serves both rows; 5..16 tokens go to the int8
+// tensor-core form in mmq_skinny_mma.cu. Measured on GB300
 // and not kept: loading two to four steps ahead (more registers, fewer
 // resident warps), a cp.async.bulk ring of whole rows, a per-warp cp.async
 // ring in shared memory, L2 prefetches (per step, or of whole rows with
@@ -353,9 +354,8 @@ cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K
   return cudaGetLastError();
 }
 
-// Two rows per warp for N <= 4 and N <= 16 (measured: 16 tokens 84 -> 58 us,
-// 4 tokens 20.8 -> 19.1 us on the ffn_down weights); the register budget per
-// thread sets the resident CTAs (5 and 3 per SM).
+// Two rows per warp for N <= 4 (measured on the ffn_down weights: 4 tokens
+// 20.8 -> 18.7 us); the register budget per thread sets the resident CTAs.
 template <int kMaxN, int kRows, int kMinB>
 cudaError_t launch_rows(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
                         const float* da, int ldda, int N, float* Y, int ldy, cudaStream_t s) {
@@ -382,7 +382,9 @@ cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* 
   if (partials) return launch_bucket<true, Q6_SKINNY_MAX_N>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s);
   if (N == 1) return launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
   if (N <= 4) return launch_rows<4, 2, 5>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, s);
-  return launch_rows<Q6_SKINNY_MAX_N, 2, 3>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, s);
+  // 5..16 tokens: the int8 tensor-core form (mmq_skinny_mma.cu) shares each
+  // activation word among 16 rows (ffn_down weights, N = 16: 58 -> 32 us)
+  return launch_mmq_skinny_mma(plane, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
 }
 
 }  // namespace q6
