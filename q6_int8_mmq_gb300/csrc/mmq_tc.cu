@@ -280,15 +280,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // descriptors of the stage's three tiles; a K step of 16 elements
             // (32 bytes) adds 2 to the start-address field
             const uint8_t* bt = smem + slot * kOpStage;
-            const uint64_t xdesc = sw128_kmajor_desc(smem_u32(bt + kOpX));
-            const uint64_t hdesc = sw128_kmajor_desc(smem_u32(bt + kOpWhi));
-            const uint64_t ldesc = sw128_kmajor_desc(smem_u32(bt + kOpWlo));
+            const uint32_t xdesc = sw128_desc_lo(smem_u32(bt + kOpX));
+            const uint32_t hdesc = sw128_desc_lo(smem_u32(bt + kOpWhi));
+            const uint32_t ldesc = sw128_desc_lo(smem_u32(bt + kOpWlo));
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
               const uint32_t d_tmem = tmem + (uint32_t)((2 * ts + q) * kBufCols);
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
-                const uint64_t koff = (uint64_t)((2 * q + h) * 2);  // sub-block within the stage
+                const uint32_t koff = (uint32_t)((2 * q + h) * 2);  // sub-block within the stage
                 umma_f16(d_tmem, xdesc + koff, hdesc + koff, idesc, (uint32_t)h);
                 umma_f16(d_tmem, xdesc + koff, ldesc + koff, idesc, 1u);
               }

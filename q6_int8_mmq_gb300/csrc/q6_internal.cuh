@@ -211,16 +211,6 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16, issued by one thread.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -233,14 +223,29 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle: rows of 128 bytes, 8-row atoms of 1024 bytes stacked
 // densely (stride-dimension offset 1024 B), atom base 1024-byte aligned.
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // bits 0-13  start address >> 4
-  d |= (uint64_t)1u << 16;                   // bits 16-29 leading offset (unused here)
-  d |= (uint64_t)(1024u >> 4) << 32;         // bits 32-45 stride offset >> 4
-  d |= (uint64_t)1u << 46;                   // bits 46-48 fixed 0b001
-  d |= (uint64_t)2u << 61;                   // bits 61-63 swizzle: 128-byte
-  return d;
+//   bits 0-13  start address >> 4        bits 16-29 leading offset (unused: 1)
+//   bits 32-45 stride offset >> 4 (64)   bits 46-48 fixed 0b001
+//   bits 61-63 swizzle: 128-byte (2)
+// Only the low word depends on the tile, so the MMA issue builds the 64-bit
+// value from a 32-bit low word and this constant high word (32-bit address
+// arithmetic per K step: +2 in the start-address field per 32 bytes).
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16, issued by one thread; the
+// operands are given by the low words of their descriptors.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 ad, {%1, %5};\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSw128DescHi)
+      : "memory");
 }
 
 // Instruction descriptor, kind::f16: f16 x f16 -> f32, both K-major.
