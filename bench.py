@@ -493,7 +493,8 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     pack_ms = e0.elapsed_time(e1) / R
     del raw_d
     Xs = [torch.from_numpy(X).to(device) for _ in range(R)]
-    acts = [q6.alloc_activations(N, K, device) for _ in range(R)]
+    # the tensor-core GEMM reads Xh and da only, so the step skips the int8 Xq
+    acts = [q6.alloc_activations(N, K, device, want_xq=N <= q6.SKINNY_MAX_N) for _ in range(R)]
     Ys = [torch.empty((N, M), dtype=torch.float32, device=device) for _ in range(R)]
     # the operand plane the GEMM reads: resident (wh) or unpacked per step
     whs = [W.wh if src == "wh" else torch.empty((2, M, K), dtype=torch.float16, device=device)
@@ -572,12 +573,13 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
             ams = a.elapsed_time(b) / args.alt_steps
             alt[other] = {"q6k_mmq_ms": ams, "q6k_mmq_tops": ops_per_step / ams / 1e9}
         # the pages' route on the legacy mma.sync int8 path, as a comparison point
+        acts8 = [q6.quantize_act(Xs[j]) for j in range(R)]  # it reads Xq
         for i in range(3):
-            q6.mmq_mma_sync(Wa, acts[0], Y=Ys[0])
+            q6.mmq_mma_sync(Wa, acts8[0], Y=Ys[0])
         a, b = ev_pair()
         a.record()
         for i in range(args.alt_steps):
-            q6.mmq_mma_sync(Wa, acts[i % R], Y=Ys[i % R])
+            q6.mmq_mma_sync(Wa, acts8[i % R], Y=Ys[i % R])
         b.record()
         torch.cuda.synchronize()
         q6.sync_status()
@@ -609,7 +611,7 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         return
     peak_t, peak_src = tensor_peak(peaks)
     tflops = ops_per_step / m_ms / 1e9
-    q_bytes = N * K * (4 + 1 + 2) + (K // 32) * N * 4
+    q_bytes = N * K * (4 + (1 if acts[0].xq is not None else 0) + 2) + (K // 32) * N * 4
     # unpack: reads the codes (qlh 0.75 B or W_exp 1 B per weight) and sc
     # (1/16 B), writes the two binary16 operand planes (4 B per weight)
     u_bytes = M * K * ((1 if src == "wexp" else 0.75) + 1 / 16 + 4)
@@ -784,7 +786,8 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     resident = sum(w.plane.numel() for pair in layers for w in pair)
     Xv, Xd = synth.sweep_activations()
     Xvd, Xdd = torch.from_numpy(Xv).to(device), torch.from_numpy(Xd).to(device)
-    av, ad = q6.alloc_activations(N, 4096, device), q6.alloc_activations(N, 11008, device)
+    av = q6.alloc_activations(N, 4096, device, want_xq=False)
+    ad = q6.alloc_activations(N, 11008, device, want_xq=False)
     Yv = torch.empty((N, 4096), dtype=torch.float32, device=device)
     Yd = torch.empty((N, 4096), dtype=torch.float32, device=device)
     ws = torch.empty(q6.workspace_bytes(4096, 11008, N), dtype=torch.uint8, device=device)

@@ -100,8 +100,10 @@ int q8_act_plane_bytes(int N, int K, size_t *xq_bytes, size_t *da_bytes,
                        size_t *xh_bytes, int *ldda);
 
 /* X: device f32 [N][ldx], ldx >= K, X and ldx*4 16-byte aligned.
- * Xq, da required; Xh may be NULL. Xq, Xh, da 16-byte aligned.
- * K % 256 == 0. N == 0 is a no-op. */
+ * da required; at least one of Xq and Xh (the other may be NULL: a prefill
+ * caller that only runs the tensor-core GEMM needs Xh and da, the few-token
+ * kernels need Xq and da). Xq, Xh, da 16-byte aligned. K % 256 == 0.
+ * N == 0 is a no-op. */
 int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da,
                     uint16_t *Xh, q6_stream_t s);
 

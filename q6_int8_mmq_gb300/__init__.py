@@ -110,21 +110,26 @@ class Activations:
         self.N, self.K, self.xq, self.da, self.xh, self.ldda = N, K, xq, da, xh, ldda
 
 
-def alloc_activations(N: int, K: int, device=None, want_xh: bool = True) -> Activations:
+def alloc_activations(N: int, K: int, device=None, want_xh: bool = True,
+                      want_xq: bool = True) -> Activations:
+    """Buffers for quantised activations. A prefill caller that only runs the
+    tensor-core GEMM (N > SKINNY_MAX_N) can skip xq; the few-token kernels
+    need it (and not xh)."""
     import torch
     dev = device or torch.device("cuda")
     _, dab, _, ldda = act_plane_bytes(N, K)
-    xq = torch.empty((N, K), dtype=torch.int8, device=dev)
+    xq = torch.empty((N, K), dtype=torch.int8, device=dev) if want_xq else None
     da = torch.empty((K // 32, ldda), dtype=torch.float32, device=dev)
     xh = torch.empty((N, K), dtype=torch.float16, device=dev) if want_xh else None
     return Activations(N, K, xq, da, xh, ldda)
 
 
-def quantize_act(X, out: Activations | None = None, want_xh: bool = True, stream=None) -> Activations:
+def quantize_act(X, out: Activations | None = None, want_xh: bool = True, stream=None,
+                 want_xq: bool = True) -> Activations:
     """Quantises f32 activations X [N, K] (CUDA tensor, last dim contiguous)."""
     N, K = X.shape
     if out is None:
-        out = alloc_activations(N, K, X.device, want_xh)
+        out = alloc_activations(N, K, X.device, want_xh, want_xq)
     _check(load().q8_quantize_act(_ptr(X), N, K, X.stride(0), _ptr(out.xq), _ptr(out.da),
                                   _ptr(out.xh), _stream(stream)))
     return out

@@ -183,8 +183,9 @@ int q8_quantize_act(const float* X, int N, int K, int ldx, int8_t* Xq, float* da
   if (N < 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need N >= 0, K > 0, K %% 256 == 0");
   if (ldx < K) return fail(Q6_EINVAL, "ldx (%d) < K (%d)", ldx, K);
   if (N == 0) return Q6_OK;
-  if (!X || !Xq || !da) return fail(Q6_EINVAL, "X, Xq and da are required");
-  if (!aligned(X, 16) || ldx % 4 || !aligned(Xq, 16) || !aligned(da, 16) || (Xh && !aligned(Xh, 16)))
+  if (!X || !da || (!Xq && !Xh)) return fail(Q6_EINVAL, "X, da and one of Xq, Xh are required");
+  if (!aligned(X, 16) || ldx % 4 || (Xq && !aligned(Xq, 16)) || !aligned(da, 16) ||
+      (Xh && !aligned(Xh, 16)))
     return fail(Q6_EALIGN, "X, Xq, da, Xh must be 16-byte aligned and ldx a multiple of 4");
   if ((long long)N * K > (1LL << 40)) return fail(Q6_ESIZE, "N*K too large");
   DevState* st;

@@ -1,5 +1,6 @@
 // Activation quantiser: f32 X[N][K] -> int8 Xq[N][K], f32 da[K/32][ldda] and
-// the binary16 operand plane Xh[N][K] read by the tensor-core GEMM.
+// the binary16 operand plane Xh[N][K] read by the tensor-core GEMM (either of
+// Xq and Xh may be skipped).
 //
 // Per token n and 32-element block c: amax = max|x|, da = amax/127,
 // xq = clamp(round_half_away(x/da), -127, 127); amax == 0 gives da = 0 and
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restri
     uint2 q8;
     uint4 h8;
     quant8(v0, v1, d, q8, h8);
-    reinterpret_cast<uint2*>(Xq + (size_t)n * K)[j] = q8;
+    if (Xq != nullptr) reinterpret_cast<uint2*>(Xq + (size_t)n * K)[j] = q8;
     if (Xh != nullptr) reinterpret_cast<uint4*>(Xh + (size_t)n * K)[j] = h8;
     if ((j & 3) == 0) da[(size_t)(j >> 2) * ldda + n] = d;
   }
@@ -106,7 +107,8 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
     uint4 ha, hb;
     quant8(v0, v1, d, qa, ha);
     quant8(v2, v3, d, qb, hb);
-    reinterpret_cast<uint4*>(Xq + (size_t)n * K)[j] = make_uint4(qa.x, qa.y, qb.x, qb.y);
+    if (Xq != nullptr)
+      reinterpret_cast<uint4*>(Xq + (size_t)n * K)[j] = make_uint4(qa.x, qa.y, qb.x, qb.y);
     if (Xh != nullptr) {
       uint4* h = reinterpret_cast<uint4*>(Xh + (size_t)n * K) + 2 * j;
       h[0] = ha;

@@ -92,6 +92,10 @@ def test_host_side_rejections(lib):
     assert lib.q8_quantize_act(fake, 4, 256, 128, fake, fake, None, None) == q6.Q6_EINVAL
     assert lib.q8_quantize_act(odd, 4, 256, 256, fake, fake, None, None) == q6.Q6_EALIGN
     assert lib.q8_quantize_act(None, 0, 256, 256, None, None, None, None) == q6.Q6_OK
+    # quantiser: neither Xq nor Xh; a misaligned Xq or Xh
+    assert lib.q8_quantize_act(fake, 4, 256, 256, None, fake, None, None) == q6.Q6_EINVAL
+    assert lib.q8_quantize_act(fake, 4, 256, 256, odd, fake, None, None) == q6.Q6_EALIGN
+    assert lib.q8_quantize_act(fake, 4, 256, 256, None, fake, odd, None) == q6.Q6_EALIGN
     # pack: misaligned plane or wh, missing raw
     assert lib.q6k_pack_weights(fake, 4, 256, odd, None, None, None) == q6.Q6_EALIGN
     assert lib.q6k_pack_weights(fake, 4, 256, fake, None, odd, None) == q6.Q6_EALIGN

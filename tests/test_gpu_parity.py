@@ -125,6 +125,31 @@ def test_quantize_bitexact(q6, orc, N, K, frac):
     quant_check(act, X, orc)
 
 
+def test_quantize_without_xq_and_gemm(q6, orc):
+    """A prefill caller may skip the int8 Xq: Xh and da are the same, the
+    tensor-core GEMM runs on them, and the few-token kernels refuse such
+    activations (they read Xq)."""
+    M, K, N = 256, 1024, 200
+    raw = synth.q6k_raw_weights(0x51360C01, M, K)
+    X = synth.activations(0x51360C02, N, K, outlier_frac=0.02)
+    full = q6.quantize_act(dev(X))
+    act = q6.quantize_act(dev(X), want_xq=False)
+    q6.sync_status()
+    assert act.xq is None
+    assert np.array_equal(host(act.xh), host(full.xh))
+    assert np.array_equal(host(act.da)[:, :N], host(full.da)[:, :N])
+    w = q6.pack_weights(dev(raw), M, K)
+    Y, path, _ = q6.mmq(w, act, source="raw")
+    q6.sync_status()
+    assert path == "tc_raw"
+    xq_o, da_o = orc.quantize(X)
+    check_y(host(Y), orc.mmq(raw, M, K, xq_o, da_o), "without Xq")
+    few = q6.quantize_act(dev(X[:4]), want_xq=False)
+    with pytest.raises(q6.Q6Error) as ei:
+        q6.mmq(w, few, source="raw")
+    assert ei.value.code == q6.Q6_EINVAL
+
+
 def test_quantize_strided_input(q6, orc):
     import torch
     X = synth.activations(7, 33, 512)
