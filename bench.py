@@ -462,6 +462,16 @@ def run_ours(args):
     run(args, q6, synth, device, rank, world, peaks, hbm, hbm_src)
 
 
+def epilogue_alu_bound(clk) -> float:
+    """The rescale's CUDA-core bound of the GEMM in TFLOP/s of 2*M*N*K: the
+    epilogue does one FP32 FMA per (token, weight row, 32-element chunk) plus
+    one per super-block (1.125 per 32 MACs), at 128 FMA per cycle per SM on
+    152 SMs at the SM clock seen under load."""
+    mhz = (clk or {}).get("sm_mhz") or 2070.0
+    fma_per_s = 128 * 152 * mhz * 1e6
+    return fma_per_s * 32 / 1.125 * 2 / 1e12
+
+
 def tensor_peak(peaks):
     p = peaks.get("bf16_tflops_sustained")
     if p is None:
@@ -592,7 +602,7 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     if args.e2e_steps > 0:
         Xh = torch.from_numpy(X).pin_memory()
         Yh = [torch.empty((N, M), dtype=torch.float32).pin_memory() for _ in range(R)]
-        e_ms = e2e_run_overlapped(step, [[(Xs[j], Xh)] for j in range(R)],
+        e_ms = e2e_run_overlapped(step_seq, [[(Xs[j], Xh)] for j in range(R)],
                                   [[(Yh[j], Ys[j])] for j in range(R)], args.e2e_steps, device)
         q6.sync_status()
         e2e = {"value": job_throughput(ops_per_step * args.e2e_steps, world, e_ms / 1e3) / 1e12,
@@ -630,7 +640,9 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         "clocks": clk, "clocks_ok": clocks_ok(clk),
         "kernels": {
             "q6k_mmq": {"ms": m_ms, "tflops": tflops, "path": path[0],
-                        "frac_of_int8_4.5P": tflops / 4500.0},
+                        "frac_of_int8_4.5P": tflops / 4500.0,
+                        "us_per_gmac": m_ms * 1e3 / (ops_per_step / 2e9),
+                        "frac_of_epilogue_alu_bound": tflops / epilogue_alu_bound(clk)},
             "q8_quantize_act": {"ms": q_ms, "gbs": q_bytes / q_ms / 1e6,
                                 "frac_hbm": q_bytes / q_ms / 1e6 / hbm},
             "q6k_unpack_weights": ({"ms": u_ms, "gbs": u_bytes / u_ms / 1e6,
@@ -898,7 +910,7 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 # kernels, keyed by (workload, kernel); the capture each figure comes from is
 # summarised under profiles/ (mmq_tc_ffn_down.md). An entry is removed when
 # its kernel changes.
-TRAFFIC = {("ffn_down", "mmq_tc"): None}
+TRAFFIC = {("ffn_down", "mmq_tc"): 667.22e6 + 53.22e6}
 
 
 def main():
