@@ -4,8 +4,16 @@
 //
 // Math ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.1-2.2): for each
 // 16-element sub-block s the exact integer P = sum (q - 32) * xq is formed
-// with dp4a, then Y += (f32(d) * sc[s]) * da[chunk] * P. The element map is
-// the one of Sec. 3.2 (see pack.cu).
+// with dp4a, then Y += f32(d) * (da[chunk] * (sc[s] * P)) summed over the
+// sub-blocks. The element map is the one of Sec. 3.2 (see pack.cu).
+//
+// Split form of the integer dot product: a code is q = lo + 16*hi (lo the
+// ql nibble, hi the 2-bit qh field), so  sum (q - 32) x = sum (lo - 32) x +
+// 16 * sum hi x.  lo - 32 as a signed byte is lo | 0xE0 (lo < 16), one LOP3
+// per four codes; the qh fields are masked in place (a field at bits f, f+1
+// gives 2^f * hi per byte) and the power of two is taken off the int32 sum
+// with one shift. No code is ever assembled or re-centred, which halves the
+// integer work per weight against building the 6-bit codes first.
 //
 // Row dot product: one warp per weight row; per iteration a warp covers four
 // super-blocks, eight lanes per super-block. Lane (half, s4) of a super-block
@@ -17,14 +25,18 @@
 // Streaming: warps stride over the rows, with the grid sized to one resident
 // wave (4 warps per CTA, 64 registers, 8 CTAs per SM) so every warp starts at
 // once and reads its row's qlh run in coalesced 768-byte steps; the loads of
-// the next step are in flight while the current step is computed. One token
-// (and the debug partials) take one row per warp; N <= 4 takes two rows per
-// warp, so each activation load serves both rows; 5..16 tokens go to the int8
-// tensor-core form in mmq_skinny_mma.cu. Measured on GB300
-// and not kept: loading two to four steps ahead (more registers, fewer
-// resident warps), a cp.async.bulk ring of whole rows, a per-warp cp.async
-// ring in shared memory, L2 prefetches (per step, or of whole rows with
-// cp.async.bulk.prefetch), and four rows per warp.
+// the next step are in flight while the current step is computed. Rows go to
+// warps warp-index-major (rank = warp * gridDim + block), so consecutive
+// rows land on consecutive CTAs and every SM gets the same number of rows
+// to within one. One token (and the debug partials) take one row per warp;
+// N <= 4 takes two rows per warp, so each activation load serves both rows;
+// 5..16 tokens go to the int8 tensor-core form in mmq_skinny_mma.cu.
+// Measured on GB300 and not kept: loading two to four steps ahead (more
+// registers, fewer resident warps), a cp.async.bulk ring of whole rows, a
+// per-warp cp.async ring in shared memory, L2 prefetches (per step, or of
+// whole rows with cp.async.bulk.prefetch), four rows per warp, a step-major
+// order of the weight plane (no faster than row-major), and one 8-byte load
+// of the two sub-block scales with byte permutes (slower than two byte loads).
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -55,6 +67,34 @@ __device__ __forceinline__ void unpack_pair(const uint4 L, const uint4 H, int fs
   }
 }
 
+// c + sum over the four byte pairs of a (unsigned) times b (signed).
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Exact P of a lane's two sub-blocks (split form, see the top of the file):
+// pa = sum (q - 32) * xa over the low-nibble sub-block (qh field at bits
+// fsh), pb the same over the high-nibble sub-block (field at fsh + 4), from
+// its 16 ql bytes L, 16 qh bytes H and the 16 activation bytes of each.
+__device__ __forceinline__ void dot_pair(const uint4 L, const uint4 H, int fsh, const uint4 xa,
+                                         const uint4 xb, int& pa, int& pb) {
+  const uint32_t Lw[4] = {L.x, L.y, L.z, L.w}, Hw[4] = {H.x, H.y, H.z, H.w};
+  const uint32_t Xa[4] = {xa.x, xa.y, xa.z, xa.w}, Xb[4] = {xb.x, xb.y, xb.z, xb.w};
+  const uint32_t mha = 0x03030303u << fsh, mhb = 0x30303030u << fsh;
+  int la = 0, lb = 0, ha = 0, hb = 0;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    la = __dp4a((int)((Lw[w] & 0x0F0F0F0Fu) | 0xE0E0E0E0u), (int)Xa[w], la);  // lo - 32
+    lb = __dp4a((int)(((Lw[w] >> 4) & 0x0F0F0F0Fu) | 0xE0E0E0E0u), (int)Xb[w], lb);
+    ha = __dp4a((int)(Hw[w] & mha), (int)Xa[w], ha);  // 2^fsh * hi: bytes <= 12
+    hb = dp4a_us(Hw[w] & mhb, Xb[w], hb);             // 16 * 2^fsh * hi: bytes <= 192
+  }
+  pa = la + (ha << (4 - fsh));
+  pb = lb + (hb >> fsh);  // an exact multiple of 2^fsh
+}
+
 // One lane's share of one step: sub-blocks sa = 8*half + s4 and sa + 4 of
 // super-block sb, from its 16 ql bytes L and 16 qh bytes H, for every token.
 template <bool kPartials, int kMaxN>
@@ -68,11 +108,7 @@ __device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a,
   const int s4 = lane & 3;
   const int fsh = 2 * (s4 >> 1);  // field of the low-nibble sub-block
   const int sa = 8 * half + s4;   // sub-block (0..15) of the low nibbles; sb_b = sa + 4
-  uint32_t va[4], vb[4];
-  unpack_pair(L, H, fsh, va, vb);
   const float d = __half2float(__ushort_as_half(dbits));
-  const float dsc_a = d * (float)sc_a;
-  const float dsc_b = d * (float)sc_b;
   const int ka = 256 * sb + 16 * sa;  // first element of sub-block a
   const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
 #pragma unroll
@@ -81,18 +117,12 @@ __device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a,
       const int8_t* xr = Xq + (size_t)n * K;
       const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
       const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
-      int pa = __dp4a((int)va[0], (int)xa.x, 0);
-      pa = __dp4a((int)va[1], (int)xa.y, pa);
-      pa = __dp4a((int)va[2], (int)xa.z, pa);
-      pa = __dp4a((int)va[3], (int)xa.w, pa);
-      int pb = __dp4a((int)vb[0], (int)xb.x, 0);
-      pb = __dp4a((int)vb[1], (int)xb.y, pb);
-      pb = __dp4a((int)vb[2], (int)xb.z, pb);
-      pb = __dp4a((int)vb[3], (int)xb.w, pb);
+      int pa, pb;
+      dot_pair(L, H, fsh, xa, xb, pa, pb);
       const float daa = __ldg(da + (size_t)ca_blk * ldda + n);
       const float dab = __ldg(da + (size_t)cb_blk * ldda + n);
-      acc[n] = fmaf(dsc_a * daa, (float)pa, acc[n]);
-      acc[n] = fmaf(dsc_b * dab, (float)pb, acc[n]);
+      // sc * P is an integer below 2^24 in magnitude: exact in f32
+      acc[n] = fmaf(d, fmaf(dab, (float)(sc_b * pb), daa * (float)(sc_a * pa)), acc[n]);
       if (kPartials) {
         // chunk partials sc*P summed over the chunk's two sub-blocks; the
         // other sub-block of each chunk is in lane ^ 1 (active together)
@@ -132,8 +162,8 @@ __device__ __forceinline__ void row_store(float (&acc)[kMaxN], int m, int N, flo
 // The dot products of one weight row with the N <= kMaxN activation rows.
 // Each step covers 4 super-blocks (768 bytes of codes per warp); the loads of
 // step i + 1 are issued before the math of step i (a one-step software
-// pipeline held in registers). The result is reduced across the warp and
-// written by lane 0.
+// pipeline on two register buffers). The result is reduced across the warp
+// and written by lane 0.
 template <bool kPartials, int kMaxN>
 __device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
                                         const int8_t* __restrict__ sc_row,
@@ -152,34 +182,48 @@ __device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
 #pragma unroll
   for (int n = 0; n < kMaxN; ++n) acc[n] = 0.0f;
 
-  uint4 L = make_uint4(0, 0, 0, 0), H = L;
-  int sca = 0, scb = 0;
-  uint16_t dbits = 0;
-  auto load = [&](int sb, uint4& l, uint4& h, int& a, int& b, uint16_t& dd) {
+  struct Step {
+    uint4 L, H;
+    int a, b;
+    uint16_t d;
+  };
+  auto load = [&](int sb, Step& r) {
+    r.L = make_uint4(0, 0, 0, 0);
+    r.H = r.L;
+    r.a = r.b = 0;
+    r.d = 0;
     if (sb < nsb) {
       const uint8_t* hb = qlh_row + (size_t)(2 * sb + half) * 96;
-      l = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
-      h = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
-      a = __ldg(sc_row + 16 * sb + sa);
-      b = __ldg(sc_row + 16 * sb + sa + 4);
-      dd = __ldg(d_row + sb);
+      r.L = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
+      r.H = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
+      r.a = __ldg(sc_row + 16 * sb + sa);
+      r.b = __ldg(sc_row + 16 * sb + sa + 4);
+      r.d = __ldg(d_row + sb);
     }
   };
-  load(sbi, L, H, sca, scb, dbits);
-  for (int g0 = 0; g0 < nsb; g0 += 4) {
-    uint4 L2 = make_uint4(0, 0, 0, 0), H2 = L2;
-    int sca2 = 0, scb2 = 0;
-    uint16_t dbits2 = 0;
-    load(g0 + 4 + sbi, L2, H2, sca2, scb2, dbits2);  // next step, in flight during this one
-    const int sb = g0 + sbi;
+  auto step = [&](int sb, const Step& r) {
     if (sb < nsb)
-      step_dot<kPartials, kMaxN>(L, H, sca, scb, dbits, sb, m, M, K, Xq, da, ldda, N, partials,
+      step_dot<kPartials, kMaxN>(r.L, r.H, r.a, r.b, r.d, sb, m, M, K, Xq, da, ldda, N, partials,
                                  acc);
-    L = L2;
-    H = H2;
-    sca = sca2;
-    scb = scb2;
-    dbits = dbits2;
+  };
+  Step A, B;
+  load(sbi, A);
+  if constexpr (kMaxN == 1 && !kPartials) {
+    // two step buffers used in turn, so no registers are copied between steps
+    for (int g0 = 0; g0 < nsb; g0 += 8) {
+      load(g0 + 4 + sbi, B);  // in flight during the step on A
+      step(g0 + sbi, A);
+      load(g0 + 8 + sbi, A);  // in flight during the step on B
+      step(g0 + 4 + sbi, B);
+    }
+  } else {
+    // the debug partials form (16 accumulators) keeps one buffer in flight
+    // and copies it forward, which needs fewer registers
+    for (int g0 = 0; g0 < nsb; g0 += 4) {
+      load(g0 + 4 + sbi, B);
+      step(g0 + sbi, A);
+      A = B;
+    }
   }
   row_store<kMaxN>(acc, m, N, Y, ldy);
 }
@@ -191,7 +235,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
     const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
     int32_t* __restrict__ partials) {
   const int warps = (int)gridDim.x * kWarps;
-  for (int m = blockIdx.x * kWarps + (threadIdx.x >> 5); m < M; m += warps)
+  for (int m = (threadIdx.x >> 5) * (int)gridDim.x + blockIdx.x; m < M; m += warps)
     row_dot<kPartials, kMaxN>(
         plane + g.qlh_off + (size_t)m * g.qlh_row,
         reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)m * (K / 16),
@@ -339,7 +383,8 @@ template <bool P, int kMaxN>
 cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
                           const float* da, int ldda, int N, float* Y, int ldy, int32_t* partials,
                           cudaStream_t s) {
-  // one resident wave: as many blocks as fit, warps striding over the rows
+  // one resident wave of blocks, warps striding over the rows (blocks with
+  // no row return at once; the row order spreads the rows evenly over SMs)
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -347,8 +392,7 @@ cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K
   if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mmq_skinny_kernel<P, kMaxN>,
                                                          kWarps * 32, 0)))
     return e;
-  const long long need = (M + kWarps - 1) / kWarps, cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
-  const unsigned blocks = (unsigned)(need < cap ? need : cap);
+  const unsigned blocks = (unsigned)(sms * (per_sm > 0 ? per_sm : 1));
   mmq_skinny_kernel<P, kMaxN><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y,
                                                              ldy, partials);
   return cudaGetLastError();
