@@ -1,6 +1,7 @@
-// q6_K x int8 GEMM for few tokens (N <= 16): a weight-streaming kernel on the
-// CUDA cores, bound by HBM (0.82 byte per weight: 210 bytes per 256 weights,
-// plus the 16-byte padding of each d row).
+// q6_K x int8 GEMM for one token: a weight-streaming kernel on the CUDA
+// cores, bound by HBM (0.82 byte per weight: 210 bytes per 256 weights, plus
+// the 16-byte padding of each d row). 2..16 tokens run on the tensor-core form
+// in mmq_skinny_mma.cu.
 //
 // Math ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.1-2.2): for each
 // 16-element sub-block s the exact integer P = sum (q - 32) * xq is formed
@@ -28,15 +29,12 @@
 // the next step are in flight while the current step is computed. Rows go to
 // warps warp-index-major (rank = warp * gridDim + block), so consecutive
 // rows land on consecutive CTAs and every SM gets the same number of rows
-// to within one. One token (and the debug partials) take one row per warp;
-// N <= 4 takes two rows per warp, so each activation load serves both rows;
-// 5..16 tokens go to the int8 tensor-core form in mmq_skinny_mma.cu.
-// Measured on GB300 and not kept: loading two to four steps ahead (more
-// registers, fewer resident warps), a cp.async.bulk ring of whole rows, a
-// per-warp cp.async ring in shared memory, L2 prefetches (per step, or of
-// whole rows with cp.async.bulk.prefetch), four rows per warp, a step-major
-// order of the weight plane (no faster than row-major), and one 8-byte load
-// of the two sub-block scales with byte permutes (slower than two byte loads).
+// to within one. Measured on GB300 and not kept: loading two to four steps
+// ahead (more registers, fewer resident warps), a cp.async.bulk ring of whole
+// rows, a per-warp cp.async ring in shared memory, L2 prefetches (per step,
+// or of whole rows with cp.async.bulk.prefetch), a step-major order of the
+// weight plane (no faster than row-major), and one 8-byte load of the two
+// sub-block scales with byte permutes (slower than two byte loads).
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -44,28 +42,6 @@ namespace {
 
 constexpr int kWarps = 4;      // warps per CTA
 constexpr int kMinBlocks = 8;  // resident CTAs per SM (64 registers per thread)
-
-// Bytes (code - 32) mod 256 of four 6-bit codes: code + 96 never carries out
-// of its byte, and adding 128 more is a flip of bit 7.
-__device__ __forceinline__ uint32_t center4(uint32_t code) {
-  return (code + 0x60606060u) ^ 0x80808080u;
-}
-
-// Centered codes of a lane's two sub-blocks from its 16 ql bytes L and 16 qh
-// bytes H: va (low nibbles, qh field fsh) and vb (high nibbles, field fsh + 4),
-// four codes per word.
-__device__ __forceinline__ void unpack_pair(const uint4 L, const uint4 H, int fsh, uint32_t (&va)[4],
-                                            uint32_t (&vb)[4]) {
-  const uint32_t Lw[4] = {L.x, L.y, L.z, L.w};
-  const uint32_t Hw[4] = {H.x, H.y, H.z, H.w};
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t ca = (Lw[w] & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
-    const uint32_t cb = ((Lw[w] >> 4) & 0x0F0F0F0Fu) | (((Hw[w] >> (fsh + 4)) & 0x03030303u) << 4);
-    va[w] = center4(ca);
-    vb[w] = center4(cb);
-  }
-}
 
 // c + sum over the four byte pairs of a (unsigned) times b (signed).
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -206,24 +182,14 @@ __device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
       step_dot<kPartials, kMaxN>(r.L, r.H, r.a, r.b, r.d, sb, m, M, K, Xq, da, ldda, N, partials,
                                  acc);
   };
+  // two step buffers used in turn, so no registers are copied between steps
   Step A, B;
   load(sbi, A);
-  if constexpr (kMaxN == 1 && !kPartials) {
-    // two step buffers used in turn, so no registers are copied between steps
-    for (int g0 = 0; g0 < nsb; g0 += 8) {
-      load(g0 + 4 + sbi, B);  // in flight during the step on A
-      step(g0 + sbi, A);
-      load(g0 + 8 + sbi, A);  // in flight during the step on B
-      step(g0 + 4 + sbi, B);
-    }
-  } else {
-    // the debug partials form (16 accumulators) keeps one buffer in flight
-    // and copies it forward, which needs fewer registers
-    for (int g0 = 0; g0 < nsb; g0 += 4) {
-      load(g0 + 4 + sbi, B);
-      step(g0 + sbi, A);
-      A = B;
-    }
+  for (int g0 = 0; g0 < nsb; g0 += 8) {
+    load(g0 + 4 + sbi, B);  // in flight during the step on A
+    step(g0 + sbi, A);
+    load(g0 + 8 + sbi, A);  // in flight during the step on B
+    step(g0 + 4 + sbi, B);
   }
   row_store<kMaxN>(acc, m, N, Y, ldy);
 }
@@ -244,140 +210,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
 }
 
 
-// Several tokens: kRows weight rows per warp with the same lane mapping, so
-// each activation word and scale a lane loads serves kRows rows. With 16
-// tokens the activation loads through L1 bound the one-row form (ncu: L1 84%
-// busy); two rows per warp cut that traffic in half.
-template <int kMaxN, int kRows>
-__device__ __forceinline__ void step_rows(const uint4 (&L)[kRows], const uint4 (&H)[kRows],
-                                          const int (&sca)[kRows], const int (&scb)[kRows],
-                                          const uint16_t (&dbits)[kRows], int sb, int K,
-                                          const int8_t* __restrict__ Xq,
-                                          const float* __restrict__ da, int ldda, int N,
-                                          float (&acc)[kRows][kMaxN]) {
-  const int lane = threadIdx.x & 31;
-  const int half = (lane >> 2) & 1;
-  const int s4 = lane & 3;
-  const int sa = 8 * half + s4;
-  uint32_t va[kRows][4], vb[kRows][4];
-  float dsa[kRows], dsb[kRows];
-#pragma unroll
-  for (int r = 0; r < kRows; ++r) {
-    unpack_pair(L[r], H[r], 2 * (s4 >> 1), va[r], vb[r]);
-    const float d = __half2float(__ushort_as_half(dbits[r]));
-    dsa[r] = d * (float)sca[r];
-    dsb[r] = d * (float)scb[r];
-  }
-  const int ka = 256 * sb + 16 * sa;
-  const int ca_blk = ka >> 5, cb_blk = (ka + 64) >> 5;
-#pragma unroll
-  for (int n = 0; n < kMaxN; ++n) {
-    if (n < N) {
-      const int8_t* xr = Xq + (size_t)n * K;
-      const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
-      const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
-      const float daa = __ldg(da + (size_t)ca_blk * ldda + n);
-      const float dab = __ldg(da + (size_t)cb_blk * ldda + n);
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        int pa = __dp4a((int)va[r][0], (int)xa.x, 0);
-        pa = __dp4a((int)va[r][1], (int)xa.y, pa);
-        pa = __dp4a((int)va[r][2], (int)xa.z, pa);
-        pa = __dp4a((int)va[r][3], (int)xa.w, pa);
-        int pb = __dp4a((int)vb[r][0], (int)xb.x, 0);
-        pb = __dp4a((int)vb[r][1], (int)xb.y, pb);
-        pb = __dp4a((int)vb[r][2], (int)xb.z, pb);
-        pb = __dp4a((int)vb[r][3], (int)xb.w, pb);
-        acc[r][n] = fmaf(dsa[r] * daa, (float)pa, acc[r][n]);
-        acc[r][n] = fmaf(dsb[r] * dab, (float)pb, acc[r][n]);
-      }
-    }
-  }
-}
-
-// Rows m0 .. m0 + kRows - 1 (those below M) against the N <= kMaxN
-// activation rows, with the same one-step software pipeline as row_dot.
-template <int kMaxN, int kRows>
-__device__ __forceinline__ void rows_dot(const uint8_t* __restrict__ plane, const PlaneGeom& g,
-                                         int m0, int M, int K, const int8_t* __restrict__ Xq,
-                                         const float* __restrict__ da, int ldda, int N,
-                                         float* __restrict__ Y, int ldy) {
-  const int lane = threadIdx.x & 31;
-  const int nsb = K / 256;
-  const int sbi = lane >> 3;
-  const int half = (lane >> 2) & 1;
-  const int s4 = lane & 3;
-  const int sa = 8 * half + s4;
-  const uint8_t* qrow[kRows];
-  const int8_t* srow[kRows];
-  const uint16_t* drow[kRows];
-#pragma unroll
-  for (int r = 0; r < kRows; ++r) {
-    const int m = min(m0 + r, M - 1);  // a row past the end re-reads row M-1 and is not stored
-    qrow[r] = plane + g.qlh_off + (size_t)m * g.qlh_row;
-    srow[r] = reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)m * (K / 16);
-    drow[r] = reinterpret_cast<const uint16_t*>(plane + g.d_off + (size_t)m * g.d_row);
-  }
-  float acc[kRows][kMaxN];
-#pragma unroll
-  for (int r = 0; r < kRows; ++r)
-#pragma unroll
-    for (int n = 0; n < kMaxN; ++n) acc[r][n] = 0.0f;
-  uint4 L[kRows], H[kRows];
-  int sca[kRows], scb[kRows];
-  uint16_t db[kRows];
-  auto load = [&](int sb, uint4(&l)[kRows], uint4(&h)[kRows], int(&a)[kRows], int(&b)[kRows],
-                  uint16_t(&dd)[kRows]) {
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      l[r] = make_uint4(0, 0, 0, 0);
-      h[r] = l[r];
-      a[r] = b[r] = 0;
-      dd[r] = 0;
-      if (sb < nsb) {
-        const uint8_t* hb = qrow[r] + (size_t)(2 * sb + half) * 96;
-        l[r] = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
-        h[r] = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
-        a[r] = __ldg(srow[r] + 16 * sb + sa);
-        b[r] = __ldg(srow[r] + 16 * sb + sa + 4);
-        dd[r] = __ldg(drow[r] + sb);
-      }
-    }
-  };
-  load(sbi, L, H, sca, scb, db);
-  for (int g0 = 0; g0 < nsb; g0 += 4) {
-    uint4 L2[kRows], H2[kRows];
-    int sca2[kRows], scb2[kRows];
-    uint16_t db2[kRows];
-    load(g0 + 4 + sbi, L2, H2, sca2, scb2, db2);  // next step, in flight during this one
-    const int sb = g0 + sbi;
-    if (sb < nsb) step_rows<kMaxN, kRows>(L, H, sca, scb, db, sb, K, Xq, da, ldda, N, acc);
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      L[r] = L2[r];
-      H[r] = H2[r];
-      sca[r] = sca2[r];
-      scb[r] = scb2[r];
-      db[r] = db2[r];
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < kRows; ++r)
-    if (m0 + r < M) row_store<kMaxN>(acc[r], m0 + r, N, Y, ldy);
-}
-
-// kRows rows per warp, warps striding over the row groups.
-template <int kMaxN, int kRows, int kMinB>
-__global__ void __launch_bounds__(kWarps * 32, kMinB) mmq_skinny_rows_kernel(
-    const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
-    const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy) {
-  const int warps = (int)gridDim.x * kWarps;
-  for (int m = (blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRows; m < M; m += warps * kRows)
-    rows_dot<kMaxN, kRows>(plane, g, m, M, K, Xq, da, ldda, N, Y, ldy);
-}
 }  // namespace
 
-cudaError_t mmq_skinny_prepare() { return cudaSuccess; }
+cudaError_t mmq_skinny_prepare() { return mmq_skinny_mma_prepare(); }
 
 template <bool P, int kMaxN>
 cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
@@ -398,37 +233,17 @@ cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K
   return cudaGetLastError();
 }
 
-// Two rows per warp for N <= 4 (measured on the ffn_down weights: 4 tokens
-// 20.8 -> 18.7 us); the register budget per thread sets the resident CTAs.
-template <int kMaxN, int kRows, int kMinB>
-cudaError_t launch_rows(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
-                        const float* da, int ldda, int N, float* Y, int ldy, cudaStream_t s) {
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-           &per_sm, mmq_skinny_rows_kernel<kMaxN, kRows, kMinB>, kWarps * 32, 0)))
-    return e;
-  const long long need = (M + kWarps * kRows - 1) / (kWarps * kRows);
-  const long long cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
-  const unsigned blocks = (unsigned)(need < cap ? need : cap);
-  mmq_skinny_rows_kernel<kMaxN, kRows, kMinB>
-      <<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y, ldy);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
                               unsigned int* status, cudaStream_t s) {
-  (void)status;  // the skinny kernel has no waits to bound
   const PlaneGeom g = plane_geom(M, K);
-  if (partials) return launch_bucket<true, Q6_SKINNY_MAX_N>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s);
-  if (N == 1) return launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
-  if (N <= 4) return launch_rows<4, 2, 5>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, s);
-  // 5..16 tokens: the int8 tensor-core form (mmq_skinny_mma.cu) shares each
-  // activation word among 16 rows (ffn_down weights, N = 16: 58 -> 32 us)
-  return launch_mmq_skinny_mma(plane, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+  // one token: the dp4a weight-streaming kernel (the debug partials come from
+  // the same dot products); 2..16 tokens: the f16 tensor form with TMA-staged
+  // weights (mmq_skinny_mma.cu), partials included
+  if (N == 1)
+    return partials ? launch_bucket<true, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s)
+                    : launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+  return launch_mmq_skinny_mma(plane, M, K, Xq, da, ldda, N, Y, ldy, partials, status, s);
 }
 
 }  // namespace q6

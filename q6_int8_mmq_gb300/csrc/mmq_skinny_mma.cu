@@ -1,222 +1,433 @@
-// q6_K x int8 GEMM for a few tokens (N <= 16) on the warp-level int8 tensor
-// path: the weights are streamed from the packed plane once (HBM-bound, 0.82
-// byte per weight), and the products run as mma.sync.m16n8k16.s8 so that one
-// activation word serves sixteen weight rows instead of one.
+// q6_K x int8 GEMM for a few tokens (2 <= N <= 16) on the warp-level f16
+// tensor path, with the weights streamed into shared memory by TMA. HBM-bound
+// by design: every weight byte is read once (0.82 byte per weight).
 //
 // Math ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.1-2.4): per
-// 16-element sub-block s the exact integer P = sum (q - 32) * xq comes from one
-// MMA (A = 16 weight rows x 16 codes, B = 16 activations x 8 tokens); per
-// 32-element chunk the scale is folded in integers, S = sc[2c] * P[2c] +
-// sc[2c+1] * P[2c+1] (|S| < 2^24), and Y += (d * da) * S in f32.
+// 16-element sub-block s the exact integer P = sum (q - 32) * xq is formed on
+// the tensor cores, per 32-element chunk the sub-block scales are applied,
+// S = sc[2c] * P[2c] + sc[2c+1] * P[2c+1], and Y += d * (da * S) in f32.
 //
-// Layout: a CTA of 8 warps owns 16 weight rows; warp w takes super-blocks
-// w, w + 8, ... of the rows (the eight warps read neighbouring super-blocks of
-// the same rows at the same time) and the partial sums of the eight warps are
-// added in shared memory at the end. Lane (g, t) = (lane / 4, lane % 4) holds
-// the MMA fragments of rows g and g + 8 at codes 4t .. 4t + 3 of each
-// sub-block, which it builds from 4-byte words of the qlh run ("r41 -- q6_K
-// B-expand widened to uint4 group loads", Sec. 3.2 element map): within a
-// 128-element half, sub-block s (0..7) takes the low (s < 4) or high nibbles
-// of ql word s % 4 at byte 16 (s % 4) + 4t, and the 2-bit field s / 2 of qh
-// word s % 2 at byte 64 + 16 (s % 2) + 4t. The next super-block's words are
-// loaded while the current one is computed.
+// Why f16 and not int8 MMA: on this GPU an int8 mma.sync.m16n8k16 takes about
+// 16 cycles per SM and an f16 one about 2 (measured), and the sub-block scale
+// needs one MMA per 16 codes. The products are exact in f16 with f32
+// accumulation: codes (q - 32) and activations (-127..127) are small
+// integers, and every partial sum of a sub-block is at most 16 * 32 * 127.
+// Each lane assembles its four 6-bit codes of a sub-block in one 32-bit word
+// (ql nibbles | qh field << 4) and turns byte pairs into binary16 pairs with
+// one byte permute (exponent byte 0x64 above each code: 1024 + code) and one
+// f16x2 subtraction of 1056.
+//
+// MMA mapping: m16n8k16, A = 16 weight rows x 16 codes, B = 16 codes x 8
+// tokens, both with the same order of the 16 codes: lane (g, t) = (lane / 4,
+// lane % 4) holds codes 4t .. 4t + 3 of the sub-block, as the pairs (4t, 4t+2)
+// in k-slots (2t, 2t+1) and (4t+1, 4t+3) in k-slots (2t+8, 2t+9). Those four
+// codes sit in the same byte positions of one ql word and one qh word (the
+// element map of Sec. 3.2, "r41 -- q6_K B-expand widened to uint4 group
+// loads"): in half h of a super-block's 192-byte qlh run (64 ql bytes, then
+// 32 qh bytes, per half), sub-block j (0..7) takes the low (j < 4) or high
+// nibbles of the ql word at byte 96 h + 16 (j % 4) + 4t and the 2-bit field
+// j / 2 of the qh word at byte 96 h + 64 + 16 (j % 2) + 4t.
+//
+// Work: CTA u takes R consecutive weight rows (R = ceil(M / SMs) up to 32,
+// so every SM gets the same number of rows to within one) and all of K. A
+// producer thread streams stages of 8 super-blocks of those rows through a
+// 3-stage ring with three 2D TMA loads (qlh, sc, d); each row of a qlh stage
+// box is 1552 bytes (1536 plus 16 of the next stage), so that the 8 rows of
+// an A fragment fall on different shared-memory banks. Consumer warp (s, g)
+// of 16 takes super-block s of every stage for rows 16g .. 16g + 15 of the
+// unit (16 warps, four per scheduler, hide the MMA and shared-memory
+// latencies), and the eight super-block warps' sums of a row are added in
+// shared memory at the end (fixed order).
+// Every mbarrier wait is bounded (see q6_internal.cuh).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "q6_internal.cuh"
 
 namespace q6 {
 namespace {
 
-constexpr int kWarps = 8;  // warps per CTA (the K split of a row tile)
+constexpr int kSbs = 8;                  // super-blocks per stage
+constexpr int kCW = 2 * kSbs;            // consumer warps: super-block x row group of 16
+constexpr int kThreads = 32 * (kCW + 1);  // + one producer warp
+constexpr int kNS = 3;                   // ring stages
+constexpr int kMaxR = 32;                // rows per unit (two MMA row groups)
+constexpr int kQPitch = 1552;            // bytes per row of a qlh stage (194 x 8)
+constexpr int kScPitch = 144;            // bytes per row of an sc stage (18 x 8)
+constexpr int kDPitch = 16;              // bytes per row of a d stage (2 x 8)
+constexpr int kRedBytes = kSbs * kMaxR * 16 * 4;
 
-__device__ __forceinline__ uint32_t ldg32(const uint8_t* p) {
-  return __ldg(reinterpret_cast<const unsigned int*>(p));
-}
+enum : uint32_t { kSiteEmpty = 21, kSiteFull = 22 };
 
-// Bytes (code - 32) mod 256 of four 6-bit codes (code + 96 never carries out of
-// its byte; adding 128 more flips bit 7).
-__device__ __forceinline__ uint32_t centered(uint32_t code) {
-  return (code + 0x60606060u) ^ 0x80808080u;
-}
-
-// Codes 4t .. 4t + 3 of sub-block s (0..7) of a half, as centered int8.
-__device__ __forceinline__ uint32_t codes_of(const uint32_t (&ql)[4], const uint32_t (&qh)[2], int s) {
-  const uint32_t lo = (s < 4 ? ql[s] : ql[s - 4] >> 4) & 0x0F0F0F0Fu;
-  const uint32_t hi = ((qh[s & 1] >> (2 * (s >> 1))) & 0x03030303u) << 4;
-  return centered(lo | hi);
-}
-
-// D = A (16x16 s8, row) * B (16x8 s8, col), int32, fresh accumulator.
-__device__ __forceinline__ void mma16816(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
-      "{%7, %7, %7, %7};"
-      : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0), "r"(0));
-}
-
-// One lane's share of a super-block of its two rows: ql / qh words of both
-// halves, the 16 sub-block scales and d.
-struct SbWords {
-  uint32_t ql[2][2][4];  // [row][half][word]
-  uint32_t qh[2][2][2];
-  uint4 sc[2];
-  uint16_t d[2];
+struct Geo {  // byte offsets of one stage's regions and the stage size, for R rows
+  int sc, d, stage;
 };
+__host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
+__host__ __device__ inline Geo stage_geo(int R) {
+  Geo g;
+  g.sc = align128(R * kQPitch);
+  g.d = align128(g.sc + R * kScPitch);
+  g.stage = align128(g.d + R * kDPitch);
+  return g;
+}
+size_t smem_bytes(int R) { return 1024 + (size_t)kNS * stage_geo(R).stage + kRedBytes + 256; }
 
-__device__ __forceinline__ void load_sb(SbWords& w, const uint8_t* const (&q)[2],
-                                        const int8_t* const (&sc)[2], const uint16_t* const (&d)[2],
-                                        int sb, int t) {
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint8_t* hb = q[r] + (size_t)sb * 192 + 96 * h + 4 * t;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) w.ql[r][h][j] = ldg32(hb + 16 * j);
-      w.qh[r][h][0] = ldg32(hb + 64);
-      w.qh[r][h][1] = ldg32(hb + 80);
-    }
-    w.sc[r] = __ldg(reinterpret_cast<const uint4*>(sc[r] + 16 * sb));
-    w.d[r] = __ldg(d[r] + sb);
-  }
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
 }
 
-__device__ __forceinline__ int sc_byte(const uint4 v, int i) {
-  const uint32_t w = i < 4 ? v.x : i < 8 ? v.y : i < 12 ? v.z : v.w;
-  return (int)(int8_t)(w >> (8 * (i & 3)));
+__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t h2(float v) {  // (v, v) as f16x2 (v exact in f16)
+  const uint32_t h = __half_as_ushort(__float2half_rn(v));
+  return h | (h << 16);
+}
+
+// The four 6-bit codes (one per byte) of sub-block j (0..7 of a half) at this
+// lane's positions: the low (j < 4) or high nibbles of ql word w and the
+// 2-bit field j / 2 of qh word q, moved to bits 4-5.
+__device__ __forceinline__ uint32_t codes(uint32_t w, uint32_t q, int j) {
+  const uint32_t lo = (j < 4 ? w : w >> 4) & 0x0F0F0F0Fu;
+  const int f = j >> 1;
+  const uint32_t hi = (f < 2 ? q << (4 - 2 * f) : q >> (2 * f - 4)) & 0x30303030u;
+  return lo | hi;
+}
+// Codes of bytes (kOdd, kOdd + 2) of `code` as the binary16 pair code - 32:
+// 1024 + code (exponent byte 0x64 placed above each code byte) minus 1056.
+template <int kOdd>
+__device__ __forceinline__ uint32_t code_pair(uint32_t code) {
+  const uint32_t v = __byte_perm(code, 0x64u, kOdd ? 0x4341u : 0x4240u);
+  return hsub2u(v, h2(1056.0f));
+}
+// Activations (-127..127) of bytes (kOdd, kOdd + 2) of w as binary16 pairs,
+// given wb = w ^ 0x80808080 (x + 128 as unsigned bytes): 1024 + (x + 128) - 1152.
+template <int kOdd>
+__device__ __forceinline__ uint32_t x_pair(uint32_t wb) {
+  return hsub2u(__byte_perm(wb, 0x64u, kOdd ? 0x4341u : 0x4240u), h2(1152.0f));
+}
+
+// D = A (16x16 f16, row) * B (16x8 f16, col) + C, f32.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float sc_of(const uint4& v, int s) {  // signed byte s of 16
+  const uint32_t w = s < 4 ? v.x : s < 8 ? v.y : s < 12 ? v.z : v.w;
+  return (float)(int)(int8_t)(w >> (8 * (s & 3)));
+}
+
+__device__ __forceinline__ void bar_consumers() {  // the kCW consumer warps only
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kCW) : "memory");
 }
 
 template <int kNT, bool kPartials>
-__global__ void __launch_bounds__(kWarps * 32, 2) mmq_skinny_mma_kernel(
-    const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
-    const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
-    int32_t* __restrict__ partials) {
-  __shared__ float red[kWarps][16][17];  // [warp][row][token] partial sums
+__global__ void __launch_bounds__(kThreads, 1)
+    mmq_skinny_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
+                          const __grid_constant__ CUtensorMap tmD, int M, int K, int N, int R,
+                          int units, const int8_t* __restrict__ Xq, const float* __restrict__ da,
+                          int ldda, float* __restrict__ Y, int ldy, int32_t* __restrict__ partials,
+                          unsigned int* __restrict__ status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const Geo geo = stage_geo(R);
+  float* red = reinterpret_cast<float*>(smem + (size_t)kNS * geo.stage);  // [kSbs][kMaxR][16]
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
+  uint64_t* empty = full + kNS;
+  int* abort_word = reinterpret_cast<int*>(empty + kNS);
+  volatile int* abort_flag = abort_word;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, t = lane & 3;
-  const int nsb = K / 256, nc = K / 32;
-  const int ntiles = (M + 15) / 16;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int m0 = 16 * tile;
-    int rows[2];
-    const uint8_t* q[2];
-    const int8_t* scp[2];
-    const uint16_t* dp[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      rows[r] = m0 + gq + 8 * r;
-      const int rr = rows[r] < M ? rows[r] : M - 1;  // a row past the end reads row M-1, unused
-      q[r] = plane + g.qlh_off + (size_t)rr * g.qlh_row;
-      scp[r] = reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)rr * (K / 16);
-      dp[r] = reinterpret_cast<const uint16_t*>(plane + g.d_off + (size_t)rr * g.d_row);
-    }
-    float acc[2][2 * kNT];  // [row][2 nt + j]: tokens 8 nt + 2t + j
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int i = 0; i < 2 * kNT; ++i) acc[r][i] = 0.0f;
+  const int nsb = K / 256, nst = (nsb + kSbs - 1) / kSbs, nc = K / 32;
 
-    SbWords cur, nxt;
-    if (warp < nsb) load_sb(cur, q, scp, dp, warp, t);
-    for (int sb = warp; sb < nsb; sb += kWarps) {
-      if (sb + kWarps < nsb) load_sb(nxt, q, scp, dp, sb + kWarps, t);  // in flight meanwhile
-      const float dr[2] = {__half2float(__ushort_as_half(cur.d[0])),
-                           __half2float(__ushort_as_half(cur.d[1]))};
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kCW);
+    }
+    *abort_word = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kCW) {
+    // ----------------------------------------------------------- producer --
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmS);
+      tma_prefetch_desc(&tmD);
+      const uint32_t tx = (uint32_t)R * (kQPitch + kScPitch + kDPitch);
+      int gs = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        for (int st = 0; st < nst; ++st, ++gs) {
+          const int slot = gs % kNS;
+          if (!(ok = mbar_wait_bounded(&empty[slot], ((gs / kNS) & 1) ^ 1, abort_flag, status,
+                                       kSiteEmpty)))
+            break;
+          uint8_t* b = smem + (size_t)slot * geo.stage;
+          mbar_arrive_expect_tx(&full[slot], tx);
+          tma_load_2d(b, &tmQ, &full[slot], 192 * st, u * R);
+          tma_load_2d(b + geo.sc, &tmS, &full[slot], 16 * st, u * R);
+          tma_load_2d(b + geo.d, &tmD, &full[slot], 2 * st, u * R);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA exits
+        volatile int no_abort = 0;
+        for (int k = (gs > kNS ? gs - kNS : 0); k < gs; ++k)
+          mbar_wait_bounded(&full[k % kNS], (k / kNS) & 1, &no_abort, status, kSiteFull);
+      }
+    }
+    return;
+  }
+
+  // --------------------------------------------------------------- consumers --
+  // warp (sbw, g): super-block sbw of every stage, rows 16g .. 16g + 15 of the unit
+  const int sbw = warp % kSbs, g = warp / kSbs;
+  const int gq = lane >> 2, t = lane & 3;
+  const int ra = 16 * g + gq, rb = ra + 8;  // this lane's two rows (unit-relative)
+  const bool have_a = ra < R, have_b = rb < R, active = 16 * g < R;
+  int gs = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int r0 = u * R;
+    float acc[kNT][4];
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        int S[2][2 * kNT];
+    for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+
+    for (int st = 0; st < nst; ++st, ++gs) {
+      const int slot = gs % kNS;
+      if (ok) ok = mbar_wait_warp(&full[slot], (gs / kNS) & 1, abort_flag, status, kSiteFull);
+      const int sb = kSbs * st + sbw;
+      if (ok && active && sb < nsb) {
+        const uint8_t* b = smem + (size_t)slot * geo.stage;
+        // this lane's ql / qh words of rows ra, rb: [row][half][word]
+        uint32_t ql[2][2][4], qh[2][2][2];
+        const uint8_t* pa = b + (size_t)ra * kQPitch + 192 * sbw + 4 * t;
+        const uint8_t* pb = b + (size_t)rb * kQPitch + 192 * sbw + 4 * t;
 #pragma unroll
-          for (int i = 0; i < 2 * kNT; ++i) S[r][i] = 0;
+        for (int h = 0; h < 2; ++h) {
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int s16 = 2 * c8 + e, h = s16 >> 3, s = s16 & 7;
-          const uint32_t a0 = codes_of(cur.ql[0][h], cur.qh[0][h], s);
-          const uint32_t a1 = codes_of(cur.ql[1][h], cur.qh[1][h], s);
-          const int sc0 = sc_byte(cur.sc[0], s16), sc1 = sc_byte(cur.sc[1], s16);
-          const int k0 = 256 * sb + 16 * s16 + 4 * t;
+          for (int j = 0; j < 4; ++j) {
+            ql[0][h][j] = have_a ? lds32(pa + 96 * h + 16 * j) : 0u;
+            ql[1][h][j] = have_b ? lds32(pb + 96 * h + 16 * j) : 0u;
+          }
 #pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) {
-            const int tok = 8 * nt + gq;
-            const uint32_t b =
-                tok < N ? __ldg(reinterpret_cast<const unsigned int*>(Xq + (size_t)tok * K + k0)) : 0u;
-            int d[4];
-            mma16816(d, a0, a1, b);
-            S[0][2 * nt] += sc0 * d[0];
-            S[0][2 * nt + 1] += sc0 * d[1];
-            S[1][2 * nt] += sc1 * d[2];
-            S[1][2 * nt + 1] += sc1 * d[3];
+          for (int j = 0; j < 2; ++j) {
+            qh[0][h][j] = have_a ? lds32(pa + 96 * h + 64 + 16 * j) : 0u;
+            qh[1][h][j] = have_b ? lds32(pb + 96 * h + 64 + 16 * j) : 0u;
           }
         }
-        const int c = 8 * sb + c8;
+        const uint4 sca4 = have_a ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)ra * kScPitch + 16 * sbw)
+                                  : make_uint4(0, 0, 0, 0);
+        const uint4 scb4 = have_b ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)rb * kScPitch + 16 * sbw)
+                                  : make_uint4(0, 0, 0, 0);
+        const float da_row = have_a ? __half2float(*reinterpret_cast<const __half*>(
+                                          b + geo.d + (size_t)ra * kDPitch + 2 * sbw))
+                                    : 0.0f;
+        const float db_row = have_b ? __half2float(*reinterpret_cast<const __half*>(
+                                          b + geo.d + (size_t)rb * kDPitch + 2 * sbw))
+                                    : 0.0f;
+        float sbs[kNT][4];
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const int tok = 8 * nt + 2 * t + j;
-            if (tok < N) {
-              const float dav = __ldg(da + (size_t)c * ldda + tok);
+          for (int i = 0; i < 4; ++i) sbs[nt][i] = 0.0f;
+
+        // activation words of a chunk (two sub-blocks, each token group),
+        // loaded one chunk ahead of their use
+        auto load_x = [&](int c8, uint32_t (&xw)[2][kNT]) {
 #pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                acc[r][2 * nt + j] = fmaf(dr[r] * dav, (float)S[r][2 * nt + j], acc[r][2 * nt + j]);
-                if (kPartials && rows[r] < M)
-                  partials[((size_t)tok * M + rows[r]) * (size_t)nc + c] = S[r][2 * nt + j];
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+              const int tok = 8 * nt + gq;
+              xw[e][nt] = tok < N ? __ldg(reinterpret_cast<const unsigned int*>(
+                                        Xq + (size_t)tok * K + 256 * sb + 32 * c8 + 16 * e + 4 * t))
+                                  : 0u;
+            }
+        };
+        uint32_t xcur[2][kNT], xnxt[2][kNT];
+        load_x(0, xcur);
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const int c = 8 * sb + c8;  // chunk
+          if (c8 < 7) load_x(c8 + 1, xnxt);
+          float S[kNT][4];
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) S[nt][i] = 0.0f;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int s16 = 2 * c8 + e, h = s16 >> 3, j = s16 & 7;
+            uint32_t a[4];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const uint32_t code = codes(ql[rr][h][j & 3], qh[rr][h][j & 1], j);
+              a[rr] = code_pair<0>(code);      // codes 4t, 4t + 2
+              a[2 + rr] = code_pair<1>(code);  // codes 4t + 1, 4t + 3
+            }
+            const float sa = sc_of(sca4, s16), sbv = sc_of(scb4, s16);
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) {
+              const uint32_t wb = xcur[e][nt] ^ 0x80808080u;
+              float P[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+              mma_f16(P, a, x_pair<0>(wb), x_pair<1>(wb));
+              // sc * P and their sum over the chunk are exact in f32 (< 2^24)
+              S[nt][0] = fmaf(sa, P[0], S[nt][0]);
+              S[nt][1] = fmaf(sa, P[1], S[nt][1]);
+              S[nt][2] = fmaf(sbv, P[2], S[nt][2]);
+              S[nt][3] = fmaf(sbv, P[3], S[nt][3]);
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < kNT; ++nt) {
+            const int t0 = 8 * nt + 2 * t;
+            const float d0 = t0 < N ? __ldg(da + (size_t)c * ldda + t0) : 0.0f;
+            const float d1 = t0 + 1 < N ? __ldg(da + (size_t)c * ldda + t0 + 1) : 0.0f;
+            sbs[nt][0] = fmaf(d0, S[nt][0], sbs[nt][0]);
+            sbs[nt][1] = fmaf(d1, S[nt][1], sbs[nt][1]);
+            sbs[nt][2] = fmaf(d0, S[nt][2], sbs[nt][2]);
+            sbs[nt][3] = fmaf(d1, S[nt][3], sbs[nt][3]);
+            if (kPartials) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int rl = (i < 2) ? ra : rb, tk = t0 + (i & 1);
+                if (rl < R && r0 + rl < M && tk < N)
+                  partials[((size_t)tk * M + r0 + rl) * (size_t)nc + c] = (int32_t)S[nt][i];
               }
             }
           }
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt) xcur[e][nt] = xnxt[e][nt];
+        }
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          acc[nt][0] = fmaf(da_row, sbs[nt][0], acc[nt][0]);
+          acc[nt][1] = fmaf(da_row, sbs[nt][1], acc[nt][1]);
+          acc[nt][2] = fmaf(db_row, sbs[nt][2], acc[nt][2]);
+          acc[nt][3] = fmaf(db_row, sbs[nt][3], acc[nt][3]);
+        }
       }
-      cur = nxt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
     }
-    // the eight warps' partial sums of the tile, added in a fixed order
+
+    // the eight super-block warps' sums of each row, added in a fixed order
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
+    for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
+      for (int i = 0; i < 4; ++i) {
+        const int row = (i < 2) ? ra : rb, tk = 8 * nt + 2 * t + (i & 1);
+        red[(sbw * kMaxR + row) * 16 + tk] = acc[nt][i];
+      }
+    bar_consumers();
+    if (ok) {
+      for (int i = threadIdx.x; i < 16 * R; i += 32 * kCW) {
+        const int tk = i / R, row = i - tk * R;
+        if (tk < N && tk < 8 * kNT && r0 + row < M) {
+          float y = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) red[warp][gq + 8 * r][8 * nt + 2 * t + j] = acc[r][2 * nt + j];
-    __syncthreads();
-    {
-      const int row = threadIdx.x >> 4, tok = threadIdx.x & 15;
-      if (tok < N && tok < 8 * kNT && m0 + row < M) {
-        float y = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) y += red[w][row][tok];
-        Y[(size_t)tok * ldy + m0 + row] = y;
+          for (int w = 0; w < kSbs; ++w) y += red[(w * kMaxR + row) * 16 + tk];
+          Y[(size_t)tk * ldy + r0 + row] = y;
+        }
       }
     }
-    __syncthreads();
+    bar_consumers();
   }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_fn = nullptr;
+std::once_flag g_encode_once;
+
+CUresult encode(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode_fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 template <int kNT, bool P>
-cudaError_t launch_nt(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
-                      const float* da, int ldda, int N, float* Y, int ldy, int32_t* partials,
+cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
+                      int ldda, int N, float* Y, int ldy, int32_t* partials, unsigned int* status,
                       cudaStream_t s) {
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mmq_skinny_mma_kernel<kNT, P>,
-                                                         kWarps * 32, 0)))
-    return e;
-  const long long tiles = (M + 15) / 16, cap = (long long)sms * (per_sm > 0 ? per_sm : 1);
-  const unsigned blocks = (unsigned)(tiles < cap ? tiles : cap);
-  mmq_skinny_mma_kernel<kNT, P><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y,
-                                                               ldy, partials);
+  // R rows per unit, at most kMaxR, units in whole waves over the SMs
+  const long long waves = ((long long)M + (long long)kMaxR * sms - 1) / ((long long)kMaxR * sms);
+  const int R = (int)(((long long)M + waves * sms - 1) / (waves * sms));
+  const int units = (M + R - 1) / R;
+  const PlaneGeom g = plane_geom(M, K);
+  CUtensorMap mq, ms, md;
+  if (!g_encode_fn) return cudaErrorInitializationError;
+  if (encode(&mq, plane + g.qlh_off, g.qlh_row / 8, (uint64_t)M, g.qlh_row, kQPitch / 8,
+             (uint32_t)R) != CUDA_SUCCESS ||
+      encode(&ms, plane + g.sc_off, (uint64_t)K / 128, (uint64_t)M, (uint64_t)K / 16, kScPitch / 8,
+             (uint32_t)R) != CUDA_SUCCESS ||
+      encode(&md, plane + g.d_off, g.d_row / 8, (uint64_t)M, g.d_row, kDPitch / 8, (uint32_t)R) !=
+          CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  const unsigned grid = (unsigned)(units < sms ? units : sms);
+  mmq_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R), s>>>(
+      mq, ms, md, M, K, N, R, units, Xq, da, ldda, Y, ldy, partials, status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// Raises the dynamic shared-memory limit of every instantiation and looks up
+// the tensor-map encoder; once per device.
+cudaError_t mmq_skinny_mma_prepare() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode_fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode_fn) return cudaErrorInitializationError;
+  const int bytes = (int)smem_bytes(kMaxR);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<1, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<1, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<2, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
+    return e;
+  return cudaFuncSetAttribute(mmq_skinny_mma_kernel<2, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8_t* Xq,
                                   const float* da, int ldda, int N, float* Y, int ldy,
-                                  int32_t* partials, cudaStream_t s) {
-  const PlaneGeom g = plane_geom(M, K);
+                                  int32_t* partials, unsigned int* status, cudaStream_t s) {
   if (N <= 8)
-    return partials ? launch_nt<1, true>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s)
-                    : launch_nt<1, false>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
-  return partials ? launch_nt<2, true>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s)
-                  : launch_nt<2, false>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+    return partials ? launch_nt<1, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, partials, status, s)
+                    : launch_nt<1, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, nullptr, status, s);
+  return partials ? launch_nt<2, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, partials, status, s)
+                  : launch_nt<2, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, nullptr, status, s);
 }
 
 }  // namespace q6

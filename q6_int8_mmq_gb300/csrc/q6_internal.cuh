@@ -49,10 +49,12 @@ cudaError_t launch_pack(const uint8_t* raw, int M, int K, uint8_t* plane, int8_t
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
                               unsigned int* status, cudaStream_t s);
-// The same product on the warp-level int8 tensor path (mmq_skinny_mma.cu).
+// The same product for 2 <= N <= 16 on the warp-level f16 tensor path with
+// TMA-staged weights (mmq_skinny_mma.cu).
 cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8_t* Xq,
                                   const float* da, int ldda, int N, float* Y, int ldy,
-                                  int32_t* partials, cudaStream_t s);
+                                  int32_t* partials, unsigned int* status, cudaStream_t s);
+cudaError_t mmq_skinny_mma_prepare();
 cudaError_t mmq_skinny_prepare();
 cudaError_t launch_mmq_sync(const uint8_t* plane, const int8_t* wexp, int M, int K,
                             const int8_t* Xq, const float* da, int ldda, int N, float* Y, int ldy,

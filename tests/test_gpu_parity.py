@@ -213,8 +213,10 @@ def test_pack_bitexact(q6, orc, M, K):
 
 SMALL = [
     # (M, K, N) spanning tiles and ragged tails of both kernels
-    (256, 512, 1), (256, 512, 4), (256, 512, 8), (200, 768, 16),      # skinny kernel
-    (257, 512, 3), (129, 768, 16),                                    # odd M: two-row warps
+    (256, 512, 1), (256, 512, 4), (256, 512, 8), (200, 768, 16),      # skinny kernels
+    (257, 512, 3), (129, 768, 16), (131, 2816, 2), (1000, 2560, 5),  # odd M, partial stages
+    (3001, 768, 9),   # 20-row units: a partial second row group, a one-row last unit
+    (5000, 512, 16),  # more units than SMs: CTAs take two units each
     (128, 256, 17), (256, 512, 128), (200, 512, 129), (384, 768, 300),  # tensor-core kernel
     (130, 1024, 255), (64, 256, 40),
 ]
