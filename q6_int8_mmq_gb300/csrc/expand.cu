@@ -18,7 +18,7 @@
 // operand give the integer sum of sc * v * xq of a sub-block.
 //
 // Both kernels are bandwidth-bound (0.81 or 1.06 bytes read and 4 written per
-// weight).
+// weight); each warp's stores cover whole 512-byte runs.
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -49,80 +49,66 @@ __device__ __forceinline__ void i8_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi
   hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
-// o[8] (sixteen binary16 v) -> W_hi and W_lo runs of one sub-block.
-__device__ __forceinline__ void store_folded(const uint32_t (&o)[8], int sc, __half* hi, __half* lo) {
+// o[4] (eight binary16 v of one sub-block) -> 16 bytes of W_hi and of W_lo.
+__device__ __forceinline__ void store_folded8(const uint32_t (&o)[4], int sc, __half* hi, __half* lo) {
   const int sh = sc >> 4, sl = sc & 15;  // arithmetic shift: floor(sc / 16)
   const __half2 fh = __half2half2(__int2half_rn(16 * sh));
   const __half2 fl = __half2half2(__int2half_rn(sl));
-  uint32_t h[8], l[8];
+  uint32_t h[4], l[4];
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
+  for (int w = 0; w < 4; ++w) {
     const __half2 v = *reinterpret_cast<const __half2*>(&o[w]);
     const __half2 a = __hmul2(v, fh), b = __hmul2(v, fl);
     h[w] = *reinterpret_cast<const uint32_t*>(&a);
     l[w] = *reinterpret_cast<const uint32_t*>(&b);
   }
-  uint4* dh = reinterpret_cast<uint4*>(hi);
-  uint4* dl = reinterpret_cast<uint4*>(lo);
-  dh[0] = make_uint4(h[0], h[1], h[2], h[3]);
-  dh[1] = make_uint4(h[4], h[5], h[6], h[7]);
-  dl[0] = make_uint4(l[0], l[1], l[2], l[3]);
-  dl[1] = make_uint4(l[4], l[5], l[6], l[7]);
+  *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// One thread per 32-element chunk (two sub-blocks of one half block): its
-// two 16-byte ql runs and the half block's 32 qh bytes are loaded together
-// before any conversion.
+// One warp per super-block, lane l owning its elements 8l .. 8l + 7 (half p =
+// l % 2 of sub-block s = l / 2), so that each 16-byte store of the warp lands
+// in one contiguous 512-byte run of W_hi or W_lo. A lane reads the 8 ql bytes
+// and the 8 qh bytes of its elements (sub-block s of half h = s / 8 is group
+// j = s % 8 of the element map) and the sub-block's scale.
 __global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restrict__ qlh,
                                                          const int8_t* __restrict__ sc, int M, int K,
                                                          size_t qlh_row, __half* __restrict__ wh) {
-  const int chunks = K / 32;
-  const long long items = (long long)M * chunks;
-  const long long stride = (long long)gridDim.x * blockDim.x;
+  const int nsb = K / 256;
+  const long long blocks = (long long)M * nsb;  // super-blocks
+  const long long wstride = (long long)gridDim.x * (blockDim.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int s = lane >> 1, p = lane & 1, h = s >> 3, j = s & 7;
+  const int nsh = 4 * (j >> 2), fsh = 2 * (j >> 1);
   const size_t plane = (size_t)M * K;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
-    const int m = (int)(i / chunks), c = (int)(i - (long long)m * chunks);
-    const int hb = c >> 2, g0 = 2 * (c & 3);  // half block, first group (even) within it
-    const uint8_t* src = qlh + (size_t)m * qlh_row + (size_t)hb * 96;
-    const uint4 La = __ldg(reinterpret_cast<const uint4*>(src + 16 * (g0 & 3)));
-    const uint4 Lb = __ldg(reinterpret_cast<const uint4*>(src + 16 * ((g0 + 1) & 3)));
-    const uint4 H0 = __ldg(reinterpret_cast<const uint4*>(src + 64));
-    const uint4 H1 = __ldg(reinterpret_cast<const uint4*>(src + 80));
-    const uint16_t s2 = __ldg(reinterpret_cast<const uint16_t*>(sc + 2 * i));
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int g = g0 + u;
-      const uint4 L = u ? Lb : La;
-      const uint4 H = (g & 1) ? H1 : H0;
-      const int nsh = 4 * (g >> 2), fsh = 2 * ((g >> 1) & 3);
-      const uint32_t Lw[4] = {L.x, L.y, L.z, L.w}, Hw[4] = {H.x, H.y, H.z, H.w};
-      uint32_t o[8];
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint32_t code = ((Lw[w] >> nsh) & 0x0F0F0F0Fu) | (((Hw[w] >> fsh) & 0x03030303u) << 4);
-        codes_to_f16(code, o[2 * w], o[2 * w + 1]);
-      }
-      const int scv = (int)(int8_t)(u ? (s2 >> 8) : (s2 & 0xFF));
-      const size_t off = (size_t)m * K + (size_t)(2 * c + u) * 16;
-      store_folded(o, scv, wh + off, wh + plane + off);
-    }
+  for (long long b = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < blocks;
+       b += wstride) {
+    const int m = (int)(b / nsb), sb = (int)(b - (long long)m * nsb);
+    const uint8_t* src = qlh + (size_t)m * qlh_row + (size_t)sb * 192 + 96 * h;
+    const uint2 L = __ldg(reinterpret_cast<const uint2*>(src + 16 * (j & 3) + 8 * p));
+    const uint2 H = __ldg(reinterpret_cast<const uint2*>(src + 64 + 16 * (j & 1) + 8 * p));
+    const int scv = __ldg(sc + (size_t)m * (K / 16) + 16 * sb + s);
+    uint32_t o[4];
+    codes_to_f16(((L.x >> nsh) & 0x0F0F0F0Fu) | (((H.x >> fsh) & 0x03030303u) << 4), o[0], o[1]);
+    codes_to_f16(((L.y >> nsh) & 0x0F0F0F0Fu) | (((H.y >> fsh) & 0x03030303u) << 4), o[2], o[3]);
+    const size_t off = (size_t)m * K + (size_t)sb * 256 + 8 * lane;
+    store_folded8(o, scv, wh + off, wh + plane + off);
   }
 }
 
+// The same from the W_exp plane: one thread per eight elements.
 __global__ void __launch_bounds__(256) expand_wexp_kernel(const int8_t* __restrict__ wexp,
-                                                          const int8_t* __restrict__ sc, long long n16,
+                                                          const int8_t* __restrict__ sc, long long n8,
                                                           __half* __restrict__ wh) {
   const long long stride = (long long)gridDim.x * blockDim.x;
-  const size_t plane = (size_t)n16 * 16;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(wexp) + i);
-    const int s = __ldg(sc + i);
-    uint32_t o[8];
+  const size_t plane = (size_t)n8 * 8;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(wexp) + i);
+    const int s = __ldg(sc + (i >> 1));
+    uint32_t o[4];
     i8_to_f16(v.x, o[0], o[1]);
     i8_to_f16(v.y, o[2], o[3]);
-    i8_to_f16(v.z, o[4], o[5]);
-    i8_to_f16(v.w, o[6], o[7]);
-    store_folded(o, s, wh + 16 * (size_t)i, wh + plane + 16 * (size_t)i);
+    store_folded8(o, s, wh + 8 * (size_t)i, wh + plane + 8 * (size_t)i);
   }
 }
 
@@ -136,7 +122,7 @@ unsigned grid_for(long long items) {
 
 cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
-  expand_raw_kernel<<<grid_for((long long)M * (K / 32)), 256, 0, s>>>(
+  expand_raw_kernel<<<grid_for((long long)M * (K / 256) * 32), 256, 0, s>>>(
       plane + g.qlh_off, reinterpret_cast<const int8_t*>(plane + g.sc_off), M, K, g.qlh_row, wh);
   return cudaGetLastError();
 }
@@ -144,9 +130,9 @@ cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cu
 cudaError_t launch_expand_wexp(const int8_t* wexp, const uint8_t* plane, int M, int K, __half* wh,
                                cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
-  const long long n16 = (long long)M * K / 16;
-  expand_wexp_kernel<<<grid_for(n16), 256, 0, s>>>(
-      wexp, reinterpret_cast<const int8_t*>(plane + g.sc_off), n16, wh);
+  const long long n8 = (long long)M * K / 8;
+  expand_wexp_kernel<<<grid_for(n8), 256, 0, s>>>(
+      wexp, reinterpret_cast<const int8_t*>(plane + g.sc_off), n8, wh);
   return cudaGetLastError();
 }
 

@@ -7,6 +7,8 @@
 // xq = 0. The per-32 activation scale is the one the q6_K rescale consumes
 // ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2); the pages print no
 // quantiser, so the division and the rounding are IEEE f32 and half-away.
+// The kernels reach exactly those codes with one multiply by the reciprocal
+// per element, falling back to the division next to rounding ties (qfast).
 //
 // HBM-bound: 4 bytes read and 3 written per element (plus 4 per 32 for da).
 #include "q6_internal.cuh"
@@ -20,23 +22,61 @@ __device__ __forceinline__ int quant1(float x, float d) {
   return (int)fminf(fmaxf(r, -127.0f), 127.0f);
 }
 
-// Eight elements of one row -> their int8 codes (as two words) and binary16 values.
-__device__ __forceinline__ void quant8(const float4 v0, const float4 v1, float d, uint2& q8,
-                                       uint4& h8) {
-  const int q0 = quant1(v0.x, d), q1 = quant1(v0.y, d), q2 = quant1(v0.z, d), q3 = quant1(v0.w, d);
-  const int q4 = quant1(v1.x, d), q5 = quant1(v1.y, d), q6 = quant1(v1.z, d), q7 = quant1(v1.w, d);
-  q8.x = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
-         ((uint32_t)(q3 & 0xFF) << 24);
-  q8.y = (uint32_t)(q4 & 0xFF) | ((uint32_t)(q5 & 0xFF) << 8) | ((uint32_t)(q6 & 0xFF) << 16) |
-         ((uint32_t)(q7 & 0xFF) << 24);
-  const __half2 h01 = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
-  const __half2 h23 = __halves2half2(__int2half_rn(q2), __int2half_rn(q3));
-  const __half2 h45 = __halves2half2(__int2half_rn(q4), __int2half_rn(q5));
-  const __half2 h67 = __halves2half2(__int2half_rn(q6), __int2half_rn(q7));
-  h8.x = *reinterpret_cast<const uint32_t*>(&h01);
-  h8.y = *reinterpret_cast<const uint32_t*>(&h23);
-  h8.z = *reinterpret_cast<const uint32_t*>(&h45);
-  h8.w = *reinterpret_cast<const uint32_t*>(&h67);
+// The code of x in a block with a normal scale d, given r = 1/d correctly
+// rounded. With |x| <= amax and d = amax/127 rounded, |x / d| <= 127.00001,
+// and q = x * r differs from the correctly rounded quotient x / d by at most
+// 2^-15.6 (two roundings of relative size 2^-24 each, plus half an ulp of the
+// quotient). So unless q lies within 2^-14 of a rounding tie both round to
+// the same integer, by any rounding rule: the code is rint(q). Near a tie
+// `near` is set and the caller takes the exact division.
+__device__ __forceinline__ float qfast(float x, float r, bool& near) {
+  const float q = x * r;
+  const float n = rintf(q);
+  near |= !(fabsf(q - n) < 0.5f - 0x1p-14f);
+  return n;
+}
+
+// Eight elements of one block -> their codes as floats (exact integers), the
+// fast way when possible and by the exact division otherwise.
+__device__ __forceinline__ void quant8f(const float4 v0, const float4 v1, float d, float r,
+                                        float (&n)[8]) {
+  const float x[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  bool near = !(d >= 0x1p-126f);  // zero or subnormal scale: the exact path
+#pragma unroll
+  for (int i = 0; i < 8; ++i) n[i] = qfast(x[i], r, near);
+  if (near) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) n[i] = (float)quant1(x[i], d);
+  }
+}
+
+// Codes (floats, -127..127) -> binary16 pairs, and -> int8 bytes through the
+// binary16 bits of code + 1152 (0x64 above the byte code + 128).
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  const __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_q4(uint32_t h01, uint32_t h23) {
+  const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+  const __half2 a = __hadd2(*reinterpret_cast<const __half2*>(&h01), bias);
+  const __half2 b = __hadd2(*reinterpret_cast<const __half2*>(&h23), bias);
+  const uint32_t ua = *reinterpret_cast<const uint32_t*>(&a);
+  const uint32_t ub = *reinterpret_cast<const uint32_t*>(&b);
+  return __byte_perm(ua, ub, 0x6420) ^ 0x80808080u;
+}
+
+// Eight elements -> two words of int8 codes and four binary16 pairs.
+__device__ __forceinline__ void quant8(const float4 v0, const float4 v1, float d, float r,
+                                       uint2& q8, uint4& h8) {
+  float n[8];
+  quant8f(v0, v1, d, r, n);
+  h8 = make_uint4(pack_h2(n[0], n[1]), pack_h2(n[2], n[3]), pack_h2(n[4], n[5]),
+                  pack_h2(n[6], n[7]));
+  q8 = make_uint2(pack_q4(h8.x, h8.y), pack_q4(h8.z, h8.w));
+}
+
+__device__ __forceinline__ float recip_or_zero(float d) {
+  return d >= 0x1p-126f ? __frcp_rn(d) : 0.0f;
 }
 
 // Small inputs (a few tokens): each thread owns eight consecutive elements
@@ -62,7 +102,7 @@ __global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restri
     const float d = __fdiv_rn(a, 127.0f);
     uint2 q8;
     uint4 h8;
-    quant8(v0, v1, d, q8, h8);
+    quant8(v0, v1, d, recip_or_zero(d), q8, h8);
     if (Xq != nullptr) reinterpret_cast<uint2*>(Xq + (size_t)n * K)[j] = q8;
     if (Xh != nullptr) reinterpret_cast<uint4*>(Xh + (size_t)n * K)[j] = h8;
     if ((j & 3) == 0) da[(size_t)(j >> 2) * ldda + n] = d;
@@ -103,10 +143,11 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
     if (!on) continue;
     const float d = __fdiv_rn(a, 127.0f);
+    const float r = recip_or_zero(d);
     uint2 qa, qb;
     uint4 ha, hb;
-    quant8(v0, v1, d, qa, ha);
-    quant8(v2, v3, d, qb, hb);
+    quant8(v0, v1, d, r, qa, ha);
+    quant8(v2, v3, d, r, qb, hb);
     if (Xq != nullptr)
       reinterpret_cast<uint4*>(Xq + (size_t)n * K)[j] = make_uint4(qa.x, qa.y, qb.x, qb.y);
     if (Xh != nullptr) {

@@ -125,6 +125,36 @@ def test_quantize_bitexact(q6, orc, N, K, frac):
     quant_check(act, X, orc)
 
 
+@pytest.mark.parametrize("N,K", [(3, 256), (300, 1024)])
+def test_quantize_near_ties_and_tiny_scales(q6, orc, N, K):
+    """Quotients on, one ulp beside and a little beside rounding ties, where
+    the kernels leave the reciprocal for the exact division, and blocks whose
+    scale is subnormal (also taken exactly); bit-exact against the oracle."""
+    rng = np.random.default_rng(7 + N)
+    X = synth.activations(500 + N, N, K)
+    blocks = X.reshape(N, K // 32, 32)
+    kind = rng.integers(0, 4, size=blocks.shape[:2])
+    for n, c in zip(*np.nonzero(kind == 1)):
+        # amax 127 * s for a random power-of-two or odd scale s: the quotient
+        # of x = (k + 1/2) * s and its float neighbours straddle the tie
+        s = np.float32(rng.choice([1.0, 0.75, 3.0e-3, 17.0, 2.0 ** -20]))
+        k = rng.integers(-126, 126, size=32).astype(np.float32)
+        x = (k + np.float32(0.5)) * s
+        step = rng.integers(-3, 4, size=32)
+        x = np.array([np.nextafter(v, np.float32(np.inf) if d > 0 else np.float32(-np.inf))
+                      if d else v for v, d in zip(x, step)], dtype=np.float32)
+        x[0] = np.float32(127.0) * s
+        blocks[n, c] = x
+    for n, c in zip(*np.nonzero(kind == 2)):
+        blocks[n, c] *= np.float32(1e-40)        # subnormal amax and scale
+    for n, c in zip(*np.nonzero(kind == 3)):
+        blocks[n, c] *= np.float32(1e36)         # large values, normal scale
+    X = np.ascontiguousarray(blocks.reshape(N, K))
+    act = q6.quantize_act(dev(X))
+    q6.sync_status()
+    quant_check(act, X, orc)
+
+
 def test_quantize_without_xq_and_gemm(q6, orc):
     """A prefill caller may skip the int8 Xq: Xh and da are the same, the
     tensor-core GEMM runs on them, and the few-token kernels refuse such
