@@ -765,10 +765,14 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int8 dp4a -> f32",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 dp4a -> f32" if n == 1 else "f16 x f16 -> f32 (exact int6 x int8)",
         "data": "synthetic",
         "config": dict(skinny_config(args, M, K), weight_copies=R),
-        "roofline": {"bound": "hbm", "kernel": "mmq_skinny_kernel", "achieved": gbs, "peak": hbm,
+        "roofline": {"bound": "hbm",
+                     "kernel": ("mmq_skinny_kernel (dp4a)" if n == 1 else
+                                "mmq_skinny_mma_kernel (f16 mma.sync, TMA-staged weights)"),
+                     "achieved": gbs, "peak": hbm,
                      "unit": "GB/s", "frac": gbs / hbm, "peak_source": hbm_src,
                      "traffic": traffic,
                      "algorithmic": f"M*K*210/256 + N*K + N*K/8 + 4*N*M = {alg:.4g} B per launch"},
@@ -906,11 +910,14 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes (read + write) per launch from ncu captures of the current
-# kernels, keyed by (workload, kernel); the capture each figure comes from is
-# summarised under profiles/ (mmq_tc_ffn_down.md). An entry is removed when
-# its kernel changes.
-TRAFFIC = {("ffn_down", "mmq_tc"): 667.22e6 + 53.22e6}
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
+# ncu captures of the current kernels, keyed by (workload, kernel); the
+# captures are summarised under profiles/ (mmq_tc_ffn_down.md,
+# mmq_skinny_ffn_down_n1.md, mmq_skinny_mma_ffn_down_n16.md). An entry is
+# removed when its kernel changes.
+TRAFFIC = {("ffn_down", "mmq_tc"): 667.67e6 + 53.16e6,
+           ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
+           ("skinny_ffn_down_N16", "mmq_skinny"): 37.25e6 + 0.002e6}
 
 
 def main():
