@@ -31,9 +31,11 @@
 // Work: CTA u takes R consecutive weight rows (R = ceil(M / SMs) up to 32,
 // so every SM gets the same number of rows to within one) and all of K. A
 // producer thread streams stages of 8 super-blocks of those rows through a
-// 3-stage ring with three 2D TMA loads (qlh, sc, d); each row of a qlh stage
-// box is 1552 bytes (1536 plus 16 of the next stage), so that the 8 rows of
-// an A fragment fall on different shared-memory banks. Consumer warp (s, g)
+// ring of 2 or 3 stages (as many as shared memory holds) with 2D TMA loads:
+// qlh, sc and d of the rows, and the stage's 2048 activation bytes of every
+// token as two boxes of 1040-byte token rows. Each row of a qlh stage box is
+// 1552 bytes (1536 plus 16 of the next stage) and each activation row 1040,
+// so that the 8 rows of a fragment fall on different shared-memory banks. Consumer warp (s, g)
 // of 16 takes super-block s of every stage for rows 16g .. 16g + 15 of the
 // unit (16 warps, four per scheduler, hide the MMA and shared-memory
 // latencies), and the eight super-block warps' sums of a row are added in
@@ -51,27 +53,33 @@ namespace {
 constexpr int kSbs = 8;                  // super-blocks per stage
 constexpr int kCW = 2 * kSbs;            // consumer warps: super-block x row group of 16
 constexpr int kThreads = 32 * (kCW + 1);  // + one producer warp
-constexpr int kNS = 3;                   // ring stages
+constexpr int kMaxNS = 3;                // ring stages (2 or 3, by the shared-memory budget)
 constexpr int kMaxR = 32;                // rows per unit (two MMA row groups)
 constexpr int kQPitch = 1552;            // bytes per row of a qlh stage (194 x 8)
 constexpr int kScPitch = 144;            // bytes per row of an sc stage (18 x 8)
 constexpr int kDPitch = 16;              // bytes per row of a d stage (2 x 8)
+constexpr int kXPitch = 1040;            // bytes per token row of an activation half-stage (130 x 8)
+constexpr int kSmemBudget = 227 * 1024;
 constexpr int kRedBytes = kSbs * kMaxR * 16 * 4;
 
 enum : uint32_t { kSiteEmpty = 21, kSiteFull = 22 };
 
-struct Geo {  // byte offsets of one stage's regions and the stage size, for R rows
-  int sc, d, stage;
+struct Geo {  // byte offsets of one stage's regions and the stage size, for R rows, XR tokens
+  int sc, d, x0, x1, stage;
 };
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
-__host__ __device__ inline Geo stage_geo(int R) {
+__host__ __device__ inline Geo stage_geo(int R, int XR) {
   Geo g;
   g.sc = align128(R * kQPitch);
   g.d = align128(g.sc + R * kScPitch);
-  g.stage = align128(g.d + R * kDPitch);
+  g.x0 = align128(g.d + R * kDPitch);
+  g.x1 = align128(g.x0 + XR * kXPitch);
+  g.stage = align128(g.x1 + XR * kXPitch);
   return g;
 }
-size_t smem_bytes(int R) { return 1024 + (size_t)kNS * stage_geo(R).stage + kRedBytes + 256; }
+size_t smem_bytes(int R, int XR, int ns) {
+  return 1024 + (size_t)ns * stage_geo(R, XR).stage + kRedBytes + 256;
+}
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
@@ -132,24 +140,25 @@ __device__ __forceinline__ void bar_consumers() {  // the kCW consumer warps onl
 template <int kNT, bool kPartials>
 __global__ void __launch_bounds__(kThreads, 1)
     mmq_skinny_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
-                          const __grid_constant__ CUtensorMap tmD, int M, int K, int N, int R,
-                          int units, const int8_t* __restrict__ Xq, const float* __restrict__ da,
+                          const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
+                          int M, int K, int N, int R, int units, int ns, const float* __restrict__ da,
                           int ldda, float* __restrict__ Y, int ldy, int32_t* __restrict__ partials,
                           unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const Geo geo = stage_geo(R);
-  float* red = reinterpret_cast<float*>(smem + (size_t)kNS * geo.stage);  // [kSbs][kMaxR][16]
+  constexpr int XR = 8 * kNT;  // token rows of an activation stage
+  const Geo geo = stage_geo(R, XR);
+  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kMaxR][16]
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
-  uint64_t* empty = full + kNS;
-  int* abort_word = reinterpret_cast<int*>(empty + kNS);
+  uint64_t* empty = full + kMaxNS;
+  int* abort_word = reinterpret_cast<int*>(empty + kMaxNS);
   volatile int* abort_flag = abort_word;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsb = K / 256, nst = (nsb + kSbs - 1) / kSbs, nc = K / 32;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kNS; ++s) {
+    for (int s = 0; s < ns; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kCW);
     }
@@ -164,13 +173,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmS);
       tma_prefetch_desc(&tmD);
-      const uint32_t tx = (uint32_t)R * (kQPitch + kScPitch + kDPitch);
+      tma_prefetch_desc(&tmX);
+      const uint32_t tx = (uint32_t)R * (kQPitch + kScPitch + kDPitch) + 2u * (uint32_t)N * kXPitch;
       int gs = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         for (int st = 0; st < nst; ++st, ++gs) {
-          const int slot = gs % kNS;
-          if (!(ok = mbar_wait_bounded(&empty[slot], ((gs / kNS) & 1) ^ 1, abort_flag, status,
+          const int slot = gs % ns;
+          if (!(ok = mbar_wait_bounded(&empty[slot], ((gs / ns) & 1) ^ 1, abort_flag, status,
                                        kSiteEmpty)))
             break;
           uint8_t* b = smem + (size_t)slot * geo.stage;
@@ -178,13 +188,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(b, &tmQ, &full[slot], 192 * st, u * R);
           tma_load_2d(b + geo.sc, &tmS, &full[slot], 16 * st, u * R);
           tma_load_2d(b + geo.d, &tmD, &full[slot], 2 * st, u * R);
+          // the stage's 2048 activation bytes of each token, as two boxes of
+          // 1024 (+16) bytes per token row
+          tma_load_2d(b + geo.x0, &tmX, &full[slot], 256 * st, 0);
+          tma_load_2d(b + geo.x1, &tmX, &full[slot], 256 * st + 128, 0);
         }
       }
       if (!ok) {
         // let the copies already issued land before the CTA exits
         volatile int no_abort = 0;
-        for (int k = (gs > kNS ? gs - kNS : 0); k < gs; ++k)
-          mbar_wait_bounded(&full[k % kNS], (k / kNS) & 1, &no_abort, status, kSiteFull);
+        for (int k = (gs > ns ? gs - ns : 0); k < gs; ++k)
+          mbar_wait_bounded(&full[k % ns], (k / ns) & 1, &no_abort, status, kSiteFull);
       }
     }
     return;
@@ -207,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
 
     for (int st = 0; st < nst; ++st, ++gs) {
-      const int slot = gs % kNS;
-      if (ok) ok = mbar_wait_warp(&full[slot], (gs / kNS) & 1, abort_flag, status, kSiteFull);
+      const int slot = gs % ns;
+      if (ok) ok = mbar_wait_warp(&full[slot], (gs / ns) & 1, abort_flag, status, kSiteFull);
       const int sb = kSbs * st + sbw;
       if (ok && active && sb < nsb) {
         const uint8_t* b = smem + (size_t)slot * geo.stage;
@@ -245,18 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) sbs[nt][i] = 0.0f;
 
-        // activation words of a chunk (two sub-blocks, each token group),
-        // loaded one chunk ahead of their use
+        // activation words of a chunk (two sub-blocks, each token group) from
+        // the stage's activation boxes (tokens past N were filled with 0),
+        // read one chunk ahead of their use
+        const uint8_t* xs = b + (sbw < 4 ? geo.x0 : geo.x1) + 256 * (sbw & 3) + 4 * t;
         auto load_x = [&](int c8, uint32_t (&xw)[2][kNT]) {
 #pragma unroll
           for (int e = 0; e < 2; ++e)
 #pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) {
-              const int tok = 8 * nt + gq;
-              xw[e][nt] = tok < N ? __ldg(reinterpret_cast<const unsigned int*>(
-                                        Xq + (size_t)tok * K + 256 * sb + 32 * c8 + 16 * e + 4 * t))
-                                  : 0u;
-            }
+            for (int nt = 0; nt < kNT; ++nt)
+              xw[e][nt] = lds32(xs + (size_t)(8 * nt + gq) * kXPitch + 32 * c8 + 16 * e);
         };
         uint32_t xcur[2][kNT], xnxt[2][kNT];
         load_x(0, xcur);
@@ -378,18 +390,23 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
   const int R = (int)(((long long)M + waves * sms - 1) / (waves * sms));
   const int units = (M + R - 1) / R;
   const PlaneGeom g = plane_geom(M, K);
-  CUtensorMap mq, ms, md;
+  CUtensorMap mq, ms, md, mx;
   if (!g_encode_fn) return cudaErrorInitializationError;
+  // the activation boxes hold the N token rows (the rows past N in shared
+  // memory are never stored from)
   if (encode(&mq, plane + g.qlh_off, g.qlh_row / 8, (uint64_t)M, g.qlh_row, kQPitch / 8,
              (uint32_t)R) != CUDA_SUCCESS ||
       encode(&ms, plane + g.sc_off, (uint64_t)K / 128, (uint64_t)M, (uint64_t)K / 16, kScPitch / 8,
              (uint32_t)R) != CUDA_SUCCESS ||
       encode(&md, plane + g.d_off, g.d_row / 8, (uint64_t)M, g.d_row, kDPitch / 8, (uint32_t)R) !=
+          CUDA_SUCCESS ||
+      encode(&mx, Xq, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K, kXPitch / 8, (uint32_t)N) !=
           CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  mmq_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R), s>>>(
-      mq, ms, md, M, K, N, R, units, Xq, da, ldda, Y, ldy, partials, status);
+  mmq_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R, 8 * kNT, ns), s>>>(
+      mq, ms, md, mx, M, K, N, R, units, ns, da, ldda, Y, ldy, partials, status);
   return cudaGetLastError();
 }
 
@@ -407,7 +424,7 @@ cudaError_t mmq_skinny_mma_prepare() {
       g_encode_fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
   if (!g_encode_fn) return cudaErrorInitializationError;
-  const int bytes = (int)smem_bytes(kMaxR);
+  const int bytes = kSmemBudget;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<1, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
