@@ -54,7 +54,7 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_NONE 0    /* nothing to do (N == 0) */
 #define Q6_PATH_TC_RAW 1  /* unpack of the packed q6_K plane into the workspace + tensor-core GEMM */
 #define Q6_PATH_TC_WEXP 2 /* conversion of the W_exp plane into the workspace + tensor-core GEMM */
-#define Q6_PATH_SKINNY 3  /* CUDA-core kernel for N <= Q6_SKINNY_MAX_N on the packed q6_K plane */
+#define Q6_PATH_SKINNY 3  /* few-token kernel for N <= Q6_SKINNY_MAX_N on the packed q6_K plane */
 #define Q6_PATH_TC_WH 4   /* tensor-core GEMM on resident binary16 operand planes */
 #define Q6_PATH_SYNC_WEXP 5 /* legacy mma.sync int8 GEMM on the W_exp plane (q6k_mmq_mma_sync) */
 
@@ -160,8 +160,10 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *
  *   plane : packed weights from q6k_pack_weights (required).
  *   wexp, wh : the optional planes from q6k_pack_weights, or NULL.
- *   Xq, da: quantised activations (layouts above). Xq is read by the skinny
- *           kernel (N <= Q6_SKINNY_MAX_N).
+ *   Xq, da: quantised activations (layouts above). Xq is read by the
+ *           few-token kernels (N <= Q6_SKINNY_MAX_N: dp4a on the CUDA cores
+ *           for one token, exact f16 mma.sync for 2..16 tokens; both stream
+ *           the packed plane once).
  *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
  *   workspace : device scratch of at least q6k_mmq_workspace_bytes() bytes
  *           (4 * M * K, 256-byte aligned) when N > Q6_SKINNY_MAX_N and wh is

@@ -246,6 +246,7 @@ SMALL = [
     (256, 512, 1), (256, 512, 4), (256, 512, 8), (200, 768, 16),      # skinny kernels
     (257, 512, 3), (129, 768, 16), (131, 2816, 2), (1000, 2560, 5),  # odd M, partial stages
     (3001, 768, 9),   # 20-row units: a partial second row group, a one-row last unit
+    (48, 256, 6),     # one super-block per row, one row per unit
     (5000, 512, 16),  # more units than SMs: CTAs take two units each
     (128, 256, 17), (256, 512, 128), (200, 512, 129), (384, 768, 300),  # tensor-core kernel
     (130, 1024, 255), (64, 256, 40),
