@@ -32,8 +32,9 @@
 // so every SM gets the same number of rows to within one) and all of K. A
 // producer thread streams stages of 8 super-blocks of those rows through a
 // ring of 2 or 3 stages (as many as shared memory holds) with 2D TMA loads:
-// qlh, sc and d of the rows, and the stage's 2048 activation bytes of every
-// token as two boxes of 1040-byte token rows. Each row of a qlh stage box is
+// qlh, sc and d of the rows, the stage's 2048 activation bytes of every
+// token as two boxes of 1040-byte token rows, and the activation scales of
+// the stage's 64 chunks. Each row of a qlh stage box is
 // 1552 bytes (1536 plus 16 of the next stage) and each activation row 1040,
 // so that the 8 rows of a fragment fall on different shared-memory banks. Consumer warp (s, g)
 // of 16 takes super-block s of every stage for rows 16g .. 16g + 15 of the
@@ -65,7 +66,7 @@ constexpr int kRedBytes = kSbs * kMaxR * 16 * 4;
 enum : uint32_t { kSiteEmpty = 21, kSiteFull = 22 };
 
 struct Geo {  // byte offsets of one stage's regions and the stage size, for R rows, XR tokens
-  int sc, d, x0, x1, stage;
+  int sc, d, x0, x1, da, stage;
 };
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 __host__ __device__ inline Geo stage_geo(int R, int XR) {
@@ -74,7 +75,8 @@ __host__ __device__ inline Geo stage_geo(int R, int XR) {
   g.d = align128(g.sc + R * kScPitch);
   g.x0 = align128(g.d + R * kDPitch);
   g.x1 = align128(g.x0 + XR * kXPitch);
-  g.stage = align128(g.x1 + XR * kXPitch);
+  g.da = align128(g.x1 + XR * kXPitch);
+  g.stage = align128(g.da + 8 * kSbs * XR * 4);  // da of the stage's 64 chunks x XR tokens
   return g;
 }
 size_t smem_bytes(int R, int XR, int ns) {
@@ -90,10 +92,8 @@ __device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-__device__ __forceinline__ uint32_t h2(float v) {  // (v, v) as f16x2 (v exact in f16)
-  const uint32_t h = __half_as_ushort(__float2half_rn(v));
-  return h | (h << 16);
-}
+constexpr uint32_t kH2_1056 = 0x64206420u;  // (1056, 1056) as f16x2
+constexpr uint32_t kH2_1152 = 0x64806480u;  // (1152, 1152) as f16x2
 
 // The four 6-bit codes (one per byte) of sub-block j (0..7 of a half) at this
 // lane's positions: the low (j < 4) or high nibbles of ql word w and the
@@ -109,23 +109,22 @@ __device__ __forceinline__ uint32_t codes(uint32_t w, uint32_t q, int j) {
 template <int kOdd>
 __device__ __forceinline__ uint32_t code_pair(uint32_t code) {
   const uint32_t v = __byte_perm(code, 0x64u, kOdd ? 0x4341u : 0x4240u);
-  return hsub2u(v, h2(1056.0f));
+  return hsub2u(v, kH2_1056);
 }
 // Activations (-127..127) of bytes (kOdd, kOdd + 2) of w as binary16 pairs,
 // given wb = w ^ 0x80808080 (x + 128 as unsigned bytes): 1024 + (x + 128) - 1152.
 template <int kOdd>
 __device__ __forceinline__ uint32_t x_pair(uint32_t wb) {
-  return hsub2u(__byte_perm(wb, 0x64u, kOdd ? 0x4341u : 0x4240u), h2(1152.0f));
+  return hsub2u(__byte_perm(wb, 0x64u, kOdd ? 0x4341u : 0x4240u), kH2_1152);
 }
 
-// D = A (16x16 f16, row) * B (16x8 f16, col) + C, f32.
+// D = A (16x16 f16, row) * B (16x8 f16, col), f32, from a zero accumulator.
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ float sc_of(const uint4& v, int s) {  // signed byte s of 16
@@ -141,8 +140,8 @@ template <int kNT, bool kPartials>
 __global__ void __launch_bounds__(kThreads, 1)
     mmq_skinny_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
-                          int M, int K, int N, int R, int units, int ns, const float* __restrict__ da,
-                          int ldda, float* __restrict__ Y, int ldy, int32_t* __restrict__ partials,
+                          const __grid_constant__ CUtensorMap tmA, int M, int K, int N, int R, int units,
+                          int ns, int ldda, float* __restrict__ Y, int ldy, int32_t* __restrict__ partials,
                           unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -174,7 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmS);
       tma_prefetch_desc(&tmD);
       tma_prefetch_desc(&tmX);
-      const uint32_t tx = (uint32_t)R * (kQPitch + kScPitch + kDPitch) + 2u * (uint32_t)N * kXPitch;
+      tma_prefetch_desc(&tmA);
+      const uint32_t tx = (uint32_t)R * (kQPitch + kScPitch + kDPitch) + 2u * (uint32_t)N * kXPitch +
+                          (uint32_t)(8 * kSbs) * (uint32_t)ldda * 4u;
       int gs = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -192,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // 1024 (+16) bytes per token row
           tma_load_2d(b + geo.x0, &tmX, &full[slot], 256 * st, 0);
           tma_load_2d(b + geo.x1, &tmX, &full[slot], 256 * st + 128, 0);
+          // the activation scales of the stage's 64 chunks, [chunk][ldda]
+          tma_load_2d(b + geo.da, &tmA, &full[slot], 0, 64 * st);
         }
       }
       if (!ok) {
@@ -226,33 +229,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int sb = kSbs * st + sbw;
       if (ok && active && sb < nsb) {
         const uint8_t* b = smem + (size_t)slot * geo.stage;
-        // this lane's ql / qh words of rows ra, rb: [row][half][word]
-        uint32_t ql[2][2][4], qh[2][2][2];
+        // this lane's ql / qh words of rows ra, rb in the current half block
+        // (chunks 0-3 read half 0, chunks 4-7 half 1): [row][word]
+        uint32_t ql[2][4], qh[2][2];
         const uint8_t* pa = b + (size_t)ra * kQPitch + 192 * sbw + 4 * t;
         const uint8_t* pb = b + (size_t)rb * kQPitch + 192 * sbw + 4 * t;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        auto load_half = [&](int h) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            ql[0][h][j] = have_a ? lds32(pa + 96 * h + 16 * j) : 0u;
-            ql[1][h][j] = have_b ? lds32(pb + 96 * h + 16 * j) : 0u;
+            ql[0][j] = have_a ? lds32(pa + 96 * h + 16 * j) : 0u;
+            ql[1][j] = have_b ? lds32(pb + 96 * h + 16 * j) : 0u;
           }
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
-            qh[0][h][j] = have_a ? lds32(pa + 96 * h + 64 + 16 * j) : 0u;
-            qh[1][h][j] = have_b ? lds32(pb + 96 * h + 64 + 16 * j) : 0u;
+            qh[0][j] = have_a ? lds32(pa + 96 * h + 64 + 16 * j) : 0u;
+            qh[1][j] = have_b ? lds32(pb + 96 * h + 64 + 16 * j) : 0u;
           }
-        }
+        };
         const uint4 sca4 = have_a ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)ra * kScPitch + 16 * sbw)
                                   : make_uint4(0, 0, 0, 0);
         const uint4 scb4 = have_b ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)rb * kScPitch + 16 * sbw)
                                   : make_uint4(0, 0, 0, 0);
-        const float da_row = have_a ? __half2float(*reinterpret_cast<const __half*>(
-                                          b + geo.d + (size_t)ra * kDPitch + 2 * sbw))
-                                    : 0.0f;
-        const float db_row = have_b ? __half2float(*reinterpret_cast<const __half*>(
-                                          b + geo.d + (size_t)rb * kDPitch + 2 * sbw))
-                                    : 0.0f;
+        const float d_a = have_a ? __half2float(*reinterpret_cast<const __half*>(
+                                       b + geo.d + (size_t)ra * kDPitch + 2 * sbw))
+                                 : 0.0f;
+        const float d_b = have_b ? __half2float(*reinterpret_cast<const __half*>(
+                                       b + geo.d + (size_t)rb * kDPitch + 2 * sbw))
+                                 : 0.0f;
         float sbs[kNT][4];
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt)
@@ -275,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           const int c = 8 * sb + c8;  // chunk
+          if (c8 == 0 || c8 == 4) load_half(c8 >> 2);
           if (c8 < 7) load_x(c8 + 1, xnxt);
           float S[kNT][4];
 #pragma unroll
@@ -283,11 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) S[nt][i] = 0.0f;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int s16 = 2 * c8 + e, h = s16 >> 3, j = s16 & 7;
+            const int s16 = 2 * c8 + e, j = s16 & 7;
             uint32_t a[4];
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-              const uint32_t code = codes(ql[rr][h][j & 3], qh[rr][h][j & 1], j);
+              const uint32_t code = codes(ql[rr][j & 3], qh[rr][j & 1], j);
               a[rr] = code_pair<0>(code);      // codes 4t, 4t + 2
               a[2 + rr] = code_pair<1>(code);  // codes 4t + 1, 4t + 3
             }
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int nt = 0; nt < kNT; ++nt) {
               const uint32_t wb = xcur[e][nt] ^ 0x80808080u;
-              float P[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+              float P[4];
               mma_f16(P, a, x_pair<0>(wb), x_pair<1>(wb));
               // sc * P and their sum over the chunk are exact in f32 (< 2^24)
               S[nt][0] = fmaf(sa, P[0], S[nt][0]);
@@ -307,8 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             const int t0 = 8 * nt + 2 * t;
-            const float d0 = t0 < N ? __ldg(da + (size_t)c * ldda + t0) : 0.0f;
-            const float d1 = t0 + 1 < N ? __ldg(da + (size_t)c * ldda + t0 + 1) : 0.0f;
+            const float* sda = reinterpret_cast<const float*>(b + geo.da) + (8 * sbw + c8) * ldda;
+            const float d0 = t0 < N ? sda[t0] : 0.0f;
+            const float d1 = t0 + 1 < N ? sda[t0 + 1] : 0.0f;
             sbs[nt][0] = fmaf(d0, S[nt][0], sbs[nt][0]);
             sbs[nt][1] = fmaf(d1, S[nt][1], sbs[nt][1]);
             sbs[nt][2] = fmaf(d0, S[nt][2], sbs[nt][2]);
@@ -329,10 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          acc[nt][0] = fmaf(da_row, sbs[nt][0], acc[nt][0]);
-          acc[nt][1] = fmaf(da_row, sbs[nt][1], acc[nt][1]);
-          acc[nt][2] = fmaf(db_row, sbs[nt][2], acc[nt][2]);
-          acc[nt][3] = fmaf(db_row, sbs[nt][3], acc[nt][3]);
+          acc[nt][0] = fmaf(d_a, sbs[nt][0], acc[nt][0]);
+          acc[nt][1] = fmaf(d_a, sbs[nt][1], acc[nt][1]);
+          acc[nt][2] = fmaf(d_b, sbs[nt][2], acc[nt][2]);
+          acc[nt][3] = fmaf(d_b, sbs[nt][3], acc[nt][3]);
         }
       }
       __syncwarp();
@@ -377,6 +382,17 @@ CUresult encode(CUtensorMap* map, const void* base, uint64_t inner, uint64_t out
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+CUresult encode_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode_fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 template <int kNT, bool P>
 cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                       int ldda, int N, float* Y, int ldy, int32_t* partials, unsigned int* status,
@@ -390,7 +406,7 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
   const int R = (int)(((long long)M + waves * sms - 1) / (waves * sms));
   const int units = (M + R - 1) / R;
   const PlaneGeom g = plane_geom(M, K);
-  CUtensorMap mq, ms, md, mx;
+  CUtensorMap mq, ms, md, mx, ma;
   if (!g_encode_fn) return cudaErrorInitializationError;
   // the activation boxes hold the N token rows (the rows past N in shared
   // memory are never stored from)
@@ -401,12 +417,14 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
       encode(&md, plane + g.d_off, g.d_row / 8, (uint64_t)M, g.d_row, kDPitch / 8, (uint32_t)R) !=
           CUDA_SUCCESS ||
       encode(&mx, Xq, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K, kXPitch / 8, (uint32_t)N) !=
-          CUDA_SUCCESS)
+          CUDA_SUCCESS ||
+      encode_f32(&ma, da, (uint64_t)ldda, (uint64_t)K / 32, (uint64_t)ldda * 4, (uint32_t)ldda,
+                 8 * kSbs) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
   mmq_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R, 8 * kNT, ns), s>>>(
-      mq, ms, md, mx, M, K, N, R, units, ns, da, ldda, Y, ldy, partials, status);
+      mq, ms, md, mx, ma, M, K, N, R, units, ns, ldda, Y, ldy, partials, status);
   return cudaGetLastError();
 }
 
