@@ -936,7 +936,8 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 # removed when its kernel changes.
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.67e6 + 53.16e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
-           ("skinny_ffn_down_N16", "mmq_skinny"): 37.25e6 + 0.002e6}
+           ("skinny_ffn_down_N4", "mmq_skinny"): 37.10e6,
+           ("skinny_ffn_down_N16", "mmq_skinny"): 37.26e6}
 
 
 def main():
