@@ -270,6 +270,40 @@ def test_mmq_small_bitexact_partials(q6, orc, M, K, N, source):
     check_y(host(Y2), Yo, "fast variant")
 
 
+def _sweep_shapes(count=18, seed=0x5EED):
+    """Seeded irregular shapes over the three kernel families: one token,
+    2..16 tokens, and the tensor-core GEMM (ragged M and N, 1..24
+    super-blocks per row)."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for i in range(count):
+        N = int([1, rng.integers(2, 17), rng.integers(17, 700)][i % 3])
+        M = int(rng.integers(1, 3000))
+        K = 256 * int(rng.integers(1, 25))
+        shapes.append((M, K, N))
+    return shapes
+
+
+@pytest.mark.parametrize("M,K,N", _sweep_shapes(), ids=lambda v: str(v))
+def test_mmq_seeded_shape_sweep(q6, orc, M, K, N):
+    """Y within tolerance on every output of seeded irregular shapes (raw
+    weight source), and bit-exact chunk partials where they stay small."""
+    raw = synth.q6k_raw_weights(900 + M + K + N, M, K)
+    X = synth.activations(901 + M + K + N, N, K, outlier_frac=0.01)
+    want_p = N * M * (K // 16) <= 20_000_000
+    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, "raw", partials=want_p)
+    xq_o, da_o = quant_check(act, X, orc)
+    if want_p:
+        Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+        assert np.array_equal(host(P), chunk_sums(Po, raw, M, K)), "chunk partials differ"
+    else:
+        Yo = orc.mmq_all(raw, M, K, xq_o, da_o)
+    check_y(host(Y), Yo, f"{M}x{K}x{N}")
+    Y2, _, _ = q6.mmq(w, act, source="raw")
+    q6.sync_status()
+    check_y(host(Y2), Yo, f"{M}x{K}x{N} fast")
+
+
 def test_mmq_degenerate_inputs(q6, orc):
     M, K, N = 128, 512, 130
     blk = np.zeros(210, np.uint8)
