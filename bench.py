@@ -149,12 +149,19 @@ def time_oracle(raw, X, M, K, budget_s: float, max_tokens: int):
     t0 = time.perf_counter()
     orc.mmq(raw, M, K, xq, da)
     one = time.perf_counter() - t0
-    ntok = int(max(1, min(max_tokens, budget_s / max(one, 1e-6))))
-    t0 = time.perf_counter()
-    xq, da = orc.quantize(X[:ntok])
-    orc.mmq(raw, M, K, xq, da)
-    dt = time.perf_counter() - t0
-    return 2.0 * M * K * ntok, dt, ntok
+    # a one-token call streams every weight row once per token, so it is
+    # slower per token than a larger sample; size the sample from a first
+    # estimate and, if that ran well under the budget, once more from it
+    ntok = int(max(1, min(max_tokens, budget_s / 4 / max(one, 1e-6))))
+    while True:
+        t0 = time.perf_counter()
+        xq, da = orc.quantize(X[:ntok])
+        orc.mmq(raw, M, K, xq, da)
+        dt = time.perf_counter() - t0
+        grow = int(min(max_tokens, ntok * budget_s / max(dt, 1e-6)))
+        if dt >= 0.5 * budget_s or grow <= ntok or ntok == max_tokens:
+            return 2.0 * M * K * ntok, dt, ntok
+        ntok = grow
 
 
 def run_reference(args):
