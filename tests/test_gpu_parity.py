@@ -304,6 +304,24 @@ def test_mmq_seeded_shape_sweep(q6, orc, M, K, N):
     check_y(host(Y2), Yo, f"{M}x{K}x{N} fast")
 
 
+@pytest.mark.parametrize("M,K,N", [(1016, 768, 2555), (4096, 2048, 16), (3001, 768, 9),
+                                    (2059, 1024, 1)], ids=lambda v: str(v))
+def test_mmq_deterministic(q6, M, K, N):
+    """Repeated calls give bit-identical Y: the split last round of the
+    tensor-core GEMM adds two halves onto zero, and the few-token kernels
+    reduce in a fixed order."""
+    import torch
+    raw = synth.q6k_raw_weights(1200 + M + N, M, K)
+    X = synth.activations(1201 + M + N, N, K, outlier_frac=0.01)
+    w = q6.pack_weights(dev(raw), M, K, wh=True)
+    act = q6.quantize_act(dev(X))
+    Y0, _, _ = q6.mmq(w, act, source="wh")
+    for _ in range(3):
+        Y1, _, _ = q6.mmq(w, act, source="wh")
+        q6.sync_status()
+        assert torch.equal(Y0, Y1)
+
+
 def test_mmq_degenerate_inputs(q6, orc):
     M, K, N = 128, 512, 130
     blk = np.zeros(210, np.uint8)
