@@ -714,7 +714,7 @@ def other_configs(args, q6, synth, device, hbm):
 
 
 def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
-    """The memory-bound case: N = --tokens (1, 4 or 16) tokens against the
+    """The memory-bound case: N = --tokens (1..16) tokens against the
     ffn_down or attn_v weights. One step = quantise + q6k_mmq (skinny path),
     weights rotated over copies totalling more than 4x L2."""
     import torch
@@ -792,11 +792,12 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8 dp4a -> f32" if n == 1 else "f16 x f16 -> f32 (exact int6 x int8)",
+        "dtype": ("int8 dp4a -> f32" if n <= SKINNY_DP4A_MAX_N else
+                  "f16 x f16 -> f32 (exact int6 x int8)"),
         "data": "synthetic",
         "config": dict(skinny_config(args, M, K), weight_copies=R),
         "roofline": {"bound": "hbm",
-                     "kernel": ("mmq_skinny_kernel (dp4a)" if n == 1 else
+                     "kernel": ("mmq_skinny_kernel (dp4a)" if n <= SKINNY_DP4A_MAX_N else
                                 "mmq_skinny_mma_kernel (f16 mma.sync, TMA-staged weights)"),
                      "achieved": gbs, "peak": hbm,
                      "unit": "GB/s", "frac": gbs / hbm, "peak_source": hbm_src,
@@ -937,12 +938,18 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
+# the library's few-token dispatch: the dp4a kernel up to this many tokens,
+# the f16 mma.sync kernel above it (labels only; the library decides)
+SKINNY_DP4A_MAX_N = 2
+
 # ncu captures of the current kernels, keyed by (workload, kernel); the
 # captures are summarised under profiles/ (mmq_tc_ffn_down.md,
-# mmq_skinny_ffn_down_n1.md, mmq_skinny_mma_ffn_down_n16.md). An entry is
+# mmq_skinny_ffn_down_n1.md for one and two tokens,
+# mmq_skinny_mma_ffn_down_n16.md). An entry is
 # removed when its kernel changes.
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.67e6 + 53.16e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
+           ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
            ("skinny_ffn_down_N4", "mmq_skinny"): 37.10e6,
            ("skinny_ffn_down_N16", "mmq_skinny"): 37.26e6}
 
@@ -957,7 +964,7 @@ def main():
                     choices=["ffn_down", "attn_v", "pages_ffn_down", "pages_attn_v", "skinny",
                              "sweep"])
     ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
-    ap.add_argument("--tokens", type=int, default=1, choices=[1, 4, 16],
+    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 17), metavar="{1..16}",
                     help="tokens of the skinny workload")
     ap.add_argument("--no-other-configs", dest="other_configs", action="store_false",
                     help="skip the attn_v and skinny measurements beside ffn_down")

@@ -162,8 +162,8 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *   wexp, wh : the optional planes from q6k_pack_weights, or NULL.
  *   Xq, da: quantised activations (layouts above). Xq is read by the
  *           few-token kernels (N <= Q6_SKINNY_MAX_N: dp4a on the CUDA cores
- *           for one token, exact f16 mma.sync for 2..16 tokens; both stream
- *           the packed plane once).
+ *           for one or two tokens, exact f16 mma.sync for 3..16 tokens; both
+ *           stream the packed plane once).
  *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
  *   workspace : device scratch of at least q6k_mmq_workspace_bytes() bytes
  *           (4 * M * K, 256-byte aligned) when N > Q6_SKINNY_MAX_N and wh is

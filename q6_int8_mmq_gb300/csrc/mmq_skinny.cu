@@ -1,7 +1,10 @@
-// q6_K x int8 GEMM for one token: a weight-streaming kernel on the CUDA
-// cores, bound by HBM (0.82 byte per weight: 210 bytes per 256 weights, plus
-// the 16-byte padding of each d row). 2..16 tokens run on the tensor-core form
-// in mmq_skinny_mma.cu.
+// q6_K x int8 GEMM for one or two tokens: a weight-streaming kernel on the
+// CUDA cores, bound by HBM (0.82 byte per weight: 210 bytes per 256 weights,
+// plus the 16-byte padding of each d row). 3..16 tokens run on the
+// tensor-core form in mmq_skinny_mma.cu. Measured on GB300 (ffn_down
+// weights, us per launch, this form / the tensor form): 2 tokens 14.4 / 16.5,
+// 3 tokens 18.1 / 16.5, 4 tokens 24.9 / 17.3; each token adds its own dp4a
+// work, while the tensor form pays once for the weight conversion.
 //
 // Math ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.1-2.2): for each
 // 16-element sub-block s the exact integer P = sum (q - 32) * xq is formed
@@ -237,12 +240,15 @@ cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* 
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
                               unsigned int* status, cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
-  // one token: the dp4a weight-streaming kernel (the debug partials come from
-  // the same dot products); 2..16 tokens: the f16 tensor form with TMA-staged
-  // weights (mmq_skinny_mma.cu), partials included
+  // one or two tokens: the dp4a weight-streaming kernel (the debug partials
+  // come from the same dot products); 3..16 tokens: the f16 tensor form with
+  // TMA-staged weights (mmq_skinny_mma.cu), partials included
   if (N == 1)
     return partials ? launch_bucket<true, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s)
                     : launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+  if (N == 2)
+    return partials ? launch_bucket<true, 2>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s)
+                    : launch_bucket<false, 2>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
   return launch_mmq_skinny_mma(plane, M, K, Xq, da, ldda, N, Y, ldy, partials, status, s);
 }
 

@@ -1,4 +1,4 @@
-// q6_K x int8 GEMM for a few tokens (2 <= N <= 16) on the warp-level f16
+// q6_K x int8 GEMM for a few tokens (3 <= N <= 16) on the warp-level f16
 // tensor path, with the weights streamed into shared memory by TMA. HBM-bound
 // by design: every weight byte is read once (0.82 byte per weight).
 //

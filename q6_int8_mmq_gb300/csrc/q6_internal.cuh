@@ -49,8 +49,8 @@ cudaError_t launch_pack(const uint8_t* raw, int M, int K, uint8_t* plane, int8_t
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
                               int ldda, int N, float* Y, int ldy, int32_t* partials,
                               unsigned int* status, cudaStream_t s);
-// The same product for 2 <= N <= 16 on the warp-level f16 tensor path with
-// TMA-staged weights (mmq_skinny_mma.cu).
+// The same product for 3 <= N <= 16 (correct from N = 2) on the warp-level
+// f16 tensor path with TMA-staged weights (mmq_skinny_mma.cu).
 cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8_t* Xq,
                                   const float* da, int ldda, int N, float* Y, int ldy,
                                   int32_t* partials, unsigned int* status, cudaStream_t s);

@@ -54,7 +54,7 @@ WORKLOADS = {
     "pages_attn_v": dict(M=512, K=3584, N=3325, outlier_frac=0.0),
 }
 SKINNY_SHAPES = {"ffn_down": (4096, 11008), "attn_v": (4096, 4096)}
-SKINNY_N = (1, 4, 16)
+SKINNY_N = (1, 2, 4, 16)
 SWEEP_LAYERS = 32
 SWEEP_N = 3314
 

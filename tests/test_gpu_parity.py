@@ -271,8 +271,8 @@ def test_mmq_small_bitexact_partials(q6, orc, M, K, N, source):
 
 
 def _sweep_shapes(count=18, seed=0x5EED):
-    """Seeded irregular shapes over the three kernel families: one token,
-    2..16 tokens, and the tensor-core GEMM (ragged M and N, 1..24
+    """Seeded irregular shapes over the three kernel families: one or two
+    tokens, 3..16 tokens, and the tensor-core GEMM (ragged M and N, 1..24
     super-blocks per row)."""
     rng = np.random.default_rng(seed)
     shapes = []
