@@ -9,6 +9,8 @@ device is not sm_103, or an argument is rejected.
 from __future__ import annotations
 
 import ctypes
+import dataclasses
+import functools
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -77,6 +79,42 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _tensor(t, name, dtype, shape, device=None, rows=False):
+    """Checks that t is laid out as the C ABI reads it and returns t: a torch
+    tensor of this dtype and shape, contiguous (or, with rows=True, a 2-D view
+    whose rows are contiguous and do not overlap), on a CUDA device (`device`
+    when given). Raises Q6Error(Q6_EINVAL) before anything is launched."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise Q6Error(Q6_EINVAL, f"{name} must be a torch tensor")
+    if t.dtype is not dtype:
+        raise Q6Error(Q6_EINVAL, f"{name} must be {dtype}, not {t.dtype}")
+    if t.shape != shape:
+        raise Q6Error(Q6_EINVAL, f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+    if not t.is_contiguous() and not (
+            rows and t.dim() == 2 and (t.shape[1] <= 1 or t.stride(1) == 1)
+            and (t.shape[0] <= 1 or t.stride(0) >= t.shape[1])):
+        raise Q6Error(Q6_EINVAL, f"{name} has an unsupported layout (strides {tuple(t.stride())})")
+    if not t.is_cuda or (device is not None and t.device != device):
+        raise Q6Error(Q6_EINVAL, f"{name} must be a CUDA tensor on {device or 'a CUDA device'}")
+    return t
+
+
+def _same_device(*specs):
+    """_tensor() on each (tensor or None, name, dtype, shape), then one CUDA
+    device for all of them."""
+    devs = {_tensor(t, name, dtype, shape).device for t, name, dtype, shape in specs
+            if t is not None}
+    if len(devs) > 1:
+        raise Q6Error(Q6_EINVAL, f"tensors on different devices: {sorted(map(str, devs))}")
+
+
+def _row_stride(t):
+    """The row stride the C ABI gets for a 2-D rows view (any value >= the
+    width is valid; a single row's stride is not used)."""
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
 def _stream(stream=None):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -85,6 +123,7 @@ def _stream(stream=None):
 
 # ---------------------------------------------------------------- sizes ---
 
+@functools.lru_cache(maxsize=256)
 def act_plane_bytes(N: int, K: int):
     """(xq_bytes, da_bytes, xh_bytes, ldda) of an N x K activation."""
     a, b, c, ld = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_int()
@@ -93,6 +132,7 @@ def act_plane_bytes(N: int, K: int):
     return a.value, b.value, c.value, ld.value
 
 
+@functools.lru_cache(maxsize=256)
 def plane_bytes(M: int, K: int):
     """(packed plane bytes, W_exp bytes) of an M x K q6_K weight."""
     a, b = ctypes.c_size_t(), ctypes.c_size_t()
@@ -102,12 +142,28 @@ def plane_bytes(M: int, K: int):
 
 # ------------------------------------------------------------ operations ---
 
+@dataclasses.dataclass(frozen=True)
 class Activations:
     """Quantised activations on the device: xq [N,K] int8, da [K/32, ldda] f32,
-    xh [N,K] f16 (or None)."""
+    xh [N,K] f16 (xq or xh may be None). Checked once, when made; read-only."""
+    N: int
+    K: int
+    xq: object
+    da: object
+    xh: object
+    ldda: int
 
-    def __init__(self, N, K, xq, da, xh, ldda):
-        self.N, self.K, self.xq, self.da, self.xh, self.ldda = N, K, xq, da, xh, ldda
+    def __post_init__(self):
+        import torch
+        N, K = self.N, self.K
+        if self.ldda != act_plane_bytes(N, K)[3]:
+            raise Q6Error(Q6_EINVAL, f"ldda {self.ldda} does not match {act_plane_bytes(N, K)[3]}")
+        _same_device((self.xq, "xq", torch.int8, (N, K)), (self.xh, "xh", torch.float16, (N, K)),
+                     (self.da, "da", torch.float32, (K // 32, self.ldda)))
+
+    @property
+    def device(self):
+        return self.da.device
 
 
 def alloc_activations(N: int, K: int, device=None, want_xh: bool = True,
@@ -127,21 +183,42 @@ def alloc_activations(N: int, K: int, device=None, want_xh: bool = True,
 def quantize_act(X, out: Activations | None = None, want_xh: bool = True, stream=None,
                  want_xq: bool = True) -> Activations:
     """Quantises f32 activations X [N, K] (CUDA tensor, last dim contiguous)."""
+    import torch
+    if not isinstance(X, torch.Tensor) or X.dim() != 2:
+        raise Q6Error(Q6_EINVAL, "X must be a 2-D torch tensor [N, K]")
     N, K = X.shape
+    _tensor(X, "X", torch.float32, (N, K), rows=True)
     if out is None:
         out = alloc_activations(N, K, X.device, want_xh, want_xq)
-    _check(load().q8_quantize_act(_ptr(X), N, K, X.stride(0), _ptr(out.xq), _ptr(out.da),
+    elif out.N != N or out.K != K or out.device != X.device:
+        raise Q6Error(Q6_EINVAL, f"out holds {out.N} x {out.K} activations on {out.device}, "
+                                 f"X is {N} x {K} on {X.device}")
+    _check(load().q8_quantize_act(_ptr(X), N, K, _row_stride(X), _ptr(out.xq), _ptr(out.da),
                                   _ptr(out.xh), _stream(stream)))
     return out
 
 
+@dataclasses.dataclass(frozen=True)
 class Weights:
     """A packed q6_K weight on the device: the packed plane, and optionally the
     W_exp (int8) plane and the resident operand planes wh [2, M, K] binary16
-    (W_hi, W_lo: the sub-block scale folded into the centered codes)."""
+    (W_hi, W_lo: the sub-block scale folded into the centered codes).
+    Checked once, when made; read-only."""
+    M: int
+    K: int
+    plane: object
+    wexp: object
+    wh: object
 
-    def __init__(self, M, K, plane, wexp, wh):
-        self.M, self.K, self.plane, self.wexp, self.wh = M, K, plane, wexp, wh
+    def __post_init__(self):
+        import torch
+        _same_device((self.wexp, "wexp", torch.int8, (self.M, self.K)),
+                     (self.wh, "wh", torch.float16, (2, self.M, self.K)),
+                     (self.plane, "plane", torch.uint8, (plane_bytes(self.M, self.K)[0],)))
+
+    @property
+    def device(self):
+        return self.plane.device
 
 
 def pack_weights(raw, M: int, K: int, wexp: bool = False, wh: bool = False, stream=None) -> Weights:
@@ -163,8 +240,10 @@ def unpack_weights(w: Weights, out=None, from_wexp: bool = False, stream=None):
     W_lo) from the packed plane (or from the W_exp plane and the packed
     plane's sub-block scales)."""
     import torch
+    dev = w.device
     if out is None:
-        out = torch.empty((2, w.M, w.K), dtype=torch.float16, device=w.plane.device)
+        out = torch.empty((2, w.M, w.K), dtype=torch.float16, device=dev)
+    _tensor(out, "out", torch.float16, (2, w.M, w.K), dev)
     src8 = w.wexp if from_wexp else None
     if from_wexp and src8 is None:
         raise Q6Error(Q6_EINVAL, "weights were packed without the W_exp plane")
@@ -173,6 +252,7 @@ def unpack_weights(w: Weights, out=None, from_wexp: bool = False, stream=None):
     return out
 
 
+@functools.lru_cache(maxsize=256)
 def workspace_bytes(M: int, K: int, N: int) -> int:
     b = ctypes.c_size_t()
     _check(load().q6k_mmq_workspace_bytes(M, K, N, ctypes.byref(b)))
@@ -218,16 +298,24 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
     w16 = (wh if wh is not None else w.wh) if source == "wh" else None
     if source in ("wexp", "wh") and (wx if source == "wexp" else w16) is None:
         raise Q6Error(Q6_EINVAL, f"weights were packed without the {source} plane")
-    dev = w.plane.device
+    dev = w.device
+    if wh is not None and w16 is wh:
+        _tensor(w16, "wh", torch.float16, (2, M, K), dev)
+    if act.device != dev:
+        raise Q6Error(Q6_EINVAL, f"activations on {act.device}, weights on {dev}")
     if Y is None:
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
     P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
     ws_need = workspace_bytes(M, K, N) if w16 is None else 0
+    if workspace is not None:
+        _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
+                tuple(getattr(workspace, "shape", ())), dev)
     ws = workspace if workspace is not None else (_workspace(ws_need, dev) if ws_need else None)
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     path = ctypes.c_int(-1)
     _check(load().q6k_mmq(_ptr(w.plane), _ptr(wx), _ptr(w16), M, K, _ptr(act.xq), _ptr(act.da),
-                          _ptr(act.xh), N, _ptr(Y), Y.stride(0), _ptr(ws), ws_bytes, _ptr(P),
+                          _ptr(act.xh), N, _ptr(Y), _row_stride(Y), _ptr(ws), ws_bytes, _ptr(P),
                           ctypes.byref(path), _stream(stream)))
     return Y, PATH_NAMES.get(path.value, str(path.value)), P
 
@@ -241,13 +329,16 @@ def mmq_mma_sync(w: Weights, act: Activations, Y=None, partials: bool = False, s
         raise Q6Error(Q6_EINVAL, "activation K does not match the weight")
     if w.wexp is None:
         raise Q6Error(Q6_EINVAL, "weights were packed without the wexp plane")
-    dev = w.plane.device
+    dev = w.device
+    if act.device != dev:
+        raise Q6Error(Q6_EINVAL, f"activations on {act.device}, weights on {dev}")
     if Y is None:
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
     P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
     path = ctypes.c_int(-1)
     _check(load().q6k_mmq_mma_sync(_ptr(w.plane), _ptr(w.wexp), M, K, _ptr(act.xq), _ptr(act.da), N,
-                                   _ptr(Y), Y.stride(0), _ptr(P), ctypes.byref(path),
+                                   _ptr(Y), _row_stride(Y), _ptr(P), ctypes.byref(path),
                                    _stream(stream)))
     return Y, PATH_NAMES.get(path.value, str(path.value)), P
 

@@ -106,3 +106,63 @@ def test_host_side_rejections(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(q6.Q6Error):
         q6.load(str(tmp_path / "nope.so"))
+
+
+def test_binding_checks_tensor_layouts():
+    """The binding refuses a tensor the C ABI would misread (wrong dtype,
+    shape, overlapping or non-contiguous rows, host memory) before anything is
+    launched; a rows view with a wider row stride is accepted as it is."""
+    import numpy as np
+    import torch
+    t = torch.zeros(4, 8)
+    with pytest.raises(q6.Q6Error, match="float16"):
+        q6._tensor(t, "Y", torch.float16, (4, 8))
+    with pytest.raises(q6.Q6Error, match="shape"):
+        q6._tensor(t, "Y", torch.float32, (4, 7))
+    with pytest.raises(q6.Q6Error, match="torch tensor"):
+        q6._tensor(np.zeros((4, 8), np.float32), "Y", torch.float32, (4, 8))
+    with pytest.raises(q6.Q6Error, match="layout"):          # columns not contiguous
+        q6._tensor(torch.zeros(8, 4).t(), "Y", torch.float32, (4, 8), rows=True)
+    with pytest.raises(q6.Q6Error, match="layout"):          # rows overlap
+        q6._tensor(torch.zeros(40).as_strided((4, 8), (5, 1)), "Y", torch.float32, (4, 8),
+                   rows=True)
+    wide = torch.zeros(4, 13)[:, :8]
+    with pytest.raises(q6.Q6Error, match="layout"):          # contiguity required
+        q6._tensor(wide, "xq", torch.float32, (4, 8))
+    with pytest.raises(q6.Q6Error, match="CUDA"):            # layout fine, host memory
+        q6._tensor(wide, "Y", torch.float32, (4, 8), rows=True)
+    assert q6._row_stride(wide) == 13
+    assert q6._row_stride(torch.zeros(1, 8)) == 8
+    assert q6._row_stride(torch.zeros(0, 8)) == 8
+
+
+def test_quantize_refuses_bad_inputs_on_the_host():
+    import torch
+    with pytest.raises(q6.Q6Error, match="float32"):
+        q6.quantize_act(torch.zeros(2, 256, dtype=torch.float64))
+    with pytest.raises(q6.Q6Error, match="layout"):
+        q6.quantize_act(torch.zeros(256, 2).t())
+    with pytest.raises(q6.Q6Error, match="2-D"):
+        q6.quantize_act(torch.zeros(256))
+    with pytest.raises(q6.Q6Error, match="CUDA"):
+        q6.quantize_act(torch.zeros(2, 256))
+
+
+def test_binding_objects_are_checked_when_made():
+    """Activations and Weights validate their tensors once, when made (the
+    per-call work is then only the caller's own buffers)."""
+    import torch
+    ldda = q6.act_plane_bytes(4, 256)[3]
+    with pytest.raises(q6.Q6Error, match="ldda"):
+        q6.Activations(4, 256, None, torch.zeros(8, ldda), None, ldda + 4)
+    with pytest.raises(q6.Q6Error, match="shape"):
+        q6.Activations(4, 256, None, torch.zeros(8, ldda + 1), None, ldda)
+    with pytest.raises(q6.Q6Error, match="int8"):
+        q6.Activations(4, 256, torch.zeros(4, 256), torch.zeros(8, ldda), None, ldda)
+    with pytest.raises(q6.Q6Error, match="CUDA"):
+        q6.Activations(4, 256, None, torch.zeros(8, ldda), None, ldda)
+    pb = q6.plane_bytes(128, 256)[0]
+    with pytest.raises(q6.Q6Error, match="shape"):
+        q6.Weights(128, 256, torch.zeros(pb - 1, dtype=torch.uint8), None, None)
+    with pytest.raises(q6.Q6Error, match="CUDA"):
+        q6.Weights(128, 256, torch.zeros(pb, dtype=torch.uint8), None, None)

@@ -11,6 +11,8 @@ output, in the launch configuration the benchmark uses, against the oracle run
 over disjoint weight-row ranges on the host cores; their chunk partials are
 checked bit-exactly on sampled tokens.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -425,6 +427,65 @@ def test_mmq_empty(q6):
     Y, path, _ = q6.mmq(w, act, Y=torch.empty((0, M), device="cuda"))
     q6.sync_status()
     assert path == "none"
+
+
+@pytest.mark.parametrize("M,K,N,kind", [
+    (328, 1024, 1, "raw"), (328, 1024, 2, "raw"), (328, 1024, 7, "raw"),  # skinny kernels
+    (1016, 768, 2555, "raw"), (1016, 768, 2555, "wh"),   # tensor-core GEMM, split last round
+    (256, 512, 40, "mma_sync")], ids=lambda v: str(v))
+def test_mmq_strided_unaligned_output(q6, orc, M, K, N, kind):
+    """Y as a view with an odd row stride (M + 37 floats) starting 4 bytes past
+    a 16-byte boundary: every kernel family takes its scalar stores, writes
+    Y[:N, :M] and leaves every other float of the buffer untouched."""
+    import torch
+    raw = synth.q6k_raw_weights(0x51360B01 + N, M, K)
+    X = synth.activations(0x51360B02 + N, N, K, outlier_frac=0.01)
+    w = q6.pack_weights(dev(raw), M, K, wh=kind == "wh", wexp=kind == "mma_sync")
+    act = q6.quantize_act(dev(X))
+    xq_o, da_o = quant_check(act, X, orc)
+    ldy = M + 37
+    buf = torch.full((N * ldy + 1,), float("nan"), dtype=torch.float32, device="cuda")
+    Y = buf[1:].view(N, ldy)[:, :M]
+    assert Y.data_ptr() % 16 == 4 and Y.stride(0) == ldy
+    if kind == "mma_sync":
+        Y2, path, _ = q6.mmq_mma_sync(w, act, Y=Y)
+    else:
+        Y2, path, _ = q6.mmq(w, act, Y=Y, source=kind)
+        assert path == ("skinny" if N <= q6.SKINNY_MAX_N else TC_PATH[kind])
+    q6.sync_status()
+    assert Y2.data_ptr() == Y.data_ptr()
+    b = host(buf)
+    assert np.isnan(b[0]) and np.all(np.isnan(b[1:].reshape(N, ldy)[:, M:]))
+    Yh = host(Y)
+    assert np.all(np.isfinite(Yh))
+    tok = sampled_tokens(N, extra=(1535, 1536, 2047, 2432, 2500))
+    check_y(Yh[tok], orc.mmq(raw, M, K, xq_o[tok], da_o[tok]), f"strided {M}x{K}x{N} {kind}")
+
+
+def test_mmq_refuses_mismatched_buffers(q6):
+    """An output or activation buffer the kernels would misread is refused by
+    the binding before anything is launched, and the path still works after."""
+    import torch
+    M, K, N = 256, 512, 5
+    raw = synth.q6k_raw_weights(0x51360B10, M, K)
+    w = q6.pack_weights(dev(raw), M, K)
+    X = dev(synth.activations(0x51360B11, N, K))
+    act = q6.quantize_act(X)
+    for Y in (torch.empty((N, M - 1), device="cuda"),                # too narrow
+              torch.empty((M, N), device="cuda").t(),                # columns not contiguous
+              torch.empty((N, M), dtype=torch.float16, device="cuda"),
+              torch.empty((N, M))):                                  # host memory
+        with pytest.raises(q6.Q6Error):
+            q6.mmq(w, act, Y=Y)
+    with pytest.raises(q6.Q6Error):
+        q6.quantize_act(X, out=q6.alloc_activations(N + 1, K))
+    with pytest.raises(q6.Q6Error):
+        q6.mmq(w, q6.quantize_act(X[:, :256].contiguous()))         # K does not match
+    with pytest.raises(dataclasses.FrozenInstanceError):
+        act.xq = torch.empty((N + 1, K), dtype=torch.int8, device="cuda")
+    Y, path, _ = q6.mmq(w, act)
+    q6.sync_status()
+    assert path == "skinny" and bool(torch.isfinite(Y).all())
 
 
 # ------------------------------------------------------ full-size workloads --
