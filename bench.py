@@ -228,10 +228,12 @@ def workload_config(args, cfg):
 
 
 def skinny_config(args, M, K):
+    fused = args.tokens <= SKINNY_FUSED_MAX_N
     return {"workload": f"skinny q6_K GEMM ({args.skinny_weight} weights) M={M} K={K} "
                         f"N={args.tokens}",
             "M": M, "K": K, "N": args.tokens,
-            "step": "q8_quantize_act + q6k_mmq (skinny path)",
+            "step": ("q6k_mmq_f32 (the quantiser and the GEMM in one kernel)" if fused else
+                     "q8_quantize_act + q6k_mmq (skinny path)"),
             "l2": "weights rotated over packed copies totalling more than 4x L2",
             "parallelism": "replicas"}
 
@@ -415,6 +417,12 @@ def skinny_bytes(M, K, N):
     """Algorithmic HBM bytes of one skinny GEMM: q6_K weights at 210 B per 256,
     int8 activations + their per-32 scales, f32 output."""
     return M * K * 210 / 256 + N * K + N * (K // 32) * 4 + 4 * N * M
+
+
+def fused_bytes(M, K, N):
+    """The same for the fused one/two-token call: the weights, the f32
+    activations it quantises itself, f32 output."""
+    return M * K * 210 / 256 + 4 * N * K + 4 * N * M
 
 
 def skinny_kernel_times(q6, synth, device, iters: int = 10):
@@ -732,8 +740,13 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     Xd, act, Y = Xds[0], acts[0], Ys[0]
     path = [None]
 
+    fused = n <= SKINNY_FUSED_MAX_N
+
     def step(i, ev=None):
         j = i % S
+        if fused:
+            _, path[0] = q6.mmq_f32(Ws[i % R], Xds[j], Y=Ys[j])
+            return
         if ev is not None:
             ev[0].record()
         q6.quantize_act(Xds[j], out=acts[j])
@@ -759,8 +772,12 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     graph.replay()
     max_ms, clk = timed_region(lambda i: graph.replay(), 1, device, rank == 0)
     q6.sync_status()
-    m_ms = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y), 20 * R)
-    q_ms = graph_ms(lambda i: q6.quantize_act(Xd, out=act), 200)
+    if fused:
+        m_ms = graph_ms(lambda i: q6.mmq_f32(Ws[i % R], Xd, Y=Y), 20 * R)
+        q_ms = None
+    else:
+        m_ms = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y), 20 * R)
+        q_ms = graph_ms(lambda i: q6.quantize_act(Xd, out=act), 200)
     q6.sync_status()
     ops_per_step = 2.0 * M * n * K
     value = job_throughput(ops_per_step * args.steps, world, max_ms / 1e3) / 1e12
@@ -784,10 +801,20 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         cpu = oracle_baseline(raw, X, M, K, args.cpu_budget, n)
     if rank != 0:
         return
-    alg = skinny_bytes(M, K, n)
+    alg = fused_bytes(M, K, n) if fused else skinny_bytes(M, K, n)
     gbs = alg / m_ms / 1e6
     traffic = args.traffic if args.traffic is not None else TRAFFIC.get(
-        (f"skinny_{wname}_N{n}", "mmq_skinny"))
+        (f"skinny_{wname}_N{n}", "mmq_skinny_fused" if fused else "mmq_skinny"))
+    if fused:
+        kname = "mmq_skinny_fused_kernel (dp4a, quantiser in the same kernel)"
+        formula = "M*K*210/256 + 4*N*K + 4*N*M"
+        kernels = {"q6k_mmq_f32": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]}}
+    else:
+        kname = ("mmq_skinny_kernel (dp4a)" if n <= SKINNY_DP4A_MAX_N else
+                 "mmq_skinny_mma_kernel (f16 mma.sync, TMA-staged weights)")
+        formula = "M*K*210/256 + N*K + N*K/8 + 4*N*M"
+        kernels = {"q6k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
+                   "q8_quantize_act": {"us": q_ms * 1e3}}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
@@ -796,18 +823,15 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
                   "f16 x f16 -> f32 (exact int6 x int8)"),
         "data": "synthetic",
         "config": dict(skinny_config(args, M, K), weight_copies=R),
-        "roofline": {"bound": "hbm",
-                     "kernel": ("mmq_skinny_kernel (dp4a)" if n <= SKINNY_DP4A_MAX_N else
-                                "mmq_skinny_mma_kernel (f16 mma.sync, TMA-staged weights)"),
+        "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": gbs, "peak": hbm,
                      "unit": "GB/s", "frac": gbs / hbm, "peak_source": hbm_src,
                      "traffic": traffic,
-                     "algorithmic": f"M*K*210/256 + N*K + N*K/8 + 4*N*M = {alg:.4g} B per launch"},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps,
+                     "algorithmic": f"{formula} = {alg:.4g} B per launch"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 if fused else 2) * args.steps,
         "clocks": clk, "clocks_ok": clocks_ok(clk),
         "timing": "the K steps replayed as one CUDA graph; kernel times by graph replay",
-        "kernels": {"q6k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
-                    "q8_quantize_act": {"us": q_ms * 1e3}},
+        "kernels": kernels,
     }
     print(json.dumps(line), flush=True)
 
@@ -939,8 +963,10 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
 # the library's few-token dispatch: the dp4a kernel up to this many tokens,
-# the f16 mma.sync kernel above it (labels only; the library decides)
+# the f16 mma.sync kernel above it (labels only; the library decides); up to
+# SKINNY_FUSED_MAX_N tokens the skinny step is the fused call q6k_mmq_f32
 SKINNY_DP4A_MAX_N = 2
+SKINNY_FUSED_MAX_N = 2
 
 # ncu captures of the current kernels, keyed by (workload, kernel); the
 # captures are summarised under profiles/ (mmq_tc_ffn_down.md,
@@ -950,6 +976,7 @@ SKINNY_DP4A_MAX_N = 2
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.67e6 + 53.16e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
            ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
+           ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
            ("skinny_ffn_down_N4", "mmq_skinny"): 37.10e6,
            ("skinny_ffn_down_N16", "mmq_skinny"): 37.26e6}
 

@@ -57,8 +57,10 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_SKINNY 3  /* few-token kernel for N <= Q6_SKINNY_MAX_N on the packed q6_K plane */
 #define Q6_PATH_TC_WH 4   /* tensor-core GEMM on resident binary16 operand planes */
 #define Q6_PATH_SYNC_WEXP 5 /* legacy mma.sync int8 GEMM on the W_exp plane (q6k_mmq_mma_sync) */
+#define Q6_PATH_SKINNY_FUSED 6 /* quantiser and one/two-token GEMM in one kernel (q6k_mmq_f32) */
 
 #define Q6_SKINNY_MAX_N 16
+#define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
 
 /* Text of the calling thread's last error ("" if none). Owned by the library. */
 const char *q6_last_error(void);
@@ -244,6 +246,27 @@ int q6k_mmq_mma_sync(const void *plane, const int8_t *wexp, int M, int K, const 
 int q6k_mmq_noalloc(const void *plane, const int8_t *wexp, int M, int K, const int8_t *Xq,
                     const float *da, const uint16_t *Xh, int N, float *Y, int ldy, int *path_out,
                     q6_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * One or two tokens straight from f32 activations, in one kernel launch:
+ * Y = what q8_quantize_act followed by q6k_mmq gives for the same X (the
+ * per-32 quantisation of "r38 -- q6_K BT-style raw-byte mma kernel" Sec. 2.2
+ * with the same arithmetic, then the q6_K GEMM of Sec. 2.1-2.2), without
+ * writing the codes and scales to memory. For decode steps, where the
+ * quantiser's separate launch is a large share of the step.
+ *
+ *   plane : packed weights from q6k_pack_weights (device, 256-byte aligned).
+ *   X     : device f32 [N][ldx], ldx >= K; X 16-byte aligned, ldx % 4 == 0.
+ *   N     : 0 .. Q6_FUSED_MAX_N (more tokens: q8_quantize_act + q6k_mmq).
+ *   Y     : device f32 [N][ldy], ldy >= M, 4-byte aligned.
+ *   K     : K % 256 == 0 and N * K * 9 / 8 <= 232,448 (the codes and scales
+ *           of X staged in shared memory): K <= 103,168 for two tokens,
+ *           206,592 for one; Q6_ESIZE beyond.
+ *   path_out : NULL or receives Q6_PATH_SKINNY_FUSED (Q6_PATH_NONE for N == 0).
+ * Errors: Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA as above; no
+ * allocation, no bounded waits, asynchronous on s. */
+int q6k_mmq_f32(const void *plane, int M, int K, const float *X, int ldx, int N, float *Y,
+                int ldy, int *path_out, q6_stream_t s);
 
 #ifdef __cplusplus
 }

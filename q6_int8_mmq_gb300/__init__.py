@@ -17,10 +17,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
 
 Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
-PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH, PATH_SYNC_WEXP = range(6)
+(PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH, PATH_SYNC_WEXP,
+ PATH_SKINNY_FUSED) = range(7)
 PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
-              PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh", PATH_SYNC_WEXP: "sync_wexp"}
+              PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh", PATH_SYNC_WEXP: "sync_wexp",
+              PATH_SKINNY_FUSED: "skinny_fused"}
 SKINNY_MAX_N = 16
+FUSED_MAX_N = 2
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).
 _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)
@@ -41,6 +44,7 @@ SIGNATURES = [
                      _P]),
     ("q6k_mmq_noalloc", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _IP, _P]),
     ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _IP, _P]),
+    ("q6k_mmq_f32", _I, [_P, _I, _I, _P, _I, _I, _P, _I, _IP, _P]),
 ]
 
 
@@ -318,6 +322,25 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
                           _ptr(act.xh), N, _ptr(Y), _row_stride(Y), _ptr(ws), ws_bytes, _ptr(P),
                           ctypes.byref(path), _stream(stream)))
     return Y, PATH_NAMES.get(path.value, str(path.value)), P
+
+
+def mmq_f32(w: Weights, X, Y=None, stream=None):
+    """One or two tokens straight from f32 activations X [N, K] (N <= 2), in
+    one kernel: the same Y as quantize_act(X) followed by mmq(). Returns
+    (Y, path name)."""
+    import torch
+    if not isinstance(X, torch.Tensor) or X.dim() != 2:
+        raise Q6Error(Q6_EINVAL, "X must be a 2-D torch tensor [N, K]")
+    N, K, M = X.shape[0], w.K, w.M
+    dev = w.device
+    _tensor(X, "X", torch.float32, (N, K), dev, rows=True)
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
+    path = ctypes.c_int(-1)
+    _check(load().q6k_mmq_f32(_ptr(w.plane), M, K, _ptr(X), _row_stride(X), N, _ptr(Y),
+                              _row_stride(Y), ctypes.byref(path), _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value))
 
 
 def mmq_mma_sync(w: Weights, act: Activations, Y=None, partials: bool = False, stream=None):

@@ -38,7 +38,7 @@
 // or of whole rows with cp.async.bulk.prefetch), a step-major order of the
 // weight plane (no faster than row-major), and one 8-byte load of the two
 // sub-block scales with byte permutes (slower than two byte loads).
-#include "q6_internal.cuh"
+#include "q6_quant.cuh"
 
 namespace q6 {
 namespace {
@@ -76,7 +76,9 @@ __device__ __forceinline__ void dot_pair(const uint4 L, const uint4 H, int fsh, 
 
 // One lane's share of one step: sub-blocks sa = 8*half + s4 and sa + 4 of
 // super-block sb, from its 16 ql bytes L and 16 qh bytes H, for every token.
-template <bool kPartials, int kMaxN>
+// The codes Xq [N][K] and scales da come from global memory, or (kSmem) from
+// the fused kernel's shared-memory copy.
+template <bool kPartials, int kMaxN, bool kSmem = false>
 __device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a, int sc_b,
                                          uint16_t dbits, int sb, int m, int M, int K,
                                          const int8_t* __restrict__ Xq,
@@ -94,12 +96,21 @@ __device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a,
   for (int n = 0; n < kMaxN; ++n) {
     if (n < N) {
       const int8_t* xr = Xq + (size_t)n * K;
-      const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
-      const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
+      uint4 xa, xb;
+      float daa, dab;
+      if (kSmem) {
+        xa = *reinterpret_cast<const uint4*>(xr + ka);
+        xb = *reinterpret_cast<const uint4*>(xr + ka + 64);
+        daa = da[(size_t)ca_blk * ldda + n];
+        dab = da[(size_t)cb_blk * ldda + n];
+      } else {
+        xa = __ldg(reinterpret_cast<const uint4*>(xr + ka));
+        xb = __ldg(reinterpret_cast<const uint4*>(xr + ka + 64));
+        daa = __ldg(da + (size_t)ca_blk * ldda + n);
+        dab = __ldg(da + (size_t)cb_blk * ldda + n);
+      }
       int pa, pb;
       dot_pair(L, H, fsh, xa, xb, pa, pb);
-      const float daa = __ldg(da + (size_t)ca_blk * ldda + n);
-      const float dab = __ldg(da + (size_t)cb_blk * ldda + n);
       // sc * P is an integer below 2^24 in magnitude: exact in f32
       acc[n] = fmaf(d, fmaf(dab, (float)(sc_b * pb), daa * (float)(sc_a * pa)), acc[n]);
       if (kPartials) {
@@ -138,6 +149,14 @@ __device__ __forceinline__ void row_store(float (&acc)[kMaxN], int m, int N, flo
   }
 }
 
+// One step of a row as a lane holds it: 16 ql bytes, 16 qh bytes, the two
+// sub-block scales and the super-block scale bits.
+struct Step {
+  uint4 L, H;
+  int a, b;
+  uint16_t d;
+};
+
 // The dot products of one weight row with the N <= kMaxN activation rows.
 // Each step covers 4 super-blocks (768 bytes of codes per warp); the loads of
 // step i + 1 are issued before the math of step i (a one-step software
@@ -161,11 +180,6 @@ __device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
 #pragma unroll
   for (int n = 0; n < kMaxN; ++n) acc[n] = 0.0f;
 
-  struct Step {
-    uint4 L, H;
-    int a, b;
-    uint16_t d;
-  };
   auto load = [&](int sb, Step& r) {
     r.L = make_uint4(0, 0, 0, 0);
     r.H = r.L;
@@ -213,9 +227,152 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
 }
 
 
+// One or two tokens straight from f32 activations, in one launch: a CTA of
+// 32 warps per SM, rows to warps as in mmq_skinny_kernel. Each warp requests
+// the first two steps of its first row, the CTA then quantises the N rows of
+// X into shared memory with the standalone quantiser's arithmetic
+// (q6_quant.cuh: the same codes and scales as q8_quantize_act), and after one
+// barrier the warps form the same dot products as mmq_skinny_kernel from the
+// staged codes. Every CTA quantises all of X (N*K*4 bytes, from L2 after the
+// first CTAs), so no CTA waits on another and nothing else is launched.
+constexpr int kFusedWarps = 32;
+
+template <int kMaxN>
+__global__ void __launch_bounds__(kFusedWarps * 32, 1) mmq_skinny_fused_kernel(
+    const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const float* __restrict__ X,
+    int ldx, int N, float* __restrict__ Y, int ldy) {
+  extern __shared__ __align__(16) uint8_t fused_smem[];
+  int8_t* xs = reinterpret_cast<int8_t*>(fused_smem);                     // codes [N][K]
+  float* das = reinterpret_cast<float*>(fused_smem + (size_t)kMaxN * K);  // scales [K/32][kMaxN]
+  const int lane = threadIdx.x & 31;
+  const int nsb = K / 256;
+  const int sbi = lane >> 3;
+  const int half = (lane >> 2) & 1;
+  const int s4 = lane & 3;
+  const int sa = 8 * half + s4;
+  const int warps = (int)gridDim.x * kFusedWarps;
+  int m = (threadIdx.x >> 5) * (int)gridDim.x + blockIdx.x;
+
+  const uint8_t* qlh_row = nullptr;
+  const int8_t* sc_row = nullptr;
+  const uint16_t* d_row = nullptr;
+  auto row = [&](int mm) {
+    qlh_row = plane + g.qlh_off + (size_t)mm * g.qlh_row;
+    sc_row = reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)mm * (K / 16);
+    d_row = reinterpret_cast<const uint16_t*>(plane + g.d_off + (size_t)mm * g.d_row);
+  };
+  auto load = [&](int sb, Step& r) {
+    r.L = make_uint4(0, 0, 0, 0);
+    r.H = r.L;
+    r.a = r.b = 0;
+    r.d = 0;
+    if (sb < nsb) {
+      const uint8_t* hb = qlh_row + (size_t)(2 * sb + half) * 96;
+      r.L = __ldg(reinterpret_cast<const uint4*>(hb + 16 * s4));
+      r.H = __ldg(reinterpret_cast<const uint4*>(hb + 64 + 16 * (s4 & 1)));
+      r.a = __ldg(sc_row + 16 * sb + sa);
+      r.b = __ldg(sc_row + 16 * sb + sa + 4);
+      r.d = __ldg(d_row + sb);
+    }
+  };
+
+  // the first row's first two steps are in flight while the codes are made
+  Step A, B;
+  if (m < M) {
+    row(m);
+    load(sbi, A);
+    load(4 + sbi, B);
+  }
+  {
+    // eight elements per thread, four threads per 32-element block (as the
+    // standalone few-token quantiser); N*K/8 is a multiple of 32, so every
+    // warp runs the shuffles whole. Measured and not kept: two groups per
+    // thread with their loads issued together (spills: 10.6 -> 11.3 us for
+    // one token on the ffn_down weights) and the first two steps requested
+    // into L2 instead of registers (10.8 us).
+    const int per_row = K >> 3;
+    const int total = N * per_row;
+    for (int gi = threadIdx.x; gi < total; gi += blockDim.x) {
+      const int n = gi / per_row;
+      const int j = gi - n * per_row;
+      const float4* src = reinterpret_cast<const float4*>(X + (size_t)n * ldx) + 2 * j;
+      const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+      float a = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                      fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+      a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+      const float d = __fdiv_rn(a, 127.0f);
+      uint2 q8;
+      uint4 h8;
+      quant8(v0, v1, d, recip_or_zero(d), q8, h8);
+      *reinterpret_cast<uint2*>(xs + (size_t)n * K + 8 * j) = q8;
+      if ((j & 3) == 0) das[(j >> 2) * kMaxN + n] = d;
+    }
+  }
+  __syncthreads();
+
+  for (bool first = true; m < M; m += warps, first = false) {
+    if (!first) {
+      row(m);
+      load(sbi, A);
+      load(4 + sbi, B);
+    }
+    float acc[kMaxN];
+#pragma unroll
+    for (int n = 0; n < kMaxN; ++n) acc[n] = 0.0f;
+    auto step = [&](int sb, const Step& r) {
+      if (sb < nsb)
+        step_dot<false, kMaxN, true>(r.L, r.H, r.a, r.b, r.d, sb, m, M, K, xs, das, kMaxN, N,
+                                     nullptr, acc);
+    };
+    // the first iteration of mmq_skinny_kernel's loop with both of its
+    // loads already issued, then the same loop
+    step(sbi, A);
+    load(8 + sbi, A);
+    step(4 + sbi, B);
+    for (int g0 = 8; g0 < nsb; g0 += 8) {
+      load(g0 + 4 + sbi, B);
+      step(g0 + sbi, A);
+      load(g0 + 8 + sbi, A);
+      step(g0 + 4 + sbi, B);
+    }
+    row_store<kMaxN>(acc, m, N, Y, ldy);
+  }
+}
+
+size_t fused_smem_bytes(int K, int kmax) { return (size_t)kmax * K + (size_t)(K / 32) * kmax * 4; }
+
+template <int kMaxN>
+cudaError_t launch_fused(const uint8_t* plane, int M, int K, const float* X, int ldx, int N,
+                         float* Y, int ldy, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  mmq_skinny_fused_kernel<kMaxN><<<(unsigned)sms, kFusedWarps * 32, fused_smem_bytes(K, kMaxN), s>>>(
+      plane, plane_geom(M, K), M, K, X, ldx, N, Y, ldy);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t mmq_skinny_prepare() { return mmq_skinny_mma_prepare(); }
+cudaError_t mmq_skinny_prepare() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(mmq_skinny_fused_kernel<1>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemMax)) ||
+      (e = cudaFuncSetAttribute(mmq_skinny_fused_kernel<2>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemMax)))
+    return e;
+  return mmq_skinny_mma_prepare();
+}
+
+size_t mmq_skinny_fused_smem(int K, int N) { return fused_smem_bytes(K, N); }
+
+cudaError_t launch_mmq_skinny_fused(const uint8_t* plane, int M, int K, const float* X, int ldx,
+                                    int N, float* Y, int ldy, cudaStream_t s) {
+  return N == 1 ? launch_fused<1>(plane, M, K, X, ldx, N, Y, ldy, s)
+                : launch_fused<2>(plane, M, K, X, ldx, N, Y, ldy, s);
+}
 
 template <bool P, int kMaxN>
 cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,

@@ -56,6 +56,13 @@ cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8
                                   int32_t* partials, unsigned int* status, cudaStream_t s);
 cudaError_t mmq_skinny_mma_prepare();
 cudaError_t mmq_skinny_prepare();
+// Quantise + GEMM for N <= 2 tokens from f32 X [N][ldx] in one launch
+// (mmq_skinny.cu); needs mmq_skinny_fused_smem(K, N) <= kFusedSmemMax bytes
+// of shared memory.
+constexpr int kFusedSmemMax = 227 * 1024;
+size_t mmq_skinny_fused_smem(int K, int N);
+cudaError_t launch_mmq_skinny_fused(const uint8_t* plane, int M, int K, const float* X, int ldx,
+                                    int N, float* Y, int ldy, cudaStream_t s);
 cudaError_t launch_mmq_sync(const uint8_t* plane, const int8_t* wexp, int M, int K,
                             const int8_t* Xq, const float* da, int ldda, int N, float* Y, int ldy,
                             int32_t* partials, cudaStream_t s);

@@ -101,6 +101,21 @@ def test_host_side_rejections(lib):
     assert lib.q6k_pack_weights(fake, 4, 256, fake, None, odd, None) == q6.Q6_EALIGN
     assert lib.q6k_pack_weights(None, 4, 256, fake, None, None, None) == q6.Q6_EINVAL
     assert lib.q6_selftest_wait_timeout(0, None) == q6.Q6_EINVAL
+    # fused one/two-token call: too many tokens, ldx < K, ldy < M, misaligned X
+    # or ldx, K beyond the shared-memory staging, the empty case
+    def f32(plane=fake, M=64, K=256, X=fake, ldx=256, N=1, Y=fake, ldy=64):
+        return lib.q6k_mmq_f32(plane, M, K, X, ldx, N, Y, ldy, ctypes.byref(path), None)
+
+    assert f32(N=3) == q6.Q6_EINVAL and path.value == q6.PATH_NONE
+    assert f32(ldx=128) == q6.Q6_EINVAL
+    assert f32(ldy=32) == q6.Q6_EINVAL
+    assert f32(X=None) == q6.Q6_EINVAL
+    assert f32(X=odd) == q6.Q6_EALIGN
+    assert f32(ldx=258) == q6.Q6_EALIGN                    # ldx % 4 != 0
+    assert f32(plane=odd) == q6.Q6_EALIGN
+    assert f32(K=103168 + 256, ldx=103424, N=2) == q6.Q6_ESIZE
+    assert f32(K=206592 + 256, ldx=206848, N=1) == q6.Q6_ESIZE
+    assert f32(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
 
 def test_missing_library_fails_loudly(tmp_path):

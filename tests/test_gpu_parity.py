@@ -127,13 +127,13 @@ def test_quantize_bitexact(q6, orc, N, K, frac):
     quant_check(act, X, orc)
 
 
-@pytest.mark.parametrize("N,K", [(3, 256), (300, 1024)])
-def test_quantize_near_ties_and_tiny_scales(q6, orc, N, K):
-    """Quotients on, one ulp beside and a little beside rounding ties, where
-    the kernels leave the reciprocal for the exact division, and blocks whose
-    scale is subnormal (also taken exactly); bit-exact against the oracle."""
-    rng = np.random.default_rng(7 + N)
-    X = synth.activations(500 + N, N, K)
+def hard_activations(seed, N, K, big=np.float32(1e36)):
+    """Activations whose blocks put quotients on, one ulp beside and a little
+    beside rounding ties (where the kernels leave the reciprocal for the exact
+    division), have a subnormal scale (also taken exactly) or are scaled by
+    `big`."""
+    rng = np.random.default_rng(seed)
+    X = synth.activations(seed + 493, N, K)
     blocks = X.reshape(N, K // 32, 32)
     kind = rng.integers(0, 4, size=blocks.shape[:2])
     for n, c in zip(*np.nonzero(kind == 1)):
@@ -150,8 +150,15 @@ def test_quantize_near_ties_and_tiny_scales(q6, orc, N, K):
     for n, c in zip(*np.nonzero(kind == 2)):
         blocks[n, c] *= np.float32(1e-40)        # subnormal amax and scale
     for n, c in zip(*np.nonzero(kind == 3)):
-        blocks[n, c] *= np.float32(1e36)         # large values, normal scale
-    X = np.ascontiguousarray(blocks.reshape(N, K))
+        blocks[n, c] *= big                      # large values, normal scale
+    return np.ascontiguousarray(blocks.reshape(N, K))
+
+
+@pytest.mark.parametrize("N,K", [(3, 256), (300, 1024)])
+def test_quantize_near_ties_and_tiny_scales(q6, orc, N, K):
+    """Quotients on and beside rounding ties and subnormal block scales:
+    bit-exact against the oracle."""
+    X = hard_activations(7 + N, N, K)
     act = q6.quantize_act(dev(X))
     q6.sync_status()
     quant_check(act, X, orc)
@@ -486,6 +493,61 @@ def test_mmq_refuses_mismatched_buffers(q6):
     Y, path, _ = q6.mmq(w, act)
     q6.sync_status()
     assert path == "skinny" and bool(torch.isfinite(Y).all())
+
+
+@pytest.mark.parametrize("M,K,N", [(4096, 11008, 1), (4096, 11008, 2), (4096, 4096, 2),
+                                   (1, 256, 1), (131, 2816, 2), (5003, 768, 2), (2059, 1024, 1)],
+                         ids=lambda v: str(v))
+def test_mmq_f32_equals_quantise_then_mmq(q6, orc, M, K, N):
+    """The fused one/two-token call gives bit for bit the Y of quantize_act
+    followed by mmq (the same codes, dot products and order), on ordinary
+    activations and on blocks at and beside rounding ties, with subnormal and
+    very large scales; Y within tolerance of the oracle on every output. The
+    shapes cover the full-size weights, one row, more rows than warps and
+    one super-block per row."""
+    import torch
+    raw = synth.q6k_raw_weights(0x51360C01 + M + N, M, K)
+    w = q6.pack_weights(dev(raw), M, K)
+    X0 = synth.activations(0x51360C02 + K + N, N, K, outlier_frac=0.01)
+    for X in (X0, hard_activations(0x51360C03 + N, N, K, big=np.float32(1e30))):
+        Xd = dev(X)
+        Y, path = q6.mmq_f32(w, Xd)
+        act = q6.quantize_act(Xd)
+        Y2, path2, _ = q6.mmq(w, act)
+        q6.sync_status()
+        assert path == "skinny_fused" and path2 == "skinny"
+        assert torch.equal(Y, Y2), "fused and separate quantisation disagree"
+    act = q6.quantize_act(dev(X0))
+    xq_o, da_o = quant_check(act, X0, orc)
+    Yo = orc.mmq_all(raw, M, K, xq_o, da_o) if M * K > 1 << 22 else orc.mmq(raw, M, K, xq_o, da_o)
+    Y, _ = q6.mmq_f32(w, dev(X0))
+    q6.sync_status()
+    check_y(host(Y), Yo, f"fused {M}x{K}x{N}")
+
+
+def test_mmq_f32_strided_input_and_output(q6):
+    """X with a wider row stride, Y with an odd row stride at an unaligned
+    address: the floats between Y's rows stay untouched, the result equals
+    the separate path's."""
+    import torch
+    M, K, N = 328, 1024, 2
+    raw = synth.q6k_raw_weights(0x51360C11, M, K)
+    w = q6.pack_weights(dev(raw), M, K)
+    big = torch.full((N, K + 64), float("nan"), dtype=torch.float32, device="cuda")
+    big[:, :K] = dev(synth.activations(0x51360C12, N, K))
+    Xv = big[:, :K]
+    ldy = M + 37
+    buf = torch.full((N * ldy + 1,), float("nan"), dtype=torch.float32, device="cuda")
+    Yv = buf[1:].view(N, ldy)[:, :M]
+    Y, path = q6.mmq_f32(w, Xv, Y=Yv)
+    Y2, _, _ = q6.mmq(w, q6.quantize_act(Xv))
+    q6.sync_status()
+    assert path == "skinny_fused" and Y.data_ptr() == Yv.data_ptr()
+    assert torch.equal(Yv, Y2)
+    b = host(buf)
+    assert np.isnan(b[0]) and np.all(np.isnan(b[1:].reshape(N, ldy)[:, M:]))
+    with pytest.raises(q6.Q6Error):
+        q6.mmq_f32(w, dev(synth.activations(0x51360C13, 3, K)))   # three tokens
 
 
 # ------------------------------------------------------ full-size workloads --
