@@ -286,10 +286,12 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) mmq_skinny_fused_kernel(
   {
     // eight elements per thread, four threads per 32-element block (as the
     // standalone few-token quantiser); N*K/8 is a multiple of 32, so every
-    // warp runs the shuffles whole. Measured and not kept: two groups per
-    // thread with their loads issued together (spills: 10.6 -> 11.3 us for
-    // one token on the ffn_down weights) and the first two steps requested
-    // into L2 instead of registers (10.8 us).
+    // warp runs the shuffles whole. Without this loop the kernel takes 9.1
+    // us for one token on the ffn_down weights (10.6 with it). Measured and
+    // not kept: two groups per thread with their loads issued together
+    // (spills: 11.3 us), the first two steps requested into L2 instead of
+    // registers (10.8 us), sixteen elements per thread, one round for a
+    // token (11.0 us; 10.7 with the L2 requests).
     const int per_row = K >> 3;
     const int total = N * per_row;
     for (int gi = threadIdx.x; gi < total; gi += blockDim.x) {
