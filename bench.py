@@ -772,9 +772,20 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     graph.replay()
     max_ms, clk = timed_region(lambda i: graph.replay(), 1, device, rank == 0)
     q6.sync_status()
+    separate = None
     if fused:
         m_ms = graph_ms(lambda i: q6.mmq_f32(Ws[i % R], Xd, Y=Y), 20 * R)
         q_ms = None
+        # the same GEMM through the separate calls, for comparison: the GEMV on
+        # activations quantised beforehand, and the quantiser alone
+        q6.quantize_act(Xd, out=act)
+        g_ms = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y), 20 * R)
+        sq_ms = graph_ms(lambda i: q6.quantize_act(Xd, out=act), 200)
+        g_gbs = skinny_bytes(M, K, n) / g_ms / 1e6
+        separate = {"step": "q8_quantize_act + q6k_mmq",
+                    "q6k_mmq": {"kernel": "mmq_skinny_kernel (dp4a)", "us": g_ms * 1e3,
+                                "gbs": g_gbs, "frac": g_gbs / hbm},
+                    "q8_quantize_act": {"us": sq_ms * 1e3}}
     else:
         m_ms = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y), 20 * R)
         q_ms = graph_ms(lambda i: q6.quantize_act(Xd, out=act), 200)
@@ -833,6 +844,8 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         "timing": "the K steps replayed as one CUDA graph; kernel times by graph replay",
         "kernels": kernels,
     }
+    if separate is not None:
+        line["separate_calls"] = separate
     print(json.dumps(line), flush=True)
 
 
