@@ -525,6 +525,31 @@ def test_mmq_f32_equals_quantise_then_mmq(q6, orc, M, K, N):
     check_y(host(Y), Yo, f"fused {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("K,N", [(103168, 2), (206592, 1)], ids=lambda v: str(v))
+def test_mmq_f32_largest_k(q6, orc, K, N):
+    """The largest K whose codes and scales fit the fused kernel's shared
+    memory for N tokens (232,128 and 232,416 of 232,448 bytes): the same Y as
+    the separate calls, within tolerance of the oracle; one more super-block
+    is refused."""
+    import torch
+    M = 96
+    raw = synth.q6k_raw_weights(0x51360C21 + N, M, K)
+    X = synth.activations(0x51360C22 + N, N, K, outlier_frac=0.01)
+    w = q6.pack_weights(dev(raw), M, K)
+    Xd = dev(X)
+    Y, path = q6.mmq_f32(w, Xd)
+    act = q6.quantize_act(Xd)
+    Y2, _, _ = q6.mmq(w, act)
+    q6.sync_status()
+    assert path == "skinny_fused" and torch.equal(Y, Y2)
+    xq_o, da_o = quant_check(act, X, orc)
+    check_y(host(Y), orc.mmq(raw, M, K, xq_o, da_o), f"fused K={K} N={N}")
+    K2 = K + 256
+    w2 = q6.pack_weights(dev(synth.q6k_raw_weights(0x51360C23, M, K2)), M, K2)
+    with pytest.raises(q6.Q6Error):
+        q6.mmq_f32(w2, dev(synth.activations(0x51360C24, N, K2)))
+
+
 def test_mmq_f32_strided_input_and_output(q6):
     """X with a wider row stride, Y with an odd row stride at an unaligned
     address: the floats between Y's rows stay untouched, the result equals
