@@ -525,6 +525,20 @@ def test_mmq_f32_equals_quantise_then_mmq(q6, orc, M, K, N):
     check_y(host(Y), Yo, f"fused {M}x{K}x{N}")
 
 
+@pytest.mark.parametrize("N", [1, 9, 130])
+def test_mmq_long_rows(q6, orc, N):
+    """Rows of K = 65,536 (256 super-blocks, several times the longest
+    workload) through the dp4a, few-token and tensor-core kernels: Y within
+    tolerance of the oracle on every output."""
+    M, K = 128, 65536
+    raw = synth.q6k_raw_weights(0x51360C31 + N, M, K)
+    X = synth.activations(0x51360C32 + N, N, K, outlier_frac=0.01)
+    w, act, Y, path, _ = run_gemm(q6, raw, X, M, K, "raw")
+    assert path == ("skinny" if N <= q6.SKINNY_MAX_N else "tc_raw")
+    xq_o, da_o = quant_check(act, X, orc)
+    check_y(host(Y), orc.mmq_all(raw, M, K, xq_o, da_o), f"long rows N={N}")
+
+
 @pytest.mark.parametrize("K,N", [(103168, 2), (206592, 1)], ids=lambda v: str(v))
 def test_mmq_f32_largest_k(q6, orc, K, N):
     """The largest K whose codes and scales fit the fused kernel's shared
