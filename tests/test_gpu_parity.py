@@ -539,6 +539,21 @@ def test_mmq_long_rows(q6, orc, N):
     check_y(host(Y), orc.mmq_all(raw, M, K, xq_o, da_o), f"long rows N={N}")
 
 
+@pytest.mark.parametrize("M,K,N", [(20000, 512, 1), (20000, 512, 5), (20000, 512, 200),
+                                   (128, 256, 20000)], ids=lambda v: str(v))
+def test_mmq_large_extents(q6, orc, M, K, N):
+    """Many weight rows (20,000: several rounds of tiles, a ragged last band,
+    more rows than the few-token kernels' warps and units) and many tokens
+    (20,000 against one band): Y within tolerance of the oracle on every
+    output."""
+    raw = synth.q6k_raw_weights(0x51360C41 + M + N, M, K)
+    X = synth.activations(0x51360C42 + M + N, N, K, outlier_frac=0.01)
+    w, act, Y, path, _ = run_gemm(q6, raw, X, M, K, "raw")
+    assert path == ("skinny" if N <= q6.SKINNY_MAX_N else "tc_raw")
+    xq_o, da_o = quant_check(act, X, orc)
+    check_y(host(Y), orc.mmq_all(raw, M, K, xq_o, da_o), f"large {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("K,N", [(103168, 2), (206592, 1)], ids=lambda v: str(v))
 def test_mmq_f32_largest_k(q6, orc, K, N):
     """The largest K whose codes and scales fit the fused kernel's shared
