@@ -4,7 +4,10 @@
 // tensor-core form in mmq_skinny_mma.cu. Measured on GB300 (ffn_down
 // weights, us per launch, this form / the tensor form): 2 tokens 14.4 / 16.5,
 // 3 tokens 18.1 / 16.5, 4 tokens 24.9 / 17.3; each token adds its own dp4a
-// work, while the tensor form pays once for the weight conversion.
+// work, while the tensor form pays once for the weight conversion. The file
+// also holds the fused kernel behind q6k_mmq_f32 (at its end), which
+// quantises one or two f32 activation rows itself and then runs the same
+// dot products.
 //
 // Math ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.1-2.2): for each
 // 16-element sub-block s the exact integer P = sum (q - 32) * xq is formed
