@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) mmq_skinny_fused_kernel(
     // not kept: two groups per thread with their loads issued together
     // (spills: 11.3 us), the first two steps requested into L2 instead of
     // registers (10.8 us), sixteen elements per thread, one round for a
-    // token (11.0 us; 10.7 with the L2 requests).
+    // token (11.0 us; 10.7 with the L2 requests), and two or six further
+    // steps requested into L2 before the quantisation (11.0 / 11.4 us).
     const int per_row = K >> 3;
     const int total = N * per_row;
     for (int gi = threadIdx.x; gi < total; gi += blockDim.x) {
