@@ -990,6 +990,7 @@ TRAFFIC = {("ffn_down", "mmq_tc"): 667.67e6 + 53.16e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
            ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
+           ("skinny_ffn_down_N2", "mmq_skinny_fused"): 37.14e6,
            ("skinny_ffn_down_N4", "mmq_skinny"): 37.10e6,
            ("skinny_ffn_down_N16", "mmq_skinny"): 37.26e6}
 
