@@ -90,3 +90,35 @@ def test_whole_path_in_a_cuda_graph(q6):
         graph.replay()
         q6.sync_status()
         close(Y, expected(raw, M, K, X))
+
+
+@pytest.mark.parametrize("N", [1, 2])
+def test_fused_call_on_a_side_stream_and_in_a_graph(q6, N):
+    """q6k_mmq_f32 (quantiser and GEMM in one kernel) on a caller's side
+    stream, then captured into a CUDA graph and replayed for two inputs."""
+    import torch
+    M, K = 512, 2048
+    raw = synth.q6k_raw_weights(0x51360911 + N, M, K)
+    X1 = synth.activations(0x51360912 + N, N, K)
+    X2 = synth.activations(0x51360913 + N, N, K, outlier_frac=0.02)
+    w = q6.pack_weights(torch.from_numpy(raw).cuda(), M, K)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        Y, path = q6.mmq_f32(w, torch.from_numpy(X1).cuda(), stream=side)
+    q6.sync_status(side)
+    assert path == "skinny_fused"
+    close(Y, expected(raw, M, K, X1))
+    Xs = torch.from_numpy(X1).cuda()             # static input of the graph
+    Ys = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            q6.mmq_f32(w, Xs, Y=Ys)
+    for X in (X1, X2):
+        Xs.copy_(torch.from_numpy(X).cuda())
+        Ys.fill_(float("nan"))
+        graph.replay()
+        q6.sync_status()
+        close(Ys, expected(raw, M, K, X))
