@@ -487,11 +487,22 @@ def epilogue_alu_bound(clk) -> float:
     return fma_per_s * 32 / 1.125 * 2 / 1e12
 
 
-def tensor_peak(peaks):
-    p = peaks.get("bf16_tflops_sustained")
+def tensor_peak(peaks, sustained: bool = False):
+    """The dense tensor peak a kernel's rate is compared with: the burst
+    figure for a kernel timed on its own with CUDA events, the sustained one
+    for work timed inside a long loop (binary16 has bf16's nominal rate)."""
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    kind = "sustained" if sustained else "burst"
+    p = peaks.get(key)
     if p is None:
-        return 1700.0, "fallback sustained bf16 (f16 has the same nominal dense rate)"
-    return p, "measured bf16 sustained (f16 has the same nominal dense rate)"
+        return (1700.0 if sustained else 1900.0), f"fallback bf16 {kind} (f16 has the same rate)"
+    return p, f"measured bf16 {kind} (f16 has the same nominal dense rate)"
+
+
+def gemm_method_bytes(M, K, N):
+    """The method's own bytes of one GEMM: the q6_K weights at 210 B per 256,
+    the int8 activations and their per-32 f32 scales, and the f32 output."""
+    return M * K * 210 / 256 + N * K + N * (K // 32) * 4 + 4 * N * M
 
 
 def oracle_baseline(raw, X, M, K, budget, N):
@@ -654,6 +665,7 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     if rank != 0:
         return
     peak_t, peak_src = tensor_peak(peaks)
+    peak_s, _ = tensor_peak(peaks, sustained=True)
     tflops = ops_per_step / m_ms / 1e9
     q_bytes = N * K * (4 + (1 if acts[0].xq is not None else 0) + 2) + (K // 32) * N * 4
     # unpack: reads the codes (qlh 0.75 B or W_exp 1 B per weight) and sc
@@ -667,7 +679,19 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         "data": "synthetic", "config": workload_config(args, cfg),
         "roofline": {"bound": "tensor", "kernel": "mmq_tc_kernel (q6k_mmq on the operand plane)",
                      "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": tflops / peak_t, "peak_source": peak_src, "traffic": traffic,
+                     "frac": tflops / peak_t, "peak_source": peak_src,
+                     "timing": "the GEMM kernel alone, CUDA events on its stream, averaged over "
+                               "short back-to-back steps (so the burst peak applies)",
+                     "frac_of_sustained": tflops / peak_s, "traffic": traffic,
+                     "traffic_source": ("dram__bytes_read.sum + dram__bytes_write.sum of one ncu "
+                                        "capture of this kernel on this workload, kept as a "
+                                        "profile summary; null when the kernel has changed since"
+                                        if traffic is not None else "not captured for this "
+                                        "kernel version"),
+                     "algorithmic_bytes": gemm_method_bytes(M, K, N),
+                     "algorithmic_bytes_formula": "M*K*210/256 + N*K + 4*N*K/32 + 4*N*M (the "
+                                                  "method's bytes: q6_K weights, int8 "
+                                                  "activations, scales, f32 Y)",
                      "algorithmic": f"2*M*N*K = {ops_per_step:.4g} flop per launch"},
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": (1 + q6.mmq_launches(M, K, N, src == "wh")) * args.steps,
@@ -691,8 +715,9 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 def other_configs(args, q6, synth, device, hbm):
     """Short measurements of the other workloads beside the headline one: the
-    attn_v GEMM (q6k_mmq, raw plane and resident operand plane) and the skinny
-    memory-bound GEMM for N = 1, 4, 16."""
+    attn_v GEMM (q6k_mmq, raw plane and resident operand plane), the skinny
+    memory-bound GEMM for N = 1, 2, 4, 16, the pages' two shapes and the
+    32-layer sweep."""
     import torch
     raw, X, cfg = synth.workload("attn_v")
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
@@ -718,7 +743,86 @@ def other_configs(args, q6, synth, device, hbm):
     for k, v in skinny_kernel_times(q6, synth, device).items():
         v["frac_hbm"] = v["gbs"] / hbm
         res[f"skinny_{k}"] = v
+    res.update(pages_shapes(q6, synth, device))
+    res["sweep"] = sweep_short(q6, synth, device)
     return res
+
+
+def pages_shapes(q6, synth, device):
+    """The shapes the pages measure (ffn_down 3584x18944, attn_v 512x3584, N =
+    3325): the GEMM kernel on resident operand planes, and the whole step from
+    the packed plane (quantise and unpack on two streams at once, then the
+    GEMM), averaged over back-to-back calls."""
+    import torch
+    out = {}
+    for name in ("pages_ffn_down", "pages_attn_v"):
+        raw, X, cfg = synth.workload(name)
+        M, K, N = cfg["M"], cfg["K"], cfg["N"]
+        W = q6.pack_weights(torch.from_numpy(raw).to(device), M, K, wh=True)
+        Xd = torch.from_numpy(X).to(device)
+        act = q6.alloc_activations(N, K, device, want_xq=False)
+        Y = torch.empty((N, M), dtype=torch.float32, device=device)
+        planes = torch.empty((2, M, K), dtype=torch.float16, device=device)
+        side = torch.cuda.Stream(device)
+        done = torch.cuda.Event()
+
+        def step():
+            cur = torch.cuda.current_stream(device)
+            side.wait_stream(cur)
+            with torch.cuda.stream(side):
+                q6.unpack_weights(W, out=planes)
+                done.record(side)
+            q6.quantize_act(Xd, out=act)
+            cur.wait_event(done)
+            q6.mmq(W, act, Y=Y, source="wh", wh=planes)
+
+        q6.quantize_act(Xd, out=act)
+        res = {}
+        for label, fn in (("gemm_resident_planes", lambda: q6.mmq(W, act, Y=Y, source="wh")),
+                          ("step_from_packed_plane", step)):
+            for _ in range(3):
+                fn()
+            a, b = ev_pair()
+            a.record()
+            for _ in range(20):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            q6.sync_status()
+            ms = a.elapsed_time(b) / 20
+            res[label] = {"ms": ms, "tops": 2.0 * M * N * K / ms / 1e9}
+        out[name] = dict(res, workload=f"{name} q6_K GEMM M={M} K={K} N={N}",
+                         pages_figure_context=("12.76 ms (r53 kernel, GB10)" if name ==
+                                               "pages_ffn_down" else "0.654 ms (r41 kernel, GB10)"))
+        del W, planes
+    return out
+
+
+def sweep_short(q6, synth, device, sweeps: int = 3):
+    """The 32-layer sweep in short: one warm-up sweep, then `sweeps` timed
+    sweeps (quantise and unpack on two streams, then the GEMM, per weight),
+    and the per-kernel GEMM and quantiser totals of one sweep."""
+    import torch
+    sw = Sweep(q6, synth, device)
+    sw.step(0)
+    q6.sync_status()
+    a, b = ev_pair()
+    a.record()
+    for i in range(sweeps):
+        sw.step(i)
+    b.record()
+    torch.cuda.synchronize()
+    q6.sync_status()
+    ms = a.elapsed_time(b) / sweeps
+    gemm_ms, quant_ms = sw.per_kernel(2)
+    q6.sync_status()
+    out = {"workload": f"sweep: {sw.L} layers x (attn_v 4096x4096 + ffn_down 4096x11008), "
+                       f"N={sw.N}",
+           "ms_per_sweep": ms, "tops": sw.ops / ms / 1e9, "sweeps": sweeps,
+           "gemm_total_ms": gemm_ms, "gemm_tops": sw.ops / gemm_ms / 1e9,
+           "quantize_total_ms": quant_ms, "resident_plane_bytes": sw.resident}
+    del sw
+    return out
 
 
 def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
@@ -849,78 +953,107 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     print(json.dumps(line), flush=True)
 
 
+class Sweep:
+    """The 32-layer 7B-shape prefill sweep, set up on the device: per layer a
+    q6_K attn_v (4096x4096) and ffn_down (4096x11008) weight, packed once
+    (the raw planes stay resident), and the two fixed f32 activation streams
+    X_v [3314,4096] and X_d [3314,11008], re-quantised per layer.
+
+    step(i): per GEMM, quantise its stream and unpack its weights on two
+    streams at once, then the GEMM (the timed step).
+    step_seq(i, ev): per layer quantise, unpack + GEMM, one after another,
+    with an event between kernels (per-kernel times)."""
+
+    def __init__(self, q6, synth, device):
+        import torch
+        self.q6, self.device = q6, device
+        self.L, self.N = synth.SWEEP_LAYERS, synth.SWEEP_N
+        N = self.N
+        self.layers = []
+        for l in range(self.L):
+            rv, rd = synth.sweep_layer(l)
+            wv = q6.pack_weights(torch.from_numpy(rv).to(device), 4096, 4096)
+            wd = q6.pack_weights(torch.from_numpy(rd).to(device), 4096, 11008)
+            self.layers.append((wv, wd))
+        self.resident = sum(w.plane.numel() for pair in self.layers for w in pair)
+        self.Xv, self.Xd = synth.sweep_activations()
+        Xvd, Xdd = torch.from_numpy(self.Xv).to(device), torch.from_numpy(self.Xd).to(device)
+        self.av = q6.alloc_activations(N, 4096, device, want_xq=False)
+        self.ad = q6.alloc_activations(N, 11008, device, want_xq=False)
+        self.Yv = torch.empty((N, 4096), dtype=torch.float32, device=device)
+        Yd = torch.empty((N, 4096), dtype=torch.float32, device=device)
+        self.ws = torch.empty(q6.workspace_bytes(4096, 11008, N), dtype=torch.uint8, device=device)
+        self.marks = 1 + 4 * self.L
+        # the streams the end-to-end run copies in and out alternate between
+        # two buffer slots; everything else is used by one step at a time
+        self.Xvds, self.Xdds = [Xvd, Xvd.clone()], [Xdd, Xdd.clone()]
+        self.Yds = [Yd, torch.empty_like(Yd)]
+        self.side = torch.cuda.Stream(device)
+        self.prep, self.unpacked = torch.cuda.Event(), torch.cuda.Event()
+        self.wh = self.ws.view(torch.float16)
+        self.ops = self.L * 2.0 * N * (4096 * 4096 + 4096 * 11008)
+
+    def step_seq(self, i, ev=None):
+        q6 = self.q6
+        k = 0
+        Xvd, Xdd, Yd = self.Xvds[i % 2], self.Xdds[i % 2], self.Yds[i % 2]
+        if ev is not None:
+            ev[0].record()
+        for wv, wd in self.layers:
+            q6.quantize_act(Xvd, out=self.av)
+            if ev is not None:
+                ev[k + 1].record()
+            q6.mmq(wv, self.av, Y=self.Yv, source="raw", workspace=self.ws)
+            if ev is not None:
+                ev[k + 2].record()
+            q6.quantize_act(Xdd, out=self.ad)
+            if ev is not None:
+                ev[k + 3].record()
+            q6.mmq(wd, self.ad, Y=Yd, source="raw", workspace=self.ws)
+            if ev is not None:
+                ev[k + 4].record()
+            k += 4
+
+    def _gemm(self, w, X, act, Y):
+        """quantise X and unpack w on two streams at once, then the GEMM."""
+        import torch
+        q6 = self.q6
+        cur = torch.cuda.current_stream(self.device)
+        self.prep.record(cur)
+        self.side.wait_event(self.prep)
+        planes = self.wh[:2 * w.M * w.K].view(2, w.M, w.K)
+        with torch.cuda.stream(self.side):
+            q6.unpack_weights(w, out=planes)
+            self.unpacked.record(self.side)
+        q6.quantize_act(X, out=act)
+        cur.wait_event(self.unpacked)
+        q6.mmq(w, act, Y=Y, source="wh", wh=planes)
+
+    def step(self, i, ev=None):
+        Xvd, Xdd, Yd = self.Xvds[i % 2], self.Xdds[i % 2], self.Yds[i % 2]
+        for wv, wd in self.layers:
+            self._gemm(wv, Xvd, self.av, self.Yv)
+            self._gemm(wd, Xdd, self.ad, Yd)
+
+    def per_kernel(self, sweeps: int):
+        """(GEMM ms, quantiser ms) summed over one sweep, kernels in sequence."""
+        per = kernel_ms(self.step_seq, sweeps, self.marks)
+        quant_ms = sum(per[k] for k in range(0, 4 * self.L, 2))
+        gemm_ms = sum(per[k] for k in range(1, 4 * self.L, 2))
+        return gemm_ms, quant_ms
+
+
 def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     """The 32-layer 7B-shape prefill sweep: per layer, requantise the attn_v
     stream X_v [3314,4096] and run the attn_v GEMM, then requantise X_d
     [3314,11008] and run the ffn_down GEMM (both from the packed raw plane,
     unpacked per call). One step = the whole sweep."""
     import torch
-    L = synth.SWEEP_LAYERS
-    N = synth.SWEEP_N
-    layers = []
-    for l in range(L):
-        rv, rd = synth.sweep_layer(l)
-        wv = q6.pack_weights(torch.from_numpy(rv).to(device), 4096, 4096)
-        wd = q6.pack_weights(torch.from_numpy(rd).to(device), 4096, 11008)
-        layers.append((wv, wd))
-    resident = sum(w.plane.numel() for pair in layers for w in pair)
-    Xv, Xd = synth.sweep_activations()
-    Xvd, Xdd = torch.from_numpy(Xv).to(device), torch.from_numpy(Xd).to(device)
-    av = q6.alloc_activations(N, 4096, device, want_xq=False)
-    ad = q6.alloc_activations(N, 11008, device, want_xq=False)
-    Yv = torch.empty((N, 4096), dtype=torch.float32, device=device)
-    Yd = torch.empty((N, 4096), dtype=torch.float32, device=device)
-    ws = torch.empty(q6.workspace_bytes(4096, 11008, N), dtype=torch.uint8, device=device)
-    marks = 1 + 4 * L
-
-    # the streams the end-to-end run copies in and out alternate between two
-    # buffer slots; everything else is used by one step at a time
-    Xvds, Xdds = [Xvd, Xvd.clone()], [Xdd, Xdd.clone()]
-    Yds = [Yd, torch.empty_like(Yd)]
-
-    def step_seq(i, ev=None):
-        """Per layer: quantise, unpack + GEMM, one after another (per-kernel
-        event timing)."""
-        k = 0
-        Xvd, Xdd, Yd = Xvds[i % 2], Xdds[i % 2], Yds[i % 2]
-        if ev is not None:
-            ev[0].record()
-        for wv, wd in layers:
-            q6.quantize_act(Xvd, out=av)
-            if ev is not None:
-                ev[k + 1].record()
-            q6.mmq(wv, av, Y=Yv, source="raw", workspace=ws)
-            if ev is not None:
-                ev[k + 2].record()
-            q6.quantize_act(Xdd, out=ad)
-            if ev is not None:
-                ev[k + 3].record()
-            q6.mmq(wd, ad, Y=Yd, source="raw", workspace=ws)
-            if ev is not None:
-                ev[k + 4].record()
-            k += 4
-
-    side = torch.cuda.Stream(device)
-    prep, unpacked = torch.cuda.Event(), torch.cuda.Event()
-    wh = ws.view(torch.float16)
-
-    def gemm(w, X, act, Y):
-        """quantise X and unpack w on two streams at once, then the GEMM."""
-        cur = torch.cuda.current_stream(device)
-        prep.record(cur)
-        side.wait_event(prep)
-        with torch.cuda.stream(side):
-            q6.unpack_weights(w, out=wh[:2 * w.M * w.K].view(2, w.M, w.K))
-            unpacked.record(side)
-        q6.quantize_act(X, out=act)
-        cur.wait_event(unpacked)
-        q6.mmq(w, act, Y=Y, source="wh", wh=wh[:2 * w.M * w.K].view(2, w.M, w.K))
-
-    def step(i, ev=None):
-        Xvd, Xdd, Yd = Xvds[i % 2], Xdds[i % 2], Yds[i % 2]
-        for wv, wd in layers:
-            gemm(wv, Xvd, av, Yv)
-            gemm(wd, Xdd, ad, Yd)
+    sw = Sweep(q6, synth, device)
+    L, N = sw.L, sw.N
+    step, step_seq = sw.step, sw.step_seq
+    Xv, Xd, Xvds, Xdds, Yds = sw.Xv, sw.Xd, sw.Xvds, sw.Xdds, sw.Yds
+    resident = sw.resident
 
     for i in range(args.warmup):
         step(i)
@@ -928,10 +1061,8 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     steps = args.steps
     max_ms, clk = timed_region(step, steps, device, rank == 0)
     q6.sync_status()
-    per = kernel_ms(step_seq, 3, marks)
-    quant_ms = sum(per[k] for k in range(0, 4 * L, 2))
-    gemm_ms = sum(per[k] for k in range(1, 4 * L, 2))
-    ops_per_step = L * 2.0 * N * (4096 * 4096 + 4096 * 11008)
+    gemm_ms, quant_ms = sw.per_kernel(3)
+    ops_per_step = sw.ops
     value = job_throughput(ops_per_step * steps, world, max_ms / 1e3) / 1e12
     e2e = None
     if args.e2e_steps > 0:
@@ -952,7 +1083,7 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         cpu = c
     if rank != 0:
         return
-    peak_t, peak_src = tensor_peak(peaks)
+    peak_t, peak_src = tensor_peak(peaks, sustained=True)
     tflops = ops_per_step / gemm_ms / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
@@ -981,11 +1112,8 @@ def run_sweep(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 SKINNY_DP4A_MAX_N = 2
 SKINNY_FUSED_MAX_N = 2
 
-# ncu captures of the current kernels, keyed by (workload, kernel); the
-# captures are summarised under profiles/ (mmq_tc_ffn_down.md,
-# mmq_skinny_ffn_down_n1.md for one and two tokens,
-# mmq_skinny_mma_ffn_down_n16.md). An entry is
-# removed when its kernel changes.
+# DRAM bytes per launch from ncu captures of the current kernels, keyed by
+# (workload, kernel). An entry is removed when its kernel changes.
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.67e6 + 53.16e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
            ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,

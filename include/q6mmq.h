@@ -113,9 +113,15 @@ int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da
  * Weight packing (load time; "r53 -- q6_K bundle: W_exp pre-expansion
  * plane", Sec. 2.3 and 3.2).
  *
- * raw: device bytes of an M x K q6_K weight in the GGUF layout: M rows, each
+ * raw: the bytes of an M x K q6_K weight in the GGUF layout: M rows, each
  *      K/256 consecutive 210-byte super-blocks (ql[128] @0, qh[64] @128,
  *      sc[16] int8 @192, d f16 little endian @208). No alignment needed.
+ *      Device memory, or host memory the device reads directly: page-locked
+ *      host memory (cudaHostAlloc / cudaHostRegister), or any host memory on
+ *      a device that reads pageable memory (cudaDevAttrPageableMemoryAccess,
+ *      e.g. Grace-Blackwell's coherent host memory); other pageable host
+ *      memory gives Q6_EINVAL. The pack kernel reads raw asynchronously on
+ *      stream s: host memory must stay valid until the stream has passed it.
  *
  * plane (device, 256-byte aligned, q6k_plane_bytes() bytes), four sub-planes
  * at 256-byte aligned offsets, in this order:
@@ -168,17 +174,26 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *           stream the packed plane once).
  *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
  *   workspace : device scratch of at least q6k_mmq_workspace_bytes() bytes
- *           (4 * M * K, 256-byte aligned) when N > Q6_SKINNY_MAX_N and wh is
- *           NULL: the weights are first unpacked there (from wexp when given,
- *           else from the packed plane) into the two binary16 operand planes.
+ *           (4 * M * K, 256-byte aligned) when N > Q6_SKINNY_MAX_N and either
+ *           wh is NULL or partials is not NULL: the weights are first unpacked
+ *           there (from wexp when given, else from the packed plane) into the
+ *           two binary16 operand planes, and the debug passes below reuse it.
  *           Unused otherwise. Its contents after the call are unspecified.
- *   partials : NULL, or device int32 [N][M][K/32] that receives every exact
- *           chunk sum S[n][m][c] = sc[2c] * P[2c] + sc[2c+1] * P[2c+1], with
- *           P[s] = sum over the 16 elements of sub-block s of (q - 32) * xq
- *           (a debug mode; slower).
+ *   partials : NULL, or device int32 [N][M][K/16] that receives every exact
+ *           sub-block partial P[n][m][s] = sum over the 16 elements k of
+ *           sub-block s of (q[m][k] - 32) * xq[n][k] (the debug mode of "r38
+ *           -- q6_K BT-style raw-byte mma kernel", Sec. 2.4: one int32 per
+ *           sub-block; slower). The few-token kernels and the mma.sync path
+ *           write the P they form; the tensor-core path, whose operands carry
+ *           the sub-block scale, forms them in two more GEMM launches on
+ *           planes unpacked with unit scale (W_hi = 0, W_lo = v on the
+ *           sub-blocks of one parity, 0 on the others) in the workspace.
+ *   chunk_sums : NULL, or device int32 [N][M][K/32] that receives the exact
+ *           integer the kernel itself forms per 32-element chunk c,
+ *           S[n][m][c] = sc[2c] * P[2c] + sc[2c+1] * P[2c+1] (debug).
  *   path_out : NULL or receives a Q6_PATH_* code.
- * Alignment: plane, workspace 256 B; Xh, da, wexp, wh, Xq 16 B; Y 4 B.
- * Q6_ESIZE when the workspace is missing or too small.
+ * Alignment: plane, workspace 256 B; Xh, da, wexp, wh, Xq 16 B; Y, partials,
+ * chunk_sums 4 B. Q6_ESIZE when a needed workspace is missing or too small.
  *
  * Work split: the tensor-core path walks 128 x 128 output tiles with one
  * persistent CTA per SM. When the last round of tiles would leave more than
@@ -200,8 +215,8 @@ int q6k_mmq_launches(int M, int K, int N, int has_wh, int *launches);
 
 int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, int K,
             const int8_t *Xq, const float *da, const uint16_t *Xh, int N, float *Y, int ldy,
-            void *workspace, size_t workspace_bytes, int32_t *partials, int *path_out,
-            q6_stream_t s);
+            void *workspace, size_t workspace_bytes, int32_t *partials, int32_t *chunk_sums,
+            int *path_out, q6_stream_t s);
 
 /* ------------------------------------------------------------------------
  * The pages' own route on the legacy warp-level tensor path, kept as a
@@ -209,18 +224,20 @@ int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, in
  * kernel", Sec. 2.2-2.4; "r53 -- q6_K bundle: W_exp pre-expansion plane",
  * Sec. 2.3): exact int32 sub-block partials from int8 mma.sync on the W_exp
  * plane and Xq, sc folded per 32-element chunk in integers, f32 rescale.
- * Same result contract as q6k_mmq (Y within the same tolerance; partials, when
- * not NULL, are the same int32 [N][M][K/32] chunk sums).
+ * Same result contract as q6k_mmq (Y within the same tolerance; partials and
+ * chunk_sums, when not NULL, are the same int32 [N][M][K/16] sub-block
+ * partials and [N][M][K/32] chunk sums, written by the GEMM kernel itself).
  *
  *   plane : packed weights (its sc and dT sub-planes are read); required.
  *   wexp  : the W_exp plane; required.
  *   Xq, da: quantised activations (any N >= 0).
- * Alignment: plane 256 B; wexp, Xq, da 16 B; Y, partials 4 B. Allocates
- * nothing. path_out receives Q6_PATH_SYNC_WEXP (or Q6_PATH_NONE for N == 0).
+ * Alignment: plane 256 B; wexp, Xq, da 16 B; Y, partials, chunk_sums 4 B.
+ * Allocates nothing. path_out receives Q6_PATH_SYNC_WEXP (or Q6_PATH_NONE for
+ * N == 0).
  * -------------------------------------------------------------------- */
 int q6k_mmq_mma_sync(const void *plane, const int8_t *wexp, int M, int K, const int8_t *Xq,
-                     const float *da, int N, float *Y, int ldy, int32_t *partials, int *path_out,
-                     q6_stream_t s);
+                     const float *da, int N, float *Y, int ldy, int32_t *partials,
+                     int32_t *chunk_sums, int *path_out, q6_stream_t s);
 
 /* ------------------------------------------------------------------------
  * For callers that cannot allocate device memory when they make this call
@@ -234,18 +251,25 @@ int q6k_mmq_mma_sync(const void *plane, const int8_t *wexp, int M, int K, const 
  * library: 256 bytes for the kernel's status word plus 64 MiB for the
  * two unpacked binary16 operand planes, so for N > Q6_SKINNY_MAX_N it needs
  * M * K <= 16,777,216 (a 4096 x 4096 layer) and returns Q6_ESIZE otherwise.
- * Nothing on this path allocates; no partials (debug) output.
+ * Nothing on this path allocates; no debug outputs.
  *
  * The array is held by every GPU that loads this part of the library until
  * the process exits. All calls share it and it keeps the last call's
  * contents: calls that overlap on the GPU race on it. The status word is
  * cleared on the call's stream at the start of every call; a bounded-wait
- * time-out is recorded there and is not reported back. The first call on a
- * device does the set-up (architecture check, kernel attributes, the array's
- * device address) and should come before any stream capture. */
+ * time-out is recorded there and q6k_mmq_noalloc_status() reports it. The
+ * first call on a device does the set-up (architecture check, kernel
+ * attributes, the array's device address) and should come before any stream
+ * capture. */
 int q6k_mmq_noalloc(const void *plane, const int8_t *wexp, int M, int K, const int8_t *Xq,
                     const float *da, const uint16_t *Xh, int N, float *Y, int ldy, int *path_out,
                     q6_stream_t s);
+
+/* The status of the q6k_mmq_noalloc calls on this device: waits for stream
+ * `s`, then reads and clears the status word in the static array. Returns
+ * Q6_OK, Q6_ETIMEOUT (a kernel gave up a bounded wait; the text names the
+ * wait) or Q6_ECUDA. Allocates nothing. No counterpart in the pages. */
+int q6k_mmq_noalloc_status(q6_stream_t s);
 
 /* ------------------------------------------------------------------------
  * One or two tokens straight from f32 activations, in one kernel launch:

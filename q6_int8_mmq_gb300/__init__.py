@@ -12,6 +12,7 @@ import ctypes
 import dataclasses
 import functools
 import os
+from typing import NamedTuple
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
@@ -40,10 +41,11 @@ SIGNATURES = [
     ("q6k_unpack_weights", _I, [_P, _P, _I, _I, _P, _P]),
     ("q6k_mmq_workspace_bytes", _I, [_I, _I, _I, _SZ]),
     ("q6k_mmq_launches", _I, [_I, _I, _I, _I, _IP]),
-    ("q6k_mmq", _I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP,
-                     _P]),
+    ("q6k_mmq", _I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _P,
+                     _IP, _P]),
     ("q6k_mmq_noalloc", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _IP, _P]),
-    ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _IP, _P]),
+    ("q6k_mmq_noalloc_status", _I, [_P]),
+    ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _IP, _P]),
     ("q6k_mmq_f32", _I, [_P, _I, _I, _P, _I, _I, _P, _I, _IP, _P]),
 ]
 
@@ -225,17 +227,35 @@ class Weights:
         return self.plane.device
 
 
-def pack_weights(raw, M: int, K: int, wexp: bool = False, wh: bool = False, stream=None) -> Weights:
-    """Packs raw GGUF q6_K bytes (a uint8 CUDA tensor of M*K/256*210 bytes)."""
+def pack_weights(raw, M: int, K: int, wexp: bool = False, wh: bool = False, stream=None,
+                 device=None) -> Weights:
+    """Packs raw GGUF q6_K bytes: a contiguous uint8 tensor of M*K/256*210
+    bytes, on a CUDA device (the planes go there) or in host memory (the
+    planes go to `device`, default the current CUDA device). A host tensor is
+    page-locked first unless it already is, and the call waits for the pack
+    kernel, which reads it directly, before returning."""
     import torch
     pb, wb = plane_bytes(M, K)
-    if raw.numel() != M * (K // 256) * 210 or raw.dtype != torch.uint8 or not raw.is_cuda:
-        raise Q6Error(Q6_EINVAL, "raw must be a CUDA uint8 tensor of M*K/256*210 bytes")
-    plane = torch.empty(pb, dtype=torch.uint8, device=raw.device)
-    w8 = torch.empty((M, K), dtype=torch.int8, device=raw.device) if wexp else None
-    w16 = torch.empty((2, M, K), dtype=torch.float16, device=raw.device) if wh else None
-    _check(load().q6k_pack_weights(_ptr(raw), M, K, _ptr(plane), _ptr(w8), _ptr(w16),
-                                   _stream(stream)))
+    if (not isinstance(raw, torch.Tensor) or raw.numel() != M * (K // 256) * 210
+            or raw.dtype != torch.uint8 or not raw.is_contiguous()):
+        raise Q6Error(Q6_EINVAL, "raw must be a contiguous uint8 tensor of M*K/256*210 bytes")
+    on_host = not raw.is_cuda
+    if on_host:
+        dev = torch.device(device) if device is not None else torch.device(
+            "cuda", torch.cuda.current_device())
+        if not raw.is_pinned():
+            raw = raw.pin_memory()
+    else:
+        dev = raw.device
+    plane = torch.empty(pb, dtype=torch.uint8, device=dev)
+    w8 = torch.empty((M, K), dtype=torch.int8, device=dev) if wexp else None
+    w16 = torch.empty((2, M, K), dtype=torch.float16, device=dev) if wh else None
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        _check(load().q6k_pack_weights(_ptr(raw), M, K, _ptr(plane), _ptr(w8), _ptr(w16),
+                                       _stream(s)))
+        if on_host:
+            s.synchronize()      # the kernel has read the host bytes
     return Weights(M, K, plane, w8, w16)
 
 
@@ -270,6 +290,24 @@ def mmq_launches(M: int, K: int, N: int, has_wh: bool) -> int:
     return n.value
 
 
+class Debug(NamedTuple):
+    """The GEMM's optional debug outputs (int32 CUDA tensors, or None):
+    partials [N, M, K/16], the exact P = sum over each 16-element sub-block of
+    (q - 32) * xq; chunk_sums [N, M, K/32], the exact S = sc[2c] * P[2c] +
+    sc[2c+1] * P[2c+1] that the kernel forms per 32-element chunk."""
+    partials: object = None
+    chunk_sums: object = None
+
+
+def _debug_buffers(N, M, K, partials, chunk_sums, dev):
+    import torch
+    if not (partials or chunk_sums):
+        return None
+    return Debug(
+        torch.empty((N, M, K // 16), dtype=torch.int32, device=dev) if partials else None,
+        torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if chunk_sums else None)
+
+
 _workspaces = {}
 
 
@@ -285,10 +323,10 @@ def _workspace(nbytes: int, device):
 
 
 def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bool = False,
-        workspace=None, wh=None, stream=None):
-    """Y [N, M] f32 = the q6_K x int8 GEMM. Returns (Y, path name, partials or None);
-    partials (debug) are the exact chunk sums S [N, M, K/32] int32 of
-    sc * (q - 32) * xq over each 32-element chunk.
+        workspace=None, wh=None, stream=None, chunk_sums: bool = False):
+    """Y [N, M] f32 = the q6_K x int8 GEMM. Returns (Y, path name, Debug or
+    None): with partials=True and/or chunk_sums=True the debug outputs (see
+    Debug) are filled as well.
 
     source: "raw" (unpack the packed plane), "wexp" (convert the W_exp plane),
     "wh" (resident binary16 plane) or "auto" (wh, else wexp, else raw)."""
@@ -310,8 +348,8 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
     if Y is None:
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
     _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
-    P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
-    ws_need = workspace_bytes(M, K, N) if w16 is None else 0
+    D = _debug_buffers(N, M, K, partials, chunk_sums, dev)
+    ws_need = workspace_bytes(M, K, N) if (w16 is None or partials) else 0
     if workspace is not None:
         _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
                 tuple(getattr(workspace, "shape", ())), dev)
@@ -319,9 +357,10 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     path = ctypes.c_int(-1)
     _check(load().q6k_mmq(_ptr(w.plane), _ptr(wx), _ptr(w16), M, K, _ptr(act.xq), _ptr(act.da),
-                          _ptr(act.xh), N, _ptr(Y), _row_stride(Y), _ptr(ws), ws_bytes, _ptr(P),
-                          ctypes.byref(path), _stream(stream)))
-    return Y, PATH_NAMES.get(path.value, str(path.value)), P
+                          _ptr(act.xh), N, _ptr(Y), _row_stride(Y), _ptr(ws), ws_bytes,
+                          _ptr(D and D.partials), _ptr(D and D.chunk_sums), ctypes.byref(path),
+                          _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value)), D
 
 
 def mmq_f32(w: Weights, X, Y=None, stream=None):
@@ -343,9 +382,11 @@ def mmq_f32(w: Weights, X, Y=None, stream=None):
     return Y, PATH_NAMES.get(path.value, str(path.value))
 
 
-def mmq_mma_sync(w: Weights, act: Activations, Y=None, partials: bool = False, stream=None):
+def mmq_mma_sync(w: Weights, act: Activations, Y=None, partials: bool = False, stream=None,
+                 chunk_sums: bool = False):
     """The same GEMM on the legacy mma.sync int8 path (the pages' route), from
-    the W_exp plane: a comparison point for mmq(). Returns (Y, path, partials)."""
+    the W_exp plane: a comparison point for mmq(). Returns (Y, path, Debug or
+    None)."""
     import torch
     N, M, K = act.N, w.M, w.K
     if act.K != K:
@@ -358,12 +399,12 @@ def mmq_mma_sync(w: Weights, act: Activations, Y=None, partials: bool = False, s
     if Y is None:
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
     _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
-    P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
+    D = _debug_buffers(N, M, K, partials, chunk_sums, dev)
     path = ctypes.c_int(-1)
     _check(load().q6k_mmq_mma_sync(_ptr(w.plane), _ptr(w.wexp), M, K, _ptr(act.xq), _ptr(act.da), N,
-                                   _ptr(Y), _row_stride(Y), _ptr(P), ctypes.byref(path),
-                                   _stream(stream)))
-    return Y, PATH_NAMES.get(path.value, str(path.value)), P
+                                   _ptr(Y), _row_stride(Y), _ptr(D and D.partials),
+                                   _ptr(D and D.chunk_sums), ctypes.byref(path), _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value)), D
 
 
 def sync_status(stream=None):

@@ -36,6 +36,20 @@ struct DevState {
 std::mutex g_mu;
 DevState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+// The driver's tensor-map encoder, looked up once (allocates nothing).
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
 
 // The calling thread's current device, checked to be sm_103 and prepared
 // (status block allocated, kernel attributes raised) on first use.
@@ -60,15 +74,7 @@ int device_state(DevState** out) {
     if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()) ||
         (e = q6::mmq_sync_prepare()))
       return cuda_fail(e, "cudaFuncSetAttribute");
-    if (!g_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                           cudaEnableDefault, &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-        return fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
+    if (!encoder()) return fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
     st.arch_ok = 1;
     st.init = true;
   }
@@ -85,6 +91,7 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
+  if (!encoder()) return fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
   CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -100,7 +107,8 @@ namespace q6 {
 // Tensor maps of one GEMM call: Xh [N][K] and the two weight operand planes
 // (W_hi at wop, W_lo at wop + M*K) as 64 x 128 boxes with the 128-byte
 // swizzle, da [K/32][ldda] as 128 tokens x 8 chunks, and the transposed d
-// sub-plane [K/256][ldm] as 128 rows x 1 super-block.
+// sub-plane [K/256][ldm] as 128 rows x 1 super-block. Allocates nothing (the
+// no-allocation entry point uses it too).
 int encode_tc_maps(TcMaps* maps, const uint8_t* plane, const void* wop, const void* Xh,
                    const float* da, int M, int K, int N) {
   const PlaneGeom g = plane_geom(M, K);
@@ -214,7 +222,27 @@ int q6k_pack_weights(const uint8_t* raw, int M, int K, void* plane, int8_t* wexp
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
-  cudaError_t e = q6::launch_pack(raw, M, K, static_cast<uint8_t*>(plane), wexp, (cudaStream_t)s);
+  // raw may be device memory or host memory this device reads directly:
+  // page-locked (registered or cudaHostAlloc'd; its device pointer is used),
+  // or any host memory when the device reads pageable memory (coherent
+  // host memory, as on Grace-Blackwell).
+  const uint8_t* src = raw;
+  cudaPointerAttributes pa;
+  cudaError_t e = cudaPointerGetAttributes(&pa, raw);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(raw)");
+  if (pa.type == cudaMemoryTypeHost && pa.devicePointer) {
+    src = static_cast<const uint8_t*>(pa.devicePointer);
+  } else if (pa.type == cudaMemoryTypeUnregistered) {
+    int dev = 0, pageable = 0;
+    if ((e = cudaGetDevice(&dev)) ||
+        (e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev)))
+      return cuda_fail(e, "cudaDeviceGetAttribute(pageable memory access)");
+    if (!pageable)
+      return fail(Q6_EINVAL,
+                  "raw is pageable host memory this device cannot read: page-lock it "
+                  "(cudaHostRegister) or copy it to the device");
+  }
+  e = q6::launch_pack(src, M, K, static_cast<uint8_t*>(plane), wexp, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "q6k_pack_weights launch");
   if (wh) {
     e = q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K,
@@ -249,6 +277,32 @@ int q6k_mmq_workspace_bytes(int M, int K, int N, size_t* bytes) {
   return Q6_OK;
 }
 
+// The sub-block partials P of the tensor-core path (debug): two more GEMM
+// launches on operand planes unpacked into the workspace with unit scale,
+// W_hi = 0 and W_lo = v on the sub-blocks of one parity (0 on the others),
+// so each chunk accumulator holds P of one of its two sub-blocks; Y is left
+// as the main launch wrote it.
+static int tc_subblock_partials(const uint8_t* pb, int M, int K, int N, const uint16_t* Xh,
+                                const float* da, float* Y, int ldy, __half* ws, int32_t* partials,
+                                unsigned int* status, cudaStream_t s) {
+  for (int parity = 0; parity < 2; ++parity) {
+    cudaError_t e = q6::launch_expand_unit(pb, M, K, parity, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e, "debug unpack launch");
+    q6::TcMaps maps;
+    int rc = q6::encode_tc_maps(&maps, pb, ws, Xh, da, M, K, N);
+    if (rc) return rc;
+    q6::TcDebugOut dbg;
+    dbg.out = partials;
+    dbg.stride = K / 16;
+    dbg.mul = 2;
+    dbg.add = parity;
+    dbg.write_y = 0;
+    if ((e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, dbg, status, s)) != cudaSuccess)
+      return cuda_fail(e, "debug tensor-core kernel launch");
+  }
+  return Q6_OK;
+}
+
 int q6k_mmq_launches(int M, int K, int N, int has_wh, int* launches) {
   if (M <= 0 || K <= 0 || K % 256 || N < 0 || !launches)
     return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0, launches != NULL");
@@ -272,8 +326,8 @@ int q6k_mmq_launches(int M, int K, int N, int has_wh, int* launches) {
 
 int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, int K,
             const int8_t* Xq, const float* da, const uint16_t* Xh, int N, float* Y, int ldy,
-            void* workspace, size_t workspace_bytes, int32_t* partials, int* path_out,
-            q6_stream_t s) {
+            void* workspace, size_t workspace_bytes, int32_t* partials, int32_t* chunk_sums,
+            int* path_out, q6_stream_t s) {
   if (path_out) *path_out = Q6_PATH_NONE;
   if (M <= 0 || K <= 0 || K % 256 || N < 0)
     return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
@@ -286,23 +340,27 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   if (!aligned(plane, 256) || !aligned(da, 16) || !aligned(Y, 4) ||
       (wexp && !aligned(wexp, 16)) || (wh && !aligned(wh, 16)) || (Xq && !aligned(Xq, 16)) ||
       (Xh && !aligned(Xh, 16)) || (partials && !aligned(partials, 4)) ||
-      (workspace && !aligned(workspace, 256)))
-    return fail(Q6_EALIGN, "plane, workspace 256 B; Xq, Xh, da, wexp, wh 16 B; Y, partials 4 B");
+      (chunk_sums && !aligned(chunk_sums, 4)) || (workspace && !aligned(workspace, 256)))
+    return fail(Q6_EALIGN,
+                "plane, workspace 256 B; Xq, Xh, da, wexp, wh 16 B; Y, partials, chunk_sums 4 B");
   if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
     return fail(Q6_ESIZE, "problem too large");
-  if (!skinny && !wh) {
+  if (!skinny && (!wh || partials)) {
     const size_t need = (size_t)M * (size_t)K * 4;
     if (!workspace || workspace_bytes < need)
       return fail(Q6_ESIZE, "workspace of %zu bytes needed to unpack the weights (got %zu)", need,
                   workspace ? workspace_bytes : (size_t)0);
   }
+  q6::Debug dbg;
+  dbg.partials = partials;
+  dbg.chunk_sums = chunk_sums;
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
   cudaError_t e;
   if (skinny) {
     e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda_of(N), N, Y,
-                              ldy, partials, st->status, (cudaStream_t)s);
+                              ldy, dbg, st->status, (cudaStream_t)s);
     if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
     if (path_out) *path_out = Q6_PATH_SKINNY;
     return Q6_OK;
@@ -324,8 +382,15 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   }
   q6::TcMaps maps;
   if ((rc = encode_tc_maps(&maps, pb, wop, Xh, da, M, K, N))) return rc;
-  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, partials, st->status, (cudaStream_t)s);
+  q6::TcDebugOut tdbg;
+  tdbg.out = chunk_sums;
+  tdbg.stride = K / 32;
+  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, tdbg, st->status, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+  if (partials &&
+      (rc = tc_subblock_partials(pb, M, K, N, Xh, da, Y, ldy, static_cast<__half*>(workspace),
+                                 partials, st->status, (cudaStream_t)s)))
+    return rc;
   if (path_out) *path_out = path;
   return Q6_OK;
 }
@@ -356,8 +421,8 @@ int q6k_mmq_f32(const void* plane, int M, int K, const float* X, int ldx, int N,
 }
 
 int q6k_mmq_mma_sync(const void* plane, const int8_t* wexp, int M, int K, const int8_t* Xq,
-                     const float* da, int N, float* Y, int ldy, int32_t* partials, int* path_out,
-                     q6_stream_t s) {
+                     const float* da, int N, float* Y, int ldy, int32_t* partials,
+                     int32_t* chunk_sums, int* path_out, q6_stream_t s) {
   if (path_out) *path_out = Q6_PATH_NONE;
   if (M <= 0 || K <= 0 || K % 256 || N < 0)
     return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
@@ -366,15 +431,19 @@ int q6k_mmq_mma_sync(const void* plane, const int8_t* wexp, int M, int K, const 
   if (!plane || !wexp || !Xq || !da || !Y)
     return fail(Q6_EINVAL, "plane, wexp, Xq, da and Y are required");
   if (!aligned(plane, 256) || !aligned(wexp, 16) || !aligned(Xq, 16) || !aligned(da, 16) ||
-      !aligned(Y, 4) || (partials && !aligned(partials, 4)))
-    return fail(Q6_EALIGN, "plane 256 B; wexp, Xq, da 16 B; Y, partials 4 B");
+      !aligned(Y, 4) || (partials && !aligned(partials, 4)) ||
+      (chunk_sums && !aligned(chunk_sums, 4)))
+    return fail(Q6_EALIGN, "plane 256 B; wexp, Xq, da 16 B; Y, partials, chunk_sums 4 B");
   if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
     return fail(Q6_ESIZE, "problem too large");
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
+  q6::Debug dbg;
+  dbg.partials = partials;
+  dbg.chunk_sums = chunk_sums;
   cudaError_t e = q6::launch_mmq_sync(static_cast<const uint8_t*>(plane), wexp, M, K, Xq, da,
-                                      ldda_of(N), N, Y, ldy, partials, (cudaStream_t)s);
+                                      ldda_of(N), N, Y, ldy, dbg, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "mma.sync kernel launch");
   if (path_out) *path_out = Q6_PATH_SYNC_WEXP;
   return Q6_OK;

@@ -71,9 +71,13 @@ __device__ __forceinline__ void store_folded8(const uint32_t (&o)[4], int sc, __
 // in one contiguous 512-byte run of W_hi or W_lo. A lane reads the 8 ql bytes
 // and the 8 qh bytes of its elements (sub-block s of half h = s / 8 is group
 // j = s % 8 of the element map) and the sub-block's scale.
+// kUnit (debug planes): the scale is replaced by 1 on the sub-blocks of
+// parity `parity` and by 0 on the others, so W_hi = 0 and W_lo is v or 0.
+template <bool kUnit>
 __global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restrict__ qlh,
                                                          const int8_t* __restrict__ sc, int M, int K,
-                                                         size_t qlh_row, __half* __restrict__ wh) {
+                                                         size_t qlh_row, int parity,
+                                                         __half* __restrict__ wh) {
   const int nsb = K / 256;
   const long long blocks = (long long)M * nsb;  // super-blocks
   const long long wstride = (long long)gridDim.x * (blockDim.x >> 5);
@@ -87,7 +91,7 @@ __global__ void __launch_bounds__(256) expand_raw_kernel(const uint8_t* __restri
     const uint8_t* src = qlh + (size_t)m * qlh_row + (size_t)sb * 192 + 96 * h;
     const uint2 L = __ldg(reinterpret_cast<const uint2*>(src + 16 * (j & 3) + 8 * p));
     const uint2 H = __ldg(reinterpret_cast<const uint2*>(src + 64 + 16 * (j & 1) + 8 * p));
-    const int scv = __ldg(sc + (size_t)m * (K / 16) + 16 * sb + s);
+    const int scv = kUnit ? (int)((s & 1) == parity) : __ldg(sc + (size_t)m * (K / 16) + 16 * sb + s);
     uint32_t o[4];
     codes_to_f16(((L.x >> nsh) & 0x0F0F0F0Fu) | (((H.x >> fsh) & 0x03030303u) << 4), o[0], o[1]);
     codes_to_f16(((L.y >> nsh) & 0x0F0F0F0Fu) | (((H.y >> fsh) & 0x03030303u) << 4), o[2], o[3]);
@@ -122,8 +126,16 @@ unsigned grid_for(long long items) {
 
 cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
-  expand_raw_kernel<<<grid_for((long long)M * (K / 256) * 32), 256, 0, s>>>(
-      plane + g.qlh_off, reinterpret_cast<const int8_t*>(plane + g.sc_off), M, K, g.qlh_row, wh);
+  expand_raw_kernel<false><<<grid_for((long long)M * (K / 256) * 32), 256, 0, s>>>(
+      plane + g.qlh_off, reinterpret_cast<const int8_t*>(plane + g.sc_off), M, K, g.qlh_row, 0, wh);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand_unit(const uint8_t* plane, int M, int K, int parity, __half* wh,
+                               cudaStream_t s) {
+  const PlaneGeom g = plane_geom(M, K);
+  expand_raw_kernel<true><<<grid_for((long long)M * (K / 256) * 32), 256, 0, s>>>(
+      plane + g.qlh_off, nullptr, M, K, g.qlh_row, parity, wh);
   return cudaGetLastError();
 }
 

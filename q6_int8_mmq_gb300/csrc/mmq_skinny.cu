@@ -86,7 +86,8 @@ __device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a,
                                          uint16_t dbits, int sb, int m, int M, int K,
                                          const int8_t* __restrict__ Xq,
                                          const float* __restrict__ da, int ldda, int N,
-                                         int32_t* __restrict__ partials, float (&acc)[kMaxN]) {
+                                         int32_t* __restrict__ partials,
+                                         int32_t* __restrict__ chunks, float (&acc)[kMaxN]) {
   const int lane = threadIdx.x & 31;
   const int half = (lane >> 2) & 1;
   const int s4 = lane & 3;
@@ -116,15 +117,21 @@ __device__ __forceinline__ void step_dot(const uint4 L, const uint4 H, int sc_a,
       dot_pair(L, H, fsh, xa, xb, pa, pb);
       // sc * P is an integer below 2^24 in magnitude: exact in f32
       acc[n] = fmaf(d, fmaf(dab, (float)(sc_b * pb), daa * (float)(sc_a * pa)), acc[n]);
-      if (kPartials) {
-        // chunk partials sc*P summed over the chunk's two sub-blocks; the
-        // other sub-block of each chunk is in lane ^ 1 (active together)
+      if (kPartials && partials) {
+        // the sub-block partials P of this lane's two sub-blocks
+        int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 16) + (size_t)sb * 16;
+        pr[sa] = pa;
+        pr[sa + 4] = pb;
+      }
+      if (kPartials && chunks) {
+        // chunk sums sc*P over the chunk's two sub-blocks; the other
+        // sub-block of each chunk is in lane ^ 1 (active together)
         const unsigned act = __activemask();
         const int ta = sc_a * pa, tb = sc_b * pb;
         const int sa2 = ta + __shfl_xor_sync(act, ta, 1);
         const int sb2 = tb + __shfl_xor_sync(act, tb, 1);
         if ((s4 & 1) == 0) {
-          int32_t* pr = partials + ((size_t)n * M + m) * (size_t)(K / 32) + (size_t)sb * 8;
+          int32_t* pr = chunks + ((size_t)n * M + m) * (size_t)(K / 32) + (size_t)sb * 8;
           pr[sa >> 1] = sa2;
           pr[(sa + 4) >> 1] = sb2;
         }
@@ -171,7 +178,8 @@ __device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
                                         const uint16_t* __restrict__ d_row, int m, int M, int K,
                                         const int8_t* __restrict__ Xq, const float* __restrict__ da,
                                         int ldda, int N, float* __restrict__ Y, int ldy,
-                                        int32_t* __restrict__ partials) {
+                                        int32_t* __restrict__ partials,
+                                        int32_t* __restrict__ chunks) {
   const int lane = threadIdx.x & 31;
   const int nsb = K / 256;
   const int sbi = lane >> 3;  // super-block within the step
@@ -200,7 +208,7 @@ __device__ __forceinline__ void row_dot(const uint8_t* __restrict__ qlh_row,
   auto step = [&](int sb, const Step& r) {
     if (sb < nsb)
       step_dot<kPartials, kMaxN>(r.L, r.H, r.a, r.b, r.d, sb, m, M, K, Xq, da, ldda, N, partials,
-                                 acc);
+                                 chunks, acc);
   };
   // two step buffers used in turn, so no registers are copied between steps
   Step A, B;
@@ -219,14 +227,14 @@ template <bool kPartials, int kMaxN>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
     const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
     const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
-    int32_t* __restrict__ partials) {
+    int32_t* __restrict__ partials, int32_t* __restrict__ chunks) {
   const int warps = (int)gridDim.x * kWarps;
   for (int m = (threadIdx.x >> 5) * (int)gridDim.x + blockIdx.x; m < M; m += warps)
     row_dot<kPartials, kMaxN>(
         plane + g.qlh_off + (size_t)m * g.qlh_row,
         reinterpret_cast<const int8_t*>(plane + g.sc_off) + (size_t)m * (K / 16),
         reinterpret_cast<const uint16_t*>(plane + g.d_off + (size_t)m * g.d_row), m, M, K, Xq, da,
-        ldda, N, Y, ldy, partials);
+        ldda, N, Y, ldy, partials, chunks);
 }
 
 
@@ -239,6 +247,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
 // staged codes. Every CTA quantises all of X (N*K*4 bytes, from L2 after the
 // first CTAs), so no CTA waits on another and nothing else is launched.
 constexpr int kFusedWarps = 32;
+// The quantiser loop below runs full-mask shuffles: every warp must run it
+// whole and the four threads of a 32-element block must share a warp. Both
+// hold because the CTA is whole warps and N * K / 8 is a multiple of 32
+// (K % 256 == 0, checked in launch_fused).
+static_assert((kFusedWarps * 32) % 32 == 0, "the fused CTA must be whole warps");
 
 template <int kMaxN>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) mmq_skinny_fused_kernel(
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) mmq_skinny_fused_kernel(
     auto step = [&](int sb, const Step& r) {
       if (sb < nsb)
         step_dot<false, kMaxN, true>(r.L, r.H, r.a, r.b, r.d, sb, m, M, K, xs, das, kMaxN, N,
-                                     nullptr, acc);
+                                     nullptr, nullptr, acc);
     };
     // the first iteration of mmq_skinny_kernel's loop with both of its
     // loads already issued, then the same loop
@@ -351,6 +364,8 @@ size_t fused_smem_bytes(int K, int kmax) { return (size_t)kmax * K + (size_t)(K 
 template <int kMaxN>
 cudaError_t launch_fused(const uint8_t* plane, int M, int K, const float* X, int ldx, int N,
                          float* Y, int ldy, cudaStream_t s) {
+  // the quantiser's full-mask shuffles need K / 8 to be a multiple of 32
+  if (K % 256 != 0) return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -382,7 +397,7 @@ cudaError_t launch_mmq_skinny_fused(const uint8_t* plane, int M, int K, const fl
 
 template <bool P, int kMaxN>
 cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K, const int8_t* Xq,
-                          const float* da, int ldda, int N, float* Y, int ldy, int32_t* partials,
+                          const float* da, int ldda, int N, float* Y, int ldy, Debug dbg,
                           cudaStream_t s) {
   // one resident wave of blocks, warps striding over the rows (blocks with
   // no row return at once; the row order spreads the rows evenly over SMs)
@@ -395,24 +410,24 @@ cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K
     return e;
   const unsigned blocks = (unsigned)(sms * (per_sm > 0 ? per_sm : 1));
   mmq_skinny_kernel<P, kMaxN><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y,
-                                                             ldy, partials);
+                                                             ldy, dbg.partials, dbg.chunk_sums);
   return cudaGetLastError();
 }
 
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
-                              int ldda, int N, float* Y, int ldy, int32_t* partials,
+                              int ldda, int N, float* Y, int ldy, Debug dbg,
                               unsigned int* status, cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
   // one or two tokens: the dp4a weight-streaming kernel (the debug partials
   // come from the same dot products); 3..16 tokens: the f16 tensor form with
   // TMA-staged weights (mmq_skinny_mma.cu), partials included
   if (N == 1)
-    return partials ? launch_bucket<true, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s)
-                    : launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
+    return dbg.any() ? launch_bucket<true, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, dbg, s)
+                     : launch_bucket<false, 1>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, dbg, s);
   if (N == 2)
-    return partials ? launch_bucket<true, 2>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, partials, s)
-                    : launch_bucket<false, 2>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, nullptr, s);
-  return launch_mmq_skinny_mma(plane, M, K, Xq, da, ldda, N, Y, ldy, partials, status, s);
+    return dbg.any() ? launch_bucket<true, 2>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, dbg, s)
+                     : launch_bucket<false, 2>(plane, g, M, K, Xq, da, ldda, N, Y, ldy, dbg, s);
+  return launch_mmq_skinny_mma(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s);
 }
 
 }  // namespace q6

@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmA, int M, int K, int N, int R, int units,
                           int ns, int ldda, float* __restrict__ Y, int ldy, int32_t* __restrict__ partials,
-                          unsigned int* __restrict__ status) {
+                          int32_t* __restrict__ chunks, unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* abort_word = reinterpret_cast<int*>(empty + kMaxNS);
   volatile int* abort_flag = abort_word;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nsb = K / 256, nst = (nsb + kSbs - 1) / kSbs, nc = K / 32;
+  const int nsb = K / 256, nst = (nsb + kSbs - 1) / kSbs, nc = K / 32, ns16 = K / 16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < ns; ++s) {
@@ -301,6 +301,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t wb = xcur[e][nt] ^ 0x80808080u;
               float P[4];
               mma_f16(P, a, x_pair<0>(wb), x_pair<1>(wb));
+              if (kPartials && partials) {
+                // P of sub-block 16 sb + s16 (an exact integer in f32)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int rl = (i < 2) ? ra : rb, tk = 8 * nt + 2 * t + (i & 1);
+                  if (rl < R && r0 + rl < M && tk < N)
+                    partials[((size_t)tk * M + r0 + rl) * (size_t)ns16 + 16 * sb + s16] =
+                        (int32_t)P[i];
+                }
+              }
               // sc * P and their sum over the chunk are exact in f32 (< 2^24)
               S[nt][0] = fmaf(sa, P[0], S[nt][0]);
               S[nt][1] = fmaf(sa, P[1], S[nt][1]);
@@ -318,12 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             sbs[nt][1] = fmaf(d1, S[nt][1], sbs[nt][1]);
             sbs[nt][2] = fmaf(d0, S[nt][2], sbs[nt][2]);
             sbs[nt][3] = fmaf(d1, S[nt][3], sbs[nt][3]);
-            if (kPartials) {
+            if (kPartials && chunks) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const int rl = (i < 2) ? ra : rb, tk = t0 + (i & 1);
                 if (rl < R && r0 + rl < M && tk < N)
-                  partials[((size_t)tk * M + r0 + rl) * (size_t)nc + c] = (int32_t)S[nt][i];
+                  chunks[((size_t)tk * M + r0 + rl) * (size_t)nc + c] = (int32_t)S[nt][i];
               }
             }
           }
@@ -395,7 +405,7 @@ CUresult encode_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
 
 template <int kNT, bool P>
 cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
-                      int ldda, int N, float* Y, int ldy, int32_t* partials, unsigned int* status,
+                      int ldda, int N, float* Y, int ldy, Debug dbg, unsigned int* status,
                       cudaStream_t s) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -424,7 +434,8 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
   const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
   mmq_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R, 8 * kNT, ns), s>>>(
-      mq, ms, md, mx, ma, M, K, N, R, units, ns, ldda, Y, ldy, partials, status);
+      mq, ms, md, mx, ma, M, K, N, R, units, ns, ldda, Y, ldy, dbg.partials, dbg.chunk_sums,
+      status);
   return cudaGetLastError();
 }
 
@@ -457,12 +468,12 @@ cudaError_t mmq_skinny_mma_prepare() {
 
 cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8_t* Xq,
                                   const float* da, int ldda, int N, float* Y, int ldy,
-                                  int32_t* partials, unsigned int* status, cudaStream_t s) {
+                                  Debug dbg, unsigned int* status, cudaStream_t s) {
   if (N <= 8)
-    return partials ? launch_nt<1, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, partials, status, s)
-                    : launch_nt<1, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, nullptr, status, s);
-  return partials ? launch_nt<2, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, partials, status, s)
-                  : launch_nt<2, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, nullptr, status, s);
+    return dbg.any() ? launch_nt<1, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s)
+                     : launch_nt<1, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s);
+  return dbg.any() ? launch_nt<2, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s)
+                   : launch_nt<2, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s);
 }
 
 }  // namespace q6

@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(256, 1)
     mmq_sync_kernel(const int8_t* __restrict__ wexp, const int8_t* __restrict__ scp,
                     const float* __restrict__ dT, int ldm, int M, int K,
                     const int8_t* __restrict__ Xq, const float* __restrict__ da, int ldda, int N,
-                    float* __restrict__ Y, int ldy, int32_t* __restrict__ partials) {
+                    float* __restrict__ Y, int ldy, int32_t* __restrict__ partials,
+                    int32_t* __restrict__ chunks) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wm = warp & 3, wn = warp >> 2;  // 32-row x 32-token warp tile
@@ -169,7 +170,15 @@ __global__ void __launch_bounds__(256, 1)
               sbacc[mi][ni][e] = (c == 0) ? dav * (float)S : fmaf(dav, (float)S, sbacc[mi][ni][e]);
               if (kPartials) {
                 const int n = n0 + tok, m = m0 + row;
-                if (n < N && m < M) partials[((size_t)n * M + m) * (size_t)nc + 8 * sb + c] = S;
+                if (n < N && m < M) {
+                  const size_t nm = (size_t)n * M + m;
+                  if (chunks) chunks[nm * (size_t)nc + 8 * sb + c] = S;
+                  if (partials) {
+                    // P of the chunk's two sub-blocks 2c, 2c + 1
+                    partials[nm * (size_t)(2 * nc) + 16 * sb + 2 * c] = P[0][mi][ni][e];
+                    partials[nm * (size_t)(2 * nc) + 16 * sb + 2 * c + 1] = P[1][mi][ni][e];
+                  }
+                }
               }
             }
           }
@@ -214,17 +223,17 @@ cudaError_t mmq_sync_prepare() {
 
 cudaError_t launch_mmq_sync(const uint8_t* plane, const int8_t* wexp, int M, int K,
                             const int8_t* Xq, const float* da, int ldda, int N, float* Y, int ldy,
-                            int32_t* partials, cudaStream_t s) {
+                            Debug dbg, cudaStream_t s) {
   const PlaneGeom g = plane_geom(M, K);
   const int8_t* scp = reinterpret_cast<const int8_t*>(plane + g.sc_off);
   const float* dT = reinterpret_cast<const float*>(plane + g.dt_off);
   dim3 grid((unsigned)((N + SBN - 1) / SBN), (unsigned)((M + SBM - 1) / SBM));
-  if (partials)
+  if (dbg.any())
     mmq_sync_kernel<true><<<grid, 256, kSyncSmem, s>>>(wexp, scp, dT, g.ldm, M, K, Xq, da, ldda, N,
-                                                       Y, ldy, partials);
+                                                       Y, ldy, dbg.partials, dbg.chunk_sums);
   else
     mmq_sync_kernel<false><<<grid, 256, kSyncSmem, s>>>(wexp, scp, dT, g.ldm, M, K, Xq, da, ldda,
-                                                        N, Y, ldy, nullptr);
+                                                        N, Y, ldy, nullptr, nullptr);
   return cudaGetLastError();
 }
 

@@ -157,15 +157,18 @@ __device__ __forceinline__ void chunk_fma(float2* sb, const uint32_t (&p)[32], f
   }
 }
 
+// The exact integers of 32 columns of a chunk accumulator, to the debug
+// output at out[(n * M + m) * stride + off] (off = c * mul + add).
 template <bool kPartials>
-__device__ __forceinline__ void dump_partials(int32_t* __restrict__ partials, int M, int N, int nc,
-                                              int n, int m_first, int c, const uint32_t (&p)[32]) {
+__device__ __forceinline__ void dump_partials(int32_t* __restrict__ out, int M, int N,
+                                              int stride, int n, int m_first, int off,
+                                              const uint32_t (&p)[32]) {
   if (kPartials) {
     if (n < N) {
 #pragma unroll 4
       for (int j = 0; j < 32; ++j) {
         const int m = m_first + j;
-        if (m < M) partials[((size_t)n * M + m) * (size_t)nc + c] = (int32_t)__uint_as_float(p[j]);
+        if (m < M) out[((size_t)n * M + m) * (size_t)stride + off] = (int32_t)__uint_as_float(p[j]);
       }
     }
     __syncwarp();
@@ -178,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmWlo, const __grid_constant__ CUtensorMap tmDa,
                   const __grid_constant__ CUtensorMap tmD, int M, int K, int N, int Tw, int U,
                   float* __restrict__ Y, int ldy, int y_vec4, int32_t* __restrict__ partials,
+                  int p_stride, int p_mul, int p_add, int write_y,
                   unsigned int* __restrict__ status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -186,7 +190,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = (N + BT - 1) / BT;
   const int nsb = K / 256;  // super-blocks per tile
-  const int nc = K / 32;    // chunks per tile
   volatile int* abort_flag = &bars->abort;
 
   if (threadIdx.x == 0) {
@@ -396,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               chunk_fma<false>(sb, pA, da);
               chunk_fma<false>(sb + 16, pB, da);
             }
-            dump_partials<kPartials>(partials, M, N, nc, n, mcol, c, pA);
-            dump_partials<kPartials>(partials, M, N, nc, n, mcol + 32, c, pB);
+            dump_partials<kPartials>(partials, M, N, p_stride, n, mcol, c * p_mul + p_add, pA);
+            dump_partials<kPartials>(partials, M, N, p_stride, n, mcol + 32, c * p_mul + p_add,
+                                     pB);
           }
         }
         // Y += d * Sb for this super-block
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++gs;
       }
       if (!ok) break;
-      if (n < N) {
+      if (n < N && write_y) {
         float* yr = Y + (size_t)n * ldy + mcol;
         const int mleft = M - mcol;
         if (!w.split) {
@@ -472,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 int g_num_sms[64] = {0};
 
 template <bool P>
-cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ldy, int32_t* partials,
-                       unsigned int* status, cudaStream_t s) {
+cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
+                       const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -482,14 +486,15 @@ cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ld
     return e;
   const TcPlan p = mmq_tc_plan(M, K, N, sms);
   const int y_vec4 = (ldy % 4 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
-  if (p.U > p.Tw) {
+  if (p.U > p.Tw && dbg.write_y) {
     zero_split_tiles_kernel<<<dim3((unsigned)((p.U - p.Tw) / 2), BT / 32), 256, 0, s>>>(
         Y, ldy, M, N, p.Tw, y_vec4);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   mmq_tc_kernel<P><<<p.grid, kThreads, kSmemBytes, s>>>(maps.x, maps.whi, maps.wlo, maps.da, maps.d,
                                                        M, K, N, p.Tw, p.U, Y, ldy, y_vec4,
-                                                       partials, status);
+                                                       dbg.out, dbg.stride, dbg.mul, dbg.add,
+                                                       dbg.write_y, status);
   return cudaGetLastError();
 }
 
@@ -526,9 +531,9 @@ cudaError_t mmq_tc_prepare() {
 }
 
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
-                          int32_t* partials, unsigned int* status, cudaStream_t s) {
-  return partials ? launch_one<true>(maps, M, K, N, Y, ldy, partials, status, s)
-                  : launch_one<false>(maps, M, K, N, Y, ldy, nullptr, status, s);
+                          const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
+  return dbg.out ? launch_one<true>(maps, M, K, N, Y, ldy, dbg, status, s)
+                 : launch_one<false>(maps, M, K, N, Y, ldy, dbg, status, s);
 }
 
 }  // namespace q6

@@ -15,14 +15,16 @@
 // library holds it until the process exits. All calls share it and it keeps
 // the last call's contents, so calls that overlap on the GPU (different
 // streams, or other devices' threads racing on the same device) race on it.
-// The status word is cleared on the call's stream at the start of each call.
+// The status word is cleared on the call's stream at the start of each call;
+// q6k_mmq_noalloc_status() waits for the stream, reads it, clears it and
+// reports a time-out as Q6_ETIMEOUT, as q6_sync_status() does for q6k_mmq.
 //
 // Set-up happens in the first call on each device (with that device
-// current): the architecture check, the kernels' shared-memory limits, the
-// tensor-map encoder and the array's device address (cudaGetSymbolAddress).
-// That first call should come before any stream capture.
-#include <cudaTypedefs.h>
-
+// current): the architecture check, the kernels' shared-memory limits and
+// the array's device address (cudaGetSymbolAddress; in host code the array's
+// name is only a stand-in, so kernels get that address). That first call
+// should come before any stream capture. The tensor maps are encoded by the
+// library's shared encoder, which allocates nothing.
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -53,8 +55,9 @@ struct NaDev {
 };
 std::mutex g_na_mu;
 NaDev g_na_dev[64];
-PFN_cuTensorMapEncodeTiled_v12000 g_na_encode = nullptr;
 
+// Set-up of the calling thread's current device, once: the architecture
+// check, the kernels' shared-memory limits and the array's device address.
 int na_setup(NaDev** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -76,15 +79,6 @@ int na_setup(NaDev** out) {
     void* addr = nullptr;
     if ((e = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) || !addr)
       return na_fail(Q6_ECUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    if (!g_na_encode) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-        return na_fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
-      g_na_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
     st.scratch = static_cast<unsigned char*>(addr);
     st.ready = true;
   }
@@ -93,19 +87,6 @@ int na_setup(NaDev** out) {
 }
 
 bool na_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-int na_encode(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-              CUtensorMapSwizzle swz) {
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_na_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? Q6_OK : na_fail(Q6_ECUDA, "cuTensorMapEncodeTiled failed: %d", (int)r);
-}
 
 }  // namespace
 
@@ -129,7 +110,8 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
                    "M*K*4 = %zu bytes exceeds this entry point's static scratch of %zu bytes "
                    "(M*K <= %zu weights)",
                    (size_t)M * (size_t)K * 4, kScratchWeightBytes, kScratchWeightBytes / 4);
-  if ((long long)N * ldy > (1LL << 40)) return na_fail(Q6_ESIZE, "problem too large");
+  if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
+    return na_fail(Q6_ESIZE, "problem too large");
   NaDev* st;
   int rc = na_setup(&st);
   if (rc) return rc;
@@ -140,7 +122,7 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
     return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
   if (skinny) {
     e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda, N, Y, ldy,
-                              nullptr, status, (cudaStream_t)s);
+                              q6::Debug{}, status, (cudaStream_t)s);
     if (e != cudaSuccess) return na_fail(Q6_ECUDA, "skinny kernel launch: %s", cudaGetErrorString(e));
     if (path_out) *path_out = Q6_PATH_SKINNY;
     return Q6_OK;
@@ -150,22 +132,26 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
   e = wexp ? q6::launch_expand_wexp(wexp, pb, M, K, wh, (cudaStream_t)s)
            : q6::launch_expand_raw(pb, M, K, wh, (cudaStream_t)s);
   if (e != cudaSuccess) return na_fail(Q6_ECUDA, "weight unpack launch: %s", cudaGetErrorString(e));
-  const q6::PlaneGeom g = q6::plane_geom(M, K);
-  const __half* wlo = wh + (size_t)M * (size_t)K;
   q6::TcMaps maps;
-  if ((rc = na_encode(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-      (rc = na_encode(&maps.whi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wh, (uint64_t)K, (uint64_t)M,
-                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-      (rc = na_encode(&maps.wlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wlo, (uint64_t)K, (uint64_t)M,
-                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
-      (rc = na_encode(&maps.da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
-                      (uint64_t)ldda * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-      (rc = na_encode(&maps.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, pb + g.dt_off, (uint64_t)M,
-                      (uint64_t)K / 256, (uint64_t)g.ldm * 4, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE)))
-    return rc;
-  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, nullptr, status, (cudaStream_t)s);
+  if ((rc = q6::encode_tc_maps(&maps, pb, wh, Xh, da, M, K, N))) return rc;
+  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, q6::TcDebugOut{}, status, (cudaStream_t)s);
   if (e != cudaSuccess) return na_fail(Q6_ECUDA, "tensor-core kernel launch: %s", cudaGetErrorString(e));
   if (path_out) *path_out = wexp ? Q6_PATH_TC_WEXP : Q6_PATH_TC_RAW;
   return Q6_OK;
+}
+
+extern "C" int q6k_mmq_noalloc_status(q6_stream_t s) {
+  NaDev* st;
+  int rc = na_setup(&st);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)s);
+  if (e != cudaSuccess) return na_fail(Q6_ECUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+  unsigned int word = 0;
+  if ((e = cudaMemcpy(&word, st->scratch, sizeof(word), cudaMemcpyDeviceToHost)))
+    return na_fail(Q6_ECUDA, "reading the status word: %s", cudaGetErrorString(e));
+  if (word == 0) return Q6_OK;
+  if ((e = cudaMemset(st->scratch, 0, sizeof(word))))
+    return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
+  return na_fail(Q6_ETIMEOUT, "a kernel gave up a bounded wait (status 0x%x, wait site %u)", word,
+                 (word >> 8) & 0xFFu);
 }

@@ -46,14 +46,22 @@ cudaError_t launch_quantize(const float* X, int N, int K, int ldx, int8_t* Xq, f
                             __half* Xh, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* raw, int M, int K, uint8_t* plane, int8_t* wexp,
                         cudaStream_t s);
+// Debug outputs of the GEMM kernels (both optional, int32, token-major):
+//   partials   [N][M][K/16]: P = sum over a 16-element sub-block of (q - 32) * xq;
+//   chunk_sums [N][M][K/32]: S = sc[2c] * P[2c] + sc[2c+1] * P[2c+1].
+struct Debug {
+  int32_t* partials = nullptr;
+  int32_t* chunk_sums = nullptr;
+  bool any() const { return partials != nullptr || chunk_sums != nullptr; }
+};
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,
-                              int ldda, int N, float* Y, int ldy, int32_t* partials,
+                              int ldda, int N, float* Y, int ldy, Debug dbg,
                               unsigned int* status, cudaStream_t s);
 // The same product for 3 <= N <= 16 (correct from N = 2) on the warp-level
 // f16 tensor path with TMA-staged weights (mmq_skinny_mma.cu).
 cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8_t* Xq,
                                   const float* da, int ldda, int N, float* Y, int ldy,
-                                  int32_t* partials, unsigned int* status, cudaStream_t s);
+                                  Debug dbg, unsigned int* status, cudaStream_t s);
 cudaError_t mmq_skinny_mma_prepare();
 cudaError_t mmq_skinny_prepare();
 // Quantise + GEMM for N <= 2 tokens from f32 X [N][ldx] in one launch
@@ -65,7 +73,7 @@ cudaError_t launch_mmq_skinny_fused(const uint8_t* plane, int M, int K, const fl
                                     int N, float* Y, int ldy, cudaStream_t s);
 cudaError_t launch_mmq_sync(const uint8_t* plane, const int8_t* wexp, int M, int K,
                             const int8_t* Xq, const float* da, int ldda, int N, float* Y, int ldy,
-                            int32_t* partials, cudaStream_t s);
+                            Debug dbg, cudaStream_t s);
 cudaError_t mmq_sync_prepare();
 
 struct TcMaps {
@@ -75,12 +83,33 @@ struct TcMaps {
   CUtensorMap da;   // da   [K/32][ldda] f32, box {128, 8}
   CUtensorMap d;    // d^T  [K/256][ldm] f32, box {128, 1}
 };
+// What one tensor-core GEMM launch writes besides (or instead of) Y: the
+// exact integer of each (token, weight row, 32-element chunk c) accumulator
+// at out[(n * M + m) * stride + c * mul + add], when out is not NULL.
+//   chunk sums of the folded planes: stride K/32, mul 1, add 0;
+//   P of sub-block parity p (planes from launch_expand_unit): stride K/16,
+//   mul 2, add p.
+// write_y == 0 leaves Y untouched (a debug pass on unit-scale planes).
+struct TcDebugOut {
+  int32_t* out = nullptr;
+  int stride = 0, mul = 1, add = 0;
+  int write_y = 1;
+};
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
-                          int32_t* partials, unsigned int* status, cudaStream_t s);
+                          const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
+// Tensor maps of one tensor-core GEMM call (api.cu): Xh [N][K], the operand
+// planes W_hi at wop and W_lo at wop + M*K, da [K/32][ldda], and the
+// transposed d sub-plane of the packed plane. Allocates nothing.
+int encode_tc_maps(TcMaps* maps, const uint8_t* plane, const void* wop, const void* Xh,
+                   const float* da, int M, int K, int N);
 // The two binary16 operand planes W_hi, W_lo [M][K] (W_lo at wh + M*K) with
 // the sub-block scale folded in, from the packed plane's qlh and sc
 // sub-planes, or from the W_exp plane and the sc sub-plane.
 cudaError_t launch_expand_raw(const uint8_t* plane, int M, int K, __half* wh, cudaStream_t s);
+// Debug planes: W_hi = 0 and W_lo = v on the sub-blocks of parity `parity`
+// (0 elsewhere), so the GEMM's chunk accumulator holds P of that sub-block.
+cudaError_t launch_expand_unit(const uint8_t* plane, int M, int K, int parity, __half* wh,
+                               cudaStream_t s);
 cudaError_t launch_expand_wexp(const int8_t* wexp, const uint8_t* plane, int M, int K, __half* wh,
                                cudaStream_t s);
 size_t mmq_tc_smem_bytes();

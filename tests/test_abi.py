@@ -68,9 +68,9 @@ def test_host_side_rejections(lib):
     path = ctypes.c_int(-1)
 
     def mmq(plane=fake, wexp=None, wh=None, M=64, K=256, xq=fake, da=fake, xh=fake, N=64,
-            Y=fake, ldy=64, ws=fake, ws_bytes=1 << 30, partials=None):
+            Y=fake, ldy=64, ws=fake, ws_bytes=1 << 30, partials=None, chunk_sums=None):
         return lib.q6k_mmq(plane, wexp, wh, M, K, xq, da, xh, N, Y, ldy, ws, ws_bytes, partials,
-                           ctypes.byref(path), None)
+                           chunk_sums, ctypes.byref(path), None)
 
     assert mmq(K=300) == q6.Q6_EINVAL                       # K not a multiple of 256
     assert path.value == q6.PATH_NONE
@@ -83,6 +83,13 @@ def test_host_side_rejections(lib):
     assert mmq(ws=odd) == q6.Q6_EALIGN                      # misaligned workspace
     assert mmq(ws=None) == q6.Q6_ESIZE                      # unpack needs a workspace
     assert mmq(ws_bytes=64 * 256 * 4 - 1) == q6.Q6_ESIZE    # ... of M*K*4 bytes
+    # resident planes need no workspace, unless the sub-block partials are wanted
+    assert mmq(wh=fake, ws=None, partials=fake) == q6.Q6_ESIZE
+    odd1 = ctypes.c_void_p(0x10001)                           # not 4-byte aligned
+    assert mmq(partials=odd1) == q6.Q6_EALIGN               # misaligned debug outputs
+    assert mmq(chunk_sums=odd1) == q6.Q6_EALIGN
+    assert lib.q6k_mmq_mma_sync(fake, fake, 64, 256, fake, fake, 8, fake, 64, None, odd1,
+                                ctypes.byref(path), None) == q6.Q6_EALIGN
     size = ctypes.c_size_t()
     assert lib.q6k_mmq_workspace_bytes(64, 256, 64, ctypes.byref(size)) == q6.Q6_OK
     assert size.value == 64 * 256 * 4

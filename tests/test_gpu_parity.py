@@ -1,16 +1,19 @@
 """Parity of the CUDA library with the CPU oracle (needs a GB300).
 
-Integer results (quantised activations, packed planes, chunk partials) must
-be bit-exact. The kernels' debug output is the exact integer chunk sum
-S[n][m][c] = sum over the chunk's two sub-blocks s of sc[m][s] * P[n][m][s];
-the expected S is formed here from the oracle's sub-block partials P and the
-raw sub-block scales. Y must satisfy the floating-point tolerance of the method:
+Integer results (quantised activations, packed planes, the debug partials)
+must be bit-exact. The kernels have two debug outputs: the sub-block partials
+P[n][m][s] = sum over the 16 elements of sub-block s of (q - 32) * xq, which
+are compared with the oracle's P directly, and the chunk sums the kernels form
+themselves, S[n][m][c] = sc[m][2c] * P[2c] + sc[m][2c+1] * P[2c+1], whose
+expected value is formed here from the oracle's P and the raw sub-block
+scales. Y must satisfy the floating-point tolerance of the method:
 max|Y - Yo| <= 1e-3 * max|Yo| and sum|Y - Yo| / sum|Yo| <= 1e-5 (the normwise
 reading of "mean relative error"). Full-size workloads are checked on every
 output, in the launch configuration the benchmark uses, against the oracle run
-over disjoint weight-row ranges on the host cores; their chunk partials are
+over disjoint weight-row ranges on the host cores; their debug partials are
 checked bit-exactly on sampled tokens.
 """
+import ctypes
 import dataclasses
 
 import numpy as np
@@ -85,12 +88,25 @@ SOURCES = ["raw", "wexp", "wh"]
 TC_PATH = {"raw": "tc_raw", "wexp": "tc_wexp", "wh": "tc_wh"}
 
 
+def check_debug(D, Po, raw, M, K, tok=None, label=""):
+    """Both debug outputs bit-exact: the sub-block partials against the
+    oracle's P, the chunk sums against S formed from P and the raw scales
+    (rows `tok` of the kernel's outputs when given)."""
+    P, S = host(D.partials), host(D.chunk_sums)
+    if tok is not None:
+        P, S = P[tok], S[tok]
+    assert np.array_equal(P, Po), f"{label}: sub-block partials differ"
+    assert np.array_equal(S, chunk_sums(Po, raw, M, K)), f"{label}: chunk sums differ"
+
+
 def run_gemm(q6, raw, X, M, K, source, partials=False):
+    """Packs, quantises and runs the GEMM; with partials=True both debug
+    outputs are requested."""
     w = q6.pack_weights(dev(raw), M, K, wexp=source == "wexp", wh=source == "wh")
     act = q6.quantize_act(dev(X))
-    Y, path, P = q6.mmq(w, act, source=source, partials=partials)
+    Y, path, D = q6.mmq(w, act, source=source, partials=partials, chunk_sums=partials)
     q6.sync_status()
-    return w, act, Y, path, P
+    return w, act, Y, path, D
 
 
 # --------------------------------------------------------------- failures ---
@@ -248,6 +264,31 @@ def test_pack_bitexact(q6, orc, M, K):
     assert np.array_equal(host(q6.unpack_weights(w)).astype(np.float64), wh)
 
 
+def test_pack_from_host_memory(q6):
+    """q6k_pack_weights reads the raw bytes from host memory (page-locked, or
+    pageable where the device reads it) as well as from device memory: the
+    same planes either way."""
+    import torch
+    M, K = 300, 1024
+    raw = synth.q6k_raw_weights(0x51360D01, M, K)
+    wd = q6.pack_weights(dev(raw), M, K, wexp=True, wh=True)
+    for host_raw in (torch.from_numpy(raw).pin_memory(), torch.from_numpy(raw)):
+        wh_ = q6.pack_weights(host_raw, M, K, wexp=True, wh=True)
+        q6.sync_status()
+        assert wh_.plane.is_cuda
+        for a, b in ((wh_.plane, wd.plane), (wh_.wexp, wd.wexp), (wh_.wh, wd.wh)):
+            assert torch.equal(a, b)
+    # through the C ABI with a page-locked host pointer
+    lib = q6.load()
+    pinned = torch.from_numpy(raw).pin_memory()
+    plane = torch.empty_like(wd.plane)
+    rc = lib.q6k_pack_weights(ctypes.c_void_p(pinned.data_ptr()), M, K,
+                              ctypes.c_void_p(plane.data_ptr()), None, None, None)
+    assert rc == q6.Q6_OK, lib.q6_last_error().decode()
+    torch.cuda.synchronize()
+    assert torch.equal(plane, wd.plane)
+
+
 # --------------------------------------------------------- GEMM, small ------
 
 SMALL = [
@@ -267,11 +308,11 @@ SMALL = [
 def test_mmq_small_bitexact_partials(q6, orc, M, K, N, source):
     raw = synth.q6k_raw_weights(300 + M + N, M, K)
     X = synth.activations(400 + M + N, N, K, outlier_frac=0.02)
-    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, source, partials=True)
+    w, act, Y, path, D = run_gemm(q6, raw, X, M, K, source, partials=True)
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
     assert path == ("skinny" if N <= q6.SKINNY_MAX_N else TC_PATH[source])
-    assert np.array_equal(host(P), chunk_sums(Po, raw, M, K)), "chunk partials differ"
+    check_debug(D, Po, raw, M, K, label=f"{M}x{K}x{N} {source}")
     check_y(host(Y), Yo, f"{M}x{K}x{N}")
     # the fast (non-debug) variant gives the same Y
     Y2, _, _ = q6.mmq(w, act, source=source)
@@ -296,15 +337,15 @@ def _sweep_shapes(count=18, seed=0x5EED):
 @pytest.mark.parametrize("M,K,N", _sweep_shapes(), ids=lambda v: str(v))
 def test_mmq_seeded_shape_sweep(q6, orc, M, K, N):
     """Y within tolerance on every output of seeded irregular shapes (raw
-    weight source), and bit-exact chunk partials where they stay small."""
+    weight source), and bit-exact debug partials where they stay small."""
     raw = synth.q6k_raw_weights(900 + M + K + N, M, K)
     X = synth.activations(901 + M + K + N, N, K, outlier_frac=0.01)
     want_p = N * M * (K // 16) <= 20_000_000
-    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, "raw", partials=want_p)
+    w, act, Y, path, D = run_gemm(q6, raw, X, M, K, "raw", partials=want_p)
     xq_o, da_o = quant_check(act, X, orc)
     if want_p:
         Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-        assert np.array_equal(host(P), chunk_sums(Po, raw, M, K)), "chunk partials differ"
+        check_debug(D, Po, raw, M, K, label=f"{M}x{K}x{N}")
     else:
         Yo = orc.mmq_all(raw, M, K, xq_o, da_o)
     check_y(host(Y), Yo, f"{M}x{K}x{N}")
@@ -375,13 +416,13 @@ def test_mmq_extreme_chunk_sums_exact(q6, orc, N):
     X[1::2] *= -1.0                                                 # +-1 rows: xq = +-127
     X[0, 256:] = np.where(np.arange(256) % 3 == 0, -1.0, 1.0)
     for source in ("raw", "wh"):
-        w, act, Y, path, P = run_gemm(q6, raw, X, M, K, source, partials=True)
+        w, act, Y, path, D = run_gemm(q6, raw, X, M, K, source, partials=True)
         xq_o, da_o = quant_check(act, X, orc)
         assert np.abs(xq_o).min() == 127
         Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
         S = chunk_sums(Po, raw, M, K)
         assert np.abs(S).max() == 32 * 128 * 32 * 127                # the bound is reached
-        assert np.array_equal(host(P), S)
+        check_debug(D, Po, raw, M, K, label=f"extreme {source}")
         check_y(host(Y), Yo, f"extreme N={N}")
 
 
@@ -412,14 +453,14 @@ def test_mmq_split_last_round(q6, orc, source):
     tok = sampled_tokens(N, extra=(1535, 1536, 1700, 2047, 2300, 2431, 2432, 2500))
     for partials in (False, True):
         Y = torch.full((N, M), float("nan"), dtype=torch.float32, device="cuda")
-        Y, path, P = q6.mmq(w, act, Y=Y, source=source, partials=partials)
+        Y, path, D = q6.mmq(w, act, Y=Y, source=source, partials=partials, chunk_sums=partials)
         q6.sync_status()
         assert path == TC_PATH[source]
         Yh = host(Y)
         assert np.all(np.isfinite(Yh)), "a split tile was not zeroed or not written"
         if partials:
             Yo, Po = orc.mmq(raw, M, K, xq_o[tok], da_o[tok], partials=True)
-            assert np.array_equal(host(P)[tok], chunk_sums(Po, raw, M, K))
+            check_debug(D, Po, raw, M, K, tok=tok, label=f"split {source}")
         else:
             Yo = orc.mmq(raw, M, K, xq_o[tok], da_o[tok])
         check_y(Yh[tok], Yo, f"split {source} partials={partials}")
@@ -626,13 +667,13 @@ def test_attn_v_full(q6, orc, source):
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     w, act, path = check_full(q6, orc, raw, X, M, K, source, "attn_v")
     assert path == TC_PATH[source]
-    # chunk partials of four tokens, bit-exact
-    Y, _, P = q6.mmq(w, act, source=source, partials=True)
+    # debug partials of four tokens, bit-exact
+    Y, _, D = q6.mmq(w, act, source=source, partials=True, chunk_sums=True)
     q6.sync_status()
     tok = np.array([0, 129, 300, N - 1])
     xq_o, da_o = orc.quantize(X[tok])
     _, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-    assert np.array_equal(host(P[tok]), chunk_sums(Po, raw, M, K))
+    check_debug(D, Po, raw, M, K, tok=tok, label=f"attn_v {source}")
 
 
 @pytest.mark.parametrize("source", SOURCES)
@@ -641,20 +682,42 @@ def test_ffn_down_full(q6, orc, source):
     check_full(q6, orc, raw, X, cfg["M"], cfg["K"], source, "ffn_down")
 
 
+def test_ffn_down_debug_partials_sampled_tokens(q6, orc):
+    """The full ffn_down weights (4096 x 11008) against 136 sampled tokens of
+    its activation stream (tile edges, the ragged last tile, outlier-heavy
+    rows): enough tokens for the tensor-core path, whose sub-block partials
+    P [136][4096][688] and chunk sums are compared bit-exactly with the
+    oracle; each token is quantised on its own, so the sample is the same
+    computation as in the full GEMM. Y within tolerance on every output."""
+    raw, X, cfg = synth.workload("ffn_down")
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    tok = np.unique(np.concatenate([sampled_tokens(N, extra=(127, 128, 255, 256, 3199, 3200)),
+                                    np.linspace(0, N - 1, 136, dtype=np.int64)]))[:136]
+    assert tok.size > q6.SKINNY_MAX_N
+    Xs = np.ascontiguousarray(X[tok])
+    for source in ("raw", "wh"):
+        w, act, Y, path, D = run_gemm(q6, raw, Xs, M, K, source, partials=True)
+        assert path == TC_PATH[source]
+        xq_o, da_o = quant_check(act, Xs, orc)
+        Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+        check_debug(D, Po, raw, M, K, label=f"ffn_down sampled tokens {source}")
+        check_y(host(Y), Yo, f"ffn_down sampled tokens {source}")
+
+
 @pytest.mark.parametrize("M,K,N", [(256, 512, 8), (200, 768, 129), (384, 768, 300), (130, 1024, 1)],
                          ids=lambda v: str(v))
 def test_mma_sync_comparison_path(q6, orc, M, K, N):
-    """The legacy mma.sync path: bit-exact chunk partials and Y within tolerance."""
+    """The legacy mma.sync path: bit-exact debug partials and Y within tolerance."""
     raw = synth.q6k_raw_weights(500 + M + N, M, K)
     X = synth.activations(600 + M + N, N, K, outlier_frac=0.02)
     w = q6.pack_weights(dev(raw), M, K, wexp=True)
     act = q6.quantize_act(dev(X))
-    Y, path, P = q6.mmq_mma_sync(w, act, partials=True)
+    Y, path, D = q6.mmq_mma_sync(w, act, partials=True, chunk_sums=True)
     q6.sync_status()
     assert path == "sync_wexp"
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-    assert np.array_equal(host(P), chunk_sums(Po, raw, M, K))
+    check_debug(D, Po, raw, M, K, label=f"mma.sync {M}x{K}x{N}")
     check_y(host(Y), Yo, f"mma.sync {M}x{K}x{N}")
     Y2, _, _ = q6.mmq_mma_sync(w, act)
     q6.sync_status()
@@ -685,11 +748,11 @@ def test_pages_shapes_full(q6, orc, name):
 def test_skinny_full(q6, orc, weight, N):
     raw, X, cfg = synth.skinny_workload(weight, N)
     M, K = cfg["M"], cfg["K"]
-    w, act, Y, path, P = run_gemm(q6, raw, X, M, K, "raw", partials=True)
+    w, act, Y, path, D = run_gemm(q6, raw, X, M, K, "raw", partials=True)
     assert path == "skinny"
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-    assert np.array_equal(host(P), chunk_sums(Po, raw, M, K))
+    check_debug(D, Po, raw, M, K, label=f"skinny {weight} N={N}")
     check_y(host(Y), Yo, f"skinny {weight} N={N}")
     Y2, _, _ = q6.mmq(w, act, source="raw")            # the fast kernel of this N
     q6.sync_status()

@@ -5,15 +5,19 @@ call the GEMM (a fixed budget or pool that forbids new allocations, or a
 latency-critical path that must not enter the allocator): its scratch is a
 static device array of the library instead of a caller workspace. This test
 calls it through the C ABI twice in a row and checks each result against
-q6k_mmq on the same inputs, within the GEMM tolerance of the parity tests.
-It lives in its own file, collected last, and builds what it needs, so it
-runs the same alone in a fresh process and after the other tests.
+q6k_mmq on the same inputs and against the CPU oracle, within the GEMM
+tolerance of the parity tests, and reads the entry point's own status word
+(q6k_mmq_noalloc_status) after each call, so a bounded wait that gave up
+would fail the test. It lives in its own file, collected last, and builds
+what it needs, so it runs the same alone in a fresh process and after the
+other tests.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 from q6_int8_mmq_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -36,7 +40,9 @@ def q6():
 
 def close(Y, Yref):
     Y = Y.detach().cpu().numpy().astype(np.float64)
-    Yref = Yref.detach().cpu().numpy().astype(np.float64)
+    if not isinstance(Yref, np.ndarray):
+        Yref = Yref.detach().cpu().numpy()
+    Yref = Yref.astype(np.float64)
     err = np.abs(Y - Yref)
     scale = np.abs(Yref).max()
     assert np.all(np.isfinite(Y))
@@ -54,6 +60,9 @@ def noalloc(q6, w, act, use_wexp, stream=None):
     rc = lib.q6k_mmq_noalloc(p(w.plane), p(w.wexp if use_wexp else None), w.M, w.K, p(act.xq),
                              p(act.da), p(act.xh), act.N, p(Y), w.M, ctypes.byref(path), s)
     assert rc == q6.Q6_OK, lib.q6_last_error().decode()
+    # waits for the stream; Q6_ETIMEOUT if a kernel of the call gave up a wait
+    rc = lib.q6k_mmq_noalloc_status(s)
+    assert rc == q6.Q6_OK, lib.q6_last_error().decode()
     return Y, q6.PATH_NAMES[path.value]
 
 
@@ -65,13 +74,18 @@ def test_noalloc_matches_q6k_mmq_on_two_calls(q6, N):
     X = synth.activations(0x51360778, N, K)
     w = q6.pack_weights(torch.from_numpy(raw).cuda(), M, K, wexp=True)
     act = q6.quantize_act(torch.from_numpy(X).cuda())
+    orc = oracle.get()
+    xq_o, da_o = orc.quantize(X)
+    assert np.array_equal(act.xq.cpu().numpy(), xq_o)
+    Yo = orc.mmq_all(raw, M, K, xq_o, da_o)
     for use_wexp in (False, True):
         Yref, ref_path, _ = q6.mmq(w, act, source="wexp" if use_wexp else "raw")
+        q6.sync_status()
         for _ in range(2):                # two calls in a row share the static scratch
             Y, path = noalloc(q6, w, act, use_wexp)
-            q6.sync_status()
             assert path == ref_path
             close(Y, Yref)
+            close(Y, Yo)
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch(q6):
@@ -82,3 +96,7 @@ def test_noalloc_rejects_layers_beyond_its_scratch(q6):
                              ctypes.byref(path), None)
     assert rc == q6.Q6_ESIZE
     assert b"static scratch" in lib.q6_last_error()
+    # the few-token path takes the same size limit on M * K as q6k_mmq
+    rc = lib.q6k_mmq_noalloc(fake, None, 1 << 20, 1 << 21, fake, fake, None, 4, fake, 1 << 20,
+                             ctypes.byref(path), None)
+    assert rc == q6.Q6_ESIZE
