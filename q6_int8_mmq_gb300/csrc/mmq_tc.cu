@@ -88,10 +88,14 @@ enum : uint32_t { kSiteSEmpty = 1, kSiteSFull = 2, kSiteBEmpty = 3, kSiteBFull =
 // takes the place of an mbarrier phase on the slot's round trip (MMAs,
 // commit, epilogue loads, hand-back), which bounds the kernel; measured on
 // GB300 the ffn_down GEMM goes from 0.457 to 0.447 ms. bar.sync has no
-// time-out, so every operand stage gets exactly one arrival: in order while
-// the epilogue runs, and for the stages still ahead once it has given up a
-// wait (the issuers walk the same units, so no issuer waits for a phase that
-// is never arrived).
+// time-out, so the k-th wait of an issuer must meet the k-th arrival of the
+// epilogue on that slot, also after a bounded wait has been given up: then
+// neither side leaves its walk early; the issuer stops issuing, the epilogue
+// stops waiting and writing Y, and both still walk every operand stage of the
+// CTA's units (one arrival and one wait per stage, as in a normal run), while
+// all other waits return at once. Handing back the stages still ahead in one
+// burst instead could put two stages' arrivals into one barrier phase and
+// leave an issuer's last wait short of arrivals.
 constexpr int kBarSlot0 = 1;  // named barriers 1, 2 (0 is __syncthreads)
 constexpr int kSlotBarThreads = 32 * (kNumEpiWarps + 1);
 __device__ __forceinline__ void slot_bar_sync(int ts) {
@@ -282,25 +286,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (warp <= kNumIssuers) {
         // The whole warp walks the stages (bar.sync wants the warp
         // converged); lane 0 issues. Issuer `me` owns TMEM slot `me`.
+        // Once a wait has been given up (ok == false) the issuer issues
+        // nothing more but still walks every stage and takes every hand-back,
+        // as the epilogue still walks every stage and hands every one back:
+        // the named-barrier phases stay paired one to one (bar.sync has no
+        // time-out), and every other wait then returns at once.
         constexpr uint32_t idesc = idesc_f16_f32(BT, BW);
         const int me = warp - 1;
         bool ok = true;
         int gbase = 0;  // global index of the unit's first operand stage
-        int uses = 0;   // operand stages issued into my slot
-        for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+        int uses = 0;   // operand stages walked (issued into my slot)
+        for (int u = blockIdx.x; u < U; u += gridDim.x) {
           const Unit w = unit_of(u, Tw, nsb);
           const int nb = 4 * (w.sb1 - w.sb0);  // operand stages of the unit
-          for (int kb = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; kb < nb && ok;
+          for (int kb = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; kb < nb;
                kb += kNumIssuers) {
             const int gk = gbase + kb;  // global operand stage; gk % 2 == me
             const int slot = gk % SB;
-            if (!(ok = mbar_wait_warp(&bars->b_full[slot], (gk / SB) & 1, abort_flag, status,
-                                      kSiteBFull)))
-              break;
+            if (ok && !mbar_wait_warp(&bars->b_full[slot], (gk / SB) & 1, abort_flag, status,
+                                      kSiteBFull))
+              ok = false;
             // the epilogue has loaded the previous stage out of my slot
             if (uses++ > 0) slot_bar_sync(me);
             tc_fence_after();
-            if (lane == 0) {
+            if (lane == 0 && ok) {
               // descriptors of the stage's three tiles; a K step of 16
               // elements (32 bytes) adds 2 to the start-address field
               const uint8_t* bt = smem + slot * kOpStage;
@@ -326,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // take the epilogue's hand-back of the last stage, so every phase
         // of the slot's barrier closes
-        if (ok && uses > 0) slot_bar_sync(me);
+        if (uses > 0) slot_bar_sync(me);
         if (lane == 0) {
           // Every MMA of every issuer must be finished before TMEM is released.
           umma_commit(&bars->drain);
@@ -347,9 +356,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float2 acc[32], sb[32];
     uint32_t pA[32], pB[32];
     int gs = 0;
-    int handed = 0;  // operand stages whose TMEM slot was handed back
     bool ok = true;
-    for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
+    // Once a wait has been given up (ok == false) the epilogue stops waiting
+    // and writes no Y, but still walks every stage and hands every TMEM slot
+    // use back, so that the issuers' bar.sync phases stay paired.
+    for (int u = blockIdx.x; u < U; u += gridDim.x) {
       const Unit w = unit_of(u, Tw, nsb);
       const int m0 = (w.t / NT) * BW, n0 = (w.t % NT) * BT;
       const int n = n0 + tok;
@@ -358,10 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 32; ++j) acc[j] = make_float2(0.0f, 0.0f);
       for (int s = w.sb0; s < w.sb1; ++s) {
         const int slot = gs % SS;
-        if (!mbar_wait_warp(&bars->s_full[slot], (gs / SS) & 1, abort_flag, status, kSiteSFull)) {
+        if (ok && !mbar_wait_warp(&bars->s_full[slot], (gs / SS) & 1, abort_flag, status,
+                                  kSiteSFull))
           ok = false;
-          break;
-        }
         const uint8_t* st = smem + kRingS + slot * kScStage;
         const float* sda = reinterpret_cast<const float*>(st + kScDa) + tok;
 #pragma unroll
@@ -369,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Operand stage 4s + pp: its two chunks sit in TMEM slot pp % 2 (a
           // tile has a multiple of four stages), in the slot's use (pp / 2) % 2.
           const uint32_t ts = (uint32_t)(pp & 1);
-          if (!mbar_wait_warp(&bars->tfull[ts], (uint32_t)((pp >> 1) & 1), abort_flag, status,
-                              kSiteTFull))
+          if (ok && !mbar_wait_warp(&bars->tfull[ts], (uint32_t)((pp >> 1) & 1), abort_flag,
+                                    status, kSiteTFull))
             ok = false;
           // The stage's MMAs are complete, so its operand ring slot (pp: the
           // super-block starts at a global stage that is a multiple of SB)
@@ -390,7 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_before();
               __syncwarp();
               slot_bar_arrive((int)ts);
-              ++handed;
             }
             if (cc == 0) {
               chunk_fma<true>(sb, pA, da);
@@ -416,8 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->s_empty[slot]);
         ++gs;
       }
-      if (!ok) break;
-      if (n < N && write_y) {
+      if (ok && n < N && write_y) {
         float* yr = Y + (size_t)n * ldy + mcol;
         const int mleft = M - mcol;
         if (!w.split) {
@@ -450,18 +458,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-    }
-    if (!ok) {
-      // A wait was given up: hand back the TMEM slot of every operand stage
-      // still ahead, so that no issuer stays in bar.sync (the issuers walk
-      // the same units).
-      int total = 0;
-      for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const Unit w = unit_of(u, Tw, nsb);
-        total += 4 * (w.sb1 - w.sb0);
-      }
-      __syncwarp();
-      for (int k = handed; k < total; ++k) slot_bar_arrive(k & 1);
     }
   }
 

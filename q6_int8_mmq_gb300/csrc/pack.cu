@@ -73,6 +73,17 @@ __global__ void __launch_bounds__(256) q6k_pack_kernel(const uint8_t* __restrict
        i += (long long)gridDim.x * blockDim.x)
     reinterpret_cast<uint16_t*>(plane + g.d_off + (size_t)(i / dpad) * g.d_row)[nsb + (int)(i % dpad)] =
         0;
+  // the gaps that round each sub-plane up to 256 bytes (so that equal
+  // weights give byte-equal planes)
+  {
+    const size_t ends[4] = {(size_t)M * g.qlh_row, g.sc_off + (size_t)M * (K / 16),
+                            g.d_off + (size_t)M * g.d_row,
+                            g.dt_off + (size_t)nsb * (size_t)g.ldm * 4};
+    const size_t starts[4] = {g.sc_off, g.d_off, g.dt_off, g.total};
+    if (blockIdx.x == 0)
+      for (int r = 0; r < 4; ++r)
+        for (size_t i = ends[r] + threadIdx.x; i < starts[r]; i += blockDim.x) plane[i] = 0;
+  }
   // rows M .. ldm-1 of the transposed d sub-plane
   const int pad = g.ldm - M;
   const long long npad = (long long)pad * nsb;

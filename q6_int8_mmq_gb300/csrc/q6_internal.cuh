@@ -188,6 +188,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
                                                   uint32_t site,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
   if (MBAR_POLL(bar, parity)) return true;
+  if (*abort) return false;  // another thread has given up already
   const long long limit_cycles = (long long)(limit_ns * 21ull / 10ull);
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {

@@ -232,6 +232,10 @@ def test_pack_bitexact(q6, orc, M, K):
     o_d = o_sc + r(sc_sz)
     o_dt = o_d + r(d_sz)
     assert plane.size == o_dt + r(K // 256 * ldm * 4)
+    # the gaps that round each sub-plane up to 256 bytes are zero
+    for a, b in ((qlh_sz, o_sc), (o_sc + sc_sz, o_d), (o_d + d_sz, o_dt),
+                 (o_dt + K // 256 * ldm * 4, plane.size)):
+        assert np.all(plane[a:b] == 0)
     # qlh: per half h of super-block b: ql[64h:64h+64] then qh[32h:32h+32]
     qlh = plane[:qlh_sz].reshape(M, K // 256, 2, 96)
     for h in range(2):
