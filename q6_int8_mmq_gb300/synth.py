@@ -128,6 +128,30 @@ def q6k_raw_weights(seed: int, M: int, K: int) -> np.ndarray:
     return blk.reshape(M, (K // QK) * BLOCK_BYTES)
 
 
+Q4K_BLOCK_BYTES = 144
+
+
+def q4k_raw_weights(seed: int, M: int, K: int) -> np.ndarray:
+    """Raw q4_K weight matrix, GGUF byte layout: uint8 [M, (K/256)*144].
+
+    Block byte map (per super-block): d (f16) @0..1, dmin (f16) @2..3, the 12
+    bytes of packed 6-bit scales and mins @4..15, the 128 nibble bytes
+    @16..143. Nibbles, scales and mins are uniform (uniform bytes give
+    uniform 4-bit and 6-bit values under any bit packing), d and dmin are
+    f16(|N(0,1)| * 2e-3) like the q6_K recipe's d.
+    """
+    if K % QK:
+        raise ValueError("K must be a multiple of 256")
+    nblk = M * (K // QK)
+    blk = np.empty((nblk, Q4K_BLOCK_BYTES), dtype=np.uint8)
+    d = (np.abs(normal(substream(seed, 3), nblk)) * 2e-3).astype(np.float16)
+    dmin = (np.abs(normal(substream(seed, 4), nblk)) * 2e-3).astype(np.float16)
+    blk[:, 0:2] = d.view(np.uint8).reshape(nblk, 2)
+    blk[:, 2:4] = dmin.view(np.uint8).reshape(nblk, 2)
+    blk[:, 4:144] = uniform_bytes(substream(seed, 1), nblk * 140).reshape(nblk, 140)
+    return blk.reshape(M, (K // QK) * Q4K_BLOCK_BYTES)
+
+
 # ------------------------------------------------------------ activations ---
 
 def outlier_channels(seed: int, K: int, frac: float) -> np.ndarray:

@@ -327,10 +327,151 @@ def pin_quantizer_rounding(orc):
     assert list(xq[0, :9]) == [127, 3, -3, 1, -1, 2, 3, -4, 127]
 
 
+# -------------------------------------------------------------------- q4_K --
+# The q4_K line ("r18: Load-time B pre-expansion", Sec. 1 and 3.2; the
+# two-term rescale of "r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2).
+
+def _q4k_raw(seed, M, K):
+    return synth.q4k_raw_weights(seed, M, K)
+
+
+def _q4k_values(orc, s12):
+    return [orc.q4k_scale_min(s12, j) for j in range(8)]
+
+
+def pin_q4k_scale_example(orc):
+    """The hand-worked example of the scale/min packing reading (golden)."""
+    g = _golden("q4k_scale_min.txt")
+    vals = _q4k_values(orc, np.array(g["bytes"], np.uint8))
+    assert [v[0] for v in vals] == g["scales"]
+    assert [v[1] for v in vals] == g["mins"]
+
+
+def pin_q4k_scale_bijection(orc):
+    """Every one of the 96 bits of the 12 packed bytes moves exactly one of
+    the sixteen 6-bit values by exactly one power of two, and each (value,
+    bit) pair is reached by exactly one byte bit."""
+    rng = np.random.default_rng(41)
+    for _ in range(4):
+        s12 = rng.integers(0, 256, 12).astype(np.uint8)
+        base = np.array(_q4k_values(orc, s12)).T.reshape(16)    # 8 scales, then 8 mins
+        assert np.all((base >= 0) & (base < 64))
+        hit = set()
+        for byte in range(12):
+            for bit in range(8):
+                s2 = s12.copy()
+                s2[byte] ^= np.uint8(1 << bit)
+                diff = np.array(_q4k_values(orc, s2)).T.reshape(16) - base
+                nz = np.nonzero(diff)[0]
+                assert len(nz) == 1, (byte, bit)
+                step = abs(int(diff[nz[0]]))
+                assert step & (step - 1) == 0 and step < 64
+                hit.add((int(nz[0]), step.bit_length() - 1))
+        assert len(hit) == 96
+
+
+def pin_q4k_nibble_map(orc):
+    """The element map of the page's in-loop B expansion, restated: for
+    nibble pair p the 32 bytes at 16 + 32 p give sub-block 2 p (low nibbles)
+    and 2 p + 1 (high nibbles), element-ordered, raw values 0..15."""
+    for blk in _q4k_raw(42, 3, 256):
+        codes = orc.q4k_decode_block(blk)[0]
+        want = []
+        for p in range(4):
+            run = blk[16 + 32 * p: 16 + 32 * p + 32]
+            want += list(run & 0x0F) + list(run >> 4)
+        assert np.array_equal(codes, np.array(want, np.uint8))
+
+
+def pin_q4k_block_layout(orc):
+    """d at bytes 0-1, dmin at 2-3, the packed scales at 4-15 and the nibbles
+    at 16-143: flipping a byte changes only what lives there."""
+    blk = _q4k_raw(43, 1, 256)[0].copy()
+    c0, s0, m0, d0, n0 = orc.q4k_decode_block(blk)
+    for byte in range(144):
+        b2 = blk.copy()
+        b2[byte] ^= 0x01
+        c, s, m, d, n = orc.q4k_decode_block(b2)
+        changed = (not np.array_equal(c, c0), not (np.array_equal(s, s0) and np.array_equal(m, m0)),
+                   d != d0, n != n0)
+        want = (byte >= 16, 4 <= byte < 16, byte < 2, 2 <= byte < 4)
+        assert changed == want, byte
+
+
+def _q4k_dequant(orc, raw, M, K):
+    """Dequantised weights d*sc*q - dmin*m in f64 from the oracle's block decode."""
+    W = np.empty((M, K))
+    for m in range(M):
+        for b in range(K // 256):
+            codes, sc, mn, d, dmin = orc.q4k_decode_block(raw[m, 144 * b: 144 * (b + 1)])
+            c = np.arange(256) // 32
+            W[m, 256 * b: 256 * (b + 1)] = d * sc[c] * codes - dmin * mn[c]
+    return W
+
+
+def pin_q4k_bruteforce(orc):
+    """Dequantise both sides to f64 and multiply (numpy): the GEMM agrees."""
+    M, K, N = 7, 512, 5
+    raw = _q4k_raw(44, M, K)
+    xq, da = orc.quantize(synth.activations(45, N, K, outlier_frac=0.05))
+    X = xq.astype(np.float64) * np.repeat(da.astype(np.float64), 32, axis=1)
+    Yb = X @ _q4k_dequant(orc, raw, M, K).T
+    Y = orc.q4k_mmq(raw, M, K, xq, da)
+    assert np.max(np.abs(Y - Yb)) <= 1e-12 * np.max(np.abs(Yb))
+
+
+def pin_q4k_integer_case(orc):
+    """d = 1, dmin = 0, every scale 1 and integer activations with da = 1
+    reduce the GEMM to the int64 matmul of the nibbles and xq; the debug
+    partials are the per-32 sums of that product."""
+    M, K, N = 6, 512, 4
+    raw = _q4k_raw(46, M, K).reshape(-1, 144).copy()
+    raw[:, 0:2] = [0x00, 0x3C]                     # d = 1.0
+    raw[:, 2:4] = 0                                # dmin = 0
+    raw[:, 4:8] = 1                                # scales 0..3 = 1, top bits 0
+    raw[:, 8:12] = 0                               # mins 0..3 = 0, top bits 0
+    raw[:, 12:16] = 0x01                           # scales 4..7 = 1, mins 4..7 = 0
+    raw = raw.reshape(M, -1)
+    rng = np.random.default_rng(47)
+    X = rng.integers(-127, 128, size=(N, K)).astype(np.float32)
+    X[:, ::32] = 127.0                             # amax 127 in every block: da = 1
+    xq, da = orc.quantize(X)
+    assert np.all(da == 1.0) and np.array_equal(xq, X.astype(np.int8))
+    Q = np.stack([np.concatenate([orc.q4k_decode_block(raw[m, 144 * b: 144 * (b + 1)])[0]
+                                  for b in range(K // 256)]) for m in range(M)]).astype(np.int64)
+    Y, P = orc.q4k_mmq(raw, M, K, xq, da, partials=True)
+    assert np.array_equal(Y, (xq.astype(np.int64) @ Q.T).astype(np.float64))
+    Pw = (xq.astype(np.int64)[:, None, :] * Q[None]).reshape(N, M, K // 32, 32).sum(-1)
+    assert np.array_equal(P, Pw)
+
+
+def pin_q4k_min_term(orc):
+    """All nibbles 0 leave only the min term: Y = -sum dmin*m*da*sum(xq) over
+    the sub-blocks (closed form), and the partials are 0."""
+    M, K, N = 3, 512, 4
+    raw = _q4k_raw(48, M, K).reshape(-1, 144).copy()
+    raw[:, 16:] = 0
+    raw = raw.reshape(M, -1)
+    xq, da = orc.quantize(synth.activations(49, N, K))
+    S = xq.astype(np.int64).reshape(N, K // 32, 32).sum(-1)
+    want = np.zeros((N, M))
+    for m in range(M):
+        for b in range(K // 256):
+            _, _, mn, _, dmin = orc.q4k_decode_block(raw[m, 144 * b: 144 * (b + 1)])
+            for j in range(8):
+                c = 8 * b + j
+                want[:, m] -= dmin * mn[j] * da[:, c].astype(np.float64) * S[:, c]
+    Y, P = orc.q4k_mmq(raw, M, K, xq, da, partials=True)
+    assert np.all(P == 0)
+    assert np.max(np.abs(Y - want)) <= 1e-12 * np.max(np.abs(want))
+
+
 PINS = [pin_block_layout, pin_elem70, pin_restatements, pin_bijection, pin_all32,
         pin_d_zero, pin_f16, pin_dsc, pin_wexp, pin_bruteforce, pin_integer_case,
         pin_partials, pin_subblock_removal, pin_linearity, pin_pow2_scaling,
-        pin_single_block_closed_form, pin_quantizer_properties, pin_quantizer_rounding]
+        pin_single_block_closed_form, pin_quantizer_properties, pin_quantizer_rounding,
+        pin_q4k_scale_example, pin_q4k_scale_bijection, pin_q4k_nibble_map,
+        pin_q4k_block_layout, pin_q4k_bruteforce, pin_q4k_integer_case, pin_q4k_min_term]
 
 
 def failing_pins(orc):

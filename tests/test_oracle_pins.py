@@ -28,6 +28,11 @@ MUTANTS = {
     12: "f16 subnormals flushed",
     13: "f16 exponent bias off by one",
     14: "sequential byte map (ql[e/2], qh[e/4])",
+    15: "q4_K: min of sub-blocks 0-3 read from the scale bytes",
+    16: "q4_K: top bits of scales 4-7 taken from the min bytes",
+    17: "q4_K: low and high nibbles swapped",
+    18: "q4_K: min term added instead of subtracted",
+    19: "q4_K: neighbouring sub-block's activation scale",
 }
 
 
