@@ -744,6 +744,7 @@ def other_configs(args, q6, synth, device, hbm):
         v["frac_hbm"] = v["gbs"] / hbm
         res[f"skinny_{k}"] = v
     res.update(pages_shapes(q6, synth, device))
+    res["q4k_ffn_down"] = q4k_gemm(q6, synth, device)
     res["sweep"] = sweep_short(q6, synth, device)
     return res
 
@@ -796,6 +797,40 @@ def pages_shapes(q6, synth, device):
                                                "pages_ffn_down" else "0.654 ms (r41 kernel, GB10)"))
         del W, planes
     return out
+
+
+def q4k_gemm(q6, synth, device):
+    """The q4_K GEMM at the ffn_down shape (4096 x 11008, N = 3314, the same
+    activations): the GEMM on the resident operand plane, the call from the
+    packed plane (unpack + GEMM) and the quantiser with block sums, each
+    averaged over back-to-back calls."""
+    import torch
+    _, X, cfg = synth.workload("ffn_down")
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    raw = synth.q4k_raw_weights(0x51361401, M, K)
+    W = q6.q4k_pack_weights(torch.from_numpy(raw).to(device), M, K, wq=True)
+    Xd = torch.from_numpy(X).to(device)
+    act = q6.alloc_activations(N, K, device, want_xq=False, want_us=True)
+    Y = torch.empty((N, M), dtype=torch.float32, device=device)
+    q6.quantize_act(Xd, out=act)
+    res = {"workload": f"q4_K GEMM M={M} K={K} N={N}"}
+    for label, fn in (("gemm_resident_plane", lambda: q6.q4k_mmq(W, act, Y=Y, source="wq")),
+                      ("call_from_packed_plane", lambda: q6.q4k_mmq(W, act, Y=Y, source="raw")),
+                      ("quantize_with_sums", lambda: q6.quantize_act(Xd, out=act))):
+        for _ in range(3):
+            fn()
+        a, b = ev_pair()
+        a.record()
+        for _ in range(20):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        q6.sync_status()
+        ms = a.elapsed_time(b) / 20
+        res[label] = {"ms": ms} if label == "quantize_with_sums" else {
+            "ms": ms, "tops": 2.0 * M * N * K / ms / 1e9}
+    del W
+    return res
 
 
 def sweep_short(q6, synth, device, sweeps: int = 3):

@@ -58,6 +58,8 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_TC_WH 4   /* tensor-core GEMM on resident binary16 operand planes */
 #define Q6_PATH_SYNC_WEXP 5 /* legacy mma.sync int8 GEMM on the W_exp plane (q6k_mmq_mma_sync) */
 #define Q6_PATH_SKINNY_FUSED 6 /* quantiser and one/two-token GEMM in one kernel (q6k_mmq_f32) */
+#define Q6_PATH_Q4K_TC_RAW 7 /* q4_K: unpack of the packed plane into the workspace + tensor-core GEMM */
+#define Q6_PATH_Q4K_TC_WQ 8  /* q4_K: tensor-core GEMM on a resident binary16 operand plane */
 
 #define Q6_SKINNY_MAX_N 16
 #define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
@@ -108,6 +110,15 @@ int q8_act_plane_bytes(int N, int K, size_t *xq_bytes, size_t *da_bytes,
  * N == 0 is a no-op. */
 int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da,
                     uint16_t *Xh, q6_stream_t s);
+
+/* The same, and also the activation block sums the q4_K GEMM needs
+ * ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2: q4_K's rescale has
+ * a second term with the activation block's sum):
+ *   us : device f32 [K/32][ldda] (required, 16-byte aligned, layout of da),
+ *        us[c * ldda + n] = da[c][n] * (sum of token n's 32 codes of block c),
+ *        the product rounded to f32 once. */
+int q8_quantize_act_sums(const float *X, int N, int K, int ldx, int8_t *Xq, float *da,
+                         uint16_t *Xh, float *us, q6_stream_t s);
 
 /* ------------------------------------------------------------------------
  * Weight packing (load time; "r53 -- q6_K bundle: W_exp pre-expansion
@@ -291,6 +302,64 @@ int q6k_mmq_noalloc_status(q6_stream_t s);
  * allocation, no bounded waits, asynchronous on s. */
 int q6k_mmq_f32(const void *plane, int M, int K, const float *X, int ldx, int N, float *Y,
                 int ldy, int *path_out, q6_stream_t s);
+
+/* ------------------------------------------------------------------------
+ * The q4_K x int8 GEMM ("r18: Load-time B pre-expansion -- staging becomes a
+ * bulk copy", Sec. 1 and 3.2: the 144-byte block and its per-chunk pair
+ * (d * sc, -dmin * m); "r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2:
+ * the two-term rescale). Weights are q4_K super-blocks of 256 elements in 8
+ * sub-blocks of 32; the dequantised weight is d * sc[j] * q - dmin * m[j]
+ * (q the raw nibble 0..15, sc and m 6-bit):
+ *
+ *   Y[n][m] = sum over sub-blocks c of da[c][n] * (d * sc[c] * P[n][m][c]
+ *                                                  - dmin * m[c] * S[n][c]),
+ *   P = sum over the 32 elements of q * xq,  S = sum of the 32 xq.
+ *
+ * raw (q4k_pack_weights): M rows of K/256 consecutive 144-byte blocks in the
+ *      GGUF layout: d (f16) @0, dmin (f16) @2, 12 bytes of packed 6-bit
+ *      scales and mins @4, 128 nibble bytes @16 (nibble pair p: the 32 bytes
+ *      at 16 + 32 p, sub-block 2p in the low nibbles and 2p + 1 in the high
+ *      ones). The 12-byte packing, which the pages call but do not print, is
+ *      read as GGUF's: sub-blocks j < 4 take the low 6 bits of bytes j
+ *      (scale) and j + 4 (min); sub-blocks j >= 4 take the nibbles of byte
+ *      j + 4 (low: scale, high: min) as their low 4 bits and the top 2 bits
+ *      of bytes j - 4 (scale) and j (min) as bits 4-5. Device memory or host
+ *      memory the device reads, as for q6k_pack_weights.
+ * plane (device, 256-byte aligned, q4k_plane_bytes() bytes), sub-planes at
+ *      256-byte aligned offsets: qs uint8 [M][K/2] (the nibble bytes as they
+ *      are), sc uint8 [M][K/32], m uint8 [M][K/32] (decoded), dT f32
+ *      [K/256][ldm] (d, transposed, ldm = M rounded up to 4), mvT f32
+ *      [K/32][ldm] (dmin * m, exact, transposed); padding is zero.
+ * wq (device, optional, 16-byte aligned): the binary16 operand plane [M][K]
+ *      the tensor-core GEMM reads, sc * q (at most 945: exact).
+ * -------------------------------------------------------------------- */
+
+/* Bytes of the packed q4_K plane and of the wq plane (2 * M * K). */
+int q4k_plane_bytes(int M, int K, size_t *plane_bytes, size_t *wq_bytes);
+
+/* Fills plane (and wq when not NULL) from raw. M > 0, K % 256 == 0. */
+int q4k_pack_weights(const uint8_t *raw, int M, int K, void *plane, uint16_t *wq,
+                     q6_stream_t s);
+
+/* The unpack pass alone: wq [M][K] from the packed plane. */
+int q4k_unpack_weights(const void *plane, int M, int K, uint16_t *wq, q6_stream_t s);
+
+/* The q4_K GEMM on the tensor cores, for any N >= 0 (there is no few-token
+ * kernel for q4_K; small N run as one ragged token tile).
+ *   plane : the packed q4_K plane (required); wq : resident operand plane or
+ *           NULL (then it is unpacked into the workspace first).
+ *   Xh, da, us : from q8_quantize_act_sums (binary16 codes, scales, block sums).
+ *   workspace : device, 256-byte aligned, at least 2 * M * K bytes when wq is
+ *           NULL or partials is not NULL; contents afterwards unspecified.
+ *   partials : NULL, or device int32 [N][M][K/32] that receives every exact
+ *           P = sum over a sub-block of q * xq (debug: one more GEMM launch on
+ *           the plane of the raw nibbles, unpacked in the workspace).
+ *   path_out : NULL or receives Q6_PATH_Q4K_TC_RAW / Q6_PATH_Q4K_TC_WQ.
+ * Alignment: plane, workspace 256 B; Xh, da, us, wq 16 B; Y, partials 4 B.
+ * Errors as for q6k_mmq. */
+int q4k_mmq(const void *plane, const uint16_t *wq, int M, int K, const uint16_t *Xh,
+            const float *da, const float *us, int N, float *Y, int ldy, void *workspace,
+            size_t workspace_bytes, int32_t *partials, int *path_out, q6_stream_t s);
 
 #ifdef __cplusplus
 }

@@ -19,10 +19,11 @@ LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
 
 Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
 (PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH, PATH_SYNC_WEXP,
- PATH_SKINNY_FUSED) = range(7)
+ PATH_SKINNY_FUSED, PATH_Q4K_TC_RAW, PATH_Q4K_TC_WQ) = range(9)
 PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh", PATH_SYNC_WEXP: "sync_wexp",
-              PATH_SKINNY_FUSED: "skinny_fused"}
+              PATH_SKINNY_FUSED: "skinny_fused", PATH_Q4K_TC_RAW: "q4k_tc_raw",
+              PATH_Q4K_TC_WQ: "q4k_tc_wq"}
 SKINNY_MAX_N = 16
 FUSED_MAX_N = 2
 
@@ -47,6 +48,11 @@ SIGNATURES = [
     ("q6k_mmq_noalloc_status", _I, [_P]),
     ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _IP, _P]),
     ("q6k_mmq_f32", _I, [_P, _I, _I, _P, _I, _I, _P, _I, _IP, _P]),
+    ("q8_quantize_act_sums", _I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    ("q4k_plane_bytes", _I, [_I, _I, _SZ, _SZ]),
+    ("q4k_pack_weights", _I, [_P, _I, _I, _P, _P, _P]),
+    ("q4k_unpack_weights", _I, [_P, _I, _I, _P, _P]),
+    ("q4k_mmq", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP, _P]),
 ]
 
 
@@ -151,13 +157,16 @@ def plane_bytes(M: int, K: int):
 @dataclasses.dataclass(frozen=True)
 class Activations:
     """Quantised activations on the device: xq [N,K] int8, da [K/32, ldda] f32,
-    xh [N,K] f16 (xq or xh may be None). Checked once, when made; read-only."""
+    xh [N,K] f16 (xq or xh may be None), and optionally us [K/32, ldda] f32,
+    da times each 32-block's code sum (the q4_K GEMM's min term needs it).
+    Checked once, when made; read-only."""
     N: int
     K: int
     xq: object
     da: object
     xh: object
     ldda: int
+    us: object = None
 
     def __post_init__(self):
         import torch
@@ -165,7 +174,8 @@ class Activations:
         if self.ldda != act_plane_bytes(N, K)[3]:
             raise Q6Error(Q6_EINVAL, f"ldda {self.ldda} does not match {act_plane_bytes(N, K)[3]}")
         _same_device((self.xq, "xq", torch.int8, (N, K)), (self.xh, "xh", torch.float16, (N, K)),
-                     (self.da, "da", torch.float32, (K // 32, self.ldda)))
+                     (self.da, "da", torch.float32, (K // 32, self.ldda)),
+                     (self.us, "us", torch.float32, (K // 32, self.ldda)))
 
     @property
     def device(self):
@@ -173,7 +183,7 @@ class Activations:
 
 
 def alloc_activations(N: int, K: int, device=None, want_xh: bool = True,
-                      want_xq: bool = True) -> Activations:
+                      want_xq: bool = True, want_us: bool = False) -> Activations:
     """Buffers for quantised activations. A prefill caller that only runs the
     tensor-core GEMM (N > SKINNY_MAX_N) can skip xq; the few-token kernels
     need it (and not xh)."""
@@ -183,24 +193,31 @@ def alloc_activations(N: int, K: int, device=None, want_xh: bool = True,
     xq = torch.empty((N, K), dtype=torch.int8, device=dev) if want_xq else None
     da = torch.empty((K // 32, ldda), dtype=torch.float32, device=dev)
     xh = torch.empty((N, K), dtype=torch.float16, device=dev) if want_xh else None
-    return Activations(N, K, xq, da, xh, ldda)
+    us = torch.empty((K // 32, ldda), dtype=torch.float32, device=dev) if want_us else None
+    return Activations(N, K, xq, da, xh, ldda, us)
 
 
 def quantize_act(X, out: Activations | None = None, want_xh: bool = True, stream=None,
-                 want_xq: bool = True) -> Activations:
-    """Quantises f32 activations X [N, K] (CUDA tensor, last dim contiguous)."""
+                 want_xq: bool = True, want_us: bool = False) -> Activations:
+    """Quantises f32 activations X [N, K] (CUDA tensor, last dim contiguous);
+    with want_us (or an `out` that has us) also the block sums us."""
     import torch
     if not isinstance(X, torch.Tensor) or X.dim() != 2:
         raise Q6Error(Q6_EINVAL, "X must be a 2-D torch tensor [N, K]")
     N, K = X.shape
     _tensor(X, "X", torch.float32, (N, K), rows=True)
     if out is None:
-        out = alloc_activations(N, K, X.device, want_xh, want_xq)
+        out = alloc_activations(N, K, X.device, want_xh, want_xq, want_us)
     elif out.N != N or out.K != K or out.device != X.device:
         raise Q6Error(Q6_EINVAL, f"out holds {out.N} x {out.K} activations on {out.device}, "
                                  f"X is {N} x {K} on {X.device}")
-    _check(load().q8_quantize_act(_ptr(X), N, K, _row_stride(X), _ptr(out.xq), _ptr(out.da),
-                                  _ptr(out.xh), _stream(stream)))
+    if out.us is not None:
+        _check(load().q8_quantize_act_sums(_ptr(X), N, K, _row_stride(X), _ptr(out.xq),
+                                           _ptr(out.da), _ptr(out.xh), _ptr(out.us),
+                                           _stream(stream)))
+    else:
+        _check(load().q8_quantize_act(_ptr(X), N, K, _row_stride(X), _ptr(out.xq),
+                                      _ptr(out.da), _ptr(out.xh), _stream(stream)))
     return out
 
 
@@ -410,3 +427,107 @@ def mmq_mma_sync(w: Weights, act: Activations, Y=None, partials: bool = False, s
 def sync_status(stream=None):
     """Waits for the stream and raises if a kernel gave up a bounded wait."""
     _check(load().q6_sync_status(_stream(stream)))
+
+
+# ------------------------------------------------------------------- q4_K ---
+
+@functools.lru_cache(maxsize=256)
+def q4k_plane_bytes(M: int, K: int):
+    """(packed q4_K plane bytes, operand plane bytes) of an M x K weight."""
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().q4k_plane_bytes(M, K, ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+@dataclasses.dataclass(frozen=True)
+class Q4Weights:
+    """A packed q4_K weight on the device: the packed plane and optionally the
+    resident binary16 operand plane wq [M, K] (sc * q). Checked once, when
+    made; read-only."""
+    M: int
+    K: int
+    plane: object
+    wq: object
+
+    def __post_init__(self):
+        import torch
+        _same_device((self.wq, "wq", torch.float16, (self.M, self.K)),
+                     (self.plane, "plane", torch.uint8, (q4k_plane_bytes(self.M, self.K)[0],)))
+
+    @property
+    def device(self):
+        return self.plane.device
+
+
+def q4k_pack_weights(raw, M: int, K: int, wq: bool = False, stream=None,
+                     device=None) -> Q4Weights:
+    """Packs raw GGUF q4_K bytes (a contiguous uint8 tensor of M*K/256*144
+    bytes, on a CUDA device or in host memory, as pack_weights)."""
+    import torch
+    pb, wb = q4k_plane_bytes(M, K)
+    if (not isinstance(raw, torch.Tensor) or raw.numel() != M * (K // 256) * 144
+            or raw.dtype != torch.uint8 or not raw.is_contiguous()):
+        raise Q6Error(Q6_EINVAL, "raw must be a contiguous uint8 tensor of M*K/256*144 bytes")
+    on_host = not raw.is_cuda
+    if on_host:
+        dev = torch.device(device) if device is not None else torch.device(
+            "cuda", torch.cuda.current_device())
+        if not raw.is_pinned():
+            raw = raw.pin_memory()
+    else:
+        dev = raw.device
+    plane = torch.empty(pb, dtype=torch.uint8, device=dev)
+    w16 = torch.empty((M, K), dtype=torch.float16, device=dev) if wq else None
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        _check(load().q4k_pack_weights(_ptr(raw), M, K, _ptr(plane), _ptr(w16), _stream(s)))
+        if on_host:
+            s.synchronize()
+    return Q4Weights(M, K, plane, w16)
+
+
+def q4k_unpack_weights(w: Q4Weights, out=None, stream=None):
+    """The q4_K unpack pass: the binary16 operand plane [M, K] = sc * q."""
+    import torch
+    if out is None:
+        out = torch.empty((w.M, w.K), dtype=torch.float16, device=w.device)
+    _tensor(out, "out", torch.float16, (w.M, w.K), w.device)
+    _check(load().q4k_unpack_weights(_ptr(w.plane), w.M, w.K, _ptr(out), _stream(stream)))
+    return out
+
+
+def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",
+            partials: bool = False, workspace=None, stream=None):
+    """Y [N, M] f32 = the q4_K x int8 GEMM (tensor cores, any N). act needs xh,
+    da and us (quantize_act(..., want_us=True)). source: "raw" (unpack the
+    packed plane per call), "wq" (the resident operand plane) or "auto".
+    Returns (Y, path name, partials [N, M, K/32] int32 or None)."""
+    import torch
+    N, M, K = act.N, w.M, w.K
+    if act.K != K:
+        raise Q6Error(Q6_EINVAL, "activation K does not match the weight")
+    if act.xh is None or act.us is None:
+        raise Q6Error(Q6_EINVAL, "the q4_K GEMM needs activations with xh and us")
+    if source == "auto":
+        source = "wq" if w.wq is not None else "raw"
+    if source == "wq" and w.wq is None:
+        raise Q6Error(Q6_EINVAL, "weights were packed without the wq plane")
+    wq = w.wq if source == "wq" else None
+    dev = w.device
+    if act.device != dev:
+        raise Q6Error(Q6_EINVAL, f"activations on {act.device}, weights on {dev}")
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
+    P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
+    need = 2 * M * K if (wq is None or partials) else 0
+    if workspace is not None:
+        _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
+                tuple(getattr(workspace, "shape", ())), dev)
+    ws = workspace if workspace is not None else (_workspace(need, dev) if need else None)
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    path = ctypes.c_int(-1)
+    _check(load().q4k_mmq(_ptr(w.plane), _ptr(wq), M, K, _ptr(act.xh), _ptr(act.da),
+                          _ptr(act.us), N, _ptr(Y), _row_stride(Y), _ptr(ws), ws_bytes, _ptr(P),
+                          ctypes.byref(path), _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value)), P

@@ -101,6 +101,30 @@ int encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
 
 int ldda_of(int N) { return (N + 3) / 4 * 4; }
 
+// The address a kernel reads `raw` through: device memory as it is, or host
+// memory this device reads directly: page-locked (registered or
+// cudaHostAlloc'd; its device pointer), or any host memory when the device
+// reads pageable memory (coherent host memory, as on Grace-Blackwell).
+int device_readable(const uint8_t* raw, const uint8_t** src) {
+  *src = raw;
+  cudaPointerAttributes pa;
+  cudaError_t e = cudaPointerGetAttributes(&pa, raw);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(raw)");
+  if (pa.type == cudaMemoryTypeHost && pa.devicePointer) {
+    *src = static_cast<const uint8_t*>(pa.devicePointer);
+  } else if (pa.type == cudaMemoryTypeUnregistered) {
+    int dev = 0, pageable = 0;
+    if ((e = cudaGetDevice(&dev)) ||
+        (e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev)))
+      return cuda_fail(e, "cudaDeviceGetAttribute(pageable memory access)");
+    if (!pageable)
+      return fail(Q6_EINVAL,
+                  "raw is pageable host memory this device cannot read: page-lock it "
+                  "(cudaHostRegister) or copy it to the device");
+  }
+  return Q6_OK;
+}
+
 }  // namespace
 
 namespace q6 {
@@ -111,6 +135,7 @@ namespace q6 {
 // no-allocation entry point uses it too).
 int encode_tc_maps(TcMaps* maps, const uint8_t* plane, const void* wop, const void* Xh,
                    const float* da, int M, int K, int N) {
+  memset(maps, 0, sizeof(*maps));
   const PlaneGeom g = plane_geom(M, K);
   const uint16_t* whi = static_cast<const uint16_t*>(wop);
   const uint16_t* wlo = whi + (size_t)M * (size_t)K;
@@ -126,6 +151,29 @@ int encode_tc_maps(TcMaps* maps, const uint8_t* plane, const void* wop, const vo
       (rc = encode_2d(&maps->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, plane + g.dt_off, (uint64_t)M,
                       (uint64_t)K / 256, (uint64_t)g.ldm * 4, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
                       "d")))
+    return rc;
+  return Q6_OK;
+}
+
+int encode_tc_maps_q4k(TcMaps* maps, const uint8_t* q4plane, const void* wq, const void* Xh,
+                       const float* da, const float* us, int M, int K, int N) {
+  memset(maps, 0, sizeof(*maps));
+  const Q4Geom g = q4_geom(M, K);
+  int rc;
+  if ((rc = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Xh")) ||
+      (rc = encode_2d(&maps->whi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wq, (uint64_t)K, (uint64_t)M,
+                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Wq")) ||
+      (rc = encode_2d(&maps->da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
+                      (uint64_t)ldda_of(N) * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE, "da")) ||
+      (rc = encode_2d(&maps->us, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, us, (uint64_t)N, (uint64_t)K / 32,
+                      (uint64_t)ldda_of(N) * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE, "us")) ||
+      (rc = encode_2d(&maps->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q4plane + g.dt_off, (uint64_t)M,
+                      (uint64_t)K / 256, (uint64_t)g.ldm * 4, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      "dT")) ||
+      (rc = encode_2d(&maps->mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q4plane + g.mv_off, (uint64_t)M,
+                      (uint64_t)K / 32, (uint64_t)g.ldm * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      "mvT")))
     return rc;
   return Q6_OK;
 }
@@ -186,23 +234,34 @@ int q8_act_plane_bytes(int N, int K, size_t* xq_bytes, size_t* da_bytes, size_t*
   return Q6_OK;
 }
 
-int q8_quantize_act(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, uint16_t* Xh,
-                    q6_stream_t s) {
+static int quantize_entry(const float* X, int N, int K, int ldx, int8_t* Xq, float* da,
+                          uint16_t* Xh, float* us, q6_stream_t s, const char* name) {
   if (N < 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need N >= 0, K > 0, K %% 256 == 0");
   if (ldx < K) return fail(Q6_EINVAL, "ldx (%d) < K (%d)", ldx, K);
   if (N == 0) return Q6_OK;
   if (!X || !da || (!Xq && !Xh)) return fail(Q6_EINVAL, "X, da and one of Xq, Xh are required");
   if (!aligned(X, 16) || ldx % 4 || (Xq && !aligned(Xq, 16)) || !aligned(da, 16) ||
-      (Xh && !aligned(Xh, 16)))
-    return fail(Q6_EALIGN, "X, Xq, da, Xh must be 16-byte aligned and ldx a multiple of 4");
+      (Xh && !aligned(Xh, 16)) || (us && !aligned(us, 16)))
+    return fail(Q6_EALIGN, "X, Xq, da, Xh, us must be 16-byte aligned and ldx a multiple of 4");
   if ((long long)N * K > (1LL << 40)) return fail(Q6_ESIZE, "N*K too large");
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
   cudaError_t e = q6::launch_quantize(X, N, K, ldx, Xq, da, ldda_of(N),
-                                      reinterpret_cast<__half*>(Xh), (cudaStream_t)s);
-  if (e != cudaSuccess) return cuda_fail(e, "q8_quantize_act launch");
+                                      reinterpret_cast<__half*>(Xh), us, (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, name);
   return Q6_OK;
+}
+
+int q8_quantize_act(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, uint16_t* Xh,
+                    q6_stream_t s) {
+  return quantize_entry(X, N, K, ldx, Xq, da, Xh, nullptr, s, "q8_quantize_act launch");
+}
+
+int q8_quantize_act_sums(const float* X, int N, int K, int ldx, int8_t* Xq, float* da,
+                         uint16_t* Xh, float* us, q6_stream_t s) {
+  if (N > 0 && !us) return fail(Q6_EINVAL, "us is required");
+  return quantize_entry(X, N, K, ldx, Xq, da, Xh, us, s, "q8_quantize_act_sums launch");
 }
 
 int q6k_plane_bytes(int M, int K, size_t* plane_bytes, size_t* wexp_bytes) {
@@ -222,27 +281,9 @@ int q6k_pack_weights(const uint8_t* raw, int M, int K, void* plane, int8_t* wexp
   DevState* st;
   int rc = device_state(&st);
   if (rc) return rc;
-  // raw may be device memory or host memory this device reads directly:
-  // page-locked (registered or cudaHostAlloc'd; its device pointer is used),
-  // or any host memory when the device reads pageable memory (coherent
-  // host memory, as on Grace-Blackwell).
-  const uint8_t* src = raw;
-  cudaPointerAttributes pa;
-  cudaError_t e = cudaPointerGetAttributes(&pa, raw);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(raw)");
-  if (pa.type == cudaMemoryTypeHost && pa.devicePointer) {
-    src = static_cast<const uint8_t*>(pa.devicePointer);
-  } else if (pa.type == cudaMemoryTypeUnregistered) {
-    int dev = 0, pageable = 0;
-    if ((e = cudaGetDevice(&dev)) ||
-        (e = cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, dev)))
-      return cuda_fail(e, "cudaDeviceGetAttribute(pageable memory access)");
-    if (!pageable)
-      return fail(Q6_EINVAL,
-                  "raw is pageable host memory this device cannot read: page-lock it "
-                  "(cudaHostRegister) or copy it to the device");
-  }
-  e = q6::launch_pack(src, M, K, static_cast<uint8_t*>(plane), wexp, (cudaStream_t)s);
+  const uint8_t* src = nullptr;
+  if ((rc = device_readable(raw, &src))) return rc;
+  cudaError_t e = q6::launch_pack(src, M, K, static_cast<uint8_t*>(plane), wexp, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "q6k_pack_weights launch");
   if (wh) {
     e = q6::launch_expand_raw(static_cast<const uint8_t*>(plane), M, K,
@@ -446,6 +487,106 @@ int q6k_mmq_mma_sync(const void* plane, const int8_t* wexp, int M, int K, const 
                                       ldda_of(N), N, Y, ldy, dbg, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "mma.sync kernel launch");
   if (path_out) *path_out = Q6_PATH_SYNC_WEXP;
+  return Q6_OK;
+}
+
+/* ------------------------------------------------------------------ q4_K */
+
+int q4k_plane_bytes(int M, int K, size_t* plane_bytes, size_t* wq_bytes) {
+  if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
+  if (plane_bytes) *plane_bytes = q6::q4_geom(M, K).total;
+  if (wq_bytes) *wq_bytes = (size_t)M * (size_t)K * 2;
+  return Q6_OK;
+}
+
+int q4k_pack_weights(const uint8_t* raw, int M, int K, void* plane, uint16_t* wq, q6_stream_t s) {
+  if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
+  if (!raw || !plane) return fail(Q6_EINVAL, "raw and plane are required");
+  if (!aligned(plane, 256) || (wq && !aligned(wq, 16)))
+    return fail(Q6_EALIGN, "plane must be 256-byte aligned, wq 16-byte aligned");
+  if ((long long)M * K > (1LL << 40)) return fail(Q6_ESIZE, "M*K too large");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  const uint8_t* src = nullptr;
+  if ((rc = device_readable(raw, &src))) return rc;
+  cudaError_t e = q6::launch_q4k_pack(src, M, K, static_cast<uint8_t*>(plane), (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "q4k_pack_weights launch");
+  if (wq) {
+    e = q6::launch_q4k_expand(static_cast<const uint8_t*>(plane), M, K, false,
+                              reinterpret_cast<__half*>(wq), (cudaStream_t)s);
+    if (e != cudaSuccess) return cuda_fail(e, "q4k_pack_weights expand launch");
+  }
+  return Q6_OK;
+}
+
+int q4k_unpack_weights(const void* plane, int M, int K, uint16_t* wq, q6_stream_t s) {
+  if (M <= 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need M > 0, K > 0, K %% 256 == 0");
+  if (!plane || !wq) return fail(Q6_EINVAL, "plane and wq are required");
+  if (!aligned(plane, 256) || !aligned(wq, 16)) return fail(Q6_EALIGN, "plane 256 B, wq 16 B");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = q6::launch_q4k_expand(static_cast<const uint8_t*>(plane), M, K, false,
+                                        reinterpret_cast<__half*>(wq), (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "q4k_unpack_weights launch");
+  return Q6_OK;
+}
+
+int q4k_mmq(const void* plane, const uint16_t* wq, int M, int K, const uint16_t* Xh,
+            const float* da, const float* us, int N, float* Y, int ldy, void* workspace,
+            size_t workspace_bytes, int32_t* partials, int* path_out, q6_stream_t s) {
+  if (path_out) *path_out = Q6_PATH_NONE;
+  if (M <= 0 || K <= 0 || K % 256 || N < 0)
+    return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
+  if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
+  if (N == 0) return Q6_OK;
+  if (!plane || !Xh || !da || !us || !Y)
+    return fail(Q6_EINVAL, "plane, Xh, da, us and Y are required");
+  if (!aligned(plane, 256) || !aligned(Xh, 16) || !aligned(da, 16) || !aligned(us, 16) ||
+      !aligned(Y, 4) || (wq && !aligned(wq, 16)) || (partials && !aligned(partials, 4)) ||
+      (workspace && !aligned(workspace, 256)))
+    return fail(Q6_EALIGN, "plane, workspace 256 B; Xh, da, us, wq 16 B; Y, partials 4 B");
+  if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
+    return fail(Q6_ESIZE, "problem too large");
+  if (!wq || partials) {
+    const size_t need = (size_t)M * (size_t)K * 2;
+    if (!workspace || workspace_bytes < need)
+      return fail(Q6_ESIZE, "workspace of %zu bytes needed to unpack the weights (got %zu)", need,
+                  workspace ? workspace_bytes : (size_t)0);
+  }
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  const uint8_t* pb = static_cast<const uint8_t*>(plane);
+  __half* ws = static_cast<__half*>(workspace);
+  cudaError_t e;
+  const void* wop = wq;
+  int path = Q6_PATH_Q4K_TC_WQ;
+  if (!wq) {
+    if ((e = q6::launch_q4k_expand(pb, M, K, false, ws, (cudaStream_t)s)) != cudaSuccess)
+      return cuda_fail(e, "q4_K weight unpack launch");
+    wop = ws;
+    path = Q6_PATH_Q4K_TC_RAW;
+  }
+  q6::TcMaps maps;
+  if ((rc = q6::encode_tc_maps_q4k(&maps, pb, wop, Xh, da, us, M, K, N))) return rc;
+  e = q6::launch_mmq_tc_q4k(maps, M, K, N, Y, ldy, q6::TcDebugOut{}, st->status, (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "q4_K tensor-core kernel launch");
+  if (partials) {
+    // the per-sub-block P = sum q * xq: one more launch on the plane of the
+    // raw nibbles (unit scale), writing the chunk accumulators and not Y
+    if ((e = q6::launch_q4k_expand(pb, M, K, true, ws, (cudaStream_t)s)) != cudaSuccess)
+      return cuda_fail(e, "q4_K debug unpack launch");
+    if ((rc = q6::encode_tc_maps_q4k(&maps, pb, ws, Xh, da, us, M, K, N))) return rc;
+    q6::TcDebugOut dbg;
+    dbg.out = partials;
+    dbg.stride = K / 32;
+    dbg.write_y = 0;
+    if ((e = q6::launch_mmq_tc_q4k(maps, M, K, N, Y, ldy, dbg, st->status, (cudaStream_t)s)))
+      return cuda_fail(e, "q4_K debug kernel launch");
+  }
+  if (path_out) *path_out = path;
   return Q6_OK;
 }
 

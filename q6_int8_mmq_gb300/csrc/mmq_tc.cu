@@ -70,14 +70,27 @@ constexpr int kNumIssuers = 2;  // MMA-issuing threads: lane 0 of warps 1-2
 constexpr int kTmemCols = 512, kBufCols = 128;
 constexpr int kNumSlots = 2;  // TMEM slots of two chunk buffers (one operand stage) each
 
-constexpr int kOpX = 0, kOpWhi = BT * 128, kOpWlo = kOpWhi + BW * 128;
-constexpr int kOpStage = kOpWlo + BW * 128;                            // 48 KB
-constexpr int kScDa = 0, kScD = 8 * BT * 4, kScStage = kScD + BW * 4;  // 4.5 KB
-constexpr int kRingS = SB * kOpStage;  // the scale ring follows the operand ring
-constexpr int kRingsBytes = kRingS + SS * kScStage;
-static_assert(kOpStage % 1024 == 0, "operand stages must keep 1024-byte alignment");
+// Weight formats: q6_K (two operand planes W_hi, W_lo) and q4_K (one plane
+// sc * q, and the min term in the epilogue).
+enum : int { kFmtQ6 = 0, kFmtQ4 = 1 };
+
+// Shared-memory layout per format. Operand stage: Xh, W_hi (or sc * q) and,
+// for q6_K, W_lo tiles of 128 rows x 128 bytes. Scale stage (one
+// super-block): da [8 chunks][128 tokens], d [128 rows], and for q4_K the
+// activation block sums us = da * S [8][128 tokens] and dmin * m [8][128 rows].
+template <int kFmt>
+struct Lay {
+  static constexpr int kOpX = 0, kOpWhi = BT * 128, kOpWlo = kOpWhi + BW * 128;
+  static constexpr int kOpStage = (kFmt == kFmtQ6 ? kOpWlo + BW * 128 : kOpWlo);  // 48 / 32 KB
+  static constexpr int kScDa = 0, kScD = 8 * BT * 4, kScUs = kScD + BW * 4;
+  static constexpr int kScMv = kScUs + 8 * BT * 4;
+  static constexpr int kScStage = (kFmt == kFmtQ6 ? kScUs : kScMv + 8 * BW * 4);  // 4.5 / 12.5 KB
+  static constexpr int kRingS = SB * kOpStage;  // the scale ring follows the operand ring
+  static constexpr int kRingsBytes = kRingS + SS * kScStage;
+  static_assert(kOpStage % 1024 == 0, "operand stages must keep 1024-byte alignment");
+  static_assert(kScStage % 128 == 0, "scale stages must keep 128-byte alignment");
+};
 static_assert(SB * KB == 256, "the epilogue frees operand slot pp of each super-block");
-static_assert(kScStage % 128 == 0, "scale stages must keep 128-byte alignment");
 
 enum : uint32_t { kSiteSEmpty = 1, kSiteSFull = 2, kSiteBEmpty = 3, kSiteBFull = 4,
                   kSiteTFull = 6, kSiteDrain = 8 };
@@ -113,8 +126,12 @@ struct Bars {
   int abort;
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kRingsBytes + sizeof(Bars);
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+template <int kFmt>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Lay<kFmt>::kRingsBytes + sizeof(Bars);
+}
+static_assert(smem_bytes<kFmtQ6>() <= 232448 && smem_bytes<kFmtQ4>() <= 232448,
+              "shared memory budget");
 
 // Work units: units 0 .. Tw-1 are whole tiles; when the last round of tiles
 // would leave more than half the CTAs idle, each of its tiles is split into
@@ -161,6 +178,18 @@ __device__ __forceinline__ void chunk_fma(float2* sb, const uint32_t (&p)[32], f
   }
 }
 
+// acc[j] += (nu, nu) * (dmin * m) of 32 columns (16 pairs, 8 float4 in
+// shared memory).
+__device__ __forceinline__ void min_term(float2* acc, float nu, const float4* mv) {
+  const float2 nu2 = make_float2(nu, nu);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float4 m4 = mv[j];
+    acc[2 * j] = __ffma2_rn(nu2, make_float2(m4.x, m4.y), acc[2 * j]);
+    acc[2 * j + 1] = __ffma2_rn(nu2, make_float2(m4.z, m4.w), acc[2 * j + 1]);
+  }
+}
+
 // The exact integers of 32 columns of a chunk accumulator, to the debug
 // output at out[(n * M + m) * stride + off] (off = c * mul + add).
 template <bool kPartials>
@@ -179,18 +208,21 @@ __device__ __forceinline__ void dump_partials(int32_t* __restrict__ out, int M, 
   }
 }
 
-template <bool kPartials>
+template <int kFmt, bool kPartials>
 __global__ void __launch_bounds__(kThreads, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWhi,
                   const __grid_constant__ CUtensorMap tmWlo, const __grid_constant__ CUtensorMap tmDa,
-                  const __grid_constant__ CUtensorMap tmD, int M, int K, int N, int Tw, int U,
+                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmUs,
+                  const __grid_constant__ CUtensorMap tmMv, int M, int K, int N, int Tw, int U,
                   float* __restrict__ Y, int ldy, int y_vec4, int32_t* __restrict__ partials,
                   int p_stride, int p_mul, int p_add, int write_y,
                   unsigned int* __restrict__ status) {
+  using L = Lay<kFmt>;
+  constexpr bool kQ4 = kFmt == kFmtQ4;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + kRingsBytes);
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kRingsBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = (N + BT - 1) / BT;
   const int nsb = K / 256;  // super-blocks per tile
@@ -216,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmWlo);
     tma_prefetch_desc(&tmDa);
     tma_prefetch_desc(&tmD);
+    if (kQ4) {
+      tma_prefetch_desc(&tmUs);
+      tma_prefetch_desc(&tmMv);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -232,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ---------------------------------------------------------- producer --
       if (lane == 0) {
-        constexpr uint32_t kTxS = 8 * BT * 4 + BW * 4;
-        constexpr uint32_t kTxB = (BT + 2 * BW) * 128;
+        constexpr uint32_t kTxS = 8 * BT * 4 + BW * 4 + (kQ4 ? 8 * BT * 4 + 8 * BW * 4 : 0);
+        constexpr uint32_t kTxB = (BT + (kQ4 ? 1 : 2) * BW) * 128;
         int gs = 0, gk = 0;  // scale / operand stages issued so far
         bool ok = true;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
@@ -245,10 +281,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = mbar_wait_bounded(&bars->s_empty[slot], ((gs / SS) & 1) ^ 1, abort_flag,
                                            status, kSiteSEmpty)))
                 break;
-              uint8_t* st = smem + kRingS + slot * kScStage;
+              uint8_t* st = smem + L::kRingS + slot * L::kScStage;
               mbar_arrive_expect_tx(&bars->s_full[slot], kTxS);
-              tma_load_2d(st + kScDa, &tmDa, &bars->s_full[slot], n0, 8 * sb);
-              tma_load_2d(st + kScD, &tmD, &bars->s_full[slot], m0, sb);
+              tma_load_2d(st + L::kScDa, &tmDa, &bars->s_full[slot], n0, 8 * sb);
+              tma_load_2d(st + L::kScD, &tmD, &bars->s_full[slot], m0, sb);
+              if (kQ4) {
+                tma_load_2d(st + L::kScUs, &tmUs, &bars->s_full[slot], n0, 8 * sb);
+                tma_load_2d(st + L::kScMv, &tmMv, &bars->s_full[slot], m0, 8 * sb);
+              }
               ++gs;
             }
             for (int h = 0; h < 4; ++h) {
@@ -256,11 +296,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = mbar_wait_bounded(&bars->b_empty[slot], ((gk / SB) & 1) ^ 1, abort_flag,
                                            status, kSiteBEmpty)))
                 break;
-              uint8_t* bt = smem + slot * kOpStage;
+              uint8_t* bt = smem + slot * L::kOpStage;
               mbar_arrive_expect_tx(&bars->b_full[slot], kTxB);
-              tma_load_2d(bt + kOpX, &tmX, &bars->b_full[slot], kb * KB, n0);
-              tma_load_2d(bt + kOpWhi, &tmWhi, &bars->b_full[slot], kb * KB, m0);
-              tma_load_2d(bt + kOpWlo, &tmWlo, &bars->b_full[slot], kb * KB, m0);
+              tma_load_2d(bt + L::kOpX, &tmX, &bars->b_full[slot], kb * KB, n0);
+              tma_load_2d(bt + L::kOpWhi, &tmWhi, &bars->b_full[slot], kb * KB, m0);
+              if (!kQ4) tma_load_2d(bt + L::kOpWlo, &tmWlo, &bars->b_full[slot], kb * KB, m0);
               ++gk;
             }
           }
@@ -312,10 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0 && ok) {
               // descriptors of the stage's three tiles; a K step of 16
               // elements (32 bytes) adds 2 to the start-address field
-              const uint8_t* bt = smem + slot * kOpStage;
-              const uint32_t xdesc = sw128_desc_lo(smem_u32(bt + kOpX));
-              const uint32_t hdesc = sw128_desc_lo(smem_u32(bt + kOpWhi));
-              const uint32_t ldesc = sw128_desc_lo(smem_u32(bt + kOpWlo));
+              const uint8_t* bt = smem + slot * L::kOpStage;
+              const uint32_t xdesc = sw128_desc_lo(smem_u32(bt + L::kOpX));
+              const uint32_t hdesc = sw128_desc_lo(smem_u32(bt + L::kOpWhi));
+              const uint32_t ldesc = sw128_desc_lo(smem_u32(bt + L::kOpWlo));
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
                 const uint32_t d_tmem = tmem + (uint32_t)((2 * me + q) * kBufCols);
@@ -323,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h < 2; ++h) {
                   const uint32_t koff = (uint32_t)((2 * q + h) * 2);  // sub-block within the stage
                   umma_f16(d_tmem, xdesc + koff, hdesc + koff, idesc, (uint32_t)h);
-                  umma_f16(d_tmem, xdesc + koff, ldesc + koff, idesc, 1u);
+                  if (!kQ4) umma_f16(d_tmem, xdesc + koff, ldesc + koff, idesc, 1u);
                 }
               }
               // the epilogue frees the operand stage when it sees this commit
@@ -372,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && !mbar_wait_warp(&bars->s_full[slot], (gs / SS) & 1, abort_flag, status,
                                   kSiteSFull))
           ok = false;
-        const uint8_t* st = smem + kRingS + slot * kScStage;
-        const float* sda = reinterpret_cast<const float*>(st + kScDa) + tok;
+        const uint8_t* st = smem + L::kRingS + slot * L::kScStage;
+        const float* sda = reinterpret_cast<const float*>(st + L::kScDa) + tok;
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
           // Operand stage 4s + pp: its two chunks sit in TMEM slot pp % 2 (a
@@ -414,12 +454,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // Y += d * Sb for this super-block
-        const float4* dv = reinterpret_cast<const float4*>(st + kScD) + 16 * colh;
+        const float4* dv = reinterpret_cast<const float4*>(st + L::kScD) + 16 * colh;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float4 d4 = dv[j];
           acc[2 * j] = __ffma2_rn(make_float2(d4.x, d4.y), sb[2 * j], acc[2 * j]);
           acc[2 * j + 1] = __ffma2_rn(make_float2(d4.z, d4.w), sb[2 * j + 1], acc[2 * j + 1]);
+        }
+        if (kQ4) {
+          // q4_K: the super-block's min terms, Y -= (da * S) * (dmin * m) per
+          // chunk, S the token's block sum (here, where Sb is no longer live)
+#pragma unroll 1
+          for (int cc = 0; cc < 8; ++cc) {
+            const float nu = -reinterpret_cast<const float*>(st + L::kScUs)[cc * BT + tok];
+            const float4* mv =
+                reinterpret_cast<const float4*>(st + L::kScMv + cc * BW * 4) + 16 * colh;
+            min_term(acc, nu, mv);
+            min_term(acc + 16, nu, mv + 8);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_empty[slot]);
@@ -471,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int g_num_sms[64] = {0};
 
-template <bool P>
+template <int F, bool P>
 cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                        const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
   int dev = 0;
@@ -487,16 +539,21 @@ cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ld
         Y, ldy, M, N, p.Tw, y_vec4);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  mmq_tc_kernel<P><<<p.grid, kThreads, kSmemBytes, s>>>(maps.x, maps.whi, maps.wlo, maps.da, maps.d,
-                                                       M, K, N, p.Tw, p.U, Y, ldy, y_vec4,
-                                                       dbg.out, dbg.stride, dbg.mul, dbg.add,
-                                                       dbg.write_y, status);
+  mmq_tc_kernel<F, P><<<p.grid, kThreads, smem_bytes<F>(), s>>>(
+      maps.x, maps.whi, maps.wlo, maps.da, maps.d, maps.us, maps.mv, M, K, N, p.Tw, p.U, Y, ldy,
+      y_vec4, dbg.out, dbg.stride, dbg.mul, dbg.add, dbg.write_y, status);
   return cudaGetLastError();
+}
+
+template <int F, bool P>
+cudaError_t raise_smem() {
+  return cudaFuncSetAttribute(mmq_tc_kernel<F, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem_bytes<F>());
 }
 
 }  // namespace
 
-size_t mmq_tc_smem_bytes() { return kSmemBytes; }
+size_t mmq_tc_smem_bytes() { return smem_bytes<kFmtQ6>(); }
 
 // Grid and work units for an M x K x N GEMM on `sms` SMs: one persistent CTA
 // per SM walks the units; the last round of tiles is split in two along K
@@ -517,19 +574,25 @@ TcPlan mmq_tc_plan(int M, int K, int N, int sms) {
   return p;
 }
 
-// Raises the dynamic shared-memory limit of both instantiations; once per device.
+// Raises the dynamic shared-memory limit of every instantiation; once per device.
 cudaError_t mmq_tc_prepare() {
-  cudaError_t e = cudaFuncSetAttribute(mmq_tc_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(mmq_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kSmemBytes);
+  cudaError_t e;
+  if ((e = raise_smem<kFmtQ6, false>()) || (e = raise_smem<kFmtQ6, true>()) ||
+      (e = raise_smem<kFmtQ4, false>()))
+    return e;
+  return raise_smem<kFmtQ4, true>();
 }
 
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                           const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
-  return dbg.out ? launch_one<true>(maps, M, K, N, Y, ldy, dbg, status, s)
-                 : launch_one<false>(maps, M, K, N, Y, ldy, dbg, status, s);
+  return dbg.out ? launch_one<kFmtQ6, true>(maps, M, K, N, Y, ldy, dbg, status, s)
+                 : launch_one<kFmtQ6, false>(maps, M, K, N, Y, ldy, dbg, status, s);
+}
+
+cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
+                              const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
+  return dbg.out ? launch_one<kFmtQ4, true>(maps, M, K, N, Y, ldy, dbg, status, s)
+                 : launch_one<kFmtQ4, false>(maps, M, K, N, Y, ldy, dbg, status, s);
 }
 
 }  // namespace q6

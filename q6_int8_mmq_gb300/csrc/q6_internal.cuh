@@ -40,10 +40,35 @@ inline PlaneGeom plane_geom(int M, int K) {
   return g;
 }
 
+// Packed q4_K plane geometry (q4k.cu; all offsets 256-byte aligned).
+struct Q4Geom {
+  size_t qs_off, sc_off, mn_off, dt_off, mv_off, total;
+  int ldm;  // row stride (elements) of the transposed sub-planes: M rounded up to 4
+};
+inline Q4Geom q4_geom(int M, int K) {
+  Q4Geom g;
+  const size_t m = (size_t)M, k = (size_t)K;
+  g.ldm = (M + 3) / 4 * 4;
+  g.qs_off = 0;
+  g.sc_off = round_up(m * (k / 2), 256);
+  g.mn_off = g.sc_off + round_up(m * (k / 32), 256);
+  g.dt_off = g.mn_off + round_up(m * (k / 32), 256);
+  g.mv_off = g.dt_off + round_up((k / 256) * (size_t)g.ldm * 4, 256);
+  g.total = g.mv_off + round_up((k / 32) * (size_t)g.ldm * 4, 256);
+  return g;
+}
+
 // --------------------------------------------------------- kernel launches ---
 // Each returns cudaGetLastError() of its launch.
+// us (nullable) [K/32][ldda] receives da * (sum of the block's codes), the
+// activation block sum the q4_K min term needs.
 cudaError_t launch_quantize(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, int ldda,
-                            __half* Xh, cudaStream_t s);
+                            __half* Xh, float* us, cudaStream_t s);
+cudaError_t launch_q4k_pack(const uint8_t* raw, int M, int K, uint8_t* plane, cudaStream_t s);
+// The binary16 operand plane [M][K] of a packed q4_K plane: sc * q, or q alone
+// when unit (the debug partials).
+cudaError_t launch_q4k_expand(const uint8_t* plane, int M, int K, bool unit, __half* wq,
+                              cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* raw, int M, int K, uint8_t* plane, int8_t* wexp,
                         cudaStream_t s);
 // Debug outputs of the GEMM kernels (both optional, int32, token-major):
@@ -82,6 +107,8 @@ struct TcMaps {
   CUtensorMap wlo;  // W_lo [M][K] f16, box {64, 128}, 128B swizzle
   CUtensorMap da;   // da   [K/32][ldda] f32, box {128, 8}
   CUtensorMap d;    // d^T  [K/256][ldm] f32, box {128, 1}
+  CUtensorMap us;   // q4_K: da * S [K/32][ldda] f32, box {128, 8}
+  CUtensorMap mv;   // q4_K: (dmin * m)^T [K/32][ldm] f32, box {128, 8}
 };
 // What one tensor-core GEMM launch writes besides (or instead of) Y: the
 // exact integer of each (token, weight row, 32-element chunk c) accumulator
@@ -97,6 +124,14 @@ struct TcDebugOut {
 };
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                           const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
+// The q4_K form of the same GEMM (one operand plane, sc * q, in maps.whi; the
+// min term from maps.us and maps.mv).
+cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
+                              const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
+// Tensor maps of a q4_K GEMM call (api.cu): Xh, the operand plane wq [M][K],
+// da and us [K/32][ldda], and the packed q4_K plane's dT and mvT sub-planes.
+int encode_tc_maps_q4k(TcMaps* maps, const uint8_t* q4plane, const void* wq, const void* Xh,
+                       const float* da, const float* us, int M, int K, int N);
 // Tensor maps of one tensor-core GEMM call (api.cu): Xh [N][K], the operand
 // planes W_hi at wop and W_lo at wop + M*K, da [K/32][ldda], and the
 // transposed d sub-plane of the packed plane. Allocates nothing.

@@ -11,6 +11,10 @@
 // per element, falling back to the division next to rounding ties (qfast).
 //
 // HBM-bound: 4 bytes read and 3 written per element (plus 4 per 32 for da).
+// Optionally (kSums) it also writes us = da * S per block, S the sum of the
+// block's 32 codes (exact), the activation side of the q4_K min term
+// ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2: the prepass packs
+// the scale with the block sum).
 #include "q6_quant.cuh"
 
 namespace q6 {
@@ -20,10 +24,12 @@ namespace {
 // (two float4 loads issued together); four threads form one 32-element block
 // and reduce amax with two xor-shuffles. K % 256 == 0 makes the group count a
 // multiple of 32, so whole warps stay active.
+template <bool kSums>
 __global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restrict__ X, int N, int K,
                                                            int ldx, int8_t* __restrict__ Xq,
                                                            float* __restrict__ da, int ldda,
-                                                           __half* __restrict__ Xh) {
+                                                           __half* __restrict__ Xh,
+                                                           float* __restrict__ us) {
   const long long per_row = K >> 3;  // eight-element groups per row
   const long long total = (long long)N * per_row;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -39,10 +45,20 @@ __global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restri
     const float d = __fdiv_rn(a, 127.0f);
     uint2 q8;
     uint4 h8;
-    quant8(v0, v1, d, recip_or_zero(d), q8, h8);
+    float sum = 0.0f;
+    if (kSums) {
+      quant8_sum(v0, v1, d, recip_or_zero(d), q8, h8, sum);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    } else {
+      quant8(v0, v1, d, recip_or_zero(d), q8, h8);
+    }
     if (Xq != nullptr) reinterpret_cast<uint2*>(Xq + (size_t)n * K)[j] = q8;
     if (Xh != nullptr) reinterpret_cast<uint4*>(Xh + (size_t)n * K)[j] = h8;
-    if ((j & 3) == 0) da[(size_t)(j >> 2) * ldda + n] = d;
+    if ((j & 3) == 0) {
+      da[(size_t)(j >> 2) * ldda + n] = d;
+      if (kSums) us[(size_t)(j >> 2) * ldda + n] = d * sum;
+    }
   }
 }
 
@@ -51,10 +67,12 @@ __global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restri
 // with one xor-shuffle. Warps walk the rows' 16-element groups in lockstep
 // (a lane past the end idles through the shuffle), so the shuffle always has
 // the whole warp.
+template <bool kSums>
 __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restrict__ X, int N, int K,
                                                           int ldx, int8_t* __restrict__ Xq,
                                                           float* __restrict__ da, int ldda,
-                                                          __half* __restrict__ Xh) {
+                                                          __half* __restrict__ Xh,
+                                                          float* __restrict__ us) {
   const long long per_row = K >> 4;                // sixteen-element groups per row (even)
   const long long total = (long long)N * per_row;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -78,13 +96,24 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
     a = fmaxf(a, fmaxf(fmaxf(fmaxf(fabsf(v2.x), fabsf(v2.y)), fmaxf(fabsf(v2.z), fabsf(v2.w))),
                        fmaxf(fmaxf(fabsf(v3.x), fabsf(v3.y)), fmaxf(fabsf(v3.z), fabsf(v3.w)))));
     a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    if (!on) continue;
     const float d = __fdiv_rn(a, 127.0f);
     const float r = recip_or_zero(d);
     uint2 qa, qb;
     uint4 ha, hb;
-    quant8(v0, v1, d, r, qa, ha);
-    quant8(v2, v3, d, r, qb, hb);
+    float sum = 0.0f;
+    if (kSums) {
+      // every lane runs this (past the end on zeros), so the shuffle has the warp
+      float s0, s1;
+      quant8_sum(v0, v1, d, r, qa, ha, s0);
+      quant8_sum(v2, v3, d, r, qb, hb, s1);
+      sum = s0 + s1;
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    }
+    if (!on) continue;
+    if (!kSums) {
+      quant8(v0, v1, d, r, qa, ha);
+      quant8(v2, v3, d, r, qb, hb);
+    }
     if (Xq != nullptr)
       reinterpret_cast<uint4*>(Xq + (size_t)n * K)[j] = make_uint4(qa.x, qa.y, qb.x, qb.y);
     if (Xh != nullptr) {
@@ -92,7 +121,10 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
       h[0] = ha;
       h[1] = hb;
     }
-    if ((j & 1) == 0) da[(size_t)(j >> 1) * ldda + n] = d;
+    if ((j & 1) == 0) {
+      da[(size_t)(j >> 1) * ldda + n] = d;
+      if (kSums) us[(size_t)(j >> 1) * ldda + n] = d * sum;
+    }
   }
 }
 
@@ -103,18 +135,25 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
 // which measured fastest; a few tokens take the eight-element form, whose
 // shorter per-thread chain and twice the threads finish sooner.
 cudaError_t launch_quantize(const float* X, int N, int K, int ldx, int8_t* Xq, float* da, int ldda,
-                            __half* Xh, cudaStream_t s) {
+                            __half* Xh, float* us, cudaStream_t s) {
   const long long elems = (long long)N * K;
   if (elems < (1LL << 20)) {
     const long long blocks = (elems / 8 + 255) / 256;
-    q8_quantize8_kernel<<<(unsigned)(blocks < 1 ? 1 : blocks), 256, 0, s>>>(X, N, K, ldx, Xq, da,
-                                                                            ldda, Xh);
+    const unsigned grid = (unsigned)(blocks < 1 ? 1 : blocks);
+    if (us)
+      q8_quantize8_kernel<true><<<grid, 256, 0, s>>>(X, N, K, ldx, Xq, da, ldda, Xh, us);
+    else
+      q8_quantize8_kernel<false><<<grid, 256, 0, s>>>(X, N, K, ldx, Xq, da, ldda, Xh, nullptr);
     return cudaGetLastError();
   }
   long long blocks = (elems / 16 + 255) / 256;
   const long long cap = 152LL * 32;
   if (blocks > cap) blocks = cap;
-  q8_quantize_kernel<<<(unsigned)blocks, 256, 0, s>>>(X, N, K, ldx, Xq, da, ldda, Xh);
+  if (us)
+    q8_quantize_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(X, N, K, ldx, Xq, da, ldda, Xh, us);
+  else
+    q8_quantize_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(X, N, K, ldx, Xq, da, ldda, Xh,
+                                                               nullptr);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,179 @@
+"""Parity of the q4_K GEMM with the CPU oracle (needs a GB300).
+
+The q4_K line of the pages ("r18: Load-time B pre-expansion", Sec. 1 and 3.2;
+the two-term rescale of "r38 -- q6_K BT-style raw-byte mma kernel", Sec.
+2.2). Integer results (the packed plane, the activation block sums, the debug
+partials P = sum over a 32-element sub-block of q * xq) must be bit-exact; Y
+must satisfy max|Y - Yo| <= 1e-3 * max|Yo| and sum|Y - Yo| / sum|Yo| <= 1e-5,
+as for q6_K.
+"""
+import numpy as np
+import pytest
+
+from q6_int8_mmq_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+MAX_REL = 1e-3
+NORMWISE = 1e-5
+
+
+@pytest.fixture(scope="module")
+def q6():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import q6_int8_mmq_gb300 as q6mod
+    from q6_int8_mmq_gb300 import build as q6build
+    q6build.build()
+    q6mod.load()
+    return q6mod
+
+
+def dev(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def check_y(Y, Yo, label=""):
+    Y = np.asarray(Y, dtype=np.float64)
+    err = np.abs(Y - Yo)
+    scale = np.abs(Yo).max()
+    assert np.all(np.isfinite(Y)), label
+    if scale == 0:
+        assert err.max() == 0, label
+        return
+    assert err.max() / scale <= MAX_REL, f"{label}: max error {err.max() / scale:.3e}"
+    assert err.sum() / np.abs(Yo).sum() <= NORMWISE, f"{label}: normwise error"
+
+
+def quantize(q6, orc, X):
+    """GPU activations with block sums, checked bit-exactly against the oracle's
+    codes and scales; us against da * S rounded to f32 once."""
+    act = q6.quantize_act(dev(X), want_us=True)
+    q6.sync_status()
+    xq_o, da_o = orc.quantize(X)
+    N = X.shape[0]
+    assert np.array_equal(host(act.xq), xq_o)
+    assert np.array_equal(host(act.da)[:, :N].T, da_o)
+    S = xq_o.astype(np.int64).reshape(N, -1, 32).sum(-1).astype(np.float32)
+    assert np.array_equal(host(act.us)[:, :N].T, da_o * S)
+    return act, xq_o, da_o
+
+
+@pytest.mark.parametrize("N,K", [(3, 256), (700, 1024), (77, 11008)])
+def test_quantize_block_sums(q6, orc, N, K):
+    X = synth.activations(0x51361001 + N, N, K, outlier_frac=0.01)
+    X[0, 32:64] = 0.0
+    quantize(q6, orc, X)
+
+
+@pytest.mark.parametrize("M,K", [(64, 256), (131, 768), (300, 1024)])
+def test_q4k_pack_bitexact(q6, orc, M, K):
+    raw = synth.q4k_raw_weights(0x51361101 + M, M, K)
+    w = q6.q4k_pack_weights(dev(raw), M, K, wq=True)
+    q6.sync_status()
+    plane = host(w.plane)
+    r = lambda x: (x + 255) // 256 * 256
+    ldm = (M + 3) // 4 * 4
+    nsb, nc = K // 256, K // 32
+    o_sc = r(M * K // 2)
+    o_mn = o_sc + r(M * nc)
+    o_dt = o_mn + r(M * nc)
+    o_mv = o_dt + r(nsb * ldm * 4)
+    assert plane.size == o_mv + r(nc * ldm * 4)
+    for a, b in ((M * K // 2, o_sc), (o_sc + M * nc, o_mn), (o_mn + M * nc, o_dt),
+                 (o_dt + nsb * ldm * 4, o_mv), (o_mv + nc * ldm * 4, plane.size)):
+        assert np.all(plane[a:b] == 0)
+    blocks = raw.reshape(M, nsb, 144)
+    assert np.array_equal(plane[:M * K // 2].reshape(M, nsb, 128), blocks[:, :, 16:])
+    dec = [[orc.q4k_decode_block(blocks[m, b]) for b in range(nsb)] for m in range(M)]
+    sc = np.array([[dec[m][b][1] for b in range(nsb)] for m in range(M)]).reshape(M, nc)
+    mn = np.array([[dec[m][b][2] for b in range(nsb)] for m in range(M)]).reshape(M, nc)
+    d = np.array([[dec[m][b][3] for b in range(nsb)] for m in range(M)])
+    dmin = np.array([[dec[m][b][4] for b in range(nsb)] for m in range(M)])
+    assert np.array_equal(plane[o_sc:o_sc + M * nc].reshape(M, nc), sc)
+    assert np.array_equal(plane[o_mn:o_mn + M * nc].reshape(M, nc), mn)
+    dt = plane[o_dt:o_dt + nsb * ldm * 4].view(np.float32).reshape(nsb, ldm)
+    assert np.array_equal(dt[:, :M].astype(np.float64), d.T) and np.all(dt[:, M:] == 0)
+    mv = plane[o_mv:o_mv + nc * ldm * 4].view(np.float32).reshape(nc, ldm)
+    assert np.array_equal(mv[:, :M].astype(np.float64), (np.repeat(dmin, 8, axis=1) * mn).T)
+    assert np.all(mv[:, M:] == 0)
+    codes = np.stack([np.concatenate([dec[m][b][0] for b in range(nsb)]) for m in range(M)])
+    assert np.array_equal(host(w.wq).astype(np.int64),
+                          np.repeat(sc, 32, axis=1) * codes.astype(np.int64))
+    assert np.array_equal(host(q6.q4k_unpack_weights(w)), host(w.wq))
+    # the same planes from host memory
+    import torch
+    wh = q6.q4k_pack_weights(torch.from_numpy(raw), M, K, wq=True)
+    assert torch.equal(wh.plane, w.plane) and torch.equal(wh.wq, w.wq)
+
+
+Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 17), (200, 768, 129), (384, 768, 300),
+             (1016, 768, 2555),    # the split last round of tiles, ragged band and tile
+             (3001, 512, 40)]
+
+
+@pytest.mark.parametrize("source", ["raw", "wq"])
+@pytest.mark.parametrize("M,K,N", Q4_SHAPES, ids=lambda v: str(v))
+def test_q4k_mmq_small(q6, orc, M, K, N, source):
+    raw = synth.q4k_raw_weights(0x51361201 + M + N, M, K)
+    X = synth.activations(0x51361202 + M + N, N, K, outlier_frac=0.02)
+    w = q6.q4k_pack_weights(dev(raw), M, K, wq=source == "wq")
+    act, xq_o, da_o = quantize(q6, orc, X)
+    Y, path, P = q6.q4k_mmq(w, act, source=source, partials=True)
+    q6.sync_status()
+    assert path == {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source]
+    want_p = N * M * K // 32 <= 40_000_000
+    if want_p:
+        Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
+        assert np.array_equal(host(P), Po), "sub-block partials differ"
+    else:
+        Yo = orc.q4k_mmq_all(raw, M, K, xq_o, da_o)
+    check_y(host(Y), Yo, f"q4k {M}x{K}x{N} {source}")
+    Y2, _, _ = q6.q4k_mmq(w, act, source=source)
+    q6.sync_status()
+    check_y(host(Y2), Yo, f"q4k {M}x{K}x{N} {source} fast")
+
+
+def test_q4k_degenerate(q6, orc):
+    """All nibbles 0 leave only the min term; dmin = 0 leaves only the scale
+    term; d = dmin = 0 gives Y = 0."""
+    M, K, N = 128, 512, 130
+    X = synth.activations(0x51361301, N, K)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    base = synth.q4k_raw_weights(0x51361302, M, K).reshape(-1, 144)
+    for label, edit in (("nibbles 0", lambda r: r[:, 16:].fill(0)),
+                        ("dmin 0", lambda r: r[:, 2:4].fill(0)),
+                        ("d and dmin 0", lambda r: r[:, 0:4].fill(0))):
+        raw = base.copy()
+        edit(raw)
+        raw = raw.reshape(M, -1)
+        w = q6.q4k_pack_weights(dev(raw), M, K)
+        Y, _, _ = q6.q4k_mmq(w, act)
+        q6.sync_status()
+        Yo = orc.q4k_mmq(raw, M, K, xq_o, da_o)
+        if label == "d and dmin 0":
+            assert np.all(host(Y) == 0.0)
+        check_y(host(Y), Yo, label)
+
+
+def test_q4k_ffn_down_full(q6, orc):
+    """q4_K weights of the ffn_down shape (4096 x 11008) against its 3314-token
+    activation stream: every output within tolerance of the oracle (run over
+    disjoint weight-row ranges on the host cores), from the packed plane and
+    from the resident operand plane."""
+    _, X, cfg = synth.workload("ffn_down")
+    M, K = cfg["M"], cfg["K"]
+    raw = synth.q4k_raw_weights(0x51361401, M, K)
+    w = q6.q4k_pack_weights(dev(raw), M, K, wq=True)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    Yo = orc.q4k_mmq_all(raw, M, K, xq_o, da_o)
+    for source in ("raw", "wq"):
+        Y, _, _ = q6.q4k_mmq(w, act, source=source)
+        q6.sync_status()
+        check_y(host(Y), Yo, f"q4k ffn_down {source}")
