@@ -33,6 +33,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "q6_K MMQ effective int8 TOPS @4096x11008xN3314; % of INT8 TC / HBM peak"
+# the same measure for the q4_K weight format (a secondary workload)
+Q4K_METRIC = "q4_K MMQ effective int8 TOPS @4096x11008xN3314"
 UNIT = "TOPS"
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -140,14 +142,15 @@ def measured_peaks() -> dict:
 
 # ------------------------------------------------------------ CPU oracle ---
 
-def time_oracle(raw, X, M, K, budget_s: float, max_tokens: int):
+def time_oracle(raw, X, M, K, budget_s: float, max_tokens: int, fmt: str = "q6_K"):
     """The oracle, as it stands, on a bounded sample of tokens (all M rows):
     quantise those tokens and compute their outputs. Returns (ops, seconds, tokens)."""
     import oracle
     orc = oracle.get()
+    gemm = orc.q4k_mmq if fmt == "q4_K" else orc.mmq
     xq, da = orc.quantize(X[:1])
     t0 = time.perf_counter()
-    orc.mmq(raw, M, K, xq, da)
+    gemm(raw, M, K, xq, da)
     one = time.perf_counter() - t0
     # a one-token call streams every weight row once per token, so it is
     # slower per token than a larger sample; size the sample from a first
@@ -156,7 +159,7 @@ def time_oracle(raw, X, M, K, budget_s: float, max_tokens: int):
     while True:
         t0 = time.perf_counter()
         xq, da = orc.quantize(X[:ntok])
-        orc.mmq(raw, M, K, xq, da)
+        gemm(raw, M, K, xq, da)
         dt = time.perf_counter() - t0
         grow = int(min(max_tokens, ntok * budget_s / max(dt, 1e-6)))
         if dt >= 0.5 * budget_s or grow <= ntok or ntok == max_tokens:
@@ -175,11 +178,13 @@ def run_reference(args):
     raw, X, cfg, config = workload_inputs(args, synth)
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     orc = oracle.get()
+    q4 = args.workload == "q4k_ffn_down"
+    gemm = orc.q4k_mmq if q4 else orc.mmq
     # size one step (one token against `rows` weight rows) so the run takes ~1-2 min
     probe_rows = 256
     xq, da = orc.quantize(X[:1])
     t0 = time.perf_counter()
-    orc.mmq(raw[:probe_rows], probe_rows, K, xq, da)
+    gemm(raw[:probe_rows], probe_rows, K, xq, da)
     per_row = (time.perf_counter() - t0) / probe_rows
     total_steps = args.steps + args.warmup
     rows = int(min(M, max(1, 90.0 / max(total_steps, 1) / max(per_row, 1e-9))))
@@ -188,7 +193,7 @@ def run_reference(args):
         n = i % N
         t0 = time.perf_counter()
         xq, da = orc.quantize(X[n:n + 1])
-        orc.mmq(raw[:rows], rows, K, xq, da)
+        gemm(raw[:rows], rows, K, xq, da)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     t = sum(times)
@@ -196,7 +201,7 @@ def run_reference(args):
     value = ops / t / 1e12
     sample = f"{len(times)} steps of 1 token x {rows} of {M} weight rows, K={K}"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": Q4K_METRIC if q4 else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(len(times), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config,
@@ -224,6 +229,21 @@ def workload_config(args, cfg):
                                      "copies of every input used in turn",
                    "pages_attn_v": "inputs larger than L2 (48 MB f32 activation, 2 copies)"}.get(
                 args.workload, "2 copies of every input used in turn (attn_v inputs fit in L2)"),
+            "parallelism": "replicas"}
+
+
+def q4k_config(args, cfg):
+    return {"workload": f"q4_K GEMM (ffn_down shape and activations) M={cfg['M']} "
+                        f"K={cfg['K']} N={cfg['N']}",
+            "M": cfg["M"], "K": cfg["K"], "N": cfg["N"],
+            "weights": ("resident binary16 operand plane (sc * q)" if args.weights == "wh" else
+                        "packed q4_K plane, unpacked to the binary16 operand plane per step"),
+            "step": ("q8_quantize_act with block sums + q4k_mmq on the resident plane"
+                     if args.weights == "wh" else
+                     "q8_quantize_act with block sums and q4k_unpack_weights on two streams "
+                     "at once, then q4k_mmq on the unpacked plane (weights packed once)"),
+            "l2": "inputs larger than L2 (146 MB f32 activation per step); 2 copies of every "
+                  "input used in turn",
             "parallelism": "replicas"}
 
 
@@ -256,6 +276,9 @@ def workload_inputs(args, synth):
         _, raw = synth.sweep_layer(0)
         _, X = synth.sweep_activations()
         return raw, X, dict(M=4096, K=11008, N=synth.SWEEP_N), sweep_config(synth)
+    if args.workload == "q4k_ffn_down":
+        raw, X, cfg = synth.q4k_workload("ffn_down")
+        return raw, X, cfg, q4k_config(args, cfg)
     raw, X, cfg = synth.workload(args.workload)
     return raw, X, cfg, workload_config(args, cfg)
 
@@ -473,7 +496,8 @@ def run_ours(args):
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
     hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    run = {"skinny": run_skinny, "sweep": run_sweep}.get(args.workload, run_gemm)
+    run = {"skinny": run_skinny, "sweep": run_sweep, "q4k_ffn_down": run_q4k}.get(
+        args.workload, run_gemm)
     run(args, q6, synth, device, rank, world, peaks, hbm, hbm_src)
 
 
@@ -505,8 +529,8 @@ def gemm_method_bytes(M, K, N):
     return M * K * 210 / 256 + N * K + N * (K // 32) * 4 + 4 * N * M
 
 
-def oracle_baseline(raw, X, M, K, budget, N):
-    ops, secs, ntok = time_oracle(raw, X, M, K, budget, N)
+def oracle_baseline(raw, X, M, K, budget, N, fmt: str = "q6_K"):
+    ops, secs, ntok = time_oracle(raw, X, M, K, budget, N, fmt)
     return {"value": ops / secs / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{ntok} of {N} tokens x all {M} weight rows (quantise + GEMM), "
                       f"{secs:.1f} s single-threaded"}
@@ -713,6 +737,148 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     print(json.dumps(line), flush=True)
 
 
+def q4k_method_bytes(M, K, N):
+    """The method's own bytes of one q4_K GEMM: the weights at 144 B per 256,
+    the int8 activations, their per-32 f32 scales and block sums, the f32 Y."""
+    return M * K * 144 / 256 + N * K + 2 * N * (K // 32) * 4 + 4 * N * M
+
+
+def run_q4k(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
+    """The q4_K GEMM at the ffn_down shape: one step = quantise the step's f32
+    activation with block sums and (from the packed plane) unpack the weights
+    on a second stream, then q4k_mmq on the operand plane."""
+    import torch
+    raw, X, cfg = synth.q4k_workload("ffn_down")
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    resident = args.weights == "wh"
+    R = 2
+    raw_d = torch.from_numpy(raw).to(device)
+    e0, e1 = ev_pair()
+    e0.record()
+    Ws = [q6.q4k_pack_weights(raw_d, M, K, wq=resident) for _ in range(R)]
+    e1.record()
+    torch.cuda.synchronize()
+    pack_ms = e0.elapsed_time(e1) / R
+    del raw_d
+    Xs = [torch.from_numpy(X).to(device) for _ in range(R)]
+    acts = [q6.alloc_activations(N, K, device, want_xq=False, want_us=True) for _ in range(R)]
+    Ys = [torch.empty((N, M), dtype=torch.float32, device=device) for _ in range(R)]
+    # the GEMM reads the operand plane: resident, or unpacked into a buffer per slot
+    Wg = [W if resident else q6.Q4Weights(M, K, W.plane,
+                                          torch.empty((M, K), dtype=torch.float16, device=device))
+          for W in Ws]
+    path = [None]
+    side = torch.cuda.Stream(device)
+    unpacked = [torch.cuda.Event() for _ in range(R)]
+    gemm_done = [torch.cuda.Event() for _ in range(R)]
+    gemm_used = [False] * R
+
+    def step_seq(i, ev=None):
+        j = i % R
+        if ev is not None:
+            ev[0].record()
+        q6.quantize_act(Xs[j], out=acts[j])
+        if ev is not None:
+            ev[1].record()
+        if not resident:
+            q6.q4k_unpack_weights(Ws[j], out=Wg[j].wq)
+        if ev is not None:
+            ev[2].record()
+        _, path[0], _ = q6.q4k_mmq(Wg[j], acts[j], Y=Ys[j], source="wq")
+        if ev is not None:
+            ev[3].record()
+
+    def step(i, ev=None):
+        j = i % R
+        cur = torch.cuda.current_stream(device)
+        if not resident:
+            if i == 0:
+                side.wait_stream(cur)
+            if gemm_used[j]:
+                side.wait_event(gemm_done[j])
+            with torch.cuda.stream(side):
+                q6.q4k_unpack_weights(Ws[j], out=Wg[j].wq)
+                unpacked[j].record(side)
+        q6.quantize_act(Xs[j], out=acts[j])
+        if not resident:
+            cur.wait_event(unpacked[j])
+        _, path[0], _ = q6.q4k_mmq(Wg[j], acts[j], Y=Ys[j], source="wq")
+        gemm_done[j].record(cur)
+        gemm_used[j] = True
+
+    for i in range(args.warmup):
+        step(i)
+    q6.sync_status()
+    max_ms, clk = timed_region(step, args.steps, device, rank == 0)
+    q6.sync_status()
+    q_ms, u_ms, m_ms = kernel_ms(step_seq, max(20, min(args.steps, 200)), 4)
+    q6.sync_status()
+    ops_per_step = 2.0 * M * N * K
+    value = job_throughput(ops_per_step * args.steps, world, max_ms / 1e3) / 1e12
+    e2e = None
+    if args.e2e_steps > 0:
+        Xh = torch.from_numpy(X).pin_memory()
+        Yh = [torch.empty((N, M), dtype=torch.float32).pin_memory() for _ in range(R)]
+        e_ms = e2e_run_overlapped(step_seq, [[(Xs[j], Xh)] for j in range(R)],
+                                  [[(Yh[j], Ys[j])] for j in range(R)], args.e2e_steps, device)
+        q6.sync_status()
+        e2e = {"value": job_throughput(ops_per_step * args.e2e_steps, world, e_ms / 1e3) / 1e12,
+               "unit": UNIT, "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": N * M * 4,
+               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
+               "copies": OVERLAP}
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        cpu = oracle_baseline(raw, X, M, K, args.cpu_budget, N, fmt="q4_K")
+    if rank != 0:
+        return
+    peak_t, peak_src = tensor_peak(peaks)
+    peak_s, _ = tensor_peak(peaks, sustained=True)
+    tflops = ops_per_step / m_ms / 1e9
+    # quantiser: reads f32 X, writes Xh (2 B) and per-32 da and us; unpack:
+    # reads the nibbles (0.5 B) and sc (1/32 B), writes the operand plane (2 B)
+    q_bytes = N * K * (4 + 2) + 2 * (K // 32) * N * 4
+    u_bytes = M * K * (0.5 + 1 / 32 + 2)
+    traffic = args.traffic if args.traffic is not None else TRAFFIC.get(
+        ("q4k_ffn_down", "mmq_tc_q4k"))
+    line = {
+        "metric": Q4K_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xf16->f32 (exact int10 x int8)", "data": "synthetic",
+        "config": q4k_config(args, cfg),
+        "roofline": {"bound": "tensor", "kernel": "mmq_tc_kernel<q4_K> (q4k_mmq on the operand "
+                                                  "plane)",
+                     "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": tflops / peak_t, "peak_source": peak_src,
+                     "timing": "the GEMM kernel alone, CUDA events on its stream, averaged over "
+                               "short back-to-back steps (so the burst peak applies)",
+                     "frac_of_sustained": tflops / peak_s, "traffic": traffic,
+                     "traffic_source": ("dram__bytes_read.sum + dram__bytes_write.sum of one ncu "
+                                        "capture of this kernel on this workload"
+                                        if traffic is not None else "not captured for this "
+                                        "kernel version"),
+                     "algorithmic_bytes": q4k_method_bytes(M, K, N),
+                     "algorithmic_bytes_formula": "M*K*144/256 + N*K + 2*4*N*K/32 + 4*N*M",
+                     "algorithmic": f"2*M*N*K = {ops_per_step:.4g} flop per launch"},
+        "cpu_baseline": cpu, "e2e": e2e,
+        # quantiser, unpack, and the GEMM's launches (the tile plan does not
+        # depend on the weight format; N is past the few-token paths)
+        "gpu_launches": (1 + (0 if resident else 1) + q6.mmq_launches(M, K, N, True))
+                        * args.steps,
+        "clocks": clk, "clocks_ok": clocks_ok(clk),
+        "kernels": {
+            "q4k_mmq": {"ms": m_ms, "tflops": tflops, "path": path[0]},
+            "q8_quantize_act_sums": {"ms": q_ms, "gbs": q_bytes / q_ms / 1e6,
+                                     "frac_hbm": q_bytes / q_ms / 1e6 / hbm},
+            "q4k_unpack_weights": ({"ms": u_ms, "gbs": u_bytes / u_ms / 1e6,
+                                    "frac_hbm": u_bytes / u_ms / 1e6 / hbm}
+                                   if not resident else None),
+        },
+        "hbm_peak": {"gbs": hbm, "source": hbm_src}, "pack_ms": pack_ms,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def other_configs(args, q6, synth, device, hbm):
     """Short measurements of the other workloads beside the headline one: the
     attn_v GEMM (q6k_mmq, raw plane and resident operand plane), the skinny
@@ -805,9 +971,8 @@ def q4k_gemm(q6, synth, device):
     packed plane (unpack + GEMM) and the quantiser with block sums, each
     averaged over back-to-back calls."""
     import torch
-    _, X, cfg = synth.workload("ffn_down")
+    raw, X, cfg = synth.q4k_workload("ffn_down")
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
-    raw = synth.q4k_raw_weights(0x51361401, M, K)
     W = q6.q4k_pack_weights(torch.from_numpy(raw).to(device), M, K, wq=True)
     Xd = torch.from_numpy(X).to(device)
     act = q6.alloc_activations(N, K, device, want_xq=False, want_us=True)
@@ -1149,7 +1314,7 @@ SKINNY_FUSED_MAX_N = 2
 
 # DRAM bytes per launch from ncu captures of the current kernels, keyed by
 # (workload, kernel). An entry is removed when its kernel changes.
-TRAFFIC = {("ffn_down", "mmq_tc"): 667.67e6 + 53.16e6,
+TRAFFIC = {("ffn_down", "mmq_tc"): 667.85e6 + 54.70e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
            ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
@@ -1166,7 +1331,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_down",
                     choices=["ffn_down", "attn_v", "pages_ffn_down", "pages_attn_v", "skinny",
-                             "sweep"])
+                             "sweep", "q4k_ffn_down"])
     ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
     ap.add_argument("--tokens", type=int, default=1, choices=range(1, 17), metavar="{1..16}",
                     help="tokens of the skinny workload")

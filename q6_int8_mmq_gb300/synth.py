@@ -184,6 +184,16 @@ def workload(name: str):
     return raw, x, dict(cfg)
 
 
+Q4K_SEED = 0x51361401
+
+
+def q4k_workload(name: str = "ffn_down"):
+    """(raw q4_K weights, f32 activations, shape dict): the named workload's
+    shape and activation stream with q4_K weights in place of q6_K."""
+    _, x, cfg = workload(name)
+    return q4k_raw_weights(Q4K_SEED, cfg["M"], cfg["K"]), x, cfg
+
+
 def skinny_workload(weight: str, n: int):
     M, K = SKINNY_SHAPES[weight]
     seed = WORKLOAD_SEED["skinny"] + (0x100 if weight == "attn_v" else 0)
