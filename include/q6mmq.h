@@ -111,12 +111,22 @@ int q8_act_plane_bytes(int N, int K, size_t *xq_bytes, size_t *da_bytes,
 int q8_quantize_act(const float *X, int N, int K, int ldx, int8_t *Xq, float *da,
                     uint16_t *Xh, q6_stream_t s);
 
-/* The same, and also the activation block sums the q4_K GEMM needs
- * ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2: q4_K's rescale has
- * a second term with the activation block's sum):
- *   us : device f32 [K/32][ldda] (required, 16-byte aligned, layout of da),
- *        us[c * ldda + n] = da[c][n] * (sum of token n's 32 codes of block c),
- *        the product rounded to f32 once. */
+/* Size in bytes of the block-sum pairs us of an N x K activation (below),
+ * and their row length ldus = 32 * ceil(K / 512) f32 values. Either output
+ * may be NULL. Q6_EINVAL if N < 0, K <= 0 or K % 256. */
+int q8_act_sums_bytes(int N, int K, size_t *us_bytes, int *ldus);
+
+/* The same as q8_quantize_act, and also the activation block sums the q4_K
+ * GEMM needs ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2: q4_K's
+ * rescale has a second term with the activation block's sum), laid out as
+ * the operand of the GEMM's min-term MMAs (kind::tf32):
+ *   us : device f32 [N][ldus] (required, 16-byte aligned). For token n and
+ *        block c (super-block b = c / 8, i = c % 8), the value
+ *        v = da[c][n] * (sum of token n's 32 codes of block c), rounded to
+ *        f32 once, is stored as the pair hi = v with its low 13 mantissa bits
+ *        cleared, at us[n][16 b + i], and lo = v - hi (exact), at
+ *        us[n][16 b + 8 + i]: hi + lo == v. An odd K/256 leaves the row's
+ *        last 16 values zero. */
 int q8_quantize_act_sums(const float *X, int N, int K, int ldx, int8_t *Xq, float *da,
                          uint16_t *Xh, float *us, q6_stream_t s);
 
@@ -328,8 +338,10 @@ int q6k_mmq_f32(const void *plane, int M, int K, const float *X, int ldx, int N,
  * plane (device, 256-byte aligned, q4k_plane_bytes() bytes), sub-planes at
  *      256-byte aligned offsets: qs uint8 [M][K/2] (the nibble bytes as they
  *      are), sc uint8 [M][K/32], m uint8 [M][K/32] (decoded), dT f32
- *      [K/256][ldm] (d, transposed, ldm = M rounded up to 4), mvT f32
- *      [K/32][ldm] (dmin * m, exact, transposed); padding is zero.
+ *      [K/256][ldm] (d, transposed, ldm = M rounded up to 4), mv f32
+ *      [M][ldus] (dmin * m of every sub-block, at most 17 significant bits,
+ *      as the exact pair hi + lo in the layout of the activations' us, see
+ *      q8_quantize_act_sums; ldus = 32 * ceil(K / 512)); padding is zero.
  * wq (device, optional, 16-byte aligned): the binary16 operand plane [M][K]
  *      the tensor-core GEMM reads, sc * q (at most 945: exact).
  * -------------------------------------------------------------------- */
@@ -348,7 +360,10 @@ int q4k_unpack_weights(const void *plane, int M, int K, uint16_t *wq, q6_stream_
  * kernel for q4_K; small N run as one ragged token tile).
  *   plane : the packed q4_K plane (required); wq : resident operand plane or
  *           NULL (then it is unpacked into the workspace first).
- *   Xh, da, us : from q8_quantize_act_sums (binary16 codes, scales, block sums).
+ *   Xh, da, us : from q8_quantize_act_sums (binary16 codes, scales, block-sum
+ *           pairs). The min term sum_c us * (dmin * m) runs on the tensor cores
+ *           as kind::tf32 products of the hi/lo pairs (each product exact in
+ *           f32; us's pair is within 2^-21 |us| of it).
  *   workspace : device, 256-byte aligned, at least 2 * M * K bytes when wq is
  *           NULL or partials is not NULL; contents afterwards unspecified.
  *   partials : NULL, or device int32 [N][M][K/32] that receives every exact

@@ -48,6 +48,7 @@ SIGNATURES = [
     ("q6k_mmq_noalloc_status", _I, [_P]),
     ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _IP, _P]),
     ("q6k_mmq_f32", _I, [_P, _I, _I, _P, _I, _I, _P, _I, _IP, _P]),
+    ("q8_act_sums_bytes", _I, [_I, _I, _SZ, _IP]),
     ("q8_quantize_act_sums", _I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     ("q4k_plane_bytes", _I, [_I, _I, _SZ, _SZ]),
     ("q4k_pack_weights", _I, [_P, _I, _I, _P, _P, _P]),
@@ -145,6 +146,14 @@ def act_plane_bytes(N: int, K: int):
 
 
 @functools.lru_cache(maxsize=256)
+def act_sums_bytes(N: int, K: int):
+    """(us_bytes, ldus) of the block-sum pairs of an N x K activation."""
+    a, ld = ctypes.c_size_t(), ctypes.c_int()
+    _check(load().q8_act_sums_bytes(N, K, ctypes.byref(a), ctypes.byref(ld)))
+    return a.value, ld.value
+
+
+@functools.lru_cache(maxsize=256)
 def plane_bytes(M: int, K: int):
     """(packed plane bytes, W_exp bytes) of an M x K q6_K weight."""
     a, b = ctypes.c_size_t(), ctypes.c_size_t()
@@ -157,9 +166,10 @@ def plane_bytes(M: int, K: int):
 @dataclasses.dataclass(frozen=True)
 class Activations:
     """Quantised activations on the device: xq [N,K] int8, da [K/32, ldda] f32,
-    xh [N,K] f16 (xq or xh may be None), and optionally us [K/32, ldda] f32,
-    da times each 32-block's code sum (the q4_K GEMM's min term needs it).
-    Checked once, when made; read-only."""
+    xh [N,K] f16 (xq or xh may be None), and optionally us [N, ldus] f32, da
+    times each 32-block's code sum as hi/lo pairs (the q4_K GEMM's min term
+    needs it; see q8_quantize_act_sums in the C header). Checked once, when
+    made; read-only."""
     N: int
     K: int
     xq: object
@@ -175,7 +185,7 @@ class Activations:
             raise Q6Error(Q6_EINVAL, f"ldda {self.ldda} does not match {act_plane_bytes(N, K)[3]}")
         _same_device((self.xq, "xq", torch.int8, (N, K)), (self.xh, "xh", torch.float16, (N, K)),
                      (self.da, "da", torch.float32, (K // 32, self.ldda)),
-                     (self.us, "us", torch.float32, (K // 32, self.ldda)))
+                     (self.us, "us", torch.float32, (N, act_sums_bytes(N, K)[1])))
 
     @property
     def device(self):
@@ -193,7 +203,8 @@ def alloc_activations(N: int, K: int, device=None, want_xh: bool = True,
     xq = torch.empty((N, K), dtype=torch.int8, device=dev) if want_xq else None
     da = torch.empty((K // 32, ldda), dtype=torch.float32, device=dev)
     xh = torch.empty((N, K), dtype=torch.float16, device=dev) if want_xh else None
-    us = torch.empty((K // 32, ldda), dtype=torch.float32, device=dev) if want_us else None
+    us = (torch.empty((N, act_sums_bytes(N, K)[1]), dtype=torch.float32, device=dev)
+          if want_us else None)
     return Activations(N, K, xq, da, xh, ldda, us)
 
 

@@ -166,14 +166,15 @@ int encode_tc_maps_q4k(TcMaps* maps, const uint8_t* q4plane, const void* wq, con
                       (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Wq")) ||
       (rc = encode_2d(&maps->da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
                       (uint64_t)ldda_of(N) * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE, "da")) ||
-      (rc = encode_2d(&maps->us, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, us, (uint64_t)N, (uint64_t)K / 32,
-                      (uint64_t)ldda_of(N) * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE, "us")) ||
+      (rc = encode_2d(&maps->us, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, us, (uint64_t)q4_min_ld(K),
+                      (uint64_t)N, (uint64_t)q4_min_ld(K) * 4, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                      "us")) ||
       (rc = encode_2d(&maps->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q4plane + g.dt_off, (uint64_t)M,
                       (uint64_t)K / 256, (uint64_t)g.ldm * 4, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
                       "dT")) ||
-      (rc = encode_2d(&maps->mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q4plane + g.mv_off, (uint64_t)M,
-                      (uint64_t)K / 32, (uint64_t)g.ldm * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE,
-                      "mvT")))
+      (rc = encode_2d(&maps->mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, q4plane + g.mv_off,
+                      (uint64_t)q4_min_ld(K), (uint64_t)M, (uint64_t)q4_min_ld(K) * 4, 32, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B, "mv pairs")))
     return rc;
   return Q6_OK;
 }
@@ -231,6 +232,13 @@ int q8_act_plane_bytes(int N, int K, size_t* xq_bytes, size_t* da_bytes, size_t*
   if (da_bytes) *da_bytes = (k / 32) * (size_t)ldda_of(N) * 4;
   if (xh_bytes) *xh_bytes = n * k * 2;
   if (ldda) *ldda = ldda_of(N);
+  return Q6_OK;
+}
+
+int q8_act_sums_bytes(int N, int K, size_t* us_bytes, int* ldus) {
+  if (N < 0 || K <= 0 || K % 256) return fail(Q6_EINVAL, "need N >= 0, K > 0, K %% 256 == 0");
+  if (us_bytes) *us_bytes = (size_t)N * (size_t)q6::q4_min_ld(K) * 4;
+  if (ldus) *ldus = q6::q4_min_ld(K);
   return Q6_OK;
 }
 

@@ -54,6 +54,19 @@
 //          math; the slot is handed back as soon as the stage's second chunk
 //          is in registers.
 // Every mbarrier wait is bounded (see q6_internal.cuh).
+//
+// q4_K ("r18: Load-time B pre-expansion", Sec. 1 and 3.2; "r38 -- q6_K
+// BT-style raw-byte mma kernel", Sec. 2.2) uses the same pipeline with one
+// operand plane sc * q (at most 945, exact in binary16: two MMAs per chunk)
+// and a second term, - sum over chunks of (da * S) * (dmin * m). Done in the
+// epilogue, that term costs one FMA per (token, row, chunk) with dmin * m
+// broadcast to every lane from shared memory, 4 bytes per wavefront: more
+// shared-memory wavefronts than the tensor pipe has cycles. Here it is a
+// contraction over the K/32 chunks on the tensor cores instead: after a
+// unit's chunk stages come its min stages (min_stages below), kind::tf32
+// MMAs of the hi/lo pairs of us = da * S and mv = dmin * m into a TMEM
+// buffer that the epilogue subtracts from Y, one word per (token, row) per
+// pair of super-blocks.
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -71,20 +84,20 @@ constexpr int kTmemCols = 512, kBufCols = 128;
 constexpr int kNumSlots = 2;  // TMEM slots of two chunk buffers (one operand stage) each
 
 // Weight formats: q6_K (two operand planes W_hi, W_lo) and q4_K (one plane
-// sc * q, and the min term in the epilogue).
+// sc * q, and the min term from the tf32 min stages below).
 enum : int { kFmtQ6 = 0, kFmtQ4 = 1 };
 
 // Shared-memory layout per format. Operand stage: Xh, W_hi (or sc * q) and,
-// for q6_K, W_lo tiles of 128 rows x 128 bytes. Scale stage (one
-// super-block): da [8 chunks][128 tokens], d [128 rows], and for q4_K the
-// activation block sums us = da * S [8][128 tokens] and dmin * m [8][128 rows].
+// for q6_K, W_lo tiles of 128 rows x 128 bytes; a q4_K min stage holds the
+// block-sum pairs of 128 tokens and the dmin * m pairs of 128 weight rows for
+// two super-blocks in the Xh and W slots (32 f32 = 128 bytes a row). Scale
+// stage (one super-block): da [8 chunks][128 tokens] and d [128 rows].
 template <int kFmt>
 struct Lay {
   static constexpr int kOpX = 0, kOpWhi = BT * 128, kOpWlo = kOpWhi + BW * 128;
   static constexpr int kOpStage = (kFmt == kFmtQ6 ? kOpWlo + BW * 128 : kOpWlo);  // 48 / 32 KB
   static constexpr int kScDa = 0, kScD = 8 * BT * 4, kScUs = kScD + BW * 4;
-  static constexpr int kScMv = kScUs + 8 * BT * 4;
-  static constexpr int kScStage = (kFmt == kFmtQ6 ? kScUs : kScMv + 8 * BW * 4);  // 4.5 / 12.5 KB
+  static constexpr int kScStage = kScUs;  // 4.5 KB
   static constexpr int kRingS = SB * kOpStage;  // the scale ring follows the operand ring
   static constexpr int kRingsBytes = kRingS + SS * kScStage;
   static_assert(kOpStage % 1024 == 0, "operand stages must keep 1024-byte alignment");
@@ -178,17 +191,29 @@ __device__ __forceinline__ void chunk_fma(float2* sb, const uint32_t (&p)[32], f
   }
 }
 
-// acc[j] += (nu, nu) * (dmin * m) of 32 columns (16 pairs, 8 float4 in
-// shared memory).
-__device__ __forceinline__ void min_term(float2* acc, float nu, const float4* mv) {
-  const float2 nu2 = make_float2(nu, nu);
+// acc[j] -= T[j] for 32 columns (16 pairs): the min term of a q4_K min stage.
+__device__ __forceinline__ void sub_words(float2* acc, const uint32_t (&t)[32]) {
+  const float2 neg = make_float2(-1.0f, -1.0f);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float4 m4 = mv[j];
-    acc[2 * j] = __ffma2_rn(nu2, make_float2(m4.x, m4.y), acc[2 * j]);
-    acc[2 * j + 1] = __ffma2_rn(nu2, make_float2(m4.z, m4.w), acc[2 * j + 1]);
-  }
+  for (int j = 0; j < 16; ++j)
+    acc[j] = __ffma2_rn(neg, make_float2(__uint_as_float(t[2 * j]), __uint_as_float(t[2 * j + 1])),
+                        acc[j]);
 }
+
+// q4_K min stages of a unit. The min term of super-blocks sb0 .. sb1-1,
+//   sum over their chunks c of us[n][c] * mv[m][c]
+// (us = da * S, mv = dmin * m), runs on the tensor cores: one min stage per
+// pair of super-blocks {2g, 2g+1} that the unit touches, whose tiles hold the
+// hi/lo pairs of both (see Lay); per super-block four K = 8 kind::tf32 MMAs
+// (hi*hi, hi*lo, lo*hi, lo*lo) into one TMEM buffer, which the epilogue
+// subtracts from Y. mv has at most 17 significant bits, so its pair is exact;
+// us's pair is within 2^-21 |us|; each product of tf32 values is exact in
+// f32. The count is padded to a multiple of 4 with empty stages (no copies,
+// no MMAs) so that every unit keeps a multiple of four operand stages.
+__device__ __forceinline__ int min_groups(const Unit& w) {
+  return ((w.sb1 - 1) >> 1) - (w.sb0 >> 1) + 1;
+}
+__device__ __forceinline__ int min_stages(const Unit& w) { return (min_groups(w) + 3) & ~3; }
 
 // The exact integers of 32 columns of a chunk accumulator, to the debug
 // output at out[(n * M + m) * stride + off] (off = c * mul + add).
@@ -268,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ---------------------------------------------------------- producer --
       if (lane == 0) {
-        constexpr uint32_t kTxS = 8 * BT * 4 + BW * 4 + (kQ4 ? 8 * BT * 4 + 8 * BW * 4 : 0);
-        constexpr uint32_t kTxB = (BT + (kQ4 ? 1 : 2) * BW) * 128;
+        constexpr uint32_t kTxS = 8 * BT * 4 + BW * 4;
+        constexpr uint32_t kTxB = (BT + (kQ4 ? 1 : 2) * BW) * 128;  // also a q4_K min stage
         int gs = 0, gk = 0;  // scale / operand stages issued so far
         bool ok = true;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
@@ -285,10 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive_expect_tx(&bars->s_full[slot], kTxS);
               tma_load_2d(st + L::kScDa, &tmDa, &bars->s_full[slot], n0, 8 * sb);
               tma_load_2d(st + L::kScD, &tmD, &bars->s_full[slot], m0, sb);
-              if (kQ4) {
-                tma_load_2d(st + L::kScUs, &tmUs, &bars->s_full[slot], n0, 8 * sb);
-                tma_load_2d(st + L::kScMv, &tmMv, &bars->s_full[slot], m0, 8 * sb);
-              }
               ++gs;
             }
             for (int h = 0; h < 4; ++h) {
@@ -301,6 +322,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d(bt + L::kOpX, &tmX, &bars->b_full[slot], kb * KB, n0);
               tma_load_2d(bt + L::kOpWhi, &tmWhi, &bars->b_full[slot], kb * KB, m0);
               if (!kQ4) tma_load_2d(bt + L::kOpWlo, &tmWlo, &bars->b_full[slot], kb * KB, m0);
+              ++gk;
+            }
+          }
+          if (kQ4) {
+            // the unit's min stages: pair group g's 128-byte rows of us and mv
+            const int g0 = w.sb0 >> 1, ng = min_groups(w), ns = min_stages(w);
+            for (int i = 0; i < ns && ok; ++i) {
+              const int slot = gk % SB;
+              if (!(ok = mbar_wait_bounded(&bars->b_empty[slot], ((gk / SB) & 1) ^ 1, abort_flag,
+                                           status, kSiteBEmpty)))
+                break;
+              uint8_t* bt = smem + slot * L::kOpStage;
+              if (i < ng) {
+                mbar_arrive_expect_tx(&bars->b_full[slot], kTxB);
+                tma_load_2d(bt + L::kOpX, &tmUs, &bars->b_full[slot], 32 * (g0 + i), n0);
+                tma_load_2d(bt + L::kOpWhi, &tmMv, &bars->b_full[slot], 32 * (g0 + i), m0);
+              } else {
+                mbar_arrive(&bars->b_full[slot]);  // an empty stage: nothing to copy
+              }
               ++gk;
             }
           }
@@ -332,14 +372,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the named-barrier phases stay paired one to one (bar.sync has no
         // time-out), and every other wait then returns at once.
         constexpr uint32_t idesc = idesc_f16_f32(BT, BW);
+        constexpr uint32_t idesc_min = idesc_tf32_f32(BT, BW);
         const int me = warp - 1;
         bool ok = true;
         int gbase = 0;  // global index of the unit's first operand stage
         int uses = 0;   // operand stages walked (issued into my slot)
         for (int u = blockIdx.x; u < U; u += gridDim.x) {
           const Unit w = unit_of(u, Tw, nsb);
-          const int nb = 4 * (w.sb1 - w.sb0);  // operand stages of the unit
-          for (int kb = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; kb < nb;
+          const int nb = 4 * (w.sb1 - w.sb0);  // the unit's chunk stages
+          const int nt = nb + (kQ4 ? min_stages(w) : 0);  // and its min stages
+          for (int kb = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; kb < nt;
                kb += kNumIssuers) {
             const int gk = gbase + kb;  // global operand stage; gk % 2 == me
             const int slot = gk % SB;
@@ -349,7 +391,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the epilogue has loaded the previous stage out of my slot
             if (uses++ > 0) slot_bar_sync(me);
             tc_fence_after();
-            if (lane == 0 && ok) {
+            if (lane == 0 && ok && kQ4 && kb >= nb) {
+              // a min stage: pair group g = sb0/2 + (kb - nb); super-block
+              // 2g + h has its hi parts at byte 64 h and its lo parts at
+              // 64 h + 32 of each row (descriptor start + 4 h, + 4 h + 2)
+              const int g = (w.sb0 >> 1) + (kb - nb);
+              const uint8_t* bt = smem + slot * L::kOpStage;
+              const uint32_t udesc = sw128_desc_lo(smem_u32(bt + L::kOpX));
+              const uint32_t vdesc = sw128_desc_lo(smem_u32(bt + L::kOpWhi));
+              const uint32_t d_tmem = tmem + (uint32_t)(2 * me * kBufCols);
+              uint32_t acc_on = 0;
+              if (kb - nb < min_groups(w)) {
+                for (int h = 0; h < 2; ++h) {
+                  const int sb = 2 * g + h;
+                  if (sb < w.sb0 || sb >= w.sb1) continue;
+#pragma unroll
+                  for (int ab = 0; ab < 4; ++ab) {
+                    const uint32_t ua = (uint32_t)(4 * h + 2 * (ab >> 1));
+                    const uint32_t vb = (uint32_t)(4 * h + 2 * (ab & 1));
+                    umma_tf32(d_tmem, udesc + ua, vdesc + vb, idesc_min, acc_on);
+                    acc_on = 1;
+                  }
+                }
+              }
+              // the epilogue frees the operand stage when it sees this commit
+              umma_commit(&bars->tfull[me]);
+            } else if (lane == 0 && ok) {
               // descriptors of the stage's three tiles; a K step of 16
               // elements (32 bytes) adds 2 to the start-address field
               const uint8_t* bt = smem + slot * L::kOpStage;
@@ -371,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
           }
-          gbase += nb;
+          gbase += nt;
         }
         // take the epilogue's hand-back of the last stage, so every phase
         // of the slot's barrier closes
@@ -461,21 +528,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[2 * j] = __ffma2_rn(make_float2(d4.x, d4.y), sb[2 * j], acc[2 * j]);
           acc[2 * j + 1] = __ffma2_rn(make_float2(d4.z, d4.w), sb[2 * j + 1], acc[2 * j + 1]);
         }
-        if (kQ4) {
-          // q4_K: the super-block's min terms, Y -= (da * S) * (dmin * m) per
-          // chunk, S the token's block sum (here, where Sb is no longer live)
-#pragma unroll 1
-          for (int cc = 0; cc < 8; ++cc) {
-            const float nu = -reinterpret_cast<const float*>(st + L::kScUs)[cc * BT + tok];
-            const float4* mv =
-                reinterpret_cast<const float4*>(st + L::kScMv + cc * BW * 4) + 16 * colh;
-            min_term(acc, nu, mv);
-            min_term(acc + 16, nu, mv + 8);
-          }
-        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_empty[slot]);
         ++gs;
+      }
+      if (kQ4) {
+        // q4_K: Y -= the min term, one TMEM buffer per min stage (slot use
+        // and ring slot follow the chunk stages: every unit starts at a
+        // multiple of four operand stages, and so do its min stages)
+        const int ng = min_groups(w), ns = min_stages(w);
+        for (int i4 = 0; i4 < ns; i4 += 4) {
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            const uint32_t ts = (uint32_t)(pp & 1);
+            if (ok && !mbar_wait_warp(&bars->tfull[ts], (uint32_t)((pp >> 1) & 1), abort_flag,
+                                      status, kSiteTFull))
+              ok = false;
+            if (ew == 0 && lane == 0) mbar_arrive(&bars->b_empty[pp]);
+            tc_fence_after();
+            const bool real = i4 + pp < ng;  // warp-uniform
+            if (real) {
+              const uint32_t col = 2 * ts * kBufCols;
+              tmem_ld32(lane_addr + col, pA);
+              tmem_ld32(lane_addr + col + 32u, pB);
+              tmem_wait_ld2(pA, pB);
+            }
+            tc_fence_before();
+            __syncwarp();
+            slot_bar_arrive((int)ts);
+            if (real) {
+              sub_words(acc, pA);
+              sub_words(acc + 16, pB);
+            }
+          }
+        }
       }
       if (ok && n < N && write_y) {
         float* yr = Y + (size_t)n * ldy + mcol;

@@ -19,8 +19,12 @@
 //   sc  : uint8 [M][K/32], the decoded 6-bit scales;
 //   mn  : uint8 [M][K/32], the decoded 6-bit mins;
 //   dT  : f32 [K/256][ldm], d as f32 (exact), transposed, rows M..ldm-1 zero;
-//   mvT : f32 [K/32][ldm], dmin * m (exact in f32: 11 by 6 significant bits),
-//         transposed, rows M..ldm-1 zero.
+//   mvp : f32 [M][q4_min_ld(K)], dmin * m (at most 11 + 6 = 17 significant
+//         bits) as the exact tf32 pair hi + lo: per super-block b, the hi
+//         parts of its 8 chunks at 16 b .. 16 b + 7 and the lo parts at
+//         16 b + 8 .. 16 b + 15; an odd super-block count leaves 16 zeros at
+//         the end of each row. The GEMM's min term runs on the tensor cores
+//         from these pairs (kind::tf32).
 // Operand plane (the unpack): binary16 [M][K], sc[j] * q (at most 63 * 15 =
 // 945, exact), or with unit scale q alone (the debug partials).
 #include "q6_internal.cuh"
@@ -55,28 +59,33 @@ __global__ void __launch_bounds__(256) q4k_pack_kernel(const uint8_t* __restrict
       plane[g.sc_off + (size_t)m * (K / 32) + c] = (uint8_t)sc;
       plane[g.mn_off + (size_t)m * (K / 32) + c] = (uint8_t)mn;
       const float dmin = __half2float(__ushort_as_half((unsigned short)(src[2] | (src[3] << 8))));
-      reinterpret_cast<float*>(plane + g.mv_off)[c * g.ldm + m] = dmin * (float)mn;
+      float hi, lo;
+      tf32_split(dmin * (float)mn, hi, lo);
+      float* mv = reinterpret_cast<float*>(plane + g.mv_off) + (size_t)m * q4_min_ld(K) + 16 * b;
+      mv[lane] = hi;
+      mv[8 + lane] = lo;
+      if ((nsb & 1) && b == nsb - 1) {  // the odd super-block count's padding
+        mv[16 + lane] = 0.0f;
+        mv[24 + lane] = 0.0f;
+      }
     } else if (lane == 8) {
       reinterpret_cast<float*>(plane + g.dt_off)[(size_t)b * g.ldm + m] =
           __half2float(__ushort_as_half((unsigned short)(src[0] | (src[1] << 8))));
     }
   }
-  // rows M .. ldm-1 of the transposed sub-planes, and the gaps between sub-planes
+  // rows M .. ldm-1 of the transposed d sub-plane, and the gaps between sub-planes
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthr = (long long)gridDim.x * blockDim.x;
   const int pad = g.ldm - M;
-  for (long long j = tid; j < (long long)pad * (nsb + K / 32); j += nthr) {
+  for (long long j = tid; j < (long long)pad * nsb; j += nthr) {
     const long long r = j / pad;
     const int col = M + (int)(j - r * pad);
-    if (r < nsb)
-      reinterpret_cast<float*>(plane + g.dt_off)[(size_t)r * g.ldm + col] = 0.0f;
-    else
-      reinterpret_cast<float*>(plane + g.mv_off)[(size_t)(r - nsb) * g.ldm + col] = 0.0f;
+    reinterpret_cast<float*>(plane + g.dt_off)[(size_t)r * g.ldm + col] = 0.0f;
   }
   if (blockIdx.x == 0) {
     const size_t ends[5] = {(size_t)M * (K / 2), g.sc_off + (size_t)M * (K / 32),
                             g.mn_off + (size_t)M * (K / 32), g.dt_off + (size_t)nsb * g.ldm * 4,
-                            g.mv_off + (size_t)(K / 32) * g.ldm * 4};
+                            g.mv_off + (size_t)M * q4_min_ld(K) * 4};
     const size_t starts[5] = {g.sc_off, g.mn_off, g.dt_off, g.mv_off, g.total};
     for (int r = 0; r < 5; ++r)
       for (size_t j = ends[r] + threadIdx.x; j < starts[r]; j += blockDim.x) plane[j] = 0;

@@ -41,9 +41,15 @@ inline PlaneGeom plane_geom(int M, int K) {
 }
 
 // Packed q4_K plane geometry (q4k.cu; all offsets 256-byte aligned).
+// Row length (f32 elements) of the q4_K min-term operand planes: per
+// super-block 16 values, the hi parts of its 8 chunks then the lo parts,
+// padded to an even number of super-blocks (32 values, one 128-byte tile row,
+// per pair of super-blocks).
+__host__ __device__ constexpr int q4_min_ld(int K) { return 32 * ((K / 256 + 1) / 2); }
+
 struct Q4Geom {
   size_t qs_off, sc_off, mn_off, dt_off, mv_off, total;
-  int ldm;  // row stride (elements) of the transposed sub-planes: M rounded up to 4
+  int ldm;  // row stride (elements) of the transposed d sub-plane: M rounded up to 4
 };
 inline Q4Geom q4_geom(int M, int K) {
   Q4Geom g;
@@ -54,7 +60,7 @@ inline Q4Geom q4_geom(int M, int K) {
   g.mn_off = g.sc_off + round_up(m * (k / 32), 256);
   g.dt_off = g.mn_off + round_up(m * (k / 32), 256);
   g.mv_off = g.dt_off + round_up((k / 256) * (size_t)g.ldm * 4, 256);
-  g.total = g.mv_off + round_up((k / 32) * (size_t)g.ldm * 4, 256);
+  g.total = g.mv_off + round_up(m * (size_t)q4_min_ld(K) * 4, 256);
   return g;
 }
 
@@ -107,8 +113,8 @@ struct TcMaps {
   CUtensorMap wlo;  // W_lo [M][K] f16, box {64, 128}, 128B swizzle
   CUtensorMap da;   // da   [K/32][ldda] f32, box {128, 8}
   CUtensorMap d;    // d^T  [K/256][ldm] f32, box {128, 1}
-  CUtensorMap us;   // q4_K: da * S [K/32][ldda] f32, box {128, 8}
-  CUtensorMap mv;   // q4_K: (dmin * m)^T [K/32][ldm] f32, box {128, 8}
+  CUtensorMap us;   // q4_K: da * S as hi/lo pairs [N][q4_min_ld] f32, box {32, 128}, 128B swizzle
+  CUtensorMap mv;   // q4_K: dmin * m as hi/lo pairs [M][q4_min_ld] f32, box {32, 128}, 128B swizzle
 };
 // What one tensor-core GEMM launch writes besides (or instead of) Y: the
 // exact integer of each (token, weight row, 32-element chunk c) accumulator
@@ -125,11 +131,12 @@ struct TcDebugOut {
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                           const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
 // The q4_K form of the same GEMM (one operand plane, sc * q, in maps.whi; the
-// min term from maps.us and maps.mv).
+// min term on the tensor cores from maps.us and maps.mv).
 cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                               const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
 // Tensor maps of a q4_K GEMM call (api.cu): Xh, the operand plane wq [M][K],
-// da and us [K/32][ldda], and the packed q4_K plane's dT and mvT sub-planes.
+// da [K/32][ldda], the block-sum pairs us [N][q4_min_ld], and the packed q4_K
+// plane's dT and min-pair sub-planes.
 int encode_tc_maps_q4k(TcMaps* maps, const uint8_t* q4plane, const void* wq, const void* Xh,
                        const float* da, const float* us, int M, int K, int N);
 // Tensor maps of one tensor-core GEMM call (api.cu): Xh [N][K], the operand
@@ -328,6 +335,41 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | (0u << 7) | (0u << 10)       // A, B format: f16
          | ((uint32_t)(N >> 3) << 17)   // N >> 3
          | ((uint32_t)(M >> 4) << 24);  // M >> 4
+}
+
+// Instruction descriptor, kind::tf32: tf32 x tf32 -> f32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4)                      // D format: f32
+         | (2u << 7) | (2u << 10)       // A, B format: tf32
+         | ((uint32_t)(N >> 3) << 17)   // N >> 3
+         | ((uint32_t)(M >> 4) << 24);  // M >> 4
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::tf32 (K = 8 per instruction, 32
+// bytes of a row, as for kind::f16), issued by one thread.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 ad, {%1, %5};\n\t"
+      "mov.b64 bd, {%2, %5};\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], ad, bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kSw128DescHi)
+      : "memory");
+}
+
+// The hi/lo pair of a f32 value for a two-term tf32 product: hi keeps the
+// sign, exponent and the top 10 stored mantissa bits (a tf32 value), lo =
+// x - hi (exact in f32). A tensor core reading lo as tf32 drops its low 13
+// mantissa bits, so hi + tf32(lo) is within 2^-21 |x| of x, and equals x
+// when x has at most 17 significant bits.
+__host__ __device__ inline void tf32_split(float x, float& hi, float& lo) {
+  union { float f; uint32_t u; } v;
+  v.f = x;
+  v.u &= 0xFFFFE000u;
+  hi = v.f;
+  lo = x - hi;
 }
 
 // Issues one 32x32b.x32 TMEM load: 32 consecutive 32-bit columns of this

@@ -14,11 +14,29 @@
 // Optionally (kSums) it also writes us = da * S per block, S the sum of the
 // block's 32 codes (exact), the activation side of the q4_K min term
 // ("r38 -- q6_K BT-style raw-byte mma kernel", Sec. 2.2: the prepass packs
-// the scale with the block sum).
+// the scale with the block sum), as the tf32 pair hi + lo the GEMM's min-term
+// MMAs read: row n of us [N][q4_min_ld(K)] holds, per super-block b, the hi
+// parts of its 8 blocks at 16 b .. 16 b + 7 and the lo parts at 16 b + 8 ..
+// 16 b + 15, and 16 zeros after an odd super-block count.
 #include "q6_quant.cuh"
 
 namespace q6 {
 namespace {
+
+// Block c of token n: us = da * S as its hi/lo pair (and the padding of an
+// odd super-block count, written by the last super-block's blocks).
+__device__ __forceinline__ void store_us(float* __restrict__ us, int n, int K, int c, float v) {
+  float hi, lo;
+  tf32_split(v, hi, lo);
+  const int b = c >> 3, i = c & 7, nsb = K >> 8;
+  float* row = us + (size_t)n * q4_min_ld(K) + 16 * b;
+  row[i] = hi;
+  row[8 + i] = lo;
+  if ((nsb & 1) && b == nsb - 1) {
+    row[16 + i] = 0.0f;
+    row[24 + i] = 0.0f;
+  }
+}
 
 // Small inputs (a few tokens): each thread owns eight consecutive elements
 // (two float4 loads issued together); four threads form one 32-element block
@@ -57,7 +75,7 @@ __global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restri
     if (Xh != nullptr) reinterpret_cast<uint4*>(Xh + (size_t)n * K)[j] = h8;
     if ((j & 3) == 0) {
       da[(size_t)(j >> 2) * ldda + n] = d;
-      if (kSums) us[(size_t)(j >> 2) * ldda + n] = d * sum;
+      if (kSums) store_us(us, n, K, j >> 2, d * sum);
     }
   }
 }
@@ -123,7 +141,7 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
     }
     if ((j & 1) == 0) {
       da[(size_t)(j >> 1) * ldda + n] = d;
-      if (kSums) us[(size_t)(j >> 1) * ldda + n] = d * sum;
+      if (kSums) store_us(us, n, K, j >> 1, d * sum);
     }
   }
 }

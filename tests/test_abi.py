@@ -53,6 +53,10 @@ def test_plane_sizes(lib):
     xq, dab, xh, ldda = q6.act_plane_bytes(3314, 11008)
     assert (xq, xh, ldda) == (3314 * 11008, 3314 * 11008 * 2, 3316)
     assert dab == 11008 // 32 * 3316 * 4
+    # the q4_K block-sum pairs: 16 values per super-block, an even count of them
+    assert q6.act_sums_bytes(3314, 11008) == (3314 * 704 * 4, 704)
+    assert q6.act_sums_bytes(5, 512) == (5 * 32 * 4, 32)
+    assert q6.act_sums_bytes(5, 256) == (5 * 32 * 4, 32)
 
 
 @pytest.mark.parametrize("M,K", [(0, 256), (4, 0), (4, 100), (4, 255), (-1, 256)])

@@ -51,9 +51,42 @@ def check_y(Y, Yo, label=""):
     assert err.sum() / np.abs(Yo).sum() <= NORMWISE, f"{label}: normwise error"
 
 
+def tf32_pairs(v):
+    """[rows, K/32] f32 -> [rows, ldus]: per super-block the hi parts of its 8
+    values (low 13 mantissa bits cleared), then the lo parts v - hi; an odd
+    super-block count padded with 16 zeros (the GEMM's min-term operand)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    hi = (v.view(np.uint32) & np.uint32(0xFFFFE000)).view(np.float32)
+    lo = v - hi
+    rows, nc = v.shape
+    nsb = nc // 8
+    out = np.zeros((rows, 32 * ((nsb + 1) // 2)), dtype=np.float32)
+    pairs = np.concatenate([hi.reshape(rows, nsb, 8), lo.reshape(rows, nsb, 8)], axis=2)
+    out[:, :16 * nsb] = pairs.reshape(rows, 16 * nsb)
+    return out
+
+
+def test_tf32_pairs_are_exact_splits():
+    """hi + lo == v; hi keeps 11 significant bits; a value with at most 17
+    significant bits (dmin * m) leaves a lo of at most 6."""
+    rng = np.random.default_rng(7)
+    v = (rng.standard_normal((3, 24)) * 10.0 ** rng.integers(-6, 6, (3, 24))).astype(np.float32)
+    p = tf32_pairs(v)
+    hi, lo = p[:, :32].reshape(3, 2, 16)[:, :, :8], p[:, :32].reshape(3, 2, 16)[:, :, 8:]
+    assert np.array_equal(hi.reshape(3, 16) + lo.reshape(3, 16), v[:, :16])
+    assert np.all((hi.view(np.uint32) & np.uint32(0x1FFF)) == 0)
+    assert p.shape == (3, 64) and np.all(p[:, 48:] == 0)
+    dmin = np.float32(np.float16(0.00213))
+    mv = np.float32(dmin * np.float32(61))
+    q = tf32_pairs(np.full((1, 8), mv, dtype=np.float32))
+    lo1 = q[0, 8]
+    m, e = np.frexp(np.float64(lo1))
+    assert lo1 != 0 and (m * 2 ** 6) == np.round(m * 2 ** 6)
+
+
 def quantize(q6, orc, X):
     """GPU activations with block sums, checked bit-exactly against the oracle's
-    codes and scales; us against da * S rounded to f32 once."""
+    codes and scales; us against the pairs of da * S rounded to f32 once."""
     act = q6.quantize_act(dev(X), want_us=True)
     q6.sync_status()
     xq_o, da_o = orc.quantize(X)
@@ -61,18 +94,18 @@ def quantize(q6, orc, X):
     assert np.array_equal(host(act.xq), xq_o)
     assert np.array_equal(host(act.da)[:, :N].T, da_o)
     S = xq_o.astype(np.int64).reshape(N, -1, 32).sum(-1).astype(np.float32)
-    assert np.array_equal(host(act.us)[:, :N].T, da_o * S)
+    assert np.array_equal(host(act.us), tf32_pairs(da_o * S))
     return act, xq_o, da_o
 
 
-@pytest.mark.parametrize("N,K", [(3, 256), (700, 1024), (77, 11008)])
+@pytest.mark.parametrize("N,K", [(3, 256), (700, 1024), (77, 11008), (5, 768)])
 def test_quantize_block_sums(q6, orc, N, K):
     X = synth.activations(0x51361001 + N, N, K, outlier_frac=0.01)
     X[0, 32:64] = 0.0
     quantize(q6, orc, X)
 
 
-@pytest.mark.parametrize("M,K", [(64, 256), (131, 768), (300, 1024)])
+@pytest.mark.parametrize("M,K", [(64, 256), (131, 768), (300, 1024), (40, 1280)])
 def test_q4k_pack_bitexact(q6, orc, M, K):
     raw = synth.q4k_raw_weights(0x51361101 + M, M, K)
     w = q6.q4k_pack_weights(dev(raw), M, K, wq=True)
@@ -85,9 +118,10 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
     o_mn = o_sc + r(M * nc)
     o_dt = o_mn + r(M * nc)
     o_mv = o_dt + r(nsb * ldm * 4)
-    assert plane.size == o_mv + r(nc * ldm * 4)
+    ldus = 32 * ((nsb + 1) // 2)
+    assert plane.size == o_mv + r(M * ldus * 4)
     for a, b in ((M * K // 2, o_sc), (o_sc + M * nc, o_mn), (o_mn + M * nc, o_dt),
-                 (o_dt + nsb * ldm * 4, o_mv), (o_mv + nc * ldm * 4, plane.size)):
+                 (o_dt + nsb * ldm * 4, o_mv), (o_mv + M * ldus * 4, plane.size)):
         assert np.all(plane[a:b] == 0)
     blocks = raw.reshape(M, nsb, 144)
     assert np.array_equal(plane[:M * K // 2].reshape(M, nsb, 128), blocks[:, :, 16:])
@@ -100,9 +134,11 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
     assert np.array_equal(plane[o_mn:o_mn + M * nc].reshape(M, nc), mn)
     dt = plane[o_dt:o_dt + nsb * ldm * 4].view(np.float32).reshape(nsb, ldm)
     assert np.array_equal(dt[:, :M].astype(np.float64), d.T) and np.all(dt[:, M:] == 0)
-    mv = plane[o_mv:o_mv + nc * ldm * 4].view(np.float32).reshape(nc, ldm)
-    assert np.array_equal(mv[:, :M].astype(np.float64), (np.repeat(dmin, 8, axis=1) * mn).T)
-    assert np.all(mv[:, M:] == 0)
+    mv = plane[o_mv:o_mv + M * ldus * 4].view(np.float32).reshape(M, ldus)
+    mv_exact = np.repeat(dmin, 8, axis=1) * mn            # dmin * m in double (exact)
+    assert np.array_equal(mv, tf32_pairs(mv_exact.astype(np.float32)))
+    pairs = mv[:, :16 * nsb].reshape(M, nsb, 2, 8).astype(np.float64)
+    assert np.array_equal((pairs[:, :, 0] + pairs[:, :, 1]).reshape(M, nc), mv_exact)
     codes = np.stack([np.concatenate([dec[m][b][0] for b in range(nsb)]) for m in range(M)])
     assert np.array_equal(host(w.wq).astype(np.int64),
                           np.repeat(sc, 32, axis=1) * codes.astype(np.int64))
