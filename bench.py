@@ -834,9 +834,10 @@ def run_q4k(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     peak_t, peak_src = tensor_peak(peaks)
     peak_s, _ = tensor_peak(peaks, sustained=True)
     tflops = ops_per_step / m_ms / 1e9
-    # quantiser: reads f32 X, writes Xh (2 B) and per-32 da and us; unpack:
-    # reads the nibbles (0.5 B) and sc (1/32 B), writes the operand plane (2 B)
-    q_bytes = N * K * (4 + 2) + 2 * (K // 32) * N * 4
+    # quantiser: reads f32 X, writes Xh (2 B), per-32 da and the us pairs
+    # (8 B per 32); unpack: reads the nibbles (0.5 B) and sc (1/32 B), writes
+    # the operand plane (2 B)
+    q_bytes = N * K * (4 + 2) + 3 * (K // 32) * N * 4
     u_bytes = M * K * (0.5 + 1 / 32 + 2)
     traffic = args.traffic if args.traffic is not None else TRAFFIC.get(
         ("q4k_ffn_down", "mmq_tc_q4k"))
@@ -858,7 +859,9 @@ def run_q4k(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
                                         if traffic is not None else "not captured for this "
                                         "kernel version"),
                      "algorithmic_bytes": q4k_method_bytes(M, K, N),
-                     "algorithmic_bytes_formula": "M*K*144/256 + N*K + 2*4*N*K/32 + 4*N*M",
+                     "algorithmic_bytes_formula": "M*K*144/256 + N*K + 2*4*N*K/32 + 4*N*M (the "
+                                                  "method's bytes: q4_K weights, int8 "
+                                                  "activations, da and block sums, f32 Y)",
                      "algorithmic": f"2*M*N*K = {ops_per_step:.4g} flop per launch"},
         "cpu_baseline": cpu, "e2e": e2e,
         # quantiser, unpack, and the GEMM's launches (the tile plan does not
@@ -1315,6 +1318,7 @@ SKINNY_FUSED_MAX_N = 2
 # DRAM bytes per launch from ncu captures of the current kernels, keyed by
 # (workload, kernel). An entry is removed when its kernel changes.
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.85e6 + 54.70e6,
+           ("q4k_ffn_down", "mmq_tc_q4k"): 635.71e6 + 58.53e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
            ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
