@@ -651,6 +651,23 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
             "ms": ams, "tops": ops_per_step / ams / 1e9,
             "note": "quantise + GEMM per step, the binary16 operand planes (4 B per weight) "
                     "expanded once at load time"}
+        # the quantiser fused into the GEMM's producer (f32 X in, no Xh or da
+        # plane), on resident operand planes and from the packed plane
+        for label, fsrc in (("fused_quantiser_wh", "wh"), ("fused_quantiser_raw", "raw")):
+            for i in range(3):
+                q6.mmq_f32_tc(Wa, Xs[i % R], Y=Ys[i % R], source=fsrc)
+            a, b = ev_pair()
+            a.record()
+            for i in range(args.alt_steps):
+                q6.mmq_f32_tc(Wa, Xs[i % R], Y=Ys[i % R], source=fsrc)
+            b.record()
+            torch.cuda.synchronize()
+            q6.sync_status()
+            ams = a.elapsed_time(b) / args.alt_steps
+            alt[label] = {"ms": ams, "tops": ops_per_step / ams / 1e9,
+                          "note": "q6k_mmq_f32_tc: f32 X straight into the GEMM, which quantises "
+                                  "each block per weight band; compare step_on_resident_planes "
+                                  "(wh) and the headline step (raw)"}
         # the pages' route on the legacy mma.sync int8 path, as a comparison point
         acts8 = [q6.quantize_act(Xs[j]) for j in range(R)]  # it reads Xq
         for i in range(3):

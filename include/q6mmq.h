@@ -60,6 +60,8 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_SKINNY_FUSED 6 /* quantiser and one/two-token GEMM in one kernel (q6k_mmq_f32) */
 #define Q6_PATH_Q4K_TC_RAW 7 /* q4_K: unpack of the packed plane into the workspace + tensor-core GEMM */
 #define Q6_PATH_Q4K_TC_WQ 8  /* q4_K: tensor-core GEMM on a resident binary16 operand plane */
+#define Q6_PATH_TC_FUSED_RAW 9 /* q6k_mmq_f32_tc: unpack into the workspace + GEMM quantising X itself */
+#define Q6_PATH_TC_FUSED_WH 10 /* q6k_mmq_f32_tc: GEMM quantising X itself, resident operand planes */
 
 #define Q6_SKINNY_MAX_N 16
 #define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
@@ -312,6 +314,27 @@ int q6k_mmq_noalloc_status(q6_stream_t s);
  * allocation, no bounded waits, asynchronous on s. */
 int q6k_mmq_f32(const void *plane, int M, int K, const float *X, int ldx, int N, float *Y,
                 int ldy, int *path_out, q6_stream_t s);
+
+/* The tensor-core GEMM from f32 activations, with the quantiser fused into
+ * the GEMM's producer: the kernel reads X, forms each 32-element block's da
+ * and binary16 codes in shared memory (bit for bit those of
+ * q8_quantize_act), and runs the GEMM on them; no Xh or da plane is written.
+ * This is the inverse of the pages' prepass ("r38 -- q6_K BT-style raw-byte
+ * mma kernel", Sec. 1: r34 moved the A-side transform out of the GEMM into a
+ * prepass). Y is bit for bit that of q8_quantize_act + q6k_mmq on the
+ * tensor-core path (N > Q6_SKINNY_MAX_N), and for any N >= 1 within the
+ * tolerance of the oracle. The kernel quantises every activation block once
+ * per 128-row weight band (M / 128 times), against once for the separate
+ * quantiser.
+ *   plane : packed q6_K plane (required, for d); wh : resident operand planes
+ *           [2][M][K] or NULL (then they are unpacked into the workspace).
+ *   X : device f32 [N][ldx], 16-byte aligned, ldx >= K, ldx % 4 == 0.
+ *   workspace : 256-byte aligned, at least 4 * M * K bytes when wh is NULL.
+ *   path_out : NULL or receives Q6_PATH_TC_FUSED_RAW / Q6_PATH_TC_FUSED_WH.
+ * Errors as for q6k_mmq. */
+int q6k_mmq_f32_tc(const void *plane, const uint16_t *wh, int M, int K, const float *X, int ldx,
+                   int N, float *Y, int ldy, void *workspace, size_t workspace_bytes,
+                   int *path_out, q6_stream_t s);
 
 /* ------------------------------------------------------------------------
  * The q4_K x int8 GEMM ("r18: Load-time B pre-expansion -- staging becomes a

@@ -19,11 +19,13 @@ LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
 
 Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
 (PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH, PATH_SYNC_WEXP,
- PATH_SKINNY_FUSED, PATH_Q4K_TC_RAW, PATH_Q4K_TC_WQ) = range(9)
+ PATH_SKINNY_FUSED, PATH_Q4K_TC_RAW, PATH_Q4K_TC_WQ, PATH_TC_FUSED_RAW,
+ PATH_TC_FUSED_WH) = range(11)
 PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh", PATH_SYNC_WEXP: "sync_wexp",
               PATH_SKINNY_FUSED: "skinny_fused", PATH_Q4K_TC_RAW: "q4k_tc_raw",
-              PATH_Q4K_TC_WQ: "q4k_tc_wq"}
+              PATH_Q4K_TC_WQ: "q4k_tc_wq", PATH_TC_FUSED_RAW: "tc_fused_raw",
+              PATH_TC_FUSED_WH: "tc_fused_wh"}
 SKINNY_MAX_N = 16
 FUSED_MAX_N = 2
 
@@ -48,6 +50,7 @@ SIGNATURES = [
     ("q6k_mmq_noalloc_status", _I, [_P]),
     ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _IP, _P]),
     ("q6k_mmq_f32", _I, [_P, _I, _I, _P, _I, _I, _P, _I, _IP, _P]),
+    ("q6k_mmq_f32_tc", _I, [_P, _P, _I, _I, _P, _I, _I, _P, _I, _P, ctypes.c_size_t, _IP, _P]),
     ("q8_act_sums_bytes", _I, [_I, _I, _SZ, _IP]),
     ("q8_quantize_act_sums", _I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     ("q4k_plane_bytes", _I, [_I, _I, _SZ, _SZ]),
@@ -407,6 +410,44 @@ def mmq_f32(w: Weights, X, Y=None, stream=None):
     path = ctypes.c_int(-1)
     _check(load().q6k_mmq_f32(_ptr(w.plane), M, K, _ptr(X), _row_stride(X), N, _ptr(Y),
                               _row_stride(Y), ctypes.byref(path), _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value))
+
+
+def mmq_f32_tc(w: Weights, X, Y=None, source: str = "auto", workspace=None, wh=None,
+               stream=None):
+    """The tensor-core GEMM straight from f32 activations X [N, K], the
+    quantiser fused into the GEMM (no Xh or da plane): Y bit for bit that of
+    quantize_act(X) followed by mmq() on the tensor-core path. source: "raw"
+    (unpack the packed plane), "wh" (resident operand planes) or "auto".
+    Returns (Y, path name)."""
+    import torch
+    if not isinstance(X, torch.Tensor) or X.dim() != 2:
+        raise Q6Error(Q6_EINVAL, "X must be a 2-D torch tensor [N, K]")
+    N, K, M = X.shape[0], w.K, w.M
+    dev = w.device
+    _tensor(X, "X", torch.float32, (N, K), dev, rows=True)
+    if source == "auto":
+        source = "wh" if (wh is not None or w.wh is not None) else "raw"
+    if source not in ("raw", "wh"):
+        raise Q6Error(Q6_EINVAL, f"source must be raw, wh or auto, not {source}")
+    w16 = (wh if wh is not None else w.wh) if source == "wh" else None
+    if source == "wh" and w16 is None:
+        raise Q6Error(Q6_EINVAL, "weights were packed without the wh plane")
+    if w16 is not None:
+        _tensor(w16, "wh", torch.float16, (2, M, K), dev)
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
+    ws_need = 4 * M * K if w16 is None else 0
+    if workspace is not None:
+        _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
+                tuple(getattr(workspace, "shape", ())), dev)
+    ws = workspace if workspace is not None else (_workspace(ws_need, dev) if ws_need else None)
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    path = ctypes.c_int(-1)
+    _check(load().q6k_mmq_f32_tc(_ptr(w.plane), _ptr(w16), M, K, _ptr(X), _row_stride(X), N,
+                                 _ptr(Y), _row_stride(Y), _ptr(ws), ws_bytes, ctypes.byref(path),
+                                 _stream(stream)))
     return Y, PATH_NAMES.get(path.value, str(path.value))
 
 

@@ -140,14 +140,19 @@ int encode_tc_maps(TcMaps* maps, const uint8_t* plane, const void* wop, const vo
   const uint16_t* whi = static_cast<const uint16_t*>(wop);
   const uint16_t* wlo = whi + (size_t)M * (size_t)K;
   int rc;
-  if ((rc = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K, (uint64_t)N,
-                      (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "Xh")) ||
-      (rc = encode_2d(&maps->whi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, whi, (uint64_t)K, (uint64_t)M,
+  // Xh and da are NULL for the fused quantiser, which makes them itself
+  if (Xh && (rc = encode_2d(&maps->x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Xh, (uint64_t)K,
+                            (uint64_t)N, (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                            "Xh")))
+    return rc;
+  if (da && (rc = encode_2d(&maps->da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N,
+                            (uint64_t)K / 32, (uint64_t)ldda_of(N) * 4, 128, 8,
+                            CU_TENSOR_MAP_SWIZZLE_NONE, "da")))
+    return rc;
+  if ((rc = encode_2d(&maps->whi, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, whi, (uint64_t)K, (uint64_t)M,
                       (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "W_hi")) ||
       (rc = encode_2d(&maps->wlo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wlo, (uint64_t)K, (uint64_t)M,
                       (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "W_lo")) ||
-      (rc = encode_2d(&maps->da, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, da, (uint64_t)N, (uint64_t)K / 32,
-                      (uint64_t)ldda_of(N) * 4, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE, "da")) ||
       (rc = encode_2d(&maps->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, plane + g.dt_off, (uint64_t)M,
                       (uint64_t)K / 256, (uint64_t)g.ldm * 4, 128, 1, CU_TENSOR_MAP_SWIZZLE_NONE,
                       "d")))
@@ -466,6 +471,50 @@ int q6k_mmq_f32(const void* plane, int M, int K, const float* X, int ldx, int N,
                                               Y, ldy, (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "fused one/two-token kernel launch");
   if (path_out) *path_out = Q6_PATH_SKINNY_FUSED;
+  return Q6_OK;
+}
+
+int q6k_mmq_f32_tc(const void* plane, const uint16_t* wh, int M, int K, const float* X, int ldx,
+                   int N, float* Y, int ldy, void* workspace, size_t workspace_bytes,
+                   int* path_out, q6_stream_t s) {
+  if (path_out) *path_out = Q6_PATH_NONE;
+  if (M <= 0 || K <= 0 || K % 256 || N < 0)
+    return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
+  if (ldx < K) return fail(Q6_EINVAL, "ldx (%d) < K (%d)", ldx, K);
+  if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
+  if (N == 0) return Q6_OK;
+  if (!plane || !X || !Y) return fail(Q6_EINVAL, "plane, X and Y are required");
+  if (!aligned(plane, 256) || !aligned(X, 16) || ldx % 4 || !aligned(Y, 4) ||
+      (wh && !aligned(wh, 16)) || (workspace && !aligned(workspace, 256)))
+    return fail(Q6_EALIGN, "plane, workspace 256 B; X 16 B with ldx %% 4 == 0; wh 16 B; Y 4 B");
+  if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40) ||
+      (long long)N * ldx > (1LL << 40))
+    return fail(Q6_ESIZE, "problem too large");
+  if (!wh) {
+    const size_t need = (size_t)M * (size_t)K * 4;
+    if (!workspace || workspace_bytes < need)
+      return fail(Q6_ESIZE, "workspace of %zu bytes needed to unpack the weights (got %zu)", need,
+                  workspace ? workspace_bytes : (size_t)0);
+  }
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e;
+  const uint8_t* pb = static_cast<const uint8_t*>(plane);
+  const void* wop = wh;
+  int path = Q6_PATH_TC_FUSED_WH;
+  if (!wh) {
+    __half* ws = static_cast<__half*>(workspace);
+    if ((e = q6::launch_expand_raw(pb, M, K, ws, (cudaStream_t)s)) != cudaSuccess)
+      return cuda_fail(e, "weight unpack launch");
+    wop = ws;
+    path = Q6_PATH_TC_FUSED_RAW;
+  }
+  q6::TcMaps maps;
+  if ((rc = encode_tc_maps(&maps, pb, wop, nullptr, nullptr, M, K, N))) return rc;
+  e = q6::launch_mmq_tc_fused(maps, M, K, X, ldx, N, Y, ldy, st->status, (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "fused-quantiser tensor-core kernel launch");
+  if (path_out) *path_out = path;
   return Q6_OK;
 }
 

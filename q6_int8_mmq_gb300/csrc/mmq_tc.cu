@@ -67,7 +67,7 @@
 // MMAs of the hi/lo pairs of us = da * S and mv = dmin * m into a TMEM
 // buffer that the epilogue subtracts from Y, one word per (token, row) per
 // pair of super-blocks.
-#include "q6_internal.cuh"
+#include "q6_quant.cuh"
 
 namespace q6 {
 namespace {
@@ -99,6 +99,7 @@ struct Lay {
   static constexpr int kScDa = 0, kScD = 8 * BT * 4, kScUs = kScD + BW * 4;
   static constexpr int kScStage = kScUs;  // 4.5 KB
   static constexpr int kRingS = SB * kOpStage;  // the scale ring follows the operand ring
+  static constexpr int kXStage = kRingS + SS * kScStage;  // fused quantiser staging, 16 KB
   static constexpr int kRingsBytes = kRingS + SS * kScStage;
   static_assert(kOpStage % 1024 == 0, "operand stages must keep 1024-byte alignment");
   static_assert(kScStage % 128 == 0, "scale stages must keep 128-byte alignment");
@@ -139,12 +140,18 @@ struct Bars {
   int abort;
 };
 
-template <int kFmt>
+// Bytes of shared memory past the rings: the fused quantiser's staging rows
+// (128 rows of 128 bytes), then the barriers.
+template <bool kFuseX>
+constexpr int extra_bytes() { return kFuseX ? BT * 128 : 0; }
+template <int kFmt, bool kFuseX = false>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Lay<kFmt>::kRingsBytes + sizeof(Bars);
+  return 1024 + (size_t)Lay<kFmt>::kRingsBytes + extra_bytes<kFuseX>() + sizeof(Bars);
 }
-static_assert(smem_bytes<kFmtQ6>() <= 232448 && smem_bytes<kFmtQ4>() <= 232448,
+static_assert(smem_bytes<kFmtQ6>() <= 232448 && smem_bytes<kFmtQ4>() <= 232448 &&
+                  smem_bytes<kFmtQ6, true>() <= 232448,
               "shared memory budget");
+static_assert(Lay<kFmtQ6>::kXStage % 128 == 0, "staging rows keep 16-byte alignment");
 
 // Work units: units 0 .. Tw-1 are whole tiles; when the last round of tiles
 // would leave more than half the CTAs idle, each of its tiles is split into
@@ -215,6 +222,72 @@ __device__ __forceinline__ int min_groups(const Unit& w) {
 }
 __device__ __forceinline__ int min_stages(const Unit& w) { return (min_groups(w) + 3) & ~3; }
 
+// ---------------------------------------------------- fused quantiser ---
+// With kFuseX the epilogue warps also produce the A operand: epilogue thread
+// (tok, colh) quantises one 32-element block of each operand stage four
+// stages ahead of the one it consumes, token n = n0 + tok, elements k0 ..
+// k0 + 31, with the standalone quantiser's arithmetic (q6_quant.cuh), so the
+// codes and scales are bit for bit those of q8_quantize_act.
+// fx_issue starts the copy of the warp's 32 blocks (tokens 32 q .. 32 q +
+// 31, q = tok / 32, elements k0 .. k0 + 31) into the staging rows of their
+// threads: row t of the target stage's Xh tile (colh 0) or of the 16 KB
+// staging rows after the scale ring (colh 1), 16-byte unit i at unit
+// i ^ (t % 8) so that a warp's rows spread over all banks. Eight lanes copy
+// one 128-byte row, four rows per instruction, so each instruction touches
+// four cache lines (with one row per thread it touched 32, and the L1 tag
+// stage took more cycles than the GEMM's whole stage). Rows n >= N are
+// zero-filled, which gives the codes and scale of a zero block, as the
+// separate path's zero-filled tiles do.
+constexpr int kBarFx = 3;  // named barrier of the 256 epilogue threads
+
+__device__ __forceinline__ void fx_issue(uint32_t stg0, int tok, const float* __restrict__ Xf,
+                                         int ldx, int N, int n0w, int k0) {
+  const int lane = tok & 31, piece = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);  // row of the warp's 32
+    const int n = n0w + r;
+    const bool valid = n < N;
+    const char* src =
+        reinterpret_cast<const char*>(Xf + (size_t)(valid ? n : 0) * ldx + k0) + 16 * piece;
+    const uint32_t dst = stg0 + (uint32_t)(r * 128) + (uint32_t)((piece ^ (r & 7)) << 4);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16u : 0u)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// fx_finish waits for the copy and reads the block; after all 256 epilogue
+// threads have read theirs (the codes of row tok overwrite the staging of
+// thread (tok, 0)) it writes the block's binary16 codes into the
+// 128-byte-swizzled Xh tile (16-byte unit j of row tok at unit j ^ (tok % 8))
+// and its scale, and makes the codes visible to the tensor core.
+__device__ __forceinline__ void fx_finish(const uint8_t* stg, uint8_t* xh, int tok, int colh,
+                                          float* da_out) {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncwarp();  // the row was copied by eight lanes of this warp
+  float4 v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = reinterpret_cast<const float4*>(stg)[i ^ (tok & 7)];
+  asm volatile("bar.sync %0, %1;" ::"n"(kBarFx), "n"(32 * kNumEpiWarps) : "memory");
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    a = fmaxf(a, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  const float d = __fdiv_rn(a, 127.0f);
+  const float r = recip_or_zero(d);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 h;
+    quant8h(v[2 * i], v[2 * i + 1], d, r, h);
+    const int j = 4 * colh + i;
+    *reinterpret_cast<uint4*>(xh + tok * 128 + ((j ^ (tok & 7)) << 4)) = h;
+  }
+  *da_out = d;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // The exact integers of 32 columns of a chunk accumulator, to the debug
 // output at out[(n * M + m) * stride + off] (off = c * mul + add).
 template <bool kPartials>
@@ -233,7 +306,7 @@ __device__ __forceinline__ void dump_partials(int32_t* __restrict__ out, int M, 
   }
 }
 
-template <int kFmt, bool kPartials>
+template <int kFmt, bool kPartials, bool kFuseX>
 __global__ void __launch_bounds__(kThreads, 1)
     mmq_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmWhi,
                   const __grid_constant__ CUtensorMap tmWlo, const __grid_constant__ CUtensorMap tmDa,
@@ -241,25 +314,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmMv, int M, int K, int N, int Tw, int U,
                   float* __restrict__ Y, int ldy, int y_vec4, int32_t* __restrict__ partials,
                   int p_stride, int p_mul, int p_add, int write_y,
-                  unsigned int* __restrict__ status) {
+                  const float* __restrict__ Xf, int ldx, unsigned int* __restrict__ status) {
   using L = Lay<kFmt>;
   constexpr bool kQ4 = kFmt == kFmtQ4;
+  static_assert(!(kFuseX && kQ4), "the fused quantiser serves the q6_K kernel");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + L::kRingsBytes);
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::kRingsBytes + extra_bytes<kFuseX>());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = (N + BT - 1) / BT;
   const int nsb = K / 256;  // super-blocks per tile
   volatile int* abort_flag = &bars->abort;
 
   if (threadIdx.x == 0) {
+    // with the fused quantiser the epilogue warps also fill da and Xh, and
+    // each arrives once per scale stage and per operand stage
+    constexpr int kFillers = 1 + (kFuseX ? kNumEpiWarps : 0);
     for (int s = 0; s < SS; ++s) {
-      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_full[s], kFillers);
       mbar_init(&bars->s_empty[s], kNumEpiWarps);
     }
     for (int s = 0; s < SB; ++s) {
-      mbar_init(&bars->b_full[s], 1);
+      mbar_init(&bars->b_full[s], kFillers);
       mbar_init(&bars->b_empty[s], 1);
     }
     for (int b = 0; b < kNumSlots; ++b) mbar_init(&bars->tfull[b], 1);
@@ -268,10 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmX);
+    if (!kFuseX) {
+      tma_prefetch_desc(&tmX);
+      tma_prefetch_desc(&tmDa);
+    }
     tma_prefetch_desc(&tmWhi);
     tma_prefetch_desc(&tmWlo);
-    tma_prefetch_desc(&tmDa);
     tma_prefetch_desc(&tmD);
     if (kQ4) {
       tma_prefetch_desc(&tmUs);
@@ -293,8 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ---------------------------------------------------------- producer --
       if (lane == 0) {
-        constexpr uint32_t kTxS = 8 * BT * 4 + BW * 4;
-        constexpr uint32_t kTxB = (BT + (kQ4 ? 1 : 2) * BW) * 128;  // also a q4_K min stage
+        // (with the fused quantiser, da and the Xh tiles come from the epilogue)
+        constexpr uint32_t kTxS = (kFuseX ? 0 : 8 * BT * 4) + BW * 4;
+        constexpr uint32_t kTxB = ((kFuseX ? 0 : BT) + (kQ4 ? 1 : 2) * BW) * 128;  // and a min stage
         int gs = 0, gk = 0;  // scale / operand stages issued so far
         bool ok = true;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
@@ -308,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               uint8_t* st = smem + L::kRingS + slot * L::kScStage;
               mbar_arrive_expect_tx(&bars->s_full[slot], kTxS);
-              tma_load_2d(st + L::kScDa, &tmDa, &bars->s_full[slot], n0, 8 * sb);
+              if (!kFuseX) tma_load_2d(st + L::kScDa, &tmDa, &bars->s_full[slot], n0, 8 * sb);
               tma_load_2d(st + L::kScD, &tmD, &bars->s_full[slot], m0, sb);
               ++gs;
             }
@@ -319,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               uint8_t* bt = smem + slot * L::kOpStage;
               mbar_arrive_expect_tx(&bars->b_full[slot], kTxB);
-              tma_load_2d(bt + L::kOpX, &tmX, &bars->b_full[slot], kb * KB, n0);
+              if (!kFuseX) tma_load_2d(bt + L::kOpX, &tmX, &bars->b_full[slot], kb * KB, n0);
               tma_load_2d(bt + L::kOpWhi, &tmWhi, &bars->b_full[slot], kb * KB, m0);
               if (!kQ4) tma_load_2d(bt + L::kOpWlo, &tmWlo, &bars->b_full[slot], kb * KB, m0);
               ++gk;
@@ -464,9 +544,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t pA[32], pB[32];
     int gs = 0;
     bool ok = true;
+    // fused quantiser: the thread's staging row for operand ring slot pp, and
+    // the da entry of chunk cc of scale ring slot ss
+    auto fx_stg = [&](int pp) -> uint8_t* {
+      return colh == 0 ? smem + pp * L::kOpStage + L::kOpX + tok * 128
+                       : smem + L::kXStage + tok * 128;
+    };
+    const int wrow = 32 * quarter;  // the warp's first token row
+    auto fx_stg0 = [&](int pp) -> uint32_t {
+      return smem_u32(fx_stg(pp)) - (uint32_t)(lane * 128);
+    };
+    auto fx_da = [&](int ss, int cc) -> float* {
+      return reinterpret_cast<float*>(smem + L::kRingS + ss * L::kScStage + L::kScDa) + cc * BT +
+             tok;
+    };
+    if (kFuseX && (int)blockIdx.x < U) {
+      // the CTA's first four operand stages (its first super-block)
+      const Unit w0 = unit_of(blockIdx.x, Tw, nsb);
+      const int n0 = (w0.t % NT) * BT;
+      for (int pp = 0; pp < 4; ++pp) {
+        fx_issue(fx_stg0(pp), tok, Xf, ldx, N, n0 + wrow, (4 * w0.sb0 + pp) * KB + 32 * colh);
+        fx_finish(fx_stg(pp), smem + pp * L::kOpStage + L::kOpX, tok, colh, fx_da(0, 2 * pp + colh));
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->b_full[pp]);
+          if (pp == 3) mbar_arrive(&bars->s_full[0]);
+        }
+      }
+    }
     // Once a wait has been given up (ok == false) the epilogue stops waiting
     // and writes no Y, but still walks every stage and hands every TMEM slot
-    // use back, so that the issuers' bar.sync phases stay paired.
+    // use back, so that the issuers' bar.sync phases stay paired (and, with
+    // the fused quantiser, every thread still takes every quantisation step,
+    // so that its barrier stays paired too).
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
       const Unit w = unit_of(u, Tw, nsb);
       const int m0 = (w.t / NT) * BW, n0 = (w.t % NT) * BT;
@@ -481,6 +591,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
         const uint8_t* st = smem + L::kRingS + slot * L::kScStage;
         const float* sda = reinterpret_cast<const float*>(st + L::kScDa) + tok;
+        // fused quantiser: this super-block's stages quantise those of the
+        // next super-block (of this unit, or the CTA's next unit's first),
+        // four operand stages ahead, into the same ring slots
+        int fx_sb = s + 1, fx_n0 = n0;
+        bool fx_on = kFuseX;
+        if (kFuseX && fx_sb >= w.sb1) {
+          const int un = u + (int)gridDim.x;
+          fx_on = un < U;
+          if (fx_on) {
+            const Unit wn = unit_of(un, Tw, nsb);
+            fx_sb = wn.sb0;
+            fx_n0 = (wn.t % NT) * BT;
+          }
+        }
+        const int fx_slot = (gs + 1) % SS;
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
           // Operand stage 4s + pp: its two chunks sit in TMEM slot pp % 2 (a
@@ -489,6 +614,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && !mbar_wait_warp(&bars->tfull[ts], (uint32_t)((pp >> 1) & 1), abort_flag,
                                     status, kSiteTFull))
             ok = false;
+          // the stage's Xh tile has been read: stage the block four ahead
+          if (fx_on)
+            fx_issue(fx_stg0(pp), tok, Xf, ldx, N, fx_n0 + wrow,
+                     (4 * fx_sb + pp) * KB + 32 * colh);
           // The stage's MMAs are complete, so its operand ring slot (pp: the
           // super-block starts at a global stage that is a multiple of SB)
           // can be refilled: one arrive per stage, from one thread.
@@ -518,6 +647,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             dump_partials<kPartials>(partials, M, N, p_stride, n, mcol, c * p_mul + p_add, pA);
             dump_partials<kPartials>(partials, M, N, p_stride, n, mcol + 32, c * p_mul + p_add,
                                      pB);
+          }
+          if (fx_on) {
+            // quantise the staged block into ring slot pp's Xh tile and its
+            // scale into the next super-block's scale stage
+            fx_finish(fx_stg(pp), smem + pp * L::kOpStage + L::kOpX, tok, colh,
+                      fx_da(fx_slot, 2 * pp + colh));
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&bars->b_full[pp]);
+              if (pp == 3) mbar_arrive(&bars->s_full[fx_slot]);
+            }
           }
         }
         // Y += d * Sb for this super-block
@@ -609,9 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int g_num_sms[64] = {0};
 
-template <int F, bool P>
+template <int F, bool P, bool X = false>
 cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
-                       const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
+                       const TcDebugOut& dbg, unsigned int* status, cudaStream_t s,
+                       const float* Xf = nullptr, int ldx = 0) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -625,16 +766,16 @@ cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ld
         Y, ldy, M, N, p.Tw, y_vec4);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  mmq_tc_kernel<F, P><<<p.grid, kThreads, smem_bytes<F>(), s>>>(
+  mmq_tc_kernel<F, P, X><<<p.grid, kThreads, smem_bytes<F, X>(), s>>>(
       maps.x, maps.whi, maps.wlo, maps.da, maps.d, maps.us, maps.mv, M, K, N, p.Tw, p.U, Y, ldy,
-      y_vec4, dbg.out, dbg.stride, dbg.mul, dbg.add, dbg.write_y, status);
+      y_vec4, dbg.out, dbg.stride, dbg.mul, dbg.add, dbg.write_y, Xf, ldx, status);
   return cudaGetLastError();
 }
 
-template <int F, bool P>
+template <int F, bool P, bool X = false>
 cudaError_t raise_smem() {
-  return cudaFuncSetAttribute(mmq_tc_kernel<F, P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem_bytes<F>());
+  return cudaFuncSetAttribute(mmq_tc_kernel<F, P, X>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<F, X>());
 }
 
 }  // namespace
@@ -664,9 +805,9 @@ TcPlan mmq_tc_plan(int M, int K, int N, int sms) {
 cudaError_t mmq_tc_prepare() {
   cudaError_t e;
   if ((e = raise_smem<kFmtQ6, false>()) || (e = raise_smem<kFmtQ6, true>()) ||
-      (e = raise_smem<kFmtQ4, false>()))
+      (e = raise_smem<kFmtQ4, false>()) || (e = raise_smem<kFmtQ4, true>()))
     return e;
-  return raise_smem<kFmtQ4, true>();
+  return raise_smem<kFmtQ6, false, true>();
 }
 
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
@@ -679,6 +820,11 @@ cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y,
                               const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
   return dbg.out ? launch_one<kFmtQ4, true>(maps, M, K, N, Y, ldy, dbg, status, s)
                  : launch_one<kFmtQ4, false>(maps, M, K, N, Y, ldy, dbg, status, s);
+}
+
+cudaError_t launch_mmq_tc_fused(const TcMaps& maps, int M, int K, const float* X, int ldx, int N,
+                                float* Y, int ldy, unsigned int* status, cudaStream_t s) {
+  return launch_one<kFmtQ6, false, true>(maps, M, K, N, Y, ldy, TcDebugOut{}, status, s, X, ldx);
 }
 
 }  // namespace q6

@@ -130,6 +130,12 @@ struct TcDebugOut {
 };
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                           const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
+// The same GEMM quantising its A operand itself: f32 X [N][ldx] (16-byte
+// aligned rows) is quantised per 32-element block inside the kernel, bit for
+// bit as q8_quantize_act does, into the Xh tiles and da; maps.x and maps.da
+// are unused.
+cudaError_t launch_mmq_tc_fused(const TcMaps& maps, int M, int K, const float* X, int ldx, int N,
+                                float* Y, int ldy, unsigned int* status, cudaStream_t s);
 // The q4_K form of the same GEMM (one operand plane, sc * q, in maps.whi; the
 // min term on the tensor cores from maps.us and maps.mv).
 cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,

@@ -72,6 +72,15 @@ __device__ __forceinline__ void quant8(const float4 v0, const float4 v1, float d
   q8 = make_uint2(pack_q4(h8.x, h8.y), pack_q4(h8.z, h8.w));
 }
 
+// Eight elements -> their binary16 codes only (the operand plane).
+__device__ __forceinline__ void quant8h(const float4 v0, const float4 v1, float d, float r,
+                                        uint4& h8) {
+  float n[8];
+  quant8f(v0, v1, d, r, n);
+  h8 = make_uint4(pack_h2(n[0], n[1]), pack_h2(n[2], n[3]), pack_h2(n[4], n[5]),
+                  pack_h2(n[6], n[7]));
+}
+
 // quant8, and the sum of the eight codes (an exact integer as a float).
 __device__ __forceinline__ void quant8_sum(const float4 v0, const float4 v1, float d, float r,
                                            uint2& q8, uint4& h8, float& sum) {

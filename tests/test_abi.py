@@ -128,6 +128,25 @@ def test_host_side_rejections(lib):
     assert f32(K=206592 + 256, ldx=206848, N=1) == q6.Q6_ESIZE
     assert f32(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
+    # the tensor-core GEMM with the fused quantiser: ldx < K, ldy < M, misaligned
+    # X / ldx / wh / workspace, no workspace for the unpack, the empty case
+    def f32tc(plane=fake, wh=fake, M=64, K=256, X=fake, ldx=256, N=64, Y=fake, ldy=64,
+              ws=None, ws_bytes=0):
+        return lib.q6k_mmq_f32_tc(plane, wh, M, K, X, ldx, N, Y, ldy, ws, ws_bytes,
+                                  ctypes.byref(path), None)
+
+    assert f32tc(ldx=128) == q6.Q6_EINVAL and path.value == q6.PATH_NONE
+    assert f32tc(ldy=32) == q6.Q6_EINVAL
+    assert f32tc(X=None) == q6.Q6_EINVAL
+    assert f32tc(K=100, ldx=100) == q6.Q6_EINVAL
+    assert f32tc(X=odd) == q6.Q6_EALIGN
+    assert f32tc(ldx=258) == q6.Q6_EALIGN
+    assert f32tc(wh=odd) == q6.Q6_EALIGN
+    assert f32tc(plane=odd) == q6.Q6_EALIGN
+    assert f32tc(wh=None) == q6.Q6_ESIZE                   # the unpack needs a workspace
+    assert f32tc(wh=None, ws=fake, ws_bytes=64 * 256 * 4 - 1) == q6.Q6_ESIZE
+    assert f32tc(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
+
 
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(q6.Q6Error):
