@@ -180,26 +180,33 @@ def run_reference(args):
     orc = oracle.get()
     q4 = args.workload == "q4k_ffn_down"
     gemm = orc.q4k_mmq if q4 else orc.mmq
-    # size one step (one token against `rows` weight rows) so the run takes ~1-2 min
-    probe_rows = 256
-    xq, da = orc.quantize(X[:1])
+    # One step: a batch of TB tokens (quantised in the step) against the first
+    # `rows` weight rows, so the weight decode is shared by TB tokens as in the
+    # cpu_baseline leg's sample; `rows` is sized so the run takes ~1-2 min.
+    TB = min(32, N)
+    probe_rows = 64
+    t0 = time.perf_counter()
+    xq, da = orc.quantize(X[:TB])
+    t_quant = time.perf_counter() - t0
     t0 = time.perf_counter()
     gemm(raw[:probe_rows], probe_rows, K, xq, da)
     per_row = (time.perf_counter() - t0) / probe_rows
     total_steps = args.steps + args.warmup
-    rows = int(min(M, max(1, 90.0 / max(total_steps, 1) / max(per_row, 1e-9))))
+    per_step = 90.0 / max(total_steps, 1)
+    rows = int(min(M, max(1, (per_step - t_quant) / max(per_row, 1e-9))))
     times = []
     for i in range(total_steps):
-        n = i % N
+        n = (i * TB) % N
+        Xb = X[n:n + TB] if n + TB <= N else np.concatenate([X[n:], X[:n + TB - N]])
         t0 = time.perf_counter()
-        xq, da = orc.quantize(X[n:n + 1])
+        xq, da = orc.quantize(Xb)
         gemm(raw[:rows], rows, K, xq, da)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     t = sum(times)
-    ops = 2.0 * rows * K * len(times)
+    ops = 2.0 * rows * K * TB * len(times)
     value = ops / t / 1e12
-    sample = f"{len(times)} steps of 1 token x {rows} of {M} weight rows, K={K}"
+    sample = f"{len(times)} steps of {TB} tokens x {rows} of {M} weight rows, K={K}"
     line = {
         "impl": "reference", "metric": Q4K_METRIC if q4 else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / max(len(times), 1),
