@@ -61,6 +61,7 @@ def separate(q6, W, Xd, source):
 
 SHAPES = [(256, 512, 130), (300, 768, 257),   # ragged weight band and token tile
           (1016, 768, 2555),                  # the split last round of tiles
+          (1016, 512, 2555),                  # split halves of one super-block each
           (4096, 1024, 700), (128, 256, 129)]
 
 

@@ -151,6 +151,7 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
 
 Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 17), (200, 768, 129), (384, 768, 300),
              (1016, 768, 2555),    # the split last round of tiles, ragged band and tile
+             (1016, 512, 2555),    # split halves of one super-block each (one min pair group)
              (3001, 512, 40)]
 
 
