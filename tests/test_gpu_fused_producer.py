@@ -83,7 +83,8 @@ def test_fused_equals_separate_and_oracle(q6, orc, M, K, N, source):
     import torch
     assert torch.equal(Y, Ys), "fused quantiser differs from quantize_act + mmq"
     xq_o, da_o = orc.quantize(X)
-    Yo = orc.mmq(raw, M, K, xq_o, da_o) if N * M * K <= 1 << 30 else orc.mmq_all(raw, M, K, xq_o, da_o)
+    small = N * M * K <= 1 << 30
+    Yo = orc.mmq(raw, M, K, xq_o, da_o) if small else orc.mmq_all(raw, M, K, xq_o, da_o)
     check_y(host(Y), Yo, f"fused {M}x{K}x{N} {source}")
 
 
