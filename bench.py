@@ -938,6 +938,7 @@ def other_configs(args, q6, synth, device, hbm):
         res[f"skinny_{k}"] = v
     res.update(pages_shapes(q6, synth, device))
     res["q4k_ffn_down"] = q4k_gemm(q6, synth, device)
+    res["q4k_pages_ffn_up"] = q4k_gemm(q6, synth, device, "pages_ffn_up")
     res["sweep"] = sweep_short(q6, synth, device)
     return res
 
@@ -992,13 +993,14 @@ def pages_shapes(q6, synth, device):
     return out
 
 
-def q4k_gemm(q6, synth, device):
-    """The q4_K GEMM at the ffn_down shape (4096 x 11008, N = 3314, the same
-    activations): the GEMM on the resident operand plane, the call from the
-    packed plane (unpack + GEMM) and the quantiser with block sums, each
-    averaged over back-to-back calls."""
+def q4k_gemm(q6, synth, device, name="ffn_down"):
+    """The q4_K GEMM at a workload's shape (ffn_down 4096 x 11008, N = 3314;
+    or the pages' q4_K FFN up projection 18944 x 3584, N = 3325): the GEMM on
+    the resident operand plane, the call from the packed plane (unpack +
+    GEMM) and the quantiser with block sums, each averaged over back-to-back
+    calls."""
     import torch
-    raw, X, cfg = synth.q4k_workload("ffn_down")
+    raw, X, cfg = synth.q4k_workload(name)
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     W = q6.q4k_pack_weights(torch.from_numpy(raw).to(device), M, K, wq=True)
     Xd = torch.from_numpy(X).to(device)

@@ -40,6 +40,7 @@ WORKLOAD_SEED = {
     "sweep": 0x51360004,
     "pages_ffn_down": 0x51360005,
     "pages_attn_v": 0x51360006,
+    "pages_ffn_up": 0x51360007,
 }
 SWEEP_SEED = 0x51364000
 
@@ -52,6 +53,9 @@ WORKLOADS = {
     # 512-wide grouped V projection) at their ~3325-token prefill
     "pages_ffn_down": dict(M=3584, K=18944, N=3325, outlier_frac=0.01),
     "pages_attn_v": dict(M=512, K=3584, N=3325, outlier_frac=0.0),
+    # the pages' model is q4_k_m: its FFN gate/up projections (18944 x 3584)
+    # are q4_K weights (q4k_workload)
+    "pages_ffn_up": dict(M=18944, K=3584, N=3325, outlier_frac=0.01),
 }
 SKINNY_SHAPES = {"ffn_down": (4096, 11008), "attn_v": (4096, 4096)}
 SKINNY_N = (1, 2, 4, 16)
@@ -190,8 +194,10 @@ Q4K_SEED = 0x51361401
 def q4k_workload(name: str = "ffn_down"):
     """(raw q4_K weights, f32 activations, shape dict): the named workload's
     shape and activation stream with q4_K weights in place of q6_K."""
-    _, x, cfg = workload(name)
-    return q4k_raw_weights(Q4K_SEED, cfg["M"], cfg["K"]), x, cfg
+    cfg = WORKLOADS[name]
+    x = activations(WORKLOAD_SEED[name], cfg["N"], cfg["K"], cfg["outlier_frac"])
+    seed = Q4K_SEED ^ (WORKLOAD_SEED[name] - WORKLOAD_SEED["ffn_down"])
+    return q4k_raw_weights(seed, cfg["M"], cfg["K"]), x, dict(cfg)
 
 
 def skinny_workload(weight: str, n: int):

@@ -199,6 +199,20 @@ def test_q4k_degenerate(q6, orc):
         check_y(host(Y), Yo, label)
 
 
+def test_q4k_pages_ffn_up_full(q6, orc):
+    """The pages' model is q4_k_m: its FFN up projection (18944 x 3584) in
+    q4_K against the 3325-token prefill stream, every output within
+    tolerance of the oracle, from the resident operand plane."""
+    raw, X, cfg = synth.q4k_workload("pages_ffn_up")
+    M, K = cfg["M"], cfg["K"]
+    w = q6.q4k_pack_weights(dev(raw), M, K, wq=True)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    Y, path, _ = q6.q4k_mmq(w, act, source="wq")
+    q6.sync_status()
+    assert path == "q4k_tc_wq"
+    check_y(host(Y), orc.q4k_mmq_all(raw, M, K, xq_o, da_o), "q4k pages ffn_up")
+
+
 def test_q4k_ffn_down_full(q6, orc):
     """q4_K weights of the ffn_down shape (4096 x 11008) against its 3314-token
     activation stream: every output within tolerance of the oracle (run over
