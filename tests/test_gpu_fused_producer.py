@@ -88,6 +88,29 @@ def test_fused_equals_separate_and_oracle(q6, orc, M, K, N, source):
     check_y(host(Y), Yo, f"fused {M}x{K}x{N} {source}")
 
 
+def _fused_sweep_shapes(count=8, seed=0x5EEDF):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 3000)), 256 * int(rng.integers(1, 25)),
+             int(rng.integers(17, 2700))) for _ in range(count)]
+
+
+@pytest.mark.parametrize("M,K,N", _fused_sweep_shapes(), ids=lambda v: str(v))
+def test_fused_seeded_shape_sweep(q6, orc, M, K, N):
+    """Seeded irregular shapes: bit for bit the separate path, and within
+    tolerance of the oracle."""
+    import torch
+    raw = synth.q6k_raw_weights(0x51362301 + M + K + N, M, K)
+    X = synth.activations(0x51362302 + M + K + N, N, K, outlier_frac=0.01)
+    W = q6.pack_weights(dev(raw), M, K)
+    Xd = dev(X)
+    Y, _ = q6.mmq_f32_tc(W, Xd, source="raw")
+    Ys, _ = separate(q6, W, Xd, "raw")
+    q6.sync_status()
+    assert torch.equal(Y, Ys)
+    xq_o, da_o = orc.quantize(X)
+    check_y(host(Y), orc.mmq_all(raw, M, K, xq_o, da_o), f"fused sweep {M}x{K}x{N}")
+
+
 @pytest.mark.parametrize("N", [1, 5, 16])
 def test_fused_few_tokens_against_oracle(q6, orc, N):
     """Small N runs the tensor-core kernel with one ragged token tile (the

@@ -177,6 +177,41 @@ def test_q4k_mmq_small(q6, orc, M, K, N, source):
     check_y(host(Y2), Yo, f"q4k {M}x{K}x{N} {source} fast")
 
 
+def _q4k_sweep_shapes(count=12, seed=0x5EED4):
+    """Seeded irregular shapes: ragged M and N, 1..24 super-blocks per row,
+    token counts from one to several rounds of tiles (some with the split
+    last round)."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for i in range(count):
+        N = int([rng.integers(1, 17), rng.integers(17, 700), rng.integers(700, 2700)][i % 3])
+        M = int(rng.integers(1, 3000))
+        K = 256 * int(rng.integers(1, 25))
+        shapes.append((M, K, N))
+    return shapes
+
+
+@pytest.mark.parametrize("M,K,N", _q4k_sweep_shapes(), ids=lambda v: str(v))
+def test_q4k_seeded_shape_sweep(q6, orc, M, K, N):
+    """Y within tolerance on every output of seeded irregular shapes (from
+    the packed plane), and bit-exact sub-block partials where they stay
+    small."""
+    raw = synth.q4k_raw_weights(0x51361501 + M + K + N, M, K)
+    X = synth.activations(0x51361502 + M + K + N, N, K, outlier_frac=0.01)
+    w = q6.q4k_pack_weights(dev(raw), M, K)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    want_p = N * M * (K // 32) <= 20_000_000
+    Y, path, P = q6.q4k_mmq(w, act, source="raw", partials=want_p)
+    q6.sync_status()
+    assert path == "q4k_tc_raw"
+    if want_p:
+        Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
+        assert np.array_equal(host(P), Po), "sub-block partials differ"
+    else:
+        Yo = orc.q4k_mmq_all(raw, M, K, xq_o, da_o)
+    check_y(host(Y), Yo, f"q4k sweep {M}x{K}x{N}")
+
+
 def test_q4k_degenerate(q6, orc):
     """All nibbles 0 leave only the min term; dmin = 0 leaves only the scale
     term; d = dmin = 0 gives Y = 0."""
