@@ -483,6 +483,34 @@ def skinny_kernel_times(q6, synth, device, iters: int = 10):
     return out
 
 
+def q4k_skinny_times(q6, synth, device, iters: int = 10):
+    """The q4_K few-token kernel on q4_K weights of the ffn_down shape for
+    N = 1, 4, 12, weights rotated over copies totalling more than 4x L2,
+    timed by CUDA-graph replay; GB/s of the method's bytes (q4_K weights at
+    144 B per 256, int8 activations, da and block sums, f32 Y)."""
+    import torch
+    out = {}
+    M, K = synth.SKINNY_SHAPES["ffn_down"]
+    raw = synth.q4k_raw_weights(synth.Q4K_SEED, M, K)
+    raw_d = torch.from_numpy(raw).to(device)
+    R = max(4, (4 * 129 * 2 ** 20) // q6.q4k_plane_bytes(M, K)[0] + 1)
+    Ws = [q6.q4k_pack_weights(raw_d, M, K) for _ in range(R)]
+    del raw_d
+    for n in (1, 4, 12):
+        X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
+        act = q6.quantize_act(torch.from_numpy(X).to(device), want_xh=False, want_us=True)
+        Y = torch.empty((n, M), dtype=torch.float32, device=device)
+        for i in range(2 * R):
+            q6.q4k_mmq(Ws[i % R], act, Y=Y)
+        us = graph_ms(lambda i: q6.q4k_mmq(Ws[i % R], act, Y=Y), iters * R) * 1e3
+        q6.sync_status()
+        gbs = q4k_method_bytes(M, K, n) / us / 1e3
+        out[f"ffn_down_N{n}"] = {"us": us, "gbs": gbs, "weight_copies": R,
+                                 "path": q6.q4k_mmq(Ws[0], act, Y=Y)[1]}
+    del Ws
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -936,6 +964,9 @@ def other_configs(args, q6, synth, device, hbm):
     for k, v in skinny_kernel_times(q6, synth, device).items():
         v["frac_hbm"] = v["gbs"] / hbm
         res[f"skinny_{k}"] = v
+    for k, v in q4k_skinny_times(q6, synth, device).items():
+        v["frac_hbm"] = v["gbs"] / hbm
+        res[f"q4k_skinny_{k}"] = v
     res.update(pages_shapes(q6, synth, device))
     res["q4k_ffn_down"] = q4k_gemm(q6, synth, device)
     res["q4k_pages_ffn_up"] = q4k_gemm(q6, synth, device, "pages_ffn_up")

@@ -62,6 +62,13 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_Q4K_TC_WQ 8  /* q4_K: tensor-core GEMM on a resident binary16 operand plane */
 #define Q6_PATH_TC_FUSED_RAW 9 /* q6k_mmq_f32_tc: unpack into the workspace + GEMM quantising X itself */
 #define Q6_PATH_TC_FUSED_WH 10 /* q6k_mmq_f32_tc: GEMM quantising X itself, resident operand planes */
+#define Q6_PATH_Q4K_SKINNY 11  /* q4_K: few-token dp4a kernel on the packed plane */
+
+/* q4k_mmq runs N <= Q6_Q4K_SKINNY_MAX_N on the few-token kernel (measured on
+ * GB300, q4_K weights of 4096 x 11008: 9.1 / 26.3 / 77.1 us at 1 / 4 / 12
+ * tokens against about 105 us on the tensor cores from the packed plane and
+ * 81 us from the resident operand plane, nearly flat up to 64 tokens). */
+#define Q6_Q4K_SKINNY_MAX_N 12
 
 #define Q6_SKINNY_MAX_N 16
 #define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
@@ -364,7 +371,9 @@ int q6k_mmq_f32_tc(const void *plane, const uint16_t *wh, int M, int K, const fl
  *      [K/256][ldm] (d, transposed, ldm = M rounded up to 4), mv f32
  *      [M][ldus] (dmin * m of every sub-block, at most 17 significant bits,
  *      as the exact pair hi + lo in the layout of the activations' us, see
- *      q8_quantize_act_sums; ldus = 32 * ceil(K / 512)); padding is zero.
+ *      q8_quantize_act_sums; ldus = 32 * ceil(K / 512)), ddm f32 [M][K/256][2]
+ *      ((d, dmin) of every super-block, for the few-token kernel); padding
+ *      is zero.
  * wq (device, optional, 16-byte aligned): the binary16 operand plane [M][K]
  *      the tensor-core GEMM reads, sc * q (at most 945: exact).
  * -------------------------------------------------------------------- */
@@ -379,25 +388,32 @@ int q4k_pack_weights(const uint8_t *raw, int M, int K, void *plane, uint16_t *wq
 /* The unpack pass alone: wq [M][K] from the packed plane. */
 int q4k_unpack_weights(const void *plane, int M, int K, uint16_t *wq, q6_stream_t s);
 
-/* The q4_K GEMM on the tensor cores, for any N >= 0 (there is no few-token
- * kernel for q4_K; small N run as one ragged token tile).
+/* The q4_K GEMM. N > Q6_Q4K_SKINNY_MAX_N runs on the tensor cores; fewer
+ * tokens run a weight-streaming dp4a kernel on the packed plane (about 0.59
+ * byte per weight; wq and the workspace are not used).
  *   plane : the packed q4_K plane (required); wq : resident operand plane or
  *           NULL (then it is unpacked into the workspace first).
- *   Xh, da, us : from q8_quantize_act_sums (binary16 codes, scales, block-sum
- *           pairs). The min term sum_c us * (dmin * m) runs on the tensor cores
- *           as kind::tf32 products of the hi/lo pairs (each product exact in
- *           f32; us's pair is within 2^-21 |us| of it).
- *   workspace : device, 256-byte aligned, at least 2 * M * K bytes when wq is
- *           NULL or partials is not NULL; contents afterwards unspecified.
+ *   Xq, Xh, da, us : from q8_quantize_act_sums (int8 codes, binary16 codes,
+ *           scales, block-sum pairs); Xq is required for N <=
+ *           Q6_Q4K_SKINNY_MAX_N and Xh for more tokens. On the tensor cores the min term sum_c us * (dmin * m)
+ *           runs as kind::tf32 products of the hi/lo pairs (each product
+ *           exact in f32; us's pair is within 2^-21 |us| of it); the
+ *           few-token kernel adds each pair back to us (exact).
+ *   workspace : device, 256-byte aligned, at least 2 * M * K bytes on the
+ *           tensor-core path when wq is NULL or partials is not NULL; contents
+ *           afterwards unspecified.
  *   partials : NULL, or device int32 [N][M][K/32] that receives every exact
- *           P = sum over a sub-block of q * xq (debug: one more GEMM launch on
- *           the plane of the raw nibbles, unpacked in the workspace).
- *   path_out : NULL or receives Q6_PATH_Q4K_TC_RAW / Q6_PATH_Q4K_TC_WQ.
- * Alignment: plane, workspace 256 B; Xh, da, us, wq 16 B; Y, partials 4 B.
+ *           P = sum over a sub-block of q * xq (debug: on the tensor cores one
+ *           more GEMM launch on the plane of the raw nibbles, unpacked in the
+ *           workspace; the few-token kernel writes them from its dot products).
+ *   path_out : NULL or receives Q6_PATH_Q4K_TC_RAW / Q6_PATH_Q4K_TC_WQ /
+ *           Q6_PATH_Q4K_SKINNY.
+ * Alignment: plane, workspace 256 B; Xq, Xh, da, us, wq 16 B; Y, partials 4 B.
  * Errors as for q6k_mmq. */
-int q4k_mmq(const void *plane, const uint16_t *wq, int M, int K, const uint16_t *Xh,
-            const float *da, const float *us, int N, float *Y, int ldy, void *workspace,
-            size_t workspace_bytes, int32_t *partials, int *path_out, q6_stream_t s);
+int q4k_mmq(const void *plane, const uint16_t *wq, int M, int K, const int8_t *Xq,
+            const uint16_t *Xh, const float *da, const float *us, int N, float *Y, int ldy,
+            void *workspace, size_t workspace_bytes, int32_t *partials, int *path_out,
+            q6_stream_t s);
 
 #ifdef __cplusplus
 }

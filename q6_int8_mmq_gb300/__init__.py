@@ -20,13 +20,14 @@ LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
 Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
 (PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH, PATH_SYNC_WEXP,
  PATH_SKINNY_FUSED, PATH_Q4K_TC_RAW, PATH_Q4K_TC_WQ, PATH_TC_FUSED_RAW,
- PATH_TC_FUSED_WH) = range(11)
+ PATH_TC_FUSED_WH, PATH_Q4K_SKINNY) = range(12)
 PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh", PATH_SYNC_WEXP: "sync_wexp",
               PATH_SKINNY_FUSED: "skinny_fused", PATH_Q4K_TC_RAW: "q4k_tc_raw",
               PATH_Q4K_TC_WQ: "q4k_tc_wq", PATH_TC_FUSED_RAW: "tc_fused_raw",
-              PATH_TC_FUSED_WH: "tc_fused_wh"}
+              PATH_TC_FUSED_WH: "tc_fused_wh", PATH_Q4K_SKINNY: "q4k_skinny"}
 SKINNY_MAX_N = 16
+Q4K_SKINNY_MAX_N = 12
 FUSED_MAX_N = 2
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).
@@ -56,7 +57,8 @@ SIGNATURES = [
     ("q4k_plane_bytes", _I, [_I, _I, _SZ, _SZ]),
     ("q4k_pack_weights", _I, [_P, _I, _I, _P, _P, _P]),
     ("q4k_unpack_weights", _I, [_P, _I, _I, _P, _P]),
-    ("q4k_mmq", _I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP, _P]),
+    ("q4k_mmq", _I, [_P, _P, _I, _I, _P, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _IP,
+                     _P]),
 ]
 
 
@@ -550,16 +552,20 @@ def q4k_unpack_weights(w: Q4Weights, out=None, stream=None):
 
 def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",
             partials: bool = False, workspace=None, stream=None):
-    """Y [N, M] f32 = the q4_K x int8 GEMM (tensor cores, any N). act needs xh,
-    da and us (quantize_act(..., want_us=True)). source: "raw" (unpack the
-    packed plane per call), "wq" (the resident operand plane) or "auto".
-    Returns (Y, path name, partials [N, M, K/32] int32 or None)."""
+    """Y [N, M] f32 = the q4_K x int8 GEMM. act needs da and us
+    (quantize_act(..., want_us=True)), and xq for N <= Q4K_SKINNY_MAX_N (the
+    few-token kernel on the packed plane) or xh for more tokens (the tensor
+    cores). source (tensor cores): "raw" (unpack the packed plane per call),
+    "wq" (the resident operand plane) or "auto". Returns (Y, path name,
+    partials [N, M, K/32] int32 or None)."""
     import torch
     N, M, K = act.N, w.M, w.K
     if act.K != K:
         raise Q6Error(Q6_EINVAL, "activation K does not match the weight")
-    if act.xh is None or act.us is None:
-        raise Q6Error(Q6_EINVAL, "the q4_K GEMM needs activations with xh and us")
+    skinny = N <= Q4K_SKINNY_MAX_N
+    if act.us is None or (skinny and act.xq is None) or (not skinny and act.xh is None):
+        raise Q6Error(Q6_EINVAL, "the q4_K GEMM needs activations with us, and xq for "
+                                 f"N <= {Q4K_SKINNY_MAX_N} or xh for more tokens")
     if source == "auto":
         source = "wq" if w.wq is not None else "raw"
     if source == "wq" and w.wq is None:
@@ -572,14 +578,14 @@ def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
     _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
     P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
-    need = 2 * M * K if (wq is None or partials) else 0
+    need = 2 * M * K if (not skinny and (wq is None or partials)) else 0
     if workspace is not None:
         _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
                 tuple(getattr(workspace, "shape", ())), dev)
     ws = workspace if workspace is not None else (_workspace(need, dev) if need else None)
     ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     path = ctypes.c_int(-1)
-    _check(load().q4k_mmq(_ptr(w.plane), _ptr(wq), M, K, _ptr(act.xh), _ptr(act.da),
-                          _ptr(act.us), N, _ptr(Y), _row_stride(Y), _ptr(ws), ws_bytes, _ptr(P),
-                          ctypes.byref(path), _stream(stream)))
+    _check(load().q4k_mmq(_ptr(w.plane), _ptr(wq), M, K, _ptr(act.xq), _ptr(act.xh),
+                          _ptr(act.da), _ptr(act.us), N, _ptr(Y), _row_stride(Y), _ptr(ws),
+                          ws_bytes, _ptr(P), ctypes.byref(path), _stream(stream)))
     return Y, PATH_NAMES.get(path.value, str(path.value)), P

@@ -590,22 +590,35 @@ int q4k_unpack_weights(const void* plane, int M, int K, uint16_t* wq, q6_stream_
   return Q6_OK;
 }
 
-int q4k_mmq(const void* plane, const uint16_t* wq, int M, int K, const uint16_t* Xh,
-            const float* da, const float* us, int N, float* Y, int ldy, void* workspace,
-            size_t workspace_bytes, int32_t* partials, int* path_out, q6_stream_t s) {
+int q4k_mmq(const void* plane, const uint16_t* wq, int M, int K, const int8_t* Xq,
+            const uint16_t* Xh, const float* da, const float* us, int N, float* Y, int ldy,
+            void* workspace, size_t workspace_bytes, int32_t* partials, int* path_out,
+            q6_stream_t s) {
   if (path_out) *path_out = Q6_PATH_NONE;
   if (M <= 0 || K <= 0 || K % 256 || N < 0)
     return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0");
   if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
   if (N == 0) return Q6_OK;
-  if (!plane || !Xh || !da || !us || !Y)
-    return fail(Q6_EINVAL, "plane, Xh, da, us and Y are required");
-  if (!aligned(plane, 256) || !aligned(Xh, 16) || !aligned(da, 16) || !aligned(us, 16) ||
-      !aligned(Y, 4) || (wq && !aligned(wq, 16)) || (partials && !aligned(partials, 4)) ||
-      (workspace && !aligned(workspace, 256)))
-    return fail(Q6_EALIGN, "plane, workspace 256 B; Xh, da, us, wq 16 B; Y, partials 4 B");
+  const bool skinny = N <= Q6_Q4K_SKINNY_MAX_N;
+  if (!plane || !da || !us || !Y) return fail(Q6_EINVAL, "plane, da, us and Y are required");
+  if (skinny && !Xq) return fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_Q4K_SKINNY_MAX_N);
+  if (!skinny && !Xh) return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_Q4K_SKINNY_MAX_N);
+  if (!aligned(plane, 256) || (Xq && !aligned(Xq, 16)) || (Xh && !aligned(Xh, 16)) ||
+      !aligned(da, 16) || !aligned(us, 16) || !aligned(Y, 4) || (wq && !aligned(wq, 16)) ||
+      (partials && !aligned(partials, 4)) || (workspace && !aligned(workspace, 256)))
+    return fail(Q6_EALIGN, "plane, workspace 256 B; Xq, Xh, da, us, wq 16 B; Y, partials 4 B");
   if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
     return fail(Q6_ESIZE, "problem too large");
+  if (skinny) {
+    DevState* st;
+    int rc = device_state(&st);
+    if (rc) return rc;
+    cudaError_t e = q6::launch_q4k_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da,
+                                          ldda_of(N), us, N, Y, ldy, partials, (cudaStream_t)s);
+    if (e != cudaSuccess) return cuda_fail(e, "q4_K few-token kernel launch");
+    if (path_out) *path_out = Q6_PATH_Q4K_SKINNY;
+    return Q6_OK;
+  }
   if (!wq || partials) {
     const size_t need = (size_t)M * (size_t)K * 2;
     if (!workspace || workspace_bytes < need)

@@ -24,7 +24,9 @@
 //         parts of its 8 chunks at 16 b .. 16 b + 7 and the lo parts at
 //         16 b + 8 .. 16 b + 15; an odd super-block count leaves 16 zeros at
 //         the end of each row. The GEMM's min term runs on the tensor cores
-//         from these pairs (kind::tf32).
+//         from these pairs (kind::tf32);
+//   ddm : float2 [M][K/256], (d, dmin) of each super-block as f32 (exact),
+//         row-major, for the few-token kernel.
 // Operand plane (the unpack): binary16 [M][K], sc[j] * q (at most 63 * 15 =
 // 945, exact), or with unit scale q alone (the debug partials).
 #include "q6_internal.cuh"
@@ -71,6 +73,10 @@ __global__ void __launch_bounds__(256) q4k_pack_kernel(const uint8_t* __restrict
     } else if (lane == 8) {
       reinterpret_cast<float*>(plane + g.dt_off)[(size_t)b * g.ldm + m] =
           __half2float(__ushort_as_half((unsigned short)(src[0] | (src[1] << 8))));
+    } else if (lane == 9) {
+      reinterpret_cast<float2*>(plane + g.ddm_off)[i] =
+          make_float2(__half2float(__ushort_as_half((unsigned short)(src[0] | (src[1] << 8)))),
+                      __half2float(__ushort_as_half((unsigned short)(src[2] | (src[3] << 8)))));
     }
   }
   // rows M .. ldm-1 of the transposed d sub-plane, and the gaps between sub-planes
@@ -83,11 +89,12 @@ __global__ void __launch_bounds__(256) q4k_pack_kernel(const uint8_t* __restrict
     reinterpret_cast<float*>(plane + g.dt_off)[(size_t)r * g.ldm + col] = 0.0f;
   }
   if (blockIdx.x == 0) {
-    const size_t ends[5] = {(size_t)M * (K / 2), g.sc_off + (size_t)M * (K / 32),
+    const size_t ends[6] = {(size_t)M * (K / 2), g.sc_off + (size_t)M * (K / 32),
                             g.mn_off + (size_t)M * (K / 32), g.dt_off + (size_t)nsb * g.ldm * 4,
-                            g.mv_off + (size_t)M * q4_min_ld(K) * 4};
-    const size_t starts[5] = {g.sc_off, g.mn_off, g.dt_off, g.mv_off, g.total};
-    for (int r = 0; r < 5; ++r)
+                            g.mv_off + (size_t)M * q4_min_ld(K) * 4,
+                            g.ddm_off + (size_t)nblk * 8};
+    const size_t starts[6] = {g.sc_off, g.mn_off, g.dt_off, g.mv_off, g.ddm_off, g.total};
+    for (int r = 0; r < 6; ++r)
       for (size_t j = ends[r] + threadIdx.x; j < starts[r]; j += blockDim.x) plane[j] = 0;
   }
 }

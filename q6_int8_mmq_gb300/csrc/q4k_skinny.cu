@@ -1,0 +1,192 @@
+// q4_K x int8 GEMM for a few tokens: a weight-streaming kernel on the CUDA
+// cores, bound by HBM (0.59 byte per weight: the 0.5-byte nibbles, the 6-bit
+// scale and min bytes of each 32-element sub-block and the f32 (d, dmin) of
+// each super-block).
+//
+// Math ("r18: Load-time B pre-expansion", Sec. 1 and 3.2; "r38 -- q6_K
+// BT-style raw-byte mma kernel", Sec. 2.2): for sub-block c of token n,
+//   Y += da[c] * d * sc[c] * P  -  dmin * m[c] * us[c],
+// P = sum over the 32 elements of q * xq (q the raw nibble 0..15, exact
+// with dp4a), us = da * (sum of the block's codes) from the quantiser.
+//
+// Row dot product: one warp per weight row; per step a warp covers four
+// super-blocks, eight lanes per super-block. Lane (p, h) of a super-block
+// reads the 16 nibble bytes at 32 p + 16 h of its 128: their low nibbles
+// are elements 16 h .. 16 h + 15 of sub-block 2 p and their high nibbles the
+// same elements of sub-block 2 p + 1, so each lane forms half of two
+// sub-blocks' P with four dp4a each; the lane with h = 0 also subtracts the
+// two sub-blocks' min terms. The loads of the next step are in flight while
+// a step is computed (two register buffers used in turn), warps stride over
+// the rows with the grid sized to one resident wave. Each token repeats its
+// dot products and re-reads its activations for every row (from L1), so the
+// time grows by about 6 us a token on 4096 x 11008 weights; beyond
+// Q6_Q4K_SKINNY_MAX_N tokens the tensor cores, which share each activation
+// fragment across rows, are faster.
+#include "q6_internal.cuh"
+
+namespace q6 {
+namespace {
+
+constexpr int kWarps = 4;      // warps per CTA
+constexpr int kMinBlocks = 8;  // resident CTAs per SM (64 registers per thread)
+
+// c + sum over the four byte pairs of a (unsigned) times b (signed).
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// One step of a row as a lane holds it: 16 nibble bytes, the two sub-blocks'
+// scale and min bytes, and the super-block's (d, dmin).
+struct Step {
+  uint4 L;
+  uint32_t sc, mn;  // bytes of sub-blocks 2p, 2p + 1 in bits 0-7, 8-15
+  float2 dd;
+};
+
+template <bool kPartials, int kMaxN>
+__global__ void __launch_bounds__(kWarps * 32, kMinBlocks) q4k_skinny_kernel(
+    const uint8_t* __restrict__ plane, Q4Geom g, int M, int K, const int8_t* __restrict__ Xq,
+    const float* __restrict__ da, int ldda, const float* __restrict__ us, int N,
+    float* __restrict__ Y, int ldy, int32_t* __restrict__ partials) {
+  const int lane = threadIdx.x & 31;
+  const int nsb = K / 256, nc = K / 32, ldus = q4_min_ld(K);
+  const int sbi = lane >> 3;            // super-block within the step
+  const int p = (lane >> 1) & 3, h = lane & 1;
+  const int warps = (int)gridDim.x * kWarps;
+  for (int m = (threadIdx.x >> 5) * (int)gridDim.x + blockIdx.x; m < M; m += warps) {
+    const uint8_t* qs = plane + g.qs_off + (size_t)m * (K / 2);
+    const uint8_t* scr = plane + g.sc_off + (size_t)m * nc;
+    const uint8_t* mnr = plane + g.mn_off + (size_t)m * nc;
+    const float2* ddr = reinterpret_cast<const float2*>(plane + g.ddm_off) + (size_t)m * nsb;
+    float acc[kMaxN];
+#pragma unroll
+    for (int n = 0; n < kMaxN; ++n) acc[n] = 0.0f;
+
+    auto load = [&](int sb, Step& r) {
+      r.L = make_uint4(0, 0, 0, 0);
+      r.sc = r.mn = 0;
+      r.dd = make_float2(0.0f, 0.0f);
+      if (sb < nsb) {
+        r.L = __ldg(reinterpret_cast<const uint4*>(qs + (size_t)sb * 128 + 32 * p + 16 * h));
+        r.sc = __ldg(reinterpret_cast<const uint16_t*>(scr + 8 * sb + 2 * p));
+        r.mn = __ldg(reinterpret_cast<const uint16_t*>(mnr + 8 * sb + 2 * p));
+        r.dd = __ldg(ddr + sb);
+      }
+    };
+    auto step = [&](int sb, const Step& r) {
+      // lanes of a super-block past the end compute nothing but still take
+      // the (full-warp) shuffles of the debug partials
+      const bool valid = sb < nsb;
+      const int ca = 8 * sb + 2 * p;  // sub-blocks ca (low nibbles) and ca + 1 (high)
+      const uint32_t Lw[4] = {r.L.x, r.L.y, r.L.z, r.L.w};
+      const float sca = (float)(r.sc & 0xFF), scb = (float)(r.sc >> 8);
+      const float mna = (float)(r.mn & 0xFF), mnb = (float)(r.mn >> 8);
+#pragma unroll
+      for (int n = 0; n < kMaxN; ++n) {
+        if (n < N) {
+          int pa = 0, pb = 0;
+          if (valid) {
+            const int8_t* xr = Xq + (size_t)n * K + 32 * ca + 16 * h;
+            const uint4 xa = __ldg(reinterpret_cast<const uint4*>(xr));
+            const uint4 xb = __ldg(reinterpret_cast<const uint4*>(xr + 32));
+            const uint32_t Xa[4] = {xa.x, xa.y, xa.z, xa.w}, Xb[4] = {xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              pa = dp4a_us(Lw[w] & 0x0F0F0F0Fu, Xa[w], pa);
+              pb = dp4a_us((Lw[w] >> 4) & 0x0F0F0F0Fu, Xb[w], pb);
+            }
+            const float daa = __ldg(da + (size_t)ca * ldda + n);
+            const float dab = __ldg(da + (size_t)(ca + 1) * ldda + n);
+            // sc * P is an integer below 2^21 in magnitude: exact in f32
+            float v = r.dd.x * fmaf(dab, scb * (float)pb, daa * (sca * (float)pa));
+            if (h == 0) {
+              // us of the two sub-blocks from their exact hi/lo pairs (the
+              // two hi parts, and the two lo parts, are adjacent)
+              const float* ur = us + (size_t)n * ldus + 16 * sb + 2 * p;
+              const float2 hi = __ldg(reinterpret_cast<const float2*>(ur));
+              const float2 lo = __ldg(reinterpret_cast<const float2*>(ur + 8));
+              const float ua = hi.x + lo.x, ub = hi.y + lo.y;
+              v = fmaf(-r.dd.y, fmaf(mnb, ub, mna * ua), v);
+            }
+            acc[n] += v;
+          }
+          if (kPartials && partials) {
+            // P of the two sub-blocks: this lane's half and its neighbour's
+            const int fa = pa + __shfl_xor_sync(0xffffffffu, pa, 1);
+            const int fb = pb + __shfl_xor_sync(0xffffffffu, pb, 1);
+            if (valid && h == 0) {
+              int32_t* pr = partials + ((size_t)n * M + m) * (size_t)nc + ca;
+              pr[0] = fa;
+              pr[1] = fb;
+            }
+          }
+        }
+      }
+    };
+    Step A, B;
+    load(sbi, A);
+    for (int g0 = 0; g0 < nsb; g0 += 8) {
+      load(g0 + 4 + sbi, B);  // in flight during the step on A
+      step(g0 + sbi, A);
+      load(g0 + 8 + sbi, A);  // in flight during the step on B
+      step(g0 + 4 + sbi, B);
+    }
+#pragma unroll
+    for (int n = 0; n < kMaxN; ++n) {
+      if (n < N) {
+        float v = acc[n];
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        if (lane == 0) Y[(size_t)n * ldy + m] = v;
+      }
+    }
+  }
+}
+
+template <bool P, int kMaxN>
+cudaError_t launch_bucket(const uint8_t* plane, const Q4Geom& g, int M, int K, const int8_t* Xq,
+                          const float* da, int ldda, const float* us, int N, float* Y, int ldy,
+                          int32_t* partials, cudaStream_t s) {
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, q4k_skinny_kernel<P, kMaxN>,
+                                                         kWarps * 32, 0)))
+    return e;
+  const unsigned blocks = (unsigned)(sms * (per_sm > 0 ? per_sm : 1));
+  q4k_skinny_kernel<P, kMaxN><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, us, N,
+                                                             Y, ldy, partials);
+  return cudaGetLastError();
+}
+
+template <int kMaxN>
+cudaError_t launch_n(const uint8_t* plane, const Q4Geom& g, int M, int K, const int8_t* Xq,
+                     const float* da, int ldda, const float* us, int N, float* Y, int ldy,
+                     int32_t* partials, cudaStream_t s) {
+  return partials ? launch_bucket<true, kMaxN>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy,
+                                               partials, s)
+                  : launch_bucket<false, kMaxN>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy,
+                                                nullptr, s);
+}
+
+}  // namespace
+
+cudaError_t launch_q4k_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq,
+                              const float* da, int ldda, const float* us, int N, float* Y,
+                              int ldy, int32_t* partials, cudaStream_t s) {
+  const Q4Geom g = q4_geom(M, K);
+  if (N <= 1) return launch_n<1>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
+  if (N <= 2) return launch_n<2>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
+  if (N <= 4) return launch_n<4>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
+  if (N <= 8) return launch_n<8>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
+  static_assert(Q6_Q4K_SKINNY_MAX_N <= 12, "the largest token bucket holds 12 tokens");
+  return launch_n<12>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
+}
+
+}  // namespace q6

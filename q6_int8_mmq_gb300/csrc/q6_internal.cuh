@@ -48,7 +48,7 @@ inline PlaneGeom plane_geom(int M, int K) {
 __host__ __device__ constexpr int q4_min_ld(int K) { return 32 * ((K / 256 + 1) / 2); }
 
 struct Q4Geom {
-  size_t qs_off, sc_off, mn_off, dt_off, mv_off, total;
+  size_t qs_off, sc_off, mn_off, dt_off, mv_off, ddm_off, total;
   int ldm;  // row stride (elements) of the transposed d sub-plane: M rounded up to 4
 };
 inline Q4Geom q4_geom(int M, int K) {
@@ -60,7 +60,8 @@ inline Q4Geom q4_geom(int M, int K) {
   g.mn_off = g.sc_off + round_up(m * (k / 32), 256);
   g.dt_off = g.mn_off + round_up(m * (k / 32), 256);
   g.mv_off = g.dt_off + round_up((k / 256) * (size_t)g.ldm * 4, 256);
-  g.total = g.mv_off + round_up(m * (size_t)q4_min_ld(K) * 4, 256);
+  g.ddm_off = g.mv_off + round_up(m * (size_t)q4_min_ld(K) * 4, 256);
+  g.total = g.ddm_off + round_up(m * (k / 256) * 8, 256);
   return g;
 }
 
@@ -140,6 +141,12 @@ cudaError_t launch_mmq_tc_fused(const TcMaps& maps, int M, int K, const float* X
 // min term on the tensor cores from maps.us and maps.mv).
 cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                               const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
+// The q4_K GEMM for a few tokens (N <= Q6_Q4K_SKINNY_MAX_N): dp4a on the
+// packed plane's nibbles, Xq [N][K], da [K/32][ldda] and the block-sum pairs
+// us [N][q4_min_ld(K)]; partials (nullable) [N][M][K/32].
+cudaError_t launch_q4k_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq,
+                              const float* da, int ldda, const float* us, int N, float* Y,
+                              int ldy, int32_t* partials, cudaStream_t s);
 // Tensor maps of a q4_K GEMM call (api.cu): Xh, the operand plane wq [M][K],
 // da [K/32][ldda], the block-sum pairs us [N][q4_min_ld], and the packed q4_K
 // plane's dT and min-pair sub-planes.

@@ -147,6 +147,25 @@ def test_host_side_rejections(lib):
     assert f32tc(wh=None, ws=fake, ws_bytes=64 * 256 * 4 - 1) == q6.Q6_ESIZE
     assert f32tc(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
+    # the q4_K GEMM: Xq for N <= 16 and Xh beyond, ldy < M, K % 256, misaligned
+    # pointers, no workspace for the tensor-core unpack, the empty case
+    def q4(plane=fake, wq=None, M=64, K=256, Xq=fake, Xh=fake, da=fake, us=fake, N=4, Y=fake,
+           ldy=64, ws=None, ws_bytes=0, P=None):
+        return lib.q4k_mmq(plane, wq, M, K, Xq, Xh, da, us, N, Y, ldy, ws, ws_bytes, P,
+                           ctypes.byref(path), None)
+
+    assert q4(Xq=None) == q6.Q6_EINVAL and path.value == q6.PATH_NONE
+    assert q4(N=13, Xh=None) == q6.Q6_EINVAL
+    assert q4(us=None) == q6.Q6_EINVAL
+    assert q4(ldy=32) == q6.Q6_EINVAL
+    assert q4(K=300) == q6.Q6_EINVAL
+    assert q4(Xq=odd) == q6.Q6_EALIGN
+    assert q4(us=odd) == q6.Q6_EALIGN
+    assert q4(plane=odd) == q6.Q6_EALIGN
+    assert q4(P=odd1) == q6.Q6_EALIGN
+    assert q4(N=13) == q6.Q6_ESIZE                         # no workspace for the unpack
+    assert q4(N=0, Xq=None, Xh=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
+
 
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(q6.Q6Error):

@@ -119,9 +119,11 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
     o_dt = o_mn + r(M * nc)
     o_mv = o_dt + r(nsb * ldm * 4)
     ldus = 32 * ((nsb + 1) // 2)
-    assert plane.size == o_mv + r(M * ldus * 4)
+    o_dd = o_mv + r(M * ldus * 4)
+    assert plane.size == o_dd + r(M * nsb * 8)
     for a, b in ((M * K // 2, o_sc), (o_sc + M * nc, o_mn), (o_mn + M * nc, o_dt),
-                 (o_dt + nsb * ldm * 4, o_mv), (o_mv + M * ldus * 4, plane.size)):
+                 (o_dt + nsb * ldm * 4, o_mv), (o_mv + M * ldus * 4, o_dd),
+                 (o_dd + M * nsb * 8, plane.size)):
         assert np.all(plane[a:b] == 0)
     blocks = raw.reshape(M, nsb, 144)
     assert np.array_equal(plane[:M * K // 2].reshape(M, nsb, 128), blocks[:, :, 16:])
@@ -139,6 +141,9 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
     assert np.array_equal(mv, tf32_pairs(mv_exact.astype(np.float32)))
     pairs = mv[:, :16 * nsb].reshape(M, nsb, 2, 8).astype(np.float64)
     assert np.array_equal((pairs[:, :, 0] + pairs[:, :, 1]).reshape(M, nc), mv_exact)
+    ddm = plane[o_dd:o_dd + M * nsb * 8].view(np.float32).reshape(M, nsb, 2)
+    assert np.array_equal(ddm[:, :, 0].astype(np.float64), d)
+    assert np.array_equal(ddm[:, :, 1].astype(np.float64), dmin)
     codes = np.stack([np.concatenate([dec[m][b][0] for b in range(nsb)]) for m in range(M)])
     assert np.array_equal(host(w.wq).astype(np.int64),
                           np.repeat(sc, 32, axis=1) * codes.astype(np.int64))
@@ -149,7 +154,14 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
     assert torch.equal(wh.plane, w.plane) and torch.equal(wh.wq, w.wq)
 
 
-Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 17), (200, 768, 129), (384, 768, 300),
+def q4k_path(N, source):
+    """The path a q4_K call takes: the few-token kernel for N <= 12."""
+    return "q4k_skinny" if N <= 12 else {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source]
+
+
+Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 3), (300, 768, 12), (300, 768, 16),
+             (1001, 2816, 5),
+             (130, 1024, 17), (200, 768, 129), (384, 768, 300),
              (1016, 768, 2555),    # the split last round of tiles, ragged band and tile
              (1016, 512, 2555),    # split halves of one super-block each (one min pair group)
              (3001, 512, 40)]
@@ -164,7 +176,7 @@ def test_q4k_mmq_small(q6, orc, M, K, N, source):
     act, xq_o, da_o = quantize(q6, orc, X)
     Y, path, P = q6.q4k_mmq(w, act, source=source, partials=True)
     q6.sync_status()
-    assert path == {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source]
+    assert path == q4k_path(N, source)
     want_p = N * M * K // 32 <= 40_000_000
     if want_p:
         Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
@@ -203,7 +215,7 @@ def test_q4k_seeded_shape_sweep(q6, orc, M, K, N):
     want_p = N * M * (K // 32) <= 20_000_000
     Y, path, P = q6.q4k_mmq(w, act, source="raw", partials=want_p)
     q6.sync_status()
-    assert path == "q4k_tc_raw"
+    assert path == q4k_path(N, "raw")
     if want_p:
         Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
         assert np.array_equal(host(P), Po), "sub-block partials differ"
@@ -232,6 +244,27 @@ def test_q4k_degenerate(q6, orc):
         if label == "d and dmin 0":
             assert np.all(host(Y) == 0.0)
         check_y(host(Y), Yo, label)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 9, 12])
+def test_q4k_few_tokens_full(q6, orc, N):
+    """The few-token kernel on q4_K weights of the ffn_down shape: every
+    output within tolerance and every sub-block partial P bit-exact."""
+    _, _, cfg = synth.workload("ffn_down")
+    M, K = cfg["M"], cfg["K"]
+    raw = synth.q4k_raw_weights(0x51361601, M, K)
+    X = synth.activations(0x51361602 + N, N, K, outlier_frac=0.01)
+    w = q6.q4k_pack_weights(dev(raw), M, K)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    Y, path, P = q6.q4k_mmq(w, act, partials=True)
+    q6.sync_status()
+    assert path == "q4k_skinny"
+    Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
+    assert np.array_equal(host(P), Po), "sub-block partials differ"
+    check_y(host(Y), Yo, f"q4k few tokens N={N}")
+    Y2, _, _ = q6.q4k_mmq(w, act)
+    q6.sync_status()
+    check_y(host(Y2), Yo, f"q4k few tokens N={N} fast")
 
 
 def test_q4k_pages_ffn_up_full(q6, orc):
