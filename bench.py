@@ -485,7 +485,7 @@ def skinny_kernel_times(q6, synth, device, iters: int = 10):
 
 def q4k_skinny_times(q6, synth, device, iters: int = 10):
     """The q4_K few-token kernel on q4_K weights of the ffn_down shape for
-    N = 1, 4, 12, weights rotated over copies totalling more than 4x L2,
+    N = 1, 4, 8, weights rotated over copies totalling more than 4x L2,
     timed by CUDA-graph replay; GB/s of the method's bytes (q4_K weights at
     144 B per 256, int8 activations, da and block sums, f32 Y)."""
     import torch
@@ -496,7 +496,7 @@ def q4k_skinny_times(q6, synth, device, iters: int = 10):
     R = max(4, (4 * 129 * 2 ** 20) // q6.q4k_plane_bytes(M, K)[0] + 1)
     Ws = [q6.q4k_pack_weights(raw_d, M, K) for _ in range(R)]
     del raw_d
-    for n in (1, 4, 12):
+    for n in (1, 4, 8):
         X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
         act = q6.quantize_act(torch.from_numpy(X).to(device), want_xh=False, want_us=True)
         Y = torch.empty((n, M), dtype=torch.float32, device=device)

@@ -65,10 +65,11 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_Q4K_SKINNY 11  /* q4_K: few-token dp4a kernel on the packed plane */
 
 /* q4k_mmq runs N <= Q6_Q4K_SKINNY_MAX_N on the few-token kernel (measured on
- * GB300, q4_K weights of 4096 x 11008: 9.1 / 26.3 / 77.1 us at 1 / 4 / 12
- * tokens against about 105 us on the tensor cores from the packed plane and
- * 81 us from the resident operand plane, nearly flat up to 64 tokens). */
-#define Q6_Q4K_SKINNY_MAX_N 12
+ * GB300, q4_K weights of 4096 x 11008: 8.5 / 24.6 / 50.9 us at 1 / 4 / 8
+ * tokens against about 53 us on the tensor cores from the packed plane and
+ * 30 us from the resident operand plane, K split over the idle SMs, nearly
+ * flat up to 64 tokens). */
+#define Q6_Q4K_SKINNY_MAX_N 8
 
 #define Q6_SKINNY_MAX_N 16
 #define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
@@ -203,12 +204,17 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *           for one or two tokens, exact f16 mma.sync for 3..16 tokens; both
  *           stream the packed plane once).
  *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
- *   workspace : device scratch of at least q6k_mmq_workspace_bytes() bytes
- *           (4 * M * K, 256-byte aligned) when N > Q6_SKINNY_MAX_N and either
+ *   workspace : device scratch, 256-byte aligned, of at least
+ *           q6k_mmq_workspace_bytes() bytes when N > Q6_SKINNY_MAX_N and either
  *           wh is NULL or partials is not NULL: the weights are first unpacked
  *           there (from wexp when given, else from the packed plane) into the
- *           two binary16 operand planes, and the debug passes below reuse it.
- *           Unused otherwise. Its contents after the call are unspecified.
+ *           two binary16 operand planes (4 * M * K bytes), and the debug
+ *           passes below reuse it. After those bytes (rounded up to 256) it
+ *           may also hold the K-part partial sums of a call with few tiles
+ *           (q6k_tc_part_bytes(); with resident wh planes that is all the
+ *           workspace is used for): without room for them the call runs
+ *           unsplit, with the same Y up to rounding and slower. Its contents
+ *           after the call are unspecified.
  *   partials : NULL, or device int32 [N][M][K/16] that receives every exact
  *           sub-block partial P[n][m][s] = sum over the 16 elements k of
  *           sub-block s of (q[m][k] - 32) * xq[n][k] (the debug mode of "r38

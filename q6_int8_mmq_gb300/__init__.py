@@ -27,7 +27,7 @@ PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_Q4K_TC_WQ: "q4k_tc_wq", PATH_TC_FUSED_RAW: "tc_fused_raw",
               PATH_TC_FUSED_WH: "tc_fused_wh", PATH_Q4K_SKINNY: "q4k_skinny"}
 SKINNY_MAX_N = 16
-Q4K_SKINNY_MAX_N = 12
+Q4K_SKINNY_MAX_N = 8
 FUSED_MAX_N = 2
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).
@@ -44,6 +44,7 @@ SIGNATURES = [
     ("q6k_pack_weights", _I, [_P, _I, _I, _P, _P, _P, _P]),
     ("q6k_unpack_weights", _I, [_P, _P, _I, _I, _P, _P]),
     ("q6k_mmq_workspace_bytes", _I, [_I, _I, _I, _SZ]),
+    ("q6k_tc_part_bytes", _I, [_I, _I, _I, _SZ]),
     ("q6k_mmq_launches", _I, [_I, _I, _I, _I, _IP]),
     ("q6k_mmq", _I, [_P, _P, _P, _I, _I, _P, _P, _P, _I, _P, _I, _P, ctypes.c_size_t, _P, _P,
                      _IP, _P]),
@@ -316,6 +317,15 @@ def workspace_bytes(M: int, K: int, N: int) -> int:
     return b.value
 
 
+@functools.lru_cache(maxsize=256)
+def tc_part_bytes(M: int, K: int, N: int) -> int:
+    """Bytes of the K-part partial sums a tensor-core call of this shape uses
+    (0 when it does not split K)."""
+    b = ctypes.c_size_t()
+    _check(load().q6k_tc_part_bytes(M, K, N, ctypes.byref(b)))
+    return b.value
+
+
 def mmq_launches(M: int, K: int, N: int, has_wh: bool) -> int:
     """Kernels one q6k_mmq call launches for this shape on the current device."""
     n = ctypes.c_int()
@@ -382,7 +392,8 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
     _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
     D = _debug_buffers(N, M, K, partials, chunk_sums, dev)
-    ws_need = workspace_bytes(M, K, N) if (w16 is None or partials) else 0
+    ws_need = (workspace_bytes(M, K, N) if (w16 is None or partials)
+               else tc_part_bytes(M, K, N) if N > SKINNY_MAX_N else 0)
     if workspace is not None:
         _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
                 tuple(getattr(workspace, "shape", ())), dev)
@@ -440,7 +451,8 @@ def mmq_f32_tc(w: Weights, X, Y=None, source: str = "auto", workspace=None, wh=N
     if Y is None:
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
     _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
-    ws_need = 4 * M * K if w16 is None else 0
+    part = tc_part_bytes(M, K, N)
+    ws_need = (-(-4 * M * K // 256) * 256 + part) if w16 is None else part
     if workspace is not None:
         _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
                 tuple(getattr(workspace, "shape", ())), dev)
@@ -578,7 +590,9 @@ def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",
         Y = torch.empty((N, M), dtype=torch.float32, device=dev)
     _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
     P = torch.empty((N, M, K // 32), dtype=torch.int32, device=dev) if partials else None
-    need = 2 * M * K if (not skinny and (wq is None or partials)) else 0
+    part = tc_part_bytes(M, K, N) if not skinny else 0
+    need = ((-(-2 * M * K // 256) * 256 + part) if (not skinny and (wq is None or partials))
+            else part)
     if workspace is not None:
         _tensor(workspace, "workspace", getattr(workspace, "dtype", None),
                 tuple(getattr(workspace, "shape", ())), dev)

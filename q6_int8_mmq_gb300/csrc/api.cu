@@ -324,10 +324,44 @@ int q6k_unpack_weights(const void* plane, const int8_t* wexp, int M, int K, uint
   return Q6_OK;
 }
 
+// Bytes of the K-part partial sums a tensor-core call with few tiles uses,
+// planned for GB300's 152 SMs (independent of the device, so that it can be
+// asked anywhere); a call splits K only when its workspace holds the plan of
+// the device it runs on.
+static size_t part_bytes_bound(int M, int K, int N) {
+  const q6::TcPlan p = q6::mmq_tc_plan(M, K, N, 152, true);
+  return q6::tc_part_bytes(p, M, N);
+}
+
+int q6k_tc_part_bytes(int M, int K, int N, size_t* bytes) {
+  if (M <= 0 || K <= 0 || K % 256 || N < 0 || !bytes)
+    return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0, bytes != NULL");
+  *bytes = N > 0 ? part_bytes_bound(M, K, N) : 0;
+  return Q6_OK;
+}
+
 int q6k_mmq_workspace_bytes(int M, int K, int N, size_t* bytes) {
   if (M <= 0 || K <= 0 || K % 256 || N < 0 || !bytes)
     return fail(Q6_EINVAL, "need M > 0, N >= 0, K > 0, K %% 256 == 0, bytes != NULL");
-  *bytes = N > Q6_SKINNY_MAX_N ? (size_t)M * (size_t)K * 4 : 0;
+  *bytes = N > Q6_SKINNY_MAX_N
+               ? q6::round_up((size_t)M * (size_t)K * 4, 256) + part_bytes_bound(M, K, N)
+               : 0;
+  return Q6_OK;
+}
+
+// The K-part buffer of a tensor-core call inside the caller's workspace:
+// after the first `used` bytes (the unpacked planes), when the workspace
+// holds the device's plan; NULL otherwise (the call then runs unsplit).
+static int part_buffer(int M, int K, int N, void* workspace, size_t workspace_bytes,
+                       size_t used, float** part) {
+  *part = nullptr;
+  if (!workspace) return Q6_OK;
+  q6::TcPlan p;
+  cudaError_t e = q6::mmq_tc_plan_here(M, K, N, true, &p);
+  if (e != cudaSuccess) return cuda_fail(e, "SM count");
+  const size_t need = q6::tc_part_bytes(p, M, N), off = q6::round_up(used, 256);
+  if (need > 0 && off + need <= workspace_bytes)
+    *part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + off);
   return Q6_OK;
 }
 
@@ -373,7 +407,7 @@ int q6k_mmq_launches(int M, int K, int N, int has_wh, int* launches) {
     if ((e = cudaGetDevice(&dev)) ||
         (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
       return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
-    *launches = q6::mmq_tc_plan(M, K, N, sms).launches + (has_wh ? 0 : 1);
+    *launches = q6::mmq_tc_plan(M, K, N, sms, true).launches + (has_wh ? 0 : 1);
   }
   return Q6_OK;
 }
@@ -439,7 +473,11 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   q6::TcDebugOut tdbg;
   tdbg.out = chunk_sums;
   tdbg.stride = K / 32;
-  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, tdbg, st->status, (cudaStream_t)s);
+  float* part = nullptr;
+  if ((rc = part_buffer(M, K, N, workspace, workspace_bytes,
+                        (!wh || partials) ? (size_t)M * (size_t)K * 4 : 0, &part)))
+    return rc;
+  e = q6::launch_mmq_tc(maps, M, K, N, Y, ldy, tdbg, st->status, (cudaStream_t)s, part);
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
   if (partials &&
       (rc = tc_subblock_partials(pb, M, K, N, Xh, da, Y, ldy, static_cast<__half*>(workspace),
@@ -512,7 +550,11 @@ int q6k_mmq_f32_tc(const void* plane, const uint16_t* wh, int M, int K, const fl
   }
   q6::TcMaps maps;
   if ((rc = encode_tc_maps(&maps, pb, wop, nullptr, nullptr, M, K, N))) return rc;
-  e = q6::launch_mmq_tc_fused(maps, M, K, X, ldx, N, Y, ldy, st->status, (cudaStream_t)s);
+  float* part = nullptr;
+  if ((rc = part_buffer(M, K, N, workspace, workspace_bytes, wh ? 0 : (size_t)M * (size_t)K * 4,
+                        &part)))
+    return rc;
+  e = q6::launch_mmq_tc_fused(maps, M, K, X, ldx, N, Y, ldy, st->status, (cudaStream_t)s, part);
   if (e != cudaSuccess) return cuda_fail(e, "fused-quantiser tensor-core kernel launch");
   if (path_out) *path_out = path;
   return Q6_OK;
@@ -641,7 +683,12 @@ int q4k_mmq(const void* plane, const uint16_t* wq, int M, int K, const int8_t* X
   }
   q6::TcMaps maps;
   if ((rc = q6::encode_tc_maps_q4k(&maps, pb, wop, Xh, da, us, M, K, N))) return rc;
-  e = q6::launch_mmq_tc_q4k(maps, M, K, N, Y, ldy, q6::TcDebugOut{}, st->status, (cudaStream_t)s);
+  float* part = nullptr;
+  if ((rc = part_buffer(M, K, N, workspace, workspace_bytes,
+                        (!wq || partials) ? (size_t)M * (size_t)K * 2 : 0, &part)))
+    return rc;
+  e = q6::launch_mmq_tc_q4k(maps, M, K, N, Y, ldy, q6::TcDebugOut{}, st->status, (cudaStream_t)s,
+                            part);
   if (e != cudaSuccess) return cuda_fail(e, "q4_K tensor-core kernel launch");
   if (partials) {
     // the per-sub-block P = sum q * xq: one more launch on the plane of the

@@ -156,15 +156,24 @@ static_assert(Lay<kFmtQ6>::kXStage % 128 == 0, "staging rows keep 16-byte alignm
 // Work units: units 0 .. Tw-1 are whole tiles; when the last round of tiles
 // would leave more than half the CTAs idle, each of its tiles is split into
 // two units over the two halves of its super-blocks (units Tw + 2i and
-// Tw + 2i + 1 for tile Tw + i), which add their sums into a zeroed Y.
+// Tw + 2i + 1 for tile Tw + i), which add their sums into a zeroed Y. When
+// the tiles fill at most half of the SMs at all (few tokens or rows), every
+// tile is instead split into `splits` K parts (unit u: tile u / splits, part
+// u % splits), which store their sums to a partial-sum buffer that a second
+// kernel adds in a fixed order.
 struct Unit {
   int t, sb0, sb1;
-  bool split;
+  bool split;  // one of the two halves of a tile of the split last round
+  int part;    // K part (splits > 1)
 };
-__device__ __forceinline__ Unit unit_of(int u, int Tw, int nsb) {
-  if (u < Tw) return Unit{u, 0, nsb, false};
+__device__ __forceinline__ Unit unit_of(int u, int Tw, int nsb, int splits) {
+  if (splits > 1) {
+    const int t = u / splits, j = u - t * splits;
+    return Unit{t, nsb * j / splits, nsb * (j + 1) / splits, false, j};
+  }
+  if (u < Tw) return Unit{u, 0, nsb, false, 0};
   const int i = u - Tw, half = i & 1;
-  return Unit{Tw + (i >> 1), half ? nsb / 2 : 0, half ? nsb : nsb / 2, true};
+  return Unit{Tw + (i >> 1), half ? nsb / 2 : 0, half ? nsb : nsb / 2, true, half};
 }
 
 // Zeroes the Y blocks of the split tiles: block (i, y) clears rows 32y..32y+31
@@ -184,6 +193,21 @@ __global__ void __launch_bounds__(256) zero_split_tiles_kernel(float* __restrict
   for (int i = threadIdx.x; i < nw * (mw - mv); i += blockDim.x) {
     const int r = i / (mw - mv), c = mv + (i - r * (mw - mv));
     Y[(size_t)(n0 + r) * ldy + m0 + c] = 0.0f;
+  }
+}
+
+// Y = the sum of the K parts, added in part order (so the result does not
+// depend on which part finished first): part is [splits][N][M].
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part,
+                                                            int splits, int N, int M,
+                                                            float* __restrict__ Y, int ldy) {
+  const long long total = (long long)N * M;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int n = (int)(i / M), m = (int)(i - (long long)n * M);
+    float v = 0.0f;
+    for (int j = 0; j < splits; ++j) v += part[(size_t)j * total + i];
+    Y[(size_t)n * ldy + m] = v;
   }
 }
 
@@ -314,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmMv, int M, int K, int N, int Tw, int U,
                   float* __restrict__ Y, int ldy, int y_vec4, int32_t* __restrict__ partials,
                   int p_stride, int p_mul, int p_add, int write_y,
-                  const float* __restrict__ Xf, int ldx, unsigned int* __restrict__ status) {
+                  const float* __restrict__ Xf, int ldx, int splits, float* __restrict__ part,
+                  unsigned int* __restrict__ status) {
   using L = Lay<kFmt>;
   constexpr bool kQ4 = kFmt == kFmtQ4;
   static_assert(!(kFuseX && kQ4), "the fused quantiser serves the q6_K kernel");
@@ -378,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int gs = 0, gk = 0;  // scale / operand stages issued so far
         bool ok = true;
         for (int u = blockIdx.x; u < U && ok; u += gridDim.x) {
-          const Unit w = unit_of(u, Tw, nsb);
+          const Unit w = unit_of(u, Tw, nsb, splits);
           const int m0 = (w.t / NT) * BW, n0 = (w.t % NT) * BT;
           for (int sb = w.sb0; sb < w.sb1 && ok; ++sb) {
             {
@@ -458,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int gbase = 0;  // global index of the unit's first operand stage
         int uses = 0;   // operand stages walked (issued into my slot)
         for (int u = blockIdx.x; u < U; u += gridDim.x) {
-          const Unit w = unit_of(u, Tw, nsb);
+          const Unit w = unit_of(u, Tw, nsb, splits);
           const int nb = 4 * (w.sb1 - w.sb0);  // the unit's chunk stages
           const int nt = nb + (kQ4 ? min_stages(w) : 0);  // and its min stages
           for (int kb = (me - gbase % kNumIssuers + kNumIssuers) % kNumIssuers; kb < nt;
@@ -560,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (kFuseX && (int)blockIdx.x < U) {
       // the CTA's first four operand stages (its first super-block)
-      const Unit w0 = unit_of(blockIdx.x, Tw, nsb);
+      const Unit w0 = unit_of(blockIdx.x, Tw, nsb, splits);
       const int n0 = (w0.t % NT) * BT;
       for (int pp = 0; pp < 4; ++pp) {
         fx_issue(fx_stg0(pp), tok, Xf, ldx, N, n0 + wrow, (4 * w0.sb0 + pp) * KB + 32 * colh);
@@ -578,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the fused quantiser, every thread still takes every quantisation step,
     // so that its barrier stays paired too).
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
-      const Unit w = unit_of(u, Tw, nsb);
+      const Unit w = unit_of(u, Tw, nsb, splits);
       const int m0 = (w.t / NT) * BW, n0 = (w.t % NT) * BT;
       const int n = n0 + tok;
       const int mcol = m0 + 64 * colh;
@@ -600,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int un = u + (int)gridDim.x;
           fx_on = un < U;
           if (fx_on) {
-            const Unit wn = unit_of(un, Tw, nsb);
+            const Unit wn = unit_of(un, Tw, nsb, splits);
             fx_sb = wn.sb0;
             fx_n0 = (wn.t % NT) * BT;
           }
@@ -704,10 +729,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ok && n < N && write_y) {
-        float* yr = Y + (size_t)n * ldy + mcol;
+        // a K part stores its sums to its slice of the partial-sum buffer
+        // [splits][N][M] (row stride M, 16-byte aligned rows when M % 4 == 0)
+        const bool to_part = splits > 1;
+        float* yr = to_part ? part + ((size_t)w.part * N + n) * (size_t)M + mcol
+                            : Y + (size_t)n * ldy + mcol;
+        const int vec4 = to_part ? ((M & 3) == 0) : y_vec4;
         const int mleft = M - mcol;
         if (!w.split) {
-          if (y_vec4 && mleft >= 64) {
+          if (vec4 && mleft >= 64) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               reinterpret_cast<float4*>(yr)[j] =
@@ -749,27 +779,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int g_num_sms[64] = {0};
 
+int sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  int& n = g_num_sms[dev & 63];
+  if (n == 0 && (e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev))) return (int)e;
+  *sms = n;
+  return 0;
+}
+
 template <int F, bool P, bool X = false>
 cudaError_t launch_one(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
                        const TcDebugOut& dbg, unsigned int* status, cudaStream_t s,
-                       const float* Xf = nullptr, int ldx = 0) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+                       float* part, const float* Xf = nullptr, int ldx = 0) {
+  int sms = 0;
+  cudaError_t e = (cudaError_t)sm_count(&sms);
   if (e != cudaSuccess) return e;
-  int& sms = g_num_sms[dev & 63];
-  if (sms == 0 && (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)))
-    return e;
-  const TcPlan p = mmq_tc_plan(M, K, N, sms);
+  const TcPlan p = mmq_tc_plan(M, K, N, sms, part != nullptr);
   const int y_vec4 = (ldy % 4 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
-  if (p.U > p.Tw && dbg.write_y) {
+  if (p.splits == 1 && p.U > p.Tw && dbg.write_y) {
     zero_split_tiles_kernel<<<dim3((unsigned)((p.U - p.Tw) / 2), BT / 32), 256, 0, s>>>(
         Y, ldy, M, N, p.Tw, y_vec4);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   mmq_tc_kernel<F, P, X><<<p.grid, kThreads, smem_bytes<F, X>(), s>>>(
       maps.x, maps.whi, maps.wlo, maps.da, maps.d, maps.us, maps.mv, M, K, N, p.Tw, p.U, Y, ldy,
-      y_vec4, dbg.out, dbg.stride, dbg.mul, dbg.add, dbg.write_y, Xf, ldx, status);
-  return cudaGetLastError();
+      y_vec4, dbg.out, dbg.stride, dbg.mul, dbg.add, dbg.write_y, Xf, ldx, p.splits, part,
+      status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.splits > 1 && dbg.write_y) {
+    const long long total = (long long)N * M;
+    long long blocks = (total + 255) / 256;
+    if (blocks > (long long)sms * 8) blocks = (long long)sms * 8;
+    splitk_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(part, p.splits, N, M, Y, ldy);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 template <int F, bool P, bool X = false>
@@ -784,13 +830,30 @@ size_t mmq_tc_smem_bytes() { return smem_bytes<kFmtQ6>(); }
 
 // Grid and work units for an M x K x N GEMM on `sms` SMs: one persistent CTA
 // per SM walks the units; the last round of tiles is split in two along K
-// when that keeps more than half of the SMs busy instead of idle.
-TcPlan mmq_tc_plan(int M, int K, int N, int sms) {
+// when that keeps more than half of the SMs busy instead of idle. When the
+// tiles fill at most half of the SMs (and a partial-sum buffer is given),
+// every tile is split into sms / T K parts instead (at most one per
+// super-block, at most 8), so that 17 tokens against 4096 weight rows (32
+// tiles) take 128 SMs instead of 32.
+TcPlan mmq_tc_plan(int M, int K, int N, int sms, bool allow_splitk) {
   const long long T = (long long)((N + BT - 1) / BT) * ((M + BW - 1) / BW);
+  const int nsb = K / 256;
   TcPlan p;
+  p.splits = 1;
+  if (allow_splitk && 2 * T <= sms && nsb >= 2) {
+    long long s = sms / T;
+    if (s > nsb) s = nsb;
+    if (s > 8) s = 8;
+    p.splits = (int)s;
+    p.Tw = 0;
+    p.U = (int)(T * s);
+    p.grid = (unsigned)p.U;
+    p.launches = 2;
+    return p;
+  }
   p.grid = (unsigned)(T < sms ? T : sms);
   const long long rem = T % sms;
-  if (T > sms && rem > 0 && 2 * rem <= sms && K / 256 >= 2) {
+  if (T > sms && rem > 0 && 2 * rem <= sms && nsb >= 2) {
     p.Tw = (int)(T - rem);
     p.U = (int)(T + rem);
   } else {
@@ -799,6 +862,14 @@ TcPlan mmq_tc_plan(int M, int K, int N, int sms) {
   }
   p.launches = (p.U > p.Tw) ? 2 : 1;
   return p;
+}
+
+cudaError_t mmq_tc_plan_here(int M, int K, int N, bool allow_splitk, TcPlan* plan) {
+  int sms = 0;
+  const cudaError_t e = (cudaError_t)sm_count(&sms);
+  if (e != cudaSuccess) return e;
+  *plan = mmq_tc_plan(M, K, N, sms, allow_splitk);
+  return cudaSuccess;
 }
 
 // Raises the dynamic shared-memory limit of every instantiation; once per device.
@@ -811,20 +882,24 @@ cudaError_t mmq_tc_prepare() {
 }
 
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
-                          const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
-  return dbg.out ? launch_one<kFmtQ6, true>(maps, M, K, N, Y, ldy, dbg, status, s)
-                 : launch_one<kFmtQ6, false>(maps, M, K, N, Y, ldy, dbg, status, s);
+                          const TcDebugOut& dbg, unsigned int* status, cudaStream_t s,
+                          float* part) {
+  return dbg.out ? launch_one<kFmtQ6, true>(maps, M, K, N, Y, ldy, dbg, status, s, part)
+                 : launch_one<kFmtQ6, false>(maps, M, K, N, Y, ldy, dbg, status, s, part);
 }
 
 cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
-                              const TcDebugOut& dbg, unsigned int* status, cudaStream_t s) {
-  return dbg.out ? launch_one<kFmtQ4, true>(maps, M, K, N, Y, ldy, dbg, status, s)
-                 : launch_one<kFmtQ4, false>(maps, M, K, N, Y, ldy, dbg, status, s);
+                              const TcDebugOut& dbg, unsigned int* status, cudaStream_t s,
+                              float* part) {
+  return dbg.out ? launch_one<kFmtQ4, true>(maps, M, K, N, Y, ldy, dbg, status, s, part)
+                 : launch_one<kFmtQ4, false>(maps, M, K, N, Y, ldy, dbg, status, s, part);
 }
 
 cudaError_t launch_mmq_tc_fused(const TcMaps& maps, int M, int K, const float* X, int ldx, int N,
-                                float* Y, int ldy, unsigned int* status, cudaStream_t s) {
-  return launch_one<kFmtQ6, false, true>(maps, M, K, N, Y, ldy, TcDebugOut{}, status, s, X, ldx);
+                                float* Y, int ldy, unsigned int* status, cudaStream_t s,
+                                float* part) {
+  return launch_one<kFmtQ6, false, true>(maps, M, K, N, Y, ldy, TcDebugOut{}, status, s, part, X,
+                                         ldx);
 }
 
 }  // namespace q6

@@ -21,7 +21,8 @@
 // dot products and re-reads its activations for every row (from L1), so the
 // time grows by about 6 us a token on 4096 x 11008 weights; beyond
 // Q6_Q4K_SKINNY_MAX_N tokens the tensor cores, which share each activation
-// fragment across rows, are faster.
+// fragment across rows (with K split over the SMs the few tiles leave idle),
+// are faster.
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -184,9 +185,8 @@ cudaError_t launch_q4k_skinny(const uint8_t* plane, int M, int K, const int8_t* 
   if (N <= 1) return launch_n<1>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
   if (N <= 2) return launch_n<2>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
   if (N <= 4) return launch_n<4>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
-  if (N <= 8) return launch_n<8>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
-  static_assert(Q6_Q4K_SKINNY_MAX_N <= 12, "the largest token bucket holds 12 tokens");
-  return launch_n<12>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
+  static_assert(Q6_Q4K_SKINNY_MAX_N <= 8, "the largest token bucket holds 8 tokens");
+  return launch_n<8>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
 }
 
 }  // namespace q6

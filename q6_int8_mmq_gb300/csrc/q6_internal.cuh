@@ -129,18 +129,23 @@ struct TcDebugOut {
   int stride = 0, mul = 1, add = 0;
   int write_y = 1;
 };
+// part: a buffer of tc_part_bytes(mmq_tc_plan(.., true)) bytes (16-byte
+// aligned) that lets a call with few tiles split K over the idle SMs, or NULL.
 cudaError_t launch_mmq_tc(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
-                          const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
+                          const TcDebugOut& dbg, unsigned int* status, cudaStream_t s,
+                          float* part = nullptr);
 // The same GEMM quantising its A operand itself: f32 X [N][ldx] (16-byte
 // aligned rows) is quantised per 32-element block inside the kernel, bit for
 // bit as q8_quantize_act does, into the Xh tiles and da; maps.x and maps.da
 // are unused.
 cudaError_t launch_mmq_tc_fused(const TcMaps& maps, int M, int K, const float* X, int ldx, int N,
-                                float* Y, int ldy, unsigned int* status, cudaStream_t s);
+                                float* Y, int ldy, unsigned int* status, cudaStream_t s,
+                                float* part = nullptr);
 // The q4_K form of the same GEMM (one operand plane, sc * q, in maps.whi; the
 // min term on the tensor cores from maps.us and maps.mv).
 cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y, int ldy,
-                              const TcDebugOut& dbg, unsigned int* status, cudaStream_t s);
+                              const TcDebugOut& dbg, unsigned int* status, cudaStream_t s,
+                              float* part = nullptr);
 // The q4_K GEMM for a few tokens (N <= Q6_Q4K_SKINNY_MAX_N): dp4a on the
 // packed plane's nibbles, Xq [N][K], da [K/32][ldda] and the block-sum pairs
 // us [N][q4_min_ld(K)]; partials (nullable) [N][M][K/32].
@@ -172,9 +177,18 @@ size_t mmq_tc_smem_bytes();
 struct TcPlan {
   unsigned grid;  // persistent CTAs
   int Tw, U;      // units 0..Tw-1 are whole tiles; Tw..U-1 are K halves of split tiles
-  int launches;   // kernels per call: the GEMM, plus one that zeroes Y of split tiles
+  int splits;     // > 1: every tile is split into this many K parts (few tiles)
+  int launches;   // kernels per call: the GEMM, plus one that zeroes Y of split
+                  // tiles or one that adds the K parts
 };
-TcPlan mmq_tc_plan(int M, int K, int N, int sms);
+// allow_splitk: a partial-sum buffer of tc_part_bytes() is available.
+TcPlan mmq_tc_plan(int M, int K, int N, int sms, bool allow_splitk);
+// Bytes of the K-part partial sums of a plan (0 unless splits > 1).
+inline size_t tc_part_bytes(const TcPlan& p, int M, int N) {
+  return p.splits > 1 ? (size_t)p.splits * (size_t)N * (size_t)M * 4 : 0;
+}
+// mmq_tc_plan on the current device.
+cudaError_t mmq_tc_plan_here(int M, int K, int N, bool allow_splitk, TcPlan* plan);
 cudaError_t mmq_tc_prepare();
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t s);
 

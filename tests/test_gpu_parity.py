@@ -359,11 +359,12 @@ def test_mmq_seeded_shape_sweep(q6, orc, M, K, N):
 
 
 @pytest.mark.parametrize("M,K,N", [(1016, 768, 2555), (4096, 2048, 16), (3001, 768, 9),
-                                    (2059, 1024, 1)], ids=lambda v: str(v))
+                                    (2059, 1024, 1), (4096, 2048, 40)], ids=lambda v: str(v))
 def test_mmq_deterministic(q6, M, K, N):
     """Repeated calls give bit-identical Y: the split last round of the
-    tensor-core GEMM adds two halves onto zero, and the few-token kernels
-    reduce in a fixed order."""
+    tensor-core GEMM adds two halves onto zero, the K parts of a call with few
+    tiles are added in a fixed order, and the few-token kernels reduce in a
+    fixed order."""
     import torch
     raw = synth.q6k_raw_weights(1200 + M + N, M, K)
     X = synth.activations(1201 + M + N, N, K, outlier_frac=0.01)
@@ -374,6 +375,41 @@ def test_mmq_deterministic(q6, M, K, N):
         Y1, _, _ = q6.mmq(w, act, source="wh")
         q6.sync_status()
         assert torch.equal(Y0, Y1)
+
+
+@pytest.mark.parametrize("source", ["raw", "wh"])
+@pytest.mark.parametrize("M,K,N,splits", [(4096, 11008, 17, 4), (4096, 11008, 100, 4),
+                                          (4096, 2048, 200, 2), (1000, 768, 40, 3),
+                                          (300, 512, 130, 2)], ids=lambda v: str(v))
+def test_mmq_splitk_few_tiles(q6, orc, M, K, N, splits, source):
+    """Few tiles (at most half the SMs): each tile is split into K parts whose
+    partial sums a second kernel adds in order. Y within tolerance of the
+    oracle on every output, the debug partials bit-exact, the planned split
+    as expected, and the same Y (up to rounding) as without the split (a
+    workspace without room for the partial sums)."""
+    import torch
+    assert q6.tc_part_bytes(M, K, N) == splits * N * M * 4
+    raw = synth.q6k_raw_weights(1300 + M + N, M, K)
+    X = synth.activations(1301 + M + N, N, K, outlier_frac=0.01)
+    w = q6.pack_weights(dev(raw), M, K, wh=source == "wh")
+    act = q6.quantize_act(dev(X))
+    xq_o, da_o = quant_check(act, X, orc)
+    want_p = N * M * (K // 16) <= 40_000_000
+    Y, path, D = q6.mmq(w, act, source=source, partials=want_p, chunk_sums=want_p)
+    q6.sync_status()
+    assert path == TC_PATH[source]
+    if want_p:
+        Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+        check_debug(D, Po, raw, M, K, label=f"splitk {M}x{K}x{N}")
+    else:
+        Yo = orc.mmq_all(raw, M, K, xq_o, da_o)
+    check_y(host(Y), Yo, f"splitk {M}x{K}x{N} {source}")
+    # unsplit: a workspace with room for the unpacked planes only
+    ws = torch.empty(4 * M * K if source == "raw" else 256, dtype=torch.uint8, device="cuda")
+    Y1, _, _ = q6.mmq(w, act, source=source, workspace=ws)
+    q6.sync_status()
+    check_y(host(Y1), Yo, f"unsplit {M}x{K}x{N} {source}")
+    assert torch.allclose(Y, Y1, rtol=1e-5, atol=1e-5 * float(Y1.abs().max()))
 
 
 def test_mmq_degenerate_inputs(q6, orc):

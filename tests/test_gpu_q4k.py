@@ -155,8 +155,8 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
 
 
 def q4k_path(N, source):
-    """The path a q4_K call takes: the few-token kernel for N <= 12."""
-    return "q4k_skinny" if N <= 12 else {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source]
+    """The path a q4_K call takes: the few-token kernel for N <= 8."""
+    return "q4k_skinny" if N <= 8 else {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source]
 
 
 Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 3), (300, 768, 12), (300, 768, 16),
@@ -246,7 +246,7 @@ def test_q4k_degenerate(q6, orc):
         check_y(host(Y), Yo, label)
 
 
-@pytest.mark.parametrize("N", [1, 2, 4, 9, 12])
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8])
 def test_q4k_few_tokens_full(q6, orc, N):
     """The few-token kernel on q4_K weights of the ffn_down shape: every
     output within tolerance and every sub-block partial P bit-exact."""
