@@ -244,9 +244,11 @@ int q6k_mmq_workspace_bytes(int M, int K, int N, size_t *bytes);
 /* The number of kernels one q6k_mmq call launches for this shape on the
  * calling thread's current device: 0 for N == 0; 1 on the skinny path
  * (N <= Q6_SKINNY_MAX_N); otherwise 1 for the tensor-core GEMM, plus 1 when
- * the work split above applies, plus 1 when the weights are unpacked into the
- * workspace first (has_wh == 0). Q6_EINVAL on bad sizes or a NULL launches;
- * Q6_EARCH / Q6_ECUDA as for the other calls. */
+ * either work split above applies (the zeroing of the split last round, or
+ * the addition of the K parts, counted as if the workspace had room for
+ * them), plus 1 when the weights are unpacked into the workspace first
+ * (has_wh == 0). Q6_EINVAL on bad sizes or a NULL launches; Q6_EARCH /
+ * Q6_ECUDA as for the other calls. */
 int q6k_mmq_launches(int M, int K, int N, int has_wh, int *launches);
 
 int q6k_mmq(const void *plane, const int8_t *wexp, const uint16_t *wh, int M, int K,
