@@ -178,7 +178,7 @@ def run_reference(args):
     raw, X, cfg, config = workload_inputs(args, synth)
     M, K, N = cfg["M"], cfg["K"], cfg["N"]
     orc = oracle.get()
-    q4 = args.workload == "q4k_ffn_down"
+    q4 = args.workload in ("q4k_ffn_down", "q4k_skinny")
     gemm = orc.q4k_mmq if q4 else orc.mmq
     # One step: a batch of TB tokens (quantised in the step) against the first
     # `rows` weight rows, so the weight decode is shared by TB tokens as in the
@@ -286,6 +286,14 @@ def workload_inputs(args, synth):
     if args.workload == "q4k_ffn_down":
         raw, X, cfg = synth.q4k_workload("ffn_down")
         return raw, X, cfg, q4k_config(args, cfg)
+    if args.workload == "q4k_skinny":
+        M, K = synth.SKINNY_SHAPES["ffn_down"]
+        n = args.tokens
+        raw = synth.q4k_raw_weights(synth.Q4K_SEED, M, K)
+        X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
+        return raw, X, dict(M=M, K=K, N=n), {
+            "workload": f"q4_K few-token GEMM (ffn_down shape) M={M} K={K} N={n}",
+            "M": M, "K": K, "N": n, "parallelism": "replicas"}
     raw, X, cfg = synth.workload(args.workload)
     return raw, X, cfg, workload_config(args, cfg)
 
@@ -483,6 +491,35 @@ def skinny_kernel_times(q6, synth, device, iters: int = 10):
     return out
 
 
+def mid_tokens_times(q6, synth, device, iters: int = 4):
+    """The q6_K tensor-core GEMM with 17 to 256 tokens against the ffn_down
+    weights, where the tiles fill at most half of the SMs and K is split over
+    the idle ones: resident operand planes and from the packed plane, four
+    weight copies in turn (720 MB of operand planes), CUDA-graph replay."""
+    import torch
+    out = {}
+    M, K = synth.SKINNY_SHAPES["ffn_down"]
+    raw, _, _ = synth.skinny_workload("ffn_down", 1)
+    raw_d = torch.from_numpy(raw).to(device)
+    R = 4
+    Ws = [q6.pack_weights(raw_d, M, K, wh=True) for _ in range(R)]
+    del raw_d
+    for n in (17, 64, 128, 256):
+        X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x500 + n, n, K)
+        act = q6.quantize_act(torch.from_numpy(X).to(device))
+        Y = torch.empty((n, M), dtype=torch.float32, device=device)
+        res = {"splits": q6.tc_part_bytes(M, K, n) // (4 * n * M)}
+        for src in ("wh", "raw"):
+            for i in range(2 * R):
+                q6.mmq(Ws[i % R], act, Y=Y, source=src)
+            us = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y, source=src), iters * R) * 1e3
+            q6.sync_status()
+            res[src] = {"us": us, "tops": 2.0 * M * K * n / us / 1e6}
+        out[f"ffn_down_N{n}"] = res
+    del Ws
+    return out
+
+
 def q4k_skinny_times(q6, synth, device, iters: int = 10):
     """The q4_K few-token kernel on q4_K weights of the ffn_down shape for
     N = 1, 4, 8, weights rotated over copies totalling more than 4x L2,
@@ -531,8 +568,8 @@ def run_ours(args):
     peaks = measured_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
     hbm_src = "measured" if "hbm_gbs" in peaks else "fallback"
-    run = {"skinny": run_skinny, "sweep": run_sweep, "q4k_ffn_down": run_q4k}.get(
-        args.workload, run_gemm)
+    run = {"skinny": run_skinny, "sweep": run_sweep, "q4k_ffn_down": run_q4k,
+           "q4k_skinny": run_q4k_skinny}.get(args.workload, run_gemm)
     run(args, q6, synth, device, rank, world, peaks, hbm, hbm_src)
 
 
@@ -967,6 +1004,8 @@ def other_configs(args, q6, synth, device, hbm):
     for k, v in q4k_skinny_times(q6, synth, device).items():
         v["frac_hbm"] = v["gbs"] / hbm
         res[f"q4k_skinny_{k}"] = v
+    for k, v in mid_tokens_times(q6, synth, device).items():
+        res[f"mid_tokens_{k}"] = v
     res.update(pages_shapes(q6, synth, device))
     res["q4k_ffn_down"] = q4k_gemm(q6, synth, device)
     res["q4k_pages_ffn_up"] = q4k_gemm(q6, synth, device, "pages_ffn_up")
@@ -1213,6 +1252,100 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     print(json.dumps(line), flush=True)
 
 
+def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
+    """The q4_K few-token case: N = --tokens (1..8) tokens against q4_K
+    weights of the ffn_down shape. One step = quantise with block sums +
+    q4k_mmq (few-token kernel), weights rotated over copies totalling more
+    than 4x L2, the K steps replayed as one CUDA graph."""
+    import torch
+    n = args.tokens
+    if n > q6.Q4K_SKINNY_MAX_N:
+        raise SystemExit(f"--tokens must be at most {q6.Q4K_SKINNY_MAX_N} for q4k_skinny")
+    M, K = synth.SKINNY_SHAPES["ffn_down"]
+    raw = synth.q4k_raw_weights(synth.Q4K_SEED, M, K)
+    X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
+    raw_d = torch.from_numpy(raw).to(device)
+    R = max(4, (4 * 129 * 2 ** 20) // q6.q4k_plane_bytes(M, K)[0] + 1)
+    Ws = [q6.q4k_pack_weights(raw_d, M, K) for _ in range(R)]
+    del raw_d
+    S = 2
+    Xds = [torch.from_numpy(X).to(device) for _ in range(S)]
+    acts = [q6.alloc_activations(n, K, device, want_xh=False, want_us=True) for _ in range(S)]
+    Ys = [torch.empty((n, M), dtype=torch.float32, device=device) for _ in range(S)]
+    path = [None]
+
+    def step(i):
+        j = i % S
+        q6.quantize_act(Xds[j], out=acts[j])
+        _, path[0], _ = q6.q4k_mmq(Ws[i % R], acts[j], Y=Ys[j])
+
+    for i in range(max(args.warmup, 2 * R)):
+        step(i)
+    q6.sync_status()
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                step(i)
+    graph.replay()
+    max_ms, clk = timed_region(lambda i: graph.replay(), 1, device, rank == 0)
+    q6.sync_status()
+    m_ms = graph_ms(lambda i: q6.q4k_mmq(Ws[i % R], acts[0], Y=Ys[0]), 20 * R)
+    q_ms = graph_ms(lambda i: q6.quantize_act(Xds[0], out=acts[0]), 200)
+    q6.sync_status()
+    ops_per_step = 2.0 * M * n * K
+    value = job_throughput(ops_per_step * args.steps, world, max_ms / 1e3) / 1e12
+    e2e = None
+    if args.e2e_steps > 0:
+        Xh = torch.from_numpy(X).pin_memory()
+        Yh = [torch.empty((n, M), dtype=torch.float32).pin_memory() for _ in range(S)]
+
+        def step_host(i):
+            j = i % S
+            Xds[j].copy_(Xh, non_blocking=True)
+            step(i)
+            Yh[j].copy_(Ys[j], non_blocking=True)
+        e_ms = e2e_graph(step_host, args.e2e_steps, device)
+        e2e = {"value": job_throughput(ops_per_step * args.e2e_steps, world, e_ms / 1e3) / 1e12,
+               "unit": UNIT, "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": n * M * 4,
+               "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
+               "copies": GRAPHED}
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_budget > 0:
+        cpu = oracle_baseline(raw, X, M, K, args.cpu_budget, n, fmt="q4_K")
+    if rank != 0:
+        return
+    alg = q4k_method_bytes(M, K, n)
+    gbs = alg / m_ms / 1e6
+    line = {
+        "metric": Q4K_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 dp4a -> f32", "data": "synthetic",
+        "config": {"workload": f"q4_K few-token GEMM (ffn_down shape) M={M} K={K} N={n}",
+                   "M": M, "K": K, "N": n,
+                   "step": "q8_quantize_act with block sums + q4k_mmq (few-token kernel)",
+                   "l2": "weights rotated over packed copies totalling more than 4x L2",
+                   "parallelism": "replicas", "weight_copies": R},
+        "roofline": {"bound": "hbm", "kernel": "q4k_skinny_kernel (dp4a on the packed nibbles)",
+                     "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "peak_source": hbm_src,
+                     "traffic": args.traffic if args.traffic is not None else TRAFFIC.get(
+                         (f"q4k_skinny_N{n}", "q4k_skinny")),
+                     "algorithmic": f"M*K*144/256 + N*K + 2*4*N*K/32 + 4*N*M = {alg:.4g} B "
+                                    "per launch"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps,
+        "clocks": clk, "clocks_ok": clocks_ok(clk),
+        "timing": "the K steps replayed as one CUDA graph; kernel times by graph replay",
+        "kernels": {"q4k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
+                    "q8_quantize_act_sums": {"us": q_ms * 1e3}},
+    }
+    print(json.dumps(line), flush=True)
+
+
 class Sweep:
     """The 32-layer 7B-shape prefill sweep, set up on the device: per layer a
     q6_K attn_v (4096x4096) and ffn_down (4096x11008) weight, packed once
@@ -1376,6 +1509,7 @@ SKINNY_FUSED_MAX_N = 2
 # (workload, kernel). An entry is removed when its kernel changes.
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.93e6 + 54.75e6,
            ("q4k_ffn_down", "mmq_tc_q4k"): 635.71e6 + 58.53e6,
+           ("q4k_skinny_N1", "q4k_skinny"): 26.80e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
            ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
@@ -1392,7 +1526,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="ffn_down",
                     choices=["ffn_down", "attn_v", "pages_ffn_down", "pages_attn_v", "skinny",
-                             "sweep", "q4k_ffn_down"])
+                             "sweep", "q4k_ffn_down", "q4k_skinny"])
     ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
     ap.add_argument("--tokens", type=int, default=1, choices=range(1, 17), metavar="{1..16}",
                     help="tokens of the skinny workload")
