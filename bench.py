@@ -494,8 +494,9 @@ def skinny_kernel_times(q6, synth, device, iters: int = 10):
 def mid_tokens_times(q6, synth, device, iters: int = 4):
     """The q6_K tensor-core GEMM with 17 to 256 tokens against the ffn_down
     weights, where the tiles fill at most half of the SMs and K is split over
-    the idle ones: resident operand planes and from the packed plane, four
-    weight copies in turn (720 MB of operand planes), CUDA-graph replay."""
+    the idle ones: resident operand planes and from the packed plane (up to
+    32 tokens the few-token kernels on token groups), four weight copies in
+    turn (720 MB of operand planes), CUDA-graph replay."""
     import torch
     out = {}
     M, K = synth.SKINNY_SHAPES["ffn_down"]
@@ -504,7 +505,7 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
     R = 4
     Ws = [q6.pack_weights(raw_d, M, K, wh=True) for _ in range(R)]
     del raw_d
-    for n in (17, 64, 128, 256):
+    for n in (17, 32, 64, 128, 256):
         X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x500 + n, n, K)
         act = q6.quantize_act(torch.from_numpy(X).to(device))
         Y = torch.empty((n, M), dtype=torch.float32, device=device)
@@ -514,7 +515,8 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
                 q6.mmq(Ws[i % R], act, Y=Y, source=src)
             us = graph_ms(lambda i: q6.mmq(Ws[i % R], act, Y=Y, source=src), iters * R) * 1e3
             q6.sync_status()
-            res[src] = {"us": us, "tops": 2.0 * M * K * n / us / 1e6}
+            res[src] = {"us": us, "tops": 2.0 * M * K * n / us / 1e6,
+                        "path": q6.mmq(Ws[0], act, Y=Y, source=src)[1]}
         out[f"ffn_down_N{n}"] = res
     del Ws
     return out

@@ -71,6 +71,13 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
  * flat up to 64 tokens). */
 #define Q6_Q4K_SKINNY_MAX_N 8
 
+/* q6k_mmq without resident operand planes (wh NULL) and with Xq runs
+ * Q6_SKINNY_MAX_N < N <= Q6_SKINNY_GROUPS_MAX_N on the few-token kernels, in
+ * token groups of at most Q6_SKINNY_MAX_N (each streams the 0.82-byte packed
+ * plane once; measured on GB300, 4096 x 11008: 17 tokens in about 31 us
+ * against 77 us for unpacking 4 bytes a weight and the tensor-core GEMM). */
+#define Q6_SKINNY_GROUPS_MAX_N 32
+
 #define Q6_SKINNY_MAX_N 16
 #define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
 

@@ -401,6 +401,8 @@ int q6k_mmq_launches(int M, int K, int N, int has_wh, int* launches) {
     *launches = 0;
   } else if (N <= Q6_SKINNY_MAX_N) {
     *launches = 1;
+  } else if (!has_wh && N <= Q6_SKINNY_GROUPS_MAX_N) {
+    *launches = (N + Q6_SKINNY_MAX_N - 1) / Q6_SKINNY_MAX_N;  // token groups (given Xq)
   } else {
     int dev = 0, sms = 0;
     cudaError_t e;
@@ -423,8 +425,12 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   if (N == 0) return Q6_OK;
   if (!plane || !da || !Y) return fail(Q6_EINVAL, "plane, da and Y are required");
   const bool skinny = N <= Q6_SKINNY_MAX_N;
+  // a few more tokens without resident planes: the few-token kernels on
+  // token groups, instead of unpacking the weights for the tensor cores
+  const bool groups = !skinny && N <= Q6_SKINNY_GROUPS_MAX_N && !wh && Xq;
   if (skinny && !Xq) return fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_SKINNY_MAX_N);
-  if (!skinny && !Xh) return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
+  if (!skinny && !groups && !Xh)
+    return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
   if (!aligned(plane, 256) || !aligned(da, 16) || !aligned(Y, 4) ||
       (wexp && !aligned(wexp, 16)) || (wh && !aligned(wh, 16)) || (Xq && !aligned(Xq, 16)) ||
       (Xh && !aligned(Xh, 16)) || (partials && !aligned(partials, 4)) ||
@@ -433,7 +439,7 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
                 "plane, workspace 256 B; Xq, Xh, da, wexp, wh 16 B; Y, partials, chunk_sums 4 B");
   if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
     return fail(Q6_ESIZE, "problem too large");
-  if (!skinny && (!wh || partials)) {
+  if (!skinny && !groups && (!wh || partials)) {
     const size_t need = (size_t)M * (size_t)K * 4;
     if (!workspace || workspace_bytes < need)
       return fail(Q6_ESIZE, "workspace of %zu bytes needed to unpack the weights (got %zu)", need,
@@ -450,6 +456,22 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
     e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda_of(N), N, Y,
                               ldy, dbg, st->status, (cudaStream_t)s);
     if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch");
+    if (path_out) *path_out = Q6_PATH_SKINNY;
+    return Q6_OK;
+  }
+  if (groups) {
+    // token group g: rows n0 .. n0 + ng - 1 of Xq, Y and the debug outputs,
+    // columns n0 .. of da (n0 a multiple of 16: 16-byte aligned)
+    for (int n0 = 0; n0 < N; n0 += Q6_SKINNY_MAX_N) {
+      const int ng = N - n0 < Q6_SKINNY_MAX_N ? N - n0 : Q6_SKINNY_MAX_N;
+      q6::Debug dg;
+      dg.partials = partials ? partials + (size_t)n0 * M * (K / 16) : nullptr;
+      dg.chunk_sums = chunk_sums ? chunk_sums + (size_t)n0 * M * (K / 32) : nullptr;
+      e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq + (size_t)n0 * K,
+                                da + n0, ldda_of(N), ng, Y + (size_t)n0 * ldy, ldy, dg,
+                                st->status, (cudaStream_t)s);
+      if (e != cudaSuccess) return cuda_fail(e, "skinny kernel launch (token group)");
+    }
     if (path_out) *path_out = Q6_PATH_SKINNY;
     return Q6_OK;
   }

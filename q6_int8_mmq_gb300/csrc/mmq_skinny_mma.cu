@@ -416,6 +416,10 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
   const int R = (int)(((long long)M + waves * sms - 1) / (waves * sms));
   const int units = (M + R - 1) / R;
   const PlaneGeom g = plane_geom(M, K);
+  // the scales of the N tokens: dcols columns of the [K/32][ldda] plane (a
+  // token group of a larger call starts at a column that is a multiple of
+  // 16, so the box never reaches past the plane's rows)
+  const int dcols = (N + 3) & ~3;
   CUtensorMap mq, ms, md, mx, ma;
   if (!g_encode_fn) return cudaErrorInitializationError;
   // the activation boxes hold the N token rows (the rows past N in shared
@@ -428,13 +432,13 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
           CUDA_SUCCESS ||
       encode(&mx, Xq, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K, kXPitch / 8, (uint32_t)N) !=
           CUDA_SUCCESS ||
-      encode_f32(&ma, da, (uint64_t)ldda, (uint64_t)K / 32, (uint64_t)ldda * 4, (uint32_t)ldda,
+      encode_f32(&ma, da, (uint64_t)dcols, (uint64_t)K / 32, (uint64_t)ldda * 4, (uint32_t)dcols,
                  8 * kSbs) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
   const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
   mmq_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R, 8 * kNT, ns), s>>>(
-      mq, ms, md, mx, ma, M, K, N, R, units, ns, ldda, Y, ldy, dbg.partials, dbg.chunk_sums,
+      mq, ms, md, mx, ma, M, K, N, R, units, ns, dcols, Y, ldy, dbg.partials, dbg.chunk_sums,
       status);
   return cudaGetLastError();
 }

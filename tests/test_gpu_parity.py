@@ -88,6 +88,15 @@ SOURCES = ["raw", "wexp", "wh"]
 TC_PATH = {"raw": "tc_raw", "wexp": "tc_wexp", "wh": "tc_wh"}
 
 
+def expected_path(N, source, xq=True):
+    """The path q6k_mmq takes: the few-token kernels for N <= 16, and on token
+    groups of at most 16 for N <= 32 without resident planes (given Xq); the
+    tensor cores otherwise."""
+    if N <= 16 or (N <= 32 and source != "wh" and xq):
+        return "skinny"
+    return TC_PATH[source]
+
+
 def check_debug(D, Po, raw, M, K, tok=None, label=""):
     """Both debug outputs bit-exact: the sub-block partials against the
     oracle's P, the chunk sums against S formed from P and the raw scales
@@ -315,7 +324,7 @@ def test_mmq_small_bitexact_partials(q6, orc, M, K, N, source):
     w, act, Y, path, D = run_gemm(q6, raw, X, M, K, source, partials=True)
     xq_o, da_o = quant_check(act, X, orc)
     Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
-    assert path == ("skinny" if N <= q6.SKINNY_MAX_N else TC_PATH[source])
+    assert path == expected_path(N, source)
     check_debug(D, Po, raw, M, K, label=f"{M}x{K}x{N} {source}")
     check_y(host(Y), Yo, f"{M}x{K}x{N}")
     # the fast (non-debug) variant gives the same Y
@@ -392,8 +401,9 @@ def test_mmq_splitk_few_tiles(q6, orc, M, K, N, splits, source):
     raw = synth.q6k_raw_weights(1300 + M + N, M, K)
     X = synth.activations(1301 + M + N, N, K, outlier_frac=0.01)
     w = q6.pack_weights(dev(raw), M, K, wh=source == "wh")
-    act = q6.quantize_act(dev(X))
-    xq_o, da_o = quant_check(act, X, orc)
+    act = q6.quantize_act(dev(X), want_xq=False)   # no Xq: the tensor cores at any N > 16
+    xq_o, da_o = orc.quantize(X)
+    assert np.array_equal(host(act.da)[:, :N].T, da_o)
     want_p = N * M * (K // 16) <= 40_000_000
     Y, path, D = q6.mmq(w, act, source=source, partials=want_p, chunk_sums=want_p)
     q6.sync_status()
@@ -410,6 +420,38 @@ def test_mmq_splitk_few_tiles(q6, orc, M, K, N, splits, source):
     q6.sync_status()
     check_y(host(Y1), Yo, f"unsplit {M}x{K}x{N} {source}")
     assert torch.allclose(Y, Y1, rtol=1e-5, atol=1e-5 * float(Y1.abs().max()))
+
+
+@pytest.mark.parametrize("source", ["raw", "wexp"])
+@pytest.mark.parametrize("M,K,N", [(4096, 11008, 17), (1000, 2816, 20), (300, 768, 32),
+                                   (300, 768, 33)], ids=lambda v: str(v))
+def test_mmq_token_groups(q6, orc, M, K, N, source):
+    """17..32 tokens without resident planes run the few-token kernels on
+    token groups of at most 16 (offset rows of Xq, Y and the debug outputs,
+    offset columns of da): bit-exact partials and Y within tolerance; 33
+    tokens take the tensor cores. The same Y, up to rounding, as the tensor
+    cores on the same activations without Xq."""
+    import torch
+    raw = synth.q6k_raw_weights(1400 + M + N, M, K)
+    X = synth.activations(1401 + M + N, N, K, outlier_frac=0.01)
+    w = q6.pack_weights(dev(raw), M, K, wexp=source == "wexp")
+    act = q6.quantize_act(dev(X))
+    xq_o, da_o = quant_check(act, X, orc)
+    want_p = N * M * (K // 16) <= 40_000_000
+    Y, path, D = q6.mmq(w, act, source=source, partials=want_p, chunk_sums=want_p)
+    q6.sync_status()
+    assert path == expected_path(N, source)
+    if want_p:
+        Yo, Po = orc.mmq(raw, M, K, xq_o, da_o, partials=True)
+        check_debug(D, Po, raw, M, K, label=f"groups {M}x{K}x{N}")
+    else:
+        Yo = orc.mmq_all(raw, M, K, xq_o, da_o)
+    check_y(host(Y), Yo, f"groups {M}x{K}x{N} {source}")
+    act_tc = q6.quantize_act(dev(X), want_xq=False)
+    Yt, tpath, _ = q6.mmq(w, act_tc, source=source)
+    q6.sync_status()
+    assert tpath == TC_PATH[source]
+    assert torch.allclose(Y, Yt, rtol=1e-5, atol=1e-5 * float(Yt.abs().max()))
 
 
 def test_mmq_degenerate_inputs(q6, orc):
@@ -519,6 +561,7 @@ def test_mmq_empty(q6):
 
 @pytest.mark.parametrize("M,K,N,kind", [
     (328, 1024, 1, "raw"), (328, 1024, 2, "raw"), (328, 1024, 7, "raw"),  # skinny kernels
+    (328, 1024, 20, "raw"),                               # few-token kernels, two token groups
     (1016, 768, 2555, "raw"), (1016, 768, 2555, "wh"),   # tensor-core GEMM, split last round
     (256, 512, 40, "mma_sync")], ids=lambda v: str(v))
 def test_mmq_strided_unaligned_output(q6, orc, M, K, N, kind):
@@ -539,7 +582,7 @@ def test_mmq_strided_unaligned_output(q6, orc, M, K, N, kind):
         Y2, path, _ = q6.mmq_mma_sync(w, act, Y=Y)
     else:
         Y2, path, _ = q6.mmq(w, act, Y=Y, source=kind)
-        assert path == ("skinny" if N <= q6.SKINNY_MAX_N else TC_PATH[kind])
+        assert path == expected_path(N, kind)
     q6.sync_status()
     assert Y2.data_ptr() == Y.data_ptr()
     b = host(buf)
