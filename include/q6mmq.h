@@ -209,8 +209,10 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *   Xq, da: quantised activations (layouts above). Xq is read by the
  *           few-token kernels (N <= Q6_SKINNY_MAX_N: dp4a on the CUDA cores
  *           for one or two tokens, exact f16 mma.sync for 3..16 tokens; both
- *           stream the packed plane once).
- *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N.
+ *           stream the packed plane once), and, without wh, for up to
+ *           Q6_SKINNY_GROUPS_MAX_N tokens on token groups of at most 16.
+ *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N,
+ *           unless the token groups apply.
  *   workspace : device scratch, 256-byte aligned, of at least
  *           q6k_mmq_workspace_bytes() bytes when N > Q6_SKINNY_MAX_N and either
  *           wh is NULL or partials is not NULL: the weights are first unpacked
