@@ -523,8 +523,9 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
 
 
 def q4k_skinny_times(q6, synth, device, iters: int = 10):
-    """The q4_K few-token kernel on q4_K weights of the ffn_down shape for
-    N = 1, 4, 8, weights rotated over copies totalling more than 4x L2,
+    """The q4_K few-token kernels on q4_K weights of the ffn_down shape for
+    N = 1 .. 32 (dp4a for 1-2 tokens, the f16 MMA kernel for 3-16, token
+    groups of 16 beyond), weights rotated over copies totalling more than 4x L2,
     timed by CUDA-graph replay; GB/s of the method's bytes (q4_K weights at
     144 B per 256, int8 activations, da and block sums, f32 Y)."""
     import torch
@@ -535,7 +536,7 @@ def q4k_skinny_times(q6, synth, device, iters: int = 10):
     R = max(4, (4 * 129 * 2 ** 20) // q6.q4k_plane_bytes(M, K)[0] + 1)
     Ws = [q6.q4k_pack_weights(raw_d, M, K) for _ in range(R)]
     del raw_d
-    for n in (1, 4, 8):
+    for n in (1, 2, 3, 4, 8, 16, 32):
         X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
         act = q6.quantize_act(torch.from_numpy(X).to(device), want_xh=False, want_us=True)
         Y = torch.empty((n, M), dtype=torch.float32, device=device)
@@ -1255,14 +1256,17 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 
 def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
-    """The q4_K few-token case: N = --tokens (1..8) tokens against q4_K
+    """The q4_K few-token case: N = --tokens (1..32) tokens against q4_K
     weights of the ffn_down shape. One step = quantise with block sums +
-    q4k_mmq (few-token kernel), weights rotated over copies totalling more
-    than 4x L2, the K steps replayed as one CUDA graph."""
+    q4k_mmq (the few-token kernels, on token groups of 16 beyond 16 tokens),
+    weights rotated over copies totalling more than 4x L2, the K steps
+    replayed as one CUDA graph."""
     import torch
     n = args.tokens
-    if n > q6.Q4K_SKINNY_MAX_N:
-        raise SystemExit(f"--tokens must be at most {q6.Q4K_SKINNY_MAX_N} for q4k_skinny")
+    if n > q6.Q4K_GROUPS_MAX_N:
+        raise SystemExit(f"--tokens must be at most {q6.Q4K_GROUPS_MAX_N} for q4k_skinny")
+    dp4a = n <= q6.Q4K_DP4A_MAX_N
+    groups = -(-n // q6.Q4K_SKINNY_MAX_N)
     M, K = synth.SKINNY_SHAPES["ffn_down"]
     raw = synth.q4k_raw_weights(synth.Q4K_SEED, M, K)
     X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
@@ -1326,20 +1330,24 @@ def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         "metric": Q4K_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8 dp4a -> f32", "data": "synthetic",
+        "dtype": "int8 dp4a -> f32" if dp4a else "f16 mma.sync (exact integers) -> f32",
+        "data": "synthetic",
         "config": {"workload": f"q4_K few-token GEMM (ffn_down shape) M={M} K={K} N={n}",
                    "M": M, "K": K, "N": n,
                    "step": "q8_quantize_act with block sums + q4k_mmq (few-token kernel)",
                    "l2": "weights rotated over packed copies totalling more than 4x L2",
                    "parallelism": "replicas", "weight_copies": R},
-        "roofline": {"bound": "hbm", "kernel": "q4k_skinny_kernel (dp4a on the packed nibbles)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("q4k_skinny_kernel (dp4a on the packed nibbles)" if dp4a else
+                                "q4k_skinny_mma_kernel (warp-level f16 MMA on TMA-staged "
+                                "nibbles)"),
                      "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "peak_source": hbm_src,
                      "traffic": args.traffic if args.traffic is not None else TRAFFIC.get(
                          (f"q4k_skinny_N{n}", "q4k_skinny")),
                      "algorithmic": f"M*K*144/256 + N*K + 2*4*N*K/32 + 4*N*M = {alg:.4g} B "
                                     "per launch"},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 + groups) * args.steps,
         "clocks": clk, "clocks_ok": clocks_ok(clk),
         "timing": "the K steps replayed as one CUDA graph; kernel times by graph replay",
         "kernels": {"q4k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},

@@ -64,12 +64,16 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_TC_FUSED_WH 10 /* q6k_mmq_f32_tc: GEMM quantising X itself, resident operand planes */
 #define Q6_PATH_Q4K_SKINNY 11  /* q4_K: few-token dp4a kernel on the packed plane */
 
-/* q4k_mmq runs N <= Q6_Q4K_SKINNY_MAX_N on the few-token kernel (measured on
- * GB300, q4_K weights of 4096 x 11008: 8.5 / 24.6 / 50.9 us at 1 / 4 / 8
- * tokens against about 53 us on the tensor cores from the packed plane and
- * 30 us from the resident operand plane, K split over the idle SMs, nearly
- * flat up to 64 tokens). */
-#define Q6_Q4K_SKINNY_MAX_N 8
+/* q4k_mmq runs N <= Q6_Q4K_SKINNY_MAX_N on the few-token kernels on the
+ * packed plane: N <= Q6_Q4K_DP4A_MAX_N on dp4a (CUDA cores), more on the
+ * warp-level f16 tensor path. */
+#define Q6_Q4K_SKINNY_MAX_N 16
+#define Q6_Q4K_DP4A_MAX_N 2
+
+/* q4k_mmq without a resident operand plane (wq NULL) and with Xq runs
+ * Q6_Q4K_SKINNY_MAX_N < N <= Q6_Q4K_GROUPS_MAX_N on the few-token f16 kernel
+ * in token groups of at most Q6_Q4K_SKINNY_MAX_N. */
+#define Q6_Q4K_GROUPS_MAX_N 32
 
 /* q6k_mmq without resident operand planes (wh NULL) and with Xq runs
  * Q6_SKINNY_MAX_N < N <= Q6_SKINNY_GROUPS_MAX_N on the few-token kernels, in

@@ -27,7 +27,9 @@ PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_Q4K_TC_WQ: "q4k_tc_wq", PATH_TC_FUSED_RAW: "tc_fused_raw",
               PATH_TC_FUSED_WH: "tc_fused_wh", PATH_Q4K_SKINNY: "q4k_skinny"}
 SKINNY_MAX_N = 16
-Q4K_SKINNY_MAX_N = 8
+Q4K_SKINNY_MAX_N = 16
+Q4K_DP4A_MAX_N = 2
+Q4K_GROUPS_MAX_N = 32
 FUSED_MAX_N = 2
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).
@@ -566,23 +568,28 @@ def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",
             partials: bool = False, workspace=None, stream=None):
     """Y [N, M] f32 = the q4_K x int8 GEMM. act needs da and us
     (quantize_act(..., want_us=True)), and xq for N <= Q4K_SKINNY_MAX_N (the
-    few-token kernel on the packed plane) or xh for more tokens (the tensor
-    cores). source (tensor cores): "raw" (unpack the packed plane per call),
-    "wq" (the resident operand plane) or "auto". Returns (Y, path name,
-    partials [N, M, K/32] int32 or None)."""
+    few-token kernels on the packed plane) or xh for more tokens (the tensor
+    cores; from the packed plane, up to Q4K_GROUPS_MAX_N tokens run the
+    few-token kernel on token groups when xq is there). source (tensor
+    cores): "raw" (unpack the packed plane per call), "wq" (the resident
+    operand plane) or "auto". Returns (Y, path name, partials [N, M, K/32]
+    int32 or None)."""
     import torch
     N, M, K = act.N, w.M, w.K
     if act.K != K:
         raise Q6Error(Q6_EINVAL, "activation K does not match the weight")
     skinny = N <= Q4K_SKINNY_MAX_N
-    if act.us is None or (skinny and act.xq is None) or (not skinny and act.xh is None):
-        raise Q6Error(Q6_EINVAL, "the q4_K GEMM needs activations with us, and xq for "
-                                 f"N <= {Q4K_SKINNY_MAX_N} or xh for more tokens")
     if source == "auto":
         source = "wq" if w.wq is not None else "raw"
     if source == "wq" and w.wq is None:
         raise Q6Error(Q6_EINVAL, "weights were packed without the wq plane")
     wq = w.wq if source == "wq" else None
+    groups = not skinny and N <= Q4K_GROUPS_MAX_N and wq is None and act.xq is not None
+    if (act.us is None or (skinny and act.xq is None)
+            or (not skinny and not groups and act.xh is None)):
+        raise Q6Error(Q6_EINVAL, "the q4_K GEMM needs activations with us, and xq for "
+                                 f"N <= {Q4K_SKINNY_MAX_N} or xh for more tokens")
+    skinny = skinny or groups
     dev = w.device
     if act.device != dev:
         raise Q6Error(Q6_EINVAL, f"activations on {act.device}, weights on {dev}")

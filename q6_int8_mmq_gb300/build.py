@@ -12,7 +12,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libq6mmq.so")
 SOURCES = ["api.cu", "quantize.cu", "pack.cu", "expand.cu", "mmq_skinny.cu", "mmq_skinny_mma.cu",
-           "mmq_tc.cu", "mmq_sync.cu", "diag.cu", "noalloc.cu", "q4k.cu", "q4k_skinny.cu"]
+           "mmq_tc.cu", "mmq_sync.cu", "diag.cu", "noalloc.cu", "q4k.cu", "q4k_skinny.cu",
+           "q4k_skinny_mma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 

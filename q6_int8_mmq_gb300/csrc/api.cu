@@ -72,7 +72,7 @@ int device_state(DevState** out) {
     if ((e = cudaMalloc(&st.status, 256))) return cuda_fail(e, "cudaMalloc(status)");
     if ((e = cudaMemset(st.status, 0, 256))) return cuda_fail(e, "cudaMemset(status)");
     if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()) ||
-        (e = q6::mmq_sync_prepare()))
+        (e = q6::mmq_sync_prepare()) || (e = q6::q4k_skinny_mma_prepare()))
       return cuda_fail(e, "cudaFuncSetAttribute");
     if (!encoder()) return fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
     st.arch_ok = 1;
@@ -664,22 +664,41 @@ int q4k_mmq(const void* plane, const uint16_t* wq, int M, int K, const int8_t* X
   if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
   if (N == 0) return Q6_OK;
   const bool skinny = N <= Q6_Q4K_SKINNY_MAX_N;
+  // a few more tokens without a resident operand plane: the few-token f16
+  // kernel on token groups, instead of unpacking the weights for the tensor cores
+  const bool groups = !skinny && N <= Q6_Q4K_GROUPS_MAX_N && !wq && Xq;
   if (!plane || !da || !us || !Y) return fail(Q6_EINVAL, "plane, da, us and Y are required");
   if (skinny && !Xq) return fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_Q4K_SKINNY_MAX_N);
-  if (!skinny && !Xh) return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_Q4K_SKINNY_MAX_N);
+  if (!skinny && !groups && !Xh)
+    return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_Q4K_SKINNY_MAX_N);
   if (!aligned(plane, 256) || (Xq && !aligned(Xq, 16)) || (Xh && !aligned(Xh, 16)) ||
       !aligned(da, 16) || !aligned(us, 16) || !aligned(Y, 4) || (wq && !aligned(wq, 16)) ||
       (partials && !aligned(partials, 4)) || (workspace && !aligned(workspace, 256)))
     return fail(Q6_EALIGN, "plane, workspace 256 B; Xq, Xh, da, us, wq 16 B; Y, partials 4 B");
   if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
     return fail(Q6_ESIZE, "problem too large");
-  if (skinny) {
+  if (skinny || groups) {
     DevState* st;
     int rc = device_state(&st);
     if (rc) return rc;
-    cudaError_t e = q6::launch_q4k_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da,
-                                          ldda_of(N), us, N, Y, ldy, partials, (cudaStream_t)s);
-    if (e != cudaSuccess) return cuda_fail(e, "q4_K few-token kernel launch");
+    const uint8_t* pb = static_cast<const uint8_t*>(plane);
+    const int ldus = q6::q4_min_ld(K);
+    // token group g: rows n0 .. n0 + ng - 1 of Xq, us, Y and partials,
+    // columns n0 .. of da (n0 a multiple of 16: 16-byte aligned)
+    for (int n0 = 0; n0 < N; n0 += Q6_Q4K_SKINNY_MAX_N) {
+      const int ng = N - n0 < Q6_Q4K_SKINNY_MAX_N ? N - n0 : Q6_Q4K_SKINNY_MAX_N;
+      int32_t* pg = partials ? partials + (size_t)n0 * M * (K / 32) : nullptr;
+      const int8_t* xg = Xq + (size_t)n0 * K;
+      const float* ug = us + (size_t)n0 * ldus;
+      float* yg = Y + (size_t)n0 * ldy;
+      cudaError_t e =
+          ng <= Q6_Q4K_DP4A_MAX_N
+              ? q6::launch_q4k_skinny(pb, M, K, xg, da + n0, ldda_of(N), ug, ng, yg, ldy, pg,
+                                      (cudaStream_t)s)
+              : q6::launch_q4k_skinny_mma(pb, M, K, xg, da + n0, ldda_of(N), ug, ng, yg, ldy, pg,
+                                          st->status, (cudaStream_t)s);
+      if (e != cudaSuccess) return cuda_fail(e, "q4_K few-token kernel launch");
+    }
     if (path_out) *path_out = Q6_PATH_Q4K_SKINNY;
     return Q6_OK;
   }

@@ -87,13 +87,7 @@ __device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
 }
 
-__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 constexpr uint32_t kH2_1056 = 0x64206420u;  // (1056, 1056) as f16x2
-constexpr uint32_t kH2_1152 = 0x64806480u;  // (1152, 1152) as f16x2
 
 // The four 6-bit codes (one per byte) of sub-block j (0..7 of a half) at this
 // lane's positions: the low (j < 4) or high nibbles of ql word w and the
@@ -110,21 +104,6 @@ template <int kOdd>
 __device__ __forceinline__ uint32_t code_pair(uint32_t code) {
   const uint32_t v = __byte_perm(code, 0x64u, kOdd ? 0x4341u : 0x4240u);
   return hsub2u(v, kH2_1056);
-}
-// Activations (-127..127) of bytes (kOdd, kOdd + 2) of w as binary16 pairs,
-// given wb = w ^ 0x80808080 (x + 128 as unsigned bytes): 1024 + (x + 128) - 1152.
-template <int kOdd>
-__device__ __forceinline__ uint32_t x_pair(uint32_t wb) {
-  return hsub2u(__byte_perm(wb, 0x64u, kOdd ? 0x4341u : 0x4240u), kH2_1152);
-}
-
-// D = A (16x16 f16, row) * B (16x8 f16, col), f32, from a zero accumulator.
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                        uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%10, %10, %10, %10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
 __device__ __forceinline__ float sc_of(const uint4& v, int s) {  // signed byte s of 16
@@ -299,8 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int nt = 0; nt < kNT; ++nt) {
               const uint32_t wb = xcur[e][nt] ^ 0x80808080u;
+              const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
               float P[4];
-              mma_f16(P, a, x_pair<0>(wb), x_pair<1>(wb));
+              mma_f16(P, a, x_pair<0>(wb), x_pair<1>(wb), z);
               if (kPartials && partials) {
                 // P of sub-block 16 sb + s16 (an exact integer in f32)
 #pragma unroll
@@ -444,6 +424,14 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
 }
 
 }  // namespace
+
+CUresult skinny_tensor_map(CUtensorMap* map, bool f32, const void* base, uint64_t inner,
+                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                           uint32_t box_outer) {
+  if (!g_encode_fn) return CUDA_ERROR_NOT_INITIALIZED;
+  return f32 ? encode_f32(map, base, inner, outer, row_bytes, box_inner, box_outer)
+             : encode(map, base, inner, outer, row_bytes, box_inner, box_outer);
+}
 
 // Raises the dynamic shared-memory limit of every instantiation and looks up
 // the tensor-map encoder; once per device.

@@ -20,9 +20,8 @@
 // the rows with the grid sized to one resident wave. Each token repeats its
 // dot products and re-reads its activations for every row (from L1), so the
 // time grows by about 6 us a token on 4096 x 11008 weights; beyond
-// Q6_Q4K_SKINNY_MAX_N tokens the tensor cores, which share each activation
-// fragment across rows (with K split over the SMs the few tiles leave idle),
-// are faster.
+// Q6_Q4K_DP4A_MAX_N tokens the warp-level f16 MMA kernel, which shares each
+// activation fragment across 16 rows, is faster.
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -185,7 +184,7 @@ cudaError_t launch_q4k_skinny(const uint8_t* plane, int M, int K, const int8_t* 
   if (N <= 1) return launch_n<1>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
   if (N <= 2) return launch_n<2>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
   if (N <= 4) return launch_n<4>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
-  static_assert(Q6_Q4K_SKINNY_MAX_N <= 8, "the largest token bucket holds 8 tokens");
+  static_assert(Q6_Q4K_DP4A_MAX_N <= 8, "the largest token bucket holds 8 tokens");
   return launch_n<8>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
 }
 

@@ -96,6 +96,12 @@ cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8
                                   Debug dbg, unsigned int* status, cudaStream_t s);
 cudaError_t mmq_skinny_mma_prepare();
 cudaError_t mmq_skinny_prepare();
+// A 2D tensor map without swizzle or interleave (uint64 elements, or f32 when
+// f32 is set) for the few-token kernels' TMA stages; needs
+// mmq_skinny_mma_prepare() to have run (it looks up the encoder).
+CUresult skinny_tensor_map(CUtensorMap* map, bool f32, const void* base, uint64_t inner,
+                           uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
+                           uint32_t box_outer);
 // Quantise + GEMM for N <= 2 tokens from f32 X [N][ldx] in one launch
 // (mmq_skinny.cu); needs mmq_skinny_fused_smem(K, N) <= kFusedSmemMax bytes
 // of shared memory.
@@ -152,6 +158,13 @@ cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y,
 cudaError_t launch_q4k_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq,
                               const float* da, int ldda, const float* us, int N, float* Y,
                               int ldy, int32_t* partials, cudaStream_t s);
+// The same product for a few more tokens (N <= 16) on the warp-level f16
+// tensor path with TMA-staged nibbles and activations (q4k_skinny_mma.cu).
+cudaError_t launch_q4k_skinny_mma(const uint8_t* plane, int M, int K, const int8_t* Xq,
+                                  const float* da, int ldda, const float* us, int N, float* Y,
+                                  int ldy, int32_t* partials, unsigned int* status,
+                                  cudaStream_t s);
+cudaError_t q4k_skinny_mma_prepare();
 // Tensor maps of a q4_K GEMM call (api.cu): Xh, the operand plane wq [M][K],
 // da [K/32][ldda], the block-sum pairs us [N][q4_min_ld], and the packed q4_K
 // plane's dT and min-pair sub-planes.
@@ -449,6 +462,32 @@ __device__ __forceinline__ void regs_dealloc() {
 template <uint32_t kRegs>
 __device__ __forceinline__ void regs_alloc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegs));
+}
+
+// Warp-level f16 tensor path (mma.sync) of the few-token kernels ----------
+// a - b on f16x2 pairs.
+__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+constexpr uint32_t kH2_1024 = 0x64006400u;  // (1024, 1024) as f16x2
+constexpr uint32_t kH2_1152 = 0x64806480u;  // (1152, 1152) as f16x2
+// Activations (-127..127) of bytes (kOdd, kOdd + 2) of a word w as binary16
+// pairs, given wb = w ^ 0x80808080 (x + 128 as unsigned bytes): the exponent
+// byte 0x64 placed above each byte gives 1024 + (x + 128), minus 1152.
+template <int kOdd>
+__device__ __forceinline__ uint32_t x_pair(uint32_t wb) {
+  return hsub2u(__byte_perm(wb, 0x64u, kOdd ? 0x4341u : 0x4240u), kH2_1152);
+}
+// D = A (16x16 f16, row) * B (16x8 f16, col) + C, f32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1, const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
 }
 
 #endif  // __CUDACC__

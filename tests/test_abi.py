@@ -147,7 +147,8 @@ def test_host_side_rejections(lib):
     assert f32tc(wh=None, ws=fake, ws_bytes=64 * 256 * 4 - 1) == q6.Q6_ESIZE
     assert f32tc(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
-    # the q4_K GEMM: Xq for N <= 16 and Xh beyond, ldy < M, K % 256, misaligned
+    # the q4_K GEMM: Xq for N <= 16; Xh beyond, unless Xq is there, the plane
+    # is not resident and N <= 32 (token groups); ldy < M, K % 256, misaligned
     # pointers, no workspace for the tensor-core unpack, the empty case
     def q4(plane=fake, wq=None, M=64, K=256, Xq=fake, Xh=fake, da=fake, us=fake, N=4, Y=fake,
            ldy=64, ws=None, ws_bytes=0, P=None):
@@ -155,7 +156,9 @@ def test_host_side_rejections(lib):
                            ctypes.byref(path), None)
 
     assert q4(Xq=None) == q6.Q6_EINVAL and path.value == q6.PATH_NONE
-    assert q4(N=9, Xh=None) == q6.Q6_EINVAL
+    assert q4(N=33, Xh=None) == q6.Q6_EINVAL
+    assert q4(N=20, Xq=None, Xh=None) == q6.Q6_EINVAL
+    assert q4(N=20, wq=fake, Xh=None) == q6.Q6_EINVAL     # groups only from the packed plane
     assert q4(us=None) == q6.Q6_EINVAL
     assert q4(ldy=32) == q6.Q6_EINVAL
     assert q4(K=300) == q6.Q6_EINVAL
@@ -163,7 +166,8 @@ def test_host_side_rejections(lib):
     assert q4(us=odd) == q6.Q6_EALIGN
     assert q4(plane=odd) == q6.Q6_EALIGN
     assert q4(P=odd1) == q6.Q6_EALIGN
-    assert q4(N=9) == q6.Q6_ESIZE                          # no workspace for the unpack
+    assert q4(N=33) == q6.Q6_ESIZE                         # no workspace for the unpack
+    assert q4(N=20, Xq=None) == q6.Q6_ESIZE
     assert q4(N=0, Xq=None, Xh=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
 
