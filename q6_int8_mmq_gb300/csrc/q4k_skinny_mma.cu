@@ -8,41 +8,52 @@
 // BT-style raw-byte mma kernel", Sec. 2.2): for sub-block c of token n,
 //   Y += d * (da[c] * (sc[c] * P))  -  dmin * (m[c] * us[c]),
 // P = sum over the 32 elements of q * xq (q the raw nibble 0..15), formed on
-// the tensor cores: two m16n8k16 MMAs chained through the accumulator, each
-// over 16 of the elements. The products and sums are small integers, exact
-// in f16 x f16 -> f32 (every partial sum is at most 15 * 127 * 32 < 2^24),
-// and so is sc * P (< 63 * 15 * 127 * 32). us = da * (sum of the block's
-// codes) comes from the quantiser as an exact hi/lo pair of f32.
+// the tensor cores: two m16n8k16 f16 MMAs chained through the accumulator,
+// each over 16 of the elements. us = da * (sum of the block's codes) comes
+// from the quantiser as a hi/lo pair of f32.
 //
-// Code conversion: a lane's four nibbles of a 16-element group sit in one
-// 32-bit word (low nibbles for sub-block 2p, high for 2p + 1 of the group of
-// 32 bytes p); one byte permute places the exponent byte 0x64 above each
-// nibble (1024 + q as binary16) and one f16x2 subtraction of 1024 leaves q.
+// Nibbles as binary16 subnormals: a masked nibble word is the operand itself.
+// In a 32-bit word of nibble bytes, bits 0-3 and 16-19 (the low nibbles of
+// bytes 0 and 2) read as an f16 pair are q * 2^-24; bits 4-7 and 20-23 (the
+// high nibbles) are q * 2^-20; bytes 1 and 3 take one shift by 8 first. So a
+// pair of codes costs one logic operation. The activations (-127..127) become
+// 1024 + (x + 128) - 1152 (a byte permute and an f16x2 subtraction). Every
+// product and partial sum is an exact multiple of 2^-24 (or 2^-20) below 2^24
+// of them, so P comes out scaled by a power of two and exact; the sub-block
+// scale is applied as sc (even sub-blocks) or sc / 16 (odd), both exact, and
+// d as d * 2^24.
+//
+// The min term per super-block is a small contraction, sum over its 8
+// sub-blocks of m * us, run as two tf32 m16n8k8 MMAs (A = m of 16 rows, exact
+// in tf32; B = the hi, then the lo part of us of 8 tokens) into the same
+// fragment layout as the accumulators.
 //
 // MMA mapping: m16n8k16 with A = 16 weight rows x 16 elements and B = 16
-// elements x 8 tokens, both in the same order of the 16 elements: lane
-// (g, t) = (lane / 4, lane % 4) holds elements 4t .. 4t + 3 of the group, the
-// pairs (4t, 4t+2) in k-slots (2t, 2t+1) and (4t+1, 4t+3) in (2t+8, 2t+9).
-// In the super-block's 128 nibble bytes, group e (0, 1) of sub-block c is the
-// 16 bytes at 32 (c / 2) + 16 e, low nibbles for even c, high for odd, so a
-// lane's word of it is at 32 (c / 2) + 16 e + 4t; its activation word is at
-// byte 32 c + 16 e + 4t of the super-block's 256 codes.
+// elements x 8 tokens, both in the same order: lane (g, t) = (lane / 4,
+// lane % 4) holds bytes 8t .. 8t + 7 of the sub-block's 32 (nibble bytes of
+// its pair of sub-blocks, activation bytes of the sub-block), the first 4 for
+// the first MMA, the next 4 for the second; of each 4, bytes (0, 2) go to
+// k-slots (2t, 2t+1) and bytes (1, 3) to (2t+8, 2t+9). In the super-block's
+// 128 nibble bytes the pair of sub-blocks (2p, 2p+1) is the 32 bytes at 32 p
+// (low nibbles sub-block 2p, high 2p + 1); its activation codes are the 32
+// bytes at 32 c of the super-block's 256.
 //
 // Work: CTA u takes R consecutive weight rows (R = ceil(M / SMs) up to 32)
 // and all of K. A producer thread streams stages of 8 super-blocks through a
 // ring of 2 or 3 stages (as many as shared memory holds) with 2D TMA loads:
-// the nibbles of the R rows (each stage row 1040 bytes: 1024 plus 16 of the
-// next stage, so that the 8 rows of a fragment fall on different banks), the
-// stage's 2048 activation bytes of every token as two boxes of 1040-byte
-// token rows, the activation scales of the stage's 64 sub-blocks and the
-// block-sum pairs (528-byte token rows). The sub-block scale and min bytes
-// and (d, dmin) are not TMA-able (their rows are K/32 bytes long, not a
-// multiple of 16 when K/256 is odd): the producer warp's lanes copy them into
-// the stage with 8-byte cp.async, whose completion arrives on the stage's
-// full barrier next to the TMA bytes. Consumer warp (s, g) of 16 takes
-// super-block s of every stage for rows 16g .. 16g + 15 of the unit, and the
-// eight super-block warps' sums of a row are added in shared memory at the
-// end (fixed order). Every mbarrier wait is bounded (q6_internal.cuh).
+// the nibbles of the R rows (each stage row 1056 bytes: 1024 plus 32 of the
+// next stage, so that the 8-byte loads of a fragment's rows fall on
+// different banks), the stage's 2048 activation bytes of every token as two
+// boxes of 1056-byte token rows, the activation scales of the stage's 64
+// sub-blocks and the block-sum pairs (528-byte token rows). The sub-block
+// scale and min bytes and (d, dmin) are not TMA-able (their rows are K/32
+// bytes long, not a multiple of 16 when K/256 is odd): the producer warp's
+// lanes copy them into the stage with 8-byte cp.async, whose completion
+// arrives on the stage's full barrier next to the TMA bytes. Consumer warp
+// (s, g) of 16 takes super-block s of every stage for rows 16g .. 16g + 15 of
+// the unit, and the eight super-block warps' sums of a row are added in
+// shared memory at the end (fixed order). Every mbarrier wait is bounded
+// (q6_internal.cuh).
 #include "q6_internal.cuh"
 
 namespace q6 {
@@ -53,8 +64,8 @@ constexpr int kCW = 2 * kSbs;             // consumer warps: super-block x row g
 constexpr int kThreads = 32 * (kCW + 1);  // + one producer warp
 constexpr int kMaxNS = 3;                 // ring stages (2 or 3, by the shared-memory budget)
 constexpr int kMaxR = 32;                 // rows per unit (two MMA row groups)
-constexpr int kQPitch = 1040;             // bytes per row of a nibble stage (130 x 8)
-constexpr int kXPitch = 1040;             // bytes per token row of an activation half-stage
+constexpr int kQPitch = 1056;             // bytes per row of a nibble stage (132 x 8)
+constexpr int kXPitch = 1056;             // bytes per token row of an activation half-stage
 constexpr int kUPitch = 528;              // bytes per token row of a block-sum stage (132 f32)
 // bytes per row of a scale stage: 8 super-blocks x (sc 8 | m 8 | (d, dmin) 8),
 // padded so that the 8 rows of a fragment fall on different banks
@@ -82,19 +93,30 @@ size_t smem_bytes(int R, int XR, int ns) {
   return 1024 + (size_t)ns * stage_geo(R, XR).stage + kRedBytes + 256;
 }
 
-__device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
-}
-
-// Nibbles (0..15, one per byte) of bytes (kOdd, kOdd + 2) of `nib` as the
-// binary16 pair q: 1024 + q (exponent byte 0x64 above each) minus 1024.
-template <int kOdd>
-__device__ __forceinline__ uint32_t q_pair(uint32_t nib) {
-  return hsub2u(__byte_perm(nib, 0x64u, kOdd ? 0x4341u : 0x4240u), kH2_1024);
+__device__ __forceinline__ uint2 lds64(const uint8_t* p) {
+  return *reinterpret_cast<const uint2*>(p);
 }
 
 __device__ __forceinline__ float byte_of(uint2 v, int c) {  // unsigned byte c of 8
   return (float)(((c < 4 ? v.x : v.y) >> (8 * (c & 3))) & 0xFFu);
+}
+// Sub-block scale c of 8 as the factor of its MMA result: sc for even c, sc /
+// 16 for odd (whose codes enter the MMA 16 times larger). Exact: the byte
+// goes into the mantissa of 2^23 (or 2^19) and that power is subtracted.
+__device__ __forceinline__ float scale_of(uint2 v, int c) {
+  const uint32_t byte = ((c < 4 ? v.x : v.y) >> (8 * (c & 3))) & 0xFFu;
+  return (c & 1) ? __uint_as_float(0x49000000u | byte) - 524288.0f
+                 : __uint_as_float(0x4B000000u | byte) - 8388608.0f;
+}
+
+// D = A (16x8 tf32, row) * B (8x8 tf32, col) + C, f32 accumulation.
+__device__ __forceinline__ void mma_tf32_m16n8k8(float (&d)[4], const uint32_t (&a)[4],
+                                                 uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
 }
 
 // An 8-byte copy global -> shared; the copies of a thread complete in the
@@ -178,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[slot], tx);
           tma_load_2d(b, &tmQ, &full[slot], 128 * st, u * R);
           // the stage's 2048 activation bytes of each token, as two boxes of
-          // 1024 (+16) bytes per token row
+          // 1024 (+32) bytes per token row
           tma_load_2d(b + geo.x0, &tmX, &full[slot], 256 * st, 0);
           tma_load_2d(b + geo.x1, &tmX, &full[slot], 256 * st + 128, 0);
           // the activation scales of the stage's 64 sub-blocks, [sub-block][dcols]
@@ -234,9 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && active && sb < nsb) {
         const uint8_t* b = smem + (size_t)slot * geo.stage;
         // rows past R are not in the stage (their bytes belong to the next region)
-        const uint8_t* qa = b + (size_t)ra * kQPitch + 128 * sbw + 4 * t;
-        const uint8_t* qb = b + (size_t)rb * kQPitch + 128 * sbw + 4 * t;
-        const uint8_t* xs = b + (sbw < 4 ? geo.x0 : geo.x1) + 256 * (sbw & 3) + 4 * t;
+        const uint8_t* qa = b + (size_t)ra * kQPitch + 128 * sbw + 8 * t;
+        const uint8_t* qb = b + (size_t)rb * kQPitch + 128 * sbw + 8 * t;
+        const uint8_t* xs = b + (sbw < 4 ? geo.x0 : geo.x1) + 256 * (sbw & 3) + 8 * t;
         const float* sda = reinterpret_cast<const float*>(b + geo.da) + (size_t)(8 * sbw) * dcols;
         // this super-block's entries of rows ra, rb: sc, m, (d, dmin)
         const uint8_t* ent_a = b + geo.meta + ra * kMPitch + 24 * sbw;
@@ -244,105 +266,107 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint2 zero2 = make_uint2(0u, 0u);
         const uint2 sca = have_a ? *reinterpret_cast<const uint2*>(ent_a) : zero2;
         const uint2 scb = have_b ? *reinterpret_cast<const uint2*>(ent_b) : zero2;
-        auto load_x = [&](int c8, uint32_t (&xw)[2][kNT]) {
+        float2 sbs[kNT][2];  // [token tile][row a, b]: tokens (t0, t0 + 1)
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-#pragma unroll
-            for (int nt = 0; nt < kNT; ++nt)
-              xw[e][nt] = lds32(xs + (size_t)(8 * nt + gq) * kXPitch + 32 * c8 + 16 * e);
-        };
-        float sbs[kNT][4];
+        for (int nt = 0; nt < kNT; ++nt) {
+          sbs[nt][0] = make_float2(0.0f, 0.0f);
+          sbs[nt][1] = make_float2(0.0f, 0.0f);
+        }
+        uint2 wa = zero2, wb2 = zero2;  // nibble bytes 8t .. 8t + 7 of the current pair of sub-blocks
+        uint2 xcur[kNT], xnxt[kNT];     // activation bytes 8t .. 8t + 7 of a sub-block, per token tile
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sbs[nt][i] = 0.0f;
-        uint32_t w[2][2];  // nibble words [row][group e] of the current pair of sub-blocks
-        uint32_t xcur[2][kNT], xnxt[2][kNT];
-        load_x(0, xcur);
+          xcur[nt] = lds64(xs + (size_t)(8 * nt + gq) * kXPitch);
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
-          if ((c8 & 1) == 0) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              w[0][e] = in_a ? lds32(qa + 16 * c8 + 16 * e) : 0u;
-              w[1][e] = in_b ? lds32(qb + 16 * c8 + 16 * e) : 0u;
-            }
+          constexpr uint32_t kLo = 0x000F000Fu, kHi = 0x00F000F0u;
+          const bool odd = c8 & 1;
+          if (!odd) {
+            if (in_a) wa = lds64(qa + 16 * c8);
+            if (in_b) wb2 = lds64(qb + 16 * c8);
           }
-          if (c8 < 7) load_x(c8 + 1, xnxt);
+          if (c8 < 7) {
+#pragma unroll
+            for (int nt = 0; nt < kNT; ++nt)
+              xnxt[nt] = lds64(xs + (size_t)(8 * nt + gq) * kXPitch + 32 * (c8 + 1));
+          }
           float P[kNT][4];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const uint32_t na = ((c8 & 1) ? w[0][e] >> 4 : w[0][e]) & 0x0F0F0F0Fu;
-            const uint32_t nb = ((c8 & 1) ? w[1][e] >> 4 : w[1][e]) & 0x0F0F0F0Fu;
-            const uint32_t a[4] = {q_pair<0>(na), q_pair<0>(nb), q_pair<1>(na), q_pair<1>(nb)};
+            const uint32_t va = e ? wa.y : wa.x, vb = e ? wb2.y : wb2.x;
+            const uint32_t mask = odd ? kHi : kLo;
+            // bytes (0, 2) and (1, 3) of the words: binary16 subnormals
+            // q * 2^-24 (low nibbles) or q * 2^-20 (high nibbles)
+            const uint32_t a[4] = {va & mask, vb & mask, (va >> 8) & mask, (vb >> 8) & mask};
 #pragma unroll
             for (int nt = 0; nt < kNT; ++nt) {
-              const uint32_t wb = xcur[e][nt] ^ 0x80808080u;
+              const uint32_t xw = (e ? xcur[nt].y : xcur[nt].x) ^ 0x80808080u;
               if (e == 0) {
                 const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                mma_f16(P[nt], a, x_pair<0>(wb), x_pair<1>(wb), z);
+                mma_f16(P[nt], a, x_pair<0>(xw), x_pair<1>(xw), z);
               } else {
                 const float c[4] = {P[nt][0], P[nt][1], P[nt][2], P[nt][3]};
-                mma_f16(P[nt], a, x_pair<0>(wb), x_pair<1>(wb), c);
+                mma_f16(P[nt], a, x_pair<0>(xw), x_pair<1>(xw), c);
               }
             }
           }
-          const float sa = byte_of(sca, c8), sbv = byte_of(scb, c8);
+          // P[] = P * 2^-24 (even sub-blocks) or P * 2^-20 (odd), exact; the
+          // scales are taken as sc or sc / 16 so that every S is sc * P * 2^-24
+          const float sa = scale_of(sca, c8), sbv = scale_of(scb, c8);
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             const int t0 = 8 * nt + 2 * t;
             if (kPartials && partials) {
-              // P of sub-block 8 sb + c8 (an exact integer in f32)
+              // P of sub-block 8 sb + c8 (an exact integer)
+              const float up = odd ? 1048576.0f : 16777216.0f;
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const int rl = (i < 2) ? ra : rb, tk = t0 + (i & 1);
                 if (rl < R && r0 + rl < M && tk < N)
                   partials[((size_t)tk * M + r0 + rl) * (size_t)nc + 8 * sb + c8] =
-                      (int32_t)P[nt][i];
+                      (int32_t)(P[nt][i] * up);
               }
             }
-            const float d0 = t0 < N ? sda[c8 * dcols + t0] : 0.0f;
-            const float d1 = t0 + 1 < N ? sda[c8 * dcols + t0 + 1] : 0.0f;
-            // sc * P is exact in f32 (< 2^24)
-            sbs[nt][0] = fmaf(d0, sa * P[nt][0], sbs[nt][0]);
-            sbs[nt][1] = fmaf(d1, sa * P[nt][1], sbs[nt][1]);
-            sbs[nt][2] = fmaf(d0, sbv * P[nt][2], sbs[nt][2]);
-            sbs[nt][3] = fmaf(d1, sbv * P[nt][3], sbs[nt][3]);
+            // the scales of tokens t0, t0 + 1 (columns past N hold values
+            // that only tokens past N use); S then da * S, two tokens at once
+            const float2 d01 = *reinterpret_cast<const float2*>(sda + c8 * dcols + t0);
+            sbs[nt][0] = __ffma2_rn(
+                d01, __fmul2_rn(make_float2(sa, sa), make_float2(P[nt][0], P[nt][1])), sbs[nt][0]);
+            sbs[nt][1] = __ffma2_rn(
+                d01, __fmul2_rn(make_float2(sbv, sbv), make_float2(P[nt][2], P[nt][3])), sbs[nt][1]);
           }
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-#pragma unroll
-            for (int nt = 0; nt < kNT; ++nt) xcur[e][nt] = xnxt[e][nt];
+          for (int nt = 0; nt < kNT; ++nt) xcur[nt] = xnxt[nt];
         }
-        // the min term of the super-block: sum over its 8 sub-blocks of
-        // m * us, with us = hi + lo from the quantiser's pairs (exact); then
-        // Y += d * sbs - dmin * (that sum)
+        // the min term of the super-block, sum over its 8 sub-blocks of
+        // m * us, as two tf32 MMAs (k = the 8 sub-blocks) on the hi and lo
+        // parts of us; m (6 bits) is exact in tf32 and so is hi, lo keeps its
+        // top 11 bits (us within 2^-21 |us|). Then Y += d * sbs - dmin * that.
         const uint2 mna = have_a ? *reinterpret_cast<const uint2*>(ent_a + 8) : zero2;
         const uint2 mnb = have_b ? *reinterpret_cast<const uint2*>(ent_b + 8) : zero2;
         const float2 zf = make_float2(0.0f, 0.0f);
         const float2 dda = have_a ? *reinterpret_cast<const float2*>(ent_a + 16) : zf;
         const float2 ddb = have_b ? *reinterpret_cast<const float2*>(ent_b + 16) : zf;
+        // A (16 rows x 8 sub-blocks): rows g, g + 8 at sub-blocks t, t + 4
+        const uint32_t am[4] = {__float_as_uint(byte_of(mna, t)), __float_as_uint(byte_of(mnb, t)),
+                                __float_as_uint(byte_of(mna, t + 4)),
+                                __float_as_uint(byte_of(mnb, t + 4))};
+        const float da2 = dda.x * 16777216.0f, db2 = ddb.x * 16777216.0f;  // d * 2^24
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const float* ur = reinterpret_cast<const float*>(
-                b + geo.us + (size_t)(8 * nt + 2 * t + j) * kUPitch + 64 * sbw);
-            const float4 h0 = *reinterpret_cast<const float4*>(ur);
-            const float4 h1 = *reinterpret_cast<const float4*>(ur + 4);
-            const float4 l0 = *reinterpret_cast<const float4*>(ur + 8);
-            const float4 l1 = *reinterpret_cast<const float4*>(ur + 12);
-            const float uu[8] = {h0.x + l0.x, h0.y + l0.y, h0.z + l0.z, h0.w + l0.w,
-                                 h1.x + l1.x, h1.y + l1.y, h1.z + l1.z, h1.w + l1.w};
-            float sa = 0.0f, sb2 = 0.0f;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-              sa = fmaf(byte_of(mna, c8), uu[c8], sa);
-              sb2 = fmaf(byte_of(mnb, c8), uu[c8], sb2);
-            }
-            acc[nt][j] = fmaf(-dda.y, sa, fmaf(dda.x, sbs[nt][j], acc[nt][j]));
-            acc[nt][2 + j] = fmaf(-ddb.y, sb2, fmaf(ddb.x, sbs[nt][2 + j], acc[nt][2 + j]));
-          }
+          // B (8 sub-blocks x 8 tokens): token 8 nt + g at sub-blocks t, t + 4
+          const float* ur =
+              reinterpret_cast<const float*>(b + geo.us + (size_t)(8 * nt + gq) * kUPitch) +
+              16 * sbw;
+          const float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          float mn4[4];
+          mma_tf32_m16n8k8(mn4, am, __float_as_uint(ur[t]), __float_as_uint(ur[t + 4]), z);
+          const float c[4] = {mn4[0], mn4[1], mn4[2], mn4[3]};
+          mma_tf32_m16n8k8(mn4, am, __float_as_uint(ur[8 + t]), __float_as_uint(ur[12 + t]), c);
+          acc[nt][0] = fmaf(-dda.y, mn4[0], fmaf(da2, sbs[nt][0].x, acc[nt][0]));
+          acc[nt][1] = fmaf(-dda.y, mn4[1], fmaf(da2, sbs[nt][0].y, acc[nt][1]));
+          acc[nt][2] = fmaf(-ddb.y, mn4[2], fmaf(db2, sbs[nt][1].x, acc[nt][2]));
+          acc[nt][3] = fmaf(-ddb.y, mn4[3], fmaf(db2, sbs[nt][1].y, acc[nt][3]));
         }
       }
       __syncwarp();
