@@ -1520,6 +1520,7 @@ SKINNY_FUSED_MAX_N = 2
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.93e6 + 54.75e6,
            ("q4k_ffn_down", "mmq_tc_q4k"): 635.71e6 + 58.53e6,
            ("q4k_skinny_N1", "q4k_skinny"): 26.80e6,
+           ("q4k_skinny_N8", "q4k_skinny"): 26.92e6,
            ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
            ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,

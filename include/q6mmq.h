@@ -66,13 +66,17 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 
 /* q4k_mmq runs N <= Q6_Q4K_SKINNY_MAX_N on the few-token kernels on the
  * packed plane: N <= Q6_Q4K_DP4A_MAX_N on dp4a (CUDA cores), more on the
- * warp-level f16 tensor path. */
+ * warp-level f16 tensor path (measured on GB300, q4_K weights of 4096 x
+ * 11008: dp4a 8.5 / 13.8 us at 1 / 2 tokens; the f16 kernel about 14-15 us
+ * at 3-8 tokens and 17 us at 16, against about 53 us on the tensor cores from
+ * the packed plane and 30 us from the resident operand plane). */
 #define Q6_Q4K_SKINNY_MAX_N 16
 #define Q6_Q4K_DP4A_MAX_N 2
 
 /* q4k_mmq without a resident operand plane (wq NULL) and with Xq runs
  * Q6_Q4K_SKINNY_MAX_N < N <= Q6_Q4K_GROUPS_MAX_N on the few-token f16 kernel
- * in token groups of at most Q6_Q4K_SKINNY_MAX_N. */
+ * in token groups of at most Q6_Q4K_SKINNY_MAX_N (33 us at 32 tokens against
+ * about 53 us for the unpack and the tensor cores). */
 #define Q6_Q4K_GROUPS_MAX_N 32
 
 /* q6k_mmq without resident operand planes (wh NULL) and with Xq runs
@@ -410,23 +414,28 @@ int q4k_pack_weights(const uint8_t *raw, int M, int K, void *plane, uint16_t *wq
 int q4k_unpack_weights(const void *plane, int M, int K, uint16_t *wq, q6_stream_t s);
 
 /* The q4_K GEMM. N > Q6_Q4K_SKINNY_MAX_N runs on the tensor cores; fewer
- * tokens run a weight-streaming dp4a kernel on the packed plane (about 0.59
- * byte per weight; wq and the workspace are not used).
+ * tokens run weight-streaming few-token kernels on the packed plane (about
+ * 0.59 byte per weight; wq and the workspace are not used): dp4a for N <=
+ * Q6_Q4K_DP4A_MAX_N, exact f16 mma.sync beyond. Without wq and with Xq, up to
+ * Q6_Q4K_GROUPS_MAX_N tokens run the f16 few-token kernel on token groups of
+ * at most Q6_Q4K_SKINNY_MAX_N instead of the tensor cores.
  *   plane : the packed q4_K plane (required); wq : resident operand plane or
  *           NULL (then it is unpacked into the workspace first).
  *   Xq, Xh, da, us : from q8_quantize_act_sums (int8 codes, binary16 codes,
  *           scales, block-sum pairs); Xq is required for N <=
- *           Q6_Q4K_SKINNY_MAX_N and Xh for more tokens. On the tensor cores the min term sum_c us * (dmin * m)
- *           runs as kind::tf32 products of the hi/lo pairs (each product
- *           exact in f32; us's pair is within 2^-21 |us| of it); the
- *           few-token kernel adds each pair back to us (exact).
+ *           Q6_Q4K_SKINNY_MAX_N and Xh for more tokens (unless the token
+ *           groups run). The min term sum_c us * (dmin * m) runs as tf32
+ *           products of the hi/lo pairs on the tensor cores and in the f16
+ *           few-token kernel (each product exact in f32; us's pair is within
+ *           2^-21 |us| of it); the dp4a kernel adds each pair back to us (exact).
  *   workspace : device, 256-byte aligned, at least 2 * M * K bytes on the
  *           tensor-core path when wq is NULL or partials is not NULL; contents
  *           afterwards unspecified.
  *   partials : NULL, or device int32 [N][M][K/32] that receives every exact
  *           P = sum over a sub-block of q * xq (debug: on the tensor cores one
  *           more GEMM launch on the plane of the raw nibbles, unpacked in the
- *           workspace; the few-token kernel writes them from its dot products).
+ *           workspace; the few-token kernels write them from their dot
+ *           products).
  *   path_out : NULL or receives Q6_PATH_Q4K_TC_RAW / Q6_PATH_Q4K_TC_WQ /
  *           Q6_PATH_Q4K_SKINNY.
  * Alignment: plane, workspace 256 B; Xq, Xh, da, us, wq 16 B; Y, partials 4 B.
