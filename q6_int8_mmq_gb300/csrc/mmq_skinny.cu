@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
     const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
     const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
     int32_t* __restrict__ partials, int32_t* __restrict__ chunks) {
+  griddep_wait();  // launched as a dependent launch: global memory from here on
   const int warps = (int)gridDim.x * kWarps;
   for (int m = (threadIdx.x >> 5) * (int)gridDim.x + blockIdx.x; m < M; m += warps)
     row_dot<kPartials, kMaxN>(
@@ -409,9 +410,8 @@ cudaError_t launch_bucket(const uint8_t* plane, const PlaneGeom& g, int M, int K
                                                          kWarps * 32, 0)))
     return e;
   const unsigned blocks = (unsigned)(sms * (per_sm > 0 ? per_sm : 1));
-  mmq_skinny_kernel<P, kMaxN><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, N, Y,
-                                                             ldy, dbg.partials, dbg.chunk_sums);
-  return cudaGetLastError();
+  return launch_pdl(mmq_skinny_kernel<P, kMaxN>, dim3(blocks), dim3(kWarps * 32), 0, s, plane, g,
+                    M, K, Xq, da, ldda, N, Y, ldy, dbg.partials, dbg.chunk_sums);
 }
 
 cudaError_t launch_mmq_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq, const float* da,

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   __syncthreads();
+  griddep_wait();  // launched as a dependent launch: global memory from here on
 
   if (warp == kCW) {
     // ----------------------------------------------------------- producer --
@@ -417,10 +418,9 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
     return cudaErrorInvalidValue;
   const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  mmq_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R, 8 * kNT, ns), s>>>(
-      mq, ms, md, mx, ma, M, K, N, R, units, ns, dcols, Y, ldy, dbg.partials, dbg.chunk_sums,
-      status);
-  return cudaGetLastError();
+  return launch_pdl(mmq_skinny_mma_kernel<kNT, P>, dim3(grid), dim3(kThreads),
+                    smem_bytes(R, 8 * kNT, ns), s, mq, ms, md, mx, ma, M, K, N, R, units, ns,
+                    dcols, Y, ldy, dbg.partials, dbg.chunk_sums, status);
 }
 
 }  // namespace

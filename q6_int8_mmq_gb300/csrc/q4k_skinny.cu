@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) q4k_skinny_kernel(
     const uint8_t* __restrict__ plane, Q4Geom g, int M, int K, const int8_t* __restrict__ Xq,
     const float* __restrict__ da, int ldda, const float* __restrict__ us, int N,
     float* __restrict__ Y, int ldy, int32_t* __restrict__ partials) {
+  griddep_wait();  // launched as a dependent launch: global memory from here on
   const int lane = threadIdx.x & 31;
   const int nsb = K / 256, nc = K / 32, ldus = q4_min_ld(K);
   const int sbi = lane >> 3;            // super-block within the step
@@ -160,9 +161,8 @@ cudaError_t launch_bucket(const uint8_t* plane, const Q4Geom& g, int M, int K, c
                                                          kWarps * 32, 0)))
     return e;
   const unsigned blocks = (unsigned)(sms * (per_sm > 0 ? per_sm : 1));
-  q4k_skinny_kernel<P, kMaxN><<<blocks, kWarps * 32, 0, s>>>(plane, g, M, K, Xq, da, ldda, us, N,
-                                                             Y, ldy, partials);
-  return cudaGetLastError();
+  return launch_pdl(q4k_skinny_kernel<P, kMaxN>, dim3(blocks), dim3(kWarps * 32), 0, s, plane, g,
+                    M, K, Xq, da, ldda, us, N, Y, ldy, partials);
 }
 
 template <int kMaxN>

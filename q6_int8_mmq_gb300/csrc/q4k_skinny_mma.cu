@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   __syncthreads();
+  griddep_wait();  // launched as a dependent launch: global memory from here on
 
   if (warp == kCW) {
     // ----------------------------------------------------------- producer --
@@ -429,9 +430,9 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
     return cudaErrorInvalidValue;
   const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  q4k_skinny_mma_kernel<kNT, P><<<grid, kThreads, smem_bytes(R, 8 * kNT, ns), s>>>(
-      mq, mx, ma, mu, plane, g, M, K, N, R, units, ns, dcols, Y, ldy, partials, status);
-  return cudaGetLastError();
+  return launch_pdl(q4k_skinny_mma_kernel<kNT, P>, dim3(grid), dim3(kThreads),
+                    smem_bytes(R, 8 * kNT, ns), s, mq, mx, ma, mu, plane, g, M, K, N, R, units, ns,
+                    dcols, Y, ldy, partials, status);
 }
 
 }  // namespace

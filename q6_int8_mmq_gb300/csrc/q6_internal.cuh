@@ -205,6 +205,28 @@ cudaError_t mmq_tc_plan_here(int M, int K, int N, bool allow_splitk, TcPlan* pla
 cudaError_t mmq_tc_prepare();
 cudaError_t launch_wait_selftest(unsigned long long limit_ns, unsigned int* status, cudaStream_t s);
 
+// Launches kernel<<<grid, block, smem, s>>>(args...) as a programmatic
+// dependent launch: its CTAs may start while the previous kernel in the stream
+// is still running (once that kernel has run griddep_launch_dependents() or
+// exited), so its launch and prologue overlap that kernel's tail. The kernel
+// must run griddep_wait(), which returns once the previous kernel has
+// completed and its writes are visible, before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---------------------------------------------------------- device helpers ---
 #if defined(__CUDACC__)
 #ifndef MBAR_POLL
@@ -219,6 +241,18 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Programmatic dependent launch ---------------------------------------------
+// Waits until the grid this one depends on has completed and its writes are
+// visible (returns at once for a kernel launched without the attribute).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel in the stream, if launched with the attribute, start
+// its CTAs before this grid has finished.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // mbarrier ------------------------------------------------------------------

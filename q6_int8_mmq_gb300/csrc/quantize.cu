@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(256) q8_quantize8_kernel(const float* __restri
                                                            float* __restrict__ da, int ldda,
                                                            __half* __restrict__ Xh,
                                                            float* __restrict__ us) {
+  griddep_launch_dependents();  // the GEMM that reads these may start its prologue
   const long long per_row = K >> 3;  // eight-element groups per row
   const long long total = (long long)N * per_row;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(256) q8_quantize_kernel(const float* __restric
                                                           float* __restrict__ da, int ldda,
                                                           __half* __restrict__ Xh,
                                                           float* __restrict__ us) {
+  griddep_launch_dependents();  // the GEMM that reads these may start its prologue
   const long long per_row = K >> 4;                // sixteen-element groups per row (even)
   const long long total = (long long)N * per_row;
   const long long stride = (long long)gridDim.x * blockDim.x;

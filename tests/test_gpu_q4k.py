@@ -305,3 +305,37 @@ def test_q4k_ffn_down_full(q6, orc):
         Y, _, _ = q6.q4k_mmq(w, act, source=source)
         q6.sync_status()
         check_y(host(Y), Yo, f"q4k ffn_down {source}")
+
+
+@pytest.mark.parametrize("N", [1, 3, 9, 16, 24, 40])
+def test_q4k_extremes_every_path(q6, orc, N):
+    """Every q4_K kernel at its largest magnitudes: every nibble 15, sc = m =
+    63 (all 12 scale bytes 0xFF), d and dmin 1, every activation code +-127
+    (rows of +-1; one row mixed). P = +-15 * 127 * 32 and sc * P reach their
+    bounds, and the f16 few-token kernel's binary16 subnormal operands and
+    power-of-two-scaled sums their largest values; a second half of the blocks
+    has nibbles 0 (only the min term) for contrast. The partials are compared
+    bit for bit with the oracle's on the dp4a (N = 1), f16 (3, 9, 16), token
+    group (24, from the packed plane) and tensor-core (40) paths."""
+    M, K = 96, 768
+    nblk = M * (K // 256)
+    blocks = np.zeros((nblk, 144), np.uint8)
+    blocks[:, 0:4] = [0x00, 0x3C, 0x00, 0x3C]       # d = dmin = 1.0
+    blocks[:, 4:16] = 0xFF                           # sc = m = 63 for all 8 sub-blocks
+    blocks[:, 16:] = np.where((np.arange(nblk) % 2 == 0)[:, None], 0xFF, 0x00)
+    raw = blocks.reshape(M, -1)
+    dec = orc.q4k_decode_block(blocks[0])
+    assert np.all(dec[0] == 15) and np.all(dec[1] == 63) and np.all(dec[2] == 63)
+    X = np.ones((N, K), np.float32)
+    X[1::2] *= -1.0                                  # +-1 rows: xq = +-127
+    X[0, 256:] = np.where(np.arange(K - 256) % 3 == 0, -1.0, 1.0)
+    w = q6.q4k_pack_weights(dev(raw), M, K)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    assert np.abs(xq_o).min() == 127
+    Y, path, P = q6.q4k_mmq(w, act, source="raw", partials=True)
+    q6.sync_status()
+    assert path == q4k_path(N, "raw")
+    Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
+    assert np.abs(Po).max() == 15 * 127 * 32             # the bound is reached
+    assert np.array_equal(host(P), Po), "sub-block partials differ"
+    check_y(host(Y), Yo, f"q4k extremes N={N}")
