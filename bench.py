@@ -495,7 +495,7 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
     """The q6_K tensor-core GEMM with 17 to 256 tokens against the ffn_down
     weights, where the tiles fill at most half of the SMs and K is split over
     the idle ones: resident operand planes and from the packed plane (up to
-    32 tokens the few-token kernels on token groups), four weight copies in
+    64 tokens the few-token kernels on token groups), four weight copies in
     turn (720 MB of operand planes), CUDA-graph replay."""
     import torch
     out = {}
@@ -505,7 +505,7 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
     R = 4
     Ws = [q6.pack_weights(raw_d, M, K, wh=True) for _ in range(R)]
     del raw_d
-    for n in (17, 32, 64, 128, 256):
+    for n in (17, 32, 48, 64, 128, 256):
         X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x500 + n, n, K)
         act = q6.quantize_act(torch.from_numpy(X).to(device))
         Y = torch.empty((n, M), dtype=torch.float32, device=device)
@@ -536,7 +536,7 @@ def q4k_skinny_times(q6, synth, device, iters: int = 10):
     R = max(4, (4 * 129 * 2 ** 20) // q6.q4k_plane_bytes(M, K)[0] + 1)
     Ws = [q6.q4k_pack_weights(raw_d, M, K) for _ in range(R)]
     del raw_d
-    for n in (1, 2, 3, 4, 8, 16, 32):
+    for n in (1, 2, 3, 4, 8, 16, 32, 48):
         X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
         act = q6.quantize_act(torch.from_numpy(X).to(device), want_xh=False, want_us=True)
         Y = torch.empty((n, M), dtype=torch.float32, device=device)
@@ -1256,7 +1256,7 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 
 def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
-    """The q4_K few-token case: N = --tokens (1..32) tokens against q4_K
+    """The q4_K few-token case: N = --tokens (1..48) tokens against q4_K
     weights of the ffn_down shape. One step = quantise with block sums +
     q4k_mmq (the few-token kernels, on token groups of 16 beyond 16 tokens),
     weights rotated over copies totalling more than 4x L2, the K steps

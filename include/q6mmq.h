@@ -75,16 +75,18 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 
 /* q4k_mmq without a resident operand plane (wq NULL) and with Xq runs
  * Q6_Q4K_SKINNY_MAX_N < N <= Q6_Q4K_GROUPS_MAX_N on the few-token f16 kernel
- * in token groups of at most Q6_Q4K_SKINNY_MAX_N (33 us at 32 tokens against
- * about 53 us for the unpack and the tensor cores). */
-#define Q6_Q4K_GROUPS_MAX_N 32
+ * in token groups of at most Q6_Q4K_SKINNY_MAX_N (33 / 49 us at 32 / 48
+ * tokens against about 54 us for the unpack and the tensor cores; 62 us
+ * against 54 at 56 tokens). */
+#define Q6_Q4K_GROUPS_MAX_N 48
 
 /* q6k_mmq without resident operand planes (wh NULL) and with Xq runs
  * Q6_SKINNY_MAX_N < N <= Q6_SKINNY_GROUPS_MAX_N on the few-token kernels, in
  * token groups of at most Q6_SKINNY_MAX_N (each streams the 0.82-byte packed
- * plane once; measured on GB300, 4096 x 11008: 17 tokens in about 31 us
- * against 77 us for unpacking 4 bytes a weight and the tensor-core GEMM). */
-#define Q6_SKINNY_GROUPS_MAX_N 32
+ * plane once; measured on GB300, 4096 x 11008: 17 / 33 / 48 / 64 tokens in
+ * about 31 / 49 / 59 / 78 us against 77-79 us for unpacking 4 bytes a weight
+ * and the tensor-core GEMM). */
+#define Q6_SKINNY_GROUPS_MAX_N 64
 
 #define Q6_SKINNY_MAX_N 16
 #define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
@@ -260,7 +262,9 @@ int q6k_mmq_workspace_bytes(int M, int K, int N, size_t *bytes);
 
 /* The number of kernels one q6k_mmq call launches for this shape on the
  * calling thread's current device: 0 for N == 0; 1 on the skinny path
- * (N <= Q6_SKINNY_MAX_N); otherwise 1 for the tensor-core GEMM, plus 1 when
+ * (N <= Q6_SKINNY_MAX_N); ceil(N / Q6_SKINNY_MAX_N) on token groups
+ * (has_wh == 0 and N <= Q6_SKINNY_GROUPS_MAX_N, counted as if Xq is given);
+ * otherwise 1 for the tensor-core GEMM, plus 1 when
  * either work split above applies (the zeroing of the split last round, or
  * the addition of the K parts, counted as if the workspace had room for
  * them), plus 1 when the weights are unpacked into the workspace first

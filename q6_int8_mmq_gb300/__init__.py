@@ -27,9 +27,10 @@ PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_Q4K_TC_WQ: "q4k_tc_wq", PATH_TC_FUSED_RAW: "tc_fused_raw",
               PATH_TC_FUSED_WH: "tc_fused_wh", PATH_Q4K_SKINNY: "q4k_skinny"}
 SKINNY_MAX_N = 16
+SKINNY_GROUPS_MAX_N = 64
 Q4K_SKINNY_MAX_N = 16
 Q4K_DP4A_MAX_N = 2
-Q4K_GROUPS_MAX_N = 32
+Q4K_GROUPS_MAX_N = 48
 FUSED_MAX_N = 2
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).

@@ -71,7 +71,8 @@ def test_host_side_rejections(lib):
     odd = ctypes.c_void_p(0x10004)
     path = ctypes.c_int(-1)
 
-    def mmq(plane=fake, wexp=None, wh=None, M=64, K=256, xq=fake, da=fake, xh=fake, N=64,
+    # N = 65: past the token groups, so the tensor-core path's checks apply
+    def mmq(plane=fake, wexp=None, wh=None, M=64, K=256, xq=fake, da=fake, xh=fake, N=65,
             Y=fake, ldy=64, ws=fake, ws_bytes=1 << 30, partials=None, chunk_sums=None):
         return lib.q6k_mmq(plane, wexp, wh, M, K, xq, da, xh, N, Y, ldy, ws, ws_bytes, partials,
                            chunk_sums, ctypes.byref(path), None)
@@ -81,7 +82,9 @@ def test_host_side_rejections(lib):
     assert mmq(ldy=32) == q6.Q6_EINVAL                      # ldy < M
     assert mmq(N=0, xq=None, da=None, xh=None) == q6.Q6_OK  # empty: a no-op
     assert path.value == q6.PATH_NONE
-    assert mmq(xh=None) == q6.Q6_EINVAL                     # operand plane needed for N > 16
+    assert mmq(xh=None) == q6.Q6_EINVAL                     # operand plane needed for N > 64
+    assert mmq(N=40, xq=None, xh=None) == q6.Q6_EINVAL      # ... and for N > 16 without Xq
+    assert mmq(N=40, wh=fake, xh=None) == q6.Q6_EINVAL      # ... or with resident planes
     assert mmq(N=8, xq=None) == q6.Q6_EINVAL                # int8 activations needed for N <= 16
     assert mmq(da=odd) == q6.Q6_EALIGN                      # misaligned da
     assert mmq(ws=odd) == q6.Q6_EALIGN                      # misaligned workspace
@@ -148,7 +151,7 @@ def test_host_side_rejections(lib):
     assert f32tc(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
     # the q4_K GEMM: Xq for N <= 16; Xh beyond, unless Xq is there, the plane
-    # is not resident and N <= 32 (token groups); ldy < M, K % 256, misaligned
+    # is not resident and N <= 48 (token groups); ldy < M, K % 256, misaligned
     # pointers, no workspace for the tensor-core unpack, the empty case
     def q4(plane=fake, wq=None, M=64, K=256, Xq=fake, Xh=fake, da=fake, us=fake, N=4, Y=fake,
            ldy=64, ws=None, ws_bytes=0, P=None):
@@ -156,7 +159,7 @@ def test_host_side_rejections(lib):
                            ctypes.byref(path), None)
 
     assert q4(Xq=None) == q6.Q6_EINVAL and path.value == q6.PATH_NONE
-    assert q4(N=33, Xh=None) == q6.Q6_EINVAL
+    assert q4(N=49, Xh=None) == q6.Q6_EINVAL
     assert q4(N=20, Xq=None, Xh=None) == q6.Q6_EINVAL
     assert q4(N=20, wq=fake, Xh=None) == q6.Q6_EINVAL     # groups only from the packed plane
     assert q4(us=None) == q6.Q6_EINVAL
@@ -166,7 +169,7 @@ def test_host_side_rejections(lib):
     assert q4(us=odd) == q6.Q6_EALIGN
     assert q4(plane=odd) == q6.Q6_EALIGN
     assert q4(P=odd1) == q6.Q6_EALIGN
-    assert q4(N=33) == q6.Q6_ESIZE                         # no workspace for the unpack
+    assert q4(N=49) == q6.Q6_ESIZE                         # no workspace for the unpack
     assert q4(N=20, Xq=None) == q6.Q6_ESIZE
     assert q4(N=0, Xq=None, Xh=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 

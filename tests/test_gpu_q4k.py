@@ -156,7 +156,7 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
 
 def q4k_path(N, source):
     """The path a q4_K call with Xq takes: the few-token kernels for N <= 16,
-    and on token groups for up to 32 tokens from the packed plane."""
+    and on token groups for up to 48 tokens from the packed plane."""
     import q6_int8_mmq_gb300 as q6mod
     if N <= q6mod.Q4K_SKINNY_MAX_N or (source == "raw" and N <= q6mod.Q4K_GROUPS_MAX_N):
         return "q4k_skinny"
@@ -171,7 +171,7 @@ Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 3), (300, 768, 12), (300, 
              (130, 1024, 17), (200, 768, 129), (384, 768, 300),
              (1016, 768, 2555),    # the split last round of tiles, ragged band and tile
              (1016, 512, 2555),    # split halves of one super-block each (one min pair group)
-             (3001, 512, 40)]
+             (3001, 512, 40), (500, 1024, 48), (500, 1024, 49)]
 
 
 @pytest.mark.parametrize("source", ["raw", "wq"])
@@ -307,7 +307,7 @@ def test_q4k_ffn_down_full(q6, orc):
         check_y(host(Y), Yo, f"q4k ffn_down {source}")
 
 
-@pytest.mark.parametrize("N", [1, 3, 9, 16, 24, 40])
+@pytest.mark.parametrize("N", [1, 3, 9, 16, 24, 49])
 def test_q4k_extremes_every_path(q6, orc, N):
     """Every q4_K kernel at its largest magnitudes: every nibble 15, sc = m =
     63 (all 12 scale bytes 0xFF), d and dmin 1, every activation code +-127
@@ -316,7 +316,7 @@ def test_q4k_extremes_every_path(q6, orc, N):
     power-of-two-scaled sums their largest values; a second half of the blocks
     has nibbles 0 (only the min term) for contrast. The partials are compared
     bit for bit with the oracle's on the dp4a (N = 1), f16 (3, 9, 16), token
-    group (24, from the packed plane) and tensor-core (40) paths."""
+    group (24, from the packed plane) and tensor-core (49) paths."""
     M, K = 96, 768
     nblk = M * (K // 256)
     blocks = np.zeros((nblk, 144), np.uint8)
