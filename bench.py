@@ -1516,16 +1516,16 @@ SKINNY_DP4A_MAX_N = 2
 SKINNY_FUSED_MAX_N = 2
 
 # DRAM bytes per launch from ncu captures of the current kernels, keyed by
-# (workload, kernel). An entry is removed when its kernel changes.
+# (workload, kernel). An entry is removed when its kernel changes (the
+# few-token entries were taken again once those kernels became dependent
+# launches).
 TRAFFIC = {("ffn_down", "mmq_tc"): 667.93e6 + 54.75e6,
            ("q4k_ffn_down", "mmq_tc_q4k"): 635.71e6 + 58.53e6,
            ("q4k_skinny_N1", "q4k_skinny"): 26.80e6,
            ("q4k_skinny_N8", "q4k_skinny"): 26.92e6,
-           ("skinny_ffn_down_N1", "mmq_skinny"): 37.05e6,
-           ("skinny_ffn_down_N2", "mmq_skinny"): 37.07e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
            ("skinny_ffn_down_N2", "mmq_skinny_fused"): 37.14e6,
-           ("skinny_ffn_down_N4", "mmq_skinny"): 37.10e6,
+           ("skinny_ffn_down_N4", "mmq_skinny"): 37.11e6,
            ("skinny_ffn_down_N16", "mmq_skinny"): 37.26e6}
 
 
@@ -1539,8 +1539,8 @@ def main():
                     choices=["ffn_down", "attn_v", "pages_ffn_down", "pages_attn_v", "skinny",
                              "sweep", "q4k_ffn_down", "q4k_skinny"])
     ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
-    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 17), metavar="{1..16}",
-                    help="tokens of the skinny workload")
+    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 49), metavar="{1..48}",
+                    help="tokens of the skinny (1..16) and q4k_skinny (1..48) workloads")
     ap.add_argument("--no-other-configs", dest="other_configs", action="store_false",
                     help="skip the attn_v and skinny measurements beside ffn_down")
     ap.add_argument("--weights", choices=["raw", "wexp", "wh"], default="raw")
@@ -1550,6 +1550,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per q6k_mmq launch from an ncu capture of this kernel")
     args = ap.parse_args()
+    if args.workload == "skinny" and args.tokens > 16:
+        ap.error("--tokens must be at most 16 for the skinny workload")
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
