@@ -851,3 +851,52 @@ def test_sweep_layers(q6, orc, layer):
     X_v, X_d = synth.sweep_activations()
     check_full(q6, orc, raw_v, X_v, 4096, 4096, "raw", f"sweep layer {layer} attn_v")
     check_full(q6, orc, raw_d, X_d, 4096, 11008, "raw", f"sweep layer {layer} ffn_down")
+
+
+@pytest.mark.parametrize("fmt", ["q6_K", "q4_K"])
+def test_few_token_gemm_sees_the_previous_kernels_writes(q6, orc, fmt):
+    """The few-token GEMMs start as programmatic dependent launches and wait
+    for the previous kernel in the stream before they touch global memory.
+    Here each GEMM follows, with no synchronisation, a kernel that rewrote
+    its inputs: two weight matrices packed in turn into the same plane
+    buffer, and two activation rows quantised in turn into the same buffers
+    (the quantiser lets its dependants start early). Every Y must belong to
+    the weights and activations of its own turn: 1, 5 and 16 tokens (dp4a,
+    f16 with one and two token tiles), and 24 (token groups)."""
+    import torch
+    q4 = fmt == "q4_K"
+    M, K = 1000, 2048
+    lib = q6.load()
+    if q4:
+        raws = [synth.q4k_raw_weights(0x51360C01 + i, M, K) for i in range(2)]
+        W = q6.q4k_pack_weights(dev(raws[0]), M, K)
+    else:
+        raws = [synth.q6k_raw_weights(0x51360C01 + i, M, K) for i in range(2)]
+        W = q6.pack_weights(dev(raws[0]), M, K)
+    raw_d = [dev(r) for r in raws]
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for N in (1, 5, 16, 24):
+        Xs = [synth.activations(0x51360C10 + 4 * N + i, N, K) for i in range(2)]
+        Xd = [dev(x) for x in Xs]
+        act = q6.alloc_activations(N, K, torch.device("cuda"), want_xh=False, want_us=q4)
+        expect = {}
+        for i in range(2):
+            xq_o, da_o = orc.quantize(Xs[i])
+            for j in range(2):
+                expect[i, j] = (orc.q4k_mmq(raws[j], M, K, xq_o, da_o) if q4
+                                else orc.mmq(raws[j], M, K, xq_o, da_o))
+        torch.cuda.synchronize()
+        got = []
+        for it in range(8):
+            i, j = it % 2, (it // 2) % 2   # activations of turn i, weights of turn j
+            rc = (lib.q4k_pack_weights(q6._ptr(raw_d[j]), M, K, q6._ptr(W.plane), None, s) if q4
+                  else lib.q6k_pack_weights(q6._ptr(raw_d[j]), M, K, q6._ptr(W.plane), None,
+                                            None, s))
+            assert rc == 0
+            q6.quantize_act(Xd[i], out=act)
+            Y, path, _ = (q6.q4k_mmq(W, act) if q4 else q6.mmq(W, act, source="raw"))
+            assert path == ("q4k_skinny" if q4 else "skinny")
+            got.append(((i, j), Y.clone()))
+        q6.sync_status()
+        for key, Y in got:
+            check_y(host(Y), expect[key], f"{fmt} N={N} turn {key}")
