@@ -308,9 +308,11 @@ int q6k_mmq_mma_sync(const void *plane, const int8_t *wexp, int M, int K, const 
  * wexp when not NULL, else from the packed plane; no resident wh plane and no
  * workspace argument), but its scratch is one static device array of the
  * library: 256 bytes for the kernel's status word plus 64 MiB for the
- * two unpacked binary16 operand planes, so for N > Q6_SKINNY_MAX_N it needs
- * M * K <= 16,777,216 (a 4096 x 4096 layer) and returns Q6_ESIZE otherwise.
- * Nothing on this path allocates; no debug outputs.
+ * two unpacked binary16 operand planes, so when it unpacks (N >
+ * Q6_SKINNY_MAX_N, and not the token groups that q6k_mmq also runs for N <=
+ * Q6_SKINNY_GROUPS_MAX_N given Xq) it needs M * K <= 16,777,216 (a 4096 x
+ * 4096 layer) and returns Q6_ESIZE otherwise. Nothing on this path
+ * allocates; no debug outputs.
  *
  * The array is held by every GPU that loads this part of the library until
  * the process exits. All calls share it and it keeps the last call's

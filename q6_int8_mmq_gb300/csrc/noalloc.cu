@@ -100,12 +100,16 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
   if (N == 0) return Q6_OK;
   if (!plane || !da || !Y) return na_fail(Q6_EINVAL, "plane, da and Y are required");
   const bool skinny = N <= Q6_SKINNY_MAX_N;
+  // as q6k_mmq: a few more tokens with Xq run the few-token kernels on token
+  // groups (no scratch needed) instead of unpacking the weights
+  const bool groups = !skinny && N <= Q6_SKINNY_GROUPS_MAX_N && Xq;
   if (skinny && !Xq) return na_fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_SKINNY_MAX_N);
-  if (!skinny && !Xh) return na_fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
+  if (!skinny && !groups && !Xh)
+    return na_fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
   if (!na_aligned(plane, 256) || !na_aligned(da, 16) || !na_aligned(Y, 4) ||
       (wexp && !na_aligned(wexp, 16)) || (Xq && !na_aligned(Xq, 16)) || (Xh && !na_aligned(Xh, 16)))
     return na_fail(Q6_EALIGN, "plane 256 B; Xq, Xh, da, wexp 16 B; Y 4 B");
-  if (!skinny && (size_t)M * (size_t)K * 4 > kScratchWeightBytes)
+  if (!skinny && !groups && (size_t)M * (size_t)K * 4 > kScratchWeightBytes)
     return na_fail(Q6_ESIZE,
                    "M*K*4 = %zu bytes exceeds this entry point's static scratch of %zu bytes "
                    "(M*K <= %zu weights)",
@@ -120,10 +124,17 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
   unsigned int* status = reinterpret_cast<unsigned int*>(st->scratch);
   if ((e = cudaMemsetAsync(status, 0, sizeof(unsigned int), (cudaStream_t)s)))
     return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
-  if (skinny) {
-    e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq, da, ldda, N, Y, ldy,
-                              q6::Debug{}, status, (cudaStream_t)s);
-    if (e != cudaSuccess) return na_fail(Q6_ECUDA, "skinny kernel launch: %s", cudaGetErrorString(e));
+  if (skinny || groups) {
+    // token group g: rows n0 .. n0 + ng - 1 of Xq and Y, columns n0 .. of da
+    // (n0 a multiple of 16: 16-byte aligned); one group when N <= 16
+    for (int n0 = 0; n0 < N; n0 += Q6_SKINNY_MAX_N) {
+      const int ng = N - n0 < Q6_SKINNY_MAX_N ? N - n0 : Q6_SKINNY_MAX_N;
+      e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq + (size_t)n0 * K,
+                                da + n0, ldda, ng, Y + (size_t)n0 * ldy, ldy, q6::Debug{}, status,
+                                (cudaStream_t)s);
+      if (e != cudaSuccess)
+        return na_fail(Q6_ECUDA, "skinny kernel launch: %s", cudaGetErrorString(e));
+    }
     if (path_out) *path_out = Q6_PATH_SKINNY;
     return Q6_OK;
   }

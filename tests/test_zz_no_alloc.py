@@ -66,7 +66,7 @@ def noalloc(q6, w, act, use_wexp, stream=None):
     return Y, q6.PATH_NAMES[path.value]
 
 
-@pytest.mark.parametrize("N", [300, 8])
+@pytest.mark.parametrize("N", [300, 40, 8])     # tensor cores, token groups, few tokens
 def test_noalloc_matches_q6k_mmq_on_two_calls(q6, N):
     import torch
     M, K = 4096, 4096                     # the largest layer its static scratch holds
@@ -92,10 +92,15 @@ def test_noalloc_rejects_layers_beyond_its_scratch(q6):
     lib = q6.load()
     fake = ctypes.c_void_p(0x10000)       # rejected on the host before any use
     path = ctypes.c_int(-1)
-    rc = lib.q6k_mmq_noalloc(fake, None, 4096, 11008, fake, fake, fake, 64, fake, 4096,
+    # 65 tokens: past the token groups, so the unpack and its scratch apply
+    rc = lib.q6k_mmq_noalloc(fake, None, 4096, 11008, fake, fake, fake, 65, fake, 4096,
                              ctypes.byref(path), None)
     assert rc == q6.Q6_ESIZE
     assert b"static scratch" in lib.q6_last_error()
+    # without Xq, 40 tokens cannot run the token groups either
+    rc = lib.q6k_mmq_noalloc(fake, None, 4096, 11008, None, fake, fake, 40, fake, 4096,
+                             ctypes.byref(path), None)
+    assert rc == q6.Q6_ESIZE
     # the few-token path takes the same size limit on M * K as q6k_mmq
     rc = lib.q6k_mmq_noalloc(fake, None, 1 << 20, 1 << 21, fake, fake, None, 4, fake, 1 << 20,
                              ctypes.byref(path), None)
