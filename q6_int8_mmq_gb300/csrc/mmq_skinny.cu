@@ -42,9 +42,7 @@
 // weight plane (no faster than row-major), one 8-byte load of the two
 // sub-block scales with byte permutes (slower than two byte loads), more
 // resident CTAs (10 or 12 per SM: 10.8 / 11.3 us against 9.2 for one token
-// on 4096 x 11008; the 4096 rows already fit one wave of warps at 8), and
-// three step buffers (two steps in flight) at 7 CTAs per SM, 72 registers
-// (9.8 us).
+// on 4096 x 11008; the 4096 rows already fit one wave of warps at 8).
 #include "q6_quant.cuh"
 
 namespace q6 {
