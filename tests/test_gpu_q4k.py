@@ -339,3 +339,23 @@ def test_q4k_extremes_every_path(q6, orc, N):
     assert np.abs(Po).max() == 15 * 127 * 32             # the bound is reached
     assert np.array_equal(host(P), Po), "sub-block partials differ"
     check_y(host(Y), Yo, f"q4k extremes N={N}")
+
+
+@pytest.mark.parametrize("N", [1, 5, 16, 20, 40])
+def test_q4k_long_rows(q6, orc, N):
+    """Rows of K = 65,536 (256 super-blocks: 32 stages of the f16 few-token
+    kernel's 3-slot ring, its barrier phases wrapping many times) through the
+    dp4a (1), f16 (5, 16), token-group (20) and tensor-core (40, resident
+    plane) paths: bit-exact partials and Y within tolerance."""
+    M, K = 130, 65536
+    raw = synth.q4k_raw_weights(0x51361701 + N, M, K)
+    X = synth.activations(0x51361702 + N, N, K, outlier_frac=0.01)
+    w = q6.q4k_pack_weights(dev(raw), M, K, wq=N == 40)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    source = "wq" if N == 40 else "raw"
+    Y, path, P = q6.q4k_mmq(w, act, source=source, partials=True)
+    q6.sync_status()
+    assert path == q4k_path(N, source)
+    Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
+    assert np.array_equal(host(P), Po), "sub-block partials differ"
+    check_y(host(Y), Yo, f"q4k long rows N={N}")
