@@ -1519,8 +1519,8 @@ SKINNY_FUSED_MAX_N = 2
 # (workload, kernel). An entry is removed when its kernel changes (the
 # few-token entries were taken again once those kernels became dependent
 # launches).
-TRAFFIC = {("ffn_down", "mmq_tc"): 667.93e6 + 54.75e6,
-           ("q4k_ffn_down", "mmq_tc_q4k"): 635.71e6 + 58.53e6,
+TRAFFIC = {("ffn_down", "mmq_tc"): 670.08e6 + 54.96e6,
+           ("q4k_ffn_down", "mmq_tc_q4k"): 634.90e6 + 59.67e6,
            ("q4k_skinny_N1", "q4k_skinny"): 26.80e6,
            ("q4k_skinny_N8", "q4k_skinny"): 26.92e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
