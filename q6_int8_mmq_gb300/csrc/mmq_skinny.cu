@@ -260,6 +260,7 @@ template <int kMaxN>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) mmq_skinny_fused_kernel(
     const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const float* __restrict__ X,
     int ldx, int N, float* __restrict__ Y, int ldy) {
+  griddep_wait();  // launched as a dependent launch: global memory from here on
   extern __shared__ __align__(16) uint8_t fused_smem[];
   int8_t* xs = reinterpret_cast<int8_t*>(fused_smem);                     // codes [N][K]
   float* das = reinterpret_cast<float*>(fused_smem + (size_t)kMaxN * K);  // scales [K/32][kMaxN]
@@ -373,9 +374,9 @@ cudaError_t launch_fused(const uint8_t* plane, int M, int K, const float* X, int
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
-  mmq_skinny_fused_kernel<kMaxN><<<(unsigned)sms, kFusedWarps * 32, fused_smem_bytes(K, kMaxN), s>>>(
-      plane, plane_geom(M, K), M, K, X, ldx, N, Y, ldy);
-  return cudaGetLastError();
+  return launch_pdl(mmq_skinny_fused_kernel<kMaxN>, dim3((unsigned)sms), dim3(kFusedWarps * 32),
+                    fused_smem_bytes(K, kMaxN), s, plane, plane_geom(M, K), M, K, X, ldx, N, Y,
+                    ldy);
 }
 
 }  // namespace
