@@ -205,7 +205,9 @@ def alloc_activations(N: int, K: int, device=None, want_xh: bool = True,
                       want_xq: bool = True, want_us: bool = False) -> Activations:
     """Buffers for quantised activations. A prefill caller that only runs the
     tensor-core GEMM (N > SKINNY_MAX_N) can skip xq; the few-token kernels
-    need it (and not xh)."""
+    need it (and not xh), and with xq present and no resident operand plane,
+    up to SKINNY_GROUPS_MAX_N (q6_K) or Q4K_GROUPS_MAX_N (q4_K) tokens run
+    them on token groups instead of the tensor cores."""
     import torch
     dev = device or torch.device("cuda")
     _, dab, _, ldda = act_plane_bytes(N, K)
@@ -375,7 +377,10 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
     Debug) are filled as well.
 
     source: "raw" (unpack the packed plane), "wexp" (convert the W_exp plane),
-    "wh" (resident binary16 plane) or "auto" (wh, else wexp, else raw)."""
+    "wh" (resident binary16 plane) or "auto" (wh, else wexp, else raw). Up to
+    SKINNY_MAX_N tokens run the few-token kernels on the packed plane whatever
+    the source; up to SKINNY_GROUPS_MAX_N tokens too when act has xq and the
+    source is not "wh" (token groups of at most SKINNY_MAX_N)."""
     import torch
     N, M, K = act.N, w.M, w.K
     if act.K != K:
