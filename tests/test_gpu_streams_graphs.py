@@ -122,3 +122,49 @@ def test_fused_call_on_a_side_stream_and_in_a_graph(q6, N):
         graph.replay()
         q6.sync_status()
         close(Ys, expected(raw, M, K, X))
+
+
+@pytest.mark.parametrize("N,source", [(1, "raw"), (6, "raw"), (16, "raw"), (30, "raw"),
+                                      (30, "wq"), (200, "raw")])
+def test_q4k_path_in_a_cuda_graph(q6, N, source):
+    """The q4_K step (quantiser with block sums, then q4k_mmq) captured once
+    into a CUDA graph and replayed for two inputs, on every path: dp4a (1),
+    the f16 few-token kernel (6, 16), its token groups (30 from the packed
+    plane), the tensor cores with K split (30 on the resident plane) and the
+    unpack + tensor cores (200). The few-token kernels start as dependent
+    launches of the quantiser inside the graph."""
+    import torch
+    M, K = 300, 1536
+    raw = synth.q4k_raw_weights(0x51360921 + N, M, K)
+    X1 = synth.activations(0x51360922 + N, N, K)
+    X2 = synth.activations(0x51360923 + N, N, K, outlier_frac=0.02)
+    w = q6.q4k_pack_weights(torch.from_numpy(raw).cuda(), M, K, wq=source == "wq")
+    Xs = torch.from_numpy(X1).cuda()             # static input of the graph
+    act = q6.alloc_activations(N, K, want_us=True)
+    Y = torch.empty((N, M), dtype=torch.float32, device="cuda")
+    ws = torch.empty(4 * M * K + (1 << 22), dtype=torch.uint8, device="cuda")
+    path = [None]
+
+    def step():
+        q6.quantize_act(Xs, out=act)
+        path[0] = q6.q4k_mmq(w, act, Y=Y, source=source, workspace=ws)[1]
+
+    step()
+    q6.sync_status()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            step()
+    orc = oracle.get()
+    for X in (X1, X2):
+        Xs.copy_(torch.from_numpy(X).cuda())
+        Y.fill_(float("nan"))
+        graph.replay()
+        q6.sync_status()
+        xq, da = orc.quantize(X)
+        close(Y, orc.q4k_mmq(raw, M, K, xq, da))
+    assert path[0] == ("q4k_skinny" if N <= q6.Q4K_SKINNY_MAX_N or
+                       (source == "raw" and N <= q6.Q4K_GROUPS_MAX_N) else
+                       {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source])
