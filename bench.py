@@ -547,6 +547,14 @@ def q4k_skinny_times(q6, synth, device, iters: int = 10):
         gbs = q4k_method_bytes(M, K, n) / us / 1e3
         out[f"ffn_down_N{n}"] = {"us": us, "gbs": gbs, "weight_copies": R,
                                  "path": q6.q4k_mmq(Ws[0], act, Y=Y)[1]}
+        if n <= q6.FUSED_MAX_N:
+            # the quantiser and the GEMM in one kernel, from the f32 activations
+            Xd = torch.from_numpy(X).to(device)
+            us = graph_ms(lambda i: q6.q4k_mmq_f32(Ws[i % R], Xd, Y=Y), iters * R) * 1e3
+            q6.sync_status()
+            out[f"ffn_down_N{n}_fused"] = {
+                "us": us, "gbs": q4k_fused_bytes(M, K, n) / us / 1e3, "weight_copies": R,
+                "path": q6.q4k_mmq_f32(Ws[0], Xd, Y=Y)[1]}
     del Ws
     return out
 
@@ -833,6 +841,12 @@ def q4k_method_bytes(M, K, N):
     """The method's own bytes of one q4_K GEMM: the weights at 144 B per 256,
     the int8 activations, their per-32 f32 scales and block sums, the f32 Y."""
     return M * K * 144 / 256 + N * K + 2 * N * (K // 32) * 4 + 4 * N * M
+
+
+def q4k_fused_bytes(M, K, N):
+    """The same for the fused one/two-token q4_K call: the weights, the f32
+    activations it quantises itself, the f32 Y."""
+    return M * K * 144 / 256 + 4 * N * K + 4 * N * M
 
 
 def run_q4k(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
@@ -1257,15 +1271,17 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     """The q4_K few-token case: N = --tokens (1..48) tokens against q4_K
-    weights of the ffn_down shape. One step = quantise with block sums +
-    q4k_mmq (the few-token kernels, on token groups of 16 beyond 16 tokens),
-    weights rotated over copies totalling more than 4x L2, the K steps
-    replayed as one CUDA graph."""
+    weights of the ffn_down shape. One step = q4k_mmq_f32 (the quantiser and
+    the GEMM in one kernel) for one or two tokens, else quantise with block
+    sums + q4k_mmq (the few-token kernels, on token groups of 16 beyond 16
+    tokens); weights rotated over copies totalling more than 4x L2, the K
+    steps replayed as one CUDA graph."""
     import torch
     n = args.tokens
     if n > q6.Q4K_GROUPS_MAX_N:
         raise SystemExit(f"--tokens must be at most {q6.Q4K_GROUPS_MAX_N} for q4k_skinny")
     dp4a = n <= q6.Q4K_DP4A_MAX_N
+    fused = n <= q6.FUSED_MAX_N
     groups = -(-n // q6.Q4K_SKINNY_MAX_N)
     M, K = synth.SKINNY_SHAPES["ffn_down"]
     raw = synth.q4k_raw_weights(synth.Q4K_SEED, M, K)
@@ -1282,6 +1298,9 @@ def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
     def step(i):
         j = i % S
+        if fused:
+            _, path[0] = q6.q4k_mmq_f32(Ws[i % R], Xds[j], Y=Ys[j])
+            return
         q6.quantize_act(Xds[j], out=acts[j])
         _, path[0], _ = q6.q4k_mmq(Ws[i % R], acts[j], Y=Ys[j])
 
@@ -1299,8 +1318,11 @@ def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
     graph.replay()
     max_ms, clk = timed_region(lambda i: graph.replay(), 1, device, rank == 0)
     q6.sync_status()
-    m_ms = graph_ms(lambda i: q6.q4k_mmq(Ws[i % R], acts[0], Y=Ys[0]), 20 * R)
+    q6.quantize_act(Xds[0], out=acts[0])
+    g_ms = graph_ms(lambda i: q6.q4k_mmq(Ws[i % R], acts[0], Y=Ys[0]), 20 * R)
     q_ms = graph_ms(lambda i: q6.quantize_act(Xds[0], out=acts[0]), 200)
+    m_ms = (graph_ms(lambda i: q6.q4k_mmq_f32(Ws[i % R], Xds[0], Y=Ys[0]), 20 * R)
+            if fused else g_ms)
     q6.sync_status()
     ops_per_step = 2.0 * M * n * K
     value = job_throughput(ops_per_step * args.steps, world, max_ms / 1e3) / 1e12
@@ -1324,8 +1346,24 @@ def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         cpu = oracle_baseline(raw, X, M, K, args.cpu_budget, n, fmt="q4_K")
     if rank != 0:
         return
-    alg = q4k_method_bytes(M, K, n)
+    alg = q4k_fused_bytes(M, K, n) if fused else q4k_method_bytes(M, K, n)
     gbs = alg / m_ms / 1e6
+    if fused:
+        kname = "q4k_skinny_fused_kernel (dp4a, quantiser in the same kernel)"
+        formula = "M*K*144/256 + 4*N*K + 4*N*M"
+        kernels = {"q4k_mmq_f32": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]}}
+        g_gbs = q4k_method_bytes(M, K, n) / g_ms / 1e6
+        separate = {"step": "q8_quantize_act with block sums + q4k_mmq",
+                    "q4k_mmq": {"kernel": "q4k_skinny_kernel (dp4a)", "us": g_ms * 1e3,
+                                "gbs": g_gbs, "frac": g_gbs / hbm},
+                    "q8_quantize_act_sums": {"us": q_ms * 1e3}}
+    else:
+        kname = ("q4k_skinny_kernel (dp4a on the packed nibbles)" if dp4a else
+                 "q4k_skinny_mma_kernel (warp-level f16 MMA on TMA-staged nibbles)")
+        formula = "M*K*144/256 + N*K + 2*4*N*K/32 + 4*N*M"
+        kernels = {"q4k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
+                   "q8_quantize_act_sums": {"us": q_ms * 1e3}}
+        separate = None
     line = {
         "metric": Q4K_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
@@ -1334,25 +1372,26 @@ def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         "data": "synthetic",
         "config": {"workload": f"q4_K few-token GEMM (ffn_down shape) M={M} K={K} N={n}",
                    "M": M, "K": K, "N": n,
-                   "step": "q8_quantize_act with block sums + q4k_mmq (few-token kernel)",
+                   "step": ("q4k_mmq_f32 (the quantiser and the GEMM in one kernel)"
+                            if fused else
+                            "q8_quantize_act with block sums + q4k_mmq (few-token kernel)"),
                    "l2": "weights rotated over packed copies totalling more than 4x L2",
                    "parallelism": "replicas", "weight_copies": R},
-        "roofline": {"bound": "hbm",
-                     "kernel": ("q4k_skinny_kernel (dp4a on the packed nibbles)" if dp4a else
-                                "q4k_skinny_mma_kernel (warp-level f16 MMA on TMA-staged "
-                                "nibbles)"),
+        "roofline": {"bound": "hbm", "kernel": kname,
                      "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "peak_source": hbm_src,
                      "traffic": args.traffic if args.traffic is not None else TRAFFIC.get(
-                         (f"q4k_skinny_N{n}", "q4k_skinny")),
-                     "algorithmic": f"M*K*144/256 + N*K + 2*4*N*K/32 + 4*N*M = {alg:.4g} B "
-                                    "per launch"},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 + groups) * args.steps,
+                         (f"q4k_skinny_N{n}",
+                          "q4k_skinny_fused" if fused else "q4k_skinny")),
+                     "algorithmic": f"{formula} = {alg:.4g} B per launch"},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": (1 if fused else 1 + groups) * args.steps,
         "clocks": clk, "clocks_ok": clocks_ok(clk),
         "timing": "the K steps replayed as one CUDA graph; kernel times by graph replay",
-        "kernels": {"q4k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
-                    "q8_quantize_act_sums": {"us": q_ms * 1e3}},
+        "kernels": kernels,
     }
+    if separate is not None:
+        line["separate_calls"] = separate
     print(json.dumps(line), flush=True)
 
 
@@ -1521,7 +1560,8 @@ SKINNY_FUSED_MAX_N = 2
 # launches).
 TRAFFIC = {("ffn_down", "mmq_tc"): 670.08e6 + 54.96e6,
            ("q4k_ffn_down", "mmq_tc_q4k"): 634.90e6 + 59.67e6,
-           ("q4k_skinny_N1", "q4k_skinny"): 26.80e6,
+           ("q4k_skinny_N1", "q4k_skinny_fused"): 26.83e6,
+           ("q4k_skinny_N2", "q4k_skinny_fused"): 26.88e6,
            ("q4k_skinny_N8", "q4k_skinny"): 26.92e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
            ("skinny_ffn_down_N2", "mmq_skinny_fused"): 37.14e6,

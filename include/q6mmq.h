@@ -62,7 +62,8 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_PATH_Q4K_TC_WQ 8  /* q4_K: tensor-core GEMM on a resident binary16 operand plane */
 #define Q6_PATH_TC_FUSED_RAW 9 /* q6k_mmq_f32_tc: unpack into the workspace + GEMM quantising X itself */
 #define Q6_PATH_TC_FUSED_WH 10 /* q6k_mmq_f32_tc: GEMM quantising X itself, resident operand planes */
-#define Q6_PATH_Q4K_SKINNY 11  /* q4_K: few-token dp4a kernel on the packed plane */
+#define Q6_PATH_Q4K_SKINNY 11  /* q4_K: few-token kernels on the packed plane */
+#define Q6_PATH_Q4K_SKINNY_FUSED 12 /* q4k_mmq_f32: quantiser and one/two-token GEMM in one kernel */
 
 /* q4k_mmq runs N <= Q6_Q4K_SKINNY_MAX_N on the few-token kernels on the
  * packed plane: N <= Q6_Q4K_DP4A_MAX_N on dp4a (CUDA cores), more on the
@@ -418,6 +419,24 @@ int q4k_pack_weights(const uint8_t *raw, int M, int K, void *plane, uint16_t *wq
 
 /* The unpack pass alone: wq [M][K] from the packed plane. */
 int q4k_unpack_weights(const void *plane, int M, int K, uint16_t *wq, q6_stream_t s);
+
+/* One or two tokens of the q4_K GEMM straight from f32 activations, in one
+ * kernel launch: Y = what q8_quantize_act_sums followed by q4k_mmq gives for
+ * the same X (bit for bit), without writing the codes, scales and block sums
+ * to memory; the q4_K counterpart of q6k_mmq_f32.
+ *   plane : the packed q4_K plane (device, 256-byte aligned).
+ *   X     : device f32 [N][ldx], ldx >= K; X 16-byte aligned, ldx % 4 == 0.
+ *   N     : 0 .. Q6_FUSED_MAX_N (more tokens: q8_quantize_act_sums + q4k_mmq).
+ *   Y     : device f32 [N][ldy], ldy >= M, 4-byte aligned.
+ *   K     : K % 256 == 0 and N * K * 5 / 4 <= 232,448 (the codes, scales and
+ *           block sums of X staged in shared memory): K <= 92,928 for two
+ *           tokens, 185,856 for one; Q6_ESIZE beyond.
+ *   path_out : NULL or receives Q6_PATH_Q4K_SKINNY_FUSED (Q6_PATH_NONE for
+ *           N == 0).
+ * Errors: Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA as above; no
+ * allocation, no bounded waits, asynchronous on s. */
+int q4k_mmq_f32(const void *plane, int M, int K, const float *X, int ldx, int N, float *Y,
+                int ldy, int *path_out, q6_stream_t s);
 
 /* The q4_K GEMM. N > Q6_Q4K_SKINNY_MAX_N runs on the tensor cores; fewer
  * tokens run weight-streaming few-token kernels on the packed plane (about

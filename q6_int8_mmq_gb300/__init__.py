@@ -20,12 +20,13 @@ LIB_PATH = os.path.join(_HERE, "_build", "libq6mmq.so")
 Q6_OK, Q6_EINVAL, Q6_EALIGN, Q6_ESIZE, Q6_EARCH, Q6_ECUDA, Q6_ETIMEOUT = range(7)
 (PATH_NONE, PATH_TC_RAW, PATH_TC_WEXP, PATH_SKINNY, PATH_TC_WH, PATH_SYNC_WEXP,
  PATH_SKINNY_FUSED, PATH_Q4K_TC_RAW, PATH_Q4K_TC_WQ, PATH_TC_FUSED_RAW,
- PATH_TC_FUSED_WH, PATH_Q4K_SKINNY) = range(12)
+ PATH_TC_FUSED_WH, PATH_Q4K_SKINNY, PATH_Q4K_SKINNY_FUSED) = range(13)
 PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_SKINNY: "skinny", PATH_TC_WH: "tc_wh", PATH_SYNC_WEXP: "sync_wexp",
               PATH_SKINNY_FUSED: "skinny_fused", PATH_Q4K_TC_RAW: "q4k_tc_raw",
               PATH_Q4K_TC_WQ: "q4k_tc_wq", PATH_TC_FUSED_RAW: "tc_fused_raw",
-              PATH_TC_FUSED_WH: "tc_fused_wh", PATH_Q4K_SKINNY: "q4k_skinny"}
+              PATH_TC_FUSED_WH: "tc_fused_wh", PATH_Q4K_SKINNY: "q4k_skinny",
+              PATH_Q4K_SKINNY_FUSED: "q4k_skinny_fused"}
 SKINNY_MAX_N = 16
 SKINNY_GROUPS_MAX_N = 64
 Q4K_SKINNY_MAX_N = 16
@@ -55,6 +56,7 @@ SIGNATURES = [
     ("q6k_mmq_noalloc_status", _I, [_P]),
     ("q6k_mmq_mma_sync", _I, [_P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _P, _IP, _P]),
     ("q6k_mmq_f32", _I, [_P, _I, _I, _P, _I, _I, _P, _I, _IP, _P]),
+    ("q4k_mmq_f32", _I, [_P, _I, _I, _P, _I, _I, _P, _I, _IP, _P]),
     ("q6k_mmq_f32_tc", _I, [_P, _P, _I, _I, _P, _I, _I, _P, _I, _P, ctypes.c_size_t, _IP, _P]),
     ("q8_act_sums_bytes", _I, [_I, _I, _SZ, _IP]),
     ("q8_quantize_act_sums", _I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -568,6 +570,26 @@ def q4k_unpack_weights(w: Q4Weights, out=None, stream=None):
     _tensor(out, "out", torch.float16, (w.M, w.K), w.device)
     _check(load().q4k_unpack_weights(_ptr(w.plane), w.M, w.K, _ptr(out), _stream(stream)))
     return out
+
+
+def q4k_mmq_f32(w: Q4Weights, X, Y=None, stream=None):
+    """One or two tokens of the q4_K GEMM straight from f32 activations X
+    [N, K] (N <= 2), in one kernel: the same Y, bit for bit, as
+    quantize_act(X, want_us=True) followed by q4k_mmq(). Returns (Y, path
+    name)."""
+    import torch
+    if not isinstance(X, torch.Tensor) or X.dim() != 2:
+        raise Q6Error(Q6_EINVAL, "X must be a 2-D torch tensor [N, K]")
+    N, K, M = X.shape[0], w.K, w.M
+    dev = w.device
+    _tensor(X, "X", torch.float32, (N, K), dev, rows=True)
+    if Y is None:
+        Y = torch.empty((N, M), dtype=torch.float32, device=dev)
+    _tensor(Y, "Y", torch.float32, (N, M), dev, rows=True)
+    path = ctypes.c_int(-1)
+    _check(load().q4k_mmq_f32(_ptr(w.plane), M, K, _ptr(X), _row_stride(X), N, _ptr(Y),
+                              _row_stride(Y), ctypes.byref(path), _stream(stream)))
+    return Y, PATH_NAMES.get(path.value, str(path.value))
 
 
 def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",

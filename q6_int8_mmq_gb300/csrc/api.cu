@@ -72,7 +72,8 @@ int device_state(DevState** out) {
     if ((e = cudaMalloc(&st.status, 256))) return cuda_fail(e, "cudaMalloc(status)");
     if ((e = cudaMemset(st.status, 0, 256))) return cuda_fail(e, "cudaMemset(status)");
     if ((e = q6::mmq_tc_prepare()) || (e = q6::mmq_skinny_prepare()) ||
-        (e = q6::mmq_sync_prepare()) || (e = q6::q4k_skinny_mma_prepare()))
+        (e = q6::mmq_sync_prepare()) || (e = q6::q4k_skinny_mma_prepare()) ||
+        (e = q6::q4k_skinny_prepare()))
       return cuda_fail(e, "cudaFuncSetAttribute");
     if (!encoder()) return fail(Q6_ECUDA, "cuTensorMapEncodeTiled entry point not found");
     st.arch_ok = 1;
@@ -651,6 +652,31 @@ int q4k_unpack_weights(const void* plane, int M, int K, uint16_t* wq, q6_stream_
   cudaError_t e = q6::launch_q4k_expand(static_cast<const uint8_t*>(plane), M, K, false,
                                         reinterpret_cast<__half*>(wq), (cudaStream_t)s);
   if (e != cudaSuccess) return cuda_fail(e, "q4k_unpack_weights launch");
+  return Q6_OK;
+}
+
+int q4k_mmq_f32(const void* plane, int M, int K, const float* X, int ldx, int N, float* Y,
+                int ldy, int* path_out, q6_stream_t s) {
+  if (path_out) *path_out = Q6_PATH_NONE;
+  if (M <= 0 || K <= 0 || K % 256 || N < 0 || N > Q6_FUSED_MAX_N)
+    return fail(Q6_EINVAL, "need M > 0, 0 <= N <= %d, K > 0, K %% 256 == 0", Q6_FUSED_MAX_N);
+  if (ldx < K) return fail(Q6_EINVAL, "ldx (%d) < K (%d)", ldx, K);
+  if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
+  if (N == 0) return Q6_OK;
+  if (!plane || !X || !Y) return fail(Q6_EINVAL, "plane, X and Y are required");
+  if (!aligned(plane, 256) || !aligned(X, 16) || ldx % 4 || !aligned(Y, 4))
+    return fail(Q6_EALIGN, "plane 256 B, X 16 B with ldx %% 4 == 0, Y 4 B");
+  if (q6::q4k_skinny_fused_smem(K, N) > (size_t)q6::kFusedSmemMax)
+    return fail(Q6_ESIZE, "K = %d is too large for %d token(s) in one launch", K, N);
+  if ((long long)N * ldy > (1LL << 40) || (long long)M * K > (1LL << 40))
+    return fail(Q6_ESIZE, "problem too large");
+  DevState* st;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = q6::launch_q4k_skinny_fused(static_cast<const uint8_t*>(plane), M, K, X, ldx,
+                                              N, Y, ldy, (cudaStream_t)s);
+  if (e != cudaSuccess) return cuda_fail(e, "q4_K fused one/two-token kernel launch");
+  if (path_out) *path_out = Q6_PATH_Q4K_SKINNY_FUSED;
   return Q6_OK;
 }
 

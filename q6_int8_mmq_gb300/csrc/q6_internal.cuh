@@ -158,6 +158,12 @@ cudaError_t launch_mmq_tc_q4k(const TcMaps& maps, int M, int K, int N, float* Y,
 cudaError_t launch_q4k_skinny(const uint8_t* plane, int M, int K, const int8_t* Xq,
                               const float* da, int ldda, const float* us, int N, float* Y,
                               int ldy, int32_t* partials, cudaStream_t s);
+// q4_K quantise + GEMM for N <= 2 tokens from f32 X [N][ldx] in one launch
+// (q4k_skinny.cu); needs q4k_skinny_fused_smem(K, N) <= kFusedSmemMax bytes.
+size_t q4k_skinny_fused_smem(int K, int N);
+cudaError_t launch_q4k_skinny_fused(const uint8_t* plane, int M, int K, const float* X, int ldx,
+                                    int N, float* Y, int ldy, cudaStream_t s);
+cudaError_t q4k_skinny_prepare();
 // The same product for a few more tokens (N <= 16) on the warp-level f16
 // tensor path with TMA-staged nibbles and activations (q4k_skinny_mma.cu).
 cudaError_t launch_q4k_skinny_mma(const uint8_t* plane, int M, int K, const int8_t* Xq,

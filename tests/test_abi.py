@@ -150,6 +150,21 @@ def test_host_side_rejections(lib):
     assert f32tc(wh=None, ws=fake, ws_bytes=64 * 256 * 4 - 1) == q6.Q6_ESIZE
     assert f32tc(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
+    # the fused one/two-token q4_K call: N <= 2, ldx, alignment, the shared-memory
+    # limit on K, the empty case
+    def q4f(plane=fake, M=64, K=256, X=fake, ldx=256, N=1, Y=fake, ldy=64):
+        return lib.q4k_mmq_f32(plane, M, K, X, ldx, N, Y, ldy, ctypes.byref(path), None)
+
+    assert q4f(N=3) == q6.Q6_EINVAL and path.value == q6.PATH_NONE
+    assert q4f(ldx=128) == q6.Q6_EINVAL
+    assert q4f(X=None) == q6.Q6_EINVAL
+    assert q4f(X=odd) == q6.Q6_EALIGN
+    assert q4f(ldx=258) == q6.Q6_EALIGN
+    assert q4f(plane=odd) == q6.Q6_EALIGN
+    assert q4f(K=92928 + 256, ldx=92928 + 256, N=2) == q6.Q6_ESIZE
+    assert q4f(K=185856 + 256, ldx=185856 + 256, N=1) == q6.Q6_ESIZE
+    assert q4f(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
+
     # the q4_K GEMM: Xq for N <= 16; Xh beyond, unless Xq is there, the plane
     # is not resident and N <= 48 (token groups); ldy < M, K % 256, misaligned
     # pointers, no workspace for the tensor-core unpack, the empty case

@@ -359,3 +359,84 @@ def test_q4k_long_rows(q6, orc, N):
     Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
     assert np.array_equal(host(P), Po), "sub-block partials differ"
     check_y(host(Y), Yo, f"q4k long rows N={N}")
+
+
+@pytest.mark.parametrize("M,K,N", [(4096, 11008, 1), (4096, 11008, 2), (1, 256, 1),
+                                   (131, 2816, 2), (5003, 768, 2), (2059, 1024, 1)],
+                         ids=lambda v: str(v))
+def test_q4k_mmq_f32_equals_two_calls(q6, orc, M, K, N):
+    """The fused one/two-token q4_K call gives bit for bit the Y of
+    quantize_act (with block sums) followed by q4k_mmq (the same codes,
+    scales, block sums, dot products and order), on ordinary activations and
+    on blocks at and beside rounding ties, with subnormal and very large
+    scales; Y within tolerance of the oracle on every output. The shapes
+    cover the full-size weights, one row, an odd super-block count, more rows
+    than warps and one super-block per row."""
+    import torch
+    from test_gpu_parity import hard_activations
+    raw = synth.q4k_raw_weights(0x51361801 + M + N, M, K)
+    w = q6.q4k_pack_weights(dev(raw), M, K)
+    X0 = synth.activations(0x51361802 + K + N, N, K, outlier_frac=0.01)
+    for X in (X0, hard_activations(0x51361803 + N, N, K, big=np.float32(1e30))):
+        Xd = dev(X)
+        Y, path = q6.q4k_mmq_f32(w, Xd)
+        act = q6.quantize_act(Xd, want_us=True)
+        Y2, path2, _ = q6.q4k_mmq(w, act)
+        q6.sync_status()
+        assert path == "q4k_skinny_fused" and path2 == "q4k_skinny"
+        assert torch.equal(Y, Y2), "fused and separate quantisation disagree"
+    act, xq_o, da_o = quantize(q6, orc, X0)
+    Yo = (orc.q4k_mmq_all(raw, M, K, xq_o, da_o) if M * K > 1 << 22
+          else orc.q4k_mmq(raw, M, K, xq_o, da_o))
+    Y, _ = q6.q4k_mmq_f32(w, dev(X0))
+    q6.sync_status()
+    check_y(host(Y), Yo, f"q4k fused {M}x{K}x{N}")
+
+
+@pytest.mark.parametrize("K,N", [(92928, 2), (185856, 1)], ids=lambda v: str(v))
+def test_q4k_mmq_f32_largest_k(q6, orc, K, N):
+    """The largest K whose codes, scales and block sums fit the fused
+    kernel's shared memory for N tokens (232,320 of 232,448 bytes): the same
+    Y as the two calls, within tolerance of the oracle; one more super-block
+    is refused."""
+    import torch
+    M = 64
+    raw = synth.q4k_raw_weights(0x51361811 + N, M, K)
+    X = synth.activations(0x51361812 + N, N, K, outlier_frac=0.01)
+    w = q6.q4k_pack_weights(dev(raw), M, K)
+    Xd = dev(X)
+    Y, path = q6.q4k_mmq_f32(w, Xd)
+    act, xq_o, da_o = quantize(q6, orc, X)
+    Y2, _, _ = q6.q4k_mmq(w, act)
+    q6.sync_status()
+    assert path == "q4k_skinny_fused" and torch.equal(Y, Y2)
+    check_y(host(Y), orc.q4k_mmq(raw, M, K, xq_o, da_o), f"q4k fused K={K} N={N}")
+    K2 = K + 256
+    w2 = q6.q4k_pack_weights(dev(synth.q4k_raw_weights(0x51361813, M, K2)), M, K2)
+    with pytest.raises(q6.Q6Error):
+        q6.q4k_mmq_f32(w2, dev(synth.activations(0x51361814, N, K2)))
+
+
+def test_q4k_mmq_f32_strided_input_and_output(q6):
+    """X with a wider row stride, Y with an odd row stride at an unaligned
+    address: the floats between Y's rows stay untouched, the result equals
+    the two calls'; three tokens are refused."""
+    import torch
+    M, K, N = 328, 1024, 2
+    raw = synth.q4k_raw_weights(0x51361821, M, K)
+    w = q6.q4k_pack_weights(dev(raw), M, K)
+    big = torch.full((N, K + 64), float("nan"), dtype=torch.float32, device="cuda")
+    big[:, :K] = dev(synth.activations(0x51361822, N, K))
+    Xv = big[:, :K]
+    ldy = M + 37
+    buf = torch.full((N * ldy + 1,), float("nan"), dtype=torch.float32, device="cuda")
+    Yv = buf[1:].view(N, ldy)[:, :M]
+    Y, path = q6.q4k_mmq_f32(w, Xv, Y=Yv)
+    Y2, _, _ = q6.q4k_mmq(w, q6.quantize_act(Xv, want_us=True))
+    q6.sync_status()
+    assert path == "q4k_skinny_fused" and Y.data_ptr() == Yv.data_ptr()
+    assert torch.equal(Yv, Y2)
+    b = host(buf)
+    assert np.isnan(b[0]) and np.all(np.isnan(b[1:].reshape(N, ldy)[:, M:]))
+    with pytest.raises(q6.Q6Error):
+        q6.q4k_mmq_f32(w, dev(synth.activations(0x51361823, 3, K)))   # three tokens
