@@ -236,11 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float d_b = have_b ? __half2float(*reinterpret_cast<const __half*>(
                                        b + geo.d + (size_t)rb * kDPitch + 2 * sbw))
                                  : 0.0f;
-        float sbs[kNT][4];
+        // f32 pairs over the tokens (t0, t0 + 1) of a lane: [token tile][row a, b]
+        float2 sbs[kNT][2];
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sbs[nt][i] = 0.0f;
+        for (int nt = 0; nt < kNT; ++nt) sbs[nt][0] = sbs[nt][1] = make_float2(0.0f, 0.0f);
 
         // activation words of a chunk (two sub-blocks, each token group) from
         // the stage's activation boxes (tokens past N were filled with 0),
@@ -260,11 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = 8 * sb + c8;  // chunk
           if (c8 == 0 || c8 == 4) load_half(c8 >> 2);
           if (c8 < 7) load_x(c8 + 1, xnxt);
-          float S[kNT][4];
+          float2 S[kNT][2];
 #pragma unroll
-          for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) S[nt][i] = 0.0f;
+          for (int nt = 0; nt < kNT; ++nt) S[nt][0] = S[nt][1] = make_float2(0.0f, 0.0f);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int s16 = 2 * c8 + e, j = s16 & 7;
@@ -276,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               a[2 + rr] = code_pair<1>(code);  // codes 4t + 1, 4t + 3
             }
             const float sa = sc_of(sca4, s16), sbv = sc_of(scb4, s16);
+            const float2 sa2 = make_float2(sa, sa), sb2 = make_float2(sbv, sbv);
 #pragma unroll
             for (int nt = 0; nt < kNT; ++nt) {
               const uint32_t wb = xcur[e][nt] ^ 0x80808080u;
@@ -292,29 +290,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (int32_t)P[i];
                 }
               }
-              // sc * P and their sum over the chunk are exact in f32 (< 2^24)
-              S[nt][0] = fmaf(sa, P[0], S[nt][0]);
-              S[nt][1] = fmaf(sa, P[1], S[nt][1]);
-              S[nt][2] = fmaf(sbv, P[2], S[nt][2]);
-              S[nt][3] = fmaf(sbv, P[3], S[nt][3]);
+              // sc * P and their sum over the chunk are exact in f32 (< 2^24);
+              // one two-lane FMA per row (each lane rounds as fmaf does)
+              S[nt][0] = __ffma2_rn(sa2, make_float2(P[0], P[1]), S[nt][0]);
+              S[nt][1] = __ffma2_rn(sb2, make_float2(P[2], P[3]), S[nt][1]);
             }
           }
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             const int t0 = 8 * nt + 2 * t;
-            const float* sda = reinterpret_cast<const float*>(b + geo.da) + (8 * sbw + c8) * ldda;
-            const float d0 = t0 < N ? sda[t0] : 0.0f;
-            const float d1 = t0 + 1 < N ? sda[t0 + 1] : 0.0f;
-            sbs[nt][0] = fmaf(d0, S[nt][0], sbs[nt][0]);
-            sbs[nt][1] = fmaf(d1, S[nt][1], sbs[nt][1]);
-            sbs[nt][2] = fmaf(d0, S[nt][2], sbs[nt][2]);
-            sbs[nt][3] = fmaf(d1, S[nt][3], sbs[nt][3]);
+            // da of tokens (t0, t0 + 1): the stage's da rows have ldda (a
+            // multiple of 4) columns and 8 * kNT >= ldda, so the pair stays in
+            // the region; a column at or past N carries whatever the plane
+            // holds there and only reaches lanes of tokens that are never stored
+            const float2 d01 = *reinterpret_cast<const float2*>(
+                reinterpret_cast<const float*>(b + geo.da) + (8 * sbw + c8) * ldda + t0);
+            sbs[nt][0] = __ffma2_rn(d01, S[nt][0], sbs[nt][0]);
+            sbs[nt][1] = __ffma2_rn(d01, S[nt][1], sbs[nt][1]);
             if (kPartials && chunks) {
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
                 const int rl = (i < 2) ? ra : rb, tk = t0 + (i & 1);
+                const float2 v = S[nt][i >> 1];
                 if (rl < R && r0 + rl < M && tk < N)
-                  chunks[((size_t)tk * M + r0 + rl) * (size_t)nc + c] = (int32_t)S[nt][i];
+                  chunks[((size_t)tk * M + r0 + rl) * (size_t)nc + c] = (int32_t)((i & 1) ? v.y : v.x);
               }
             }
           }
@@ -325,10 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
-          acc[nt][0] = fmaf(d_a, sbs[nt][0], acc[nt][0]);
-          acc[nt][1] = fmaf(d_a, sbs[nt][1], acc[nt][1]);
-          acc[nt][2] = fmaf(d_b, sbs[nt][2], acc[nt][2]);
-          acc[nt][3] = fmaf(d_b, sbs[nt][3], acc[nt][3]);
+          acc[nt][0] = fmaf(d_a, sbs[nt][0].x, acc[nt][0]);
+          acc[nt][1] = fmaf(d_a, sbs[nt][0].y, acc[nt][1]);
+          acc[nt][2] = fmaf(d_b, sbs[nt][1].x, acc[nt][2]);
+          acc[nt][3] = fmaf(d_b, sbs[nt][1].y, acc[nt][3]);
         }
       }
       __syncwarp();
