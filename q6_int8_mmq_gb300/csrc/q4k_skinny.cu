@@ -21,7 +21,9 @@
 // dot products and re-reads its activations for every row (from L1), so the
 // time grows by about 6 us a token on 4096 x 11008 weights; beyond
 // Q6_Q4K_DP4A_MAX_N tokens the warp-level f16 MMA kernel, which shares each
-// activation fragment across 16 rows, is faster.
+// activation fragment across 16 rows, is faster. The file also holds the
+// fused kernel behind q4k_mmq_f32 (at its end), which quantises one or two
+// f32 activation rows itself and then runs the same row dot products.
 #include "q6_quant.cuh"
 
 namespace q6 {
