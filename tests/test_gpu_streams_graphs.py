@@ -168,3 +168,52 @@ def test_q4k_path_in_a_cuda_graph(q6, N, source):
     assert path[0] == ("q4k_skinny" if N <= q6.Q4K_SKINNY_MAX_N or
                        (source == "raw" and N <= q6.Q4K_GROUPS_MAX_N) else
                        {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source])
+
+
+@pytest.mark.parametrize("N", [1, 2])
+def test_q4k_fused_call_on_a_side_stream_and_in_a_graph(q6, N):
+    """q4k_mmq_f32 (quantiser with block sums and the q4_K GEMM in one
+    kernel) on a caller's side stream, then two such calls chained in one
+    CUDA graph, the second reading the first's Y as its activations (a
+    dependent launch that must see the previous kernel's writes), replayed
+    for two inputs."""
+    import torch
+    orc = oracle.get()
+    M1, K1, M2 = 512, 2048, 768             # layer 2 takes layer 1's 512 outputs
+    raw1 = synth.q4k_raw_weights(0x51360931 + N, M1, K1)
+    raw2 = synth.q4k_raw_weights(0x51360932 + N, M2, M1)
+    X1 = synth.activations(0x51360933 + N, N, K1)
+    X2 = synth.activations(0x51360934 + N, N, K1, outlier_frac=0.02)
+    w1 = q6.q4k_pack_weights(torch.from_numpy(raw1).cuda(), M1, K1)
+    w2 = q6.q4k_pack_weights(torch.from_numpy(raw2).cuda(), M2, M1)
+
+    def expect(raw, M, K, X):
+        xq, da = orc.quantize(X)
+        return orc.q4k_mmq(raw, M, K, xq, da)
+
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        Y, path = q6.q4k_mmq_f32(w1, torch.from_numpy(X1).cuda(), stream=side)
+    q6.sync_status(side)
+    assert path == "q4k_skinny_fused"
+    close(Y, expect(raw1, M1, K1, X1))
+    Xs = torch.from_numpy(X1).cuda()             # static input of the graph
+    Y1 = torch.empty((N, M1), dtype=torch.float32, device="cuda")
+    Y2 = torch.empty((N, M2), dtype=torch.float32, device="cuda")
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            q6.q4k_mmq_f32(w1, Xs, Y=Y1)
+            q6.q4k_mmq_f32(w2, Y1, Y=Y2)
+    for X in (X1, X2):
+        Xs.copy_(torch.from_numpy(X).cuda())
+        Y1.fill_(float("nan"))
+        Y2.fill_(float("nan"))
+        graph.replay()
+        q6.sync_status()
+        y1 = Y1.cpu().numpy()
+        close(Y1, expect(raw1, M1, K1, X))
+        # layer 2 against the oracle on the GPU's own layer-1 output
+        close(Y2, expect(raw2, M2, M1, y1))
