@@ -834,6 +834,8 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         "hbm_peak": {"gbs": hbm, "source": hbm_src},
         "pack_ms": pack_ms, "other_weight_sources": alt, "other_configs": others,
     }
+    if others:
+        line["five_configs"] = five_configs(M, K, N, m_ms, peak_t, hbm, others)
     print(json.dumps(line), flush=True)
 
 
@@ -1027,7 +1029,65 @@ def other_configs(args, q6, synth, device, hbm):
     res["q4k_ffn_down"] = q4k_gemm(q6, synth, device)
     res["q4k_pages_ffn_up"] = q4k_gemm(q6, synth, device, "pages_ffn_up")
     res["sweep"] = sweep_short(q6, synth, device)
+    res["tiny"] = tiny_times(q6, synth, device)
     return res
+
+
+def tiny_times(q6, synth, device):
+    """The tiny config (256 x 512 weights, 8 tokens): one q6k_mmq (the
+    few-token kernel) per call, timed by CUDA-graph replay; it is one short
+    launch on inputs resident in L2."""
+    import torch
+    raw, X, cfg = synth.workload("tiny")
+    M, K, N = cfg["M"], cfg["K"], cfg["N"]
+    W = q6.pack_weights(torch.from_numpy(raw).to(device), M, K)
+    act = q6.quantize_act(torch.from_numpy(X).to(device))
+    Y = torch.empty((N, M), dtype=torch.float32, device=device)
+    q6.mmq(W, act, Y=Y)
+    ms = graph_ms(lambda i: q6.mmq(W, act, Y=Y), 200)
+    q6.sync_status()
+    return {"M": M, "K": K, "N": N, "ms": ms, "tops": 2.0 * M * N * K / ms / 1e9,
+            "path": q6.mmq(W, act, Y=Y)[1]}
+
+
+def five_configs(M, K, N, gemm_ms, peak_t, hbm, others):
+    """The five configs side by side as the method is reported: effective
+    int8 TOPS (2*M*N*K per second), us per GMAC, and the fraction of the
+    roofline that bounds each (the f16 tensor burst peak for the prefill
+    GEMMs, HBM for the few-token ones, with the method's bytes)."""
+    def gemm(ms, m, k, n):
+        tops = 2.0 * m * n * k / ms / 1e9
+        return {"ms": ms, "tops": tops, "us_per_gmac": ms * 1e3 / (m * n * k / 1e9),
+                "roofline": {"bound": "tensor", "frac": tops / peak_t, "peak_tflops": peak_t}}
+
+    def skinny(v, m, k, n):
+        us = v["us"]
+        return {"us": us, "tops": 2.0 * m * n * k / us / 1e6,
+                "us_per_gmac": us / (m * n * k / 1e9),
+                "roofline": {"bound": "hbm", "frac": v["gbs"] / hbm, "peak_gbs": hbm}}
+
+    out = {}
+    t = others.get("tiny")
+    if t:
+        out["C0_tiny"] = dict(skinny({"us": t["ms"] * 1e3,
+                                      "gbs": skinny_bytes(t["M"], t["K"], t["N"]) / t["ms"] / 1e6},
+                                     t["M"], t["K"], t["N"]),
+                              note="one launch on L2-resident inputs: launch latency, not HBM")
+    if "attn_v_wh" in others:
+        out["C1_attn_v"] = gemm(others["attn_v_wh"]["ms"], 4096, 4096, 512)
+    out["C2_ffn_down"] = gemm(gemm_ms, M, K, N)
+    for w, (m, k) in (("ffn_down", (4096, 11008)), ("attn_v", (4096, 4096))):
+        for n in (1, 4, 16):
+            v = others.get(f"skinny_{w}_N{n}")
+            if v:
+                out[f"C3_{w}_N{n}"] = skinny(v, m, k, n)
+    sw = others.get("sweep")
+    if sw:
+        out["C4_sweep"] = {"ms_per_sweep": sw["ms_per_sweep"], "tops": sw["tops"],
+                           "gemm_total_ms": sw["gemm_total_ms"], "gemm_tops": sw["gemm_tops"],
+                           "roofline": {"bound": "tensor", "frac": sw["gemm_tops"] / peak_t,
+                                        "peak_tflops": peak_t}}
+    return out
 
 
 def pages_shapes(q6, synth, device):
