@@ -230,6 +230,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) mmq_skinny_kernel(
     const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const int8_t* __restrict__ Xq,
     const float* __restrict__ da, int ldda, int N, float* __restrict__ Y, int ldy,
     int32_t* __restrict__ partials, int32_t* __restrict__ chunks) {
+  // No early griddep_launch_dependents() here: with eight CTAs per SM the
+  // next few-token kernel's CTAs become resident beside this grid's tail,
+  // which measured slower (one token 9.1 -> 9.7 us, two 13.9 -> 14.8 us).
   griddep_wait();  // launched as a dependent launch: global memory from here on
   const int warps = (int)gridDim.x * kWarps;
   for (int m = (threadIdx.x >> 5) * (int)gridDim.x + blockIdx.x; m < M; m += warps)
@@ -260,6 +263,7 @@ template <int kMaxN>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) mmq_skinny_fused_kernel(
     const uint8_t* __restrict__ plane, PlaneGeom g, int M, int K, const float* __restrict__ X,
     int ldx, int N, float* __restrict__ Y, int ldy) {
+  griddep_launch_dependents();  // the next dependent launch may start its prologue
   griddep_wait();  // launched as a dependent launch: global memory from here on
   extern __shared__ __align__(16) uint8_t fused_smem[];
   int8_t* xs = reinterpret_cast<int8_t*>(fused_smem);                     // codes [N][K]

@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   __syncthreads();
+  griddep_launch_dependents();  // the next dependent launch may start its prologue
   griddep_wait();  // launched as a dependent launch: global memory from here on
 
   if (warp == kCW) {
