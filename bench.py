@@ -1616,8 +1616,8 @@ SKINNY_FUSED_MAX_N = 2
 
 # DRAM bytes per launch from ncu captures of the current kernels, keyed by
 # (workload, kernel). An entry is removed when its kernel changes (the
-# few-token entries were taken again once those kernels became dependent
-# launches).
+# few-token entries were taken again after those kernels' last change, the
+# early dependent trigger).
 TRAFFIC = {("ffn_down", "mmq_tc"): 670.08e6 + 54.96e6,
            ("q4k_ffn_down", "mmq_tc_q4k"): 634.90e6 + 59.67e6,
            ("q4k_skinny_N1", "q4k_skinny_fused"): 26.83e6,
@@ -1626,7 +1626,7 @@ TRAFFIC = {("ffn_down", "mmq_tc"): 670.08e6 + 54.96e6,
            ("skinny_ffn_down_N1", "mmq_skinny_fused"): 37.09e6,
            ("skinny_ffn_down_N2", "mmq_skinny_fused"): 37.14e6,
            ("skinny_ffn_down_N4", "mmq_skinny"): 37.11e6,
-           ("skinny_ffn_down_N16", "mmq_skinny"): 37.26e6}
+           ("skinny_ffn_down_N16", "mmq_skinny"): 37.27e6}
 
 
 def main():
