@@ -395,6 +395,49 @@ def e2e_run_overlapped(step, ins, outs, steps: int, device):
     return reduce_max(a.elapsed_time(b), device)
 
 
+def link_floor(x_dev, x_host, y_host, y_dev, reps: int = 10):
+    """The host link's floor for one step's copies: the step's H2D (x) and
+    D2H (y) issued together on two streams with no compute, averaged over
+    `reps` rounds. Returns the floor in ms and the rates it implies."""
+    import torch
+    cur = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def once():
+        up.wait_stream(cur)
+        down.wait_stream(cur)
+        with torch.cuda.stream(up):
+            x_dev.copy_(x_host, non_blocking=True)
+        with torch.cuda.stream(down):
+            y_host.copy_(y_dev, non_blocking=True)
+        cur.wait_stream(up)
+        cur.wait_stream(down)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = ev_pair()
+        a.record(cur)
+        for _ in range(reps):
+            fn()
+        b.record(cur)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def h2d():
+        up.wait_stream(cur)
+        with torch.cuda.stream(up):
+            x_dev.copy_(x_host, non_blocking=True)
+        cur.wait_stream(up)
+
+    both_ms, h2d_ms = timed(once), timed(h2d)
+    nx, ny = x_host.numel() * x_host.element_size(), y_host.numel() * y_host.element_size()
+    return {"floor_ms": both_ms, "h2d_gbs": nx / h2d_ms / 1e6,
+            "both_gbs": (nx + ny) / both_ms / 1e6,
+            "note": "the step's H2D and D2H together on two streams, no compute; frac = "
+                    "floor_ms / e2e ms_per_step"}
+
+
 def e2e_graph(step_host, steps: int, device) -> float:
     """End to end for the small-batch path, the way a decode loop runs it: the
     K steps, each with its H2D copy from pinned host memory, its compute and
@@ -778,6 +821,9 @@ def run_gemm(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
                "unit": UNIT, "h2d_bytes_per_step": X.nbytes, "d2h_bytes_per_step": N * M * 4,
                "steps": args.e2e_steps, "ms_per_step": e_ms / args.e2e_steps,
                "copies": OVERLAP}
+        link = link_floor(Xs[0], Xh, Yh[0], Ys[0])
+        link["frac"] = link["floor_ms"] / e2e["ms_per_step"]
+        e2e["host_link"] = link
 
     others = {}
     if rank == 0 and world == 1 and args.workload == "ffn_down" and args.other_configs:
