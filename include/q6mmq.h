@@ -81,13 +81,16 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
  * against 54 at 56 tokens). */
 #define Q6_Q4K_GROUPS_MAX_N 48
 
-/* q6k_mmq without resident operand planes (wh NULL) and with Xq runs
- * Q6_SKINNY_MAX_N < N <= Q6_SKINNY_GROUPS_MAX_N on the few-token kernels, in
- * token groups of at most Q6_SKINNY_MAX_N (each streams the 0.82-byte packed
- * plane once; measured on GB300, 4096 x 11008: 17 / 33 / 48 / 64 tokens in
- * about 31 / 49 / 59 / 78 us against 77-79 us for unpacking 4 bytes a weight
- * and the tensor-core GEMM). */
+/* q6k_mmq with Xq runs Q6_SKINNY_MAX_N < N <= Q6_SKINNY_GROUP_N on the
+ * few-token kernels whatever the weight source, and, without resident operand
+ * planes (wh NULL), N <= Q6_SKINNY_GROUPS_MAX_N too, in token groups of at
+ * most Q6_SKINNY_GROUP_N (each group streams the 0.82-byte packed plane once;
+ * measured on GB300, 4096 x 11008: 17 / 32 / 48 / 64 tokens in about 27 / 28 /
+ * 45 / 54 us, against 77-79 us for unpacking 4 bytes a weight and the
+ * tensor-core GEMM, and 37-38 us for the tensor cores on resident planes at
+ * 17-32 tokens). */
 #define Q6_SKINNY_GROUPS_MAX_N 64
+#define Q6_SKINNY_GROUP_N 32
 
 #define Q6_SKINNY_MAX_N 16
 #define Q6_FUSED_MAX_N 2   /* tokens q6k_mmq_f32 takes */
@@ -220,8 +223,10 @@ int q6k_unpack_weights(const void *plane, const int8_t *wexp, int M, int K, uint
  *   Xq, da: quantised activations (layouts above). Xq is read by the
  *           few-token kernels (N <= Q6_SKINNY_MAX_N: dp4a on the CUDA cores
  *           for one or two tokens, exact f16 mma.sync for 3..16 tokens; both
- *           stream the packed plane once), and, without wh, for up to
- *           Q6_SKINNY_GROUPS_MAX_N tokens on token groups of at most 16.
+ *           stream the packed plane once), and, on token groups of at most
+ *           Q6_SKINNY_GROUP_N (the same mma.sync kernel holds 17..32 tokens),
+ *           for up to Q6_SKINNY_GROUP_N tokens whatever the weight source and
+ *           without wh for up to Q6_SKINNY_GROUPS_MAX_N tokens.
  *   Xh    : the binary16 operand plane; required when N > Q6_SKINNY_MAX_N,
  *           unless the token groups apply.
  *   workspace : device scratch, 256-byte aligned, of at least
@@ -263,8 +268,9 @@ int q6k_mmq_workspace_bytes(int M, int K, int N, size_t *bytes);
 
 /* The number of kernels one q6k_mmq call launches for this shape on the
  * calling thread's current device: 0 for N == 0; 1 on the skinny path
- * (N <= Q6_SKINNY_MAX_N); ceil(N / Q6_SKINNY_MAX_N) on token groups
- * (has_wh == 0 and N <= Q6_SKINNY_GROUPS_MAX_N, counted as if Xq is given);
+ * (N <= Q6_SKINNY_MAX_N); ceil(N / Q6_SKINNY_GROUP_N) on token groups
+ * (N <= Q6_SKINNY_GROUP_N, or has_wh == 0 and N <= Q6_SKINNY_GROUPS_MAX_N,
+ * counted as if Xq is given);
  * otherwise 1 for the tensor-core GEMM, plus 1 when
  * either work split above applies (the zeroing of the split last round, or
  * the addition of the K parts, counted as if the workspace had room for

@@ -29,6 +29,7 @@ PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_Q4K_SKINNY_FUSED: "q4k_skinny_fused"}
 SKINNY_MAX_N = 16
 SKINNY_GROUPS_MAX_N = 64
+SKINNY_GROUP_N = 32
 Q4K_SKINNY_MAX_N = 16
 Q4K_DP4A_MAX_N = 2
 Q4K_GROUPS_MAX_N = 48
@@ -381,8 +382,9 @@ def mmq(w: Weights, act: Activations, Y=None, source: str = "auto", partials: bo
     source: "raw" (unpack the packed plane), "wexp" (convert the W_exp plane),
     "wh" (resident binary16 plane) or "auto" (wh, else wexp, else raw). Up to
     SKINNY_MAX_N tokens run the few-token kernels on the packed plane whatever
-    the source; up to SKINNY_GROUPS_MAX_N tokens too when act has xq and the
-    source is not "wh" (token groups of at most SKINNY_MAX_N)."""
+    the source; when act has xq, up to SKINNY_GROUP_N tokens too whatever the
+    source and up to SKINNY_GROUPS_MAX_N when the source is not "wh" (token
+    groups of at most SKINNY_GROUP_N)."""
     import torch
     N, M, K = act.N, w.M, w.K
     if act.K != K:

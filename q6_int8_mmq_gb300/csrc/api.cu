@@ -402,8 +402,8 @@ int q6k_mmq_launches(int M, int K, int N, int has_wh, int* launches) {
     *launches = 0;
   } else if (N <= Q6_SKINNY_MAX_N) {
     *launches = 1;
-  } else if (!has_wh && N <= Q6_SKINNY_GROUPS_MAX_N) {
-    *launches = (N + Q6_SKINNY_MAX_N - 1) / Q6_SKINNY_MAX_N;  // token groups (given Xq)
+  } else if (N <= Q6_SKINNY_GROUP_N || (!has_wh && N <= Q6_SKINNY_GROUPS_MAX_N)) {
+    *launches = (N + Q6_SKINNY_GROUP_N - 1) / Q6_SKINNY_GROUP_N;  // token groups (given Xq)
   } else {
     int dev = 0, sms = 0;
     cudaError_t e;
@@ -426,9 +426,12 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   if (N == 0) return Q6_OK;
   if (!plane || !da || !Y) return fail(Q6_EINVAL, "plane, da and Y are required");
   const bool skinny = N <= Q6_SKINNY_MAX_N;
-  // a few more tokens without resident planes: the few-token kernels on
-  // token groups, instead of unpacking the weights for the tensor cores
-  const bool groups = !skinny && N <= Q6_SKINNY_GROUPS_MAX_N && !wh && Xq;
+  // a few more tokens given Xq: the few-token kernels on token groups, up to
+  // one group's width whatever the weight source (faster than the tensor
+  // cores there), and up to Q6_SKINNY_GROUPS_MAX_N without resident planes
+  // (instead of unpacking the weights for the tensor cores)
+  const bool groups = !skinny && Xq &&
+                      (N <= Q6_SKINNY_GROUP_N || (N <= Q6_SKINNY_GROUPS_MAX_N && !wh));
   if (skinny && !Xq) return fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_SKINNY_MAX_N);
   if (!skinny && !groups && !Xh)
     return fail(Q6_EINVAL, "Xh is required when N > %d", Q6_SKINNY_MAX_N);
@@ -462,9 +465,9 @@ int q6k_mmq(const void* plane, const int8_t* wexp, const uint16_t* wh, int M, in
   }
   if (groups) {
     // token group g: rows n0 .. n0 + ng - 1 of Xq, Y and the debug outputs,
-    // columns n0 .. of da (n0 a multiple of 16: 16-byte aligned)
-    for (int n0 = 0; n0 < N; n0 += Q6_SKINNY_MAX_N) {
-      const int ng = N - n0 < Q6_SKINNY_MAX_N ? N - n0 : Q6_SKINNY_MAX_N;
+    // columns n0 .. of da (n0 a multiple of 32: 16-byte aligned)
+    for (int n0 = 0; n0 < N; n0 += Q6_SKINNY_GROUP_N) {
+      const int ng = N - n0 < Q6_SKINNY_GROUP_N ? N - n0 : Q6_SKINNY_GROUP_N;
       q6::Debug dg;
       dg.partials = partials ? partials + (size_t)n0 * M * (K / 16) : nullptr;
       dg.chunk_sums = chunk_sums ? chunk_sums + (size_t)n0 * M * (K / 32) : nullptr;

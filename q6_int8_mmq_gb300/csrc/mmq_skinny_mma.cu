@@ -51,17 +51,29 @@
 namespace q6 {
 namespace {
 
-constexpr int kSbs = 8;                  // super-blocks per stage
-constexpr int kCW = 2 * kSbs;            // consumer warps: super-block x row group of 16
-constexpr int kThreads = 32 * (kCW + 1);  // + one producer warp
 constexpr int kMaxNS = 3;                // ring stages (2 or 3, by the shared-memory budget)
 constexpr int kMaxR = 32;                // rows per unit (two MMA row groups)
-constexpr int kQPitch = 1552;            // bytes per row of a qlh stage (194 x 8)
-constexpr int kScPitch = 144;            // bytes per row of an sc stage (18 x 8)
 constexpr int kDPitch = 16;              // bytes per row of a d stage (2 x 8)
-constexpr int kXPitch = 1040;            // bytes per token row of an activation half-stage (130 x 8)
+constexpr int kXPitch = 1040;            // bytes per token row of an activation box (130 x 8)
 constexpr int kSmemBudget = 227 * 1024;
-constexpr int kRedBytes = kSbs * kMaxR * 16 * 4;
+
+// The stage shape for kNT token tiles of 8. Up to 16 tokens a stage holds 8
+// super-blocks and 16 consumer warps (super-block x row group) take them.
+// For 17..32 tokens (kNT = 4) the activation rows of 8 super-blocks would not
+// fit twice in shared memory, so a stage holds 4 super-blocks for 8 consumer
+// warps, each of which forms the MMAs of all four token tiles on one weight
+// fragment (more registers a warp: 9 warps a CTA instead of 17).
+template <int kNT>
+struct Shape {
+  static constexpr int kSbs = kNT <= 2 ? 8 : 4;     // super-blocks per stage
+  static constexpr int kCW = 2 * kSbs;              // consumer warps
+  static constexpr int kThreads = 32 * (kCW + 1);   // + one producer warp
+  static constexpr int kQPitch = 192 * kSbs + 16;   // bytes per row of a qlh stage (1552 / 784)
+  static constexpr int kScPitch = 16 * kSbs + 16;   // bytes per row of an sc stage (144 / 80)
+  static constexpr int kXBoxes = kSbs / 4;          // activation boxes of 1024 (+16) bytes a token
+  static constexpr int kRedTok = kNT <= 2 ? 16 : 8 * kNT;  // token columns of the final sums
+  static constexpr int kRedBytes = kSbs * kMaxR * kRedTok * 4;
+};
 
 enum : uint32_t { kSiteEmpty = 21, kSiteFull = 22 };
 
@@ -69,18 +81,22 @@ struct Geo {  // byte offsets of one stage's regions and the stage size, for R r
   int sc, d, x0, x1, da, stage;
 };
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
-__host__ __device__ inline Geo stage_geo(int R, int XR) {
+template <int kNT>
+__host__ __device__ inline Geo stage_geo(int R) {
+  using S = Shape<kNT>;
+  constexpr int XR = 8 * kNT;  // token rows of an activation stage
   Geo g;
-  g.sc = align128(R * kQPitch);
-  g.d = align128(g.sc + R * kScPitch);
+  g.sc = align128(R * S::kQPitch);
+  g.d = align128(g.sc + R * S::kScPitch);
   g.x0 = align128(g.d + R * kDPitch);
-  g.x1 = align128(g.x0 + XR * kXPitch);
+  g.x1 = S::kXBoxes == 2 ? align128(g.x0 + XR * kXPitch) : g.x0;
   g.da = align128(g.x1 + XR * kXPitch);
-  g.stage = align128(g.da + 8 * kSbs * XR * 4);  // da of the stage's 64 chunks x XR tokens
+  g.stage = align128(g.da + 8 * S::kSbs * XR * 4);  // da of the stage's chunks x XR tokens
   return g;
 }
-size_t smem_bytes(int R, int XR, int ns) {
-  return 1024 + (size_t)ns * stage_geo(R, XR).stage + kRedBytes + 256;
+template <int kNT>
+size_t smem_bytes(int R, int ns) {
+  return 1024 + (size_t)ns * stage_geo<kNT>(R).stage + Shape<kNT>::kRedBytes + 256;
 }
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) {
@@ -111,12 +127,13 @@ __device__ __forceinline__ float sc_of(const uint4& v, int s) {  // signed byte 
   return (float)(int)(int8_t)(w >> (8 * (s & 3)));
 }
 
+template <int kCW>
 __device__ __forceinline__ void bar_consumers() {  // the kCW consumer warps only
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kCW) : "memory");
 }
 
 template <int kNT, bool kPartials>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
     mmq_skinny_mma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmS,
                           const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmA, int M, int K, int N, int R, int units,
@@ -125,10 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  constexpr int XR = 8 * kNT;  // token rows of an activation stage
-  const Geo geo = stage_geo(R, XR);
-  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kMaxR][16]
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
+  using S = Shape<kNT>;
+  constexpr int kSbs = S::kSbs, kCW = S::kCW, kRedTok = S::kRedTok;
+  const Geo geo = stage_geo<kNT>(R);
+  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kMaxR][kRedTok]
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + S::kRedBytes);
   uint64_t* empty = full + kMaxNS;
   int* abort_word = reinterpret_cast<int*>(empty + kMaxNS);
   volatile int* abort_flag = abort_word;
@@ -155,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmD);
       tma_prefetch_desc(&tmX);
       tma_prefetch_desc(&tmA);
-      const uint32_t tx = (uint32_t)R * (kQPitch + kScPitch + kDPitch) + 2u * (uint32_t)N * kXPitch +
+      const uint32_t tx = (uint32_t)R * (S::kQPitch + S::kScPitch + kDPitch) +
+                          (uint32_t)S::kXBoxes * (uint32_t)N * kXPitch +
                           (uint32_t)(8 * kSbs) * (uint32_t)ldda * 4u;
       int gs = 0;
       bool ok = true;
@@ -167,15 +186,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           uint8_t* b = smem + (size_t)slot * geo.stage;
           mbar_arrive_expect_tx(&full[slot], tx);
-          tma_load_2d(b, &tmQ, &full[slot], 192 * st, u * R);
-          tma_load_2d(b + geo.sc, &tmS, &full[slot], 16 * st, u * R);
-          tma_load_2d(b + geo.d, &tmD, &full[slot], 2 * st, u * R);
-          // the stage's 2048 activation bytes of each token, as two boxes of
-          // 1024 (+16) bytes per token row
-          tma_load_2d(b + geo.x0, &tmX, &full[slot], 256 * st, 0);
-          tma_load_2d(b + geo.x1, &tmX, &full[slot], 256 * st + 128, 0);
-          // the activation scales of the stage's 64 chunks, [chunk][ldda]
-          tma_load_2d(b + geo.da, &tmA, &full[slot], 0, 64 * st);
+          // x coordinates in 8-byte units, each a multiple of two (16 bytes)
+          tma_load_2d(b, &tmQ, &full[slot], 24 * kSbs * st, u * R);
+          tma_load_2d(b + geo.sc, &tmS, &full[slot], 2 * kSbs * st, u * R);
+          // d: 16 bytes (8 super-blocks) from the even 8-byte unit at or
+          // below the stage's first super-block; the stage's own d values
+          // sit at byte 2 * (kSbs * st % 8) of each row
+          tma_load_2d(b + geo.d, &tmD, &full[slot], (kSbs * st / 4) & ~1, u * R);
+          // the stage's 256 * kSbs activation bytes of each token, as boxes
+          // of 1024 (+16) bytes per token row
+          tma_load_2d(b + geo.x0, &tmX, &full[slot], 32 * kSbs * st, 0);
+          if (S::kXBoxes == 2) tma_load_2d(b + geo.x1, &tmX, &full[slot], 32 * kSbs * st + 128, 0);
+          // the activation scales of the stage's 8 * kSbs chunks, [chunk][ldda]
+          tma_load_2d(b + geo.da, &tmA, &full[slot], 0, 8 * kSbs * st);
         }
       }
       if (!ok) {
@@ -213,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this lane's ql / qh words of rows ra, rb in the current half block
         // (chunks 0-3 read half 0, chunks 4-7 half 1): [row][word]
         uint32_t ql[2][4], qh[2][2];
-        const uint8_t* pa = b + (size_t)ra * kQPitch + 192 * sbw + 4 * t;
-        const uint8_t* pb = b + (size_t)rb * kQPitch + 192 * sbw + 4 * t;
+        const uint8_t* pa = b + (size_t)ra * S::kQPitch + 192 * sbw + 4 * t;
+        const uint8_t* pb = b + (size_t)rb * S::kQPitch + 192 * sbw + 4 * t;
         auto load_half = [&](int h) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -227,15 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             qh[1][j] = have_b ? lds32(pb + 96 * h + 64 + 16 * j) : 0u;
           }
         };
-        const uint4 sca4 = have_a ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)ra * kScPitch + 16 * sbw)
+        const uint4 sca4 = have_a ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)ra * S::kScPitch + 16 * sbw)
                                   : make_uint4(0, 0, 0, 0);
-        const uint4 scb4 = have_b ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)rb * kScPitch + 16 * sbw)
+        const uint4 scb4 = have_b ? *reinterpret_cast<const uint4*>(b + geo.sc + (size_t)rb * S::kScPitch + 16 * sbw)
                                   : make_uint4(0, 0, 0, 0);
+        const int dsb = 2 * ((kSbs * st) % 8 + sbw);  // byte of this super-block's d
         const float d_a = have_a ? __half2float(*reinterpret_cast<const __half*>(
-                                       b + geo.d + (size_t)ra * kDPitch + 2 * sbw))
+                                       b + geo.d + (size_t)ra * kDPitch + dsb))
                                  : 0.0f;
         const float d_b = have_b ? __half2float(*reinterpret_cast<const __half*>(
-                                       b + geo.d + (size_t)rb * kDPitch + 2 * sbw))
+                                       b + geo.d + (size_t)rb * kDPitch + dsb))
                                  : 0.0f;
         // f32 pairs over the tokens (t0, t0 + 1) of a lane: [token tile][row a, b]
         float2 sbs[kNT][2];
@@ -341,21 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = (i < 2) ? ra : rb, tk = 8 * nt + 2 * t + (i & 1);
-        red[(sbw * kMaxR + row) * 16 + tk] = acc[nt][i];
+        red[(sbw * kMaxR + row) * kRedTok + tk] = acc[nt][i];
       }
-    bar_consumers();
+    bar_consumers<kCW>();
     if (ok) {
-      for (int i = threadIdx.x; i < 16 * R; i += 32 * kCW) {
+      for (int i = threadIdx.x; i < kRedTok * R; i += 32 * kCW) {
         const int tk = i / R, row = i - tk * R;
         if (tk < N && tk < 8 * kNT && r0 + row < M) {
           float y = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kSbs; ++w) y += red[(w * kMaxR + row) * 16 + tk];
+          for (int w = 0; w < kSbs; ++w) y += red[(w * kMaxR + row) * kRedTok + tk];
           Y[(size_t)tk * ldy + r0 + row] = y;
         }
       }
     }
-    bar_consumers();
+    bar_consumers<kCW>();
   }
 }
 
@@ -397,29 +421,31 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
   const int R = (int)(((long long)M + waves * sms - 1) / (waves * sms));
   const int units = (M + R - 1) / R;
   const PlaneGeom g = plane_geom(M, K);
+  using S = Shape<kNT>;
   // the scales of the N tokens: dcols columns of the [K/32][ldda] plane (a
   // token group of a larger call starts at a column that is a multiple of
-  // 16, so the box never reaches past the plane's rows)
+  // 4, so the box never reaches past the plane's rows)
   const int dcols = (N + 3) & ~3;
   CUtensorMap mq, ms, md, mx, ma;
   if (!g_encode_fn) return cudaErrorInitializationError;
   // the activation boxes hold the N token rows (the rows past N in shared
   // memory are never stored from)
-  if (encode(&mq, plane + g.qlh_off, g.qlh_row / 8, (uint64_t)M, g.qlh_row, kQPitch / 8,
+  if (encode(&mq, plane + g.qlh_off, g.qlh_row / 8, (uint64_t)M, g.qlh_row, S::kQPitch / 8,
              (uint32_t)R) != CUDA_SUCCESS ||
-      encode(&ms, plane + g.sc_off, (uint64_t)K / 128, (uint64_t)M, (uint64_t)K / 16, kScPitch / 8,
-             (uint32_t)R) != CUDA_SUCCESS ||
+      encode(&ms, plane + g.sc_off, (uint64_t)K / 128, (uint64_t)M, (uint64_t)K / 16,
+             S::kScPitch / 8, (uint32_t)R) != CUDA_SUCCESS ||
       encode(&md, plane + g.d_off, g.d_row / 8, (uint64_t)M, g.d_row, kDPitch / 8, (uint32_t)R) !=
           CUDA_SUCCESS ||
       encode(&mx, Xq, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K, kXPitch / 8, (uint32_t)N) !=
           CUDA_SUCCESS ||
       encode_f32(&ma, da, (uint64_t)dcols, (uint64_t)K / 32, (uint64_t)ldda * 4, (uint32_t)dcols,
-                 8 * kSbs) != CUDA_SUCCESS)
+                 8 * S::kSbs) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
+  const int ns = smem_bytes<kNT>(R, 3) <= (size_t)kSmemBudget ? 3 : 2;
+  if (smem_bytes<kNT>(R, ns) > (size_t)kSmemBudget) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  return launch_pdl(mmq_skinny_mma_kernel<kNT, P>, dim3(grid), dim3(kThreads),
-                    smem_bytes(R, 8 * kNT, ns), s, mq, ms, md, mx, ma, M, K, N, R, units, ns,
+  return launch_pdl(mmq_skinny_mma_kernel<kNT, P>, dim3(grid), dim3(S::kThreads),
+                    smem_bytes<kNT>(R, ns), s, mq, ms, md, mx, ma, M, K, N, R, units, ns,
                     dcols, Y, ldy, dbg.partials, dbg.chunk_sums, status);
 }
 
@@ -452,9 +478,13 @@ cudaError_t mmq_skinny_mma_prepare() {
       (e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<1, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
       (e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<2, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<2, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(mmq_skinny_mma_kernel<4, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
     return e;
-  return cudaFuncSetAttribute(mmq_skinny_mma_kernel<2, true>,
+  return cudaFuncSetAttribute(mmq_skinny_mma_kernel<4, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -464,8 +494,12 @@ cudaError_t launch_mmq_skinny_mma(const uint8_t* plane, int M, int K, const int8
   if (N <= 8)
     return dbg.any() ? launch_nt<1, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s)
                      : launch_nt<1, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s);
-  return dbg.any() ? launch_nt<2, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s)
-                   : launch_nt<2, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s);
+  if (N <= 16)
+    return dbg.any() ? launch_nt<2, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s)
+                     : launch_nt<2, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s);
+  if (N > 32) return cudaErrorInvalidValue;
+  return dbg.any() ? launch_nt<4, true>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s)
+                   : launch_nt<4, false>(plane, M, K, Xq, da, ldda, N, Y, ldy, dbg, status, s);
 }
 
 }  // namespace q6

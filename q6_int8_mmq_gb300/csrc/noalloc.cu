@@ -126,9 +126,9 @@ extern "C" int q6k_mmq_noalloc(const void* plane, const int8_t* wexp, int M, int
     return na_fail(Q6_ECUDA, "clearing the status word: %s", cudaGetErrorString(e));
   if (skinny || groups) {
     // token group g: rows n0 .. n0 + ng - 1 of Xq and Y, columns n0 .. of da
-    // (n0 a multiple of 16: 16-byte aligned); one group when N <= 16
-    for (int n0 = 0; n0 < N; n0 += Q6_SKINNY_MAX_N) {
-      const int ng = N - n0 < Q6_SKINNY_MAX_N ? N - n0 : Q6_SKINNY_MAX_N;
+    // (n0 a multiple of 32: 16-byte aligned); one group when N <= 16
+    for (int n0 = 0; n0 < N; n0 += Q6_SKINNY_GROUP_N) {
+      const int ng = N - n0 < Q6_SKINNY_GROUP_N ? N - n0 : Q6_SKINNY_GROUP_N;
       e = q6::launch_mmq_skinny(static_cast<const uint8_t*>(plane), M, K, Xq + (size_t)n0 * K,
                                 da + n0, ldda, ng, Y + (size_t)n0 * ldy, ldy, q6::Debug{}, status,
                                 (cudaStream_t)s);

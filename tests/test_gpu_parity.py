@@ -90,10 +90,11 @@ TC_PATH = {"raw": "tc_raw", "wexp": "tc_wexp", "wh": "tc_wh"}
 
 def expected_path(N, source, xq=True):
     """The path q6k_mmq takes: the few-token kernels for N <= 16, and on token
-    groups of at most 16 for N <= 64 without resident planes (given Xq); the
-    tensor cores otherwise."""
+    groups of at most 32 given Xq, for N <= 32 whatever the source and for
+    N <= 64 without resident planes; the tensor cores otherwise."""
     import q6_int8_mmq_gb300 as q6mod
-    if N <= q6mod.SKINNY_MAX_N or (N <= q6mod.SKINNY_GROUPS_MAX_N and source != "wh" and xq):
+    if N <= q6mod.SKINNY_MAX_N or (xq and (N <= q6mod.SKINNY_GROUP_N or (
+            N <= q6mod.SKINNY_GROUPS_MAX_N and source != "wh"))):
         return "skinny"
     return TC_PATH[source]
 
@@ -423,21 +424,24 @@ def test_mmq_splitk_few_tiles(q6, orc, M, K, N, splits, source):
     assert torch.allclose(Y, Y1, rtol=1e-5, atol=1e-5 * float(Y1.abs().max()))
 
 
-@pytest.mark.parametrize("source", ["raw", "wexp"])
+@pytest.mark.parametrize("source", ["raw", "wexp", "wh"])
 @pytest.mark.parametrize("M,K,N", [(4096, 11008, 17), (1000, 2816, 20), (300, 768, 32),
                                    (300, 768, 33), (700, 1280, 50), (300, 768, 64),
-                                   (300, 768, 65)], ids=lambda v: str(v))
+                                   (300, 768, 65), (4096, 11008, 32), (1000, 2816, 46)],
+                         ids=lambda v: str(v))
 def test_mmq_token_groups(q6, orc, M, K, N, source):
-    """17..64 tokens without resident planes run the few-token kernels on
-    token groups of at most 16 (offset rows of Xq, Y and the debug outputs,
-    offset columns of da; a last group of one or two tokens on the dp4a
-    kernel): bit-exact partials and Y within tolerance; 65 tokens take the
-    tensor cores. The same Y, up to rounding, as the tensor cores on the same
-    activations without Xq."""
+    """Given Xq, 17..32 tokens run the few-token kernels whatever the source
+    and 33..64 tokens without resident planes, on token groups of at most 32
+    (the 17..32-token form of the MMA kernel; offset rows of Xq, Y and the
+    debug outputs, offset columns of da; a last group of one or two tokens
+    on the dp4a kernel): bit-exact partials and Y within tolerance; 65
+    tokens, and 33 and more on resident planes, take the tensor cores. The
+    same Y, up to rounding, as the tensor cores on the same activations
+    without Xq."""
     import torch
     raw = synth.q6k_raw_weights(1400 + M + N, M, K)
     X = synth.activations(1401 + M + N, N, K, outlier_frac=0.01)
-    w = q6.pack_weights(dev(raw), M, K, wexp=source == "wexp")
+    w = q6.pack_weights(dev(raw), M, K, wexp=source == "wexp", wh=source == "wh")
     act = q6.quantize_act(dev(X))
     xq_o, da_o = quant_check(act, X, orc)
     want_p = N * M * (K // 16) <= 40_000_000
