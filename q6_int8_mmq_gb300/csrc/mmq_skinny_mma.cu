@@ -1,4 +1,4 @@
-// q6_K x int8 GEMM for a few tokens (3 <= N <= 16) on the warp-level f16
+// q6_K x int8 GEMM for a few tokens (3 <= N <= 32) on the warp-level f16
 // tensor path, with the weights streamed into shared memory by TMA. HBM-bound
 // by design: every weight byte is read once (0.82 byte per weight).
 //
@@ -40,7 +40,9 @@
 // of 16 takes super-block s of every stage for rows 16g .. 16g + 15 of the
 // unit (16 warps, four per scheduler, hide the MMA and shared-memory
 // latencies), and the eight super-block warps' sums of a row are added in
-// shared memory at the end (fixed order).
+// shared memory at the end (fixed order). For 17..32 tokens a stage holds
+// 4 super-blocks (one activation box a token) for 8 consumer warps, each with
+// all four 8-token tiles (see Shape below).
 // Every mbarrier wait is bounded (see q6_internal.cuh).
 #include <cudaTypedefs.h>
 
