@@ -567,8 +567,9 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
 
 def q4k_skinny_times(q6, synth, device, iters: int = 10):
     """The q4_K few-token kernels on q4_K weights of the ffn_down shape for
-    N = 1 .. 32 (dp4a for 1-2 tokens, the f16 MMA kernel for 3-16, token
-    groups of 16 beyond), weights rotated over copies totalling more than 4x L2,
+    N = 1 .. 64 (dp4a for 1-2 tokens, the f16 MMA kernel for 3-16 and its
+    17-32-token form, token groups of 32 beyond), weights rotated over copies
+    totalling more than 4x L2,
     timed by CUDA-graph replay; GB/s of the method's bytes (q4_K weights at
     144 B per 256, int8 activations, da and block sums, f32 Y)."""
     import torch
@@ -579,7 +580,7 @@ def q4k_skinny_times(q6, synth, device, iters: int = 10):
     R = max(4, (4 * 129 * 2 ** 20) // q6.q4k_plane_bytes(M, K)[0] + 1)
     Ws = [q6.q4k_pack_weights(raw_d, M, K) for _ in range(R)]
     del raw_d
-    for n in (1, 2, 3, 4, 8, 16, 32, 48):
+    for n in (1, 2, 3, 4, 8, 16, 32, 48, 64):
         X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
         act = q6.quantize_act(torch.from_numpy(X).to(device), want_xh=False, want_us=True)
         Y = torch.empty((n, M), dtype=torch.float32, device=device)
@@ -1376,10 +1377,10 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
 
 
 def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
-    """The q4_K few-token case: N = --tokens (1..48) tokens against q4_K
+    """The q4_K few-token case: N = --tokens (1..64) tokens against q4_K
     weights of the ffn_down shape. One step = q4k_mmq_f32 (the quantiser and
     the GEMM in one kernel) for one or two tokens, else quantise with block
-    sums + q4k_mmq (the few-token kernels, on token groups of 16 beyond 16
+    sums + q4k_mmq (the few-token kernels, on token groups of 32 beyond 32
     tokens); weights rotated over copies totalling more than 4x L2, the K
     steps replayed as one CUDA graph."""
     import torch
@@ -1388,7 +1389,7 @@ def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         raise SystemExit(f"--tokens must be at most {q6.Q4K_GROUPS_MAX_N} for q4k_skinny")
     dp4a = n <= q6.Q4K_DP4A_MAX_N
     fused = n <= q6.FUSED_MAX_N
-    groups = -(-n // q6.Q4K_SKINNY_MAX_N)
+    groups = 1 if n <= q6.Q4K_SKINNY_MAX_N else -(-n // q6.Q4K_GROUP_N)
     M, K = synth.SKINNY_SHAPES["ffn_down"]
     raw = synth.q4k_raw_weights(synth.Q4K_SEED, M, K)
     X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x300 + n, n, K)
@@ -1685,8 +1686,8 @@ def main():
                     choices=["ffn_down", "attn_v", "pages_ffn_down", "pages_attn_v", "skinny",
                              "sweep", "q4k_ffn_down", "q4k_skinny"])
     ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
-    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 49), metavar="{1..48}",
-                    help="tokens of the skinny (1..16) and q4k_skinny (1..48) workloads")
+    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 65), metavar="{1..64}",
+                    help="tokens of the skinny (1..16) and q4k_skinny (1..64) workloads")
     ap.add_argument("--no-other-configs", dest="other_configs", action="store_false",
                     help="skip the attn_v and skinny measurements beside ffn_down")
     ap.add_argument("--weights", choices=["raw", "wexp", "wh"], default="raw")

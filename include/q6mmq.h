@@ -74,12 +74,15 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 #define Q6_Q4K_SKINNY_MAX_N 16
 #define Q6_Q4K_DP4A_MAX_N 2
 
-/* q4k_mmq without a resident operand plane (wq NULL) and with Xq runs
- * Q6_Q4K_SKINNY_MAX_N < N <= Q6_Q4K_GROUPS_MAX_N on the few-token f16 kernel
- * in token groups of at most Q6_Q4K_SKINNY_MAX_N (33 / 49 us at 32 / 48
- * tokens against about 54 us for the unpack and the tensor cores; 62 us
- * against 54 at 56 tokens). */
-#define Q6_Q4K_GROUPS_MAX_N 48
+/* q4k_mmq with Xq runs Q6_Q4K_SKINNY_MAX_N < N <= Q6_Q4K_GROUP_N on the
+ * few-token f16 kernel whatever the weight source, and, without a resident
+ * operand plane (wq NULL), N <= Q6_Q4K_GROUPS_MAX_N too, in token groups of
+ * at most Q6_Q4K_GROUP_N (measured on GB300, 4096 x 11008: 25.6 / 41.0 / 50.5
+ * us at 32 / 48 / 64 tokens, against 52-55 us for the unpack and the tensor
+ * cores, and 29-30 us for the tensor cores on the resident plane at 17-32
+ * tokens). */
+#define Q6_Q4K_GROUPS_MAX_N 64
+#define Q6_Q4K_GROUP_N 32
 
 /* q6k_mmq with Xq runs Q6_SKINNY_MAX_N < N <= Q6_SKINNY_GROUP_N on the
  * few-token kernels whatever the weight source, and, without resident operand
@@ -447,9 +450,10 @@ int q4k_mmq_f32(const void *plane, int M, int K, const float *X, int ldx, int N,
 /* The q4_K GEMM. N > Q6_Q4K_SKINNY_MAX_N runs on the tensor cores; fewer
  * tokens run weight-streaming few-token kernels on the packed plane (about
  * 0.59 byte per weight; wq and the workspace are not used): dp4a for N <=
- * Q6_Q4K_DP4A_MAX_N, exact f16 mma.sync beyond. Without wq and with Xq, up to
- * Q6_Q4K_GROUPS_MAX_N tokens run the f16 few-token kernel on token groups of
- * at most Q6_Q4K_SKINNY_MAX_N instead of the tensor cores.
+ * Q6_Q4K_DP4A_MAX_N, exact f16 mma.sync beyond. With Xq, up to
+ * Q6_Q4K_GROUP_N tokens (and, without wq, up to Q6_Q4K_GROUPS_MAX_N) run the
+ * f16 few-token kernel on token groups of at most Q6_Q4K_GROUP_N instead of
+ * the tensor cores.
  *   plane : the packed q4_K plane (required); wq : resident operand plane or
  *           NULL (then it is unpacked into the workspace first).
  *   Xq, Xh, da, us : from q8_quantize_act_sums (int8 codes, binary16 codes,

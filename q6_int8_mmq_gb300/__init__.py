@@ -32,7 +32,8 @@ SKINNY_GROUPS_MAX_N = 64
 SKINNY_GROUP_N = 32
 Q4K_SKINNY_MAX_N = 16
 Q4K_DP4A_MAX_N = 2
-Q4K_GROUPS_MAX_N = 48
+Q4K_GROUPS_MAX_N = 64
+Q4K_GROUP_N = 32
 FUSED_MAX_N = 2
 
 # Every function include/q6mmq.h declares: (name, restype, argtypes).
@@ -599,8 +600,9 @@ def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",
     """Y [N, M] f32 = the q4_K x int8 GEMM. act needs da and us
     (quantize_act(..., want_us=True)), and xq for N <= Q4K_SKINNY_MAX_N (the
     few-token kernels on the packed plane) or xh for more tokens (the tensor
-    cores; from the packed plane, up to Q4K_GROUPS_MAX_N tokens run the
-    few-token kernel on token groups when xq is there). source (tensor
+    cores; when xq is there, up to Q4K_GROUP_N tokens on either source and
+    up to Q4K_GROUPS_MAX_N from the packed plane run the few-token kernel on
+    token groups of at most Q4K_GROUP_N). source (tensor
     cores): "raw" (unpack the packed plane per call), "wq" (the resident
     operand plane) or "auto". Returns (Y, path name, partials [N, M, K/32]
     int32 or None)."""
@@ -614,7 +616,8 @@ def q4k_mmq(w: Q4Weights, act: Activations, Y=None, source: str = "auto",
     if source == "wq" and w.wq is None:
         raise Q6Error(Q6_EINVAL, "weights were packed without the wq plane")
     wq = w.wq if source == "wq" else None
-    groups = not skinny and N <= Q4K_GROUPS_MAX_N and wq is None and act.xq is not None
+    groups = (not skinny and act.xq is not None
+              and (N <= Q4K_GROUP_N or (N <= Q4K_GROUPS_MAX_N and wq is None)))
     if (act.us is None or (skinny and act.xq is None)
             or (not skinny and not groups and act.xh is None)):
         raise Q6Error(Q6_EINVAL, "the q4_K GEMM needs activations with us, and xq for "

@@ -693,9 +693,12 @@ int q4k_mmq(const void* plane, const uint16_t* wq, int M, int K, const int8_t* X
   if (ldy < M) return fail(Q6_EINVAL, "ldy (%d) < M (%d)", ldy, M);
   if (N == 0) return Q6_OK;
   const bool skinny = N <= Q6_Q4K_SKINNY_MAX_N;
-  // a few more tokens without a resident operand plane: the few-token f16
-  // kernel on token groups, instead of unpacking the weights for the tensor cores
-  const bool groups = !skinny && N <= Q6_Q4K_GROUPS_MAX_N && !wq && Xq;
+  // a few more tokens given Xq: the few-token f16 kernel on token groups, up
+  // to one group's width whatever the weight source (faster than the tensor
+  // cores there), and up to Q6_Q4K_GROUPS_MAX_N without a resident operand
+  // plane (instead of unpacking the weights for the tensor cores)
+  const bool groups = !skinny && Xq &&
+                      (N <= Q6_Q4K_GROUP_N || (N <= Q6_Q4K_GROUPS_MAX_N && !wq));
   if (!plane || !da || !us || !Y) return fail(Q6_EINVAL, "plane, da, us and Y are required");
   if (skinny && !Xq) return fail(Q6_EINVAL, "Xq is required when N <= %d", Q6_Q4K_SKINNY_MAX_N);
   if (!skinny && !groups && !Xh)
@@ -713,9 +716,9 @@ int q4k_mmq(const void* plane, const uint16_t* wq, int M, int K, const int8_t* X
     const uint8_t* pb = static_cast<const uint8_t*>(plane);
     const int ldus = q6::q4_min_ld(K);
     // token group g: rows n0 .. n0 + ng - 1 of Xq, us, Y and partials,
-    // columns n0 .. of da (n0 a multiple of 16: 16-byte aligned)
-    for (int n0 = 0; n0 < N; n0 += Q6_Q4K_SKINNY_MAX_N) {
-      const int ng = N - n0 < Q6_Q4K_SKINNY_MAX_N ? N - n0 : Q6_Q4K_SKINNY_MAX_N;
+    // columns n0 .. of da (n0 a multiple of 32: 16-byte aligned)
+    for (int n0 = 0; n0 < N; n0 += Q6_Q4K_GROUP_N) {
+      const int ng = N - n0 < Q6_Q4K_GROUP_N ? N - n0 : Q6_Q4K_GROUP_N;
       int32_t* pg = partials ? partials + (size_t)n0 * M * (K / 32) : nullptr;
       const int8_t* xg = Xq + (size_t)n0 * K;
       const float* ug = us + (size_t)n0 * ldus;

@@ -59,19 +59,32 @@
 namespace q6 {
 namespace {
 
-constexpr int kSbs = 8;                   // super-blocks per stage
-constexpr int kCW = 2 * kSbs;             // consumer warps: super-block x row group of 16
-constexpr int kThreads = 32 * (kCW + 1);  // + one producer warp
 constexpr int kMaxNS = 3;                 // ring stages (2 or 3, by the shared-memory budget)
 constexpr int kMaxR = 32;                 // rows per unit (two MMA row groups)
-constexpr int kQPitch = 1056;             // bytes per row of a nibble stage (132 x 8)
-constexpr int kXPitch = 1056;             // bytes per token row of an activation half-stage
-constexpr int kUPitch = 528;              // bytes per token row of a block-sum stage (132 f32)
-// bytes per row of a scale stage: 8 super-blocks x (sc 8 | m 8 | (d, dmin) 8),
-// padded so that the 8 rows of a fragment fall on different banks
-constexpr int kMPitch = 200;
+constexpr int kXPitch = 1056;             // bytes per token row of an activation box (132 x 8)
 constexpr int kSmemBudget = 227 * 1024;
-constexpr int kRedBytes = kSbs * kMaxR * 16 * 4;
+
+// The stage shape for kNT token tiles of 8. Up to 16 tokens a stage holds 8
+// super-blocks for 16 consumer warps (super-block x row group); for 17..32
+// tokens (kNT = 4) it holds 4 super-blocks for 8 consumer warps, each forming
+// the MMAs of all four token tiles on one weight fragment (the activation
+// rows of 8 super-blocks for 32 tokens would not fit twice in shared memory).
+// Row pitches are 32 bytes past a multiple of 128 (nibbles), 4 words past a
+// multiple of 32 words (block sums) and 26 words apart modulo 32 (scales), so
+// that the 8 rows of a fragment fall on different banks.
+template <int kNT>
+struct Shape {
+  static constexpr int kSbs = kNT <= 2 ? 8 : 4;     // super-blocks per stage
+  static constexpr int kCW = 2 * kSbs;              // consumer warps
+  static constexpr int kThreads = 32 * (kCW + 1);   // + one producer warp
+  static constexpr int kQPitch = 128 * kSbs + 32;   // bytes per row of a nibble stage (1056 / 544)
+  static constexpr int kUPitch = (16 * kSbs + 4) * 4;  // bytes per token row of block sums (528 / 272)
+  // bytes per row of a scale stage: kSbs x (sc 8 | m 8 | (d, dmin) 8) + 8
+  static constexpr int kMPitch = 24 * kSbs + 8;     // 200 / 104
+  static constexpr int kXBoxes = kSbs / 4;          // activation boxes of 1024 (+32) bytes a token
+  static constexpr int kRedTok = kNT <= 2 ? 16 : 8 * kNT;  // token columns of the final sums
+  static constexpr int kRedBytes = kSbs * kMaxR * kRedTok * 4;
+};
 
 enum : uint32_t { kSiteEmpty = 23, kSiteFull = 24 };
 
@@ -79,18 +92,22 @@ struct Geo {  // byte offsets of one stage's regions and the stage size, for R r
   int x0, x1, da, us, meta, stage;
 };
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
-__host__ __device__ inline Geo stage_geo(int R, int XR) {
+template <int kNT>
+__host__ __device__ inline Geo stage_geo(int R) {
+  using S = Shape<kNT>;
+  constexpr int XR = 8 * kNT;  // token rows of an activation stage
   Geo g;
-  g.x0 = align128(R * kQPitch);
-  g.x1 = align128(g.x0 + XR * kXPitch);
+  g.x0 = align128(R * S::kQPitch);
+  g.x1 = S::kXBoxes == 2 ? align128(g.x0 + XR * kXPitch) : g.x0;
   g.da = align128(g.x1 + XR * kXPitch);
-  g.us = align128(g.da + 8 * kSbs * XR * 4);  // da of the stage's 64 sub-blocks x XR tokens
-  g.meta = align128(g.us + XR * kUPitch);
-  g.stage = align128(g.meta + R * kMPitch);
+  g.us = align128(g.da + 8 * S::kSbs * XR * 4);  // da of the stage's sub-blocks x XR tokens
+  g.meta = align128(g.us + XR * S::kUPitch);
+  g.stage = align128(g.meta + R * S::kMPitch);
   return g;
 }
-size_t smem_bytes(int R, int XR, int ns) {
-  return 1024 + (size_t)ns * stage_geo(R, XR).stage + kRedBytes + 256;
+template <int kNT>
+size_t smem_bytes(int R, int ns) {
+  return 1024 + (size_t)ns * stage_geo<kNT>(R).stage + Shape<kNT>::kRedBytes + 256;
 }
 
 __device__ __forceinline__ uint2 lds64(const uint8_t* p) {
@@ -135,12 +152,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+template <int kCW>
 __device__ __forceinline__ void bar_consumers() {  // the kCW consumer warps only
   asm volatile("bar.sync 1, %0;" ::"n"(32 * kCW) : "memory");
 }
 
 template <int kNT, bool kPartials>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
     q4k_skinny_mma_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmX,
                           const __grid_constant__ CUtensorMap tmA,
@@ -151,10 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  constexpr int XR = 8 * kNT;  // token rows of an activation stage
-  const Geo geo = stage_geo(R, XR);
-  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kMaxR][16]
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);
+  using S = Shape<kNT>;
+  constexpr int kSbs = S::kSbs, kCW = S::kCW, kRedTok = S::kRedTok;
+  constexpr int kQPitch = S::kQPitch, kUPitch = S::kUPitch, kMPitch = S::kMPitch;
+  const Geo geo = stage_geo<kNT>(R);
+  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kMaxR][kRedTok]
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + S::kRedBytes);
   uint64_t* empty = full + kMaxNS;
   int* abort_word = reinterpret_cast<int*>(empty + kMaxNS);
   volatile int* abort_flag = abort_word;
@@ -184,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmU);
     }
-    const uint32_t tx = (uint32_t)R * kQPitch + 2u * (uint32_t)N * kXPitch +
+    const uint32_t tx = (uint32_t)R * kQPitch + (uint32_t)S::kXBoxes * (uint32_t)N * kXPitch +
                         (uint32_t)(8 * kSbs) * (uint32_t)dcols * 4u + (uint32_t)N * kUPitch;
     const uint8_t* scp = plane + pg.sc_off;
     const uint8_t* mnp = plane + pg.mn_off;
@@ -200,15 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* b = smem + (size_t)slot * geo.stage;
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[slot], tx);
-          tma_load_2d(b, &tmQ, &full[slot], 128 * st, u * R);
-          // the stage's 2048 activation bytes of each token, as two boxes of
+          // x coordinates in 8-byte (nibbles, activations) or 4-byte (block
+          // sums) units, each a multiple of 16 bytes
+          tma_load_2d(b, &tmQ, &full[slot], 16 * kSbs * st, u * R);
+          // the stage's 256 * kSbs activation bytes of each token, as boxes of
           // 1024 (+32) bytes per token row
-          tma_load_2d(b + geo.x0, &tmX, &full[slot], 256 * st, 0);
-          tma_load_2d(b + geo.x1, &tmX, &full[slot], 256 * st + 128, 0);
-          // the activation scales of the stage's 64 sub-blocks, [sub-block][dcols]
-          tma_load_2d(b + geo.da, &tmA, &full[slot], 0, 64 * st);
-          // the block-sum pairs of the stage's 8 super-blocks, [token][132]
-          tma_load_2d(b + geo.us, &tmU, &full[slot], 128 * st, 0);
+          tma_load_2d(b + geo.x0, &tmX, &full[slot], 32 * kSbs * st, 0);
+          if (S::kXBoxes == 2) tma_load_2d(b + geo.x1, &tmX, &full[slot], 32 * kSbs * st + 128, 0);
+          // the activation scales of the stage's sub-blocks, [sub-block][dcols]
+          tma_load_2d(b + geo.da, &tmA, &full[slot], 0, 8 * kSbs * st);
+          // the block-sum pairs of the stage's super-blocks, [token][16 kSbs + 4]
+          tma_load_2d(b + geo.us, &tmU, &full[slot], 16 * kSbs * st, 0);
         }
         // entries past M or past the last super-block are not copied (the
         // consumers do not read them)
@@ -381,21 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = (i < 2) ? ra : rb, tk = 8 * nt + 2 * t + (i & 1);
-        red[(sbw * kMaxR + row) * 16 + tk] = acc[nt][i];
+        red[(sbw * kMaxR + row) * kRedTok + tk] = acc[nt][i];
       }
-    bar_consumers();
+    bar_consumers<kCW>();
     if (ok) {
-      for (int i = threadIdx.x; i < 16 * R; i += 32 * kCW) {
+      for (int i = threadIdx.x; i < kRedTok * R; i += 32 * kCW) {
         const int tk = i / R, row = i - tk * R;
         if (tk < N && tk < 8 * kNT && r0 + row < M) {
           float y = 0.0f;
 #pragma unroll
-          for (int w8 = 0; w8 < kSbs; ++w8) y += red[(w8 * kMaxR + row) * 16 + tk];
+          for (int w8 = 0; w8 < kSbs; ++w8) y += red[(w8 * kMaxR + row) * kRedTok + tk];
           Y[(size_t)tk * ldy + r0 + row] = y;
         }
       }
     }
-    bar_consumers();
+    bar_consumers<kCW>();
   }
 }
 
@@ -412,27 +434,29 @@ cudaError_t launch_nt(const uint8_t* plane, int M, int K, const int8_t* Xq, cons
   const int R = (int)(((long long)M + waves * sms - 1) / (waves * sms));
   const int units = (M + R - 1) / R;
   const Q4Geom g = q4_geom(M, K);
+  using S = Shape<kNT>;
   // the scales of the N tokens: dcols columns of the [K/32][ldda] plane (a
   // token group of a larger call starts at a column that is a multiple of
-  // 16, so the box never reaches past the plane's rows)
+  // 4, so the box never reaches past the plane's rows)
   const int dcols = (N + 3) & ~3;
   const int ldus = q4_min_ld(K);
   CUtensorMap mq, mx, ma, mu;
   // the activation and block-sum boxes hold the N token rows (the rows past
   // N in shared memory are never stored from)
   if (skinny_tensor_map(&mq, false, plane + g.qs_off, (uint64_t)K / 16, (uint64_t)M,
-                        (uint64_t)K / 2, kQPitch / 8, (uint32_t)R) != CUDA_SUCCESS ||
+                        (uint64_t)K / 2, S::kQPitch / 8, (uint32_t)R) != CUDA_SUCCESS ||
       skinny_tensor_map(&mx, false, Xq, (uint64_t)K / 8, (uint64_t)N, (uint64_t)K, kXPitch / 8,
                         (uint32_t)N) != CUDA_SUCCESS ||
       skinny_tensor_map(&ma, true, da, (uint64_t)dcols, (uint64_t)K / 32, (uint64_t)ldda * 4,
-                        (uint32_t)dcols, 8 * kSbs) != CUDA_SUCCESS ||
+                        (uint32_t)dcols, 8 * S::kSbs) != CUDA_SUCCESS ||
       skinny_tensor_map(&mu, true, us, (uint64_t)ldus, (uint64_t)N, (uint64_t)ldus * 4,
-                        kUPitch / 4, (uint32_t)N) != CUDA_SUCCESS)
+                        S::kUPitch / 4, (uint32_t)N) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  const int ns = smem_bytes(R, 8 * kNT, 3) <= (size_t)kSmemBudget ? 3 : 2;
+  const int ns = smem_bytes<kNT>(R, 3) <= (size_t)kSmemBudget ? 3 : 2;
+  if (smem_bytes<kNT>(R, ns) > (size_t)kSmemBudget) return cudaErrorInvalidValue;
   const unsigned grid = (unsigned)(units < sms ? units : sms);
-  return launch_pdl(q4k_skinny_mma_kernel<kNT, P>, dim3(grid), dim3(kThreads),
-                    smem_bytes(R, 8 * kNT, ns), s, mq, mx, ma, mu, plane, g, M, K, N, R, units, ns,
+  return launch_pdl(q4k_skinny_mma_kernel<kNT, P>, dim3(grid), dim3(S::kThreads),
+                    smem_bytes<kNT>(R, ns), s, mq, mx, ma, mu, plane, g, M, K, N, R, units, ns,
                     dcols, Y, ldy, partials, status);
 }
 
@@ -447,9 +471,13 @@ cudaError_t q4k_skinny_mma_prepare() {
       (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<1, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
       (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<2, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<2, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<4, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
     return e;
-  return cudaFuncSetAttribute(q4k_skinny_mma_kernel<2, true>,
+  return cudaFuncSetAttribute(q4k_skinny_mma_kernel<4, true>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
@@ -462,9 +490,15 @@ cudaError_t launch_q4k_skinny_mma(const uint8_t* plane, int M, int K, const int8
                                          status, s)
                     : launch_nt<1, false>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, nullptr,
                                           status, s);
-  return partials ? launch_nt<2, true>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, partials,
+  if (N <= 16)
+    return partials ? launch_nt<2, true>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, partials,
+                                         status, s)
+                    : launch_nt<2, false>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, nullptr,
+                                          status, s);
+  if (N > 32) return cudaErrorInvalidValue;
+  return partials ? launch_nt<4, true>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, partials,
                                        status, s)
-                  : launch_nt<2, false>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, nullptr,
+                  : launch_nt<4, false>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, nullptr,
                                         status, s);
 }
 

@@ -165,18 +165,19 @@ def test_host_side_rejections(lib):
     assert q4f(K=185856 + 256, ldx=185856 + 256, N=1) == q6.Q6_ESIZE
     assert q4f(N=0, X=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 
-    # the q4_K GEMM: Xq for N <= 16; Xh beyond, unless Xq is there, the plane
-    # is not resident and N <= 48 (token groups); ldy < M, K % 256, misaligned
-    # pointers, no workspace for the tensor-core unpack, the empty case
+    # the q4_K GEMM: Xq for N <= 16; Xh beyond, unless Xq is there and N <= 32,
+    # or the plane is not resident and N <= 64 (token groups); ldy < M, K % 256,
+    # misaligned pointers, no workspace for the tensor-core unpack, the empty
+    # case (every call here is refused on the host before any launch)
     def q4(plane=fake, wq=None, M=64, K=256, Xq=fake, Xh=fake, da=fake, us=fake, N=4, Y=fake,
            ldy=64, ws=None, ws_bytes=0, P=None):
         return lib.q4k_mmq(plane, wq, M, K, Xq, Xh, da, us, N, Y, ldy, ws, ws_bytes, P,
                            ctypes.byref(path), None)
 
     assert q4(Xq=None) == q6.Q6_EINVAL and path.value == q6.PATH_NONE
-    assert q4(N=49, Xh=None) == q6.Q6_EINVAL
+    assert q4(N=65, Xh=None) == q6.Q6_EINVAL
     assert q4(N=20, Xq=None, Xh=None) == q6.Q6_EINVAL
-    assert q4(N=20, wq=fake, Xh=None) == q6.Q6_EINVAL     # groups only from the packed plane
+    assert q4(N=33, wq=fake, Xh=None) == q6.Q6_EINVAL     # past 32, groups only from the packed plane
     assert q4(us=None) == q6.Q6_EINVAL
     assert q4(ldy=32) == q6.Q6_EINVAL
     assert q4(K=300) == q6.Q6_EINVAL
@@ -184,7 +185,7 @@ def test_host_side_rejections(lib):
     assert q4(us=odd) == q6.Q6_EALIGN
     assert q4(plane=odd) == q6.Q6_EALIGN
     assert q4(P=odd1) == q6.Q6_EALIGN
-    assert q4(N=49) == q6.Q6_ESIZE                         # no workspace for the unpack
+    assert q4(N=65) == q6.Q6_ESIZE                         # no workspace for the unpack
     assert q4(N=20, Xq=None) == q6.Q6_ESIZE
     assert q4(N=0, Xq=None, Xh=None, Y=None) == q6.Q6_OK and path.value == q6.PATH_NONE
 

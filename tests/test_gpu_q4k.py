@@ -156,9 +156,11 @@ def test_q4k_pack_bitexact(q6, orc, M, K):
 
 def q4k_path(N, source):
     """The path a q4_K call with Xq takes: the few-token kernels for N <= 16,
-    and on token groups for up to 48 tokens from the packed plane."""
+    and on token groups of at most 32 for up to 32 tokens on either source and
+    up to 64 tokens from the packed plane."""
     import q6_int8_mmq_gb300 as q6mod
-    if N <= q6mod.Q4K_SKINNY_MAX_N or (source == "raw" and N <= q6mod.Q4K_GROUPS_MAX_N):
+    if N <= q6mod.Q4K_SKINNY_MAX_N or N <= q6mod.Q4K_GROUP_N or (
+            source == "raw" and N <= q6mod.Q4K_GROUPS_MAX_N):
         return "q4k_skinny"
     return {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source]
 
@@ -167,11 +169,12 @@ Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 3), (300, 768, 12), (300, 
              (1001, 2816, 5),
              (1, 256, 3), (7, 2304, 9),   # one row; 9 super-blocks: a stage of one
              (5000, 256, 4),              # more row units than SMs
-             (77, 4352, 31),              # token groups of 16 and 15
+             (77, 4352, 31),              # the 17-32-token form, 17 super-blocks
              (130, 1024, 17), (200, 768, 129), (384, 768, 300),
              (1016, 768, 2555),    # the split last round of tiles, ragged band and tile
              (1016, 512, 2555),    # split halves of one super-block each (one min pair group)
-             (3001, 512, 40), (500, 1024, 48), (500, 1024, 49)]
+             (3001, 512, 40), (500, 1024, 48), (500, 1024, 49),
+             (300, 2304, 64), (500, 1024, 65)]   # groups of 32 + 32; past the groups
 
 
 @pytest.mark.parametrize("source", ["raw", "wq"])
@@ -253,12 +256,12 @@ def test_q4k_degenerate(q6, orc):
         check_y(host(Y), Yo, label)
 
 
-@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 9, 16, 17, 32])
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8, 9, 16, 17, 24, 32, 50])
 def test_q4k_few_tokens_full(q6, orc, N):
     """The few-token kernels on q4_K weights of the ffn_down shape (dp4a for
-    one and two tokens, the f16 MMA kernel for 3-16, token groups of 16
-    beyond): every output within tolerance and every sub-block partial P
-    bit-exact."""
+    one and two tokens, the f16 MMA kernel for 3-16, its 17-32-token form,
+    token groups of 32 beyond): every output within tolerance and every
+    sub-block partial P bit-exact."""
     _, _, cfg = synth.workload("ffn_down")
     M, K = cfg["M"], cfg["K"]
     raw = synth.q4k_raw_weights(0x51361601, M, K)

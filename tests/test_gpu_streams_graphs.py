@@ -165,7 +165,7 @@ def test_q4k_path_in_a_cuda_graph(q6, N, source):
         q6.sync_status()
         xq, da = orc.quantize(X)
         close(Y, orc.q4k_mmq(raw, M, K, xq, da))
-    assert path[0] == ("q4k_skinny" if N <= q6.Q4K_SKINNY_MAX_N or
+    assert path[0] == ("q4k_skinny" if N <= q6.Q4K_GROUP_N or
                        (source == "raw" and N <= q6.Q4K_GROUPS_MAX_N) else
                        {"raw": "q4k_tc_raw", "wq": "q4k_tc_wq"}[source])
 
