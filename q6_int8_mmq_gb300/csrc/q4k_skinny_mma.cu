@@ -1,4 +1,4 @@
-// q4_K x int8 GEMM for a few tokens (3 <= N <= 16) on the warp-level f16
+// q4_K x int8 GEMM for a few tokens (3 <= N <= 32) on the warp-level f16
 // tensor path, with the nibbles and activations streamed into shared memory
 // by TMA. HBM-bound by design: every weight byte is read once (0.59 byte per
 // weight: the 0.5-byte nibbles, the 6-bit scale and min bytes of each
@@ -52,8 +52,9 @@
 // arrives on the stage's full barrier next to the TMA bytes. Consumer warp
 // (s, g) of 16 takes super-block s of every stage for rows 16g .. 16g + 15 of
 // the unit, and the eight super-block warps' sums of a row are added in
-// shared memory at the end (fixed order). Every mbarrier wait is bounded
-// (q6_internal.cuh).
+// shared memory at the end (fixed order). For 17..32 tokens a stage holds 4
+// super-blocks for 8 consumer warps, each with all four 8-token tiles (see
+// Shape below). Every mbarrier wait is bounded (q6_internal.cuh).
 #include "q6_internal.cuh"
 
 namespace q6 {
