@@ -1249,9 +1249,10 @@ def sweep_short(q6, synth, device, sweeps: int = 3):
 
 
 def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
-    """The memory-bound case: N = --tokens (1..16) tokens against the
-    ffn_down or attn_v weights. One step = quantise + q6k_mmq (skinny path),
-    weights rotated over copies totalling more than 4x L2."""
+    """The memory-bound case: N = --tokens (1..64) tokens against the
+    ffn_down or attn_v weights. One step = quantise + q6k_mmq (the few-token
+    kernels; 17..64 tokens on token groups of 32), weights rotated over copies
+    totalling more than 4x L2."""
     import torch
     wname, n = args.skinny_weight, args.tokens
     M, K = synth.SKINNY_SHAPES[wname]
@@ -1349,7 +1350,8 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         kernels = {"q6k_mmq_f32": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]}}
     else:
         kname = ("mmq_skinny_kernel (dp4a)" if n <= SKINNY_DP4A_MAX_N else
-                 "mmq_skinny_mma_kernel (f16 mma.sync, TMA-staged weights)")
+                 "mmq_skinny_mma_kernel (f16 mma.sync, TMA-staged weights)" if n <= 16 else
+                 "mmq_skinny_mma_kernel, 17-32-token form, on token groups of 32")
         formula = "M*K*210/256 + N*K + N*K/8 + 4*N*M"
         kernels = {"q6k_mmq": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]},
                    "q8_quantize_act": {"us": q_ms * 1e3}}
@@ -1366,7 +1368,8 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
                      "unit": "GB/s", "frac": gbs / hbm, "peak_source": hbm_src,
                      "traffic": traffic,
                      "algorithmic": f"{formula} = {alg:.4g} B per launch"},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 if fused else 2) * args.steps,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": (1 if fused else 1 + -(-n // q6.SKINNY_GROUP_N)) * args.steps,
         "clocks": clk, "clocks_ok": clocks_ok(clk),
         "timing": "the K steps replayed as one CUDA graph; kernel times by graph replay",
         "kernels": kernels,
@@ -1687,7 +1690,7 @@ def main():
                              "sweep", "q4k_ffn_down", "q4k_skinny"])
     ap.add_argument("--skinny-weight", default="ffn_down", choices=["ffn_down", "attn_v"])
     ap.add_argument("--tokens", type=int, default=1, choices=range(1, 65), metavar="{1..64}",
-                    help="tokens of the skinny (1..16) and q4k_skinny (1..64) workloads")
+                    help="tokens of the skinny and q4k_skinny workloads")
     ap.add_argument("--no-other-configs", dest="other_configs", action="store_false",
                     help="skip the attn_v and skinny measurements beside ffn_down")
     ap.add_argument("--weights", choices=["raw", "wexp", "wh"], default="raw")
@@ -1697,8 +1700,8 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per q6k_mmq launch from an ncu capture of this kernel")
     args = ap.parse_args()
-    if args.workload == "skinny" and args.tokens > 16:
-        ap.error("--tokens must be at most 16 for the skinny workload")
+    if args.workload == "skinny" and args.tokens > 64:
+        ap.error("--tokens must be at most 64 for the skinny workload")
     args.warmup = max(args.warmup, 3)      # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)

@@ -74,7 +74,11 @@ struct Shape {
   static constexpr int kScPitch = 16 * kSbs + 16;   // bytes per row of an sc stage (144 / 80)
   static constexpr int kXBoxes = kSbs / 4;          // activation boxes of 1024 (+16) bytes a token
   static constexpr int kRedTok = kNT <= 2 ? 16 : 8 * kNT;  // token columns of the final sums
-  static constexpr int kRedBytes = kSbs * kMaxR * kRedTok * 4;
+  // the final sums [kSbs][kRedTok][kRedPitch]: rows contiguous with a pitch of
+  // 36 words, so that the fragment stores (8 rows x 4 token pairs) and the
+  // row-order reads of the final addition are free of bank conflicts
+  static constexpr int kRedPitch = kMaxR + 4;
+  static constexpr int kRedBytes = kSbs * kRedTok * kRedPitch * 4;
 };
 
 enum : uint32_t { kSiteEmpty = 21, kSiteFull = 22 };
@@ -147,7 +151,7 @@ __global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
   using S = Shape<kNT>;
   constexpr int kSbs = S::kSbs, kCW = S::kCW, kRedTok = S::kRedTok;
   const Geo geo = stage_geo<kNT>(R);
-  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kMaxR][kRedTok]
+  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kRedTok][kRedPitch]
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + S::kRedBytes);
   uint64_t* empty = full + kMaxNS;
   int* abort_word = reinterpret_cast<int*>(empty + kMaxNS);
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = (i < 2) ? ra : rb, tk = 8 * nt + 2 * t + (i & 1);
-        red[(sbw * kMaxR + row) * kRedTok + tk] = acc[nt][i];
+        red[(sbw * kRedTok + tk) * S::kRedPitch + row] = acc[nt][i];
       }
     bar_consumers<kCW>();
     if (ok) {
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
         if (tk < N && tk < 8 * kNT && r0 + row < M) {
           float y = 0.0f;
 #pragma unroll
-          for (int w = 0; w < kSbs; ++w) y += red[(w * kMaxR + row) * kRedTok + tk];
+          for (int w = 0; w < kSbs; ++w) y += red[(w * kRedTok + tk) * S::kRedPitch + row];
           Y[(size_t)tk * ldy + r0 + row] = y;
         }
       }

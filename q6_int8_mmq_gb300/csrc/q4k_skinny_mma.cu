@@ -84,7 +84,11 @@ struct Shape {
   static constexpr int kMPitch = 24 * kSbs + 8;     // 200 / 104
   static constexpr int kXBoxes = kSbs / 4;          // activation boxes of 1024 (+32) bytes a token
   static constexpr int kRedTok = kNT <= 2 ? 16 : 8 * kNT;  // token columns of the final sums
-  static constexpr int kRedBytes = kSbs * kMaxR * kRedTok * 4;
+  // the final sums [kSbs][kRedTok][kRedPitch]: rows contiguous with a pitch of
+  // 36 words, so that the fragment stores (8 rows x 4 token pairs) and the
+  // row-order reads of the final addition are free of bank conflicts
+  static constexpr int kRedPitch = kMaxR + 4;
+  static constexpr int kRedBytes = kSbs * kRedTok * kRedPitch * 4;
 };
 
 enum : uint32_t { kSiteEmpty = 23, kSiteFull = 24 };
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
   constexpr int kSbs = S::kSbs, kCW = S::kCW, kRedTok = S::kRedTok;
   constexpr int kQPitch = S::kQPitch, kUPitch = S::kUPitch, kMPitch = S::kMPitch;
   const Geo geo = stage_geo<kNT>(R);
-  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kMaxR][kRedTok]
+  float* red = reinterpret_cast<float*>(smem + (size_t)ns * geo.stage);  // [kSbs][kRedTok][kRedPitch]
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + S::kRedBytes);
   uint64_t* empty = full + kMaxNS;
   int* abort_word = reinterpret_cast<int*>(empty + kMaxNS);
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = (i < 2) ? ra : rb, tk = 8 * nt + 2 * t + (i & 1);
-        red[(sbw * kMaxR + row) * kRedTok + tk] = acc[nt][i];
+        red[(sbw * kRedTok + tk) * S::kRedPitch + row] = acc[nt][i];
       }
     bar_consumers<kCW>();
     if (ok) {
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(Shape<kNT>::kThreads, 1)
         if (tk < N && tk < 8 * kNT && r0 + row < M) {
           float y = 0.0f;
 #pragma unroll
-          for (int w8 = 0; w8 < kSbs; ++w8) y += red[(w8 * kMaxR + row) * kRedTok + tk];
+          for (int w8 = 0; w8 < kSbs; ++w8) y += red[(w8 * kRedTok + tk) * S::kRedPitch + row];
           Y[(size_t)tk * ldy + r0 + row] = y;
         }
       }
