@@ -315,6 +315,9 @@ SMALL = [
     (5000, 512, 16),  # more units than SMs: CTAs take two units each
     (128, 256, 17), (256, 512, 128), (200, 512, 129), (384, 768, 300),  # tensor-core kernel
     (130, 1024, 255), (64, 256, 40),
+    (4800, 768, 5), (4800, 768, 12),  # 32-row units (the largest), 17-warp form
+    (4800, 768, 24), (4800, 2304, 32),  # 32-row units, 17-32-token form; 9 super-blocks
+    (1000, 1280, 20),  # 17-32-token form: 5 super-blocks, a last stage of one
 ]
 
 

@@ -174,7 +174,9 @@ Q4_SHAPES = [(64, 256, 1), (256, 512, 8), (130, 1024, 3), (300, 768, 12), (300, 
              (1016, 768, 2555),    # the split last round of tiles, ragged band and tile
              (1016, 512, 2555),    # split halves of one super-block each (one min pair group)
              (3001, 512, 40), (500, 1024, 48), (500, 1024, 49),
-             (300, 2304, 64), (500, 1024, 65)]   # groups of 32 + 32; past the groups
+             (300, 2304, 64), (500, 1024, 65),   # groups of 32 + 32; past the groups
+             (4800, 768, 12), (4800, 768, 24),   # 32-row units in both MMA forms
+             (1000, 1280, 20)]                   # 17-32 form: a last stage of one
 
 
 @pytest.mark.parametrize("source", ["raw", "wq"])
