@@ -253,3 +253,15 @@ def test_binding_objects_are_checked_when_made():
         q6.Weights(128, 256, torch.zeros(pb - 1, dtype=torch.uint8), None, None)
     with pytest.raises(q6.Q6Error, match="CUDA"):
         q6.Weights(128, 256, torch.zeros(pb, dtype=torch.uint8), None, None)
+
+
+def test_binding_constants_match_the_header():
+    """The routing limits the binding mirrors (token counts of the few-token
+    paths, the token groups, the fused calls) equal the header's #defines, so
+    the binding sizes its buffers for the path the library takes."""
+    text = open(HEADER).read()
+    defines = {k: int(v) for k, v in re.findall(r"^#define\s+Q6_(\w+)\s+(\d+)", text, flags=re.M)}
+    for name in ("SKINNY_MAX_N", "SKINNY_GROUPS_MAX_N", "SKINNY_GROUP_N", "FUSED_MAX_N",
+                 "Q4K_SKINNY_MAX_N", "Q4K_DP4A_MAX_N", "Q4K_GROUPS_MAX_N", "Q4K_GROUP_N"):
+        assert getattr(q6, name) == defines[name], name
+    assert q6.SKINNY_GROUP_N >= q6.SKINNY_MAX_N and q6.Q4K_GROUP_N >= q6.Q4K_SKINNY_MAX_N
