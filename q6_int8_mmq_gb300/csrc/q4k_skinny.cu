@@ -289,11 +289,49 @@ cudaError_t launch_fused(const uint8_t* plane, int M, int K, const float* X, int
                     ldy);
 }
 
+// Two tokens of already quantised activations: the fused kernel's CTA shape
+// and row loop, with the codes, scales and block sums copied into shared
+// memory instead of formed there (us as the f32 sum of its hi/lo pair, which
+// is exact). Each token's activations are then read from shared memory by
+// every row instead of from L1, and the block sum of a sub-block is one word
+// instead of two 8-byte pairs; the dot products and their order are those of
+// q4k_skinny_kernel, so Y is the same bit for bit.
+__global__ void __launch_bounds__(kFusedWarps * 32, 1) q4k_skinny_staged_kernel(
+    const uint8_t* __restrict__ plane, Q4Geom g, int M, int K, const int8_t* __restrict__ Xq,
+    const float* __restrict__ da, int ldda, const float* __restrict__ us, int N,
+    float* __restrict__ Y, int ldy) {
+  constexpr int kMaxN = 2;
+  griddep_launch_dependents();  // the next dependent launch may start its prologue
+  griddep_wait();  // launched as a dependent launch: global memory from here on
+  extern __shared__ __align__(16) uint8_t fused_smem[];
+  const int nc = K / 32, ldus = q4_min_ld(K);
+  int8_t* xs = reinterpret_cast<int8_t*>(fused_smem);                     // codes [N][K]
+  float* das = reinterpret_cast<float*>(fused_smem + (size_t)kMaxN * K);  // da [K/32][kMaxN]
+  float* uss = das + (size_t)nc * kMaxN;                                  // us [N][K/32]
+  for (int i = threadIdx.x; i < N * (K / 16); i += blockDim.x) {
+    const int n = i / (K / 16), j = i - n * (K / 16);
+    reinterpret_cast<uint4*>(xs + (size_t)n * K)[j] =
+        __ldg(reinterpret_cast<const uint4*>(Xq + (size_t)n * K) + j);
+  }
+  for (int i = threadIdx.x; i < N * nc; i += blockDim.x) {
+    const int n = i / nc, c = i - n * nc;
+    const float* ur = us + (size_t)n * ldus + 16 * (c >> 3) + (c & 7);
+    das[c * kMaxN + n] = __ldg(da + (size_t)c * ldda + n);
+    uss[(size_t)n * nc + c] = __ldg(ur) + __ldg(ur + 8);
+  }
+  __syncthreads();
+  const int warps = (int)gridDim.x * kFusedWarps;
+  for (int m = (threadIdx.x >> 5) * (int)gridDim.x + blockIdx.x; m < M; m += warps)
+    q4_row<false, kMaxN, true>(plane, g, m, M, K, xs, das, kMaxN, uss, N, Y, ldy, nullptr);
+}
+
 }  // namespace
 
 cudaError_t q4k_skinny_prepare() {
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(q4k_skinny_fused_kernel<1>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemMax)) ||
+      (e = cudaFuncSetAttribute(q4k_skinny_staged_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemMax)))
     return e;
   return cudaFuncSetAttribute(q4k_skinny_fused_kernel<2>,
@@ -313,6 +351,15 @@ cudaError_t launch_q4k_skinny(const uint8_t* plane, int M, int K, const int8_t* 
                               int ldy, int32_t* partials, cudaStream_t s) {
   const Q4Geom g = q4_geom(M, K);
   if (N <= 1) return launch_n<1>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
+  if (N == 2 && !partials && fused_smem_bytes(K, 2) <= (size_t)kFusedSmemMax) {
+    // two tokens: the activations staged in shared memory once per CTA
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+    return launch_pdl(q4k_skinny_staged_kernel, dim3((unsigned)sms), dim3(kFusedWarps * 32),
+                      fused_smem_bytes(K, 2), s, plane, g, M, K, Xq, da, ldda, us, N, Y, ldy);
+  }
   if (N <= 2) return launch_n<2>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
   if (N <= 4) return launch_n<4>(plane, g, M, K, Xq, da, ldda, us, N, Y, ldy, partials, s);
   static_assert(Q6_Q4K_DP4A_MAX_N <= 8, "the largest token bucket holds 8 tokens");

@@ -346,12 +346,15 @@ def test_q4k_extremes_every_path(q6, orc, N):
     check_y(host(Y), Yo, f"q4k extremes N={N}")
 
 
-@pytest.mark.parametrize("N", [1, 5, 16, 20, 40])
+@pytest.mark.parametrize("N", [1, 2, 5, 16, 20, 40])
 def test_q4k_long_rows(q6, orc, N):
     """Rows of K = 65,536 (256 super-blocks: 32 stages of the f16 few-token
     kernel's 3-slot ring, its barrier phases wrapping many times) through the
-    dp4a (1), f16 (5, 16), token-group (20) and tensor-core (40, resident
-    plane) paths: bit-exact partials and Y within tolerance."""
+    dp4a (1, 2), f16 (5, 16), its 17-32-token form (20) and tensor-core (40,
+    resident plane) paths: bit-exact partials and Y within tolerance; without
+    the debug outputs the same Y bit for bit (two tokens: the kernel with the
+    activations staged in shared memory)."""
+    import torch
     M, K = 130, 65536
     raw = synth.q4k_raw_weights(0x51361701 + N, M, K)
     X = synth.activations(0x51361702 + N, N, K, outlier_frac=0.01)
@@ -364,6 +367,35 @@ def test_q4k_long_rows(q6, orc, N):
     Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
     assert np.array_equal(host(P), Po), "sub-block partials differ"
     check_y(host(Y), Yo, f"q4k long rows N={N}")
+    Y2, _, _ = q6.q4k_mmq(w, act, source=source)
+    q6.sync_status()
+    if N <= q6.Q4K_DP4A_MAX_N:
+        assert torch.equal(Y, Y2)
+    check_y(host(Y2), Yo, f"q4k long rows N={N} fast")
+
+
+@pytest.mark.parametrize("K", [92928, 93184])
+def test_q4k_two_tokens_staged_and_past_its_shared_memory(q6, orc, K):
+    """Two tokens on the kernel that stages the activations in shared memory
+    (the largest K it holds, 92,928) and, one super-block beyond, on the
+    plain dp4a kernel: Y bit for bit that of the debug run (the plain kernel
+    with the partials), and within tolerance of the oracle; as the last group
+    of 34 tokens too."""
+    import torch
+    M = 96
+    raw = synth.q4k_raw_weights(0x51361711 + K, M, K)
+    w = q6.q4k_pack_weights(dev(raw), M, K)
+    for N in (2, 34):
+        X = synth.activations(0x51361712 + K + N, N, K, outlier_frac=0.01)
+        act, xq_o, da_o = quantize(q6, orc, X)
+        Y, path, P = q6.q4k_mmq(w, act, partials=True)
+        Y2, path2, _ = q6.q4k_mmq(w, act)
+        q6.sync_status()
+        assert path == path2 == "q4k_skinny"
+        assert torch.equal(Y, Y2)
+        Yo, Po = orc.q4k_mmq(raw, M, K, xq_o, da_o, partials=True)
+        assert np.array_equal(host(P), Po)
+        check_y(host(Y2), Yo, f"q4k two tokens K={K} N={N}")
 
 
 @pytest.mark.parametrize("M,K,N", [(4096, 11008, 1), (4096, 11008, 2), (1, 256, 1),
