@@ -68,7 +68,7 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 /* q4k_mmq runs N <= Q6_Q4K_SKINNY_MAX_N on the few-token kernels on the
  * packed plane: N <= Q6_Q4K_DP4A_MAX_N on dp4a (CUDA cores), more on the
  * warp-level f16 tensor path (measured on GB300, q4_K weights of 4096 x
- * 11008: dp4a 8.5 / 13.8 us at 1 / 2 tokens; the f16 kernel about 14-15 us
+ * 11008: dp4a 8.6 / 11.2 us at 1 / 2 tokens; the f16 kernel about 13-14 us
  * at 3-8 tokens and 17 us at 16, against about 53 us on the tensor cores from
  * the packed plane and 30 us from the resident operand plane). */
 #define Q6_Q4K_SKINNY_MAX_N 16
