@@ -1464,7 +1464,9 @@ def run_q4k_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         kernels = {"q4k_mmq_f32": {"us": m_ms * 1e3, "gbs": gbs, "path": path[0]}}
         g_gbs = q4k_method_bytes(M, K, n) / g_ms / 1e6
         separate = {"step": "q8_quantize_act with block sums + q4k_mmq",
-                    "q4k_mmq": {"kernel": "q4k_skinny_kernel (dp4a)", "us": g_ms * 1e3,
+                    "q4k_mmq": {"kernel": ("q4k_skinny_kernel (dp4a)" if n == 1 else
+                                           "q4k_skinny_staged_kernel (dp4a, activations "
+                                           "staged in shared memory)"), "us": g_ms * 1e3,
                                 "gbs": g_gbs, "frac": g_gbs / hbm},
                     "q8_quantize_act_sums": {"us": q_ms * 1e3}}
     else:
