@@ -907,3 +907,28 @@ def test_few_token_gemm_sees_the_previous_kernels_writes(q6, orc, fmt):
         q6.sync_status()
         for key, Y in got:
             check_y(host(Y), expect[key], f"{fmt} N={N} turn {key}")
+
+
+@pytest.mark.parametrize("M,K", [(4096, 11008), (131, 2816), (64, 103168), (64, 103424)],
+                         ids=lambda v: str(v))
+def test_two_tokens_staged_equals_plain(q6, orc, M, K):
+    """Two tokens without debug outputs run the kernel that stages the codes
+    and scales in shared memory (up to K = 103,168, the largest its shared
+    memory holds; one super-block beyond, the plain dp4a kernel): Y bit for
+    bit that of the plain kernel (the debug run), within tolerance of the
+    oracle; also as the last group of 34 tokens."""
+    import torch
+    raw = synth.q6k_raw_weights(0x51362401 + M + K, M, K)
+    w = q6.pack_weights(dev(raw), M, K)
+    for N in (2, 34):
+        X = synth.activations(0x51362402 + K + N, N, K, outlier_frac=0.01)
+        act = q6.quantize_act(dev(X))
+        Y, path, D = q6.mmq(w, act, partials=True)
+        Y2, path2, _ = q6.mmq(w, act)
+        q6.sync_status()
+        assert path == path2 == "skinny"
+        assert torch.equal(Y, Y2)
+        xq_o, da_o = quant_check(act, X, orc)
+        Yo = orc.mmq_all(raw, M, K, xq_o, da_o) if M * K > 1 << 22 else orc.mmq(raw, M, K,
+                                                                               xq_o, da_o)
+        check_y(host(Y2), Yo, f"two tokens staged {M}x{K}x{N}")
