@@ -1311,7 +1311,9 @@ def run_skinny(args, q6, synth, device, rank, world, peaks, hbm, hbm_src):
         sq_ms = graph_ms(lambda i: q6.quantize_act(Xd, out=act), 200)
         g_gbs = skinny_bytes(M, K, n) / g_ms / 1e6
         separate = {"step": "q8_quantize_act + q6k_mmq",
-                    "q6k_mmq": {"kernel": "mmq_skinny_kernel (dp4a)", "us": g_ms * 1e3,
+                    "q6k_mmq": {"kernel": ("mmq_skinny_kernel (dp4a)" if n == 1 else
+                                           "mmq_skinny_staged_kernel (dp4a, activations "
+                                           "staged in shared memory)"), "us": g_ms * 1e3,
                                 "gbs": g_gbs, "frac": g_gbs / hbm},
                     "q8_quantize_act": {"us": sq_ms * 1e3}}
     else:
