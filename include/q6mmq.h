@@ -88,11 +88,11 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
  * few-token kernels whatever the weight source, and, without resident operand
  * planes (wh NULL), N <= Q6_SKINNY_GROUPS_MAX_N too, in token groups of at
  * most Q6_SKINNY_GROUP_N (each group streams the 0.82-byte packed plane once;
- * measured on GB300, 4096 x 11008: 17 / 32 / 48 / 64 tokens in about 27 / 28 /
- * 45 / 54 us, against 77-79 us for unpacking 4 bytes a weight and the
- * tensor-core GEMM, and 37-38 us for the tensor cores on resident planes at
- * 17-32 tokens). */
-#define Q6_SKINNY_GROUPS_MAX_N 64
+ * measured on GB300, 4096 x 11008: 17 / 32 / 48 / 64 / 80 / 96 tokens in about
+ * 27 / 28 / 45 / 53 / 70 / 78 us, against 77-80 us for unpacking 4 bytes a
+ * weight and the tensor-core GEMM, and 37-38 us for the tensor cores on
+ * resident planes at 17-32 tokens). */
+#define Q6_SKINNY_GROUPS_MAX_N 96
 #define Q6_SKINNY_GROUP_N 32
 
 #define Q6_SKINNY_MAX_N 16

@@ -28,7 +28,7 @@ PATH_NAMES = {PATH_NONE: "none", PATH_TC_RAW: "tc_raw", PATH_TC_WEXP: "tc_wexp",
               PATH_TC_FUSED_WH: "tc_fused_wh", PATH_Q4K_SKINNY: "q4k_skinny",
               PATH_Q4K_SKINNY_FUSED: "q4k_skinny_fused"}
 SKINNY_MAX_N = 16
-SKINNY_GROUPS_MAX_N = 64
+SKINNY_GROUPS_MAX_N = 96
 SKINNY_GROUP_N = 32
 Q4K_SKINNY_MAX_N = 16
 Q4K_DP4A_MAX_N = 2

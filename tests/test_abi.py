@@ -71,8 +71,8 @@ def test_host_side_rejections(lib):
     odd = ctypes.c_void_p(0x10004)
     path = ctypes.c_int(-1)
 
-    # N = 65: past the token groups, so the tensor-core path's checks apply
-    def mmq(plane=fake, wexp=None, wh=None, M=64, K=256, xq=fake, da=fake, xh=fake, N=65,
+    # N = 97: past the token groups, so the tensor-core path's checks apply
+    def mmq(plane=fake, wexp=None, wh=None, M=64, K=256, xq=fake, da=fake, xh=fake, N=97,
             Y=fake, ldy=64, ws=fake, ws_bytes=1 << 30, partials=None, chunk_sums=None):
         return lib.q6k_mmq(plane, wexp, wh, M, K, xq, da, xh, N, Y, ldy, ws, ws_bytes, partials,
                            chunk_sums, ctypes.byref(path), None)
@@ -82,7 +82,7 @@ def test_host_side_rejections(lib):
     assert mmq(ldy=32) == q6.Q6_EINVAL                      # ldy < M
     assert mmq(N=0, xq=None, da=None, xh=None) == q6.Q6_OK  # empty: a no-op
     assert path.value == q6.PATH_NONE
-    assert mmq(xh=None) == q6.Q6_EINVAL                     # operand plane needed for N > 64
+    assert mmq(xh=None) == q6.Q6_EINVAL                     # operand plane needed for N > 96
     assert mmq(N=40, xq=None, xh=None) == q6.Q6_EINVAL      # ... and for N > 16 without Xq
     assert mmq(N=40, wh=fake, xh=None) == q6.Q6_EINVAL      # ... or with resident planes
     assert mmq(N=8, xq=None) == q6.Q6_EINVAL                # int8 activations needed for N <= 16

@@ -430,14 +430,15 @@ def test_mmq_splitk_few_tiles(q6, orc, M, K, N, splits, source):
 @pytest.mark.parametrize("source", ["raw", "wexp", "wh"])
 @pytest.mark.parametrize("M,K,N", [(4096, 11008, 17), (1000, 2816, 20), (300, 768, 32),
                                    (300, 768, 33), (700, 1280, 50), (300, 768, 64),
-                                   (300, 768, 65), (4096, 11008, 32), (1000, 2816, 46)],
+                                   (300, 768, 65), (4096, 11008, 32), (1000, 2816, 46),
+                                   (300, 768, 96), (300, 768, 97)],
                          ids=lambda v: str(v))
 def test_mmq_token_groups(q6, orc, M, K, N, source):
     """Given Xq, 17..32 tokens run the few-token kernels whatever the source
-    and 33..64 tokens without resident planes, on token groups of at most 32
+    and 33..96 tokens without resident planes, on token groups of at most 32
     (the 17..32-token form of the MMA kernel; offset rows of Xq, Y and the
     debug outputs, offset columns of da; a last group of one or two tokens
-    on the dp4a kernel): bit-exact partials and Y within tolerance; 65
+    on the dp4a kernel): bit-exact partials and Y within tolerance; 97
     tokens, and 33 and more on resident planes, take the tensor cores. The
     same Y, up to rounding, as the tensor cores on the same activations
     without Xq."""

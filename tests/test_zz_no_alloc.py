@@ -92,8 +92,8 @@ def test_noalloc_rejects_layers_beyond_its_scratch(q6):
     lib = q6.load()
     fake = ctypes.c_void_p(0x10000)       # rejected on the host before any use
     path = ctypes.c_int(-1)
-    # 65 tokens: past the token groups, so the unpack and its scratch apply
-    rc = lib.q6k_mmq_noalloc(fake, None, 4096, 11008, fake, fake, fake, 65, fake, 4096,
+    # 97 tokens: past the token groups, so the unpack and its scratch apply
+    rc = lib.q6k_mmq_noalloc(fake, None, 4096, 11008, fake, fake, fake, 97, fake, 4096,
                              ctypes.byref(path), None)
     assert rc == q6.Q6_ESIZE
     assert b"static scratch" in lib.q6_last_error()
