@@ -538,7 +538,8 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
     """The q6_K tensor-core GEMM with 17 to 256 tokens against the ffn_down
     weights, where the tiles fill at most half of the SMs and K is split over
     the idle ones: resident operand planes and from the packed plane (up to
-    64 tokens the few-token kernels on token groups), four weight copies in
+    96 tokens the few-token kernels on token groups; up to 32 on resident
+    planes too), four weight copies in
     turn (720 MB of operand planes), CUDA-graph replay."""
     import torch
     out = {}
@@ -548,7 +549,7 @@ def mid_tokens_times(q6, synth, device, iters: int = 4):
     R = 4
     Ws = [q6.pack_weights(raw_d, M, K, wh=True) for _ in range(R)]
     del raw_d
-    for n in (17, 32, 48, 64, 128, 256):
+    for n in (17, 32, 48, 64, 96, 128, 256):
         X = synth.activations(synth.WORKLOAD_SEED["skinny"] + 0x500 + n, n, K)
         act = q6.quantize_act(torch.from_numpy(X).to(device))
         Y = torch.empty((n, M), dtype=torch.float32, device=device)
