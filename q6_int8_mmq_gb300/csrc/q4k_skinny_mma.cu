@@ -67,7 +67,7 @@ constexpr int kSmemBudget = 227 * 1024;
 
 // The stage shape for kNT token tiles of 8. Up to 16 tokens a stage holds 8
 // super-blocks for 16 consumer warps (super-block x row group); for 17..32
-// tokens (kNT = 4) it holds 4 super-blocks for 8 consumer warps, each forming
+// tokens (kNT = 3 or 4) it holds 4 super-blocks for 8 consumer warps, each forming
 // the MMAs of all four token tiles on one weight fragment (the activation
 // rows of 8 super-blocks for 32 tokens would not fit twice in shared memory).
 // Row pitches are 32 bytes past a multiple of 128 (nibbles), 4 words past a
@@ -480,6 +480,10 @@ cudaError_t q4k_skinny_mma_prepare() {
       (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<2, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
       (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<4, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<3, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) ||
+      (e = cudaFuncSetAttribute(q4k_skinny_mma_kernel<3, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)))
     return e;
   return cudaFuncSetAttribute(q4k_skinny_mma_kernel<4, true>,
@@ -501,6 +505,11 @@ cudaError_t launch_q4k_skinny_mma(const uint8_t* plane, int M, int K, const int8
                     : launch_nt<2, false>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, nullptr,
                                           status, s);
   if (N > 32) return cudaErrorInvalidValue;
+  if (N <= 24)  // 17..24 tokens on three token tiles
+    return partials ? launch_nt<3, true>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, partials,
+                                         status, s)
+                    : launch_nt<3, false>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, nullptr,
+                                          status, s);
   return partials ? launch_nt<4, true>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, partials,
                                        status, s)
                   : launch_nt<4, false>(plane, M, K, Xq, da, ldda, us, N, Y, ldy, nullptr,
