@@ -89,7 +89,7 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
  * planes (wh NULL), N <= Q6_SKINNY_GROUPS_MAX_N too, in token groups of at
  * most Q6_SKINNY_GROUP_N (each group streams the 0.82-byte packed plane once;
  * measured on GB300, 4096 x 11008: 17 / 32 / 48 / 64 / 80 / 96 tokens in about
- * 27 / 28 / 45 / 53 / 70 / 78 us, against 77-80 us for unpacking 4 bytes a
+ * 23 / 27 / 44 / 53 / 70 / 78 us, against 77-80 us for unpacking 4 bytes a
  * weight and the tensor-core GEMM, and 37-38 us for the tensor cores on
  * resident planes at 17-32 tokens). */
 #define Q6_SKINNY_GROUPS_MAX_N 96
