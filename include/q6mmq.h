@@ -77,8 +77,8 @@ typedef struct CUstream_st *q6_stream_t; /* the same type as cudaStream_t */
 /* q4k_mmq with Xq runs Q6_Q4K_SKINNY_MAX_N < N <= Q6_Q4K_GROUP_N on the
  * few-token f16 kernel whatever the weight source, and, without a resident
  * operand plane (wq NULL), N <= Q6_Q4K_GROUPS_MAX_N too, in token groups of
- * at most Q6_Q4K_GROUP_N (measured on GB300, 4096 x 11008: 25.6 / 41.0 / 50.5
- * us at 32 / 48 / 64 tokens, against 52-55 us for the unpack and the tensor
+ * at most Q6_Q4K_GROUP_N (measured on GB300, 4096 x 11008: 21.6 / 24.4 / 39.2 /
+ * 48.3 us at 17 / 32 / 48 / 64 tokens, against 52-55 us for the unpack and the tensor
  * cores, and 29-30 us for the tensor cores on the resident plane at 17-32
  * tokens). */
 #define Q6_Q4K_GROUPS_MAX_N 64
