@@ -66,7 +66,7 @@ def noalloc(q6, w, act, use_wexp, stream=None):
     return Y, q6.PATH_NAMES[path.value]
 
 
-@pytest.mark.parametrize("N", [300, 40, 8])     # tensor cores, token groups, few tokens
+@pytest.mark.parametrize("N", [300, 40, 20, 8, 2])  # tensor cores, token groups, 17-24 form, few tokens, two staged
 def test_noalloc_matches_q6k_mmq_on_two_calls(q6, N):
     import torch
     M, K = 4096, 4096                     # the largest layer its static scratch holds
